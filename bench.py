@@ -1,0 +1,414 @@
+#!/usr/bin/env python
+"""Benchmark of one GDN-layer batched prefill on GB300.
+
+Metric: GDN-layer prefill tokens/s on the 9B-like layer (hidden 4096, 16 q/k
+heads and 32 v heads of dim 128, Q4_K weights, bf16 activations) at N = 32768
+tokens, zero initial state, drawn gates (log a ~ U(-0.5, 0)).  One step is one
+gdn_prefill call over the whole prompt: Q4_K decode of both weight matrices,
+activation quantisation, input projection, conv, chunked delta rule, gated
+norm, output projection.  Inputs (x 268 MB, workspace ~4 GB) are larger than
+L2, so no flush is needed between steps.
+
+Arms:
+  default            the CUDA library (``value``: inputs resident in HBM;
+                     ``e2e``: the same call fed from pinned host buffers, with
+                     the host->device copy of x and the gates and the
+                     device->host read of y inside the timed region);
+  --impl reference   the fp64 CPU oracle on this machine's cores, each step a
+                     bounded sample of the same workload.
+
+Multi-GPU (torchrun, N ranks): the layer does not shard across GPUs here
+("replicas only"): every rank prefills its own prompt on its own GPU, with no
+data-path collective; timings are reduced (max) over ranks on the CPU.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+_CORES = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, str(_CORES))
+
+import numpy as np  # noqa: E402
+
+METRIC = "GDN-layer prefill tokens/s at N=32768 (1 GB300); % int8 tensor / HBM roofline"
+UNIT = "tokens/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="h4096")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ distributed
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            dist.init_process_group("gloo")
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, v: float) -> float:
+        if not self.pg:
+            return v
+        import torch
+        t = torch.tensor([v], dtype=torch.float64)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons, kept with timestamps."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", gpu_id, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return []
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                ts = time.mktime(time.strptime(f[0].split(".")[0], "%Y/%m/%d %H:%M:%S")) + float("0." + f[0].split(".")[1])
+                rows.append({"t": ts, "sm": float(f[1]), "sm_max": float(f[2]), "power": f[3], "active": f[4],
+                             "hw_slowdown": f[5], "hw_thermal_slowdown": f[6], "sw_thermal_slowdown": f[7],
+                             "sw_power_cap": f[8]})
+            except (ValueError, IndexError):
+                continue
+        return rows
+
+    @staticmethod
+    def summarize(rows, t0, t1):
+        inside = [r for r in rows if t0 - 0.06 <= r["t"] <= t1 + 0.06] or rows
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+        reasons = sorted({k for r in inside for k in ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                                        "sw_power_cap") if r[k].lower() == "active"})
+        return {"sm_mhz": statistics.median(r["sm"] for r in inside), "sm_max_mhz": max(r["sm_max"] for r in inside),
+                "reasons": reasons, "samples": len(inside)}
+
+
+REJECT = {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"}
+
+
+# ------------------------------------------------------------------ roofline figures
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm": p["hbm_gbs"], "tensor": p.get("bf16_tflops_sustained", p["bf16_tflops"]),
+                "src": "of measured (MEASURED_PEAKS.json: hbm_gbs; bf16_tflops_sustained, fp16 at the bf16 rate)"}
+    return {"hbm": 6800.0, "tensor": 1700.0, "src": "of fallback (6.8 TB/s, 1.7 PFLOP/s sustained bf16)"}
+
+
+def stage_work(spec, n):
+    """Algorithmic bytes (HBM-bound stages) or FLOPs (projections) per call."""
+    H, hv, d = spec.hidden, spec.n_v_heads, spec.dk
+    c_qk, c_v, c_conv, r_in = spec.c_qk, spec.c_v, spec.c_conv, spec.r_in
+    nbf = 2 * c_qk + 2 * c_v
+    w_el = r_in * H + H * c_v
+    C = 64
+    nch = (n + C - 1) // C
+    return {
+        # Q4_K blocks read (144 B / 256 weights) + fp16 codes and scales written
+        "dequant": ("hbm", w_el * 144 / 256 + w_el * 2 + (r_in + H) * 4),
+        # bf16 x read, fp16 codes + scales written
+        "act_quant": ("hbm", n * H * 2 + n * H * 2 + n * 4),
+        "in_proj": ("tensor", 2.0 * n * r_in * H),
+        # raw q|k|v read (bf16), conv output written (bf16), beta/alpha read; conv state
+        "conv": ("hbm", n * c_conv * 2 * 2 + c_conv * 4 * 4),
+        # q, k, v (bf16) + gates read, o (fp32) written, per-chunk scratch written and read once
+        "delta_rule": ("hbm", n * c_conv * 2 + 2 * n * hv * 4 + n * c_v * 4
+                       + 2 * nch * hv * C * (2 * d + C + 1) * 4),
+        # o (fp32) + z (bf16) read, fp16 codes + scales written
+        "gated_norm": ("hbm", n * c_v * 4 + n * c_v * 2 + n * c_v * 2 + n * 4),
+        "out_proj": ("tensor", 2.0 * n * H * c_v),
+    }
+
+
+def traffic_from_profile(kernel_src: str, profile_md: str):
+    """DRAM bytes per launch recorded in a committed ncu summary, if the kernel source is unchanged."""
+    if not os.path.exists(profile_md):
+        return None
+    text = open(profile_md).read()
+    m = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
+    t = re.search(r"dram_bytes_per_launch_full_size:\s*([0-9.eE+]+)", text)
+    if not m or not t:
+        return None
+    h = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
+    return float(t.group(1)) if h == m.group(1) else None
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def oracle_params(spec, layer):
+    from oracle import q4k
+    p = dict(wtype=spec.wtype, hidden=spec.hidden, n_qk_heads=spec.n_qk_heads, n_v_heads=spec.n_v_heads,
+             dk=spec.dk, dv=spec.dv, conv_w=layer["conv_w"], A_log=layer["A_log"], dt_bias=layer["dt_bias"],
+             norm_w=layer["norm_w"], eps_l2=1e-6, eps_rms=1e-6, q_scale=spec.dk ** -0.5)
+    p["w_in"] = q4k.pack_q4k(layer["w_in"]) if spec.wtype == "q4k" else layer["w_in"]
+    p["w_out"] = q4k.pack_q4k(layer["w_out"]) if spec.wtype == "q4k" else layer["w_out"]
+    return p
+
+
+def time_oracle(spec, layer, tok, n_sample):
+    """Oracle (as it stands) on the first n_sample tokens; returns seconds."""
+    from oracle import layer as OL
+    p = oracle_params(spec, layer)
+    t0 = time.perf_counter()
+    OL.layer_forward(p, tok["x"][:n_sample], gate_log_a=tok["log_a"][:n_sample], gate_b=tok["b"][:n_sample])
+    return time.perf_counter() - t0
+
+
+# ------------------------------------------------------------------ arms
+
+def run_reference(args, dist, spec):
+    if dist.rank != 0:
+        return
+    from hybrid_gated_deltanet_q4k_gb300 import synth
+    layer = synth.make_layer(spec)
+    n_sample = 256
+    tok = synth.make_tokens(spec, n_sample, seed=spec.seed + 10)
+    for _ in range(args.warmup):
+        time_oracle(spec, layer, tok, n_sample)
+    times = [time_oracle(spec, layer, tok, n_sample) for _ in range(args.steps)]
+    t = sum(times) / len(times)
+    v = n_sample / t
+    sample = (f"first {n_sample} tokens of the {spec.workload} workload per step (weights decoded each call, "
+              f"recurrence one token at a time in fp64)")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": spec.workload, "tokens_per_step": n_sample},
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": _CORES, "kind": "oracle", "sample": sample},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def run_ours(args, dist, spec):
+    import ctypes
+
+    import torch
+
+    from hybrid_gated_deltanet_q4k_gb300 import lib as gl
+    from hybrid_gated_deltanet_q4k_gb300 import synth
+    from hybrid_gated_deltanet_q4k_gb300.api import DeviceLayer
+
+    torch.cuda.set_device(dist.local)
+    dev = f"cuda:{dist.local}"
+    L = gl.load(build=True)
+    n = spec.n_tokens
+    layer = synth.make_layer(spec)
+    tok = synth.make_tokens(spec, n, seed=spec.seed + 10 + dist.rank)
+    dl = DeviceLayer(spec, layer, device=dev)
+    x = torch.from_numpy(tok["x_bits"].view(np.int16)).to(dev).view(torch.bfloat16)
+    la = torch.from_numpy(tok["log_a"]).to(dev)
+    bb = torch.from_numpy(tok["b"]).to(dev)
+    state, conv = dl.new_state()
+    y = torch.empty(n, spec.hidden, dtype=torch.bfloat16, device=dev)
+    ws = dl.new_workspace(n)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        conv.zero_()
+        dl.prefill(x, None, state, conv, y, ws, gate_log_a=la, gate_b=bb)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    assert L.gdn_sync_status(stream.cuda_stream, check=False) == 0, L.last_error()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(gl.GDN_N_STAGE_EVENTS)] for _ in range(K)]
+    for row in ev:              # torch creates the CUDA event at its first record
+        for e in row:
+            e.record(stream)
+
+    def timed():
+        dist.barrier()
+        torch.cuda.synchronize()
+        t_host0 = time.time()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(K):
+            arr = (ctypes.c_void_p * gl.GDN_N_STAGE_EVENTS)(*[e.cuda_event for e in ev[i]])
+            L.gdn_set_stage_events(arr, gl.GDN_N_STAGE_EVENTS)
+            step()
+        e1.record(stream)
+        L.gdn_set_stage_events(None, 0)
+        torch.cuda.synchronize()
+        t_host1 = time.time()
+        dist.barrier()
+        return e0.elapsed_time(e1) / K, t_host0, t_host1
+
+    gpu_id = str(getattr(torch.cuda.get_device_properties(dist.local), "uuid", dist.local))
+    if not gpu_id.startswith("GPU-") and len(gpu_id) == 36:
+        gpu_id = "GPU-" + gpu_id
+    sampler = ClockSampler(gpu_id)
+    time.sleep(0.3)
+    ms, h0, h1 = timed()
+    clocks = ClockSampler.summarize(sampler.stop(), h0, h1)
+    if REJECT & set(clocks["reasons"]):     # throttled: measure once more
+        sampler = ClockSampler(gpu_id)
+        time.sleep(0.3)
+        ms, h0, h1 = timed()
+        clocks = ClockSampler.summarize(sampler.stop(), h0, h1)
+        clocks["remeasured"] = True
+    assert L.gdn_sync_status(stream.cuda_stream, check=False) == 0, L.last_error()
+    ms_max = dist.max(ms)
+
+    # per-stage average durations (ms) from the stage events
+    names = gl.STAGE_NAMES
+    stage_ms = {nm: sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K)) / K for j, nm in enumerate(names)}
+    pk = peaks()
+    work = stage_work(spec, n)
+    stages = {}
+    for nm in names:
+        kind, amount = work[nm]
+        sec = stage_ms[nm] / 1e3
+        if kind == "tensor":
+            a = amount / sec / 1e12
+            stages[nm] = {"ms": stage_ms[nm], "bound": "tensor", "achieved": a, "unit": "TFLOP/s", "frac": a / pk["tensor"]}
+        else:
+            a = amount / sec / 1e9
+            stages[nm] = {"ms": stage_ms[nm], "bound": "hbm", "achieved": a, "unit": "GB/s", "frac": a / pk["hbm"]}
+    dom = stages["in_proj"]
+    traffic = traffic_from_profile(os.path.join(ROOT, "hybrid_gated_deltanet_q4k_gb300", "csrc", "k_gemm.cu"),
+                                   os.path.join(ROOT, "profiles", "gemm_codes_in_proj_h4096_n32768.md"))
+    roofline = {"bound": "tensor", "achieved": dom["achieved"], "peak": pk["tensor"], "unit": "TFLOP/s",
+                "frac": dom["frac"], "traffic": traffic, "kernel": "gemm_codes_kernel (input projection, 3.316 TFLOP/launch)",
+                "peak_source": pk["src"]}
+
+    # end to end through the public call, fed from pinned host memory
+    e2e = None
+    if not args.no_e2e:
+        xh = torch.from_numpy(tok["x_bits"].view(np.int16)).pin_memory()
+        lah = torch.from_numpy(tok["log_a"]).pin_memory()
+        bh = torch.from_numpy(tok["b"]).pin_memory()
+        yh = torch.empty(n, spec.hidden, dtype=torch.int16).pin_memory()
+        xv = x.view(torch.int16)
+
+        def e2e_step():
+            xv.copy_(xh, non_blocking=True)
+            la.copy_(lah, non_blocking=True)
+            bb.copy_(bh, non_blocking=True)
+            step()
+            yh.copy_(y.view(torch.int16), non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        dist.barrier()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        dist.barrier()
+        e2e_ms = dist.max(e0.elapsed_time(e1) / K)
+        e2e = {"value": n * dist.world / (e2e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": xh.numel() * 2 + lah.numel() * 4 + bh.numel() * 4,
+               "d2h_bytes_per_step": yh.numel() * 2, "ms_per_step": e2e_ms}
+
+    cpu = None
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        n_sample = 1024
+        t = time_oracle(spec, layer, tok, n_sample)
+        cpu = {"value": n_sample / t, "unit": UNIT, "cores": _CORES, "kind": "oracle",
+               "sample": f"first {n_sample} of the {n} tokens of {spec.workload} (one call: weight decode, "
+                         f"projections as fp64 matmuls on the exact int8 operands, recurrence one token at a time)"}
+
+    passes = 1
+    launches = (2 + 8 * passes) * K
+    if dist.rank == 0:
+        print(json.dumps({
+            "metric": METRIC, "value": n * dist.world / (ms_max / 1e3), "unit": UNIT, "n_gpus": dist.world,
+            "steps": K, "warmup": max(args.warmup, 3), "ms_per_step": ms_max, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int8",
+            "dtype_detail": "int8 codes (exact in fp16) on fp16 tcgen05 tensor cores with exact int32 sums; "
+                            "bf16 activations; fp32 conv/norm/recurrence state",
+            "data": "synthetic (seeded random weights and inputs of the stated distributions)",
+            "config": {"workload": spec.workload, "n_tokens": n, "hidden": spec.hidden,
+                       "heads": f"{spec.n_qk_heads}x{spec.dk} q/k, {spec.n_v_heads}x{spec.dv} v",
+                       "weights": "Q4_K", "state": "zero", "gates": "drawn, log a ~ U(-0.5,0)",
+                       "l2": "no flush: inputs larger than L2 (x 268 MB, workspace %.1f GB)" % (ws.numel() / 1e9),
+                       "parallelism": "replicas only" if dist.world > 1 else "single GPU"},
+            "roofline": roofline, "stages": stages, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+            "clocks": clocks,
+        }), flush=True)
+
+
+def main():
+    args = parse()
+    dist = Dist()
+    from hybrid_gated_deltanet_q4k_gb300 import synth
+    spec = synth.SPECS[args.config]
+    try:
+        if args.impl == "reference":
+            run_reference(args, dist, spec)
+        else:
+            run_ours(args, dist, spec)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,68 @@
+"""User-facing wrapper: a GDN layer resident on the GPU, prefilled through the C ABI.
+
+Weights are encoded to Q4_K on the host by the library's ``q4k_pack`` (or kept
+fp32 for an F32 layer) and uploaded once; ``prefill`` enqueues one
+``gdn_prefill`` call.  PyTorch only provides device memory and the stream.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+import torch
+
+from . import lib as gl
+
+
+def pack_q4k(w: np.ndarray) -> np.ndarray:
+    """Host Q4_K encoding through the library (``q4k_pack``)."""
+    w = np.ascontiguousarray(w, np.float32)
+    out = np.zeros((w.shape[0], w.shape[1] // 256 * 144), np.uint8)
+    gl.load().q4k_pack(gl.ptr(w), w.shape[0], w.shape[1], gl.ptr(out))
+    return out
+
+
+class DeviceLayer:
+    """One GDN layer's parameters in device memory, in the layouts ``gdn_layer`` names."""
+
+    def __init__(self, spec, params: dict, device: str = "cuda", eps_l2: float = 1e-6, eps_rms: float = 1e-6,
+                 q_scale: float | None = None, blocks: dict | None = None):
+        self.spec = spec
+        self.device = device
+        self.lib = gl.load()
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)  # noqa: E731
+        if spec.wtype == "q4k":
+            b_in = blocks["w_in"] if blocks else pack_q4k(params["w_in"])
+            b_out = blocks["w_out"] if blocks else pack_q4k(params["w_out"])
+            self.host_blocks = {"w_in": b_in, "w_out": b_out}
+            self.dev = {"w_in": t(b_in), "w_out": t(b_out)}
+        else:
+            self.dev = {"w_in": t(params["w_in"].astype(np.float32)), "w_out": t(params["w_out"].astype(np.float32))}
+        for k in ("conv_w", "A_log", "dt_bias", "norm_w"):
+            self.dev[k] = t(params[k].astype(np.float32))
+        self.eps_l2, self.eps_rms = eps_l2, eps_rms
+        self.q_scale = spec.dk ** -0.5 if q_scale is None else q_scale
+
+    def struct(self, gate_log_a=None, gate_b=None) -> gl.GdnLayer:
+        return gl.make_layer_struct(self.spec, self.dev, self.eps_l2, self.eps_rms, self.q_scale, gate_log_a, gate_b)
+
+    def workspace_bytes(self, ubatch_tokens: int) -> int:
+        s = self.struct()
+        return self.lib.gdn_workspace_size(ctypes.byref(s), int(ubatch_tokens))
+
+    def new_workspace(self, ubatch_tokens: int) -> torch.Tensor:
+        return torch.empty(self.workspace_bytes(ubatch_tokens), dtype=torch.uint8, device=self.device)
+
+    def new_state(self) -> tuple:
+        sp = self.spec
+        state = torch.zeros(sp.n_v_heads, sp.dv, sp.dk, dtype=torch.float32, device=self.device)
+        conv = torch.zeros(sp.c_conv, 3, dtype=torch.float32, device=self.device)
+        return state, conv
+
+    def prefill(self, x: torch.Tensor, state_in, state_out, conv_state, y, workspace, gate_log_a=None, gate_b=None,
+                stream=None, check=True) -> int:
+        """Enqueue gdn_prefill over x's rows; returns the status (raises if check and it is not 0)."""
+        s = self.struct(gate_log_a, gate_b)
+        return self.lib.gdn_prefill(ctypes.byref(s), gl.ptr(x), x.shape[0], gl.ptr(state_in), gl.ptr(state_out),
+                                    gl.ptr(conv_state), gl.ptr(y), gl.ptr(workspace), workspace.numel(),
+                                    gl.stream_handle(stream), check=check)

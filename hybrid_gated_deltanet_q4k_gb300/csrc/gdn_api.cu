@@ -1,0 +1,386 @@
+// C ABI of the GDN prefill library: argument checks, workspace layout, the
+// ubatch loop of gdn_prefill, and the stage entry points.
+//
+// The batched-prefill entry of the pages refuses what it cannot run instead of
+// falling back (sparkinfer PR #464, discussion: "if (!s.gguf || !c.hybrid ||
+// !c.dense_ffn || n <= 0) return -1;"), and a prefill whose workspace is sized
+// by end position rather than by the tokens in flight collapsed to one token
+// at a time ("CRUX parity spike" #4220, part 2, the 512-row workspace).  Here
+// every unsupported input returns a negative status, and the workspace is
+// sized per ubatch of tokens: when it holds fewer than N tokens the call runs
+// in passes, each an exact extend of the previous one.
+#include "common.cuh"
+
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+
+namespace gdn {
+cudaError_t launch_q4k_deq_i8(const void*, int64_t, int64_t, int8_t*, float*, cudaStream_t);
+cudaError_t launch_q4k_deq_codes(const void*, int64_t, int64_t, uint16_t*, float*, cudaStream_t);
+cudaError_t launch_quant_rows(const uint16_t*, int64_t, int64_t, uint16_t*, float*, cudaStream_t);
+cudaError_t launch_gemm_codes(const uint16_t*, const float*, const uint16_t*, const float*, int64_t, int64_t, int64_t,
+                              uint16_t*, int64_t, int64_t, float*, int64_t, cudaStream_t);
+cudaError_t launch_gemm_f32(const float*, const float*, int64_t, int64_t, int64_t, uint16_t*, int64_t, int64_t, float*,
+                            int64_t, cudaStream_t);
+cudaError_t launch_conv(const gdn_layer&, const uint16_t*, int64_t, int64_t, const float*, const float*, int64_t,
+                        uint16_t*, float*, float*, cudaStream_t);
+cudaError_t launch_conv_state(const gdn_layer&, const uint16_t*, int64_t, int64_t, float*, cudaStream_t);
+cudaError_t launch_delta(const gdn_layer&, const uint16_t*, const float*, const float*, int64_t, const float*, float*,
+                         float*, void*, cudaStream_t);
+size_t delta_scratch_bytes(int hv, int d, int64_t n);
+cudaError_t launch_gated_norm(const gdn_layer&, const float*, const uint16_t*, int64_t, int64_t, uint16_t*, float*,
+                              float*, cudaStream_t);
+int read_and_clear_gemm_error();
+}  // namespace gdn
+
+using namespace gdn;
+
+namespace {
+
+thread_local std::string t_last_error;
+thread_local cudaEvent_t t_stage_events[GDN_N_STAGE_EVENTS];
+thread_local bool t_stage_events_on = false;
+
+// Record stage event i on the stream (first pass only), when instrumentation is on.
+cudaError_t mark(int i, bool first_pass, cudaStream_t st) {
+    if (!t_stage_events_on || !first_pass) return cudaSuccess;
+    return cudaEventRecord(t_stage_events[i], st);
+}
+
+int fail(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+    return fail(GDN_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define GDN_LAUNCH(expr, what)                               \
+    do {                                                     \
+        cudaError_t e_ = (expr);                             \
+        if (e_ != cudaSuccess) return cuda_fail(e_, what);   \
+    } while (0)
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct Sizes {
+    int64_t H, hk, hv, d, c_qk, c_v, c_conv, n_bf16, r_in;
+};
+
+int check_layer(const gdn_layer* L, Sizes* s) {
+    if (!L) return fail(GDN_EINVAL, "layer is NULL");
+    if (L->conv_taps != 4) return fail(GDN_EINVAL, "conv_taps must be 4 (got %d)", L->conv_taps);
+    if (L->wtype != GDN_W_Q4K && L->wtype != GDN_W_F32) return fail(GDN_EINVAL, "unknown wtype %d", L->wtype);
+    if (L->dk != L->dv || (L->dk != 64 && L->dk != 128)) return fail(GDN_EINVAL, "dk = dv in {64, 128} required (got %d, %d)", L->dk, L->dv);
+    if (L->n_qk_heads < 1 || L->n_v_heads < 1 || L->n_v_heads % L->n_qk_heads)
+        return fail(GDN_EINVAL, "n_v_heads must be a positive multiple of n_qk_heads (got %d, %d)", L->n_v_heads, L->n_qk_heads);
+    if (L->n_v_heads > 64) return fail(GDN_EINVAL, "n_v_heads <= 64 required (got %d)", L->n_v_heads);
+    if (L->hidden < 256 || L->hidden > 16384 || L->hidden % 256)
+        return fail(GDN_EINVAL, "hidden must be a multiple of 256 in [256, 16384] (got %d)", L->hidden);
+    s->H = L->hidden;
+    s->hk = L->n_qk_heads;
+    s->hv = L->n_v_heads;
+    s->d = L->dk;
+    s->c_qk = s->hk * s->d;
+    s->c_v = s->hv * s->d;
+    s->c_conv = 2 * s->c_qk + s->c_v;
+    s->n_bf16 = 2 * s->c_qk + 2 * s->c_v;
+    s->r_in = s->n_bf16 + 2 * s->hv;
+    if (s->c_v % 256 || s->c_v > 16384) return fail(GDN_EINVAL, "n_v_heads * dv must be a multiple of 256 and <= 16384 (got %lld)", (long long)s->c_v);
+    if (!L->w_in || !L->w_out || !L->conv_w || !L->A_log || !L->dt_bias || !L->norm_w)
+        return fail(GDN_EINVAL, "a layer weight pointer is NULL");
+    if ((L->gate_log_a == nullptr) != (L->gate_b == nullptr)) return fail(GDN_EINVAL, "gate_log_a and gate_b: both or neither");
+    if (!aligned(L->w_in, 16) || !aligned(L->w_out, 16) || !aligned(L->conv_w, 16))
+        return fail(GDN_EINVAL, "w_in, w_out and conv_w must be 16-byte aligned");
+    if (L->reserved0 != 0) return fail(GDN_EINVAL, "reserved0 must be 0");
+    return GDN_OK;
+}
+
+// Workspace layout for a pass of B tokens.  Every buffer starts on 256 bytes.
+struct Workspace {
+    uint16_t* wc_in; float* ws_in;    // decoded W_in codes [r_in][H], scales [r_in]
+    uint16_t* wc_out; float* ws_out;  // decoded W_out codes [H][c_v], scales [H]
+    uint16_t* xc; float* sx;          // x codes [B][H], scales [B]
+    uint16_t* qkvz;                   // projection, bf16 [B][n_bf16]
+    float* ba;                        // projection, fp32 [B][2 hv]
+    uint16_t* qkv;                    // conv output, bf16 [B][c_conv]
+    float* log_a; float* b;           // gates [B][hv]
+    float* o;                         // recurrence output [B][c_v]
+    uint16_t* oc; float* so;          // gated-norm codes [B][c_v], scales [B]  (Q4_K)
+    float* ohat;                      // gated-norm output [B][c_v]               (F32)
+    void* delta; size_t delta_bytes;  // chunked delta-rule scratch
+    size_t total;
+};
+
+size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+Workspace carve(const gdn_layer* L, const Sizes& s, int64_t B, void* base) {
+    Workspace w{};
+    uint8_t* p = static_cast<uint8_t*>(base);
+    size_t off = 0;
+    auto take = [&](size_t bytes) -> void* {
+        void* r = p ? static_cast<void*>(p + off) : nullptr;
+        off += up256(bytes);
+        return r;
+    };
+    const bool q4k = L->wtype == GDN_W_Q4K;
+    if (q4k) {
+        w.wc_in = static_cast<uint16_t*>(take(s.r_in * s.H * 2));
+        w.ws_in = static_cast<float*>(take(s.r_in * 4));
+        w.wc_out = static_cast<uint16_t*>(take(s.H * s.c_v * 2));
+        w.ws_out = static_cast<float*>(take(s.H * 4));
+        w.xc = static_cast<uint16_t*>(take(B * s.H * 2));
+        w.sx = static_cast<float*>(take(B * 4));
+        w.oc = static_cast<uint16_t*>(take(B * s.c_v * 2));
+        w.so = static_cast<float*>(take(B * 4));
+    } else {
+        w.ohat = static_cast<float*>(take(B * s.c_v * 4));
+    }
+    w.qkvz = static_cast<uint16_t*>(take(B * s.n_bf16 * 2));
+    w.ba = static_cast<float*>(take(B * 2 * s.hv * 4));
+    w.qkv = static_cast<uint16_t*>(take(B * s.c_conv * 2));
+    w.log_a = static_cast<float*>(take(B * s.hv * 4));
+    w.b = static_cast<float*>(take(B * s.hv * 4));
+    w.o = static_cast<float*>(take(B * s.c_v * 4));
+    w.delta_bytes = delta_scratch_bytes(static_cast<int>(s.hv), static_cast<int>(s.d), B);
+    w.delta = take(w.delta_bytes);
+    w.total = off;
+    return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* gdn_last_error(void) { return t_last_error.c_str(); }
+
+int gdn_set_stage_events(void* const* events, int n_events) {
+    if (n_events == 0) {
+        t_stage_events_on = false;
+        return GDN_OK;
+    }
+    if (n_events != GDN_N_STAGE_EVENTS || !events) return fail(GDN_EINVAL, "gdn_set_stage_events: n_events must be 0 or %d", GDN_N_STAGE_EVENTS);
+    for (int i = 0; i < GDN_N_STAGE_EVENTS; ++i) {
+        if (!events[i]) return fail(GDN_EINVAL, "gdn_set_stage_events: event %d is NULL", i);
+        t_stage_events[i] = static_cast<cudaEvent_t>(events[i]);
+    }
+    t_stage_events_on = true;
+    return GDN_OK;
+}
+
+int q4k_deq_i8(const void* blocks, int64_t rows, int64_t cols, int8_t* q, float* row_scale, void* stream) {
+    if (!blocks || !q || !row_scale) return fail(GDN_EINVAL, "q4k_deq_i8: NULL pointer");
+    if (rows < 1 || rows > 0x7fffffff || cols < 256 || cols > 16384 || cols % 256)
+        return fail(GDN_EINVAL, "q4k_deq_i8: rows >= 1 and cols a multiple of 256 in [256, 16384] required");
+    if (!aligned(blocks, 16) || !aligned(q, 8)) return fail(GDN_EINVAL, "q4k_deq_i8: blocks 16-byte and q 8-byte alignment required");
+    GDN_LAUNCH(launch_q4k_deq_i8(blocks, rows, cols, q, row_scale, static_cast<cudaStream_t>(stream)), "q4k_deq_i8");
+    return GDN_OK;
+}
+
+int gdn_q4k_deq_codes(const void* blocks, int64_t rows, int64_t cols, uint16_t* codes, float* row_scale, void* stream) {
+    if (!blocks || !codes || !row_scale) return fail(GDN_EINVAL, "gdn_q4k_deq_codes: NULL pointer");
+    if (rows < 1 || rows > 0x7fffffff || cols < 256 || cols > 16384 || cols % 256)
+        return fail(GDN_EINVAL, "gdn_q4k_deq_codes: rows >= 1 and cols a multiple of 256 in [256, 16384] required");
+    if (!aligned(blocks, 16) || !aligned(codes, 16)) return fail(GDN_EINVAL, "gdn_q4k_deq_codes: 16-byte alignment required");
+    GDN_LAUNCH(launch_q4k_deq_codes(blocks, rows, cols, codes, row_scale, static_cast<cudaStream_t>(stream)), "gdn_q4k_deq_codes");
+    return GDN_OK;
+}
+
+int gdn_quant_rows(const uint16_t* x, int64_t rows, int64_t cols, uint16_t* codes, float* scale, void* stream) {
+    if (!x || !codes || !scale) return fail(GDN_EINVAL, "gdn_quant_rows: NULL pointer");
+    if (rows < 1 || rows > 0x7fffffff || cols < 8 || cols > 16384 || cols % 8)
+        return fail(GDN_EINVAL, "gdn_quant_rows: rows >= 1 and cols a multiple of 8 in [8, 16384] required");
+    if (!aligned(x, 16) || !aligned(codes, 16)) return fail(GDN_EINVAL, "gdn_quant_rows: 16-byte alignment required");
+    GDN_LAUNCH(launch_quant_rows(x, rows, cols, codes, scale, static_cast<cudaStream_t>(stream)), "gdn_quant_rows");
+    return GDN_OK;
+}
+
+int gdn_gemm_codes(const uint16_t* a, const float* sa, const uint16_t* b, const float* sb, int64_t M, int64_t Nn,
+                   int64_t K, uint16_t* out_bf16, int64_t ld_bf16, int64_t n_bf16, float* out_f32, int64_t ld_f32,
+                   void* stream) {
+    if (!a || !sa || !b || !sb) return fail(GDN_EINVAL, "gdn_gemm_codes: NULL operand");
+    if (M < 1 || Nn < 1 || M > 0x7fffffff || Nn > 0x7fffffff || K < 64 || K > 65536 || K % 64)
+        return fail(GDN_EINVAL, "gdn_gemm_codes: M, N >= 1 and K a multiple of 64 in [64, 65536] required");
+    if (n_bf16 < 0) return fail(GDN_EINVAL, "gdn_gemm_codes: n_bf16 < 0");
+    if (n_bf16 > 0 && (!out_bf16 || ld_bf16 < (n_bf16 < Nn ? n_bf16 : Nn))) return fail(GDN_EINVAL, "gdn_gemm_codes: bf16 output");
+    if (n_bf16 < Nn && (!out_f32 || ld_f32 < Nn - n_bf16)) return fail(GDN_EINVAL, "gdn_gemm_codes: fp32 output");
+    if (!aligned(a, 16) || !aligned(b, 16)) return fail(GDN_EINVAL, "gdn_gemm_codes: operands must be 16-byte aligned");
+    cudaError_t e = launch_gemm_codes(a, sa, b, sb, M, Nn, K, out_bf16, ld_bf16, n_bf16, out_f32, ld_f32,
+                                      static_cast<cudaStream_t>(stream));
+    if (e == cudaErrorInvalidValue) return fail(GDN_EINVAL, "gdn_gemm_codes: tensor map rejected (alignment or driver entry point)");
+    if (e != cudaSuccess) return cuda_fail(e, "gdn_gemm_codes");
+    return GDN_OK;
+}
+
+int gdn_gemm_f32(const float* a, const float* b, int64_t M, int64_t Nn, int64_t K, uint16_t* out_bf16, int64_t ld_bf16,
+                 int64_t n_bf16, float* out_f32, int64_t ld_f32, void* stream) {
+    if (!a || !b) return fail(GDN_EINVAL, "gdn_gemm_f32: NULL operand");
+    if (M < 1 || Nn < 1 || K < 1 || M > 0x7fffffff || Nn > 0x7fffffff || K > 0x7fffffff) return fail(GDN_EINVAL, "gdn_gemm_f32: sizes");
+    if (n_bf16 < 0) return fail(GDN_EINVAL, "gdn_gemm_f32: n_bf16 < 0");
+    if (n_bf16 > 0 && !out_bf16) return fail(GDN_EINVAL, "gdn_gemm_f32: bf16 output");
+    if (n_bf16 < Nn && !out_f32) return fail(GDN_EINVAL, "gdn_gemm_f32: fp32 output");
+    GDN_LAUNCH(launch_gemm_f32(a, b, M, Nn, K, out_bf16, ld_bf16, n_bf16, out_f32, ld_f32, static_cast<cudaStream_t>(stream)),
+               "gdn_gemm_f32");
+    return GDN_OK;
+}
+
+int gdn_conv(const gdn_layer* layer, const uint16_t* qkvz, int64_t ld_qkvz, int64_t n_tokens, const float* conv_state,
+             const float* ba, int64_t ld_ba, uint16_t* qkv, float* log_a, float* b, void* stream) {
+    Sizes s;
+    int r = check_layer(layer, &s);
+    if (r) return r;
+    if (n_tokens < 1 || n_tokens > 0x7fffffff) return fail(GDN_EINVAL, "gdn_conv: n_tokens >= 1 required");
+    if (!qkvz || !conv_state || !qkv) return fail(GDN_EINVAL, "gdn_conv: NULL pointer");
+    if (ld_qkvz < s.c_conv || ld_qkvz % 4 || !aligned(qkvz, 8)) return fail(GDN_EINVAL, "gdn_conv: qkvz layout");
+    if (layer->gate_log_a == nullptr && (!ba || !log_a || !b || ld_ba < 2 * s.hv)) return fail(GDN_EINVAL, "gdn_conv: gate buffers");
+    GDN_LAUNCH(launch_conv(*layer, qkvz, ld_qkvz, n_tokens, conv_state, ba, ld_ba, qkv, log_a, b, static_cast<cudaStream_t>(stream)),
+               "gdn_conv");
+    return GDN_OK;
+}
+
+int gdn_conv_state_update(const gdn_layer* layer, const uint16_t* qkvz, int64_t ld_qkvz, int64_t n_tokens,
+                          float* conv_state, void* stream) {
+    Sizes s;
+    int r = check_layer(layer, &s);
+    if (r) return r;
+    if (n_tokens < 1 || !qkvz || !conv_state || ld_qkvz < s.c_conv) return fail(GDN_EINVAL, "gdn_conv_state_update: arguments");
+    GDN_LAUNCH(launch_conv_state(*layer, qkvz, ld_qkvz, n_tokens, conv_state, static_cast<cudaStream_t>(stream)),
+               "gdn_conv_state_update");
+    return GDN_OK;
+}
+
+size_t gdn_delta_rule_scratch_size(const gdn_layer* layer, int64_t n_tokens) {
+    Sizes s;
+    if (check_layer(layer, &s) || n_tokens < 1) return 0;
+    return delta_scratch_bytes(static_cast<int>(s.hv), static_cast<int>(s.d), n_tokens);
+}
+
+int gdn_delta_rule(const gdn_layer* layer, const uint16_t* qkv, const float* log_a, const float* b, int64_t n_tokens,
+                   const float* state_in, float* state_out, float* o, void* scratch, size_t scratch_bytes, void* stream) {
+    Sizes s;
+    int r = check_layer(layer, &s);
+    if (r) return r;
+    if (n_tokens < 1 || n_tokens > 0x7fffffff) return fail(GDN_EINVAL, "gdn_delta_rule: n_tokens >= 1 required");
+    if (!qkv || !log_a || !b || !state_out || !o || !scratch) return fail(GDN_EINVAL, "gdn_delta_rule: NULL pointer");
+    if (scratch_bytes < delta_scratch_bytes(static_cast<int>(s.hv), static_cast<int>(s.d), n_tokens))
+        return fail(GDN_ENOMEM, "gdn_delta_rule: scratch too small");
+    GDN_LAUNCH(launch_delta(*layer, qkv, log_a, b, n_tokens, state_in, state_out, o, scratch, static_cast<cudaStream_t>(stream)),
+               "gdn_delta_rule");
+    return GDN_OK;
+}
+
+int gdn_gated_norm(const gdn_layer* layer, const float* o, const uint16_t* z, int64_t ld_z, int64_t n_tokens,
+                   uint16_t* codes, float* scale, float* out_f32, void* stream) {
+    Sizes s;
+    int r = check_layer(layer, &s);
+    if (r) return r;
+    if (n_tokens < 1 || n_tokens > 0x7fffffff || !o || !z) return fail(GDN_EINVAL, "gdn_gated_norm: arguments");
+    if (ld_z < s.c_v || ld_z % 4 || !aligned(z, 8) || !aligned(o, 16)) return fail(GDN_EINVAL, "gdn_gated_norm: layout");
+    if (layer->wtype == GDN_W_Q4K && (!codes || !scale || !aligned(codes, 8))) return fail(GDN_EINVAL, "gdn_gated_norm: codes");
+    if (layer->wtype == GDN_W_F32 && !out_f32) return fail(GDN_EINVAL, "gdn_gated_norm: out_f32");
+    GDN_LAUNCH(launch_gated_norm(*layer, o, z, ld_z, n_tokens, codes, scale, out_f32, static_cast<cudaStream_t>(stream)),
+               "gdn_gated_norm");
+    return GDN_OK;
+}
+
+size_t gdn_workspace_size(const gdn_layer* layer, int64_t ubatch_tokens) {
+    Sizes s;
+    if (check_layer(layer, &s) || ubatch_tokens < 1) return 0;
+    return carve(layer, s, ubatch_tokens, nullptr).total;
+}
+
+int gdn_prefill(const gdn_layer* layer, const void* x, int64_t n_tokens, const float* state_in, float* state_out,
+                float* conv_state, void* y, void* workspace, size_t ws_bytes, void* stream) {
+    Sizes s;
+    int r = check_layer(layer, &s);
+    if (r) return r;
+    if (n_tokens < 1 || n_tokens > 0x7fffffff) return fail(GDN_EINVAL, "gdn_prefill: n_tokens >= 1 required (got %lld)", (long long)n_tokens);
+    if (!x || !state_out || !conv_state || !y || !workspace) return fail(GDN_EINVAL, "gdn_prefill: NULL pointer");
+    if (!aligned(x, 16) || !aligned(y, 16) || !aligned(workspace, 256)) return fail(GDN_EINVAL, "gdn_prefill: x, y 16-byte and workspace 256-byte alignment required");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // Largest pass that fits: the workspace grows linearly in B.
+    const size_t w1 = carve(layer, s, 1, nullptr).total;
+    if (ws_bytes < w1) return fail(GDN_ENOMEM, "gdn_prefill: workspace %zu B < %zu B needed for one token", ws_bytes, w1);
+    int64_t B = n_tokens;
+    if (carve(layer, s, B, nullptr).total > ws_bytes) {
+        int64_t lo = 1, hi = n_tokens;  // carve(lo) fits, carve(hi) does not
+        while (hi - lo > 1) {
+            const int64_t mid = lo + (hi - lo) / 2;
+            if (carve(layer, s, mid, nullptr).total <= ws_bytes) lo = mid; else hi = mid;
+        }
+        B = lo >= GDN_CHUNK ? lo - lo % GDN_CHUNK : lo;
+    }
+    Workspace w = carve(layer, s, B, workspace);
+    const bool q4k = layer->wtype == GDN_W_Q4K;
+    GDN_LAUNCH(mark(0, true, st), "stage event");
+    if (q4k) {
+        GDN_LAUNCH(launch_q4k_deq_codes(layer->w_in, s.r_in, s.H, w.wc_in, w.ws_in, st), "dequant W_in");
+        GDN_LAUNCH(launch_q4k_deq_codes(layer->w_out, s.H, s.c_v, w.wc_out, w.ws_out, st), "dequant W_out");
+    }
+    GDN_LAUNCH(mark(1, true, st), "stage event");
+    for (int64_t u0 = 0; u0 < n_tokens; u0 += B) {
+        const int64_t nb = (n_tokens - u0) < B ? (n_tokens - u0) : B;
+        const bool first = u0 == 0;
+        if (q4k) {
+            const uint16_t* xs = static_cast<const uint16_t*>(x) + u0 * s.H;
+            GDN_LAUNCH(launch_quant_rows(xs, nb, s.H, w.xc, w.sx, st), "quantise x");
+            GDN_LAUNCH(mark(2, first, st), "stage event");
+            cudaError_t e = launch_gemm_codes(w.xc, w.sx, w.wc_in, w.ws_in, nb, s.r_in, s.H, w.qkvz, s.n_bf16, s.n_bf16,
+                                              w.ba, 2 * s.hv, st);
+            if (e != cudaSuccess) return cuda_fail(e, "input projection");
+        } else {
+            GDN_LAUNCH(mark(2, first, st), "stage event");
+            const float* xs = static_cast<const float*>(x) + u0 * s.H;
+            GDN_LAUNCH(launch_gemm_f32(xs, static_cast<const float*>(layer->w_in), nb, s.r_in, s.H, w.qkvz, s.n_bf16,
+                                       s.n_bf16, w.ba, 2 * s.hv, st),
+                       "input projection");
+        }
+        GDN_LAUNCH(mark(3, first, st), "stage event");
+        gdn_layer lu = *layer;
+        if (layer->gate_log_a) {
+            lu.gate_log_a = layer->gate_log_a + u0 * s.hv;
+            lu.gate_b = layer->gate_b + u0 * s.hv;
+        }
+        GDN_LAUNCH(launch_conv(lu, w.qkvz, s.n_bf16, nb, conv_state, w.ba, 2 * s.hv, w.qkv, w.log_a, w.b, st), "conv");
+        GDN_LAUNCH(launch_conv_state(lu, w.qkvz, s.n_bf16, nb, conv_state, st), "conv state");
+        GDN_LAUNCH(mark(4, first, st), "stage event");
+        const float* la = lu.gate_log_a ? lu.gate_log_a : w.log_a;
+        const float* bb = lu.gate_b ? lu.gate_b : w.b;
+        GDN_LAUNCH(launch_delta(lu, w.qkv, la, bb, nb, first ? state_in : state_out, state_out, w.o, w.delta, st),
+                   "delta rule");
+        GDN_LAUNCH(mark(5, first, st), "stage event");
+        const uint16_t* z = w.qkvz + s.c_conv;
+        GDN_LAUNCH(launch_gated_norm(lu, w.o, z, s.n_bf16, nb, w.oc, w.so, w.ohat, st), "gated norm");
+        GDN_LAUNCH(mark(6, first, st), "stage event");
+        if (q4k) {
+            uint16_t* ys = static_cast<uint16_t*>(y) + u0 * s.H;
+            cudaError_t e = launch_gemm_codes(w.oc, w.so, w.wc_out, w.ws_out, nb, s.H, s.c_v, ys, s.H, s.H, nullptr, 0, st);
+            if (e != cudaSuccess) return cuda_fail(e, "output projection");
+        } else {
+            float* ys = static_cast<float*>(y) + u0 * s.H;
+            GDN_LAUNCH(launch_gemm_f32(w.ohat, static_cast<const float*>(layer->w_out), nb, s.H, s.c_v, nullptr, 0, 0, ys,
+                                       s.H, st),
+                       "output projection");
+        }
+        GDN_LAUNCH(mark(7, first, st), "stage event");
+    }
+    return GDN_OK;
+}
+
+int gdn_sync_status(void* stream) {
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "gdn_sync_status");
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "gdn_sync_status");
+    if (read_and_clear_gemm_error()) return fail(GDN_ETIMEOUT, "a bounded wait in the projection kernel ran out");
+    return GDN_OK;
+}
+
+}  // extern "C"

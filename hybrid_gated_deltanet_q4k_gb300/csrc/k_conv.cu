@@ -1,0 +1,197 @@
+// Step 2: token-parallel causal 4-tap depthwise conv + SiLU + per-head L2 norm,
+// and the gates.
+//
+// sparkinfer PR #464 ("fused Q4K/Q6K->int8 dequant + token-parallel GDN conv
+// ..."), Summary, "Token-parallel GDN conv": the causal 4-tap conv reads only
+// the raw projected inputs, so every token is independent; the page runs one
+// block per (token, head) with the taps, SiLU, L2 norm and conv-state layout
+// of the sequential kernel it replaced.
+//
+// Here one warp owns one head (dk = dv = d channels, d/32 per lane) over a
+// run of CONV_TOKENS consecutive tokens and keeps the last three raw inputs of
+// its channels in registers, so each raw input is read from HBM once (plus a
+// three-token halo per run).  The L2 norm of a q or k head is a warp
+// reduction.  Inputs and outputs are bf16; arithmetic is fp32.
+//
+// Gates (when not drawn directly): log a = -exp(A_log) * softplus(alpha +
+// dt_bias), b = sigmoid(beta), from the fp32 beta | alpha columns of the
+// projection; computed by the extra blocks of the same launch.
+#include "common.cuh"
+
+namespace gdn {
+
+constexpr int CONV_WARPS = 8;
+constexpr int CONV_TOKENS = 64;
+
+struct ConvArgs {
+    const uint16_t* qkvz;
+    int64_t ld_qkvz;
+    int n;
+    int c_qk;        // q channels (= k channels)
+    int c_conv;
+    int d;           // head dim (dk = dv)
+    int n_heads;     // 2*Hk + Hv heads of d channels
+    int n_qk_norm;   // heads 0 .. 2*Hk-1 are L2-normed
+    int n_q;         // heads 0 .. Hk-1 are q (scaled)
+    float eps;
+    float q_scale;
+    const float* conv_w;   // [c_conv][4]
+    const float* tail;     // [c_conv][3]
+    uint16_t* out;         // [n][c_conv]
+    // gates
+    const float* ba;
+    int64_t ld_ba;
+    int hv;
+    const float* A_log;
+    const float* dt_bias;
+    float* log_a;
+    float* b;
+    int conv_blocks_y;     // gridDim.y slices that run the conv; the rest run gates
+};
+
+template <int CPL>
+__device__ __forceinline__ void conv_head_run(const ConvArgs& a, int head, int t0) {
+    const int lane = threadIdx.x & 31;
+    const int c0 = head * a.d + lane * CPL;
+    float w[CPL][4];
+    float h0[CPL], h1[CPL], h2[CPL];  // x_{t-3}, x_{t-2}, x_{t-1}
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+        const float4 wv = *reinterpret_cast<const float4*>(a.conv_w + static_cast<int64_t>(c0 + i) * 4);
+        w[i][0] = wv.x; w[i][1] = wv.y; w[i][2] = wv.z; w[i][3] = wv.w;
+    }
+    auto raw = [&](int t, int i) -> float {
+        // raw input x_t of channel c0+i; t < 0 reads the conv state (oldest first)
+        if (t >= 0) return bf16_bits_to_float(a.qkvz[static_cast<int64_t>(t) * a.ld_qkvz + c0 + i]);
+        return a.tail[static_cast<int64_t>(c0 + i) * 3 + (3 + t)];
+    };
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+        h0[i] = raw(t0 - 3, i);
+        h1[i] = raw(t0 - 2, i);
+        h2[i] = raw(t0 - 1, i);
+    }
+    const bool norm = head < a.n_qk_norm;
+    const float mul = head < a.n_q ? a.q_scale : 1.0f;
+    const int t1 = min(a.n, t0 + CONV_TOKENS);
+    for (int t = t0; t < t1; ++t) {
+        float x[CPL];
+        const uint16_t* src = a.qkvz + static_cast<int64_t>(t) * a.ld_qkvz + c0;
+        if (CPL == 4) {
+            const uint2 u = *reinterpret_cast<const uint2*>(src);
+            x[0] = __uint_as_float(u.x << 16); x[1] = __uint_as_float(u.x & 0xffff0000u);
+            x[2 % CPL] = __uint_as_float(u.y << 16); x[3 % CPL] = __uint_as_float(u.y & 0xffff0000u);
+        } else {
+            const uint32_t u = *reinterpret_cast<const uint32_t*>(src);
+            x[0] = __uint_as_float(u << 16); x[1 % CPL] = __uint_as_float(u & 0xffff0000u);
+        }
+        float y[CPL];
+        float ss = 0.0f;
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) {
+            float u = w[i][0] * h0[i];
+            u = fmaf(w[i][1], h1[i], u);
+            u = fmaf(w[i][2], h2[i], u);
+            u = fmaf(w[i][3], x[i], u);
+            y[i] = silu_f(u);
+            ss = fmaf(y[i], y[i], ss);
+            h0[i] = h1[i]; h1[i] = h2[i]; h2[i] = x[i];
+        }
+        if (norm) {
+            ss = warp_sum(ss);
+            const float r = rsqrtf(ss + a.eps) * mul;
+#pragma unroll
+            for (int i = 0; i < CPL; ++i) y[i] *= r;
+        }
+        uint16_t* dst = a.out + static_cast<int64_t>(t) * a.c_conv + c0;
+        if (CPL == 4) {
+            const uint32_t lo = static_cast<uint32_t>(float_to_bf16_bits(y[0])) | (static_cast<uint32_t>(float_to_bf16_bits(y[1 % CPL])) << 16);
+            const uint32_t hi = static_cast<uint32_t>(float_to_bf16_bits(y[2 % CPL])) | (static_cast<uint32_t>(float_to_bf16_bits(y[3 % CPL])) << 16);
+            *reinterpret_cast<uint2*>(dst) = make_uint2(lo, hi);
+        } else {
+            *reinterpret_cast<uint32_t*>(dst) = static_cast<uint32_t>(float_to_bf16_bits(y[0])) |
+                                                (static_cast<uint32_t>(float_to_bf16_bits(y[1 % CPL])) << 16);
+        }
+    }
+}
+
+template <int CPL>
+__global__ void __launch_bounds__(CONV_WARPS * 32) conv_kernel(ConvArgs a) {
+    const int t0 = blockIdx.x * CONV_TOKENS;
+    if (static_cast<int>(blockIdx.y) < a.conv_blocks_y) {
+        const int head = blockIdx.y * CONV_WARPS + (threadIdx.x >> 5);
+        if (head < a.n_heads) conv_head_run<CPL>(a, head, t0);
+        return;
+    }
+    // gate block: tokens t0 .. t0+CONV_TOKENS-1, all value heads
+    const int t1 = min(a.n, t0 + CONV_TOKENS);
+    for (int i = threadIdx.x; i < (t1 - t0) * a.hv; i += blockDim.x) {
+        const int t = t0 + i / a.hv, h = i % a.hv;
+        const float beta = a.ba[static_cast<int64_t>(t) * a.ld_ba + h];
+        const float alpha = a.ba[static_cast<int64_t>(t) * a.ld_ba + a.hv + h];
+        const float u = alpha + a.dt_bias[h];
+        const float sp = fmaxf(u, 0.0f) + log1pf(expf(-fabsf(u)));
+        a.log_a[static_cast<int64_t>(t) * a.hv + h] = -expf(a.A_log[h]) * sp;
+        a.b[static_cast<int64_t>(t) * a.hv + h] = 1.0f / (1.0f + expf(-beta));
+    }
+}
+
+cudaError_t launch_conv(const gdn_layer& L, const uint16_t* qkvz, int64_t ld_qkvz, int64_t n, const float* tail,
+                        const float* ba, int64_t ld_ba, uint16_t* out, float* log_a, float* b, cudaStream_t st) {
+    ConvArgs a;
+    a.qkvz = qkvz;
+    a.ld_qkvz = ld_qkvz;
+    a.n = static_cast<int>(n);
+    a.c_qk = L.n_qk_heads * L.dk;
+    a.c_conv = 2 * a.c_qk + L.n_v_heads * L.dv;
+    a.d = L.dk;
+    a.n_heads = 2 * L.n_qk_heads + L.n_v_heads;
+    a.n_qk_norm = 2 * L.n_qk_heads;
+    a.n_q = L.n_qk_heads;
+    a.eps = L.eps_l2;
+    a.q_scale = L.q_scale;
+    a.conv_w = L.conv_w;
+    a.tail = tail;
+    a.out = out;
+    a.ba = ba;
+    a.ld_ba = ld_ba;
+    a.hv = L.n_v_heads;
+    a.A_log = L.A_log;
+    a.dt_bias = L.dt_bias;
+    a.log_a = log_a;
+    a.b = b;
+    a.conv_blocks_y = (a.n_heads + CONV_WARPS - 1) / CONV_WARPS;
+    const bool gates = L.gate_log_a == nullptr;
+    dim3 grid(static_cast<unsigned>((n + CONV_TOKENS - 1) / CONV_TOKENS), static_cast<unsigned>(a.conv_blocks_y + (gates ? 1 : 0)));
+    if (L.dk == 128)
+        conv_kernel<4><<<grid, CONV_WARPS * 32, 0, st>>>(a);
+    else
+        conv_kernel<2><<<grid, CONV_WARPS * 32, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+// conv_state <- the last three raw inputs per channel (x_{N-3}, x_{N-2}, x_{N-1}),
+// from the projection, or from the old state for N < 3.  One thread per channel
+// reads its three old values before writing, so the update is in place.
+__global__ void conv_state_kernel(const uint16_t* __restrict__ qkvz, int64_t ld, int n, int c_conv, float* state) {
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= c_conv) return;
+    float old[3] = {state[c * 3 + 0], state[c * 3 + 1], state[c * 3 + 2]};
+    float nw[3];
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+        const int t = n - 3 + j;
+        nw[j] = t >= 0 ? bf16_bits_to_float(qkvz[static_cast<int64_t>(t) * ld + c]) : old[3 + t];
+    }
+#pragma unroll
+    for (int j = 0; j < 3; ++j) state[c * 3 + j] = nw[j];
+}
+
+cudaError_t launch_conv_state(const gdn_layer& L, const uint16_t* qkvz, int64_t ld, int64_t n, float* state,
+                              cudaStream_t st) {
+    const int c_conv = 2 * L.n_qk_heads * L.dk + L.n_v_heads * L.dv;
+    conv_state_kernel<<<(c_conv + 255) / 256, 256, 0, st>>>(qkvz, ld, static_cast<int>(n), c_conv, state);
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -1,0 +1,505 @@
+// Steps 1c and 5: the quantised projections, out = ((float)(A . B^T) * sa) * sb.
+//
+// The pages feed int8 weight rows and int8 activations to an int8 tensor-core
+// GEMM (sparkinfer PR #464, Summary: "int8 tensor-core GEMM"; its follow-up
+// "int8-native prefill GEMM (mma.sync m16n8k32)").  sm_103a's fifth-generation
+// tensor cores have no int8 MMA kind (ptxas rejects tcgen05.mma .kind::i8 for
+// sm_103a), so the same integer product is taken on fp16 operands: every int8
+// code is exact in fp16, every product (|q| <= 127, so < 2^14) is exact, and an
+// fp32 accumulator holds every partial sum of up to 1024 such products exactly
+// (1024 * 127^2 < 2^24).  The K loop therefore runs in segments of 1024: each
+// segment accumulates in its own TMEM buffer, the epilogue converts the
+// segment to int32 and sums the segments in registers.  The result is the
+// exact integer product whatever the data.
+//
+// Kernel structure (one persistent CTA per SM, 320 threads):
+//   warp 0      TMA producer: 128x64 A tile + 256x64 B tile per stage into
+//               128-byte-swizzled shared memory, 4 stages (48 KB each);
+//   warp 1      TMEM allocator and MMA issuer: tcgen05.mma kind::f16,
+//               M=128 N=256 K=16, one elected thread, fp32 accumulators in
+//               two 256-column TMEM buffers (one per K segment, ping-pong);
+//   warps 2-9   epilogue: tcgen05.ld of each finished segment (warp w reads
+//               TMEM lanes 32*(w%4).., half (w-2)/4 of the 256 columns), int32
+//               running sums in registers, then the fp32 rescale and the
+//               stores.  The buffer is released right after it is read, so
+//               the next segment's MMAs overlap the conversion and stores.
+// Every wait is bounded (about two seconds); a wait that runs out records
+// ERR_WAIT_TIMEOUT in this unit's error word and the CTA winds down: it waits
+// (bounded) for its own TMA copies and MMAs in flight, frees its TMEM and
+// returns.
+#include "common.cuh"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+namespace gdn {
+
+static __device__ int g_gemm_error;
+
+namespace tc {
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;               // fp16 elements = 128 bytes = one swizzle row
+constexpr int STAGES = 4;
+constexpr int SEG_KB = 16;           // k-blocks per exact fp32 segment (16 * 64 = 1024)
+constexpr int A_BYTES = BM * BK * 2; // 16 KB
+constexpr int B_BYTES = BN * BK * 2; // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int NUM_EPI_WARPS = 8;
+constexpr int THREADS = 64 + NUM_EPI_WARPS * 32;
+constexpr uint32_t TMEM_COLS = 512;  // two accumulator buffers of BN columns
+constexpr int BAR_BYTES = 256;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;  // + alignment slack
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
+constexpr uint64_t DRAIN_LIMIT_NS = 20000000ull;
+
+// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B fp16
+// (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0), N>>3 at bits 17-22,
+// M>>4 at bits 24-28.
+constexpr uint32_t IDESC = (1u << 4) | (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
+}  // namespace tc
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase of `bar` with the given parity to complete.  Gives up
+// when another role has aborted, or after `limit` ns (recording the timeout).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          uint64_t limit = tc::WAIT_LIMIT_NS) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (global_ns() - t0 > limit) {
+            atomicCAS(&g_gemm_error, 0, ERR_WAIT_TIMEOUT);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor, K-major, 128-byte swizzle: start address
+// >> 4 (bits 0-13), stride between 8-row groups 1024 B >> 4 (bits 32-45),
+// descriptor version 1 (bit 46), swizzle mode 2 = 128 B (bits 61-63).  The
+// leading-dimension offset is unused for swizzled K-major operands whose K
+// extent per MMA (32 B) stays inside one 128-byte swizzle row.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(1) << 16) |
+           (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+           (static_cast<uint64_t>(2) << 61);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(tc::IDESC), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+struct GemmArgs {
+    const float* sa;
+    const float* sb;
+    int M, N, K;
+    uint16_t* out_bf16;
+    int64_t ld_bf16;
+    int n_bf16;
+    float* out_f32;
+    int64_t ld_f32;
+    int vec_ok;  // 16-byte vector stores are aligned
+};
+
+__device__ __forceinline__ void store_group8(const GemmArgs& g, int row, int n, const float* y) {
+    if (g.vec_ok && n + 8 <= g.N && n + 8 <= g.n_bf16) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            w[i] = static_cast<uint32_t>(float_to_bf16_bits(y[2 * i])) |
+                   (static_cast<uint32_t>(float_to_bf16_bits(y[2 * i + 1])) << 16);
+        *reinterpret_cast<uint4*>(g.out_bf16 + row * g.ld_bf16 + n) = make_uint4(w[0], w[1], w[2], w[3]);
+    } else if (g.vec_ok && n >= g.n_bf16 && n + 8 <= g.N) {
+        float4* p = reinterpret_cast<float4*>(g.out_f32 + row * g.ld_f32 + (n - g.n_bf16));
+        p[0] = make_float4(y[0], y[1], y[2], y[3]);
+        p[1] = make_float4(y[4], y[5], y[6], y[7]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int c = n + j;
+            if (c < g.N) {
+                if (c < g.n_bf16)
+                    g.out_bf16[row * g.ld_bf16 + c] = float_to_bf16_bits(y[j]);
+                else
+                    g.out_f32[row * g.ld_f32 + (c - g.n_bf16)] = y[j];
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(tc::THREADS, 1)
+gemm_codes_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmArgs g) {
+    using namespace tc;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    uint64_t* empty = full + STAGES;
+    uint64_t* acc_full = empty + STAGES;
+    uint64_t* acc_empty = acc_full + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int num_m = (g.M + BM - 1) / BM, num_n = (g.N + BN - 1) / BN;
+    const int num_tiles = num_m * num_n;
+    const int nkb = g.K / BK;
+    const int nseg = (nkb + SEG_KB - 1) / SEG_KB;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], NUM_EPI_WARPS * 32);
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+            uint32_t stage = 0, phase = 0;
+            uint32_t armed = 0;              // bit s: stage s has been filled at least once
+            uint32_t armed_parity = 0;       // bit s: parity of its last fill
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                const int m0 = (tile / num_n) * BM, n0 = (tile % num_n) * BN;
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
+                    uint8_t* sA = smem + stage * STAGE_BYTES;
+                    mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+                    tma_load_2d(sA, &tmA, &full[stage], kb * BK, m0);
+                    tma_load_2d(sA + A_BYTES, &tmB, &full[stage], kb * BK, n0);
+                    armed |= 1u << stage;
+                    armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+            // Let every copy this thread issued land before the CTA exits.
+            for (int s = 0; s < STAGES; ++s)
+                if (armed & (1u << s)) {
+                    int dummy = 0;
+                    mbar_wait(&full[s], (armed_parity >> s) & 1u, reinterpret_cast<volatile int*>(&dummy), DRAIN_LIMIT_NS);
+                }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------ MMA issuer
+            uint32_t stage = 0, phase = 0, acc_ctr = 0;
+            bool ok = true, committed = false;
+            uint32_t last_buf = 0, last_par = 0;
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                for (int seg = 0; ok && seg < nseg; ++seg) {
+                    const uint32_t buf = acc_ctr & 1u, par = (acc_ctr >> 1) & 1u;
+                    if (!mbar_wait(&acc_empty[buf], par ^ 1u, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + buf * BN;
+                    const int kb0 = seg * SEG_KB, kb1 = min(nkb, kb0 + SEG_KB);
+                    for (int kb = kb0; kb < kb1; ++kb) {
+                        if (!mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint32_t sa_addr = smem_u32(smem + stage * STAGE_BYTES);
+                        const uint64_t adesc = sw128_desc(sa_addr);
+                        const uint64_t bdesc = sw128_desc(sa_addr + A_BYTES);
+#pragma unroll
+                        for (int kk = 0; kk < BK / 16; ++kk)
+                            mma_f16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, (kb > kb0 || kk > 0) ? 1u : 0u);
+                        mma_commit(&empty[stage]);
+                        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                    }
+                    mma_commit(&acc_full[buf]);
+                    committed = true;
+                    last_buf = buf;
+                    last_par = par;
+                    ++acc_ctr;
+                }
+            }
+            // Let the last MMAs finish before TMEM is freed.
+            if (committed) {
+                int dummy = 0;
+                mbar_wait(&acc_full[last_buf], last_par, reinterpret_cast<volatile int*>(&dummy), DRAIN_LIMIT_NS);
+            }
+        }
+    } else {
+        // ---------------------------------------------------- epilogue
+        const int quarter = warp & 3;
+        const int half = (warp - 2) >> 2;
+        uint32_t acc_ctr = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            const int m0 = (tile / num_n) * BM, n0 = (tile % num_n) * BN;
+            int32_t acc[128];
+#pragma unroll
+            for (int i = 0; i < 128; ++i) acc[i] = 0;
+            for (int seg = 0; seg < nseg; ++seg) {
+                const uint32_t buf = acc_ctr & 1u, par = (acc_ctr >> 1) & 1u;
+                bool w = mbar_wait(&acc_full[buf], par, abort_flag);
+                if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * BN + half * 128;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(taddr + c * 32, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) acc[c * 32 + j] += __float2int_rn(__uint_as_float(r[j]));
+                }
+                tc_fence_before();
+                mbar_arrive(&acc_empty[buf]);
+                ++acc_ctr;
+            }
+            if (!ok) break;
+            const int row = m0 + quarter * 32 + lane;
+            if (row < g.M) {
+                const float srow = g.sa[row];
+                const int nbase = n0 + half * 128;
+#pragma unroll
+                for (int grp = 0; grp < 16; ++grp) {
+                    const int n = nbase + grp * 8;
+                    if (n < g.N) {
+                        float y[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const float scol = (n + j < g.N) ? __ldg(g.sb + n + j) : 0.0f;
+                            y[j] = __fmul_rn(__fmul_rn(__int2float_rn(acc[grp * 8 + j]), srow), scol);
+                        }
+                        store_group8(g, row, n, y);
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS) : "memory");
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void* p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D fp16 tensor [rows][K], box of box_rows x 64 elements, 128-byte swizzle,
+// zero fill outside the tensor.
+static bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int box_rows) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(tc::BK), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+static int sm_count() {
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 1;
+}
+
+// Returns cudaErrorInvalidValue when a tensor map cannot be built (caller
+// validated shapes and alignment first).
+cudaError_t launch_gemm_codes(const uint16_t* a, const float* sa, const uint16_t* b, const float* sb, int64_t M,
+                              int64_t N, int64_t K, uint16_t* out_bf16, int64_t ld_bf16, int64_t n_bf16,
+                              float* out_f32, int64_t ld_f32, cudaStream_t st) {
+    CUtensorMap ma, mb;
+    if (!make_map(&ma, a, M, K, tc::BM) || !make_map(&mb, b, N, K, tc::BN)) return cudaErrorInvalidValue;
+    static std::once_flag attr_once;
+    std::call_once(attr_once, [] {
+        cudaFuncSetAttribute(gemm_codes_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_BYTES);
+    });
+    GemmArgs g;
+    g.sa = sa;
+    g.sb = sb;
+    g.M = static_cast<int>(M);
+    g.N = static_cast<int>(N);
+    g.K = static_cast<int>(K);
+    g.out_bf16 = out_bf16;
+    g.ld_bf16 = ld_bf16;
+    g.n_bf16 = static_cast<int>(n_bf16);
+    g.out_f32 = out_f32;
+    g.ld_f32 = ld_f32;
+    const bool bf_ok = out_bf16 == nullptr || ((reinterpret_cast<uintptr_t>(out_bf16) & 15) == 0 && ld_bf16 % 8 == 0);
+    const bool f_ok = out_f32 == nullptr ||
+                      ((reinterpret_cast<uintptr_t>(out_f32) & 15) == 0 && ld_f32 % 4 == 0 && n_bf16 % 4 == 0);
+    g.vec_ok = (bf_ok && f_ok) ? 1 : 0;
+    const int64_t tiles = ((M + tc::BM - 1) / tc::BM) * ((N + tc::BN - 1) / tc::BN);
+    const int grid = static_cast<int>(tiles < sm_count() ? tiles : sm_count());
+    gemm_codes_kernel<<<grid, tc::THREADS, tc::SMEM_BYTES, st>>>(ma, mb, g);
+    return cudaGetLastError();
+}
+
+int read_and_clear_gemm_error() {
+    int v = 0, z = 0;
+    cudaMemcpyFromSymbol(&v, g_gemm_error, sizeof(int));
+    if (v) cudaMemcpyToSymbol(g_gemm_error, &z, sizeof(int));
+    return v;
+}
+
+// ------------------------------------------------------------ fp32 projection
+// F32 layers only (no quantisation): a plain shared-memory tiled fp32 product
+// on the CUDA cores, 64x64 tiles, 4x4 outputs per thread.
+__global__ void __launch_bounds__(256) gemm_f32_kernel(const float* __restrict__ A, const float* __restrict__ B, int M,
+                                                       int N, int K, uint16_t* out_bf16, int64_t ld_bf16, int n_bf16,
+                                                       float* out_f32, int64_t ld_f32) {
+    __shared__ float As[16][64 + 4];
+    __shared__ float Bs[16][64 + 4];
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
+    float acc[4][4] = {};
+    for (int k0 = 0; k0 < K; k0 += 16) {
+        for (int i = threadIdx.x; i < 64 * 16; i += 256) {
+            const int r = i / 16, c = i % 16;
+            As[c][r] = (m0 + r < M && k0 + c < K) ? A[static_cast<int64_t>(m0 + r) * K + k0 + c] : 0.0f;
+            Bs[c][r] = (n0 + r < N && k0 + c < K) ? B[static_cast<int64_t>(n0 + r) * K + k0 + c] : 0.0f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {
+            float av[4], bv[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                av[i] = As[kk][ty * 4 + i];
+                bv[i] = Bs[kk][tx * 4 + i];
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int m = m0 + ty * 4 + i;
+        if (m >= M) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int n = n0 + tx * 4 + j;
+            if (n >= N) continue;
+            if (n < n_bf16)
+                out_bf16[m * ld_bf16 + n] = float_to_bf16_bits(acc[i][j]);
+            else
+                out_f32[m * ld_f32 + (n - n_bf16)] = acc[i][j];
+        }
+    }
+}
+
+cudaError_t launch_gemm_f32(const float* a, const float* b, int64_t M, int64_t N, int64_t K, uint16_t* out_bf16,
+                            int64_t ld_bf16, int64_t n_bf16, float* out_f32, int64_t ld_f32, cudaStream_t st) {
+    dim3 grid(static_cast<unsigned>((N + 63) / 64), static_cast<unsigned>((M + 63) / 64));
+    gemm_f32_kernel<<<grid, 256, 0, st>>>(a, b, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), out_bf16,
+                                          ld_bf16, static_cast<int>(n_bf16), out_f32, ld_f32);
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -1,0 +1,108 @@
+// Step 4 (+ the quantisation of step 5's input): gated RMSNorm per value head,
+//     o_hat = o / sqrt(mean(o^2) + eps) * norm_w * SiLU(z),
+// then, for Q4_K layers, the token row of o_hat (all Hv*dv values) quantised
+// to int8 codes with one fp32 scale (amax/127, IEEE fp32) for the output
+// projection.  The pages list the "gated-norm" kernel among a GDN layer's
+// kernels ("CRUX parity spike" #4220, technique table row 2); the int8 rows
+// feed the same integer product as step 1.
+//
+// One CTA per token; warp w normalises heads w, w+8, ...; the row stays in
+// registers between the per-head norms, the row amax and the quantisation, so
+// o and z are read once and the codes written once.
+#include "common.cuh"
+
+namespace gdn {
+
+constexpr int NORM_THREADS = 256;
+constexpr int NORM_MAX_HEADS_PER_WARP = 8;  // Hv <= 64
+
+template <int CPL, bool QUANT>
+__global__ void __launch_bounds__(NORM_THREADS)
+gated_norm_kernel(const float* __restrict__ o, const uint16_t* __restrict__ z, int64_t ld_z, int hv,
+                  const float* __restrict__ norm_w, float eps, uint16_t* __restrict__ codes,
+                  float* __restrict__ scale, float* __restrict__ out_f32) {
+    __shared__ float red[32];
+    constexpr int D = CPL * 32;
+    const int64_t t = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c_v = hv * D;
+    float wv[CPL];
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) wv[i] = norm_w[lane * CPL + i];
+    float v[NORM_MAX_HEADS_PER_WARP][CPL];
+    float amax = 0.0f;
+#pragma unroll
+    for (int hh = 0; hh < NORM_MAX_HEADS_PER_WARP; ++hh) {
+        const int h = warp + 8 * hh;
+        if (h < hv) {
+            const int c0 = h * D + lane * CPL;
+            float ov[CPL], zv[CPL];
+            if (CPL == 4) {
+                const float4 f = *reinterpret_cast<const float4*>(o + t * c_v + c0);
+                ov[0] = f.x; ov[1 % CPL] = f.y; ov[2 % CPL] = f.z; ov[3 % CPL] = f.w;
+                const uint2 u = *reinterpret_cast<const uint2*>(z + t * ld_z + c0);
+                zv[0] = __uint_as_float(u.x << 16); zv[1 % CPL] = __uint_as_float(u.x & 0xffff0000u);
+                zv[2 % CPL] = __uint_as_float(u.y << 16); zv[3 % CPL] = __uint_as_float(u.y & 0xffff0000u);
+            } else {
+                const float2 f = *reinterpret_cast<const float2*>(o + t * c_v + c0);
+                ov[0] = f.x; ov[1 % CPL] = f.y;
+                const uint32_t u = *reinterpret_cast<const uint32_t*>(z + t * ld_z + c0);
+                zv[0] = __uint_as_float(u << 16); zv[1 % CPL] = __uint_as_float(u & 0xffff0000u);
+            }
+            float ss = 0.0f;
+#pragma unroll
+            for (int i = 0; i < CPL; ++i) ss = fmaf(ov[i], ov[i], ss);
+            ss = warp_sum(ss);
+            const float r = rsqrtf(ss / static_cast<float>(D) + eps);
+#pragma unroll
+            for (int i = 0; i < CPL; ++i) {
+                v[hh][i] = ov[i] * r * wv[i] * silu_f(zv[i]);
+                amax = fmaxf(amax, fabsf(v[hh][i]));
+            }
+            if (!QUANT) {
+#pragma unroll
+                for (int i = 0; i < CPL; ++i) out_f32[t * c_v + c0 + i] = v[hh][i];
+            }
+        }
+    }
+    if (!QUANT) return;
+    amax = block_max(amax, red);
+    const float s = __fdiv_rn(amax, 127.0f);
+    if (threadIdx.x == 0) scale[t] = s;
+#pragma unroll
+    for (int hh = 0; hh < NORM_MAX_HEADS_PER_WARP; ++hh) {
+        const int h = warp + 8 * hh;
+        if (h < hv) {
+            const int c0 = h * D + lane * CPL;
+            uint32_t w[CPL / 2];
+#pragma unroll
+            for (int i = 0; i < CPL / 2; ++i)
+                w[i] = static_cast<uint32_t>(code_to_f16_bits(quant_code(v[hh][2 * i], s))) |
+                       (static_cast<uint32_t>(code_to_f16_bits(quant_code(v[hh][2 * i + 1], s))) << 16);
+            if (CPL == 4)
+                *reinterpret_cast<uint2*>(codes + t * c_v + c0) = make_uint2(w[0], w[1 % (CPL / 2)]);
+            else
+                *reinterpret_cast<uint32_t*>(codes + t * c_v + c0) = w[0];
+        }
+    }
+}
+
+cudaError_t launch_gated_norm(const gdn_layer& L, const float* o, const uint16_t* z, int64_t ld_z, int64_t n,
+                              uint16_t* codes, float* scale, float* out_f32, cudaStream_t st) {
+    const bool quant = L.wtype == GDN_W_Q4K;
+    const unsigned grid = static_cast<unsigned>(n);
+    if (L.dv == 128) {
+        if (quant)
+            gated_norm_kernel<4, true><<<grid, NORM_THREADS, 0, st>>>(o, z, ld_z, L.n_v_heads, L.norm_w, L.eps_rms, codes, scale, out_f32);
+        else
+            gated_norm_kernel<4, false><<<grid, NORM_THREADS, 0, st>>>(o, z, ld_z, L.n_v_heads, L.norm_w, L.eps_rms, codes, scale, out_f32);
+    } else {
+        if (quant)
+            gated_norm_kernel<2, true><<<grid, NORM_THREADS, 0, st>>>(o, z, ld_z, L.n_v_heads, L.norm_w, L.eps_rms, codes, scale, out_f32);
+        else
+            gated_norm_kernel<2, false><<<grid, NORM_THREADS, 0, st>>>(o, z, ld_z, L.n_v_heads, L.norm_w, L.eps_rms, codes, scale, out_f32);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

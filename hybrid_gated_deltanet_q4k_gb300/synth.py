@@ -81,11 +81,29 @@ SPECS = {
 }
 
 
+def _round_bf16_inplace(x32: np.ndarray) -> np.ndarray:
+    """Round finite float32 values to the nearest-even bf16, in place, in row
+    blocks (input recipe only); returns the bf16 bit patterns."""
+    u = x32.reshape(-1).view(np.uint32)
+    bits = np.empty(u.shape, np.uint16)
+    step = 1 << 22
+    tmp = np.empty(min(step, u.size), np.uint32)
+    for i in range(0, u.size, step):
+        seg = u[i:i + step]
+        t = tmp[:seg.size]
+        np.right_shift(seg, 16, out=t)
+        t &= 1
+        t += 0x7FFF
+        seg += t
+        seg &= 0xFFFF0000
+        np.right_shift(seg, 16, out=t)
+        bits[i:i + step] = t
+    return bits.reshape(x32.shape)
+
+
 def _to_bf16_bits(x32: np.ndarray) -> np.ndarray:
-    """Nearest-even bf16 bit pattern of float32 input values (input recipe only)."""
-    u = np.ascontiguousarray(x32, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
-    return u.astype(np.uint16)
+    """Nearest-even bf16 bit pattern of finite float32 input values (input recipe only)."""
+    return _round_bf16_inplace(np.array(x32, dtype=np.float32, copy=True))
 
 
 def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
@@ -96,10 +114,11 @@ def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
 def make_layer(spec: LayerSpec, seed: int | None = None) -> dict:
     """Random layer parameters in float32 (weights are quantised later, by each side)."""
     rng = np.random.default_rng(spec.seed if seed is None else seed)
-    w_in = rng.normal(0.0, 0.02, size=(spec.r_in, spec.hidden)).astype(np.float32)
-    w_out = rng.normal(0.0, 0.02, size=(spec.hidden, spec.c_v)).astype(np.float32)
-    conv_w = rng.normal(0.0, 0.02, size=(spec.c_conv, spec.conv_taps)).astype(np.float32)
-    norm_w = (1.0 + rng.normal(0.0, 0.02, size=(spec.dv,))).astype(np.float32)
+    f32 = np.float32
+    w_in = rng.standard_normal((spec.r_in, spec.hidden), dtype=f32) * f32(0.02)
+    w_out = rng.standard_normal((spec.hidden, spec.c_v), dtype=f32) * f32(0.02)
+    conv_w = rng.standard_normal((spec.c_conv, spec.conv_taps), dtype=f32) * f32(0.02)
+    norm_w = f32(1.0) + rng.standard_normal(spec.dv, dtype=f32) * f32(0.02)
     return {
         "w_in": w_in,
         "w_out": w_out,
@@ -116,7 +135,7 @@ def make_tokens(spec: LayerSpec, n_tokens: int, seed: int) -> dict:
     For Q4_K layers x is returned both as bf16 bit patterns (``x_bits``) and as
     the exact float32 value of those patterns (``x``)."""
     rng = np.random.default_rng(seed)
-    x = rng.normal(0.0, 1.0, size=(n_tokens, spec.hidden)).astype(np.float32)
+    x = rng.standard_normal((n_tokens, spec.hidden), dtype=np.float32)
     hv = spec.n_v_heads
     if spec.gates == "uniform_logdecay":
         log_a = rng.uniform(-0.5, 0.0, size=(n_tokens, hv))
@@ -126,9 +145,8 @@ def make_tokens(spec: LayerSpec, n_tokens: int, seed: int) -> dict:
     b = 1.0 / (1.0 + np.exp(-rng.normal(0.0, 1.0, size=(n_tokens, hv))))
     out = {"log_a": log_a.astype(np.float32), "b": b.astype(np.float32)}
     if spec.wtype == "q4k":
-        bits = _to_bf16_bits(x)
-        out["x_bits"] = bits
-        out["x"] = bf16_bits_to_f32(bits)
+        out["x_bits"] = _round_bf16_inplace(x)   # x now holds the bf16 values
+        out["x"] = x
     else:
         out["x"] = x
     return out

@@ -1,0 +1,265 @@
+/*
+ * gdn.h -- C ABI of the GB300 (sm_103a) batched-prefill library for one
+ * Gated DeltaNet (GDN) layer with Q4_K weights.
+ *
+ * The layer (one call of gdn_prefill) runs five steps, as the pages on the
+ * subject describe them:
+ *   1. the fused input projection: Q4_K weight superblocks decoded straight to
+ *      int8 rows with one fp32 scale per row, activations quantised to int8
+ *      rows, an integer tensor-core product and an fp32 rescale
+ *      (sparkinfer PR #464 "fused Q4K/Q6K->int8 dequant + token-parallel GDN
+ *      conv ...", Summary, "Fused Q4_K/Q6_K -> int8-row dequant");
+ *   2. the token-parallel causal 4-tap conv with SiLU and per-head L2 norm
+ *      (same page, "Token-parallel GDN conv");
+ *   3. the gated delta rule per value head, chunk-parallel (WY/UT form) with the
+ *      state carried across chunks ("Verbs Are Fast" epic #3598, parked
+ *      ticket "chunk-resident delta-rule scan vs the WY-chunked (tensor-core)
+ *      form"; CRUX parity spike #4220, technique table row 1);
+ *   4. the gated RMSNorm with a SiLU(z) gate (CRUX parity spike #4220,
+ *      technique table row 2: "gated-norm");
+ *   5. the output projection, quantised like step 1.
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers named "host" are host memory; every other pointer is device
+ *     memory on the current CUDA device, owned by the caller.  The library
+ *     never allocates, frees or keeps device memory across calls.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Device
+ *     work is enqueued asynchronously on it; the call returns when the work is
+ *     enqueued.  A fault inside a kernel shows up at gdn_sync_status().
+ *   - Return value: GDN_OK (0) or a negative GDN_E* code; the message of the
+ *     last failure on the calling thread is gdn_last_error().  A failing call
+ *     enqueues nothing unless the code is GDN_ECUDA (a launch that failed).
+ *   - There is no fallback path: an unsupported shape is an error, never a
+ *     slower route.
+ *   - bf16 and fp16 tensors are passed as their 16-bit patterns.
+ *   - "codes" tensors carry int8 quantisation codes q (|q| <= 127) stored in
+ *     fp16 bit patterns.  Every such q is exact in fp16, and sm_103a's
+ *     tensor cores multiply fp16 operands (they have no int8 MMA kind), so the
+ *     integer product is taken on fp16 operands with fp32 accumulation, exact
+ *     in segments of <= 1024 terms (1024 * 127^2 < 2^24), and the segments are
+ *     summed as int32.
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GDN_OK 0
+#define GDN_EINVAL (-1)   /* null pointer, size out of range, unsupported shape or alignment */
+#define GDN_ENOMEM (-2)   /* workspace smaller than one ubatch of tokens needs */
+#define GDN_ECUDA (-3)    /* a CUDA call or kernel launch failed */
+#define GDN_ETIMEOUT (-4) /* a bounded device-side wait ran out; the kernel returned early */
+
+#define GDN_W_Q4K 0 /* weights are GGUF Q4_K superblocks, activations bf16 */
+#define GDN_W_F32 1 /* weights and activations fp32, no quantisation anywhere */
+
+#define GDN_CHUNK 64 /* tokens per chunk of the chunked delta rule */
+
+/*
+ * One GDN layer.  Sizes: Hk = n_qk_heads, Hv = n_v_heads (a multiple of Hk;
+ * value head h reads key head h / (Hv/Hk)), dk = dv (64 or 128),
+ * C_qk = Hk*dk, C_v = Hv*dv, C_conv = 2*C_qk + C_v,
+ * R_in = 2*C_qk + 2*C_v + 2*Hv (rows of the fused input projection, in the
+ * order q | k | v | z | beta | alpha).  hidden and C_v are multiples of 256.
+ */
+typedef struct gdn_layer {
+    int32_t hidden;
+    int32_t n_qk_heads;
+    int32_t n_v_heads;
+    int32_t dk;
+    int32_t dv;
+    int32_t conv_taps; /* must be 4 */
+    int32_t wtype;     /* GDN_W_Q4K or GDN_W_F32 */
+    int32_t reserved0; /* must be 0 */
+    const void *w_in;  /* Q4_K: [R_in][hidden/256] blocks of 144 B (16-byte aligned); F32: fp32 [R_in][hidden] */
+    const void *w_out; /* Q4_K: [hidden][C_v/256] blocks; F32: fp32 [hidden][C_v] */
+    const float *conv_w;  /* [C_conv][4]; tap 3 multiplies the current token */
+    const float *A_log;   /* [Hv] */
+    const float *dt_bias; /* [Hv] */
+    const float *norm_w;  /* [dv], shared by all value heads */
+    /* Optional per-token gates for this call, both or neither: [N][Hv] each,
+     * log a_t and b_t drawn directly.  NULL: log a = -exp(A_log) *
+     * softplus(alpha + dt_bias) and b = sigmoid(beta) from the projection. */
+    const float *gate_log_a;
+    const float *gate_b;
+    float eps_l2;  /* L2 norm of q and k: x / sqrt(sum x^2 + eps_l2) */
+    float eps_rms; /* gated RMSNorm: o / sqrt(mean o^2 + eps_rms) */
+    float q_scale; /* multiplies q after its L2 norm (dk^-1/2 for the model family) */
+    float reserved1;
+} gdn_layer;
+
+/*
+ * q4k_pack -- encode fp32 weights into GGUF Q4_K blocks (host only, no GPU).
+ * w: host fp32 [rows][cols], cols a multiple of 256.  blocks: host output,
+ * rows * cols/256 * 144 bytes.  Per 32-weight sub-block the range
+ * [min(0, min w), max w] is split into 15 steps; d and dmin are the largest
+ * step and min over the superblock divided by 63, rounded to fp16; the 6-bit
+ * indices and 4-bit codes are nearest-even roundings in fp32, clamped.
+ * The pages give no encoder (they only decode); this is the plain min-max one.
+ * Returns GDN_EINVAL for null pointers, rows < 0 or cols % 256 != 0.
+ */
+int q4k_pack(const float *w, int64_t rows, int64_t cols, void *blocks);
+
+/*
+ * q4k_deq_i8 -- step 1a as its own call: decode Q4_K rows in registers and
+ * quantise each row straight to int8 with one fp32 scale, no bf16 scratch
+ * (sparkinfer PR #464, Summary, "Fused Q4_K/Q6_K -> int8-row dequant":
+ * "decodes superblocks in registers and writes int8 + per-row scale
+ * directly"; Correctness paragraph: from "the exact fp32 dequant").
+ * The decoded weight is fma(d*sc, q, -(dmin*m)) in fp32 (one rounding);
+ * row_scale = amax/127 and q = clamp(rne(w/row_scale), -127, 127), IEEE fp32.
+ * blocks: device [rows][cols/256][144 B], 16-byte aligned.  q: device int8
+ * [rows][cols], 8-byte aligned.  row_scale: device fp32 [rows].
+ * 256 <= cols <= 16384, cols % 256 == 0, rows >= 1.
+ */
+int q4k_deq_i8(const void *blocks, int64_t rows, int64_t cols, int8_t *q, float *row_scale, void *stream);
+
+/*
+ * gdn_workspace_size -- bytes of device workspace gdn_prefill needs to run
+ * `ubatch_tokens` tokens per internal pass (the decoded weights plus every
+ * per-token intermediate of one pass).  0 for an invalid layer.
+ */
+size_t gdn_workspace_size(const gdn_layer *layer, int64_t ubatch_tokens);
+
+/*
+ * gdn_prefill -- the whole layer over N prompt tokens, optionally extending a
+ * saved state ("Qwen3.5 on CPU prefills one token at a time" #5475: a prompt
+ * that extends the held tokens prefills only the suffix from the held state).
+ *   x          Q4_K layers: bf16 [N][hidden]; F32 layers: fp32 [N][hidden]
+ *   state_in   fp32 [Hv][dv][dk], the recurrent state S before token 0;
+ *              NULL = zero state
+ *   state_out  fp32 [Hv][dv][dk], S after token N-1; may equal state_in
+ *   conv_state fp32 [C_conv][3], in/out: the last 3 raw conv inputs per
+ *              channel, oldest first.  Read before token 0 (NULL state_in
+ *              with a non-NULL conv_state still reads it), written after.
+ *   y          Q4_K layers: bf16 [N][hidden]; F32 layers: fp32 [N][hidden]
+ *   workspace  device scratch of ws_bytes >= gdn_workspace_size(layer, 1);
+ *              the tokens run in passes of as many tokens as it holds, with
+ *              the state and conv tail carried between passes (exact: a pass
+ *              boundary is the same as an extend).  256-byte aligned.
+ * N >= 1.  Returns GDN_ENOMEM if the workspace holds less than one token.
+ */
+int gdn_prefill(const gdn_layer *layer, const void *x, int64_t n_tokens, const float *state_in,
+                float *state_out, float *conv_state, void *y, void *workspace, size_t ws_bytes,
+                void *stream);
+
+/*
+ * gdn_sync_status -- wait for `stream`, then report (and clear) the device
+ * error word the kernels set when a bounded wait runs out: GDN_OK,
+ * GDN_ETIMEOUT or GDN_ECUDA (a CUDA error from the stream).
+ */
+int gdn_sync_status(void *stream);
+
+/* gdn_last_error -- message of the last failure on this thread ("" if none). */
+const char *gdn_last_error(void);
+
+/*
+ * gdn_set_stage_events -- instrumentation for per-stage timing.  While set,
+ * every gdn_prefill call on this thread records events[i] (cudaEvent_t
+ * handles created by the caller) on its stream after stage i of its first
+ * pass: 0 entry, 1 weight decode, 2 activation quantisation, 3 input
+ * projection, 4 conv (+ conv state), 5 delta rule, 6 gated norm, 7 output
+ * projection.  n_events must be 0 (turns it off, events may be NULL) or
+ * GDN_N_STAGE_EVENTS.  The events are not owned by the library.
+ */
+#define GDN_N_STAGE_EVENTS 8
+int gdn_set_stage_events(void *const *events, int n_events);
+
+/* ---------------------------------------------------------------------------
+ * Stage entry points.  Each runs exactly the kernel gdn_prefill runs for its
+ * step, on caller-provided buffers, so that every step can be checked on its
+ * own.  Shapes and layouts are those gdn_prefill uses internally.
+ * ------------------------------------------------------------------------- */
+
+/*
+ * gdn_q4k_deq_codes -- step 1a as gdn_prefill runs it: like q4k_deq_i8 but
+ * the int8 codes are written as fp16 bit patterns (codes: [rows][cols],
+ * 16-byte aligned), the operand form of the tensor-core product.
+ */
+int gdn_q4k_deq_codes(const void *blocks, int64_t rows, int64_t cols, uint16_t *codes,
+                      float *row_scale, void *stream);
+
+/*
+ * gdn_quant_rows -- step 1b (and the quantisation of step 4's output): per row
+ * of a bf16 matrix x [rows][cols], scale = amax/127 and codes =
+ * clamp(rne(x/scale), -127, 127) in IEEE fp32, written as fp16 patterns.
+ * 8 <= cols <= 16384, cols % 8 == 0, x and codes 16-byte aligned.
+ */
+int gdn_quant_rows(const uint16_t *x, int64_t rows, int64_t cols, uint16_t *codes, float *scale,
+                   void *stream);
+
+/*
+ * gdn_gemm_codes -- steps 1c and 5: out[m][n] = ((float)sum_k A[m][k]*B[n][k]
+ * * sa[m]) * sb[n] with A, B int8 codes in fp16 patterns ([M][K], [Nn][K]
+ * row-major, 16-byte aligned), the integer sum exact, the rescale in fp32
+ * (nearest-even at each step).  Columns n < n_bf16 go to out_bf16[m*ld_bf16 +
+ * n] rounded to bf16; columns n >= n_bf16 go to out_f32[m*ld_f32 + n - n_bf16]
+ * (either pointer may be NULL if no column lands there).  K % 64 == 0,
+ * 64 <= K <= 65536; M, Nn >= 1.  tcgen05 tensor cores, TMEM accumulators,
+ * TMA-fed shared memory.
+ */
+int gdn_gemm_codes(const uint16_t *a, const float *sa, const uint16_t *b, const float *sb, int64_t M,
+                   int64_t Nn, int64_t K, uint16_t *out_bf16, int64_t ld_bf16, int64_t n_bf16,
+                   float *out_f32, int64_t ld_f32, void *stream);
+
+/*
+ * gdn_gemm_f32 -- steps 1c and 5 of an F32 layer: out[m][n] = sum_k
+ * A[m][k]*B[n][k] in fp32, split into bf16 and fp32 columns as gdn_gemm_codes.
+ */
+int gdn_gemm_f32(const float *a, const float *b, int64_t M, int64_t Nn, int64_t K, uint16_t *out_bf16,
+                 int64_t ld_bf16, int64_t n_bf16, float *out_f32, int64_t ld_f32, void *stream);
+
+/*
+ * gdn_conv -- step 2: causal 4-tap depthwise conv over the q|k|v channels of
+ * the projection (qkvz: bf16 [N][ld_qkvz], channel c at column c), SiLU, L2
+ * norm of each q and k head (q then scaled by q_scale), written as bf16
+ * qkv [N][C_conv].  conv_state [C_conv][3] holds the raw inputs before token 0
+ * (read only here).  When gates are not drawn (layer gate pointers NULL) it
+ * also writes log_a, b [N][Hv] from beta | alpha (ba: fp32 [N][ld_ba],
+ * beta at column h, alpha at column Hv + h); otherwise ba, log_a, b unused.
+ */
+int gdn_conv(const gdn_layer *layer, const uint16_t *qkvz, int64_t ld_qkvz, int64_t n_tokens,
+             const float *conv_state, const float *ba, int64_t ld_ba, uint16_t *qkv, float *log_a,
+             float *b, void *stream);
+
+/*
+ * gdn_conv_state_update -- after gdn_conv: conv_state <- the last 3 raw conv
+ * inputs (x_{N-3}, x_{N-2}, x_{N-1}), taken from qkvz or, for N < 3, from the
+ * old conv_state.
+ */
+int gdn_conv_state_update(const gdn_layer *layer, const uint16_t *qkvz, int64_t ld_qkvz,
+                          int64_t n_tokens, float *conv_state, void *stream);
+
+/*
+ * gdn_delta_rule -- step 3: the gated delta rule
+ *     S_t = a_t S_{t-1} (I - b_t k_t k_t^T) + b_t v_t k_t^T,   o_t = S_t q_t
+ * per value head, in chunks of GDN_CHUNK tokens (WY/UT form).  qkv: bf16
+ * [N][C_conv] as written by gdn_conv; log_a, b: fp32 [N][Hv]; state_in /
+ * state_out fp32 [Hv][dv][dk] (state_in NULL = zero; may alias); o: fp32
+ * [N][C_v].  scratch: device bytes >= gdn_delta_rule_scratch_size(layer, N).
+ */
+int gdn_delta_rule(const gdn_layer *layer, const uint16_t *qkv, const float *log_a, const float *b,
+                   int64_t n_tokens, const float *state_in, float *state_out, float *o,
+                   void *scratch, size_t scratch_bytes, void *stream);
+size_t gdn_delta_rule_scratch_size(const gdn_layer *layer, int64_t n_tokens);
+
+/*
+ * gdn_gated_norm -- step 4: per token and value head
+ * o_hat = o / sqrt(mean(o^2) + eps_rms) * norm_w * SiLU(z), z bf16 at
+ * z[t*ld_z + h*dv + i].  Q4_K layers: each token row of o_hat (all C_v
+ * values) is quantised like gdn_quant_rows into codes [N][C_v] + scale [N]
+ * (out_f32 unused).  F32 layers: o_hat is written to out_f32 [N][C_v].
+ */
+int gdn_gated_norm(const gdn_layer *layer, const float *o, const uint16_t *z, int64_t ld_z,
+                   int64_t n_tokens, uint16_t *codes, float *scale, float *out_f32, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

@@ -26,8 +26,9 @@ evaluation followed by one cast to fp32 is therefore that single rounding.
 
 The encoder is a plain reading (the pages give none): per sub-block the
 min-max range [min(0, min x), max x] is split into 15 steps; d and dmin are the
-largest sub-block scale and min divided by 63, rounded to fp16; sc_j, m_j and
-the codes are nearest-even roundings clamped to their ranges, all in fp32.
+largest sub-block scale and min divided by 63, rounded to fp16 (a zero of
+either sign stored as +0); sc_j, m_j and the codes are nearest-even roundings
+clamped to their ranges, all in fp32.
 """
 from __future__ import annotations
 
@@ -90,6 +91,8 @@ def pack_q4k(w: np.ndarray) -> np.ndarray:
     mins = (-mn).astype(f32)
     d16 = (scale.max(axis=-1) / f32(63)).astype(f32).astype(np.float16)
     dm16 = (mins.max(axis=-1) / f32(63)).astype(f32).astype(np.float16)
+    d16 = np.where(d16 == 0, np.float16(0), d16)     # a zero super-scale of either sign is stored as +0
+    dm16 = np.where(dm16 == 0, np.float16(0), dm16)
     d = d16.astype(f32)[..., None]
     dm = dm16.astype(f32)[..., None]
     with np.errstate(divide="ignore", invalid="ignore"):

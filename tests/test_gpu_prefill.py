@@ -1,0 +1,173 @@
+"""End-to-end parity of gdn_prefill with the oracle, plus the session-extend,
+ubatching and determinism properties.
+
+End to end the oracle is fed only x, the drawn gates and the packed weights.
+The projections are bit-exact, so every difference comes from the
+floating-point stages (bf16 activations between stages, fp32 recurrence,
+int8 re-quantisation of the gated-norm output): y and the final state must
+agree within relative L2 1e-2 (the tolerance for int8 projections), the conv
+state exactly (it holds raw projection outputs).
+"""
+import numpy as np
+import pytest
+import torch
+
+from hybrid_gated_deltanet_q4k_gb300 import synth
+from hybrid_gated_deltanet_q4k_gb300.api import DeviceLayer
+from oracle import layer as OL
+
+from gpu_util import DEV, bf16_dev, bf16_host_f32, f32_dev, oracle_params, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+
+def _x_dev(spec, tok):
+    return bf16_dev(tok["x_bits"]) if spec.wtype == "q4k" else f32_dev(tok["x"])
+
+
+def _y_host(spec, y):
+    return bf16_host_f32(y) if spec.wtype == "q4k" else y.cpu().numpy()
+
+
+def _new_y(spec, n):
+    return torch.empty(n, spec.hidden, dtype=torch.bfloat16 if spec.wtype == "q4k" else torch.float32, device=DEV)
+
+
+def _run(dl, spec, tok, n=None, ws_tokens=None, state=None, conv=None, start=0):
+    n = tok["x"].shape[0] - start if n is None else n
+    sl = slice(start, start + n)
+    x = _x_dev(spec, {k: v[sl] for k, v in tok.items() if k in ("x", "x_bits")})
+    la, b = f32_dev(tok["log_a"][sl]), f32_dev(tok["b"][sl])
+    if state is None:
+        state, conv = dl.new_state()
+    y = _new_y(spec, n)
+    ws = dl.new_workspace(ws_tokens or n)
+    dl.prefill(x, state, state, conv, y, ws, gate_log_a=la, gate_b=b)
+    torch.cuda.synchronize()
+    return y, state, conv
+
+
+def _check_vs_oracle(spec, dl, layer, tok, y, state, conv):
+    p = oracle_params(spec, layer)
+    ref = OL.layer_forward(p, tok["x"], gate_log_a=tok["log_a"], gate_b=tok["b"])
+    assert rel_l2(_y_host(spec, y), ref["y"]) <= 1e-2
+    assert rel_l2(state.cpu().numpy(), ref["state"]) <= 1e-2
+    if spec.wtype == "q4k":
+        assert np.array_equal(conv.cpu().numpy(), ref["conv_tail"].astype(np.float32))
+    else:
+        assert rel_l2(conv.cpu().numpy(), ref["conv_tail"]) <= 2 ** -8
+    return ref
+
+
+@pytest.mark.parametrize("name", ["tiny_f32", "h1024", "h2560"])
+def test_prefill_matches_oracle(name):
+    spec = synth.SPECS[name]
+    layer = synth.make_layer(spec)
+    tok = synth.make_tokens(spec, spec.n_tokens, seed=spec.seed + 10)
+    dl = DeviceLayer(spec, layer)
+    y, state, conv = _run(dl, spec, tok)
+    _check_vs_oracle(spec, dl, layer, tok, y, state, conv)
+
+
+SMALL = synth.LayerSpec("small", 512, 2, 4, 128, 128, 0, "q4k", 11, "softplus_normal")
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 63, 65, 127, 513])
+def test_prefill_ragged_lengths(n):
+    spec = SMALL
+    layer = synth.make_layer(spec)
+    tok = synth.make_tokens(spec, n, seed=n)
+    dl = DeviceLayer(spec, layer)
+    y, state, conv = _run(dl, spec, tok)
+    _check_vs_oracle(spec, dl, layer, tok, y, state, conv)
+
+
+def test_prefill_computed_gates():
+    """Gates from the beta/alpha projection rows (no drawn gates)."""
+    spec = SMALL
+    layer = synth.make_layer(spec)
+    layer["A_log"] = np.full(spec.n_v_heads, -1.0, np.float32)
+    layer["dt_bias"] = np.full(spec.n_v_heads, 0.5, np.float32)
+    tok = synth.make_tokens(spec, 100, seed=3)
+    dl = DeviceLayer(spec, layer)
+    state, conv = dl.new_state()
+    y = _new_y(spec, 100)
+    ws = dl.new_workspace(100)
+    dl.prefill(bf16_dev(tok["x_bits"]), None, state, conv, y, ws)
+    torch.cuda.synchronize()
+    ref = OL.layer_forward(oracle_params(spec, layer), tok["x"])
+    assert rel_l2(bf16_host_f32(y), ref["y"]) <= 1e-2
+    assert rel_l2(state.cpu().numpy(), ref["state"]) <= 1e-2
+
+
+def test_extend_equals_full_prefill_4b_layer():
+    """Session extend on the 4B-like layer: 8 sequences, a 2048-token prefix with its
+    saved fp32 state and conv tail, then U[1, 4096] more tokens; against a full
+    re-prefill of the concatenation.  With the prefix a whole number of chunks
+    the two runs do the same arithmetic, so they agree bit for bit."""
+    spec = synth.SPECS["extend"]
+    layer = synth.make_layer(spec)
+    dl = DeviceLayer(spec, layer)
+    cases = synth.make_extend_case(spec)
+    for i, tok in enumerate(cases):
+        n0, m = tok["prefix"], tok["extension"]
+        yf, sf, cf_ = _run(dl, spec, tok)
+        ya, sa, ca = _run(dl, spec, tok, n=n0)
+        yb, sb, cb = _run(dl, spec, tok, start=n0, state=sa, conv=ca)
+        assert torch.equal(torch.cat([ya, yb]).view(torch.int16), yf.view(torch.int16))
+        assert torch.equal(sb, sf) and torch.equal(cb, cf_)
+        if i == 0:   # and against the oracle's re-prefill
+            _check_vs_oracle(spec, dl, layer, tok, yf, sf, cf_)
+
+
+@pytest.mark.parametrize("n0", [1, 37, 100])
+def test_extend_at_odd_boundaries(n0):
+    spec = SMALL
+    layer = synth.make_layer(spec)
+    dl = DeviceLayer(spec, layer)
+    tok = synth.make_tokens(spec, 300, seed=n0)
+    yf, sf, cf_ = _run(dl, spec, tok)
+    ya, sa, ca = _run(dl, spec, tok, n=n0)
+    yb, sb, cb = _run(dl, spec, tok, start=n0, state=sa, conv=ca)
+    y2 = torch.cat([ya, yb])
+    assert rel_l2(bf16_host_f32(y2), bf16_host_f32(yf)) <= 2e-3
+    assert rel_l2(sb.cpu().numpy(), sf.cpu().numpy()) <= 2e-3
+    assert torch.equal(cb, cf_)
+
+
+def test_ubatched_workspace_is_bit_identical():
+    """A workspace holding fewer tokens than N runs in passes; with passes of whole
+    chunks the result is the same bits as one pass."""
+    spec = synth.SPECS["h1024"]
+    layer = synth.make_layer(spec)
+    dl = DeviceLayer(spec, layer)
+    tok = synth.make_tokens(spec, 700, seed=4)
+    y1, s1, c1 = _run(dl, spec, tok)
+    y2, s2, c2 = _run(dl, spec, tok, ws_tokens=128)
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    assert torch.equal(s1, s2) and torch.equal(c1, c2)
+    y3, s3, c3 = _run(dl, spec, tok, ws_tokens=1)    # one token per pass
+    assert rel_l2(bf16_host_f32(y3), bf16_host_f32(y1)) <= 2e-3
+    assert rel_l2(s3.cpu().numpy(), s1.cpu().numpy()) <= 2e-3
+
+
+def test_runs_are_deterministic():
+    spec = synth.SPECS["h2560"]
+    layer = synth.make_layer(spec)
+    dl = DeviceLayer(spec, layer)
+    tok = synth.make_tokens(spec, 1000, seed=5)
+    y1, s1, _ = _run(dl, spec, tok)
+    y2, s2, _ = _run(dl, spec, tok)
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16)) and torch.equal(s1, s2)
+
+
+def test_errors_are_statuses_not_fallbacks():
+    spec = SMALL
+    dl = DeviceLayer(spec, synth.make_layer(spec))
+    tok = synth.make_tokens(spec, 10, seed=1)
+    state, conv = dl.new_state()
+    y = _new_y(spec, 10)
+    small = torch.empty(dl.workspace_bytes(1) - 4096, dtype=torch.uint8, device=DEV)
+    assert dl.prefill(bf16_dev(tok["x_bits"]), None, state, conv, y, small, check=False) == -2
+    ws = dl.new_workspace(10)
+    assert dl.prefill(bf16_dev(tok["x_bits"])[:0], None, state, conv, y, ws, check=False) == -1
