@@ -24,9 +24,9 @@ cudaError_t launch_gemm_codes(const uint16_t*, const float*, const uint16_t*, co
 cudaError_t launch_gemm_f32(const float*, const float*, int64_t, int64_t, int64_t, uint16_t*, int64_t, int64_t, float*,
                             int64_t, cudaStream_t);
 cudaError_t launch_conv(const gdn_layer&, const uint16_t*, int64_t, int64_t, const float*, const float*, int64_t,
-                        uint16_t*, float*, float*, cudaStream_t);
+                        float*, float*, float*, cudaStream_t);
 cudaError_t launch_conv_state(const gdn_layer&, const uint16_t*, int64_t, int64_t, float*, cudaStream_t);
-cudaError_t launch_delta(const gdn_layer&, const uint16_t*, const float*, const float*, int64_t, const float*, float*,
+cudaError_t launch_delta(const gdn_layer&, const float*, const float*, const float*, int64_t, const float*, float*,
                          float*, void*, cudaStream_t);
 size_t delta_scratch_bytes(int hv, int d, int64_t n);
 cudaError_t launch_gated_norm(const gdn_layer&, const float*, const uint16_t*, int64_t, int64_t, uint16_t*, float*,
@@ -93,7 +93,8 @@ int check_layer(const gdn_layer* L, Sizes* s) {
     s->c_conv = 2 * s->c_qk + s->c_v;
     s->n_bf16 = 2 * s->c_qk + 2 * s->c_v;
     s->r_in = s->n_bf16 + 2 * s->hv;
-    if (s->c_v % 256 || s->c_v > 16384) return fail(GDN_EINVAL, "n_v_heads * dv must be a multiple of 256 and <= 16384 (got %lld)", (long long)s->c_v);
+    if (s->c_v > 16384 || (L->wtype == GDN_W_Q4K && s->c_v % 256))
+        return fail(GDN_EINVAL, "n_v_heads * dv must be <= 16384 (and a multiple of 256 for Q4_K) (got %lld)", (long long)s->c_v);
     if (!L->w_in || !L->w_out || !L->conv_w || !L->A_log || !L->dt_bias || !L->norm_w)
         return fail(GDN_EINVAL, "a layer weight pointer is NULL");
     if ((L->gate_log_a == nullptr) != (L->gate_b == nullptr)) return fail(GDN_EINVAL, "gate_log_a and gate_b: both or neither");
@@ -110,7 +111,7 @@ struct Workspace {
     uint16_t* xc; float* sx;          // x codes [B][H], scales [B]
     uint16_t* qkvz;                   // projection, bf16 [B][n_bf16]
     float* ba;                        // projection, fp32 [B][2 hv]
-    uint16_t* qkv;                    // conv output, bf16 [B][c_conv]
+    float* qkv;                       // conv output, fp32 [B][c_conv]
     float* log_a; float* b;           // gates [B][hv]
     float* o;                         // recurrence output [B][c_v]
     uint16_t* oc; float* so;          // gated-norm codes [B][c_v], scales [B]  (Q4_K)
@@ -145,7 +146,7 @@ Workspace carve(const gdn_layer* L, const Sizes& s, int64_t B, void* base) {
     }
     w.qkvz = static_cast<uint16_t*>(take(B * s.n_bf16 * 2));
     w.ba = static_cast<float*>(take(B * 2 * s.hv * 4));
-    w.qkv = static_cast<uint16_t*>(take(B * s.c_conv * 2));
+    w.qkv = static_cast<float*>(take(B * s.c_conv * 4));
     w.log_a = static_cast<float*>(take(B * s.hv * 4));
     w.b = static_cast<float*>(take(B * s.hv * 4));
     w.o = static_cast<float*>(take(B * s.c_v * 4));
@@ -232,12 +233,13 @@ int gdn_gemm_f32(const float* a, const float* b, int64_t M, int64_t Nn, int64_t 
 }
 
 int gdn_conv(const gdn_layer* layer, const uint16_t* qkvz, int64_t ld_qkvz, int64_t n_tokens, const float* conv_state,
-             const float* ba, int64_t ld_ba, uint16_t* qkv, float* log_a, float* b, void* stream) {
+             const float* ba, int64_t ld_ba, float* qkv, float* log_a, float* b, void* stream) {
     Sizes s;
     int r = check_layer(layer, &s);
     if (r) return r;
     if (n_tokens < 1 || n_tokens > 0x7fffffff) return fail(GDN_EINVAL, "gdn_conv: n_tokens >= 1 required");
     if (!qkvz || !conv_state || !qkv) return fail(GDN_EINVAL, "gdn_conv: NULL pointer");
+    if (!aligned(qkv, 16)) return fail(GDN_EINVAL, "gdn_conv: qkv must be 16-byte aligned");
     if (ld_qkvz < s.c_conv || ld_qkvz % 4 || !aligned(qkvz, 8)) return fail(GDN_EINVAL, "gdn_conv: qkvz layout");
     if (layer->gate_log_a == nullptr && (!ba || !log_a || !b || ld_ba < 2 * s.hv)) return fail(GDN_EINVAL, "gdn_conv: gate buffers");
     GDN_LAUNCH(launch_conv(*layer, qkvz, ld_qkvz, n_tokens, conv_state, ba, ld_ba, qkv, log_a, b, static_cast<cudaStream_t>(stream)),
@@ -262,7 +264,7 @@ size_t gdn_delta_rule_scratch_size(const gdn_layer* layer, int64_t n_tokens) {
     return delta_scratch_bytes(static_cast<int>(s.hv), static_cast<int>(s.d), n_tokens);
 }
 
-int gdn_delta_rule(const gdn_layer* layer, const uint16_t* qkv, const float* log_a, const float* b, int64_t n_tokens,
+int gdn_delta_rule(const gdn_layer* layer, const float* qkv, const float* log_a, const float* b, int64_t n_tokens,
                    const float* state_in, float* state_out, float* o, void* scratch, size_t scratch_bytes, void* stream) {
     Sizes s;
     int r = check_layer(layer, &s);

@@ -11,7 +11,10 @@
 // run of CONV_TOKENS consecutive tokens and keeps the last three raw inputs of
 // its channels in registers, so each raw input is read from HBM once (plus a
 // three-token halo per run).  The L2 norm of a q or k head is a warp
-// reduction.  Inputs and outputs are bf16; arithmetic is fp32.
+// reduction.  Inputs are the bf16 projection outputs; arithmetic and outputs
+// are fp32 (the recurrence reads fp32 q, k, v: rounding them to bf16 would
+// move o by ~0.3%, which the int8 re-quantisation of the gated-norm output
+// amplifies about threefold in y).
 //
 // Gates (when not drawn directly): log a = -exp(A_log) * softplus(alpha +
 // dt_bias), b = sigmoid(beta), from the fp32 beta | alpha columns of the
@@ -37,7 +40,7 @@ struct ConvArgs {
     float q_scale;
     const float* conv_w;   // [c_conv][4]
     const float* tail;     // [c_conv][3]
-    uint16_t* out;         // [n][c_conv]
+    float* out;            // [n][c_conv]
     // gates
     const float* ba;
     int64_t ld_ba;
@@ -103,15 +106,11 @@ __device__ __forceinline__ void conv_head_run(const ConvArgs& a, int head, int t
 #pragma unroll
             for (int i = 0; i < CPL; ++i) y[i] *= r;
         }
-        uint16_t* dst = a.out + static_cast<int64_t>(t) * a.c_conv + c0;
-        if (CPL == 4) {
-            const uint32_t lo = static_cast<uint32_t>(float_to_bf16_bits(y[0])) | (static_cast<uint32_t>(float_to_bf16_bits(y[1 % CPL])) << 16);
-            const uint32_t hi = static_cast<uint32_t>(float_to_bf16_bits(y[2 % CPL])) | (static_cast<uint32_t>(float_to_bf16_bits(y[3 % CPL])) << 16);
-            *reinterpret_cast<uint2*>(dst) = make_uint2(lo, hi);
-        } else {
-            *reinterpret_cast<uint32_t*>(dst) = static_cast<uint32_t>(float_to_bf16_bits(y[0])) |
-                                                (static_cast<uint32_t>(float_to_bf16_bits(y[1 % CPL])) << 16);
-        }
+        float* dst = a.out + static_cast<int64_t>(t) * a.c_conv + c0;
+        if (CPL == 4)
+            *reinterpret_cast<float4*>(dst) = make_float4(y[0], y[1 % CPL], y[2 % CPL], y[3 % CPL]);
+        else
+            *reinterpret_cast<float2*>(dst) = make_float2(y[0], y[1 % CPL]);
     }
 }
 
@@ -137,7 +136,7 @@ __global__ void __launch_bounds__(CONV_WARPS * 32) conv_kernel(ConvArgs a) {
 }
 
 cudaError_t launch_conv(const gdn_layer& L, const uint16_t* qkvz, int64_t ld_qkvz, int64_t n, const float* tail,
-                        const float* ba, int64_t ld_ba, uint16_t* out, float* log_a, float* b, cudaStream_t st) {
+                        const float* ba, int64_t ld_ba, float* out, float* log_a, float* b, cudaStream_t st) {
     ConvArgs a;
     a.qkvz = qkvz;
     a.ld_qkvz = ld_qkvz;

@@ -37,7 +37,7 @@ constexpr int DELTA_THREADS = 256;
 constexpr int STATE_NV = 16;   // rows of S per state-pass CTA
 
 struct DeltaArgs {
-    const uint16_t* qkv;  // [n][c_conv] bf16: q | k | v
+    const float* qkv;     // [n][c_conv] fp32: q | k | v
     const float* log_a;   // [n][hv]
     const float* b;       // [n][hv]
     int n, hv, ratio, c_qk, c_conv, c_v;
@@ -69,10 +69,10 @@ __global__ void __launch_bounds__(DELTA_THREADS) delta_prep_kernel(DeltaArgs a) 
         const int i = idx / D, c = idx % D, t = t0 + i;
         float kq = 0.f, qq = 0.f, vv = 0.f;
         if (t < a.n) {
-            const uint16_t* row = a.qkv + static_cast<int64_t>(t) * a.c_conv;
-            qq = bf16_bits_to_float(row[hk * D + c]);
-            kq = bf16_bits_to_float(row[a.c_qk + hk * D + c]);
-            vv = bf16_bits_to_float(row[2 * a.c_qk + h * D + c]);
+            const float* row = a.qkv + static_cast<int64_t>(t) * a.c_conv;
+            qq = row[hk * D + c];
+            kq = row[a.c_qk + hk * D + c];
+            vv = row[2 * a.c_qk + h * D + c];
         }
         Ks[i * P + c] = kq;
         Qs[i * P + c] = qq;
@@ -193,9 +193,9 @@ __global__ void __launch_bounds__(DELTA_THREADS) delta_state_kernel(DeltaArgs a)
             Ws[i * P + c] = wsrc[idx];
             float qq = 0.f, kq = 0.f;
             if (t < a.n) {
-                const uint16_t* row = a.qkv + static_cast<int64_t>(t) * a.c_conv;
-                qq = bf16_bits_to_float(row[hk * D + c]);
-                kq = bf16_bits_to_float(row[a.c_qk + hk * D + c]);
+                const float* row = a.qkv + static_cast<int64_t>(t) * a.c_conv;
+                qq = row[hk * D + c];
+                kq = row[a.c_qk + hk * D + c];
             }
             Qs[i * P + c] = qq;
             Ks[i * P + c] = kq;
@@ -283,7 +283,7 @@ static cudaError_t launch_delta_d(DeltaArgs& a, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_delta(const gdn_layer& L, const uint16_t* qkv, const float* log_a, const float* b, int64_t n,
+cudaError_t launch_delta(const gdn_layer& L, const float* qkv, const float* log_a, const float* b, int64_t n,
                          const float* state_in, float* state_out, float* o, void* scratch, cudaStream_t st) {
     DeltaArgs a;
     const int d = L.dk;

@@ -65,7 +65,8 @@ extern "C" {
  * value head h reads key head h / (Hv/Hk)), dk = dv (64 or 128),
  * C_qk = Hk*dk, C_v = Hv*dv, C_conv = 2*C_qk + C_v,
  * R_in = 2*C_qk + 2*C_v + 2*Hv (rows of the fused input projection, in the
- * order q | k | v | z | beta | alpha).  hidden and C_v are multiples of 256.
+ * order q | k | v | z | beta | alpha).  hidden is a multiple of 256, and so
+ * is C_v for Q4_K layers (it is the K extent of the output projection).
  */
 typedef struct gdn_layer {
     int32_t hidden;
@@ -217,14 +218,14 @@ int gdn_gemm_f32(const float *a, const float *b, int64_t M, int64_t Nn, int64_t 
 /*
  * gdn_conv -- step 2: causal 4-tap depthwise conv over the q|k|v channels of
  * the projection (qkvz: bf16 [N][ld_qkvz], channel c at column c), SiLU, L2
- * norm of each q and k head (q then scaled by q_scale), written as bf16
- * qkv [N][C_conv].  conv_state [C_conv][3] holds the raw inputs before token 0
+ * norm of each q and k head (q then scaled by q_scale), written as fp32
+ * qkv [N][C_conv] (16-byte aligned).  conv_state [C_conv][3] holds the raw inputs before token 0
  * (read only here).  When gates are not drawn (layer gate pointers NULL) it
  * also writes log_a, b [N][Hv] from beta | alpha (ba: fp32 [N][ld_ba],
  * beta at column h, alpha at column Hv + h); otherwise ba, log_a, b unused.
  */
 int gdn_conv(const gdn_layer *layer, const uint16_t *qkvz, int64_t ld_qkvz, int64_t n_tokens,
-             const float *conv_state, const float *ba, int64_t ld_ba, uint16_t *qkv, float *log_a,
+             const float *conv_state, const float *ba, int64_t ld_ba, float *qkv, float *log_a,
              float *b, void *stream);
 
 /*
@@ -238,12 +239,12 @@ int gdn_conv_state_update(const gdn_layer *layer, const uint16_t *qkvz, int64_t 
 /*
  * gdn_delta_rule -- step 3: the gated delta rule
  *     S_t = a_t S_{t-1} (I - b_t k_t k_t^T) + b_t v_t k_t^T,   o_t = S_t q_t
- * per value head, in chunks of GDN_CHUNK tokens (WY/UT form).  qkv: bf16
+ * per value head, in chunks of GDN_CHUNK tokens (WY/UT form).  qkv: fp32
  * [N][C_conv] as written by gdn_conv; log_a, b: fp32 [N][Hv]; state_in /
  * state_out fp32 [Hv][dv][dk] (state_in NULL = zero; may alias); o: fp32
  * [N][C_v].  scratch: device bytes >= gdn_delta_rule_scratch_size(layer, N).
  */
-int gdn_delta_rule(const gdn_layer *layer, const uint16_t *qkv, const float *log_a, const float *b,
+int gdn_delta_rule(const gdn_layer *layer, const float *qkv, const float *log_a, const float *b,
                    int64_t n_tokens, const float *state_in, float *state_out, float *o,
                    void *scratch, size_t scratch_bytes, void *stream);
 size_t gdn_delta_rule_scratch_size(const gdn_layer *layer, int64_t n_tokens);

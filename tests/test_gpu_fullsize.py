@@ -60,7 +60,7 @@ def test_h4096_n32768_prefill():
     L.gdn_gemm_codes(gl.ptr(xc), gl.ptr(sx), gl.ptr(wc_in), gl.ptr(ws_in), n, r_in, H, gl.ptr(qkvz), nbf, nbf,
                      gl.ptr(ba), 2 * hv, st)
     conv2 = torch.zeros(c_conv, 3, dtype=torch.float32, device=DEV)
-    qkv = torch.empty(n, c_conv, dtype=torch.bfloat16, device=DEV)
+    qkv = torch.empty(n, c_conv, dtype=torch.float32, device=DEV)
     L.gdn_conv(sp, gl.ptr(qkvz), nbf, n, gl.ptr(conv2), gl.ptr(ba), 2 * hv, gl.ptr(qkv), 0, 0, st)
     L.gdn_conv_state_update(sp, gl.ptr(qkvz), nbf, n, gl.ptr(conv2), st)
     nbytes = L.gdn_delta_rule_scratch_size(sp, n)
@@ -101,10 +101,10 @@ def test_h4096_n32768_prefill():
     for t in rows[rows >= 3][:16]:
         qq, kk, vv, _ = OL.conv_stage(p, raw_all[t - 3:t + 1], np.zeros((c_conv, 3)))
         ref = np.concatenate([qq[-1].ravel(), kk[-1].ravel(), vv[-1].ravel()])
-        got = bf16_host_f32(qkv[t])
-        assert np.all(np.abs(got - ref) <= 2 ** -8 * np.abs(ref) + 1e-5 * np.abs(ref).max())
+        got = qkv[t].cpu().numpy()
+        assert np.all(np.abs(got - ref) <= 3e-5 * np.abs(ref) + 1e-6 * np.abs(ref).max())
     # 3: the whole recurrence of two value heads from the GPU's own q, k, v
-    qkv_h = bf16_host_f32(qkv).astype(np.float64)
+    qkv_h = qkv.cpu().numpy().astype(np.float64)
     for h in (0, hv - 1):
         hk = h // (hv // spec.n_qk_heads)
         qh = qkv_h[:, hk * d:(hk + 1) * d][:, None, :]

@@ -4,9 +4,10 @@ Integer and byte work (Q4_K decode to int8 rows, activation quantisation, the
 integer product and its fp32 rescale) must be bit-exact.  Floating-point
 stages are fed the same inputs as the oracle and compared within tolerances
 derived from their arithmetic:
-  * conv + SiLU + L2 norm, written as bf16: each element within one bf16
-    rounding (relative 2^-8) of the fp64 value, plus 1e-5 of the tensor's
-    largest magnitude for fp32 evaluation;
+  * conv + SiLU + L2 norm (fp32 out): each element within 3e-5 relative of
+    the fp64 value (a few fp32 roundings in the 4-tap sum, expf, the
+    128-term norm and rsqrtf) plus 1e-6 of the tensor's largest magnitude
+    (cancellation in the tap sum);
   * gated delta rule (fp32 state, chunked): relative L2 <= 2e-3 for o and the
     final state;
   * gated RMSNorm: fp32 output within relative L2 1e-5; int8 codes within
@@ -174,7 +175,7 @@ def test_conv_stage(L, spec, n):
     tail = synth.bf16_bits_to_f32(synth._to_bf16_bits(rng.normal(0, 1.3, size=(spec.c_conv, 3)).astype(np.float32)))
     ba = rng.normal(0, 1, size=(n, 2 * spec.n_v_heads)).astype(np.float32)
     qkvz, taild, bad = bf16_dev(bits), f32_dev(tail), f32_dev(ba)
-    qkv = torch.empty(n, spec.c_conv, dtype=torch.bfloat16, device=DEV)
+    qkv = torch.empty(n, spec.c_conv, dtype=torch.float32, device=DEV)
     la = torch.empty(n, spec.n_v_heads, dtype=torch.float32, device=DEV)
     bb = torch.empty_like(la)
     L.gdn_conv(ctypes.byref(s), gl.ptr(qkvz), nb, n, gl.ptr(taild), gl.ptr(bad), 2 * spec.n_v_heads, gl.ptr(qkv),
@@ -185,8 +186,8 @@ def test_conv_stage(L, spec, n):
              eps_l2=1e-6, q_scale=spec.dk ** -0.5, wtype=spec.wtype, hidden=spec.hidden)
     q, k, v, new_tail = OL.conv_stage(p, raw[:, :spec.c_conv], tail)
     ref = np.concatenate([q.reshape(n, -1), k.reshape(n, -1), v.reshape(n, -1)], axis=1)
-    got = bf16_host_f32(qkv)
-    bound = 2 ** -8 * np.abs(ref) + 1e-5 * np.abs(ref).max()
+    got = qkv.cpu().numpy()
+    bound = 3e-5 * np.abs(ref) + 1e-6 * np.abs(ref).max()
     assert np.all(np.abs(got - ref) <= bound)
     assert np.array_equal(taild.cpu().numpy(), new_tail.astype(np.float32))
     rla, rb = OL.gates(ba[:, spec.n_v_heads:], ba[:, :spec.n_v_heads], layer["A_log"], layer["dt_bias"])
@@ -202,8 +203,7 @@ def _delta_inputs(spec, n, rng):
     k = OL.l2norm_heads(rng.normal(size=(n, hk, d)), 1e-6)
     v = OL.silu(rng.normal(0, 1, size=(n, hv, d)))
     qkv = np.concatenate([q.reshape(n, -1), k.reshape(n, -1), v.reshape(n, -1)], axis=1).astype(np.float32)
-    bits = synth._to_bf16_bits(qkv)
-    vals = synth.bf16_bits_to_f32(bits).astype(np.float64)
+    vals = qkv.astype(np.float64)
     c = spec.c_qk
     qe = OL.expand_kv_heads(vals[:, :c].reshape(n, hk, d), hv)
     ke = OL.expand_kv_heads(vals[:, c:2 * c].reshape(n, hk, d), hv)
@@ -213,7 +213,7 @@ def _delta_inputs(spec, n, rng):
     else:
         la = -np.logaddexp(0, rng.normal(size=(n, hv)))
     b = 1 / (1 + np.exp(-rng.normal(size=(n, hv))))
-    return bits, qe, ke, ve, la.astype(np.float32), b.astype(np.float32)
+    return qkv, qe, ke, ve, la.astype(np.float32), b.astype(np.float32)
 
 
 DELTA_SPECS = [synth.SPECS["tiny_f32"], synth.LayerSpec("d4", 512, 2, 4, 128, 128, 0, "q4k", 6, "softplus_normal"),
@@ -226,9 +226,9 @@ DELTA_SPECS = [synth.SPECS["tiny_f32"], synth.LayerSpec("d4", 512, 2, 4, 128, 12
 def test_delta_rule_stage(L, spec, n, with_state):
     _, dev, s = _layer(spec, L)
     rng = np.random.default_rng(1000 + n)
-    bits, qe, ke, ve, la, b = _delta_inputs(spec, n, rng)
+    qkv_h, qe, ke, ve, la, b = _delta_inputs(spec, n, rng)
     S0 = rng.normal(0, 0.3, size=(spec.n_v_heads, spec.dv, spec.dk)).astype(np.float32) if with_state else None
-    qkv, lad, bd = bf16_dev(bits), f32_dev(la), f32_dev(b)
+    qkv, lad, bd = f32_dev(qkv_h), f32_dev(la), f32_dev(b)
     sin = f32_dev(S0) if with_state else None
     sout = torch.empty(spec.n_v_heads, spec.dv, spec.dk, dtype=torch.float32, device=DEV)
     o = torch.empty(n, spec.c_v, dtype=torch.float32, device=DEV)
@@ -248,9 +248,9 @@ def test_delta_rule_state_aliasing(L):
     _, dev, s = _layer(spec, L)
     rng = np.random.default_rng(77)
     n = 150
-    bits, qe, ke, ve, la, b = _delta_inputs(spec, n, rng)
+    qkv_h, qe, ke, ve, la, b = _delta_inputs(spec, n, rng)
     S0 = rng.normal(0, 0.3, size=(spec.n_v_heads, spec.dv, spec.dk)).astype(np.float32)
-    qkv, lad, bd, st = bf16_dev(bits), f32_dev(la), f32_dev(b), f32_dev(S0)
+    qkv, lad, bd, st = f32_dev(qkv_h), f32_dev(la), f32_dev(b), f32_dev(S0)
     o = torch.empty(n, spec.c_v, dtype=torch.float32, device=DEV)
     nbytes = L.gdn_delta_rule_scratch_size(ctypes.byref(s), n)
     scratch = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
