@@ -13,6 +13,7 @@
 
 #include <cstdarg>
 #include <cstdio>
+#include <mutex>
 #include <string>
 
 namespace gdn {
@@ -386,3 +387,54 @@ int gdn_sync_status(void* stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// gdn_delta_rule_noalloc: the delta rule with its scratch in a static device
+// array, for callers that must not allocate device memory.  The array's host
+// name is only a stand-in; its device address is looked up once per device
+// (with that device current) and passed to the kernels.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[GDN_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 256;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_addr[kMaxDevices] = {};
+}  // namespace
+
+extern "C" int gdn_delta_rule_noalloc(const gdn_layer* layer, const float* qkv, const float* log_a, const float* b,
+                                      int64_t n_tokens, const float* state_in, float* state_out, float* o,
+                                      void* stream) {
+    Sizes s;
+    int r = check_layer(layer, &s);
+    if (r) return r;
+    if (n_tokens < 1 || n_tokens > 0x7fffffff) return fail(GDN_EINVAL, "gdn_delta_rule_noalloc: n_tokens >= 1 required");
+    if (!qkv || !log_a || !b || !state_out || !o) return fail(GDN_EINVAL, "gdn_delta_rule_noalloc: NULL pointer");
+    const size_t need = delta_scratch_bytes(static_cast<int>(s.hv), static_cast<int>(s.d), n_tokens);
+    if (need > GDN_NOALLOC_SCRATCH_BYTES) {
+        const size_t per_chunk = delta_scratch_bytes(static_cast<int>(s.hv), static_cast<int>(s.d), 1);
+        return fail(GDN_EINVAL,
+                    "gdn_delta_rule_noalloc: %lld tokens need %zu bytes of scratch, more than the static %u bytes "
+                    "(at most %lld tokens for this layer)",
+                    (long long)n_tokens, need, GDN_NOALLOC_SCRATCH_BYTES,
+                    (long long)(GDN_NOALLOC_SCRATCH_BYTES / per_chunk) * GDN_CHUNK);
+    }
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "gdn_delta_rule_noalloc: cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(GDN_EINVAL, "gdn_delta_rule_noalloc: device ordinal %d out of range", dev);
+    void* scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+        if (!g_noalloc_addr[dev]) {
+            void* p = nullptr;
+            e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+            if (e != cudaSuccess) return cuda_fail(e, "gdn_delta_rule_noalloc: cudaGetSymbolAddress");
+            g_noalloc_addr[dev] = p;
+        }
+        scratch = g_noalloc_addr[dev];
+    }
+    GDN_LAUNCH(launch_delta(*layer, qkv, log_a, b, n_tokens, state_in, state_out, o, scratch,
+                            static_cast<cudaStream_t>(stream)),
+               "gdn_delta_rule_noalloc");
+    return GDN_OK;
+}

@@ -19,6 +19,7 @@ GDN_OK, GDN_EINVAL, GDN_ENOMEM, GDN_ECUDA, GDN_ETIMEOUT = 0, -1, -2, -3, -4
 GDN_W_Q4K, GDN_W_F32 = 0, 1
 GDN_CHUNK = 64
 GDN_N_STAGE_EVENTS = 8
+GDN_NOALLOC_SCRATCH_BYTES = 32 << 20
 STAGE_NAMES = ["dequant", "act_quant", "in_proj", "conv", "delta_rule", "gated_norm", "out_proj"]
 
 
@@ -50,6 +51,7 @@ _SIGNATURES = {
     "gdn_conv_state_update": (c_int32, [_P, _P, c_int64, c_int64, _P, _P]),
     "gdn_delta_rule": (c_int32, [_P, _P, _P, _P, c_int64, _P, _P, _P, _P, c_size_t, _P]),
     "gdn_delta_rule_scratch_size": (c_size_t, [_P, c_int64]),
+    "gdn_delta_rule_noalloc": (c_int32, [_P, _P, _P, _P, c_int64, _P, _P, _P, _P]),
     "gdn_gated_norm": (c_int32, [_P, _P, _P, c_int64, c_int64, _P, _P, _P, _P]),
 }
 

@@ -250,6 +250,34 @@ int gdn_delta_rule(const gdn_layer *layer, const float *qkv, const float *log_a,
 size_t gdn_delta_rule_scratch_size(const gdn_layer *layer, int64_t n_tokens);
 
 /*
+ * gdn_delta_rule_noalloc -- the same computation as gdn_delta_rule, for
+ * callers that must not allocate device memory: for example a plug-in whose
+ * host engine owns every device allocation through its own pool and forbids
+ * its plug-ins to call cudaMalloc, or a loop that cannot afford the implicit
+ * device synchronisation of cudaMalloc/cudaFree.  The pages have no
+ * counterpart to this entry point; it exists only for such callers.
+ *   - No scratch argument: the scratch lives in one file-scope device array of
+ *     GDN_NOALLOC_SCRATCH_BYTES (32 MiB), which every GPU that loads this
+ *     library holds until the process exits.  The call itself allocates
+ *     nothing (no cudaMalloc, no cudaFree, no allocating library routine).
+ *   - A call whose gdn_delta_rule_scratch_size(layer, n_tokens) exceeds that
+ *     size returns GDN_EINVAL with a message (e.g. at most 768 tokens for 32
+ *     value heads of 128, 12 chunks of 64).
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call shares the one array and it keeps the last call's contents
+ *     (nothing in it needs to start at zero: each call writes every scratch
+ *     entry it reads).  Calls that overlap on the GPU (other streams, other
+ *     host threads) race on it: serialise them.
+ * Arguments, layouts and results are those of gdn_delta_rule.
+ */
+#define GDN_NOALLOC_SCRATCH_BYTES (32u << 20)
+int gdn_delta_rule_noalloc(const gdn_layer *layer, const float *qkv, const float *log_a, const float *b,
+                           int64_t n_tokens, const float *state_in, float *state_out, float *o,
+                           void *stream);
+
+/*
  * gdn_gated_norm -- step 4: per token and value head
  * o_hat = o / sqrt(mean(o^2) + eps_rms) * norm_w * SiLU(z), z bf16 at
  * z[t*ld_z + h*dv + i].  Q4_K layers: each token row of o_hat (all C_v
