@@ -55,6 +55,9 @@ def parse():
     ap.add_argument("--config", default="h4096")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--stage", choices=["in_proj", "delta_rule"], default=None,
+                    help="time one stage kernel alone through its stage entry point (profiling case)")
+    ap.add_argument("--tokens", type=int, default=None, help="tokens for --stage (default: the workload's N)")
     return ap.parse_args()
 
 
@@ -396,8 +399,68 @@ def run_ours(args, dist, spec):
         }), flush=True)
 
 
+def run_stage(args, spec):
+    """One stage kernel alone, on the workload's shapes with `--tokens` rows (a profiling case)."""
+    import ctypes
+
+    import torch
+
+    from hybrid_gated_deltanet_q4k_gb300 import lib as gl
+    from hybrid_gated_deltanet_q4k_gb300 import synth
+    from hybrid_gated_deltanet_q4k_gb300.api import DeviceLayer
+
+    L = gl.load(build=True)
+    n = args.tokens or spec.n_tokens
+    H, r_in, hv, d = spec.hidden, spec.r_in, spec.n_v_heads, spec.dk
+    nbf = 2 * spec.c_qk + 2 * spec.c_v
+    layer = synth.make_layer(spec)
+    dl = DeviceLayer(spec, layer)
+    st = torch.cuda.current_stream().cuda_stream
+    g = torch.Generator(device="cuda").manual_seed(0)
+    if args.stage == "in_proj":
+        wc = torch.empty(r_in, H, dtype=torch.float16, device="cuda")
+        ws = torch.empty(r_in, dtype=torch.float32, device="cuda")
+        L.gdn_q4k_deq_codes(gl.ptr(dl.dev["w_in"]), r_in, H, gl.ptr(wc), gl.ptr(ws), st)
+        xc = torch.randint(-127, 128, (n, H), device="cuda", generator=g).to(torch.float16)
+        sx = torch.rand(n, device="cuda", generator=g)
+        out = torch.empty(n, nbf, dtype=torch.bfloat16, device="cuda")
+        ba = torch.empty(n, 2 * hv, dtype=torch.float32, device="cuda")
+        fn = lambda: L.gdn_gemm_codes(gl.ptr(xc), gl.ptr(sx), gl.ptr(wc), gl.ptr(ws), n, r_in, H, gl.ptr(out), nbf,  # noqa: E731
+                                      nbf, gl.ptr(ba), 2 * hv, st)
+        work, unit = 2.0 * n * r_in * H / 1e12, "TFLOP"
+    else:
+        s = dl.struct()
+        qkv = torch.randn(n, spec.c_conv, device="cuda", generator=g) * 0.05
+        la = -0.5 * torch.rand(n, hv, device="cuda", generator=g)
+        b = torch.rand(n, hv, device="cuda", generator=g)
+        stt = torch.zeros(hv, d, d, device="cuda")
+        o = torch.empty(n, spec.c_v, device="cuda")
+        nbytes = L.gdn_delta_rule_scratch_size(ctypes.byref(s), n)
+        scratch = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        fn = lambda: L.gdn_delta_rule(ctypes.byref(s), gl.ptr(qkv), gl.ptr(la), gl.ptr(b), n, 0, gl.ptr(stt),  # noqa: E731
+                                      gl.ptr(o), gl.ptr(scratch), nbytes, st)
+        work, unit = n / 1e6, "Mtoken"
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    assert L.gdn_sync_status(st, check=False) == 0, L.last_error()
+    ms = e0.elapsed_time(e1) / args.steps
+    print(json.dumps({"stage": args.stage, "workload": spec.workload, "tokens": n, "ms_per_launch": ms,
+                      "rate": work / (ms / 1e3), "rate_unit": unit + "/s"}), flush=True)
+
+
 def main():
     args = parse()
+    if args.stage:
+        from hybrid_gated_deltanet_q4k_gb300 import synth
+        run_stage(args, synth.SPECS[args.config])
+        return
     dist = Dist()
     from hybrid_gated_deltanet_q4k_gb300 import synth
     spec = synth.SPECS[args.config]

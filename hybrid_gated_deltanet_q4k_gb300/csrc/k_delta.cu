@@ -1,5 +1,5 @@
 // Step 3: the gated delta rule, chunked (WY/UT form) with the state carried
-// across chunks.
+// across chunks, on tensor cores.
 //
 // Per value head h (key head hk = h / (Hv/Hk)) the rule of Gated DeltaNet is
 //     S_t = a_t S_{t-1} (I - b_t k_t k_t^T) + b_t v_t k_t^T,   o_t = S_t q_t,
@@ -10,31 +10,36 @@
 // registers ("CRUX parity spike" #4220, technique table row 1).
 //
 // Within a chunk of C tokens entering with state S, gamma_i = sum_{j<=i} log a_j:
-//     Lm_ij = b_i e^{gamma_i-gamma_j} k_i.k_j (j < i)
-//     W = (I + Lm)^{-1} diag(b e^gamma) K,   U = (I + Lm)^{-1} diag(b) V
-//     Delta = U - W S^T
-//     O = diag(e^gamma) Q S^T + (M o Q K^T) Delta,   M_ij = e^{gamma_i-gamma_j} (j <= i)
+//     L_ij = b_i e^{gamma_i-gamma_j} k_i.k_j (j < i),   T = (I + L)^{-1}
+//     R = diag(b) V - diag(b e^gamma) K S^T             (C x dv)
+//     Delta = T R                                        (= U - W S^T of the WY form)
+//     O = diag(e^gamma) Q S^T + A Delta,   A_ij = e^{gamma_i-gamma_j} q_i.k_j (j <= i)
 //     S <- e^{gamma_C} S + Delta^T diag(e^{gamma_C - gamma}) K
 // All exponents are <= 0.  Tokens past N are padded with log a = 0, b = 0,
 // which leaves S unchanged.
 //
 // Two kernels:
 //   delta_prep   one CTA per (chunk, head), all chunks in parallel: gamma,
-//                K K^T and Q K^T, the masked A_qk = M o Q K^T, and W, U by
-//                forward substitution of (I + Lm) X = rhs (each thread owns one
-//                column of W or U, so the substitution needs no barriers).
-//   delta_state  one CTA per (head, 16 rows of S): the chunks in order,
-//                Delta, O and the state update; rows of S evolve
-//                independently (row i only reads v[i]), so the rows split
-//                across CTAs with no communication.
-// fp32 throughout on the CUDA cores (no tensor cores in this form).
+//                K K^T and Q K^T on tensor cores, the masked A, and T by
+//                blocked inversion of the unit lower-triangular I + L (16x16
+//                diagonal blocks by substitution, off-diagonal blocks by
+//                block products).  Writes T, A, gamma: 32 KB per (chunk, head).
+//   delta_state  one CTA per (head, 32 rows of S): the chunks in order.  Rows
+//                of S evolve independently (row i only reads v[i]), so the
+//                rows split across CTAs with no communication.  The fp32 state
+//                stays in registers as the accumulator fragments of the
+//                update product.
+// Products use mma.sync m16n8k8 with tf32 operands rounded to nearest
+// (cvt.rna) and fp32 accumulation; everything else is fp32.  Rounding every
+// operand to tf32 keeps o and S within ~5e-4 (relative L2) of the exact
+// recurrence on the test workloads.
 #include "common.cuh"
 
 namespace gdn {
 
 constexpr int DC = GDN_CHUNK;  // 64
 constexpr int DELTA_THREADS = 256;
-constexpr int STATE_NV = 16;   // rows of S per state-pass CTA
+constexpr int NV = 32;         // rows of S per state CTA
 
 struct DeltaArgs {
     const float* qkv;     // [n][c_conv] fp32: q | k | v
@@ -42,234 +47,407 @@ struct DeltaArgs {
     const float* b;       // [n][hv]
     int n, hv, ratio, c_qk, c_conv, c_v;
     int nchunks;
-    float* w;      // [nchunks][hv][DC][D]
-    float* u;      // [nchunks][hv][DC][D]
-    float* aqk;    // [nchunks][hv][DC][DC]
+    float* T;      // [nchunks][hv][DC][DC]
+    float* A;      // [nchunks][hv][DC][DC]
     float* gam;    // [nchunks][hv][DC]
     const float* state_in;  // [hv][D][D] or null
     float* state_out;
     float* o;      // [n][c_v]
 };
 
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+__device__ __forceinline__ float tf32f(float x) { return __uint_as_float(to_tf32(x)); }
+
+// D += A(16x8, row) * B(8x8, col); fragments as in the PTX m16n8k8 .tf32 layout:
+// a0 (g, t) a1 (g+8, t) a2 (g, t+4) a3 (g+8, t+4); b0 (k=t, n=g) b1 (k=t+4, n=g);
+// c0 (g, 2t) c1 (g, 2t+1) c2 (g+8, 2t) c3 (g+8, 2t+1), g = lane/4, t = lane%4.
+__device__ __forceinline__ void mma_tf32(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t lds_u32(const float* p) { return __float_as_uint(*p); }
+
+// Load rows [t0, t0+DC) of a head slice of the fp32 qkv buffer into smem
+// (pitch P floats), rounded to tf32; rows past n are zero.
+template <int D, int P>
+__device__ __forceinline__ void load_rows_tf32(float* dst, const float* qkv, int64_t ld, int col0, int t0, int n) {
+    constexpr int V4 = D / 4;
+    for (int idx = threadIdx.x; idx < DC * V4; idx += DELTA_THREADS) {
+        const int r = idx / V4, c4 = idx % V4, t = t0 + r;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (t < n) v = *reinterpret_cast<const float4*>(qkv + static_cast<int64_t>(t) * ld + col0 + 4 * c4);
+        float* d = dst + r * P + 4 * c4;
+        d[0] = tf32f(v.x); d[1] = tf32f(v.y); d[2] = tf32f(v.z); d[3] = tf32f(v.w);
+    }
+}
+
+// ------------------------------------------------------------------ prep
+
 template <int D>
-__global__ void __launch_bounds__(DELTA_THREADS) delta_prep_kernel(DeltaArgs a) {
-    constexpr int P = D + 1;
+__global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(DeltaArgs a) {
+    constexpr int P = D + 4;        // row pitch of K, Q (conflict-free A/B fragment loads)
+    constexpr int PL = DC + 4;      // row pitch of L, T
     extern __shared__ float sm[];
     float* Ks = sm;                 // [DC][P]
-    float* Qs = Ks + DC * P;        // [DC][P]  (Q, later the W right-hand side / W)
-    float* Vs = Qs + DC * P;        // [DC][P]  (V, later U)
-    float* Lm = Vs + DC * P;        // [DC][DC + 1]
-    float* gl = Lm + DC * (DC + 1); // [DC] log a, then gamma
+    float* Qs = Ks + DC * P;        // [DC][P]
+    float* Ls = Qs + DC * P;        // [DC][PL]
+    float* Ts = Ls + DC * PL;       // [DC][PL]
+    float* Zs = Ts + DC * PL;       // [3][16][16]
+    float* gl = Zs + 3 * 256;       // [DC] log a, then gamma
     float* bb = gl + DC;            // [DC]
 
     const int chunk = blockIdx.x, h = blockIdx.y, hk = h / a.ratio;
     const int t0 = chunk * DC;
-    const int tid = threadIdx.x;
-    for (int idx = tid; idx < DC * D; idx += DELTA_THREADS) {
-        const int i = idx / D, c = idx % D, t = t0 + i;
-        float kq = 0.f, qq = 0.f, vv = 0.f;
-        if (t < a.n) {
-            const float* row = a.qkv + static_cast<int64_t>(t) * a.c_conv;
-            qq = row[hk * D + c];
-            kq = row[a.c_qk + hk * D + c];
-            vv = row[2 * a.c_qk + h * D + c];
-        }
-        Ks[i * P + c] = kq;
-        Qs[i * P + c] = qq;
-        Vs[i * P + c] = vv;
-    }
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, tg = lane & 3;
+
+    load_rows_tf32<D, P>(Ks, a.qkv, a.c_conv, a.c_qk + hk * D, t0, a.n);
+    load_rows_tf32<D, P>(Qs, a.qkv, a.c_conv, hk * D, t0, a.n);
     if (tid < DC) {
         const int t = t0 + tid;
         gl[tid] = t < a.n ? a.log_a[static_cast<int64_t>(t) * a.hv + h] : 0.f;
         bb[tid] = t < a.n ? a.b[static_cast<int64_t>(t) * a.hv + h] : 0.f;
     }
+    for (int i = tid; i < DC * PL; i += DELTA_THREADS) Ts[i] = 0.f;
     __syncthreads();
     if (tid < 32) {  // inclusive prefix sum of log a over the chunk (2 per lane)
-        float x0 = gl[2 * tid], x1 = gl[2 * tid + 1];
+        const float x0 = gl[2 * tid], x1 = gl[2 * tid + 1];
         float s = x0 + x1;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const float y = __shfl_up_sync(0xffffffffu, s, o);
             if (tid >= o) s += y;
         }
-        const float excl = s - (x0 + x1);
-        gl[2 * tid] = excl + x0;
+        gl[2 * tid] = s - x1;
         gl[2 * tid + 1] = s;
     }
     __syncthreads();
 
-    // K K^T and Q K^T, 4x4 outputs per thread at rows ti+16r, cols tj+16c.
-    const int ti = tid >> 4, tj = tid & 15;
-    float* aqk = a.aqk + (static_cast<int64_t>(chunk) * a.hv + h) * DC * DC;
-#pragma unroll 1
-    for (int pass = 0; pass < 2; ++pass) {
-        const float* A = pass == 0 ? Ks : Qs;
-        float acc[4][4] = {};
+    // K K^T and Q K^T on the lower-triangular 16x8 tiles: warp -> m-tile warp/2,
+    // n-tiles 4*(warp%2) .. +3 (skipping tiles wholly above the diagonal).
+    {
+        const int mt = warp >> 1, nt0 = 4 * (warp & 1);
+        float ck[4][4] = {}, cq[4][4] = {};
+        const float* ka = Ks + (16 * mt + g) * P + tg;
+        const float* qa = Qs + (16 * mt + g) * P + tg;
 #pragma unroll 4
-        for (int c = 0; c < D; ++c) {
-            float av[4], bv[4];
+        for (int ks = 0; ks < D / 8; ++ks) {
+            const int c = 8 * ks;
+            const uint32_t k0 = lds_u32(ka + c), k1 = lds_u32(ka + 8 * P + c), k2 = lds_u32(ka + c + 4),
+                           k3 = lds_u32(ka + 8 * P + c + 4);
+            const uint32_t q0 = lds_u32(qa + c), q1 = lds_u32(qa + 8 * P + c), q2 = lds_u32(qa + c + 4),
+                           q3 = lds_u32(qa + 8 * P + c + 4);
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                av[r] = A[(ti + 16 * r) * P + c];
-                bv[r] = Ks[(tj + 16 * r) * P + c];
+            for (int j = 0; j < 4; ++j) {
+                const int nt = nt0 + j;
+                if (8 * nt <= 16 * mt + 15) {
+                    const float* kb = Ks + (8 * nt + g) * P + c + tg;
+                    const uint32_t b0 = lds_u32(kb), b1 = lds_u32(kb + 4);
+                    mma_tf32(ck[j], k0, k1, k2, k3, b0, b1);
+                    mma_tf32(cq[j], q0, q1, q2, q3, b0, b1);
+                }
             }
+        }
+        float* aout = a.A + (static_cast<int64_t>(chunk) * a.hv + h) * DC * DC;
 #pragma unroll
-            for (int r = 0; r < 4; ++r)
+        for (int j = 0; j < 4; ++j) {
+            const int nt = nt0 + j;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) acc[r][q] = fmaf(av[r], bv[q], acc[r][q]);
+            for (int e = 0; e < 4; ++e) {
+                const int i = 16 * mt + g + (e >> 1) * 8, jj = 8 * nt + 2 * tg + (e & 1);
+                const bool live = 8 * nt <= 16 * mt + 15;
+                const float dec = (live && jj <= i) ? expf(gl[i] - gl[jj]) : 0.f;
+                Ls[i * PL + jj] = (jj < i) ? bb[i] * dec * ck[j][e] : 0.f;
+                aout[i * DC + jj] = dec * cq[j][e];
+            }
+        }
+    }
+    __syncthreads();
+
+    // T = (I + L)^{-1}: diagonal 16x16 blocks by substitution, one column per thread.
+    if (tid < 64) {
+        const int blk = tid >> 4, c = tid & 15, o = 16 * blk;
+        float col[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            float v;
+            if (r < c) {
+                v = 0.f;
+            } else if (r == c) {
+                v = 1.f;
+            } else {
+                float s = 0.f;
+#pragma unroll
+                for (int k = 0; k < r; ++k)
+                    if (k >= c) s = fmaf(Ls[(o + r) * PL + o + k], col[k], s);
+                v = -s;
+            }
+            col[r] = v;
         }
 #pragma unroll
-        for (int r = 0; r < 4; ++r)
+        for (int r = 0; r < 16; ++r) Ts[(o + r) * PL + o + c] = col[r];
+    }
+    __syncthreads();
+    // Off-diagonal blocks, block row by block row:
+    //   T_IJ = -T_II * sum_{K=J}^{I-1} L_IK T_KJ   (J < I)
+    for (int I = 1; I < 4; ++I) {
+        for (int e = tid; e < I * 256; e += DELTA_THREADS) {
+            const int J = e >> 8, r = (e >> 4) & 15, c = e & 15;
+            float z = 0.f;
+            for (int K = J; K < I; ++K)
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int i = ti + 16 * r, j = tj + 16 * q;
-                const float dec = j <= i ? expf(gl[i] - gl[j]) : 0.f;
-                if (pass == 0)
-                    Lm[i * (DC + 1) + j] = j < i ? bb[i] * dec * acc[r][q] : 0.f;
-                else
-                    aqk[i * DC + j] = dec * acc[r][q];
-            }
-    }
-    __syncthreads();
-    // right-hand sides: W <- diag(b e^gamma) K (into Qs), U <- diag(b) V (in place)
-    for (int idx = tid; idx < DC * D; idx += DELTA_THREADS) {
-        const int i = idx / D, c = idx % D;
-        Qs[i * P + c] = bb[i] * expf(gl[i]) * Ks[i * P + c];
-        Vs[i * P + c] = bb[i] * Vs[i * P + c];
-    }
-    __syncthreads();
-    // forward substitution (I + Lm) X = rhs, one column per thread
-    if (tid < 2 * D) {
-        float* X = tid < D ? Qs : Vs;
-        const int c = tid < D ? tid : tid - D;
-        for (int i = 1; i < DC; ++i) {
+                for (int m = 0; m < 16; ++m)
+                    z = fmaf(Ls[(16 * I + r) * PL + 16 * K + m], Ts[(16 * K + m) * PL + 16 * J + c], z);
+            Zs[J * 256 + r * 16 + c] = z;
+        }
+        __syncthreads();
+        for (int e = tid; e < I * 256; e += DELTA_THREADS) {
+            const int J = e >> 8, r = (e >> 4) & 15, c = e & 15;
             float s = 0.f;
-            for (int j = 0; j < i; ++j) s = fmaf(Lm[i * (DC + 1) + j], X[j * P + c], s);
-            X[i * P + c] -= s;
+#pragma unroll
+            for (int m = 0; m < 16; ++m) s = fmaf(Ts[(16 * I + r) * PL + 16 * I + m], Zs[J * 256 + m * 16 + c], s);
+            Ts[(16 * I + r) * PL + 16 * J + c] = -s;
         }
+        __syncthreads();
     }
-    __syncthreads();
-    float* wout = a.w + (static_cast<int64_t>(chunk) * a.hv + h) * DC * D;
-    float* uout = a.u + (static_cast<int64_t>(chunk) * a.hv + h) * DC * D;
-    for (int idx = tid; idx < DC * D; idx += DELTA_THREADS) {
-        const int i = idx / D, c = idx % D;
-        wout[idx] = Qs[i * P + c];
-        uout[idx] = Vs[i * P + c];
-    }
+    float* tout = a.T + (static_cast<int64_t>(chunk) * a.hv + h) * DC * DC;
+    for (int idx = tid; idx < DC * DC; idx += DELTA_THREADS) tout[idx] = Ts[(idx / DC) * PL + idx % DC];
     if (tid < DC) a.gam[(static_cast<int64_t>(chunk) * a.hv + h) * DC + tid] = gl[tid];
 }
 
+// ------------------------------------------------------------------ state pass
+
 template <int D>
-__global__ void __launch_bounds__(DELTA_THREADS) delta_state_kernel(DeltaArgs a) {
-    constexpr int NV = STATE_NV;
-    constexpr int P = D + 1;
+__global__ void __launch_bounds__(DELTA_THREADS, 1) delta_state_kernel(DeltaArgs a) {
+    constexpr int P = D + 4;        // K, Q, S row pitch
+    constexpr int PT = DC + 4;      // T, A row pitch
+    constexpr int PR = NV + 8;      // V/R/Delta row pitch (conflict-free for both fragment orientations)
+    constexpr int NT_D = D / 8;     // n-tiles across d
+    constexpr int DW = NT_D / 4;    // n-tiles of d per warp in the update (4 warps across d)
     extern __shared__ float sm[];
-    float* S = sm;                  // [NV][P]
-    float* Ws = S + NV * P;         // [DC][P]
-    float* Qs = Ws + DC * P;        // [DC][P]
-    float* Ks = Qs + DC * P;        // [DC][P]
-    float* Aq = Ks + DC * P;        // [DC][DC + 1]
-    float* Dl = Aq + DC * (DC + 1); // [DC][NV + 1]  U, then Delta
-    float* gm = Dl + DC * (NV + 1); // [DC]
-    float* kd = gm + DC;            // [DC] e^{gamma_C - gamma_t}
+    float* Ks = sm;                 // [DC][P]
+    float* Qs = Ks + DC * P;        // [DC][P]
+    float* Ss = Qs + DC * P;        // [NV][P]   S tile (tf32) as the B operand
+    float* Ts = Ss + NV * P;        // [DC][PT]
+    float* As = Ts + DC * PT;       // [DC][PT]
+    float* Rs = As + DC * PT;       // [DC][PR]  V, then R, then Delta
+    float* gm = Rs + DC * PR;       // [DC] gamma
+    float* ex = gm + DC;            // [DC] e^gamma
+    float* kd = ex + DC;            // [DC] e^{gamma_C - gamma}
+    float* bb = kd + DC;            // [DC] b
 
     const int h = blockIdx.x, i0 = blockIdx.y * NV, hk = h / a.ratio;
-    const int tid = threadIdx.x;
-    for (int idx = tid; idx < NV * D; idx += DELTA_THREADS) {
-        const int i = idx / D, c = idx % D;
-        S[i * P + c] = a.state_in ? a.state_in[(static_cast<int64_t>(h) * D + i0 + i) * D + c] : 0.f;
-    }
-    const int ci = tid & 15;          // column of S^T / row of S owned in the Delta and O phase
-    const int trow = tid >> 4;        // tokens trow + 16k
-    const int si = tid >> 4;          // row of S owned in the update phase
-    const int sc = tid & 15;          // columns sc + 16m
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, tg = lane & 3;
+
+    // State fragments: warp owns rows 16*(warp/4) .. +15 of the tile and d columns
+    // 8*DW*(warp%4) .. +8*DW-1, as m16n8 accumulators.
+    const int smt = warp >> 2, snt0 = DW * (warp & 3);
+    float S[DW][4];
+#pragma unroll
+    for (int j = 0; j < DW; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int i = 16 * smt + g + (e >> 1) * 8, d = 8 * (snt0 + j) + 2 * tg + (e & 1);
+            S[j][e] = a.state_in ? a.state_in[(static_cast<int64_t>(h) * D + i0 + i) * D + d] : 0.f;
+        }
+
+    // Output-tile ownership for the C x NV products: m-tile warp/2, n-tiles 2*(warp%2), +1.
+    const int omt = warp >> 1, ont0 = 2 * (warp & 1);
 
     for (int chunk = 0; chunk < a.nchunks; ++chunk) {
         const int t0 = chunk * DC;
         const int64_t ch = static_cast<int64_t>(chunk) * a.hv + h;
-        const float* wsrc = a.w + ch * DC * D;
-        for (int idx = tid; idx < DC * D; idx += DELTA_THREADS) {
-            const int i = idx / D, c = idx % D, t = t0 + i;
-            Ws[i * P + c] = wsrc[idx];
-            float qq = 0.f, kq = 0.f;
-            if (t < a.n) {
-                const float* row = a.qkv + static_cast<int64_t>(t) * a.c_conv;
-                qq = row[hk * D + c];
-                kq = row[a.c_qk + hk * D + c];
+        // ---- stage the chunk's operands and the current state
+#pragma unroll
+        for (int j = 0; j < DW; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int i = 16 * smt + g + (e >> 1) * 8, d = 8 * (snt0 + j) + 2 * tg + (e & 1);
+                Ss[i * P + d] = tf32f(S[j][e]);
             }
-            Qs[i * P + c] = qq;
-            Ks[i * P + c] = kq;
+        load_rows_tf32<D, P>(Ks, a.qkv, a.c_conv, a.c_qk + hk * D, t0, a.n);
+        load_rows_tf32<D, P>(Qs, a.qkv, a.c_conv, hk * D, t0, a.n);
+        {
+            const float* tsrc = a.T + ch * DC * DC;
+            const float* asrc = a.A + ch * DC * DC;
+            for (int idx = tid; idx < DC * DC / 4; idx += DELTA_THREADS) {
+                const int r = idx / (DC / 4), c4 = idx % (DC / 4);
+                const float4 tv = *reinterpret_cast<const float4*>(tsrc + 4 * idx);
+                const float4 av = *reinterpret_cast<const float4*>(asrc + 4 * idx);
+                float* td = Ts + r * PT + 4 * c4;
+                float* ad = As + r * PT + 4 * c4;
+                td[0] = tf32f(tv.x); td[1] = tf32f(tv.y); td[2] = tf32f(tv.z); td[3] = tf32f(tv.w);
+                ad[0] = tf32f(av.x); ad[1] = tf32f(av.y); ad[2] = tf32f(av.z); ad[3] = tf32f(av.w);
+            }
+            for (int idx = tid; idx < DC * NV / 4; idx += DELTA_THREADS) {
+                const int r = idx / (NV / 4), c4 = idx % (NV / 4), t = t0 + r;
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (t < a.n)
+                    v = *reinterpret_cast<const float4*>(a.qkv + static_cast<int64_t>(t) * a.c_conv + 2 * a.c_qk +
+                                                         h * D + i0 + 4 * c4);
+                float* vd = Rs + r * PR + 4 * c4;
+                vd[0] = v.x; vd[1] = v.y; vd[2] = v.z; vd[3] = v.w;
+            }
+            if (tid < DC) {
+                const int t = t0 + tid;
+                const float gv = a.gam[ch * DC + tid];
+                gm[tid] = gv;
+                ex[tid] = expf(gv);
+                bb[tid] = t < a.n ? a.b[static_cast<int64_t>(t) * a.hv + h] : 0.f;
+            }
         }
-        const float* asrc = a.aqk + ch * DC * DC;
-        for (int idx = tid; idx < DC * DC; idx += DELTA_THREADS) Aq[(idx / DC) * (DC + 1) + idx % DC] = asrc[idx];
-        const float* usrc = a.u + ch * DC * D;
-        for (int idx = tid; idx < DC * NV; idx += DELTA_THREADS) {
-            const int t = idx / NV, i = idx % NV;
-            Dl[t * (NV + 1) + i] = usrc[t * D + i0 + i];
-        }
-        if (tid < DC) gm[tid] = a.gam[ch * DC + tid];
         __syncthreads();
         if (tid < DC) kd[tid] = expf(gm[DC - 1] - gm[tid]);
 
-        // Delta = U - W S^T and O_inter = diag(e^gamma) Q S^T for column ci, tokens trow+16k
-        float dw[4] = {}, dq[4] = {};
+        // ---- step 1: X = K S^T (C x NV); R = diag(b) V - diag(b e^gamma) X
+        float x[2][4] = {};
+        {
+            const float* ka = Ks + (16 * omt + g) * P + tg;
 #pragma unroll 4
-        for (int c = 0; c < D; ++c) {
-            const float s = S[ci * P + c];
+            for (int ks = 0; ks < D / 8; ++ks) {
+                const int c = 8 * ks;
+                const uint32_t a0 = lds_u32(ka + c), a1 = lds_u32(ka + 8 * P + c), a2 = lds_u32(ka + c + 4),
+                               a3 = lds_u32(ka + 8 * P + c + 4);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                dw[k] = fmaf(Ws[(trow + 16 * k) * P + c], s, dw[k]);
-                dq[k] = fmaf(Qs[(trow + 16 * k) * P + c], s, dq[k]);
+                for (int j = 0; j < 2; ++j) {
+                    const float* sb = Ss + (8 * (ont0 + j) + g) * P + c + tg;
+                    mma_tf32(x[j], a0, a1, a2, a3, lds_u32(sb), lds_u32(sb + 4));
+                }
             }
         }
-        float oacc[4];
+        __syncthreads();   // V is read below and R overwrites it in place: every warp reads its own elements
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int t = trow + 16 * k;
-            Dl[t * (NV + 1) + ci] -= dw[k];
-            oacc[k] = expf(gm[t]) * dq[k];
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int t = 16 * omt + g + (e >> 1) * 8, i = 8 * (ont0 + j) + 2 * tg + (e & 1);
+                const float r = bb[t] * (Rs[t * PR + i] - ex[t] * x[j][e]);
+                Rs[t * PR + i] = tf32f(r);
+            }
+        __syncthreads();
+
+        // ---- step 2: Delta = T R (T unit lower triangular)
+        float dl[2][4] = {};
+        {
+            const float* ta = Ts + (16 * omt + g) * PT + tg;
+            for (int ks = 0; ks < 2 * omt + 2; ++ks) {
+                const int c = 8 * ks;
+                const uint32_t a0 = lds_u32(ta + c), a1 = lds_u32(ta + 8 * PT + c), a2 = lds_u32(ta + c + 4),
+                               a3 = lds_u32(ta + 8 * PT + c + 4);
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const float* rb = Rs + (c + tg) * PR + 8 * (ont0 + j) + g;
+                    mma_tf32(dl[j], a0, a1, a2, a3, lds_u32(rb), lds_u32(rb + 4 * PR));
+                }
+            }
         }
         __syncthreads();
-        // O += (M o Q K^T) Delta  (A_qk already masked and decayed)
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int t = trow + 16 * k;
-            float s = oacc[k];
-            for (int j = 0; j <= t; ++j) s = fmaf(Aq[t * (DC + 1) + j], Dl[j * (NV + 1) + ci], s);
-            if (t0 + t < a.n) a.o[static_cast<int64_t>(t0 + t) * a.c_v + h * D + i0 + ci] = s;
-        }
-        // S <- e^{gamma_C} S + Delta^T diag(e^{gamma_C - gamma}) K for row si, columns sc+16m
-        const float decay = expf(gm[DC - 1]);
-        float sn[D / 16];
+        for (int j = 0; j < 2; ++j)
 #pragma unroll
-        for (int m = 0; m < D / 16; ++m) sn[m] = decay * S[si * P + sc + 16 * m];
-        for (int t = 0; t < DC; ++t) {
-            const float coef = Dl[t * (NV + 1) + si] * kd[t];
-#pragma unroll
-            for (int m = 0; m < D / 16; ++m) sn[m] = fmaf(coef, Ks[t * P + sc + 16 * m], sn[m]);
-        }
+            for (int e = 0; e < 4; ++e) {
+                const int t = 16 * omt + g + (e >> 1) * 8, i = 8 * (ont0 + j) + 2 * tg + (e & 1);
+                Rs[t * PR + i] = tf32f(dl[j][e]);
+            }
         __syncthreads();
+
+        // ---- step 3: O = diag(e^gamma) Q S^T + A Delta
+        {
+            float oc[2][4] = {};
+            const float* qa = Qs + (16 * omt + g) * P + tg;
+#pragma unroll 4
+            for (int ks = 0; ks < D / 8; ++ks) {
+                const int c = 8 * ks;
+                const uint32_t a0 = lds_u32(qa + c), a1 = lds_u32(qa + 8 * P + c), a2 = lds_u32(qa + c + 4),
+                               a3 = lds_u32(qa + 8 * P + c + 4);
 #pragma unroll
-        for (int m = 0; m < D / 16; ++m) S[si * P + sc + 16 * m] = sn[m];
+                for (int j = 0; j < 2; ++j) {
+                    const float* sb = Ss + (8 * (ont0 + j) + g) * P + c + tg;
+                    mma_tf32(oc[j], a0, a1, a2, a3, lds_u32(sb), lds_u32(sb + 4));
+                }
+            }
+            const float e_lo = ex[16 * omt + g], e_hi = ex[16 * omt + g + 8];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                oc[j][0] *= e_lo; oc[j][1] *= e_lo; oc[j][2] *= e_hi; oc[j][3] *= e_hi;
+            }
+            const float* aa = As + (16 * omt + g) * PT + tg;
+            for (int ks = 0; ks < 2 * omt + 2; ++ks) {
+                const int c = 8 * ks;
+                const uint32_t a0 = lds_u32(aa + c), a1 = lds_u32(aa + 8 * PT + c), a2 = lds_u32(aa + c + 4),
+                               a3 = lds_u32(aa + 8 * PT + c + 4);
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const float* rb = Rs + (c + tg) * PR + 8 * (ont0 + j) + g;
+                    mma_tf32(oc[j], a0, a1, a2, a3, lds_u32(rb), lds_u32(rb + 4 * PR));
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int t = 16 * omt + g + 8 * hh, i = 8 * (ont0 + j) + 2 * tg;
+                    if (t0 + t < a.n)
+                        *reinterpret_cast<float2*>(a.o + static_cast<int64_t>(t0 + t) * a.c_v + h * D + i0 + i) =
+                            make_float2(oc[j][2 * hh], oc[j][2 * hh + 1]);
+                }
+        }
+
+        // ---- step 4: S <- e^{gamma_C} S + Delta~^T K, Delta~ = diag(e^{gamma_C - gamma}) Delta
+        {
+            const float dec = expf(gm[DC - 1]);
+#pragma unroll
+            for (int j = 0; j < DW; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) S[j][e] *= dec;
+#pragma unroll 2
+            for (int ks = 0; ks < DC / 8; ++ks) {
+                const int t = 8 * ks + tg;
+                const float* da = Rs + t * PR + 16 * smt + g;
+                const float k0 = kd[t], k1 = kd[t + 4];
+                const uint32_t a0 = to_tf32(da[0] * k0), a1 = to_tf32(da[8] * k0), a2 = to_tf32(da[4 * PR] * k1),
+                               a3 = to_tf32(da[4 * PR + 8] * k1);
+#pragma unroll
+                for (int j = 0; j < DW; ++j) {
+                    const float* kb = Ks + t * P + 8 * (snt0 + j) + g;
+                    mma_tf32(S[j], a0, a1, a2, a3, lds_u32(kb), lds_u32(kb + 4 * P));
+                }
+            }
+        }
         __syncthreads();
     }
-    for (int idx = tid; idx < NV * D; idx += DELTA_THREADS) {
-        const int i = idx / D, c = idx % D;
-        a.state_out[(static_cast<int64_t>(h) * D + i0 + i) * D + c] = S[i * P + c];
-    }
+#pragma unroll
+    for (int j = 0; j < DW; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int i = 16 * smt + g + (e >> 1) * 8, d = 8 * (snt0 + j) + 2 * tg + (e & 1);
+            a.state_out[(static_cast<int64_t>(h) * D + i0 + i) * D + d] = S[j][e];
+        }
 }
 
 size_t delta_scratch_bytes(int hv, int d, int64_t n) {
+    (void)d;
     const int64_t nch = (n + DC - 1) / DC;
-    const int64_t per = static_cast<int64_t>(hv) * DC * (2 * d + DC + 1);
+    const int64_t per = static_cast<int64_t>(hv) * DC * (2 * DC + 1);
     return static_cast<size_t>(nch * per) * sizeof(float);
 }
 
 template <int D>
 static cudaError_t launch_delta_d(DeltaArgs& a, cudaStream_t st) {
-    constexpr int P = D + 1;
-    const size_t prep_smem = (3 * DC * P + DC * (DC + 1) + 2 * DC) * sizeof(float);
-    const size_t state_smem = (STATE_NV * P + 3 * DC * P + DC * (DC + 1) + DC * (STATE_NV + 1) + 2 * DC) * sizeof(float);
+    constexpr int P = D + 4;
+    const size_t prep_smem = (2 * DC * P + 2 * DC * (DC + 4) + 3 * 256 + 2 * DC) * sizeof(float);
+    const size_t state_smem =
+        (2 * DC * P + NV * P + 2 * DC * (DC + 4) + DC * (NV + 8) + 4 * DC) * sizeof(float);
     static bool attr = false;
     if (!attr) {
         cudaFuncSetAttribute(delta_prep_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(prep_smem));
@@ -279,7 +457,7 @@ static cudaError_t launch_delta_d(DeltaArgs& a, cudaStream_t st) {
     delta_prep_kernel<D><<<dim3(a.nchunks, a.hv), DELTA_THREADS, prep_smem, st>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    delta_state_kernel<D><<<dim3(a.hv, D / STATE_NV), DELTA_THREADS, state_smem, st>>>(a);
+    delta_state_kernel<D><<<dim3(a.hv, D / NV), DELTA_THREADS, state_smem, st>>>(a);
     return cudaGetLastError();
 }
 
@@ -299,10 +477,9 @@ cudaError_t launch_delta(const gdn_layer& L, const float* qkv, const float* log_
     a.nchunks = static_cast<int>((n + DC - 1) / DC);
     const int64_t nch = a.nchunks;
     float* base = static_cast<float*>(scratch);
-    a.w = base;
-    a.u = a.w + nch * a.hv * DC * d;
-    a.aqk = a.u + nch * a.hv * DC * d;
-    a.gam = a.aqk + nch * a.hv * DC * DC;
+    a.T = base;
+    a.A = a.T + nch * a.hv * DC * DC;
+    a.gam = a.A + nch * a.hv * DC * DC;
     a.state_in = state_in;
     a.state_out = state_out;
     a.o = o;

@@ -261,8 +261,8 @@ size_t gdn_delta_rule_scratch_size(const gdn_layer *layer, int64_t n_tokens);
  *     library holds until the process exits.  The call itself allocates
  *     nothing (no cudaMalloc, no cudaFree, no allocating library routine).
  *   - A call whose gdn_delta_rule_scratch_size(layer, n_tokens) exceeds that
- *     size returns GDN_EINVAL with a message (e.g. at most 768 tokens for 32
- *     value heads of 128, 12 chunks of 64).
+ *     size returns GDN_EINVAL with a message (e.g. at most 1984 tokens, 31
+ *     chunks of 64, for 32 value heads).
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture.
