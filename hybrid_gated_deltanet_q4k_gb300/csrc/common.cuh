@@ -50,6 +50,14 @@ __device__ __forceinline__ int quant_code(float w, float s) {
 
 __device__ __forceinline__ float silu_f(float u) { return u / (1.0f + expf(-u)); }
 
+// fp32 -> tf32 (10 explicit mantissa bits), round to nearest, ties away; as fp32 bits.
+__device__ __forceinline__ uint32_t tf32_bits(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ float round_tf32(float x) { return __uint_as_float(tf32_bits(x)); }
+
 // Block-wide max of a non-negative value; all threads get the result.
 // `red` must hold 32 floats of shared memory.
 __device__ __forceinline__ float block_max(float v, float* red) {

@@ -11,10 +11,12 @@
 // run of CONV_TOKENS consecutive tokens and keeps the last three raw inputs of
 // its channels in registers, so each raw input is read from HBM once (plus a
 // three-token halo per run).  The L2 norm of a q or k head is a warp
-// reduction.  Inputs are the bf16 projection outputs; arithmetic and outputs
-// are fp32 (the recurrence reads fp32 q, k, v: rounding them to bf16 would
-// move o by ~0.3%, which the int8 re-quantisation of the gated-norm output
-// amplifies about threefold in y).
+// reduction.  Inputs are the bf16 projection outputs; arithmetic is fp32 and
+// the outputs are fp32 values rounded to tf32 (nearest), the precision the
+// recurrence's tensor-core products consume, so that kernel can copy them
+// into shared memory untouched.  (bf16 outputs would move o by ~0.3%, which
+// the int8 re-quantisation of the gated-norm output amplifies about threefold
+// in y; tf32 keeps o within ~5e-4.)
 //
 // Gates (when not drawn directly): log a = -exp(A_log) * softplus(alpha +
 // dt_bias), b = sigmoid(beta), from the fp32 beta | alpha columns of the
@@ -107,6 +109,8 @@ __device__ __forceinline__ void conv_head_run(const ConvArgs& a, int head, int t
             for (int i = 0; i < CPL; ++i) y[i] *= r;
         }
         float* dst = a.out + static_cast<int64_t>(t) * a.c_conv + c0;
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) y[i] = round_tf32(y[i]);
         if (CPL == 4)
             *reinterpret_cast<float4*>(dst) = make_float4(y[0], y[1 % CPL], y[2 % CPL], y[3 % CPL]);
         else

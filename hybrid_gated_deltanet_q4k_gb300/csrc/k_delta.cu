@@ -23,16 +23,22 @@
 //                K K^T and Q K^T on tensor cores, the masked A, and T by
 //                blocked inversion of the unit lower-triangular I + L (16x16
 //                diagonal blocks by substitution, off-diagonal blocks by
-//                block products).  Writes T, A, gamma: 32 KB per (chunk, head).
+//                block products).  Writes T and A (tf32-rounded) and a gate
+//                table (gamma, e^gamma, b, e^{gamma_C - gamma}) per token:
+//                33 KB per (chunk, head).
 //   delta_state  one CTA per (head, 32 rows of S): the chunks in order.  Rows
 //                of S evolve independently (row i only reads v[i]), so the
 //                rows split across CTAs with no communication.  The fp32 state
 //                stays in registers as the accumulator fragments of the
-//                update product.
-// Products use mma.sync m16n8k8 with tf32 operands rounded to nearest
-// (cvt.rna) and fp32 accumulation; everything else is fp32.  Rounding every
-// operand to tf32 keeps o and S within ~5e-4 (relative L2) of the exact
-// recurrence on the test workloads.
+//                update product.  Every operand of chunk c+1 is copied into
+//                shared memory with cp.async while chunk c computes: each
+//                copy is issued right after the operand's last use in chunk c
+//                (K, used first and last, is double-buffered).
+// Products use mma.sync m16n8k8 with tf32 operands rounded to nearest (the
+// conv writes q, k, v already rounded; T, A, S, R, Delta are rounded where
+// they are produced) and fp32 accumulation; everything else is fp32.
+// Rounding every operand to tf32 keeps o and S within ~5e-4 (relative L2) of
+// the exact recurrence on the test workloads.
 #include "common.cuh"
 
 namespace gdn {
@@ -47,21 +53,24 @@ struct DeltaArgs {
     const float* b;       // [n][hv]
     int n, hv, ratio, c_qk, c_conv, c_v;
     int nchunks;
-    float* T;      // [nchunks][hv][DC][DC]
-    float* A;      // [nchunks][hv][DC][DC]
-    float* gam;    // [nchunks][hv][DC]
+    float* T;      // [nchunks][hv][DC][DC]   tf32-rounded
+    float* A;      // [nchunks][hv][DC][DC]   tf32-rounded
+    float* G;      // [nchunks][hv][DC][4]    gamma, e^gamma, b, e^{gamma_C - gamma}
     const float* state_in;  // [hv][D][D] or null
     float* state_out;
     float* o;      // [n][c_v]
 };
 
-__device__ __forceinline__ uint32_t to_tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
-}
+__device__ __forceinline__ uint32_t to_tf32(float x) { return tf32_bits(x); }
+__device__ __forceinline__ float tf32f(float x) { return round_tf32(x); }
 
-__device__ __forceinline__ float tf32f(float x) { return __uint_as_float(to_tf32(x)); }
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool valid) {
+    const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(s), "l"(gmem), "r"(valid ? 16 : 0) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 // D += A(16x8, row) * B(8x8, col); fragments as in the PTX m16n8k8 .tf32 layout:
 // a0 (g, t) a1 (g+8, t) a2 (g, t+4) a3 (g+8, t+4); b0 (k=t, n=g) b1 (k=t+4, n=g);
@@ -167,7 +176,7 @@ __global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(DeltaArgs 
                 const bool live = 8 * nt <= 16 * mt + 15;
                 const float dec = (live && jj <= i) ? expf(gl[i] - gl[jj]) : 0.f;
                 Ls[i * PL + jj] = (jj < i) ? bb[i] * dec * ck[j][e] : 0.f;
-                aout[i * DC + jj] = dec * cq[j][e];
+                aout[i * DC + jj] = tf32f(dec * cq[j][e]);
             }
         }
     }
@@ -220,34 +229,89 @@ __global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(DeltaArgs 
         __syncthreads();
     }
     float* tout = a.T + (static_cast<int64_t>(chunk) * a.hv + h) * DC * DC;
-    for (int idx = tid; idx < DC * DC; idx += DELTA_THREADS) tout[idx] = Ts[(idx / DC) * PL + idx % DC];
-    if (tid < DC) a.gam[(static_cast<int64_t>(chunk) * a.hv + h) * DC + tid] = gl[tid];
+    for (int idx = tid; idx < DC * DC; idx += DELTA_THREADS) tout[idx] = tf32f(Ts[(idx / DC) * PL + idx % DC]);
+    if (tid < DC) {
+        const float gv = gl[tid];
+        *reinterpret_cast<float4*>(a.G + ((static_cast<int64_t>(chunk) * a.hv + h) * DC + tid) * 4) =
+            make_float4(gv, expf(gv), bb[tid], expf(gl[DC - 1] - gv));
+    }
 }
 
 // ------------------------------------------------------------------ state pass
 
 template <int D>
+struct StateSmem {
+    static constexpr int P = D + 4;    // K, Q, S row pitch (conflict-free fragment loads)
+    static constexpr int PT = DC + 4;  // T, A row pitch
+    static constexpr int PR = NV + 8;  // V, R/Delta row pitch (conflict-free in both orientations)
+    static constexpr int K0 = 0;                   // Ks[2][DC][P]
+    static constexpr int Q0 = K0 + 2 * DC * P;     // Qs[DC][P]
+    static constexpr int S0 = Q0 + DC * P;         // Ss[NV][P]
+    static constexpr int T0 = S0 + NV * P;         // Ts[DC][PT]
+    static constexpr int A0 = T0 + DC * PT;        // As[DC][PT]
+    static constexpr int V0 = A0 + DC * PT;        // Vs[DC][PR]
+    static constexpr int R0 = V0 + DC * PR;        // Rs[DC][PR]
+    static constexpr int G0 = R0 + DC * PR;        // Gs[2][DC][4]
+    static constexpr int FLOATS = G0 + 2 * DC * 4;
+};
+
+template <int D>
 __global__ void __launch_bounds__(DELTA_THREADS, 1) delta_state_kernel(DeltaArgs a) {
-    constexpr int P = D + 4;        // K, Q, S row pitch
-    constexpr int PT = DC + 4;      // T, A row pitch
-    constexpr int PR = NV + 8;      // V/R/Delta row pitch (conflict-free for both fragment orientations)
+    using L = StateSmem<D>;
+    constexpr int P = L::P, PT = L::PT, PR = L::PR;
     constexpr int NT_D = D / 8;     // n-tiles across d
     constexpr int DW = NT_D / 4;    // n-tiles of d per warp in the update (4 warps across d)
-    extern __shared__ float sm[];
-    float* Ks = sm;                 // [DC][P]
-    float* Qs = Ks + DC * P;        // [DC][P]
-    float* Ss = Qs + DC * P;        // [NV][P]   S tile (tf32) as the B operand
-    float* Ts = Ss + NV * P;        // [DC][PT]
-    float* As = Ts + DC * PT;       // [DC][PT]
-    float* Rs = As + DC * PT;       // [DC][PR]  V, then R, then Delta
-    float* gm = Rs + DC * PR;       // [DC] gamma
-    float* ex = gm + DC;            // [DC] e^gamma
-    float* kd = ex + DC;            // [DC] e^{gamma_C - gamma}
-    float* bb = kd + DC;            // [DC] b
+    extern __shared__ __align__(16) float sm[];
+    float* Ss = sm + L::S0;
+    float* Qs = sm + L::Q0;
+    float* Ts = sm + L::T0;
+    float* As = sm + L::A0;
+    float* Vs = sm + L::V0;
+    float* Rs = sm + L::R0;
 
     const int h = blockIdx.x, i0 = blockIdx.y * NV, hk = h / a.ratio;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, tg = lane & 3;
+
+    // ---- asynchronous copies of one chunk's operands (rows past n are zero-filled)
+    auto rows = [&](float* dst, int pitch, int col0, int width, int c) {   // token rows of qkv
+        const int t0 = c * DC, w4 = width / 4;
+        for (int idx = tid; idx < DC * w4; idx += DELTA_THREADS) {
+            const int r = idx / w4, c4 = idx % w4, t = t0 + r;
+            const bool ok = t < a.n;
+            const float* src = ok ? a.qkv + static_cast<int64_t>(t) * a.c_conv + col0 + 4 * c4 : a.qkv;
+            cp_async16(dst + r * pitch + 4 * c4, src, ok);
+        }
+    };
+    auto mat = [&](float* dst, const float* src) {                        // a [DC][DC] scratch matrix
+        for (int idx = tid; idx < DC * DC / 4; idx += DELTA_THREADS) {
+            const int r = idx / (DC / 4), c4 = idx % (DC / 4);
+            cp_async16(dst + r * PT + 4 * c4, src + 4 * idx, true);
+        }
+    };
+    auto chunk_base = [&](int c) { return static_cast<int64_t>(c) * a.hv + h; };
+    auto issue_K = [&](int c) {
+        if (c < a.nchunks) rows(sm + L::K0 + (c & 1) * DC * P, P, a.c_qk + hk * D, D, c);
+        cp_async_commit();
+    };
+    auto issue_VG = [&](int c) {
+        if (c < a.nchunks) {
+            rows(Vs, PR, 2 * a.c_qk + h * D + i0, NV, c);
+            if (tid < DC) cp_async16(sm + L::G0 + (c & 1) * DC * 4 + 4 * tid, a.G + (chunk_base(c) * DC + tid) * 4, true);
+        }
+        cp_async_commit();
+    };
+    auto issue_T = [&](int c) {
+        if (c < a.nchunks) mat(Ts, a.T + chunk_base(c) * DC * DC);
+        cp_async_commit();
+    };
+    auto issue_QA = [&](int c) {
+        if (c < a.nchunks) {
+            rows(Qs, P, hk * D, D, c);
+            mat(As, a.A + chunk_base(c) * DC * DC);
+        }
+        cp_async_commit();
+    };
 
     // State fragments: warp owns rows 16*(warp/4) .. +15 of the tile and d columns
     // 8*DW*(warp%4) .. +8*DW-1, as m16n8 accumulators.
@@ -260,14 +324,17 @@ __global__ void __launch_bounds__(DELTA_THREADS, 1) delta_state_kernel(DeltaArgs
             const int i = 16 * smt + g + (e >> 1) * 8, d = 8 * (snt0 + j) + 2 * tg + (e & 1);
             S[j][e] = a.state_in ? a.state_in[(static_cast<int64_t>(h) * D + i0 + i) * D + d] : 0.f;
         }
-
     // Output-tile ownership for the C x NV products: m-tile warp/2, n-tiles 2*(warp%2), +1.
     const int omt = warp >> 1, ont0 = 2 * (warp & 1);
 
+    issue_K(0);
+    issue_VG(0);
+    issue_T(0);
+    issue_QA(0);
     for (int chunk = 0; chunk < a.nchunks; ++chunk) {
         const int t0 = chunk * DC;
-        const int64_t ch = static_cast<int64_t>(chunk) * a.hv + h;
-        // ---- stage the chunk's operands and the current state
+        const float* Ks = sm + L::K0 + (chunk & 1) * DC * P;
+        const float* Gs = sm + L::G0 + (chunk & 1) * DC * 4;
 #pragma unroll
         for (int j = 0; j < DW; ++j)
 #pragma unroll
@@ -275,43 +342,13 @@ __global__ void __launch_bounds__(DELTA_THREADS, 1) delta_state_kernel(DeltaArgs
                 const int i = 16 * smt + g + (e >> 1) * 8, d = 8 * (snt0 + j) + 2 * tg + (e & 1);
                 Ss[i * P + d] = tf32f(S[j][e]);
             }
-        load_rows_tf32<D, P>(Ks, a.qkv, a.c_conv, a.c_qk + hk * D, t0, a.n);
-        load_rows_tf32<D, P>(Qs, a.qkv, a.c_conv, hk * D, t0, a.n);
-        {
-            const float* tsrc = a.T + ch * DC * DC;
-            const float* asrc = a.A + ch * DC * DC;
-            for (int idx = tid; idx < DC * DC / 4; idx += DELTA_THREADS) {
-                const int r = idx / (DC / 4), c4 = idx % (DC / 4);
-                const float4 tv = *reinterpret_cast<const float4*>(tsrc + 4 * idx);
-                const float4 av = *reinterpret_cast<const float4*>(asrc + 4 * idx);
-                float* td = Ts + r * PT + 4 * c4;
-                float* ad = As + r * PT + 4 * c4;
-                td[0] = tf32f(tv.x); td[1] = tf32f(tv.y); td[2] = tf32f(tv.z); td[3] = tf32f(tv.w);
-                ad[0] = tf32f(av.x); ad[1] = tf32f(av.y); ad[2] = tf32f(av.z); ad[3] = tf32f(av.w);
-            }
-            for (int idx = tid; idx < DC * NV / 4; idx += DELTA_THREADS) {
-                const int r = idx / (NV / 4), c4 = idx % (NV / 4), t = t0 + r;
-                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (t < a.n)
-                    v = *reinterpret_cast<const float4*>(a.qkv + static_cast<int64_t>(t) * a.c_conv + 2 * a.c_qk +
-                                                         h * D + i0 + 4 * c4);
-                float* vd = Rs + r * PR + 4 * c4;
-                vd[0] = v.x; vd[1] = v.y; vd[2] = v.z; vd[3] = v.w;
-            }
-            if (tid < DC) {
-                const int t = t0 + tid;
-                const float gv = a.gam[ch * DC + tid];
-                gm[tid] = gv;
-                ex[tid] = expf(gv);
-                bb[tid] = t < a.n ? a.b[static_cast<int64_t>(t) * a.hv + h] : 0.f;
-            }
-        }
+        issue_K(chunk + 1);
+        cp_async_wait<3>();        // K(c), V(c), G(c) have landed
         __syncthreads();
-        if (tid < DC) kd[tid] = expf(gm[DC - 1] - gm[tid]);
 
-        // ---- step 1: X = K S^T (C x NV); R = diag(b) V - diag(b e^gamma) X
-        float x[2][4] = {};
+        // ---- step 1: X = K S^T (C x NV); R = diag(b) (V - diag(e^gamma) X)
         {
+            float x[2][4] = {};
             const float* ka = Ks + (16 * omt + g) * P + tg;
 #pragma unroll 4
             for (int ks = 0; ks < D / 8; ++ks) {
@@ -324,21 +361,22 @@ __global__ void __launch_bounds__(DELTA_THREADS, 1) delta_state_kernel(DeltaArgs
                     mma_tf32(x[j], a0, a1, a2, a3, lds_u32(sb), lds_u32(sb + 4));
                 }
             }
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int t = 16 * omt + g + (e >> 1) * 8, i = 8 * (ont0 + j) + 2 * tg + (e & 1);
+                    Rs[t * PR + i] = tf32f(Gs[4 * t + 2] * (Vs[t * PR + i] - Gs[4 * t + 1] * x[j][e]));
+                }
         }
-        __syncthreads();   // V is read below and R overwrites it in place: every warp reads its own elements
-#pragma unroll
-        for (int j = 0; j < 2; ++j)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int t = 16 * omt + g + (e >> 1) * 8, i = 8 * (ont0 + j) + 2 * tg + (e & 1);
-                const float r = bb[t] * (Rs[t * PR + i] - ex[t] * x[j][e]);
-                Rs[t * PR + i] = tf32f(r);
-            }
+        __syncthreads();
+        issue_VG(chunk + 1);
+        cp_async_wait<3>();        // T(c) has landed
         __syncthreads();
 
         // ---- step 2: Delta = T R (T unit lower triangular)
-        float dl[2][4] = {};
         {
+            float dl[2][4] = {};
             const float* ta = Ts + (16 * omt + g) * PT + tg;
             for (int ks = 0; ks < 2 * omt + 2; ++ks) {
                 const int c = 8 * ks;
@@ -350,15 +388,18 @@ __global__ void __launch_bounds__(DELTA_THREADS, 1) delta_state_kernel(DeltaArgs
                     mma_tf32(dl[j], a0, a1, a2, a3, lds_u32(rb), lds_u32(rb + 4 * PR));
                 }
             }
+            __syncthreads();       // every warp has read R
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int t = 16 * omt + g + (e >> 1) * 8, i = 8 * (ont0 + j) + 2 * tg + (e & 1);
+                    Rs[t * PR + i] = tf32f(dl[j][e]);
+                }
         }
         __syncthreads();
-#pragma unroll
-        for (int j = 0; j < 2; ++j)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int t = 16 * omt + g + (e >> 1) * 8, i = 8 * (ont0 + j) + 2 * tg + (e & 1);
-                Rs[t * PR + i] = tf32f(dl[j][e]);
-            }
+        issue_T(chunk + 1);
+        cp_async_wait<3>();        // Q(c), A(c) have landed
         __syncthreads();
 
         // ---- step 3: O = diag(e^gamma) Q S^T + A Delta
@@ -376,7 +417,7 @@ __global__ void __launch_bounds__(DELTA_THREADS, 1) delta_state_kernel(DeltaArgs
                     mma_tf32(oc[j], a0, a1, a2, a3, lds_u32(sb), lds_u32(sb + 4));
                 }
             }
-            const float e_lo = ex[16 * omt + g], e_hi = ex[16 * omt + g + 8];
+            const float e_lo = Gs[4 * (16 * omt + g) + 1], e_hi = Gs[4 * (16 * omt + g + 8) + 1];
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 oc[j][0] *= e_lo; oc[j][1] *= e_lo; oc[j][2] *= e_hi; oc[j][3] *= e_hi;
@@ -402,10 +443,12 @@ __global__ void __launch_bounds__(DELTA_THREADS, 1) delta_state_kernel(DeltaArgs
                             make_float2(oc[j][2 * hh], oc[j][2 * hh + 1]);
                 }
         }
+        __syncthreads();           // every warp has read Q and A
+        issue_QA(chunk + 1);
 
         // ---- step 4: S <- e^{gamma_C} S + Delta~^T K, Delta~ = diag(e^{gamma_C - gamma}) Delta
         {
-            const float dec = expf(gm[DC - 1]);
+            const float dec = Gs[4 * (DC - 1) + 1];
 #pragma unroll
             for (int j = 0; j < DW; ++j)
 #pragma unroll
@@ -414,7 +457,7 @@ __global__ void __launch_bounds__(DELTA_THREADS, 1) delta_state_kernel(DeltaArgs
             for (int ks = 0; ks < DC / 8; ++ks) {
                 const int t = 8 * ks + tg;
                 const float* da = Rs + t * PR + 16 * smt + g;
-                const float k0 = kd[t], k1 = kd[t + 4];
+                const float k0 = Gs[4 * t + 3], k1 = Gs[4 * (t + 4) + 3];
                 const uint32_t a0 = to_tf32(da[0] * k0), a1 = to_tf32(da[8] * k0), a2 = to_tf32(da[4 * PR] * k1),
                                a3 = to_tf32(da[4 * PR + 8] * k1);
 #pragma unroll
@@ -426,6 +469,7 @@ __global__ void __launch_bounds__(DELTA_THREADS, 1) delta_state_kernel(DeltaArgs
         }
         __syncthreads();
     }
+    cp_async_wait<0>();
 #pragma unroll
     for (int j = 0; j < DW; ++j)
 #pragma unroll
@@ -438,7 +482,7 @@ __global__ void __launch_bounds__(DELTA_THREADS, 1) delta_state_kernel(DeltaArgs
 size_t delta_scratch_bytes(int hv, int d, int64_t n) {
     (void)d;
     const int64_t nch = (n + DC - 1) / DC;
-    const int64_t per = static_cast<int64_t>(hv) * DC * (2 * DC + 1);
+    const int64_t per = static_cast<int64_t>(hv) * DC * (2 * DC + 4);
     return static_cast<size_t>(nch * per) * sizeof(float);
 }
 
@@ -446,8 +490,7 @@ template <int D>
 static cudaError_t launch_delta_d(DeltaArgs& a, cudaStream_t st) {
     constexpr int P = D + 4;
     const size_t prep_smem = (2 * DC * P + 2 * DC * (DC + 4) + 3 * 256 + 2 * DC) * sizeof(float);
-    const size_t state_smem =
-        (2 * DC * P + NV * P + 2 * DC * (DC + 4) + DC * (NV + 8) + 4 * DC) * sizeof(float);
+    const size_t state_smem = StateSmem<D>::FLOATS * sizeof(float);
     static bool attr = false;
     if (!attr) {
         cudaFuncSetAttribute(delta_prep_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(prep_smem));
@@ -479,7 +522,7 @@ cudaError_t launch_delta(const gdn_layer& L, const float* qkv, const float* log_
     float* base = static_cast<float*>(scratch);
     a.T = base;
     a.A = a.T + nch * a.hv * DC * DC;
-    a.gam = a.A + nch * a.hv * DC * DC;
+    a.G = a.A + nch * a.hv * DC * DC;
     a.state_in = state_in;
     a.state_out = state_out;
     a.o = o;

@@ -219,7 +219,8 @@ int gdn_gemm_f32(const float *a, const float *b, int64_t M, int64_t Nn, int64_t 
  * gdn_conv -- step 2: causal 4-tap depthwise conv over the q|k|v channels of
  * the projection (qkvz: bf16 [N][ld_qkvz], channel c at column c), SiLU, L2
  * norm of each q and k head (q then scaled by q_scale), written as fp32
- * qkv [N][C_conv] (16-byte aligned).  conv_state [C_conv][3] holds the raw inputs before token 0
+ * values rounded to tf32 (nearest; the precision gdn_delta_rule's tensor
+ * cores consume) into qkv [N][C_conv] (16-byte aligned).  conv_state [C_conv][3] holds the raw inputs before token 0
  * (read only here).  When gates are not drawn (layer gate pointers NULL) it
  * also writes log_a, b [N][Hv] from beta | alpha (ba: fp32 [N][ld_ba],
  * beta at column h, alpha at column Hv + h); otherwise ba, log_a, b unused.
@@ -239,8 +240,10 @@ int gdn_conv_state_update(const gdn_layer *layer, const uint16_t *qkvz, int64_t 
 /*
  * gdn_delta_rule -- step 3: the gated delta rule
  *     S_t = a_t S_{t-1} (I - b_t k_t k_t^T) + b_t v_t k_t^T,   o_t = S_t q_t
- * per value head, in chunks of GDN_CHUNK tokens (WY/UT form).  qkv: fp32
- * [N][C_conv] as written by gdn_conv; log_a, b: fp32 [N][Hv]; state_in /
+ * per value head, in chunks of GDN_CHUNK tokens (WY/UT form), products on
+ * tensor cores with tf32 operands and fp32 accumulation; the state stays
+ * fp32.  qkv: fp32 [N][C_conv] as written by gdn_conv (q, k and v are read at
+ * tf32 precision: pass them rounded to tf32, as gdn_conv writes them); log_a, b: fp32 [N][Hv]; state_in /
  * state_out fp32 [Hv][dv][dk] (state_in NULL = zero; may alias); o: fp32
  * [N][C_v].  scratch: device bytes >= gdn_delta_rule_scratch_size(layer, N).
  */

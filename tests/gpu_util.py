@@ -40,6 +40,14 @@ def oracle_params(spec, layer: dict, eps=1e-6) -> dict:
     return p
 
 
+def tf32_round(x) -> np.ndarray:
+    """float32 values rounded to tf32 (10 explicit mantissa bits), nearest, ties away from zero."""
+    u = np.array(x, dtype=np.float32, copy=True).view(np.uint32)
+    u += np.uint32(0x1000)
+    u &= np.uint32(0xFFFFE000)
+    return u.view(np.float32)
+
+
 def rel_l2(a, b) -> float:
     a = np.asarray(a, np.float64)
     b = np.asarray(b, np.float64)

@@ -4,10 +4,11 @@ Integer and byte work (Q4_K decode to int8 rows, activation quantisation, the
 integer product and its fp32 rescale) must be bit-exact.  Floating-point
 stages are fed the same inputs as the oracle and compared within tolerances
 derived from their arithmetic:
-  * conv + SiLU + L2 norm (fp32 out): each element within 3e-5 relative of
-    the fp64 value (a few fp32 roundings in the 4-tap sum, expf, the
-    128-term norm and rsqrtf) plus 1e-6 of the tensor's largest magnitude
-    (cancellation in the tap sum);
+  * conv + SiLU + L2 norm (fp32 out, rounded to tf32 for the recurrence's
+    tensor cores): each element within 2^-11 + 3e-5 relative of the fp64
+    value (the tf32 rounding, plus a few fp32 roundings in the 4-tap sum,
+    expf, the 128-term norm and rsqrtf) plus 1e-6 of the tensor's largest
+    magnitude (cancellation in the tap sum);
   * gated delta rule (fp32 state, chunked): relative L2 <= 2e-3 for o and the
     final state;
   * gated RMSNorm: fp32 output within relative L2 1e-5; int8 codes within
@@ -24,7 +25,7 @@ from hybrid_gated_deltanet_q4k_gb300 import synth
 from oracle import layer as OL
 from oracle import q4k, quant
 
-from gpu_util import DEV, bf16_dev, bf16_host_f32, f16_codes, f32_dev, rel_l2, stream, sync
+from gpu_util import DEV, bf16_dev, bf16_host_f32, f16_codes, f32_dev, rel_l2, stream, sync, tf32_round
 
 pytestmark = pytest.mark.gpu
 
@@ -187,7 +188,7 @@ def test_conv_stage(L, spec, n):
     q, k, v, new_tail = OL.conv_stage(p, raw[:, :spec.c_conv], tail)
     ref = np.concatenate([q.reshape(n, -1), k.reshape(n, -1), v.reshape(n, -1)], axis=1)
     got = qkv.cpu().numpy()
-    bound = 3e-5 * np.abs(ref) + 1e-6 * np.abs(ref).max()
+    bound = (2 ** -11 + 3e-5) * np.abs(ref) + 1e-6 * np.abs(ref).max()
     assert np.all(np.abs(got - ref) <= bound)
     assert np.array_equal(taild.cpu().numpy(), new_tail.astype(np.float32))
     rla, rb = OL.gates(ba[:, spec.n_v_heads:], ba[:, :spec.n_v_heads], layer["A_log"], layer["dt_bias"])
@@ -202,7 +203,8 @@ def _delta_inputs(spec, n, rng):
     q = OL.l2norm_heads(rng.normal(size=(n, hk, d)), 1e-6) * d ** -0.5
     k = OL.l2norm_heads(rng.normal(size=(n, hk, d)), 1e-6)
     v = OL.silu(rng.normal(0, 1, size=(n, hv, d)))
-    qkv = np.concatenate([q.reshape(n, -1), k.reshape(n, -1), v.reshape(n, -1)], axis=1).astype(np.float32)
+    # the recurrence consumes q, k, v at tf32 precision, as gdn_conv writes them
+    qkv = tf32_round(np.concatenate([q.reshape(n, -1), k.reshape(n, -1), v.reshape(n, -1)], axis=1))
     vals = qkv.astype(np.float64)
     c = spec.c_qk
     qe = OL.expand_kv_heads(vals[:, :c].reshape(n, hk, d), hv)

@@ -14,7 +14,7 @@ from hybrid_gated_deltanet_q4k_gb300 import lib as gl
 from hybrid_gated_deltanet_q4k_gb300 import synth
 from oracle import layer as OL
 
-from gpu_util import DEV, f32_dev, rel_l2, stream, sync
+from gpu_util import DEV, f32_dev, rel_l2, stream, sync, tf32_round
 
 pytestmark = pytest.mark.gpu
 
@@ -25,7 +25,7 @@ def _inputs(spec, n, seed):
     q = OL.l2norm_heads(rng.normal(size=(n, hk, d)), 1e-6) * d ** -0.5
     k = OL.l2norm_heads(rng.normal(size=(n, hk, d)), 1e-6)
     v = OL.silu(rng.normal(size=(n, hv, d)))
-    qkv = np.concatenate([q.reshape(n, -1), k.reshape(n, -1), v.reshape(n, -1)], axis=1).astype(np.float32)
+    qkv = tf32_round(np.concatenate([q.reshape(n, -1), k.reshape(n, -1), v.reshape(n, -1)], axis=1))
     la = rng.uniform(-0.5, 0, size=(n, hv)).astype(np.float32)
     b = (1 / (1 + np.exp(-rng.normal(size=(n, hv))))).astype(np.float32)
     s0 = rng.normal(0, 0.3, size=(hv, d, d)).astype(np.float32)
