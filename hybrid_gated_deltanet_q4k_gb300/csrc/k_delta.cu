@@ -33,7 +33,7 @@
 //                update product.  Every operand of chunk c+1 is copied into
 //                shared memory with cp.async while chunk c computes: each
 //                copy is issued right after the operand's last use in chunk c
-//                (K, used first and last, is double-buffered).
+//                (K and Q, used in the first phase, are double-buffered).
 // Products use mma.sync m16n8k8 with tf32 operands rounded to nearest (the
 // conv writes q, k, v already rounded; T, A, S, R, Delta are rounded where
 // they are produced) and fp32 accumulation; everything else is fp32.
@@ -245,8 +245,8 @@ struct StateSmem {
     static constexpr int PT = DC + 4;  // T, A row pitch
     static constexpr int PR = NV + 8;  // V, R/Delta row pitch (conflict-free in both orientations)
     static constexpr int K0 = 0;                   // Ks[2][DC][P]
-    static constexpr int Q0 = K0 + 2 * DC * P;     // Qs[DC][P]
-    static constexpr int S0 = Q0 + DC * P;         // Ss[NV][P]
+    static constexpr int Q0 = K0 + 2 * DC * P;     // Qs[2][DC][P]
+    static constexpr int S0 = Q0 + 2 * DC * P;     // Ss[NV][P]
     static constexpr int T0 = S0 + NV * P;         // Ts[DC][PT]
     static constexpr int A0 = T0 + DC * PT;        // As[DC][PT]
     static constexpr int V0 = A0 + DC * PT;        // Vs[DC][PR]
@@ -255,6 +255,13 @@ struct StateSmem {
     static constexpr int FLOATS = G0 + 2 * DC * 4;
 };
 
+// One chunk step in three phases, each a set of independent MMA chains:
+//   A: X = K S^T and Y = Q S^T together (k split in even/odd halves);
+//      R = diag(b) (V - diag(e^gamma) X)
+//   B: Delta = T R
+//   C: O = diag(e^gamma) Y + A Delta, and S <- e^{gamma_C} S + Delta~^T K
+// Operand copies for chunk c+1: K and Q (double-buffered) at the start of
+// chunk c, V and the gate table after phase A, T after B, A after C.
 template <int D>
 __global__ void __launch_bounds__(DELTA_THREADS, 1) delta_state_kernel(DeltaArgs a) {
     using L = StateSmem<D>;
@@ -263,7 +270,6 @@ __global__ void __launch_bounds__(DELTA_THREADS, 1) delta_state_kernel(DeltaArgs
     constexpr int DW = NT_D / 4;    // n-tiles of d per warp in the update (4 warps across d)
     extern __shared__ __align__(16) float sm[];
     float* Ss = sm + L::S0;
-    float* Qs = sm + L::Q0;
     float* Ts = sm + L::T0;
     float* As = sm + L::A0;
     float* Vs = sm + L::V0;
@@ -290,8 +296,11 @@ __global__ void __launch_bounds__(DELTA_THREADS, 1) delta_state_kernel(DeltaArgs
         }
     };
     auto chunk_base = [&](int c) { return static_cast<int64_t>(c) * a.hv + h; };
-    auto issue_K = [&](int c) {
-        if (c < a.nchunks) rows(sm + L::K0 + (c & 1) * DC * P, P, a.c_qk + hk * D, D, c);
+    auto issue_KQ = [&](int c) {
+        if (c < a.nchunks) {
+            rows(sm + L::K0 + (c & 1) * DC * P, P, a.c_qk + hk * D, D, c);
+            rows(sm + L::Q0 + (c & 1) * DC * P, P, hk * D, D, c);
+        }
         cp_async_commit();
     };
     auto issue_VG = [&](int c) {
@@ -305,11 +314,8 @@ __global__ void __launch_bounds__(DELTA_THREADS, 1) delta_state_kernel(DeltaArgs
         if (c < a.nchunks) mat(Ts, a.T + chunk_base(c) * DC * DC);
         cp_async_commit();
     };
-    auto issue_QA = [&](int c) {
-        if (c < a.nchunks) {
-            rows(Qs, P, hk * D, D, c);
-            mat(As, a.A + chunk_base(c) * DC * DC);
-        }
+    auto issue_A = [&](int c) {
+        if (c < a.nchunks) mat(As, a.A + chunk_base(c) * DC * DC);
         cp_async_commit();
     };
 
@@ -327,13 +333,14 @@ __global__ void __launch_bounds__(DELTA_THREADS, 1) delta_state_kernel(DeltaArgs
     // Output-tile ownership for the C x NV products: m-tile warp/2, n-tiles 2*(warp%2), +1.
     const int omt = warp >> 1, ont0 = 2 * (warp & 1);
 
-    issue_K(0);
+    issue_KQ(0);
     issue_VG(0);
     issue_T(0);
-    issue_QA(0);
+    issue_A(0);
     for (int chunk = 0; chunk < a.nchunks; ++chunk) {
         const int t0 = chunk * DC;
         const float* Ks = sm + L::K0 + (chunk & 1) * DC * P;
+        const float* Qs = sm + L::Q0 + (chunk & 1) * DC * P;
         const float* Gs = sm + L::G0 + (chunk & 1) * DC * 4;
 #pragma unroll
         for (int j = 0; j < DW; ++j)
@@ -342,31 +349,44 @@ __global__ void __launch_bounds__(DELTA_THREADS, 1) delta_state_kernel(DeltaArgs
                 const int i = 16 * smt + g + (e >> 1) * 8, d = 8 * (snt0 + j) + 2 * tg + (e & 1);
                 Ss[i * P + d] = tf32f(S[j][e]);
             }
-        issue_K(chunk + 1);
-        cp_async_wait<3>();        // K(c), V(c), G(c) have landed
+        issue_KQ(chunk + 1);
+        cp_async_wait<3>();        // K(c), Q(c), V(c), G(c) have landed
         __syncthreads();
 
-        // ---- step 1: X = K S^T (C x NV); R = diag(b) (V - diag(e^gamma) X)
+        // ---- phase A: X = K S^T, Y = Q S^T; R = diag(b) (V - diag(e^gamma) X)
+        float y[2][4];
         {
-            float x[2][4] = {};
+            float xa[2][2][4] = {}, ya[2][2][4] = {};
             const float* ka = Ks + (16 * omt + g) * P + tg;
-#pragma unroll 4
-            for (int ks = 0; ks < D / 8; ++ks) {
-                const int c = 8 * ks;
-                const uint32_t a0 = lds_u32(ka + c), a1 = lds_u32(ka + 8 * P + c), a2 = lds_u32(ka + c + 4),
-                               a3 = lds_u32(ka + 8 * P + c + 4);
+            const float* qa = Qs + (16 * omt + g) * P + tg;
+#pragma unroll 2
+            for (int ks = 0; ks < D / 8; ks += 2) {
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const float* sb = Ss + (8 * (ont0 + j) + g) * P + c + tg;
-                    mma_tf32(x[j], a0, a1, a2, a3, lds_u32(sb), lds_u32(sb + 4));
+                for (int p = 0; p < 2; ++p) {
+                    const int c = 8 * (ks + p);
+                    const uint32_t k0 = lds_u32(ka + c), k1 = lds_u32(ka + 8 * P + c), k2 = lds_u32(ka + c + 4),
+                                   k3 = lds_u32(ka + 8 * P + c + 4);
+                    const uint32_t q0 = lds_u32(qa + c), q1 = lds_u32(qa + 8 * P + c), q2 = lds_u32(qa + c + 4),
+                                   q3 = lds_u32(qa + 8 * P + c + 4);
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const float* sb = Ss + (8 * (ont0 + j) + g) * P + c + tg;
+                        const uint32_t b0 = lds_u32(sb), b1 = lds_u32(sb + 4);
+                        mma_tf32(xa[j][p], k0, k1, k2, k3, b0, b1);
+                        mma_tf32(ya[j][p], q0, q1, q2, q3, b0, b1);
+                    }
                 }
             }
+            const float e_lo = Gs[4 * (16 * omt + g) + 1], e_hi = Gs[4 * (16 * omt + g + 8) + 1];
 #pragma unroll
             for (int j = 0; j < 2; ++j)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int t = 16 * omt + g + (e >> 1) * 8, i = 8 * (ont0 + j) + 2 * tg + (e & 1);
-                    Rs[t * PR + i] = tf32f(Gs[4 * t + 2] * (Vs[t * PR + i] - Gs[4 * t + 1] * x[j][e]));
+                    const float ex = (e >> 1) ? e_hi : e_lo;
+                    const float x = xa[j][0][e] + xa[j][1][e];
+                    y[j][e] = ex * (ya[j][0][e] + ya[j][1][e]);
+                    Rs[t * PR + i] = tf32f(Gs[4 * t + 2] * (Vs[t * PR + i] - ex * x));
                 }
         }
         __syncthreads();
@@ -374,7 +394,7 @@ __global__ void __launch_bounds__(DELTA_THREADS, 1) delta_state_kernel(DeltaArgs
         cp_async_wait<3>();        // T(c) has landed
         __syncthreads();
 
-        // ---- step 2: Delta = T R (T unit lower triangular)
+        // ---- phase B: Delta = T R (T unit lower triangular)
         {
             float dl[2][4] = {};
             const float* ta = Ts + (16 * omt + g) * PT + tg;
@@ -399,29 +419,11 @@ __global__ void __launch_bounds__(DELTA_THREADS, 1) delta_state_kernel(DeltaArgs
         }
         __syncthreads();
         issue_T(chunk + 1);
-        cp_async_wait<3>();        // Q(c), A(c) have landed
+        cp_async_wait<3>();        // A(c) has landed
         __syncthreads();
 
-        // ---- step 3: O = diag(e^gamma) Q S^T + A Delta
+        // ---- phase C: O = Y + A Delta;  S <- e^{gamma_C} S + Delta~^T K
         {
-            float oc[2][4] = {};
-            const float* qa = Qs + (16 * omt + g) * P + tg;
-#pragma unroll 4
-            for (int ks = 0; ks < D / 8; ++ks) {
-                const int c = 8 * ks;
-                const uint32_t a0 = lds_u32(qa + c), a1 = lds_u32(qa + 8 * P + c), a2 = lds_u32(qa + c + 4),
-                               a3 = lds_u32(qa + 8 * P + c + 4);
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const float* sb = Ss + (8 * (ont0 + j) + g) * P + c + tg;
-                    mma_tf32(oc[j], a0, a1, a2, a3, lds_u32(sb), lds_u32(sb + 4));
-                }
-            }
-            const float e_lo = Gs[4 * (16 * omt + g) + 1], e_hi = Gs[4 * (16 * omt + g + 8) + 1];
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                oc[j][0] *= e_lo; oc[j][1] *= e_lo; oc[j][2] *= e_hi; oc[j][3] *= e_hi;
-            }
             const float* aa = As + (16 * omt + g) * PT + tg;
             for (int ks = 0; ks < 2 * omt + 2; ++ks) {
                 const int c = 8 * ks;
@@ -430,24 +432,9 @@ __global__ void __launch_bounds__(DELTA_THREADS, 1) delta_state_kernel(DeltaArgs
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     const float* rb = Rs + (c + tg) * PR + 8 * (ont0 + j) + g;
-                    mma_tf32(oc[j], a0, a1, a2, a3, lds_u32(rb), lds_u32(rb + 4 * PR));
+                    mma_tf32(y[j], a0, a1, a2, a3, lds_u32(rb), lds_u32(rb + 4 * PR));
                 }
             }
-#pragma unroll
-            for (int j = 0; j < 2; ++j)
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int t = 16 * omt + g + 8 * hh, i = 8 * (ont0 + j) + 2 * tg;
-                    if (t0 + t < a.n)
-                        *reinterpret_cast<float2*>(a.o + static_cast<int64_t>(t0 + t) * a.c_v + h * D + i0 + i) =
-                            make_float2(oc[j][2 * hh], oc[j][2 * hh + 1]);
-                }
-        }
-        __syncthreads();           // every warp has read Q and A
-        issue_QA(chunk + 1);
-
-        // ---- step 4: S <- e^{gamma_C} S + Delta~^T K, Delta~ = diag(e^{gamma_C - gamma}) Delta
-        {
             const float dec = Gs[4 * (DC - 1) + 1];
 #pragma unroll
             for (int j = 0; j < DW; ++j)
@@ -466,8 +453,18 @@ __global__ void __launch_bounds__(DELTA_THREADS, 1) delta_state_kernel(DeltaArgs
                     mma_tf32(S[j], a0, a1, a2, a3, lds_u32(kb), lds_u32(kb + 4 * P));
                 }
             }
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int t = 16 * omt + g + 8 * hh, i = 8 * (ont0 + j) + 2 * tg;
+                    if (t0 + t < a.n)
+                        *reinterpret_cast<float2*>(a.o + static_cast<int64_t>(t0 + t) * a.c_v + h * D + i0 + i) =
+                            make_float2(y[j][2 * hh], y[j][2 * hh + 1]);
+                }
         }
-        __syncthreads();
+        __syncthreads();           // every warp has read A, Delta, K(c), Q(c), S
+        issue_A(chunk + 1);
     }
     cp_async_wait<0>();
 #pragma unroll
