@@ -33,6 +33,7 @@ size_t delta_scratch_bytes(int hv, int d, int64_t n);
 cudaError_t launch_gated_norm(const gdn_layer&, const float*, const uint16_t*, int64_t, int64_t, uint16_t*, float*,
                               float*, cudaStream_t);
 int read_and_clear_gemm_error();
+int read_and_clear_delta_error();
 }  // namespace gdn
 
 using namespace gdn;
@@ -272,6 +273,7 @@ int gdn_delta_rule(const gdn_layer* layer, const float* qkv, const float* log_a,
     if (r) return r;
     if (n_tokens < 1 || n_tokens > 0x7fffffff) return fail(GDN_EINVAL, "gdn_delta_rule: n_tokens >= 1 required");
     if (!qkv || !log_a || !b || !state_out || !o || !scratch) return fail(GDN_EINVAL, "gdn_delta_rule: NULL pointer");
+    if (!aligned(qkv, 16) || !aligned(scratch, 16) || !aligned(o, 8)) return fail(GDN_EINVAL, "gdn_delta_rule: qkv and scratch 16-byte, o 8-byte alignment required");
     if (scratch_bytes < delta_scratch_bytes(static_cast<int>(s.hv), static_cast<int>(s.d), n_tokens))
         return fail(GDN_ENOMEM, "gdn_delta_rule: scratch too small");
     GDN_LAUNCH(launch_delta(*layer, qkv, log_a, b, n_tokens, state_in, state_out, o, scratch, static_cast<cudaStream_t>(stream)),
@@ -383,6 +385,7 @@ int gdn_sync_status(void* stream) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "gdn_sync_status");
     if (read_and_clear_gemm_error()) return fail(GDN_ETIMEOUT, "a bounded wait in the projection kernel ran out");
+    if (read_and_clear_delta_error()) return fail(GDN_ETIMEOUT, "a bounded wait in the delta-rule kernel ran out");
     return GDN_OK;
 }
 
@@ -409,6 +412,7 @@ extern "C" int gdn_delta_rule_noalloc(const gdn_layer* layer, const float* qkv, 
     if (r) return r;
     if (n_tokens < 1 || n_tokens > 0x7fffffff) return fail(GDN_EINVAL, "gdn_delta_rule_noalloc: n_tokens >= 1 required");
     if (!qkv || !log_a || !b || !state_out || !o) return fail(GDN_EINVAL, "gdn_delta_rule_noalloc: NULL pointer");
+    if (!aligned(qkv, 16) || !aligned(o, 8)) return fail(GDN_EINVAL, "gdn_delta_rule_noalloc: qkv 16-byte, o 8-byte alignment required");
     const size_t need = delta_scratch_bytes(static_cast<int>(s.hv), static_cast<int>(s.d), n_tokens);
     if (need > GDN_NOALLOC_SCRATCH_BYTES) {
         const size_t per_chunk = delta_scratch_bytes(static_cast<int>(s.hv), static_cast<int>(s.d), 1);

@@ -31,17 +31,26 @@
 //                rows split across CTAs with no communication.  The fp32 state
 //                stays in registers as the accumulator fragments of the
 //                update product.  Every operand of chunk c+1 is copied into
-//                shared memory with cp.async while chunk c computes: each
-//                copy is issued right after the operand's last use in chunk c
-//                (K and Q, used in the first phase, are double-buffered).
+//                shared memory by TMA (issued by one thread, completion on
+//                mbarriers) while chunk c computes: each copy is issued right
+//                after the operand's last use in chunk c (K and Q, used in the
+//                first phase, are double-buffered).  K, Q, V arrive as 2-D
+//                boxes of 64 tokens x 32 floats with the 128-byte swizzle; T
+//                and A are written by delta_prep in that same swizzled image,
+//                so a 1-D bulk copy lands them ready.
 // Products use mma.sync m16n8k8 with tf32 operands rounded to nearest (the
 // conv writes q, k, v already rounded; T, A, S, R, Delta are rounded where
 // they are produced) and fp32 accumulation; everything else is fp32.
 // Rounding every operand to tf32 keeps o and S within ~5e-4 (relative L2) of
 // the exact recurrence on the test workloads.
 #include "common.cuh"
+#include "tma.cuh"
+
+#include <mutex>
 
 namespace gdn {
+
+static __device__ int g_delta_error;
 
 constexpr int DC = GDN_CHUNK;  // 64
 constexpr int DELTA_THREADS = 256;
@@ -85,6 +94,29 @@ __device__ __forceinline__ void mma_tf32(float (&c)[4], uint32_t a0, uint32_t a1
 
 __device__ __forceinline__ uint32_t lds_u32(const float* p) { return __float_as_uint(*p); }
 
+// ldmatrix on fp32 data: an 8x4 block of fp32 is an 8x8 block of b16 pairs, and
+// the b16 fragment of thread l (row l/4, elements 2(l%4), 2(l%4)+1) is exactly
+// fp32 element (l/4, l%4) -- the tf32 m16n8k8 fragment position.  Lane l passes
+// the address of row l%8 of matrix l/8.
+__device__ __forceinline__ void ldsm_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3, const float* p) {
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(a));
+}
+// A fragment (16x8 tile at row0, col0 of a row-major [m][k] array with pitch P).
+template <int P>
+__device__ __forceinline__ const float* a_frag_addr(const float* base, int row0, int col0, int lane) {
+    const int mat = lane >> 3, r = lane & 7;
+    return base + (row0 + r + 8 * (mat & 1)) * P + col0 + 4 * (mat >> 1);
+}
+// Two B fragments (n-tiles n0 and n0+8, k-block col0) of an [n][k] array with pitch P.
+template <int P>
+__device__ __forceinline__ const float* b2_frag_addr(const float* base, int n0, int col0, int lane) {
+    const int mat = lane >> 3, r = lane & 7;
+    return base + (n0 + r + 8 * (mat >> 1)) * P + col0 + 4 * (mat & 1);
+}
+
 // Load rows [t0, t0+DC) of a head slice of the fp32 qkv buffer into smem
 // (pitch P floats), rounded to tf32; rows past n are zero.
 template <int D, int P>
@@ -97,6 +129,13 @@ __device__ __forceinline__ void load_rows_tf32(float* dst, const float* qkv, int
         float* d = dst + r * P + 4 * c4;
         d[0] = tf32f(v.x); d[1] = tf32f(v.y); d[2] = tf32f(v.z); d[3] = tf32f(v.w);
     }
+}
+
+// Float index of element (r, c) of a [DC][DC] matrix stored as the shared-memory
+// image the state pass reads: two slabs of DC rows x 32 floats (c / 32), each
+// with 128-byte rows and the 128-byte swizzle.
+__device__ __forceinline__ int swz64(int r, int c) {
+    return (c >> 5) * (DC * 32) + static_cast<int>(sw128_f32(r, c & 31) >> 2);
 }
 
 // ------------------------------------------------------------------ prep
@@ -176,7 +215,7 @@ __global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(DeltaArgs 
                 const bool live = 8 * nt <= 16 * mt + 15;
                 const float dec = (live && jj <= i) ? expf(gl[i] - gl[jj]) : 0.f;
                 Ls[i * PL + jj] = (jj < i) ? bb[i] * dec * ck[j][e] : 0.f;
-                aout[i * DC + jj] = tf32f(dec * cq[j][e]);
+                aout[swz64(i, jj)] = tf32f(dec * cq[j][e]);
             }
         }
     }
@@ -229,7 +268,10 @@ __global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(DeltaArgs 
         __syncthreads();
     }
     float* tout = a.T + (static_cast<int64_t>(chunk) * a.hv + h) * DC * DC;
-    for (int idx = tid; idx < DC * DC; idx += DELTA_THREADS) tout[idx] = tf32f(Ts[(idx / DC) * PL + idx % DC]);
+    for (int idx = tid; idx < DC * DC; idx += DELTA_THREADS) {
+        const int r = idx / DC, c = idx % DC;
+        tout[swz64(r, c)] = tf32f(Ts[r * PL + c]);
+    }
     if (tid < DC) {
         const float gv = gl[tid];
         *reinterpret_cast<float4*>(a.G + ((static_cast<int64_t>(chunk) * a.hv + h) * DC + tid) * 4) =
@@ -241,82 +283,100 @@ __global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(DeltaArgs 
 
 template <int D>
 struct StateSmem {
-    static constexpr int P = D + 4;    // K, Q, S row pitch (conflict-free fragment loads)
-    static constexpr int PT = DC + 4;  // T, A row pitch
-    static constexpr int PR = NV + 8;  // V, R/Delta row pitch (conflict-free in both orientations)
-    static constexpr int K0 = 0;                   // Ks[2][DC][P]
-    static constexpr int Q0 = K0 + 2 * DC * P;     // Qs[2][DC][P]
-    static constexpr int S0 = Q0 + 2 * DC * P;     // Ss[NV][P]
-    static constexpr int T0 = S0 + NV * P;         // Ts[DC][PT]
-    static constexpr int A0 = T0 + DC * PT;        // As[DC][PT]
-    static constexpr int V0 = A0 + DC * PT;        // Vs[DC][PR]
-    static constexpr int R0 = V0 + DC * PR;        // Rs[DC][PR]
-    static constexpr int G0 = R0 + DC * PR;        // Gs[2][DC][4]
-    static constexpr int FLOATS = G0 + 2 * DC * 4;
+    // byte offsets; every TMA destination is 1024-byte aligned
+    static constexpr int SLAB = DC * 128;          // 64 token rows x 32 floats
+    static constexpr int NSLAB = D / 32;
+    static constexpr int KQ_BYTES = NSLAB * SLAB;  // one K or Q tile
+    static constexpr int P = D + 4;                // S row pitch (floats)
+    static constexpr int PT = DC + 4;              // R^T, Delta^T row pitch (floats)
+    static constexpr int K0 = 0;                               // Ks[2]
+    static constexpr int Q0 = K0 + 2 * KQ_BYTES;               // Qs[2]
+    static constexpr int T0 = Q0 + 2 * KQ_BYTES;               // Ts (2 slabs)
+    static constexpr int A0 = T0 + 2 * SLAB;                   // As (2 slabs)
+    static constexpr int V0 = A0 + 2 * SLAB;                   // Vs (1 slab: NV = 32 floats)
+    static constexpr int G0 = V0 + SLAB;                       // Gs[2][DC][4]
+    static constexpr int S0 = G0 + 2 * DC * 16;                // Ss[NV][P]
+    static constexpr int R0 = S0 + NV * P * 4;                 // Rt[NV][PT]
+    static constexpr int E0 = R0 + NV * PT * 4;                // Et[NV][PT]
+    static constexpr int B0 = E0 + NV * PT * 4;                // mbarriers: KQ[2], V, T, A
+    static constexpr int BYTES = B0 + 64;
 };
 
 // One chunk step in three phases, each a set of independent MMA chains:
 //   A: X = K S^T and Y = Q S^T together (k split in even/odd halves);
-//      R = diag(b) (V - diag(e^gamma) X)
-//   B: Delta = T R
+//      R = diag(b) (V - diag(e^gamma) X), stored transposed
+//   B: Delta = T R, stored transposed (plain and scaled by e^{gamma_C - gamma})
 //   C: O = diag(e^gamma) Y + A Delta, and S <- e^{gamma_C} S + Delta~^T K
-// Operand copies for chunk c+1: K and Q (double-buffered) at the start of
-// chunk c, V and the gate table after phase A, T after B, A after C.
+// Operand copies for chunk c+1 (one thread, TMA): K and Q (double-buffered) at
+// the start of chunk c, V and the gate table after phase A, T after B, A after
+// C.  Fragments come from shared memory by ldmatrix, except K in the update,
+// whose [token][d] layout is the transpose of what ldmatrix delivers.
 template <int D>
-__global__ void __launch_bounds__(DELTA_THREADS, 1) delta_state_kernel(DeltaArgs a) {
+__global__ void __launch_bounds__(DELTA_THREADS, 1)
+delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
     using L = StateSmem<D>;
-    constexpr int P = L::P, PT = L::PT, PR = L::PR;
+    constexpr int P = L::P, PT = L::PT;
     constexpr int NT_D = D / 8;     // n-tiles across d
     constexpr int DW = NT_D / 4;    // n-tiles of d per warp in the update (4 warps across d)
-    extern __shared__ __align__(16) float sm[];
-    float* Ss = sm + L::S0;
-    float* Ts = sm + L::T0;
-    float* As = sm + L::A0;
-    float* Vs = sm + L::V0;
-    float* Rs = sm + L::R0;
+    extern __shared__ __align__(1024) unsigned char smb[];
+    unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smb) + 1023) & ~uintptr_t(1023));
+    float* Ss = reinterpret_cast<float*>(base + L::S0);
+    float* Rt = reinterpret_cast<float*>(base + L::R0);
+    float* Et = reinterpret_cast<float*>(base + L::E0);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(base + L::B0);
+    uint64_t* bKQ = bars;       // [2]
+    uint64_t* bV = bars + 2;
+    uint64_t* bT = bars + 3;
+    uint64_t* bA = bars + 4;
+    __shared__ int abort_flag;
 
     const int h = blockIdx.x, i0 = blockIdx.y * NV, hk = h / a.ratio;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, tg = lane & 3;
+    const bool issuer = tid == 0;
 
-    // ---- asynchronous copies of one chunk's operands (rows past n are zero-filled)
-    auto rows = [&](float* dst, int pitch, int col0, int width, int c) {   // token rows of qkv
-        const int t0 = c * DC, w4 = width / 4;
-        for (int idx = tid; idx < DC * w4; idx += DELTA_THREADS) {
-            const int r = idx / w4, c4 = idx % w4, t = t0 + r;
-            const bool ok = t < a.n;
-            const float* src = ok ? a.qkv + static_cast<int64_t>(t) * a.c_conv + col0 + 4 * c4 : a.qkv;
-            cp_async16(dst + r * pitch + 4 * c4, src, ok);
-        }
-    };
-    auto mat = [&](float* dst, const float* src) {                        // a [DC][DC] scratch matrix
-        for (int idx = tid; idx < DC * DC / 4; idx += DELTA_THREADS) {
-            const int r = idx / (DC / 4), c4 = idx % (DC / 4);
-            cp_async16(dst + r * PT + 4 * c4, src + 4 * idx, true);
-        }
-    };
+    if (issuer) {
+        for (int i = 0; i < 5; ++i) mbar_init_cta(bars + i, 1);
+        mbar_init_fence();
+        abort_flag = 0;
+    }
+    __syncthreads();
+
     auto chunk_base = [&](int c) { return static_cast<int64_t>(c) * a.hv + h; };
+    // ---- one-thread TMA copies of a chunk's operands (rows past n arrive as zeros)
     auto issue_KQ = [&](int c) {
-        if (c < a.nchunks) {
-            rows(sm + L::K0 + (c & 1) * DC * P, P, a.c_qk + hk * D, D, c);
-            rows(sm + L::Q0 + (c & 1) * DC * P, P, hk * D, D, c);
+        if (c >= a.nchunks) return;
+        uint64_t* bar = bKQ + (c & 1);
+        unsigned char* kd = base + L::K0 + (c & 1) * L::KQ_BYTES;
+        unsigned char* qd = base + L::Q0 + (c & 1) * L::KQ_BYTES;
+        mbar_expect_tx(bar, 2 * L::KQ_BYTES);
+        for (int sl = 0; sl < L::NSLAB; ++sl) {
+            tma_load_2d_tile(kd + sl * L::SLAB, &qkv_map, bar, a.c_qk + hk * D + 32 * sl, c * DC);
+            tma_load_2d_tile(qd + sl * L::SLAB, &qkv_map, bar, hk * D + 32 * sl, c * DC);
         }
-        cp_async_commit();
     };
     auto issue_VG = [&](int c) {
-        if (c < a.nchunks) {
-            rows(Vs, PR, 2 * a.c_qk + h * D + i0, NV, c);
-            if (tid < DC) cp_async16(sm + L::G0 + (c & 1) * DC * 4 + 4 * tid, a.G + (chunk_base(c) * DC + tid) * 4, true);
-        }
-        cp_async_commit();
+        if (c >= a.nchunks) return;
+        mbar_expect_tx(bV, L::SLAB + DC * 16);
+        tma_load_2d_tile(base + L::V0, &qkv_map, bV, 2 * a.c_qk + h * D + i0, c * DC);
+        bulk_load_1d(base + L::G0 + (c & 1) * DC * 16, a.G + chunk_base(c) * DC * 4, DC * 16, bV);
     };
     auto issue_T = [&](int c) {
-        if (c < a.nchunks) mat(Ts, a.T + chunk_base(c) * DC * DC);
-        cp_async_commit();
+        if (c >= a.nchunks) return;
+        mbar_expect_tx(bT, 2 * L::SLAB);
+        bulk_load_1d(base + L::T0, a.T + chunk_base(c) * DC * DC, 2 * L::SLAB, bT);
     };
     auto issue_A = [&](int c) {
-        if (c < a.nchunks) mat(As, a.A + chunk_base(c) * DC * DC);
-        cp_async_commit();
+        if (c >= a.nchunks) return;
+        mbar_expect_tx(bA, 2 * L::SLAB);
+        bulk_load_1d(base + L::A0, a.A + chunk_base(c) * DC * DC, 2 * L::SLAB, bA);
+    };
+    auto wait = [&](uint64_t* bar, uint32_t parity) {
+        if (!mbar_wait_bounded(bar, parity, &g_delta_error, ERR_WAIT_TIMEOUT)) abort_flag = 1;
+    };
+    // fp32 element (r, c) of a swizzled tile of 32-float slabs, as a float pointer
+    auto tile = [&](int off, int r, int c) {
+        return reinterpret_cast<const float*>(base + off + (c >> 5) * L::SLAB + sw128_f32(r, c & 31));
     };
 
     // State fragments: warp owns rows 16*(warp/4) .. +15 of the tile and d columns
@@ -332,16 +392,20 @@ __global__ void __launch_bounds__(DELTA_THREADS, 1) delta_state_kernel(DeltaArgs
         }
     // Output-tile ownership for the C x NV products: m-tile warp/2, n-tiles 2*(warp%2), +1.
     const int omt = warp >> 1, ont0 = 2 * (warp & 1);
+    // ldmatrix row of this lane: matrix lane/8, row lane%8
+    const int lm = lane >> 3, lr = lane & 7;
 
-    issue_KQ(0);
-    issue_VG(0);
-    issue_T(0);
-    issue_A(0);
+    if (issuer) {
+        issue_KQ(0);
+        issue_VG(0);
+        issue_T(0);
+        issue_A(0);
+    }
     for (int chunk = 0; chunk < a.nchunks; ++chunk) {
         const int t0 = chunk * DC;
-        const float* Ks = sm + L::K0 + (chunk & 1) * DC * P;
-        const float* Qs = sm + L::Q0 + (chunk & 1) * DC * P;
-        const float* Gs = sm + L::G0 + (chunk & 1) * DC * 4;
+        const int KO = L::K0 + (chunk & 1) * L::KQ_BYTES;
+        const int QO = L::Q0 + (chunk & 1) * L::KQ_BYTES;
+        const float* Gs = reinterpret_cast<const float*>(base + L::G0 + (chunk & 1) * DC * 16);
 #pragma unroll
         for (int j = 0; j < DW; ++j)
 #pragma unroll
@@ -349,32 +413,34 @@ __global__ void __launch_bounds__(DELTA_THREADS, 1) delta_state_kernel(DeltaArgs
                 const int i = 16 * smt + g + (e >> 1) * 8, d = 8 * (snt0 + j) + 2 * tg + (e & 1);
                 Ss[i * P + d] = tf32f(S[j][e]);
             }
-        issue_KQ(chunk + 1);
-        cp_async_wait<3>();        // K(c), Q(c), V(c), G(c) have landed
+        if (issuer) {
+            fence_proxy_async_smem();
+            issue_KQ(chunk + 1);
+        }
+        wait(bKQ + (chunk & 1), (chunk >> 1) & 1);
+        wait(bV, chunk & 1);
         __syncthreads();
+        if (abort_flag) break;     // uniform: read after a barrier
 
         // ---- phase A: X = K S^T, Y = Q S^T; R = diag(b) (V - diag(e^gamma) X)
         float y[2][4];
         {
             float xa[2][2][4] = {}, ya[2][2][4] = {};
-            const float* ka = Ks + (16 * omt + g) * P + tg;
-            const float* qa = Qs + (16 * omt + g) * P + tg;
+            const int arow = 16 * omt + lr + 8 * (lm & 1);
+            const float* sb = b2_frag_addr<P>(Ss, 8 * ont0, 0, lane);
 #pragma unroll 2
             for (int ks = 0; ks < D / 8; ks += 2) {
 #pragma unroll
                 for (int p = 0; p < 2; ++p) {
-                    const int c = 8 * (ks + p);
-                    const uint32_t k0 = lds_u32(ka + c), k1 = lds_u32(ka + 8 * P + c), k2 = lds_u32(ka + c + 4),
-                                   k3 = lds_u32(ka + 8 * P + c + 4);
-                    const uint32_t q0 = lds_u32(qa + c), q1 = lds_u32(qa + 8 * P + c), q2 = lds_u32(qa + c + 4),
-                                   q3 = lds_u32(qa + 8 * P + c + 4);
-#pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        const float* sb = Ss + (8 * (ont0 + j) + g) * P + c + tg;
-                        const uint32_t b0 = lds_u32(sb), b1 = lds_u32(sb + 4);
-                        mma_tf32(xa[j][p], k0, k1, k2, k3, b0, b1);
-                        mma_tf32(ya[j][p], q0, q1, q2, q3, b0, b1);
-                    }
+                    const int c = 8 * (ks + p) + 4 * (lm >> 1);
+                    uint32_t k0, k1, k2, k3, q0, q1, q2, q3, b0, b1, b2, b3;
+                    ldsm_x4(k0, k1, k2, k3, tile(KO, arow, c));
+                    ldsm_x4(q0, q1, q2, q3, tile(QO, arow, c));
+                    ldsm_x4(b0, b1, b2, b3, sb + 8 * (ks + p));
+                    mma_tf32(xa[0][p], k0, k1, k2, k3, b0, b1);
+                    mma_tf32(ya[0][p], q0, q1, q2, q3, b0, b1);
+                    mma_tf32(xa[1][p], k0, k1, k2, k3, b2, b3);
+                    mma_tf32(ya[1][p], q0, q1, q2, q3, b2, b3);
                 }
             }
             const float e_lo = Gs[4 * (16 * omt + g) + 1], e_hi = Gs[4 * (16 * omt + g + 8) + 1];
@@ -386,27 +452,29 @@ __global__ void __launch_bounds__(DELTA_THREADS, 1) delta_state_kernel(DeltaArgs
                     const float ex = (e >> 1) ? e_hi : e_lo;
                     const float x = xa[j][0][e] + xa[j][1][e];
                     y[j][e] = ex * (ya[j][0][e] + ya[j][1][e]);
-                    Rs[t * PR + i] = tf32f(Gs[4 * t + 2] * (Vs[t * PR + i] - ex * x));
+                    Rt[i * PT + t] = tf32f(Gs[4 * t + 2] * (*tile(L::V0, t, i) - ex * x));
                 }
         }
         __syncthreads();
-        issue_VG(chunk + 1);
-        cp_async_wait<3>();        // T(c) has landed
+        if (issuer) {
+            fence_proxy_async_smem();
+            issue_VG(chunk + 1);
+        }
+        wait(bT, chunk & 1);
         __syncthreads();
+        if (abort_flag) break;
 
         // ---- phase B: Delta = T R (T unit lower triangular)
         {
             float dl[2][4] = {};
-            const float* ta = Ts + (16 * omt + g) * PT + tg;
+            const int arow = 16 * omt + lr + 8 * (lm & 1);
+            const float* rb = b2_frag_addr<PT>(Rt, 8 * ont0, 0, lane);
             for (int ks = 0; ks < 2 * omt + 2; ++ks) {
-                const int c = 8 * ks;
-                const uint32_t a0 = lds_u32(ta + c), a1 = lds_u32(ta + 8 * PT + c), a2 = lds_u32(ta + c + 4),
-                               a3 = lds_u32(ta + 8 * PT + c + 4);
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const float* rb = Rs + (c + tg) * PR + 8 * (ont0 + j) + g;
-                    mma_tf32(dl[j], a0, a1, a2, a3, lds_u32(rb), lds_u32(rb + 4 * PR));
-                }
+                uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+                ldsm_x4(a0, a1, a2, a3, tile(L::T0, arow, 8 * ks + 4 * (lm >> 1)));
+                ldsm_x4(b0, b1, b2, b3, rb + 8 * ks);
+                mma_tf32(dl[0], a0, a1, a2, a3, b0, b1);
+                mma_tf32(dl[1], a0, a1, a2, a3, b2, b3);
             }
             __syncthreads();       // every warp has read R
 #pragma unroll
@@ -414,44 +482,55 @@ __global__ void __launch_bounds__(DELTA_THREADS, 1) delta_state_kernel(DeltaArgs
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int t = 16 * omt + g + (e >> 1) * 8, i = 8 * (ont0 + j) + 2 * tg + (e & 1);
-                    Rs[t * PR + i] = tf32f(dl[j][e]);
+                    Rt[i * PT + t] = tf32f(dl[j][e]);
+                    Et[i * PT + t] = tf32f(dl[j][e] * Gs[4 * t + 3]);
                 }
         }
         __syncthreads();
-        issue_T(chunk + 1);
-        cp_async_wait<3>();        // A(c) has landed
+        if (issuer) {
+            fence_proxy_async_smem();
+            issue_T(chunk + 1);
+        }
+        wait(bA, chunk & 1);
         __syncthreads();
+        if (abort_flag) break;
 
         // ---- phase C: O = Y + A Delta;  S <- e^{gamma_C} S + Delta~^T K
         {
-            const float* aa = As + (16 * omt + g) * PT + tg;
+            const int arow = 16 * omt + lr + 8 * (lm & 1);
+            const float* db = b2_frag_addr<PT>(Rt, 8 * ont0, 0, lane);
             for (int ks = 0; ks < 2 * omt + 2; ++ks) {
-                const int c = 8 * ks;
-                const uint32_t a0 = lds_u32(aa + c), a1 = lds_u32(aa + 8 * PT + c), a2 = lds_u32(aa + c + 4),
-                               a3 = lds_u32(aa + 8 * PT + c + 4);
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const float* rb = Rs + (c + tg) * PR + 8 * (ont0 + j) + g;
-                    mma_tf32(y[j], a0, a1, a2, a3, lds_u32(rb), lds_u32(rb + 4 * PR));
-                }
+                uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+                ldsm_x4(a0, a1, a2, a3, tile(L::A0, arow, 8 * ks + 4 * (lm >> 1)));
+                ldsm_x4(b0, b1, b2, b3, db + 8 * ks);
+                mma_tf32(y[0], a0, a1, a2, a3, b0, b1);
+                mma_tf32(y[1], a0, a1, a2, a3, b2, b3);
             }
             const float dec = Gs[4 * (DC - 1) + 1];
 #pragma unroll
             for (int j = 0; j < DW; ++j)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) S[j][e] *= dec;
+            const float* ea = a_frag_addr<PT>(Et, 16 * smt, 0, lane);
+            // B fragment (k = token tg / tg+4, n = d) of K(c): byte offsets within the swizzled
+            // tile for ks = 0; token 8ks+r sits 1024*ks bytes further (same swizzle key r).
+            const unsigned char* kbase = base + KO;
+            uint32_t koff[DW][2];
+#pragma unroll
+            for (int j = 0; j < DW; ++j) {
+                const int d = 8 * (snt0 + j) + g;
+                koff[j][0] = (d >> 5) * L::SLAB + sw128_f32(tg, d & 31);
+                koff[j][1] = (d >> 5) * L::SLAB + sw128_f32(tg + 4, d & 31);
+            }
 #pragma unroll 2
             for (int ks = 0; ks < DC / 8; ++ks) {
-                const int t = 8 * ks + tg;
-                const float* da = Rs + t * PR + 16 * smt + g;
-                const float k0 = Gs[4 * t + 3], k1 = Gs[4 * (t + 4) + 3];
-                const uint32_t a0 = to_tf32(da[0] * k0), a1 = to_tf32(da[8] * k0), a2 = to_tf32(da[4 * PR] * k1),
-                               a3 = to_tf32(da[4 * PR + 8] * k1);
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(a0, a1, a2, a3, ea + 8 * ks);
+                const unsigned char* kb = kbase + 1024 * ks;
 #pragma unroll
-                for (int j = 0; j < DW; ++j) {
-                    const float* kb = Ks + t * P + 8 * (snt0 + j) + g;
-                    mma_tf32(S[j], a0, a1, a2, a3, lds_u32(kb), lds_u32(kb + 4 * P));
-                }
+                for (int j = 0; j < DW; ++j)
+                    mma_tf32(S[j], a0, a1, a2, a3, *reinterpret_cast<const uint32_t*>(kb + koff[j][0]),
+                             *reinterpret_cast<const uint32_t*>(kb + koff[j][1]));
             }
 #pragma unroll
             for (int j = 0; j < 2; ++j)
@@ -464,9 +543,18 @@ __global__ void __launch_bounds__(DELTA_THREADS, 1) delta_state_kernel(DeltaArgs
                 }
         }
         __syncthreads();           // every warp has read A, Delta, K(c), Q(c), S
-        issue_A(chunk + 1);
+        if (issuer) {
+            fence_proxy_async_smem();
+            issue_A(chunk + 1);
+        }
     }
-    cp_async_wait<0>();
+    if (abort_flag) {
+        // A wait ran out: let the copies still in flight land (bounded) and return.
+        if (issuer)
+            for (int i = 0; i < 5; ++i)
+                for (uint32_t par = 0; par < 2; ++par) mbar_wait_bounded(bars + i, par, nullptr, 0, 20000000ull);
+        return;
+    }
 #pragma unroll
     for (int j = 0; j < DW; ++j)
 #pragma unroll
@@ -483,11 +571,44 @@ size_t delta_scratch_bytes(int hv, int d, int64_t n) {
     return static_cast<size_t>(nch * per) * sizeof(float);
 }
 
+static PFN_cuTensorMapEncodeTiled_v12000 delta_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void* p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// fp32 qkv [n][c_conv]: boxes of DC tokens x 32 floats, 128-byte swizzle, zero fill.
+static bool make_qkv_map(CUtensorMap* map, const float* qkv, int64_t n, int c_conv) {
+    auto enc = delta_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(c_conv), static_cast<cuuint64_t>(n)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(c_conv) * 4};
+    cuuint32_t box[2] = {32, static_cast<cuuint32_t>(DC)};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(qkv), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int read_and_clear_delta_error() {
+    int v = 0, z = 0;
+    cudaMemcpyFromSymbol(&v, g_delta_error, sizeof(int));
+    if (v) cudaMemcpyToSymbol(g_delta_error, &z, sizeof(int));
+    return v;
+}
+
 template <int D>
 static cudaError_t launch_delta_d(DeltaArgs& a, cudaStream_t st) {
     constexpr int P = D + 4;
     const size_t prep_smem = (2 * DC * P + 2 * DC * (DC + 4) + 3 * 256 + 2 * DC) * sizeof(float);
-    const size_t state_smem = StateSmem<D>::FLOATS * sizeof(float);
+    const size_t state_smem = StateSmem<D>::BYTES + 1024;
     static bool attr = false;
     if (!attr) {
         cudaFuncSetAttribute(delta_prep_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(prep_smem));
@@ -497,7 +618,9 @@ static cudaError_t launch_delta_d(DeltaArgs& a, cudaStream_t st) {
     delta_prep_kernel<D><<<dim3(a.nchunks, a.hv), DELTA_THREADS, prep_smem, st>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    delta_state_kernel<D><<<dim3(a.hv, D / NV), DELTA_THREADS, state_smem, st>>>(a);
+    CUtensorMap map;
+    if (!make_qkv_map(&map, a.qkv, a.n, a.c_conv)) return cudaErrorInvalidValue;
+    delta_state_kernel<D><<<dim3(a.hv, D / NV), DELTA_THREADS, state_smem, st>>>(map, a);
     return cudaGetLastError();
 }
 
