@@ -84,6 +84,7 @@ int check_layer(const gdn_layer* L, Sizes* s) {
     if (L->n_qk_heads < 1 || L->n_v_heads < 1 || L->n_v_heads % L->n_qk_heads)
         return fail(GDN_EINVAL, "n_v_heads must be a positive multiple of n_qk_heads (got %d, %d)", L->n_v_heads, L->n_qk_heads);
     if (L->n_v_heads > 64) return fail(GDN_EINVAL, "n_v_heads <= 64 required (got %d)", L->n_v_heads);
+    if (L->n_v_heads / L->n_qk_heads > 8) return fail(GDN_EINVAL, "at most 8 value heads per key head (got %d)", L->n_v_heads / L->n_qk_heads);
     if (L->hidden < 256 || L->hidden > 16384 || L->hidden % 256)
         return fail(GDN_EINVAL, "hidden must be a multiple of 256 in [256, 16384] (got %d)", L->hidden);
     s->H = L->hidden;

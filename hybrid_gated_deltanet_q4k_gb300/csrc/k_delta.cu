@@ -19,8 +19,9 @@
 // which leaves S unchanged.
 //
 // Two kernels:
-//   delta_prep   one CTA per (chunk, head), all chunks in parallel: gamma,
-//                K K^T and Q K^T on tensor cores, the masked A, and T by
+//   delta_prep   one CTA per (chunk, key head), all chunks in parallel: K K^T
+//                and Q K^T once on tensor cores, then per value head gamma,
+//                the masked A, and T by
 //                blocked inversion of the unit lower-triangular I + L (16x16
 //                diagonal blocks by substitution, off-diagonal blocks by
 //                block products).  Writes T and A (tf32-rounded) and a gate
@@ -117,20 +118,6 @@ __device__ __forceinline__ const float* b2_frag_addr(const float* base, int n0, 
     return base + (n0 + r + 8 * (mat >> 1)) * P + col0 + 4 * (mat & 1);
 }
 
-// Load rows [t0, t0+DC) of a head slice of the fp32 qkv buffer into smem
-// (pitch P floats), rounded to tf32; rows past n are zero.
-template <int D, int P>
-__device__ __forceinline__ void load_rows_tf32(float* dst, const float* qkv, int64_t ld, int col0, int t0, int n) {
-    constexpr int V4 = D / 4;
-    for (int idx = threadIdx.x; idx < DC * V4; idx += DELTA_THREADS) {
-        const int r = idx / V4, c4 = idx % V4, t = t0 + r;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (t < n) v = *reinterpret_cast<const float4*>(qkv + static_cast<int64_t>(t) * ld + col0 + 4 * c4);
-        float* d = dst + r * P + 4 * c4;
-        d[0] = tf32f(v.x); d[1] = tf32f(v.y); d[2] = tf32f(v.z); d[3] = tf32f(v.w);
-    }
-}
-
 // Float index of element (r, c) of a [DC][DC] matrix stored as the shared-memory
 // image the state pass reads: two slabs of DC rows x 32 floats (c / 32), each
 // with 128-byte rows and the 128-byte swizzle.
@@ -140,44 +127,78 @@ __device__ __forceinline__ int swz64(int r, int c) {
 
 // ------------------------------------------------------------------ prep
 
+constexpr int PREP_MAX_RATIO = 8;  // value heads per key head handled by one CTA
+
+template <int D>
+struct PrepSmem {
+    static constexpr int P = D + 4;    // K, Q row pitch (floats)
+    static constexpr int PL = DC + 4;  // KK, QK, L, T row pitch (floats)
+    static constexpr int K0 = 0;                      // Ks[DC][P]   (later: Ls, Ts)
+    static constexpr int Q0 = K0 + DC * P;            // Qs[DC][P]
+    static constexpr int L0 = K0;                     // Ls[DC][PL]  aliases Ks after the products
+    static constexpr int T0 = L0 + DC * PL;           // Ts[DC][PL]
+    static constexpr int KK0 = Q0 + DC * P;           // KK[DC][PL]  k_i . k_j (lower triangle)
+    static constexpr int QK0 = KK0 + DC * PL;         // QK[DC][PL]  q_i . k_j (lower triangle)
+    static constexpr int Z0 = QK0 + DC * PL;          // Zs[3][256]
+    static constexpr int GL0 = Z0 + 3 * 256;          // gamma[PREP_MAX_RATIO][DC]
+    static constexpr int BB0 = GL0 + PREP_MAX_RATIO * DC;  // b[PREP_MAX_RATIO][DC]
+    static constexpr int FLOATS = BB0 + PREP_MAX_RATIO * DC;
+    static_assert(2 * DC * PL <= 2 * DC * P, "L and T must fit in the K and Q region");
+};
+
+// One CTA per (chunk, key head): K K^T and Q K^T once (the value heads of a key
+// head share them), then for each of its value heads the gated L, T = (I+L)^-1,
+// the masked A and the gate table.
 template <int D>
 __global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(DeltaArgs a) {
-    constexpr int P = D + 4;        // row pitch of K, Q (conflict-free A/B fragment loads)
-    constexpr int PL = DC + 4;      // row pitch of L, T
-    extern __shared__ float sm[];
-    float* Ks = sm;                 // [DC][P]
-    float* Qs = Ks + DC * P;        // [DC][P]
-    float* Ls = Qs + DC * P;        // [DC][PL]
-    float* Ts = Ls + DC * PL;       // [DC][PL]
-    float* Zs = Ts + DC * PL;       // [3][16][16]
-    float* gl = Zs + 3 * 256;       // [DC] log a, then gamma
-    float* bb = gl + DC;            // [DC]
+    using L = PrepSmem<D>;
+    constexpr int P = L::P, PL = L::PL;
+    extern __shared__ __align__(16) float sm[];
+    float* Ks = sm + L::K0;
+    float* Qs = sm + L::Q0;
+    float* Ls = sm + L::L0;
+    float* Ts = sm + L::T0;
+    float* KK = sm + L::KK0;
+    float* QK = sm + L::QK0;
+    float* Zs = sm + L::Z0;
 
-    const int chunk = blockIdx.x, h = blockIdx.y, hk = h / a.ratio;
+    const int chunk = blockIdx.x, hk = blockIdx.y;
     const int t0 = chunk * DC;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, tg = lane & 3;
+    const int r = a.ratio;
 
-    load_rows_tf32<D, P>(Ks, a.qkv, a.c_conv, a.c_qk + hk * D, t0, a.n);
-    load_rows_tf32<D, P>(Qs, a.qkv, a.c_conv, hk * D, t0, a.n);
-    if (tid < DC) {
-        const int t = t0 + tid;
-        gl[tid] = t < a.n ? a.log_a[static_cast<int64_t>(t) * a.hv + h] : 0.f;
-        bb[tid] = t < a.n ? a.b[static_cast<int64_t>(t) * a.hv + h] : 0.f;
+    // K and Q rows (tf32 values from the conv) by asynchronous copies; rows past n are zero.
+    for (int idx = tid; idx < 2 * DC * (D / 4); idx += DELTA_THREADS) {
+        const int which = idx / (DC * (D / 4)), rem = idx % (DC * (D / 4));
+        const int row = rem / (D / 4), c4 = rem % (D / 4), t = t0 + row;
+        const bool ok = t < a.n;
+        const int col = (which == 0 ? a.c_qk : 0) + hk * D + 4 * c4;
+        const float* src = ok ? a.qkv + static_cast<int64_t>(t) * a.c_conv + col : a.qkv;
+        cp_async16((which == 0 ? Ks : Qs) + row * P + 4 * c4, src, ok);
     }
-    for (int i = tid; i < DC * PL; i += DELTA_THREADS) Ts[i] = 0.f;
-    __syncthreads();
-    if (tid < 32) {  // inclusive prefix sum of log a over the chunk (2 per lane)
-        const float x0 = gl[2 * tid], x1 = gl[2 * tid + 1];
+    cp_async_commit();
+    // gates of the value heads h = hk*r + j: log a -> inclusive prefix sum (one warp per head)
+    for (int j = warp; j < r; j += DELTA_THREADS / 32) {
+        const int h = hk * r + j;
+        float* gl = sm + L::GL0 + j * DC;
+        float* bb = sm + L::BB0 + j * DC;
+        float x0 = 0.f, x1 = 0.f;
+        const int ta = t0 + 2 * lane, tb = ta + 1;
+        if (ta < a.n) x0 = a.log_a[static_cast<int64_t>(ta) * a.hv + h];
+        if (tb < a.n) x1 = a.log_a[static_cast<int64_t>(tb) * a.hv + h];
+        bb[2 * lane] = ta < a.n ? a.b[static_cast<int64_t>(ta) * a.hv + h] : 0.f;
+        bb[2 * lane + 1] = tb < a.n ? a.b[static_cast<int64_t>(tb) * a.hv + h] : 0.f;
         float s = x0 + x1;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const float y = __shfl_up_sync(0xffffffffu, s, o);
-            if (tid >= o) s += y;
+            if (lane >= o) s += y;
         }
-        gl[2 * tid] = s - x1;
-        gl[2 * tid + 1] = s;
+        gl[2 * lane] = s - x1;
+        gl[2 * lane + 1] = s;
     }
+    cp_async_wait<0>();
     __syncthreads();
 
     // K K^T and Q K^T on the lower-triangular 16x8 tiles: warp -> m-tile warp/2,
@@ -185,97 +206,113 @@ __global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(DeltaArgs 
     {
         const int mt = warp >> 1, nt0 = 4 * (warp & 1);
         float ck[4][4] = {}, cq[4][4] = {};
-        const float* ka = Ks + (16 * mt + g) * P + tg;
-        const float* qa = Qs + (16 * mt + g) * P + tg;
+        const float* ka = a_frag_addr<P>(Ks, 16 * mt, 0, lane);
+        const float* qa = a_frag_addr<P>(Qs, 16 * mt, 0, lane);
+        const float* kb0 = b2_frag_addr<P>(Ks, 8 * nt0, 0, lane);
+        const float* kb1 = b2_frag_addr<P>(Ks, 8 * nt0 + 16, 0, lane);
+        const bool live01 = 8 * nt0 <= 16 * mt + 15, live23 = 8 * (nt0 + 2) <= 16 * mt + 15;
 #pragma unroll 4
         for (int ks = 0; ks < D / 8; ++ks) {
             const int c = 8 * ks;
-            const uint32_t k0 = lds_u32(ka + c), k1 = lds_u32(ka + 8 * P + c), k2 = lds_u32(ka + c + 4),
-                           k3 = lds_u32(ka + 8 * P + c + 4);
-            const uint32_t q0 = lds_u32(qa + c), q1 = lds_u32(qa + 8 * P + c), q2 = lds_u32(qa + c + 4),
-                           q3 = lds_u32(qa + 8 * P + c + 4);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int nt = nt0 + j;
-                if (8 * nt <= 16 * mt + 15) {
-                    const float* kb = Ks + (8 * nt + g) * P + c + tg;
-                    const uint32_t b0 = lds_u32(kb), b1 = lds_u32(kb + 4);
-                    mma_tf32(ck[j], k0, k1, k2, k3, b0, b1);
-                    mma_tf32(cq[j], q0, q1, q2, q3, b0, b1);
-                }
+            uint32_t k0, k1, k2, k3, q0, q1, q2, q3, b0, b1, b2, b3;
+            ldsm_x4(k0, k1, k2, k3, ka + c);
+            ldsm_x4(q0, q1, q2, q3, qa + c);
+            if (live01) {
+                ldsm_x4(b0, b1, b2, b3, kb0 + c);
+                mma_tf32(ck[0], k0, k1, k2, k3, b0, b1);
+                mma_tf32(cq[0], q0, q1, q2, q3, b0, b1);
+                mma_tf32(ck[1], k0, k1, k2, k3, b2, b3);
+                mma_tf32(cq[1], q0, q1, q2, q3, b2, b3);
+            }
+            if (live23) {
+                ldsm_x4(b0, b1, b2, b3, kb1 + c);
+                mma_tf32(ck[2], k0, k1, k2, k3, b0, b1);
+                mma_tf32(cq[2], q0, q1, q2, q3, b0, b1);
+                mma_tf32(ck[3], k0, k1, k2, k3, b2, b3);
+                mma_tf32(cq[3], q0, q1, q2, q3, b2, b3);
             }
         }
-        float* aout = a.A + (static_cast<int64_t>(chunk) * a.hv + h) * DC * DC;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int nt = nt0 + j;
+        for (int j = 0; j < 4; ++j)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int i = 16 * mt + g + (e >> 1) * 8, jj = 8 * nt + 2 * tg + (e & 1);
-                const bool live = 8 * nt <= 16 * mt + 15;
-                const float dec = (live && jj <= i) ? expf(gl[i] - gl[jj]) : 0.f;
-                Ls[i * PL + jj] = (jj < i) ? bb[i] * dec * ck[j][e] : 0.f;
-                aout[swz64(i, jj)] = tf32f(dec * cq[j][e]);
+                const int i = 16 * mt + g + (e >> 1) * 8, jj = 8 * (nt0 + j) + 2 * tg + (e & 1);
+                KK[i * PL + jj] = ck[j][e];
+                QK[i * PL + jj] = cq[j][e];
             }
-        }
     }
-    __syncthreads();
+    __syncthreads();   // K and Q are no longer needed: L and T reuse their space
 
-    // T = (I + L)^{-1}: diagonal 16x16 blocks by substitution, one column per thread.
-    if (tid < 64) {
-        const int blk = tid >> 4, c = tid & 15, o = 16 * blk;
-        float col[16];
+    for (int j = 0; j < r; ++j) {
+        const int h = hk * r + j;
+        const int64_t cb = static_cast<int64_t>(chunk) * a.hv + h;
+        const float* gl = sm + L::GL0 + j * DC;
+        const float* bb = sm + L::BB0 + j * DC;
+        float* aout = a.A + cb * DC * DC;
+        for (int idx = tid; idx < DC * DC; idx += DELTA_THREADS) {
+            const int i = idx / DC, jj = idx % DC;
+            const float dec = jj <= i ? expf(gl[i] - gl[jj]) : 0.f;
+            Ls[i * PL + jj] = jj < i ? bb[i] * dec * KK[i * PL + jj] : 0.f;
+            Ts[i * PL + jj] = 0.f;
+            aout[swz64(i, jj)] = tf32f(dec * QK[i * PL + jj]);
+        }
+        __syncthreads();
+        // T = (I + L)^{-1}: diagonal 16x16 blocks by substitution, one column per thread.
+        if (tid < 64) {
+            const int blk = tid >> 4, c = tid & 15, o = 16 * blk;
+            float col[16];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            float v;
-            if (r < c) {
-                v = 0.f;
-            } else if (r == c) {
-                v = 1.f;
-            } else {
+            for (int rr = 0; rr < 16; ++rr) {
+                float v;
+                if (rr < c) {
+                    v = 0.f;
+                } else if (rr == c) {
+                    v = 1.f;
+                } else {
+                    float s = 0.f;
+#pragma unroll
+                    for (int k = 0; k < rr; ++k)
+                        if (k >= c) s = fmaf(Ls[(o + rr) * PL + o + k], col[k], s);
+                    v = -s;
+                }
+                col[rr] = v;
+            }
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr) Ts[(o + rr) * PL + o + c] = col[rr];
+        }
+        __syncthreads();
+        // Off-diagonal blocks, block row by block row:
+        //   T_IJ = -T_II * sum_{K=J}^{I-1} L_IK T_KJ   (J < I)
+        for (int I = 1; I < 4; ++I) {
+            for (int e = tid; e < I * 256; e += DELTA_THREADS) {
+                const int J = e >> 8, rr = (e >> 4) & 15, c = e & 15;
+                float z = 0.f;
+                for (int K = J; K < I; ++K)
+#pragma unroll
+                    for (int m = 0; m < 16; ++m)
+                        z = fmaf(Ls[(16 * I + rr) * PL + 16 * K + m], Ts[(16 * K + m) * PL + 16 * J + c], z);
+                Zs[J * 256 + rr * 16 + c] = z;
+            }
+            __syncthreads();
+            for (int e = tid; e < I * 256; e += DELTA_THREADS) {
+                const int J = e >> 8, rr = (e >> 4) & 15, c = e & 15;
                 float s = 0.f;
 #pragma unroll
-                for (int k = 0; k < r; ++k)
-                    if (k >= c) s = fmaf(Ls[(o + r) * PL + o + k], col[k], s);
-                v = -s;
+                for (int m = 0; m < 16; ++m) s = fmaf(Ts[(16 * I + rr) * PL + 16 * I + m], Zs[J * 256 + m * 16 + c], s);
+                Ts[(16 * I + rr) * PL + 16 * J + c] = -s;
             }
-            col[r] = v;
+            __syncthreads();
         }
-#pragma unroll
-        for (int r = 0; r < 16; ++r) Ts[(o + r) * PL + o + c] = col[r];
-    }
-    __syncthreads();
-    // Off-diagonal blocks, block row by block row:
-    //   T_IJ = -T_II * sum_{K=J}^{I-1} L_IK T_KJ   (J < I)
-    for (int I = 1; I < 4; ++I) {
-        for (int e = tid; e < I * 256; e += DELTA_THREADS) {
-            const int J = e >> 8, r = (e >> 4) & 15, c = e & 15;
-            float z = 0.f;
-            for (int K = J; K < I; ++K)
-#pragma unroll
-                for (int m = 0; m < 16; ++m)
-                    z = fmaf(Ls[(16 * I + r) * PL + 16 * K + m], Ts[(16 * K + m) * PL + 16 * J + c], z);
-            Zs[J * 256 + r * 16 + c] = z;
+        float* tout = a.T + cb * DC * DC;
+        for (int idx = tid; idx < DC * DC; idx += DELTA_THREADS) {
+            const int rr = idx / DC, c = idx % DC;
+            tout[swz64(rr, c)] = tf32f(Ts[rr * PL + c]);
         }
-        __syncthreads();
-        for (int e = tid; e < I * 256; e += DELTA_THREADS) {
-            const int J = e >> 8, r = (e >> 4) & 15, c = e & 15;
-            float s = 0.f;
-#pragma unroll
-            for (int m = 0; m < 16; ++m) s = fmaf(Ts[(16 * I + r) * PL + 16 * I + m], Zs[J * 256 + m * 16 + c], s);
-            Ts[(16 * I + r) * PL + 16 * J + c] = -s;
+        if (tid < DC) {
+            const float gv = gl[tid];
+            *reinterpret_cast<float4*>(a.G + (cb * DC + tid) * 4) = make_float4(gv, expf(gv), bb[tid], expf(gl[DC - 1] - gv));
         }
-        __syncthreads();
-    }
-    float* tout = a.T + (static_cast<int64_t>(chunk) * a.hv + h) * DC * DC;
-    for (int idx = tid; idx < DC * DC; idx += DELTA_THREADS) {
-        const int r = idx / DC, c = idx % DC;
-        tout[swz64(r, c)] = tf32f(Ts[r * PL + c]);
-    }
-    if (tid < DC) {
-        const float gv = gl[tid];
-        *reinterpret_cast<float4*>(a.G + ((static_cast<int64_t>(chunk) * a.hv + h) * DC + tid) * 4) =
-            make_float4(gv, expf(gv), bb[tid], expf(gl[DC - 1] - gv));
+        __syncthreads();   // before the next head overwrites L and T
     }
 }
 
@@ -606,8 +643,7 @@ int read_and_clear_delta_error() {
 
 template <int D>
 static cudaError_t launch_delta_d(DeltaArgs& a, cudaStream_t st) {
-    constexpr int P = D + 4;
-    const size_t prep_smem = (2 * DC * P + 2 * DC * (DC + 4) + 3 * 256 + 2 * DC) * sizeof(float);
+    const size_t prep_smem = PrepSmem<D>::FLOATS * sizeof(float);
     const size_t state_smem = StateSmem<D>::BYTES + 1024;
     static bool attr = false;
     if (!attr) {
@@ -615,7 +651,7 @@ static cudaError_t launch_delta_d(DeltaArgs& a, cudaStream_t st) {
         cudaFuncSetAttribute(delta_state_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(state_smem));
         attr = true;
     }
-    delta_prep_kernel<D><<<dim3(a.nchunks, a.hv), DELTA_THREADS, prep_smem, st>>>(a);
+    delta_prep_kernel<D><<<dim3(a.nchunks, a.hv / a.ratio), DELTA_THREADS, prep_smem, st>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     CUtensorMap map;

@@ -61,8 +61,8 @@ extern "C" {
 #define GDN_CHUNK 64 /* tokens per chunk of the chunked delta rule */
 
 /*
- * One GDN layer.  Sizes: Hk = n_qk_heads, Hv = n_v_heads (a multiple of Hk;
- * value head h reads key head h / (Hv/Hk)), dk = dv (64 or 128),
+ * One GDN layer.  Sizes: Hk = n_qk_heads, Hv = n_v_heads (a multiple of Hk,
+ * at most 8 Hk and 64; value head h reads key head h / (Hv/Hk)), dk = dv (64 or 128),
  * C_qk = Hk*dk, C_v = Hv*dv, C_conv = 2*C_qk + C_v,
  * R_in = 2*C_qk + 2*C_v + 2*Hv (rows of the fused input projection, in the
  * order q | k | v | z | beta | alpha).  hidden is a multiple of 256, and so
