@@ -32,10 +32,10 @@
 //                rows split across CTAs with no communication.  The fp32 state
 //                stays in registers as the accumulator fragments of the
 //                update product.  Every operand of chunk c+1 is copied into
-//                shared memory by TMA (issued by one thread, completion on
-//                mbarriers) while chunk c computes: each copy is issued right
-//                after the operand's last use in chunk c (K and Q, used in the
-//                first phase, are double-buffered).  K, Q, V arrive as 2-D
+//                shared memory by TMA (issued by a producer warp, completion
+//                on mbarriers) while chunk c computes: each copy is issued
+//                right after the operand's last use in chunk c (K and Q, used
+//                in the first phase, are double-buffered).  K, Q, V arrive as 2-D
 //                boxes of 64 tokens x 32 floats with the 128-byte swizzle; T
 //                and A are written by delta_prep in that same swizzled image,
 //                so a 1-D bulk copy lands them ready.
@@ -54,7 +54,8 @@ namespace gdn {
 static __device__ int g_delta_error;
 
 constexpr int DC = GDN_CHUNK;  // 64
-constexpr int DELTA_THREADS = 256;
+constexpr int DELTA_THREADS = 256;            // prep; compute warps of the state pass
+constexpr int STATE_THREADS = DELTA_THREADS + 32;  // + one TMA producer warp
 constexpr int NV = 32;         // rows of S per state CTA
 
 struct DeltaArgs {
@@ -335,8 +336,8 @@ struct StateSmem {
     static constexpr int S0 = G0 + 2 * DC * 16;                // Ss[NV][P]
     static constexpr int R0 = S0 + NV * P * 4;                 // Rt[NV][PT]
     static constexpr int E0 = R0 + NV * PT * 4;                // Et[NV][PT]
-    static constexpr int B0 = E0 + NV * PT * 4;                // mbarriers: KQ[2], V, T, A
-    static constexpr int BYTES = B0 + 64;
+    static constexpr int B0 = E0 + NV * PT * 4;                // mbarriers: full KQ[2], V, T, A; freed KQ[2], V, T, A
+    static constexpr int BYTES = B0 + 128;
 };
 
 // One chunk step in three phases, each a set of independent MMA chains:
@@ -344,12 +345,22 @@ struct StateSmem {
 //      R = diag(b) (V - diag(e^gamma) X), stored transposed
 //   B: Delta = T R, stored transposed (plain and scaled by e^{gamma_C - gamma})
 //   C: O = diag(e^gamma) Y + A Delta, and S <- e^{gamma_C} S + Delta~^T K
-// Operand copies for chunk c+1 (one thread, TMA): K and Q (double-buffered) at
-// the start of chunk c, V and the gate table after phase A, T after B, A after
-// C.  Fragments come from shared memory by ldmatrix, except K in the update,
+// Warps 0-7 compute; warp 8 is the TMA producer.  For each operand buffer a
+// "full" mbarrier (TMA bytes) and a "freed" mbarrier (the 256 compute threads
+// arrive after their last read) pace the producer: K and Q of chunk c+1
+// (double-buffered) once chunk c-1 is done, V and the gate table after phase A,
+// T after phase B, A after phase C.  The compute warps synchronise among
+// themselves with a named barrier, so the producer never holds them up.
+// Fragments come from shared memory by ldmatrix, except K in the update,
 // whose [token][d] layout is the transpose of what ldmatrix delivers.
+__device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, %0;" ::"n"(DELTA_THREADS) : "memory"); }
+
+__device__ __forceinline__ void mbar_arrive_cta(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
 template <int D>
-__global__ void __launch_bounds__(DELTA_THREADS, 1)
+__global__ void __launch_bounds__(STATE_THREADS, 1)
 delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
     using L = StateSmem<D>;
     constexpr int P = L::P, PT = L::PT;
@@ -361,53 +372,70 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
     float* Rt = reinterpret_cast<float*>(base + L::R0);
     float* Et = reinterpret_cast<float*>(base + L::E0);
     uint64_t* bars = reinterpret_cast<uint64_t*>(base + L::B0);
-    uint64_t* bKQ = bars;       // [2]
-    uint64_t* bV = bars + 2;
-    uint64_t* bT = bars + 3;
-    uint64_t* bA = bars + 4;
+    uint64_t* fKQ = bars;       // full [2]
+    uint64_t* fV = bars + 2;
+    uint64_t* fT = bars + 3;
+    uint64_t* fA = bars + 4;
+    uint64_t* eKQ = bars + 5;   // freed [2]
+    uint64_t* eV = bars + 7;
+    uint64_t* eT = bars + 8;
+    uint64_t* eA = bars + 9;
     __shared__ int abort_flag;
 
     const int h = blockIdx.x, i0 = blockIdx.y * NV, hk = h / a.ratio;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, tg = lane & 3;
-    const bool issuer = tid == 0;
 
-    if (issuer) {
+    if (tid == 0) {
         for (int i = 0; i < 5; ++i) mbar_init_cta(bars + i, 1);
+        for (int i = 5; i < 10; ++i) mbar_init_cta(bars + i, DELTA_THREADS);
         mbar_init_fence();
         abort_flag = 0;
     }
     __syncthreads();
 
-    auto chunk_base = [&](int c) { return static_cast<int64_t>(c) * a.hv + h; };
-    // ---- one-thread TMA copies of a chunk's operands (rows past n arrive as zeros)
-    auto issue_KQ = [&](int c) {
-        if (c >= a.nchunks) return;
-        uint64_t* bar = bKQ + (c & 1);
-        unsigned char* kd = base + L::K0 + (c & 1) * L::KQ_BYTES;
-        unsigned char* qd = base + L::Q0 + (c & 1) * L::KQ_BYTES;
-        mbar_expect_tx(bar, 2 * L::KQ_BYTES);
-        for (int sl = 0; sl < L::NSLAB; ++sl) {
-            tma_load_2d_tile(kd + sl * L::SLAB, &qkv_map, bar, a.c_qk + hk * D + 32 * sl, c * DC);
-            tma_load_2d_tile(qd + sl * L::SLAB, &qkv_map, bar, hk * D + 32 * sl, c * DC);
+    if (warp == DELTA_THREADS / 32) {
+        // ------------------------------------------------------------ producer
+        if (lane != 0) return;
+        auto chunk_base = [&](int c) { return static_cast<int64_t>(c) * a.hv + h; };
+        bool ok = true;
+        auto wait_freed = [&](uint64_t* bar, uint32_t parity) {
+            if (ok && !mbar_wait_bounded(bar, parity, &g_delta_error, ERR_WAIT_TIMEOUT)) ok = false;
+            return ok;
+        };
+        for (int c = 0; c < a.nchunks && ok; ++c) {
+            // K, Q of chunk c into buffer c&1: freed when chunk c-2 finished
+            if (c >= 2 && !wait_freed(eKQ + (c & 1), ((c - 2) >> 1) & 1)) break;
+            {
+                uint64_t* bar = fKQ + (c & 1);
+                unsigned char* kd = base + L::K0 + (c & 1) * L::KQ_BYTES;
+                unsigned char* qd = base + L::Q0 + (c & 1) * L::KQ_BYTES;
+                mbar_expect_tx(bar, 2 * L::KQ_BYTES);
+                for (int sl = 0; sl < L::NSLAB; ++sl) {
+                    tma_load_2d_tile(kd + sl * L::SLAB, &qkv_map, bar, a.c_qk + hk * D + 32 * sl, c * DC);
+                    tma_load_2d_tile(qd + sl * L::SLAB, &qkv_map, bar, hk * D + 32 * sl, c * DC);
+                }
+            }
+            // V and the gate table of chunk c: V freed after phase A of chunk c-1,
+            // gate buffer c&1 after chunk c-2 (covered by the K/Q wait above)
+            if (c >= 1 && !wait_freed(eV, (c - 1) & 1)) break;
+            mbar_expect_tx(fV, L::SLAB + DC * 16);
+            tma_load_2d_tile(base + L::V0, &qkv_map, fV, 2 * a.c_qk + h * D + i0, c * DC);
+            bulk_load_1d(base + L::G0 + (c & 1) * DC * 16, a.G + chunk_base(c) * DC * 4, DC * 16, fV);
+            // T of chunk c: freed after phase B of chunk c-1
+            if (c >= 1 && !wait_freed(eT, (c - 1) & 1)) break;
+            mbar_expect_tx(fT, 2 * L::SLAB);
+            bulk_load_1d(base + L::T0, a.T + chunk_base(c) * DC * DC, 2 * L::SLAB, fT);
+            // A of chunk c: freed after phase C of chunk c-1
+            if (c >= 1 && !wait_freed(eA, (c - 1) & 1)) break;
+            mbar_expect_tx(fA, 2 * L::SLAB);
+            bulk_load_1d(base + L::A0, a.A + chunk_base(c) * DC * DC, 2 * L::SLAB, fA);
         }
-    };
-    auto issue_VG = [&](int c) {
-        if (c >= a.nchunks) return;
-        mbar_expect_tx(bV, L::SLAB + DC * 16);
-        tma_load_2d_tile(base + L::V0, &qkv_map, bV, 2 * a.c_qk + h * D + i0, c * DC);
-        bulk_load_1d(base + L::G0 + (c & 1) * DC * 16, a.G + chunk_base(c) * DC * 4, DC * 16, bV);
-    };
-    auto issue_T = [&](int c) {
-        if (c >= a.nchunks) return;
-        mbar_expect_tx(bT, 2 * L::SLAB);
-        bulk_load_1d(base + L::T0, a.T + chunk_base(c) * DC * DC, 2 * L::SLAB, bT);
-    };
-    auto issue_A = [&](int c) {
-        if (c >= a.nchunks) return;
-        mbar_expect_tx(bA, 2 * L::SLAB);
-        bulk_load_1d(base + L::A0, a.A + chunk_base(c) * DC * DC, 2 * L::SLAB, bA);
-    };
+        if (!ok) abort_flag = 1;
+        return;
+    }
+
+    // ---------------------------------------------------------------- compute
     auto wait = [&](uint64_t* bar, uint32_t parity) {
         if (!mbar_wait_bounded(bar, parity, &g_delta_error, ERR_WAIT_TIMEOUT)) abort_flag = 1;
     };
@@ -432,12 +460,6 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
     // ldmatrix row of this lane: matrix lane/8, row lane%8
     const int lm = lane >> 3, lr = lane & 7;
 
-    if (issuer) {
-        issue_KQ(0);
-        issue_VG(0);
-        issue_T(0);
-        issue_A(0);
-    }
     for (int chunk = 0; chunk < a.nchunks; ++chunk) {
         const int t0 = chunk * DC;
         const int KO = L::K0 + (chunk & 1) * L::KQ_BYTES;
@@ -450,13 +472,9 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
                 const int i = 16 * smt + g + (e >> 1) * 8, d = 8 * (snt0 + j) + 2 * tg + (e & 1);
                 Ss[i * P + d] = tf32f(S[j][e]);
             }
-        if (issuer) {
-            fence_proxy_async_smem();
-            issue_KQ(chunk + 1);
-        }
-        wait(bKQ + (chunk & 1), (chunk >> 1) & 1);
-        wait(bV, chunk & 1);
-        __syncthreads();
+        wait(fKQ + (chunk & 1), (chunk >> 1) & 1);
+        wait(fV, chunk & 1);
+        compute_sync();
         if (abort_flag) break;     // uniform: read after a barrier
 
         // ---- phase A: X = K S^T, Y = Q S^T; R = diag(b) (V - diag(e^gamma) X)
@@ -492,13 +510,9 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
                     Rt[i * PT + t] = tf32f(Gs[4 * t + 2] * (*tile(L::V0, t, i) - ex * x));
                 }
         }
-        __syncthreads();
-        if (issuer) {
-            fence_proxy_async_smem();
-            issue_VG(chunk + 1);
-        }
-        wait(bT, chunk & 1);
-        __syncthreads();
+        mbar_arrive_cta(eV);       // V of this chunk is consumed
+        wait(fT, chunk & 1);
+        compute_sync();
         if (abort_flag) break;
 
         // ---- phase B: Delta = T R (T unit lower triangular)
@@ -513,7 +527,8 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
                 mma_tf32(dl[0], a0, a1, a2, a3, b0, b1);
                 mma_tf32(dl[1], a0, a1, a2, a3, b2, b3);
             }
-            __syncthreads();       // every warp has read R
+            mbar_arrive_cta(eT);   // T of this chunk is consumed
+            compute_sync();        // every warp has read R
 #pragma unroll
             for (int j = 0; j < 2; ++j)
 #pragma unroll
@@ -523,13 +538,8 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
                     Et[i * PT + t] = tf32f(dl[j][e] * Gs[4 * t + 3]);
                 }
         }
-        __syncthreads();
-        if (issuer) {
-            fence_proxy_async_smem();
-            issue_T(chunk + 1);
-        }
-        wait(bA, chunk & 1);
-        __syncthreads();
+        wait(fA, chunk & 1);
+        compute_sync();
         if (abort_flag) break;
 
         // ---- phase C: O = Y + A Delta;  S <- e^{gamma_C} S + Delta~^T K
@@ -543,6 +553,7 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
                 mma_tf32(y[0], a0, a1, a2, a3, b0, b1);
                 mma_tf32(y[1], a0, a1, a2, a3, b2, b3);
             }
+            mbar_arrive_cta(eA);   // A of this chunk is consumed
             const float dec = Gs[4 * (DC - 1) + 1];
 #pragma unroll
             for (int j = 0; j < DW; ++j)
@@ -569,6 +580,7 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
                     mma_tf32(S[j], a0, a1, a2, a3, *reinterpret_cast<const uint32_t*>(kb + koff[j][0]),
                              *reinterpret_cast<const uint32_t*>(kb + koff[j][1]));
             }
+            mbar_arrive_cta(eKQ + (chunk & 1));   // K, Q and the gate table of this chunk are consumed
 #pragma unroll
             for (int j = 0; j < 2; ++j)
 #pragma unroll
@@ -579,15 +591,12 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
                             make_float2(y[j][2 * hh], y[j][2 * hh + 1]);
                 }
         }
-        __syncthreads();           // every warp has read A, Delta, K(c), Q(c), S
-        if (issuer) {
-            fence_proxy_async_smem();
-            issue_A(chunk + 1);
-        }
+        compute_sync();            // every warp has read Delta and S before they are rewritten
     }
     if (abort_flag) {
-        // A wait ran out: let the copies still in flight land (bounded) and return.
-        if (issuer)
+        // A wait ran out.  Copies the producer issued for this CTA land in their own
+        // time; let them finish (bounded) before the CTA's shared memory is released.
+        if (tid == 0)
             for (int i = 0; i < 5; ++i)
                 for (uint32_t par = 0; par < 2; ++par) mbar_wait_bounded(bars + i, par, nullptr, 0, 20000000ull);
         return;
@@ -656,7 +665,7 @@ static cudaError_t launch_delta_d(DeltaArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     CUtensorMap map;
     if (!make_qkv_map(&map, a.qkv, a.n, a.c_conv)) return cudaErrorInvalidValue;
-    delta_state_kernel<D><<<dim3(a.hv, D / NV), DELTA_THREADS, state_smem, st>>>(map, a);
+    delta_state_kernel<D><<<dim3(a.hv, D / NV), STATE_THREADS, state_smem, st>>>(map, a);
     return cudaGetLastError();
 }
 
