@@ -48,7 +48,50 @@ __device__ __forceinline__ int quant_code(float w, float s) {
     return max(-127, min(127, q));
 }
 
-__device__ __forceinline__ float silu_f(float u) { return u / (1.0f + expf(-u)); }
+// The same code as a float (an integer value, +0 for zero), by the IEEE divide.
+__device__ __forceinline__ float qcode_exact(float w, float s) {
+    if (s == 0.0f) return 0.0f;
+    const float r = rintf(__fdiv_rn(w, s));
+    if (r != r) return 0.0f;
+    return fminf(fmaxf(r, -127.0f), 127.0f) + 0.0f;
+}
+
+// Row scale s = amax/127 with its reciprocal for the fast quantiser.
+struct QScale {
+    float s, rs;
+    bool fast;   // s and 1/s are normal numbers far from overflow
+};
+__device__ __forceinline__ QScale make_qscale(float amax) {
+    QScale q;
+    q.s = __fdiv_rn(amax, 127.0f);
+    q.rs = __frcp_rn(q.s);
+    q.fast = q.s >= 1e-30f && q.s <= 1e30f;
+    return q;
+}
+
+// Fast quantiser: y = w * fl(1/s) is within 2^-22 (relative) of w/s, and |w/s|
+// <= 127.5 in a row whose amax gave s, so y and fl(w/s) lie within 3e-5 of each
+// other; rounding to nearest can tell them apart only when they straddle a
+// half-integer.  When y is within 1e-3 of one (or is not a number), `redo` is
+// set and the caller recomputes with qcode_exact, so the result always equals
+// qcode_exact(w, s).
+__device__ __forceinline__ float qcode_fast(float w, const QScale& q, bool& redo) {
+    const float y = w * q.rs;
+    const float r = rintf(y);
+    redo |= !(fabsf(y - r) <= 0.499f);
+    return fminf(fmaxf(r, -127.0f), 127.0f) + 0.0f;
+}
+
+// Two codes (integer-valued floats) as a pair of fp16 values, low half first.
+__device__ __forceinline__ uint32_t codes_to_f16x2(float c0, float c1) {
+    const __half2 h = __floats2half2_rn(c0, c1);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// SiLU(u) = u / (1 + e^-u) with the hardware exponential and reciprocal
+// (a few ulp; its consumers round to tf32 or to int8 codes).  u << 0 gives
+// e^-u = inf and the quotient -0.
+__device__ __forceinline__ float silu_f(float u) { return __fdividef(u, 1.0f + __expf(-u)); }
 
 // fp32 -> tf32 (10 explicit mantissa bits), round to nearest, ties away; as fp32 bits.
 __device__ __forceinline__ uint32_t tf32_bits(float x) {

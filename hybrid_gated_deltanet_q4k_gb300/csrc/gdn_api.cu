@@ -19,6 +19,8 @@
 namespace gdn {
 cudaError_t launch_q4k_deq_i8(const void*, int64_t, int64_t, int8_t*, float*, cudaStream_t);
 cudaError_t launch_q4k_deq_codes(const void*, int64_t, int64_t, uint16_t*, float*, cudaStream_t);
+cudaError_t launch_q4k_deq_codes2(const void*, int64_t, int64_t, uint16_t*, float*, const void*, int64_t, int64_t,
+                                  uint16_t*, float*, cudaStream_t);
 cudaError_t launch_quant_rows(const uint16_t*, int64_t, int64_t, uint16_t*, float*, cudaStream_t);
 cudaError_t launch_gemm_codes(const uint16_t*, const float*, const uint16_t*, const float*, int64_t, int64_t, int64_t,
                               uint16_t*, int64_t, int64_t, float*, int64_t, cudaStream_t);
@@ -327,8 +329,9 @@ int gdn_prefill(const gdn_layer* layer, const void* x, int64_t n_tokens, const f
     const bool q4k = layer->wtype == GDN_W_Q4K;
     GDN_LAUNCH(mark(0, true, st), "stage event");
     if (q4k) {
-        GDN_LAUNCH(launch_q4k_deq_codes(layer->w_in, s.r_in, s.H, w.wc_in, w.ws_in, st), "dequant W_in");
-        GDN_LAUNCH(launch_q4k_deq_codes(layer->w_out, s.H, s.c_v, w.wc_out, w.ws_out, st), "dequant W_out");
+        GDN_LAUNCH(launch_q4k_deq_codes2(layer->w_in, s.r_in, s.H, w.wc_in, w.ws_in, layer->w_out, s.H, s.c_v,
+                                         w.wc_out, w.ws_out, st),
+                   "dequant W_in, W_out");
     }
     GDN_LAUNCH(mark(1, true, st), "stage event");
     for (int64_t u0 = 0; u0 < n_tokens; u0 += B) {

@@ -26,7 +26,7 @@
 namespace gdn {
 
 constexpr int CONV_WARPS = 8;
-constexpr int CONV_TOKENS = 64;
+constexpr int CONV_TOKENS = 16;
 
 struct ConvArgs {
     const uint16_t* qkvz;
@@ -79,28 +79,41 @@ __device__ __forceinline__ void conv_head_run(const ConvArgs& a, int head, int t
     const bool norm = head < a.n_qk_norm;
     const float mul = head < a.n_q ? a.q_scale : 1.0f;
     const int t1 = min(a.n, t0 + CONV_TOKENS);
-    for (int t = t0; t < t1; ++t) {
-        float x[CPL];
-        const uint16_t* src = a.qkvz + static_cast<int64_t>(t) * a.ld_qkvz + c0;
-        if (CPL == 4) {
-            const uint2 u = *reinterpret_cast<const uint2*>(src);
-            x[0] = __uint_as_float(u.x << 16); x[1] = __uint_as_float(u.x & 0xffff0000u);
-            x[2 % CPL] = __uint_as_float(u.y << 16); x[3 % CPL] = __uint_as_float(u.y & 0xffff0000u);
+    // All CONV_TOKENS rows of the run are loaded (packed bf16 pairs) before the
+    // first is used, so each warp keeps the whole run in flight.
+    uint32_t xr[CONV_TOKENS][CPL / 2];
+#pragma unroll
+    for (int k = 0; k < CONV_TOKENS; ++k) {
+        const int t = t0 + k;
+        if (t < t1) {
+            const uint16_t* src = a.qkvz + static_cast<int64_t>(t) * a.ld_qkvz + c0;
+            if (CPL == 4) {
+                const uint2 u = __ldg(reinterpret_cast<const uint2*>(src));
+                xr[k][0] = u.x; xr[k][1 % (CPL / 2)] = u.y;
+            } else {
+                xr[k][0] = __ldg(reinterpret_cast<const uint32_t*>(src));
+            }
         } else {
-            const uint32_t u = *reinterpret_cast<const uint32_t*>(src);
-            x[0] = __uint_as_float(u << 16); x[1 % CPL] = __uint_as_float(u & 0xffff0000u);
+#pragma unroll
+            for (int i = 0; i < CPL / 2; ++i) xr[k][i] = 0u;
         }
+    }
+#pragma unroll
+    for (int k = 0; k < CONV_TOKENS; ++k) {
+        const int t = t0 + k;
         float y[CPL];
         float ss = 0.0f;
 #pragma unroll
         for (int i = 0; i < CPL; ++i) {
+            const uint32_t xw = xr[k][i >> 1];
+            const float x = __uint_as_float((i & 1) ? (xw & 0xffff0000u) : (xw << 16));
             float u = w[i][0] * h0[i];
             u = fmaf(w[i][1], h1[i], u);
             u = fmaf(w[i][2], h2[i], u);
-            u = fmaf(w[i][3], x[i], u);
+            u = fmaf(w[i][3], x, u);
             y[i] = silu_f(u);
             ss = fmaf(y[i], y[i], ss);
-            h0[i] = h1[i]; h1[i] = h2[i]; h2[i] = x[i];
+            h0[i] = h1[i]; h1[i] = h2[i]; h2[i] = x;
         }
         if (norm) {
             ss = warp_sum(ss);
@@ -108,18 +121,20 @@ __device__ __forceinline__ void conv_head_run(const ConvArgs& a, int head, int t
 #pragma unroll
             for (int i = 0; i < CPL; ++i) y[i] *= r;
         }
-        float* dst = a.out + static_cast<int64_t>(t) * a.c_conv + c0;
+        if (t < t1) {
+            float* dst = a.out + static_cast<int64_t>(t) * a.c_conv + c0;
 #pragma unroll
-        for (int i = 0; i < CPL; ++i) y[i] = round_tf32(y[i]);
-        if (CPL == 4)
-            *reinterpret_cast<float4*>(dst) = make_float4(y[0], y[1 % CPL], y[2 % CPL], y[3 % CPL]);
-        else
-            *reinterpret_cast<float2*>(dst) = make_float2(y[0], y[1 % CPL]);
+            for (int i = 0; i < CPL; ++i) y[i] = round_tf32(y[i]);
+            if (CPL == 4)
+                *reinterpret_cast<float4*>(dst) = make_float4(y[0], y[1 % CPL], y[2 % CPL], y[3 % CPL]);
+            else
+                *reinterpret_cast<float2*>(dst) = make_float2(y[0], y[1 % CPL]);
+        }
     }
 }
 
 template <int CPL>
-__global__ void __launch_bounds__(CONV_WARPS * 32) conv_kernel(ConvArgs a) {
+__global__ void __launch_bounds__(CONV_WARPS * 32, 3) conv_kernel(ConvArgs a) {
     const int t0 = blockIdx.x * CONV_TOKENS;
     if (static_cast<int>(blockIdx.y) < a.conv_blocks_y) {
         const int head = blockIdx.y * CONV_WARPS + (threadIdx.x >> 5);

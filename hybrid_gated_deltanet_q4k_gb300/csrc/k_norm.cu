@@ -29,34 +29,43 @@ gated_norm_kernel(const float* __restrict__ o, const uint16_t* __restrict__ z, i
     float wv[CPL];
 #pragma unroll
     for (int i = 0; i < CPL; ++i) wv[i] = norm_w[lane * CPL + i];
+    // All of the warp's loads first (o as fp32, z as bf16 pairs), then the math:
+    // a warp keeps its whole share of the row in flight.
     float v[NORM_MAX_HEADS_PER_WARP][CPL];
+    uint32_t zb[NORM_MAX_HEADS_PER_WARP][CPL / 2];
+#pragma unroll
+    for (int hh = 0; hh < NORM_MAX_HEADS_PER_WARP; ++hh) {
+        const int h = warp + 8 * hh;
+        if (h < hv) {
+            const int c0 = h * D + lane * CPL;
+            if (CPL == 4) {
+                const float4 f = __ldg(reinterpret_cast<const float4*>(o + t * c_v + c0));
+                v[hh][0] = f.x; v[hh][1 % CPL] = f.y; v[hh][2 % CPL] = f.z; v[hh][3 % CPL] = f.w;
+                const uint2 u = __ldg(reinterpret_cast<const uint2*>(z + t * ld_z + c0));
+                zb[hh][0] = u.x; zb[hh][1 % (CPL / 2)] = u.y;
+            } else {
+                const float2 f = __ldg(reinterpret_cast<const float2*>(o + t * c_v + c0));
+                v[hh][0] = f.x; v[hh][1 % CPL] = f.y;
+                zb[hh][0] = __ldg(reinterpret_cast<const uint32_t*>(z + t * ld_z + c0));
+            }
+        }
+    }
     float amax = 0.0f;
 #pragma unroll
     for (int hh = 0; hh < NORM_MAX_HEADS_PER_WARP; ++hh) {
         const int h = warp + 8 * hh;
         if (h < hv) {
             const int c0 = h * D + lane * CPL;
-            float ov[CPL], zv[CPL];
-            if (CPL == 4) {
-                const float4 f = *reinterpret_cast<const float4*>(o + t * c_v + c0);
-                ov[0] = f.x; ov[1 % CPL] = f.y; ov[2 % CPL] = f.z; ov[3 % CPL] = f.w;
-                const uint2 u = *reinterpret_cast<const uint2*>(z + t * ld_z + c0);
-                zv[0] = __uint_as_float(u.x << 16); zv[1 % CPL] = __uint_as_float(u.x & 0xffff0000u);
-                zv[2 % CPL] = __uint_as_float(u.y << 16); zv[3 % CPL] = __uint_as_float(u.y & 0xffff0000u);
-            } else {
-                const float2 f = *reinterpret_cast<const float2*>(o + t * c_v + c0);
-                ov[0] = f.x; ov[1 % CPL] = f.y;
-                const uint32_t u = *reinterpret_cast<const uint32_t*>(z + t * ld_z + c0);
-                zv[0] = __uint_as_float(u << 16); zv[1 % CPL] = __uint_as_float(u & 0xffff0000u);
-            }
             float ss = 0.0f;
 #pragma unroll
-            for (int i = 0; i < CPL; ++i) ss = fmaf(ov[i], ov[i], ss);
+            for (int i = 0; i < CPL; ++i) ss = fmaf(v[hh][i], v[hh][i], ss);
             ss = warp_sum(ss);
             const float r = rsqrtf(ss / static_cast<float>(D) + eps);
 #pragma unroll
             for (int i = 0; i < CPL; ++i) {
-                v[hh][i] = ov[i] * r * wv[i] * silu_f(zv[i]);
+                const uint32_t zw = zb[hh][i >> 1];
+                const float zv = __uint_as_float((i & 1) ? (zw & 0xffff0000u) : (zw << 16));
+                v[hh][i] = v[hh][i] * r * wv[i] * silu_f(zv);
                 amax = fmaxf(amax, fabsf(v[hh][i]));
             }
             if (!QUANT) {
@@ -67,18 +76,24 @@ gated_norm_kernel(const float* __restrict__ o, const uint16_t* __restrict__ z, i
     }
     if (!QUANT) return;
     amax = block_max(amax, red);
-    const float s = __fdiv_rn(amax, 127.0f);
-    if (threadIdx.x == 0) scale[t] = s;
+    const QScale qsc = make_qscale(amax);
+    if (threadIdx.x == 0) scale[t] = qsc.s;
 #pragma unroll
     for (int hh = 0; hh < NORM_MAX_HEADS_PER_WARP; ++hh) {
         const int h = warp + 8 * hh;
         if (h < hv) {
             const int c0 = h * D + lane * CPL;
+            float c[CPL];
+            bool redo = !qsc.fast;
+#pragma unroll
+            for (int i = 0; i < CPL; ++i) c[i] = qcode_fast(v[hh][i], qsc, redo);
+            if (redo) {
+#pragma unroll
+                for (int i = 0; i < CPL; ++i) c[i] = qcode_exact(v[hh][i], qsc.s);
+            }
             uint32_t w[CPL / 2];
 #pragma unroll
-            for (int i = 0; i < CPL / 2; ++i)
-                w[i] = static_cast<uint32_t>(code_to_f16_bits(quant_code(v[hh][2 * i], s))) |
-                       (static_cast<uint32_t>(code_to_f16_bits(quant_code(v[hh][2 * i + 1], s))) << 16);
+            for (int i = 0; i < CPL / 2; ++i) w[i] = codes_to_f16x2(c[2 * i], c[2 * i + 1]);
             if (CPL == 4)
                 *reinterpret_cast<uint2*>(codes + t * c_v + c0) = make_uint2(w[0], w[1 % (CPL / 2)]);
             else

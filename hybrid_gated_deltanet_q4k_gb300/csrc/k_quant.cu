@@ -3,30 +3,36 @@
 // The int8 projections of the pages (sparkinfer PR #464, Summary) take int8
 // rows with one fp32 scale each; the activation side is quantised the same
 // way as the weights: scale = amax/127, code = clamp(rne(x/scale), -127, 127),
-// IEEE fp32.  One CTA per row; the row (<= 16384 values) stays in registers
-// between the amax reduction and the quantisation, so the kernel reads each
-// input byte once and writes each code once, with 16-byte accesses.
+// IEEE fp32 (the fast quantiser of common.cuh returns exactly those codes).
+// One CTA per row with up to QR_VEC 16-byte vectors per thread, all loads
+// issued before the first use; the row stays in registers between the amax
+// reduction and the quantisation, so the kernel reads each input byte once and
+// writes each code once.  Rows of up to 4096 values take 64-thread CTAs (two
+// warps per row, up to 32 rows resident per SM), longer rows 256 threads.
 #include "common.cuh"
 
 namespace gdn {
 
-constexpr int QR_THREADS = 256;
-constexpr int QR_MAX_VEC = 16384 / 8 / QR_THREADS;  // 16-byte vectors per thread
+constexpr int QR_VEC = 8;   // 16-byte vectors per thread
 
-__global__ void __launch_bounds__(QR_THREADS)
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS)
 quant_rows_bf16_kernel(const uint16_t* __restrict__ x, int cols, uint16_t* __restrict__ codes,
                        float* __restrict__ scale) {
     __shared__ float red[32];
     const int64_t row = blockIdx.x;
     const int nvec = cols >> 3;
     const uint4* src = reinterpret_cast<const uint4*>(x + row * cols);
-    uint4 v[QR_MAX_VEC];
+    uint4 v[QR_VEC];
+#pragma unroll
+    for (int i = 0; i < QR_VEC; ++i) {
+        const int j = threadIdx.x + i * THREADS;
+        if (j < nvec) v[i] = __ldg(src + j);
+    }
     float amax = 0.0f;
 #pragma unroll
-    for (int i = 0; i < QR_MAX_VEC; ++i) {
-        const int j = threadIdx.x + i * QR_THREADS;
-        if (j < nvec) {
-            v[i] = __ldg(src + j);
+    for (int i = 0; i < QR_VEC; ++i) {
+        if (static_cast<int>(threadIdx.x) + i * THREADS < nvec) {
             const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -36,29 +42,40 @@ quant_rows_bf16_kernel(const uint16_t* __restrict__ x, int cols, uint16_t* __res
         }
     }
     amax = block_max(amax, red);
-    const float s = __fdiv_rn(amax, 127.0f);
-    if (threadIdx.x == 0) scale[row] = s;
+    const QScale qsc = make_qscale(amax);
+    if (threadIdx.x == 0) scale[row] = qsc.s;
     uint4* dst = reinterpret_cast<uint4*>(codes + row * cols);
 #pragma unroll
-    for (int i = 0; i < QR_MAX_VEC; ++i) {
-        const int j = threadIdx.x + i * QR_THREADS;
+    for (int i = 0; i < QR_VEC; ++i) {
+        const int j = threadIdx.x + i * THREADS;
         if (j < nvec) {
             const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-            uint32_t o[4];
+            float xv[8], c[8];
+            bool redo = !qsc.fast;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int q0 = quant_code(__uint_as_float(w[e] << 16), s);
-                const int q1 = quant_code(__uint_as_float(w[e] & 0xffff0000u), s);
-                o[e] = static_cast<uint32_t>(code_to_f16_bits(q0)) | (static_cast<uint32_t>(code_to_f16_bits(q1)) << 16);
+                xv[2 * e] = __uint_as_float(w[e] << 16);
+                xv[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
             }
-            dst[j] = make_uint4(o[0], o[1], o[2], o[3]);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) c[e] = qcode_fast(xv[e], qsc, redo);
+            if (redo) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) c[e] = qcode_exact(xv[e], qsc.s);
+            }
+            dst[j] = make_uint4(codes_to_f16x2(c[0], c[1]), codes_to_f16x2(c[2], c[3]), codes_to_f16x2(c[4], c[5]),
+                                codes_to_f16x2(c[6], c[7]));
         }
     }
 }
 
 cudaError_t launch_quant_rows(const uint16_t* x, int64_t rows, int64_t cols, uint16_t* codes, float* scale,
                               cudaStream_t st) {
-    quant_rows_bf16_kernel<<<static_cast<unsigned>(rows), QR_THREADS, 0, st>>>(x, static_cast<int>(cols), codes, scale);
+    static_assert(16384 / 8 <= QR_VEC * 256, "the widest row must fit a 256-thread CTA");
+    if (cols <= QR_VEC * 64 * 8)
+        quant_rows_bf16_kernel<64><<<static_cast<unsigned>(rows), 64, 0, st>>>(x, static_cast<int>(cols), codes, scale);
+    else
+        quant_rows_bf16_kernel<256><<<static_cast<unsigned>(rows), 256, 0, st>>>(x, static_cast<int>(cols), codes, scale);
     return cudaGetLastError();
 }
 

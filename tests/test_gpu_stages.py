@@ -65,10 +65,12 @@ def test_q4k_deq_bit_exact(L, rows, cols):
 
 # ------------------------------------------------------------------ step 1b
 
-@pytest.mark.parametrize("rows,cols", [(1, 8), (300, 1024), (77, 2560), (33, 4096), (3, 16384)])
+@pytest.mark.parametrize("rows,cols", [(1, 8), (300, 1024), (77, 2560), (33, 4096), (3, 16384), (4096, 4096)])
 def test_quant_rows_bit_exact(L, rows, cols):
     rng = np.random.default_rng(cols)
-    x = rng.normal(0, 1, size=(rows, cols)).astype(np.float32)
+    # per-row magnitudes over six decades: many rows, so the codes that fall near a
+    # rounding tie of x / scale (the fast quantiser's exact fallback) are covered
+    x = (rng.normal(0, 1, size=(rows, cols)) * 10.0 ** rng.uniform(-3, 3, size=(rows, 1))).astype(np.float32)
     if rows >= 3:
         x[0] = 0.0
         x[1, :] = 0.0
