@@ -93,12 +93,13 @@ __device__ __forceinline__ uint32_t codes_to_f16x2(float c0, float c1) {
 // e^-u = inf and the quotient -0.
 __device__ __forceinline__ float silu_f(float u) { return __fdividef(u, 1.0f + __expf(-u)); }
 
-// fp32 -> tf32 (10 explicit mantissa bits), round to nearest, ties away; as fp32 bits.
-__device__ __forceinline__ uint32_t tf32_bits(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
-}
+// fp32 -> tf32 (10 explicit mantissa bits), round to nearest with ties away
+// from zero, as fp32 bits: half a tf32 unit (0x1000) is added to the
+// magnitude bits and the 13 low bits cleared; a carry into the exponent rounds
+// up correctly and values past the largest tf32 number become infinity.  For
+// finite inputs this is the rounding of cvt.rna.tf32.f32, in two integer
+// operations.
+__device__ __forceinline__ uint32_t tf32_bits(float x) { return (__float_as_uint(x) + 0x1000u) & 0xffffe000u; }
 __device__ __forceinline__ float round_tf32(float x) { return __uint_as_float(tf32_bits(x)); }
 
 // Block-wide max of a non-negative value; all threads get the result.

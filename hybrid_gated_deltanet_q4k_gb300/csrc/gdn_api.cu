@@ -31,7 +31,7 @@ cudaError_t launch_conv(const gdn_layer&, const uint16_t*, int64_t, int64_t, con
 cudaError_t launch_conv_state(const gdn_layer&, const uint16_t*, int64_t, int64_t, float*, cudaStream_t);
 cudaError_t launch_delta(const gdn_layer&, const float*, const float*, const float*, int64_t, const float*, float*,
                          float*, void*, cudaStream_t);
-size_t delta_scratch_bytes(int hv, int d, int64_t n);
+size_t delta_scratch_bytes(int hv, int hk, int d, int64_t n);
 cudaError_t launch_gated_norm(const gdn_layer&, const float*, const uint16_t*, int64_t, int64_t, uint16_t*, float*,
                               float*, cudaStream_t);
 int read_and_clear_gemm_error();
@@ -155,7 +155,7 @@ Workspace carve(const gdn_layer* L, const Sizes& s, int64_t B, void* base) {
     w.log_a = static_cast<float*>(take(B * s.hv * 4));
     w.b = static_cast<float*>(take(B * s.hv * 4));
     w.o = static_cast<float*>(take(B * s.c_v * 4));
-    w.delta_bytes = delta_scratch_bytes(static_cast<int>(s.hv), static_cast<int>(s.d), B);
+    w.delta_bytes = delta_scratch_bytes(static_cast<int>(s.hv), static_cast<int>(s.hk), static_cast<int>(s.d), B);
     w.delta = take(w.delta_bytes);
     w.total = off;
     return w;
@@ -266,7 +266,7 @@ int gdn_conv_state_update(const gdn_layer* layer, const uint16_t* qkvz, int64_t 
 size_t gdn_delta_rule_scratch_size(const gdn_layer* layer, int64_t n_tokens) {
     Sizes s;
     if (check_layer(layer, &s) || n_tokens < 1) return 0;
-    return delta_scratch_bytes(static_cast<int>(s.hv), static_cast<int>(s.d), n_tokens);
+    return delta_scratch_bytes(static_cast<int>(s.hv), static_cast<int>(s.hk), static_cast<int>(s.d), n_tokens);
 }
 
 int gdn_delta_rule(const gdn_layer* layer, const float* qkv, const float* log_a, const float* b, int64_t n_tokens,
@@ -277,7 +277,7 @@ int gdn_delta_rule(const gdn_layer* layer, const float* qkv, const float* log_a,
     if (n_tokens < 1 || n_tokens > 0x7fffffff) return fail(GDN_EINVAL, "gdn_delta_rule: n_tokens >= 1 required");
     if (!qkv || !log_a || !b || !state_out || !o || !scratch) return fail(GDN_EINVAL, "gdn_delta_rule: NULL pointer");
     if (!aligned(qkv, 16) || !aligned(scratch, 16) || !aligned(o, 8)) return fail(GDN_EINVAL, "gdn_delta_rule: qkv and scratch 16-byte, o 8-byte alignment required");
-    if (scratch_bytes < delta_scratch_bytes(static_cast<int>(s.hv), static_cast<int>(s.d), n_tokens))
+    if (scratch_bytes < delta_scratch_bytes(static_cast<int>(s.hv), static_cast<int>(s.hk), static_cast<int>(s.d), n_tokens))
         return fail(GDN_ENOMEM, "gdn_delta_rule: scratch too small");
     GDN_LAUNCH(launch_delta(*layer, qkv, log_a, b, n_tokens, state_in, state_out, o, scratch, static_cast<cudaStream_t>(stream)),
                "gdn_delta_rule");
@@ -417,9 +417,9 @@ extern "C" int gdn_delta_rule_noalloc(const gdn_layer* layer, const float* qkv, 
     if (n_tokens < 1 || n_tokens > 0x7fffffff) return fail(GDN_EINVAL, "gdn_delta_rule_noalloc: n_tokens >= 1 required");
     if (!qkv || !log_a || !b || !state_out || !o) return fail(GDN_EINVAL, "gdn_delta_rule_noalloc: NULL pointer");
     if (!aligned(qkv, 16) || !aligned(o, 8)) return fail(GDN_EINVAL, "gdn_delta_rule_noalloc: qkv 16-byte, o 8-byte alignment required");
-    const size_t need = delta_scratch_bytes(static_cast<int>(s.hv), static_cast<int>(s.d), n_tokens);
+    const size_t need = delta_scratch_bytes(static_cast<int>(s.hv), static_cast<int>(s.hk), static_cast<int>(s.d), n_tokens);
     if (need > GDN_NOALLOC_SCRATCH_BYTES) {
-        const size_t per_chunk = delta_scratch_bytes(static_cast<int>(s.hv), static_cast<int>(s.d), 1);
+        const size_t per_chunk = delta_scratch_bytes(static_cast<int>(s.hv), static_cast<int>(s.hk), static_cast<int>(s.d), 1);
         return fail(GDN_EINVAL,
                     "gdn_delta_rule_noalloc: %lld tokens need %zu bytes of scratch, more than the static %u bytes "
                     "(at most %lld tokens for this layer)",

@@ -46,6 +46,7 @@
 // the exact recurrence on the test workloads.
 #include "common.cuh"
 #include "tma.cuh"
+#include "tcgen05.cuh"
 
 #include <mutex>
 
@@ -55,7 +56,7 @@ static __device__ int g_delta_error;
 
 constexpr int DC = GDN_CHUNK;  // 64
 constexpr int DELTA_THREADS = 256;            // prep; compute warps of the state pass
-constexpr int STATE_THREADS = DELTA_THREADS + 32;  // + one TMA producer warp
+constexpr int STATE_THREADS = DELTA_THREADS + 64;  // + TMA producer warp + MMA warp
 constexpr int NV = 32;         // rows of S per state CTA
 
 struct DeltaArgs {
@@ -67,6 +68,7 @@ struct DeltaArgs {
     float* T;      // [nchunks][hv][DC][DC]   tf32-rounded
     float* A;      // [nchunks][hv][DC][DC]   tf32-rounded
     float* G;      // [nchunks][hv][DC][4]    gamma, e^gamma, b, e^{gamma_C - gamma}
+    float* KT;     // [nchunks][hk][D][DC]    K^T, in the swizzled operand image
     const float* state_in;  // [hv][D][D] or null
     float* state_out;
     float* o;      // [n][c_v]
@@ -242,6 +244,18 @@ __global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(DeltaArgs 
                 QK[i * PL + jj] = cq[j][e];
             }
     }
+    // K^T of this (chunk, key head) for the state pass's update product, in its
+    // shared-memory operand image: two slabs (tokens 0-31, 32-63) of D rows of
+    // 32 floats with the 128-byte swizzle.  Lanes take consecutive d, so the
+    // column reads of Ks are conflict-free.
+    {
+        float* kt = a.KT + (static_cast<int64_t>(chunk) * gridDim.y + hk) * D * DC;
+        for (int idx = tid; idx < D * (DC / 4); idx += DELTA_THREADS) {
+            const int d = idx % D, t = 4 * (idx / D);
+            const float4 v = make_float4(Ks[t * P + d], Ks[(t + 1) * P + d], Ks[(t + 2) * P + d], Ks[(t + 3) * P + d]);
+            *reinterpret_cast<float4*>(kt + (t >> 5) * (D * 32) + (sw128_f32(d, t & 31) >> 2)) = v;
+        }
+    }
     __syncthreads();   // K and Q are no longer needed: L and T reuse their space
 
     for (int j = 0; j < r; ++j) {
@@ -319,301 +333,344 @@ __global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(DeltaArgs 
 
 // ------------------------------------------------------------------ state pass
 
+// Shared-memory layout of the state pass (byte offsets; every operand base is
+// 1024-byte aligned, as the 128-byte swizzle requires).  Operands are slabs of
+// rows of 32 fp32 (128 bytes) with the 128-byte swizzle, K-major for the
+// tensor cores: the image a 2-D TMA box with SWIZZLE_128B writes, and the one
+// delta_prep writes for T, A and K^T.
 template <int D>
 struct StateSmem {
-    // byte offsets; every TMA destination is 1024-byte aligned
-    static constexpr int SLAB = DC * 128;          // 64 token rows x 32 floats
+    static constexpr int SLAB = DC * 128;          // 64 rows x 32 floats
     static constexpr int NSLAB = D / 32;
-    static constexpr int KQ_BYTES = NSLAB * SLAB;  // one K or Q tile
-    static constexpr int P = D + 4;                // S row pitch (floats)
-    static constexpr int PT = DC + 4;              // R^T, Delta^T row pitch (floats)
-    static constexpr int K0 = 0;                               // Ks[2]
-    static constexpr int Q0 = K0 + 2 * KQ_BYTES;               // Qs[2]
-    static constexpr int T0 = Q0 + 2 * KQ_BYTES;               // Ts (2 slabs)
-    static constexpr int A0 = T0 + 2 * SLAB;                   // As (2 slabs)
-    static constexpr int V0 = A0 + 2 * SLAB;                   // Vs (1 slab: NV = 32 floats)
-    static constexpr int G0 = V0 + SLAB;                       // Gs[2][DC][4]
-    static constexpr int S0 = G0 + 2 * DC * 16;                // Ss[NV][P]
-    static constexpr int R0 = S0 + NV * P * 4;                 // Rt[NV][PT]
-    static constexpr int E0 = R0 + NV * PT * 4;                // Et[NV][PT]
-    static constexpr int B0 = E0 + NV * PT * 4;                // mbarriers: full KQ[2], V, T, A; freed KQ[2], V, T, A
-    static constexpr int BYTES = B0 + 128;
+    static constexpr int QK_SLAB = 2 * SLAB;       // Q rows 0-63, K rows 64-127
+    static constexpr int SOP = NV * 128;           // 32 rows x 32 floats
+    static constexpr int KT_SLAB = D * 128;        // D rows x 32 floats
+    static constexpr int KT_BYTES = 2 * KT_SLAB;   // one K^T [D][DC]
+    static constexpr int QK0 = 0;                  // [Q; K] [2*DC][D]  (TMA)
+    static constexpr int KT0 = QK0 + NSLAB * QK_SLAB;   // K^T [2][D][DC] (bulk copies)
+    static constexpr int T0 = KT0 + 2 * KT_BYTES;  // T [DC][DC]        (bulk copy)
+    static constexpr int A0 = T0 + 2 * SLAB;       // [A; 0] [2*DC][DC] (bulk copies into the upper rows)
+    static constexpr int V0 = A0 + 2 * QK_SLAB;    // V [DC][NV]        (TMA)
+    static constexpr int S0 = V0 + SLAB;           // S [NV][D]         tf32 operand of X, Y
+    static constexpr int R0 = S0 + NSLAB * SOP;    // R^T, then Delta^T [NV][DC]
+    static constexpr int E0 = R0 + 2 * SOP;        // Delta~^T [NV][DC]
+    static constexpr int G0 = E0 + 2 * SOP;        // gate table [2][DC] x (gamma, e^gamma, b, e^{gamma_C-gamma})
+    static constexpr int B0 = G0 + 2 * DC * 16;    // mbarriers
+    static constexpr int NBAR = 20;
+    static constexpr int MISC0 = B0 + NBAR * 8;    // TMEM base address, abort flag
+    static constexpr int BYTES = MISC0 + 16;
+    static_assert(BYTES + 1024 <= 227 * 1024, "state pass shared memory");
 };
 
-// One chunk step in three phases, each a set of independent MMA chains:
-//   A: X = K S^T and Y = Q S^T together (k split in even/odd halves);
-//      R = diag(b) (V - diag(e^gamma) X), stored transposed
-//   B: Delta = T R, stored transposed (plain and scaled by e^{gamma_C - gamma})
-//   C: O = diag(e^gamma) Y + A Delta, and S <- e^{gamma_C} S + Delta~^T K
-// Warps 0-7 compute; warp 8 is the TMA producer.  For each operand buffer a
-// "full" mbarrier (TMA bytes) and a "freed" mbarrier (the 256 compute threads
-// arrive after their last read) pace the producer: K and Q of chunk c+1
-// (double-buffered) once chunk c-1 is done, V and the gate table after phase A,
-// T after phase B, A after phase C.  The compute warps synchronise among
-// themselves with a named barrier, so the producer never holds them up.
-// Fragments come from shared memory by ldmatrix, except K in the update,
-// whose [token][d] layout is the transpose of what ldmatrix delivers.
-__device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, %0;" ::"n"(DELTA_THREADS) : "memory"); }
+// TMEM columns (fp32 accumulators of NV = 32 columns).  [Q; K] S^T is
+// double-buffered: the output reads Y of chunk c while X, Y of chunk c+1 run.
+constexpr uint32_t TM_XY = 0, TM_D = 64, TM_U = 96, TM_Z = 128;
+constexpr uint32_t TM_COLS = 256;
+
+enum StateBar : int {
+    F_QK, F_KT0, F_KT1, F_V, F_T, F_A,   // copies landed (tx bytes)
+    E_QK, E_KT0, E_KT1, E_V, E_T, E_A,   // buffer free again
+    M_XY, M_D, M_U, M_Z,                 // MMA groups complete (tcgen05.commit)
+    R_S, R_R, R_D,                       // operands written by the compute warps
+    M_FIN,                               // every MMA of the CTA complete (shutdown)
+};
+
+// Bounded wait on an mbarrier phase that also gives up when another role of
+// the CTA has aborted.
+__device__ __forceinline__ bool state_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+    if (mbar_test(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_test(bar, parity)) return true;
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 > 2000000000ull) {
+            atomicCAS(&g_delta_error, 0, ERR_WAIT_TIMEOUT);
+            *abort = 1;
+            return false;
+        }
+    }
+}
 
 __device__ __forceinline__ void mbar_arrive_cta(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
+// Issue the k steps [k0, k1) of one MMA chain; a K step is 8 fp32 = 32 bytes,
+// four per 128-byte swizzle row, then the next slab.
+template <int K0, int K1, int A_SLAB, int B_SLAB>
+__device__ __forceinline__ void mma_chain(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc) {
+#pragma unroll
+    for (int k = K0; k < K1; ++k)
+        t5::mma_tf32(d_tmem, adesc + static_cast<uint64_t>((k >> 2) * (A_SLAB >> 4) + 2 * (k & 3)),
+                     bdesc + static_cast<uint64_t>((k >> 2) * (B_SLAB >> 4) + 2 * (k & 3)), idesc, k > K0 ? 1u : 0u);
+}
+
+// One CTA per (value head, NV rows of S); 320 threads:
+//   warps 0-7  compute.  Warp w reads TMEM lanes 32*(w%4) .. +31 and columns
+//              16*(w/4) .. +15 of each 32-column accumulator.
+//   warp 8     producer: TMA boxes of Q, K, V; bulk copies of K^T, T, A, gates.
+//   warp 9     TMEM owner and MMA issuer (one thread).
+// Per chunk, with S the NV x D slice of the state (tf32 operands, fp32 sums):
+//   MMA  [Y; X] = [Q; K] S^T          (M = 128: Y in lanes 0-63, X in 64-127)
+//   warps 2,3,6,7 (lanes 64-127)  R = diag(b)(V - diag(e^gamma) X) -> R^T
+//   MMA  Delta = T R                  (M = 64: row j in lane 32*(j/16) + j%16)
+//   warps, lanes 0-15  Delta^T and Delta~^T = (diag(e^{gamma_C-gamma}) Delta)^T
+//   MMA  U = K^T Delta~               (M = D: row d in lane d, or 32*(d/16)+d%16)
+//   MMA  [Z; 0] = [A; 0] Delta        (M = 128: Z in lanes 0-63, next to Y)
+//   warps  S <- e^{gamma_C} S + U in fp32 registers, its tf32 image -> S
+//   warps 0,1,4,5 (lanes 0-63)  O = diag(e^gamma) Y + Z, while the next chunk's
+//        [Q; K] S^T runs.
+// The state's chain per chunk is four dependent steps (X, R, Delta, U); the
+// output products stay off it.
 template <int D>
 __global__ void __launch_bounds__(STATE_THREADS, 1)
 delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
     using L = StateSmem<D>;
-    constexpr int P = L::P, PT = L::PT;
-    constexpr int NT_D = D / 8;     // n-tiles across d
-    constexpr int DW = NT_D / 4;    // n-tiles of d per warp in the update (4 warps across d)
     extern __shared__ __align__(1024) unsigned char smb[];
     unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smb) + 1023) & ~uintptr_t(1023));
-    float* Ss = reinterpret_cast<float*>(base + L::S0);
-    float* Rt = reinterpret_cast<float*>(base + L::R0);
-    float* Et = reinterpret_cast<float*>(base + L::E0);
     uint64_t* bars = reinterpret_cast<uint64_t*>(base + L::B0);
-    uint64_t* fKQ = bars;       // full [2]
-    uint64_t* fV = bars + 2;
-    uint64_t* fT = bars + 3;
-    uint64_t* fA = bars + 4;
-    uint64_t* eKQ = bars + 5;   // freed [2]
-    uint64_t* eV = bars + 7;
-    uint64_t* eT = bars + 8;
-    uint64_t* eA = bars + 9;
-    __shared__ int abort_flag;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(base + L::MISC0);
+    volatile int* abort = reinterpret_cast<volatile int*>(base + L::MISC0 + 4);
 
     const int h = blockIdx.x, i0 = blockIdx.y * NV, hk = h / a.ratio;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int g = lane >> 2, tg = lane & 3;
+    const uint32_t sbase = smem_addr(base);
 
     if (tid == 0) {
-        for (int i = 0; i < 5; ++i) mbar_init_cta(bars + i, 1);
-        for (int i = 5; i < 10; ++i) mbar_init_cta(bars + i, DELTA_THREADS);
+        for (int i = F_QK; i <= F_A; ++i) mbar_init_cta(bars + i, 1);
+        for (int i = E_QK; i <= E_A; ++i) mbar_init_cta(bars + i, 1);
+        mbar_init_cta(bars + E_V, DELTA_THREADS);
+        for (int i = M_XY; i <= M_Z; ++i) mbar_init_cta(bars + i, 1);
+        mbar_init_cta(bars + R_S, DELTA_THREADS);
+        mbar_init_cta(bars + R_R, DELTA_THREADS / 2);
+        mbar_init_cta(bars + R_D, DELTA_THREADS);
+        mbar_init_cta(bars + M_FIN, 1);
         mbar_init_fence();
-        abort_flag = 0;
+        *abort = 0;
     }
+    // the zero rows 64-127 of the [A; 0] operand
+    for (int idx = tid; idx < 2 * L::SLAB / 16; idx += STATE_THREADS) {
+        const int sl = idx / (L::SLAB / 16), off = idx % (L::SLAB / 16);
+        *reinterpret_cast<uint4*>(base + L::A0 + sl * L::QK_SLAB + L::SLAB + 16 * off) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    fence_proxy_async_smem();
+    if (warp == 9) t5::alloc(tslot, TM_COLS);
+    t5::fence_before();
     __syncthreads();
+    t5::fence_after();
+    const uint32_t tmem = *tslot;
 
-    if (warp == DELTA_THREADS / 32) {
+    if (warp == 8) {
         // ------------------------------------------------------------ producer
-        if (lane != 0) return;
-        auto chunk_base = [&](int c) { return static_cast<int64_t>(c) * a.hv + h; };
+        if (lane == 0) {
+            auto cb = [&](int c) { return static_cast<int64_t>(c) * a.hv + h; };
+            for (int c = 0; c < a.nchunks; ++c) {
+                const uint32_t pp = (c - 1) & 1;   // phase of the previous chunk's release
+                if (c >= 1 && !state_wait(bars + E_QK, pp, abort)) break;
+                mbar_expect_tx(bars + F_QK, 2 * L::NSLAB * L::SLAB);
+                for (int sl = 0; sl < L::NSLAB; ++sl) {
+                    unsigned char* dst = base + L::QK0 + sl * L::QK_SLAB;
+                    tma_load_2d_tile(dst, &qkv_map, bars + F_QK, hk * D + 32 * sl, c * DC);
+                    tma_load_2d_tile(dst + L::SLAB, &qkv_map, bars + F_QK, a.c_qk + hk * D + 32 * sl, c * DC);
+                }
+                const int kb = c & 1;
+                if (c >= 2 && !state_wait(bars + E_KT0 + kb, ((c - 2) >> 1) & 1, abort)) break;
+                mbar_expect_tx(bars + F_KT0 + kb, L::KT_BYTES);
+                bulk_load_1d(base + L::KT0 + kb * L::KT_BYTES,
+                             a.KT + (static_cast<int64_t>(c) * (a.hv / a.ratio) + hk) * D * DC, L::KT_BYTES,
+                             bars + F_KT0 + kb);
+                if (c >= 1 && !state_wait(bars + E_V, pp, abort)) break;
+                mbar_expect_tx(bars + F_V, L::SLAB + DC * 16);
+                tma_load_2d_tile(base + L::V0, &qkv_map, bars + F_V, 2 * a.c_qk + h * D + i0, c * DC);
+                bulk_load_1d(base + L::G0 + (c & 1) * DC * 16, a.G + cb(c) * DC * 4, DC * 16, bars + F_V);
+                if (c >= 1 && !state_wait(bars + E_T, pp, abort)) break;
+                mbar_expect_tx(bars + F_T, 2 * L::SLAB);
+                bulk_load_1d(base + L::T0, a.T + cb(c) * DC * DC, 2 * L::SLAB, bars + F_T);
+                if (c >= 1 && !state_wait(bars + E_A, pp, abort)) break;
+                mbar_expect_tx(bars + F_A, 2 * L::SLAB);
+                for (int sl = 0; sl < 2; ++sl)
+                    bulk_load_1d(base + L::A0 + sl * L::QK_SLAB, a.A + cb(c) * DC * DC + sl * (DC * 32), L::SLAB,
+                                 bars + F_A);
+            }
+        }
+    } else if (warp == 9) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t ID64 = t5::idesc_tf32(64, NV);
+            constexpr uint32_t ID128 = t5::idesc_tf32(128, NV);
+            constexpr uint32_t IDU = t5::idesc_tf32(D, NV);
+            const uint64_t dQK = t5::desc_sw128(sbase + L::QK0), dS = t5::desc_sw128(sbase + L::S0);
+            const uint64_t dT = t5::desc_sw128(sbase + L::T0), dR = t5::desc_sw128(sbase + L::R0);
+            const uint64_t dA = t5::desc_sw128(sbase + L::A0), dE = t5::desc_sw128(sbase + L::E0);
+            const uint64_t dKT = t5::desc_sw128(sbase + L::KT0);
+            for (int c = 0; c < a.nchunks; ++c) {
+                const uint32_t ph = c & 1;
+                if (!state_wait(bars + R_S, ph, abort) || !state_wait(bars + F_QK, ph, abort)) break;
+                t5::fence_after();
+                mma_chain<0, D / 8, L::QK_SLAB, L::SOP>(tmem + TM_XY + 32 * ph, dQK, dS, ID128);
+                t5::commit(bars + M_XY);
+                t5::commit(bars + E_QK);
+                if (!state_wait(bars + R_R, ph, abort) || !state_wait(bars + F_T, ph, abort)) break;
+                t5::fence_after();
+                mma_chain<0, DC / 8, L::SLAB, L::SOP>(tmem + TM_D, dT, dR, ID64);
+                t5::commit(bars + M_D);
+                t5::commit(bars + E_T);
+                if (!state_wait(bars + R_D, ph, abort) || !state_wait(bars + F_KT0 + ph, (c >> 1) & 1, abort)) break;
+                t5::fence_after();
+                mma_chain<0, DC / 8, L::KT_SLAB, L::SOP>(tmem + TM_U, dKT + ph * (L::KT_BYTES >> 4), dE, IDU);
+                t5::commit(bars + M_U);
+                t5::commit(bars + E_KT0 + ph);
+                if (!state_wait(bars + F_A, ph, abort)) break;
+                t5::fence_after();
+                mma_chain<0, DC / 8, L::QK_SLAB, L::SOP>(tmem + TM_Z, dA, dR, ID128);
+                t5::commit(bars + M_Z);
+                t5::commit(bars + E_A);
+            }
+            // every MMA issued above has completed before TMEM is released
+            t5::commit(bars + M_FIN);
+            mbar_wait_bounded(bars + M_FIN, 0, nullptr, 0, 200000000ull);
+        }
+    } else {
+        // ------------------------------------------------------------ compute
+        const int q = warp & 3, hc = warp >> 2;
+        const int v0 = 16 * hc;
+        const bool xw = q >= 2;                 // lanes 64-127: X rows; lanes 0-63: Y rows
+        const int tok = 32 * (q & 1) + lane;    // token of this lane in the M = 128 products
+        const bool act = lane < 16;             // owns token j = 16q + lane of the M = 64 product
+        const int j = 16 * q + lane;
+        const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q) << 16) + v0;   // this warp's lanes, columns v0..
+        // key-dimension row d of U owned by this thread (all lanes for D = 128, lanes 0-15 for D = 64)
+        const bool own_d = D == 128 ? true : act;
+        const int d = D == 128 ? 32 * q + lane : 16 * q + lane;
+        float S[16];
+#pragma unroll
+        for (int v = 0; v < 16; ++v)
+            S[v] = (own_d && a.state_in) ? a.state_in[(static_cast<int64_t>(h) * D + i0 + v0 + v) * D + d] : 0.f;
+        auto write_s = [&]() {
+            if (own_d) {
+                unsigned char* sp = base + L::S0 + (d >> 5) * L::SOP;
+#pragma unroll
+                for (int v = 0; v < 16; ++v)
+                    *reinterpret_cast<float*>(sp + sw128_f32(v0 + v, d & 31)) = tf32f(S[v]);
+            }
+        };
+        // column t of an [NV][DC] operand (R^T, Delta^T, Delta~^T), rows v0 .. v0+15
+        auto write_col = [&](int off, int t, const float (&x)[16]) {
+            unsigned char* cp = base + off + (t >> 5) * L::SOP;
+#pragma unroll
+            for (int v = 0; v < 16; ++v) *reinterpret_cast<float*>(cp + sw128_f32(v0 + v, t & 31)) = x[v];
+        };
+        auto release = [&](int bar) {       // operands written by this thread -> the MMA issuer
+            fence_proxy_async_smem();
+            t5::fence_before();
+            mbar_arrive_cta(bars + bar);
+        };
+        write_s();
+        release(R_S);
+
         bool ok = true;
-        auto wait_freed = [&](uint64_t* bar, uint32_t parity) {
-            if (ok && !mbar_wait_bounded(bar, parity, &g_delta_error, ERR_WAIT_TIMEOUT)) ok = false;
+        auto wait_all = [&](int bar, uint32_t parity) {
+            ok = ok && state_wait(bars + bar, parity, abort);
+            ok = __all_sync(0xffffffffu, ok);
             return ok;
         };
-        for (int c = 0; c < a.nchunks && ok; ++c) {
-            // K, Q of chunk c into buffer c&1: freed when chunk c-2 finished
-            if (c >= 2 && !wait_freed(eKQ + (c & 1), ((c - 2) >> 1) & 1)) break;
-            {
-                uint64_t* bar = fKQ + (c & 1);
-                unsigned char* kd = base + L::K0 + (c & 1) * L::KQ_BYTES;
-                unsigned char* qd = base + L::Q0 + (c & 1) * L::KQ_BYTES;
-                mbar_expect_tx(bar, 2 * L::KQ_BYTES);
-                for (int sl = 0; sl < L::NSLAB; ++sl) {
-                    tma_load_2d_tile(kd + sl * L::SLAB, &qkv_map, bar, a.c_qk + hk * D + 32 * sl, c * DC);
-                    tma_load_2d_tile(qd + sl * L::SLAB, &qkv_map, bar, hk * D + 32 * sl, c * DC);
+        for (int c = 0; c < a.nchunks; ++c) {
+            const uint32_t ph = c & 1;
+            const float4* G = reinterpret_cast<const float4*>(base + L::G0 + ph * DC * 16);
+            if (!wait_all(F_V, ph)) break;
+            const float4 gt = G[tok];            // gates of this lane's token (M = 128 products)
+            const float sc = G[j].w;             // e^{gamma_C - gamma_j}
+            const float dec = G[DC - 1].y;       // e^{gamma_C}
+
+            // ---- R = diag(b) (V - diag(e^gamma) X), stored as R^T (X rows: lanes 64-127)
+            if (xw) {
+                if (!wait_all(M_XY, ph)) break;
+                t5::fence_after();
+                float x[16];
+                t5::ld16(tl + TM_XY + 32 * ph, x);
+                const unsigned char* vp = base + L::V0;
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const float4 vv = *reinterpret_cast<const float4*>(vp + sw128_f32(tok, v0 + 4 * m));
+                    x[4 * m + 0] = tf32f(gt.z * (vv.x - gt.y * x[4 * m + 0]));
+                    x[4 * m + 1] = tf32f(gt.z * (vv.y - gt.y * x[4 * m + 1]));
+                    x[4 * m + 2] = tf32f(gt.z * (vv.z - gt.y * x[4 * m + 2]));
+                    x[4 * m + 3] = tf32f(gt.z * (vv.w - gt.y * x[4 * m + 3]));
+                }
+                write_col(L::R0, tok, x);
+                release(R_R);
+            }
+            mbar_arrive_cta(bars + E_V);         // V and this chunk's gate reads are done
+
+            // ---- Delta = T R -> Delta^T (over R^T) and Delta~^T
+            if (!wait_all(M_D, ph)) break;
+            t5::fence_after();
+            float dl[16];
+            t5::ld16(tl + TM_D, dl);
+            if (act) {
+                float de[16];
+#pragma unroll
+                for (int v = 0; v < 16; ++v) {
+                    de[v] = tf32f(dl[v] * sc);
+                    dl[v] = tf32f(dl[v]);
+                }
+                write_col(L::R0, j, dl);
+                write_col(L::E0, j, de);
+            }
+            release(R_D);
+
+            // ---- S <- e^{gamma_C} S + U
+            if (!wait_all(M_U, ph)) break;
+            t5::fence_after();
+            float u[16];
+            t5::ld16(tl + TM_U, u);
+#pragma unroll
+            for (int v = 0; v < 16; ++v) S[v] = fmaf(dec, S[v], u[v]);
+            write_s();
+            release(R_S);
+
+            // ---- O = diag(e^gamma) Y + Z (Y rows: lanes 0-63)
+            if (!xw) {
+                if (!wait_all(M_Z, ph)) break;
+                t5::fence_after();
+                float y[16], z[16];
+                t5::ld16x2(tl + TM_XY + 32 * ph, y, tl + TM_Z, z);
+                const int t = c * DC + tok;
+                if (t < a.n) {
+                    float4* dst = reinterpret_cast<float4*>(a.o + static_cast<int64_t>(t) * a.c_v + h * D + i0 + v0);
+#pragma unroll
+                    for (int m = 0; m < 4; ++m)
+                        dst[m] = make_float4(fmaf(gt.y, y[4 * m], z[4 * m]), fmaf(gt.y, y[4 * m + 1], z[4 * m + 1]),
+                                             fmaf(gt.y, y[4 * m + 2], z[4 * m + 2]),
+                                             fmaf(gt.y, y[4 * m + 3], z[4 * m + 3]));
                 }
             }
-            // V and the gate table of chunk c: V freed after phase A of chunk c-1,
-            // gate buffer c&1 after chunk c-2 (covered by the K/Q wait above)
-            if (c >= 1 && !wait_freed(eV, (c - 1) & 1)) break;
-            mbar_expect_tx(fV, L::SLAB + DC * 16);
-            tma_load_2d_tile(base + L::V0, &qkv_map, fV, 2 * a.c_qk + h * D + i0, c * DC);
-            bulk_load_1d(base + L::G0 + (c & 1) * DC * 16, a.G + chunk_base(c) * DC * 4, DC * 16, fV);
-            // T of chunk c: freed after phase B of chunk c-1
-            if (c >= 1 && !wait_freed(eT, (c - 1) & 1)) break;
-            mbar_expect_tx(fT, 2 * L::SLAB);
-            bulk_load_1d(base + L::T0, a.T + chunk_base(c) * DC * DC, 2 * L::SLAB, fT);
-            // A of chunk c: freed after phase C of chunk c-1
-            if (c >= 1 && !wait_freed(eA, (c - 1) & 1)) break;
-            mbar_expect_tx(fA, 2 * L::SLAB);
-            bulk_load_1d(base + L::A0, a.A + chunk_base(c) * DC * DC, 2 * L::SLAB, fA);
         }
-        if (!ok) abort_flag = 1;
-        return;
+        if (ok && own_d) {
+#pragma unroll
+            for (int v = 0; v < 16; ++v) a.state_out[(static_cast<int64_t>(h) * D + i0 + v0 + v) * D + d] = S[v];
+        }
     }
 
-    // ---------------------------------------------------------------- compute
-    auto wait = [&](uint64_t* bar, uint32_t parity) {
-        if (!mbar_wait_bounded(bar, parity, &g_delta_error, ERR_WAIT_TIMEOUT)) abort_flag = 1;
-    };
-    // fp32 element (r, c) of a swizzled tile of 32-float slabs, as a float pointer
-    auto tile = [&](int off, int r, int c) {
-        return reinterpret_cast<const float*>(base + off + (c >> 5) * L::SLAB + sw128_f32(r, c & 31));
-    };
-
-    // State fragments: warp owns rows 16*(warp/4) .. +15 of the tile and d columns
-    // 8*DW*(warp%4) .. +8*DW-1, as m16n8 accumulators.
-    const int smt = warp >> 2, snt0 = DW * (warp & 3);
-    float S[DW][4];
-#pragma unroll
-    for (int j = 0; j < DW; ++j)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int i = 16 * smt + g + (e >> 1) * 8, d = 8 * (snt0 + j) + 2 * tg + (e & 1);
-            S[j][e] = a.state_in ? a.state_in[(static_cast<int64_t>(h) * D + i0 + i) * D + d] : 0.f;
-        }
-    // Output-tile ownership for the C x NV products: m-tile warp/2, n-tiles 2*(warp%2), +1.
-    const int omt = warp >> 1, ont0 = 2 * (warp & 1);
-    // ldmatrix row of this lane: matrix lane/8, row lane%8
-    const int lm = lane >> 3, lr = lane & 7;
-
-    for (int chunk = 0; chunk < a.nchunks; ++chunk) {
-        const int t0 = chunk * DC;
-        const int KO = L::K0 + (chunk & 1) * L::KQ_BYTES;
-        const int QO = L::Q0 + (chunk & 1) * L::KQ_BYTES;
-        const float* Gs = reinterpret_cast<const float*>(base + L::G0 + (chunk & 1) * DC * 16);
-#pragma unroll
-        for (int j = 0; j < DW; ++j)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int i = 16 * smt + g + (e >> 1) * 8, d = 8 * (snt0 + j) + 2 * tg + (e & 1);
-                Ss[i * P + d] = tf32f(S[j][e]);
-            }
-        wait(fKQ + (chunk & 1), (chunk >> 1) & 1);
-        wait(fV, chunk & 1);
-        compute_sync();
-        if (abort_flag) break;     // uniform: read after a barrier
-
-        // ---- phase A: X = K S^T, Y = Q S^T; R = diag(b) (V - diag(e^gamma) X)
-        float y[2][4];
-        {
-            float xa[2][2][4] = {}, ya[2][2][4] = {};
-            const int arow = 16 * omt + lr + 8 * (lm & 1);
-            const float* sb = b2_frag_addr<P>(Ss, 8 * ont0, 0, lane);
-#pragma unroll 2
-            for (int ks = 0; ks < D / 8; ks += 2) {
-#pragma unroll
-                for (int p = 0; p < 2; ++p) {
-                    const int c = 8 * (ks + p) + 4 * (lm >> 1);
-                    uint32_t k0, k1, k2, k3, q0, q1, q2, q3, b0, b1, b2, b3;
-                    ldsm_x4(k0, k1, k2, k3, tile(KO, arow, c));
-                    ldsm_x4(q0, q1, q2, q3, tile(QO, arow, c));
-                    ldsm_x4(b0, b1, b2, b3, sb + 8 * (ks + p));
-                    mma_tf32(xa[0][p], k0, k1, k2, k3, b0, b1);
-                    mma_tf32(ya[0][p], q0, q1, q2, q3, b0, b1);
-                    mma_tf32(xa[1][p], k0, k1, k2, k3, b2, b3);
-                    mma_tf32(ya[1][p], q0, q1, q2, q3, b2, b3);
-                }
-            }
-            const float e_lo = Gs[4 * (16 * omt + g) + 1], e_hi = Gs[4 * (16 * omt + g + 8) + 1];
-#pragma unroll
-            for (int j = 0; j < 2; ++j)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int t = 16 * omt + g + (e >> 1) * 8, i = 8 * (ont0 + j) + 2 * tg + (e & 1);
-                    const float ex = (e >> 1) ? e_hi : e_lo;
-                    const float x = xa[j][0][e] + xa[j][1][e];
-                    y[j][e] = ex * (ya[j][0][e] + ya[j][1][e]);
-                    Rt[i * PT + t] = tf32f(Gs[4 * t + 2] * (*tile(L::V0, t, i) - ex * x));
-                }
-        }
-        mbar_arrive_cta(eV);       // V of this chunk is consumed
-        wait(fT, chunk & 1);
-        compute_sync();
-        if (abort_flag) break;
-
-        // ---- phase B: Delta = T R (T unit lower triangular)
-        {
-            float dl[2][4] = {};
-            const int arow = 16 * omt + lr + 8 * (lm & 1);
-            const float* rb = b2_frag_addr<PT>(Rt, 8 * ont0, 0, lane);
-            for (int ks = 0; ks < 2 * omt + 2; ++ks) {
-                uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-                ldsm_x4(a0, a1, a2, a3, tile(L::T0, arow, 8 * ks + 4 * (lm >> 1)));
-                ldsm_x4(b0, b1, b2, b3, rb + 8 * ks);
-                mma_tf32(dl[0], a0, a1, a2, a3, b0, b1);
-                mma_tf32(dl[1], a0, a1, a2, a3, b2, b3);
-            }
-            mbar_arrive_cta(eT);   // T of this chunk is consumed
-            compute_sync();        // every warp has read R
-#pragma unroll
-            for (int j = 0; j < 2; ++j)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int t = 16 * omt + g + (e >> 1) * 8, i = 8 * (ont0 + j) + 2 * tg + (e & 1);
-                    Rt[i * PT + t] = tf32f(dl[j][e]);
-                    Et[i * PT + t] = tf32f(dl[j][e] * Gs[4 * t + 3]);
-                }
-        }
-        wait(fA, chunk & 1);
-        compute_sync();
-        if (abort_flag) break;
-
-        // ---- phase C: O = Y + A Delta;  S <- e^{gamma_C} S + Delta~^T K
-        {
-            const int arow = 16 * omt + lr + 8 * (lm & 1);
-            const float* db = b2_frag_addr<PT>(Rt, 8 * ont0, 0, lane);
-            for (int ks = 0; ks < 2 * omt + 2; ++ks) {
-                uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-                ldsm_x4(a0, a1, a2, a3, tile(L::A0, arow, 8 * ks + 4 * (lm >> 1)));
-                ldsm_x4(b0, b1, b2, b3, db + 8 * ks);
-                mma_tf32(y[0], a0, a1, a2, a3, b0, b1);
-                mma_tf32(y[1], a0, a1, a2, a3, b2, b3);
-            }
-            mbar_arrive_cta(eA);   // A of this chunk is consumed
-            const float dec = Gs[4 * (DC - 1) + 1];
-#pragma unroll
-            for (int j = 0; j < DW; ++j)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) S[j][e] *= dec;
-            const float* ea = a_frag_addr<PT>(Et, 16 * smt, 0, lane);
-            // B fragment (k = token tg / tg+4, n = d) of K(c): byte offsets within the swizzled
-            // tile for ks = 0; token 8ks+r sits 1024*ks bytes further (same swizzle key r).
-            const unsigned char* kbase = base + KO;
-            uint32_t koff[DW][2];
-#pragma unroll
-            for (int j = 0; j < DW; ++j) {
-                const int d = 8 * (snt0 + j) + g;
-                koff[j][0] = (d >> 5) * L::SLAB + sw128_f32(tg, d & 31);
-                koff[j][1] = (d >> 5) * L::SLAB + sw128_f32(tg + 4, d & 31);
-            }
-#pragma unroll 2
-            for (int ks = 0; ks < DC / 8; ++ks) {
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4(a0, a1, a2, a3, ea + 8 * ks);
-                const unsigned char* kb = kbase + 1024 * ks;
-#pragma unroll
-                for (int j = 0; j < DW; ++j)
-                    mma_tf32(S[j], a0, a1, a2, a3, *reinterpret_cast<const uint32_t*>(kb + koff[j][0]),
-                             *reinterpret_cast<const uint32_t*>(kb + koff[j][1]));
-            }
-            mbar_arrive_cta(eKQ + (chunk & 1));   // K, Q and the gate table of this chunk are consumed
-#pragma unroll
-            for (int j = 0; j < 2; ++j)
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int t = 16 * omt + g + 8 * hh, i = 8 * (ont0 + j) + 2 * tg;
-                    if (t0 + t < a.n)
-                        *reinterpret_cast<float2*>(a.o + static_cast<int64_t>(t0 + t) * a.c_v + h * D + i0 + i) =
-                            make_float2(y[j][2 * hh], y[j][2 * hh + 1]);
-                }
-        }
-        compute_sync();            // every warp has read Delta and S before they are rewritten
+    if (*abort && tid == 0) {
+        // A wait ran out.  Copies already issued land in their own time; let them
+        // finish (bounded) before the CTA's shared memory is released.
+        for (int i = F_QK; i <= F_A; ++i)
+            for (uint32_t par = 0; par < 2; ++par) mbar_wait_bounded(bars + i, par, nullptr, 0, 20000000ull);
     }
-    if (abort_flag) {
-        // A wait ran out.  Copies the producer issued for this CTA land in their own
-        // time; let them finish (bounded) before the CTA's shared memory is released.
-        if (tid == 0)
-            for (int i = 0; i < 5; ++i)
-                for (uint32_t par = 0; par < 2; ++par) mbar_wait_bounded(bars + i, par, nullptr, 0, 20000000ull);
-        return;
+    t5::fence_before();
+    __syncthreads();
+    if (warp == 9) {
+        t5::fence_after();
+        t5::dealloc(tmem, TM_COLS);
     }
-#pragma unroll
-    for (int j = 0; j < DW; ++j)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int i = 16 * smt + g + (e >> 1) * 8, d = 8 * (snt0 + j) + 2 * tg + (e & 1);
-            a.state_out[(static_cast<int64_t>(h) * D + i0 + i) * D + d] = S[j][e];
-        }
 }
 
-size_t delta_scratch_bytes(int hv, int d, int64_t n) {
-    (void)d;
+size_t delta_scratch_bytes(int hv, int hk, int d, int64_t n) {
     const int64_t nch = (n + DC - 1) / DC;
-    const int64_t per = static_cast<int64_t>(hv) * DC * (2 * DC + 4);
+    const int64_t per = static_cast<int64_t>(hv) * DC * (2 * DC + 4) + static_cast<int64_t>(hk) * d * DC;
     return static_cast<size_t>(nch * per) * sizeof(float);
 }
 
@@ -688,6 +745,7 @@ cudaError_t launch_delta(const gdn_layer& L, const float* qkv, const float* log_
     a.T = base;
     a.A = a.T + nch * a.hv * DC * DC;
     a.G = a.A + nch * a.hv * DC * DC;
+    a.KT = a.G + nch * a.hv * DC * 4;
     a.state_in = state_in;
     a.state_out = state_out;
     a.o = o;

@@ -19,7 +19,7 @@ GDN_OK, GDN_EINVAL, GDN_ENOMEM, GDN_ECUDA, GDN_ETIMEOUT = 0, -1, -2, -3, -4
 GDN_W_Q4K, GDN_W_F32 = 0, 1
 GDN_CHUNK = 64
 GDN_N_STAGE_EVENTS = 8
-GDN_NOALLOC_SCRATCH_BYTES = 32 << 20
+GDN_NOALLOC_SCRATCH_BYTES = 48 << 20
 STAGE_NAMES = ["dequant", "act_quant", "in_proj", "conv", "delta_rule", "gated_norm", "out_proj"]
 
 

@@ -260,12 +260,12 @@ size_t gdn_delta_rule_scratch_size(const gdn_layer *layer, int64_t n_tokens);
  * device synchronisation of cudaMalloc/cudaFree.  The pages have no
  * counterpart to this entry point; it exists only for such callers.
  *   - No scratch argument: the scratch lives in one file-scope device array of
- *     GDN_NOALLOC_SCRATCH_BYTES (32 MiB), which every GPU that loads this
+ *     GDN_NOALLOC_SCRATCH_BYTES (48 MiB), which every GPU that loads this
  *     library holds until the process exits.  The call itself allocates
  *     nothing (no cudaMalloc, no cudaFree, no allocating library routine).
  *   - A call whose gdn_delta_rule_scratch_size(layer, n_tokens) exceeds that
  *     size returns GDN_EINVAL with a message (e.g. at most 1984 tokens, 31
- *     chunks of 64, for 32 value heads).
+ *     chunks of 64, for 32 value heads over 16 key heads of d = 128).
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture.
@@ -275,7 +275,7 @@ size_t gdn_delta_rule_scratch_size(const gdn_layer *layer, int64_t n_tokens);
  *     host threads) race on it: serialise them.
  * Arguments, layouts and results are those of gdn_delta_rule.
  */
-#define GDN_NOALLOC_SCRATCH_BYTES (32u << 20)
+#define GDN_NOALLOC_SCRATCH_BYTES (48u << 20)
 int gdn_delta_rule_noalloc(const gdn_layer *layer, const float *qkv, const float *log_a, const float *b,
                            int64_t n_tokens, const float *state_in, float *state_out, float *o,
                            void *stream);

@@ -67,7 +67,7 @@ def test_noalloc_rejects_more_tokens_than_its_scratch():
     L = gl.load(build=True)
     spec = synth.SPECS["h4096"]
     s, _keep = _layer_struct(spec)
-    n = 1985                                       # 32 chunks of 64 > the 31 that fit in 32 MiB
+    n = 1985                                       # 32 chunks of 64 > the 31 that fit in 48 MiB
     assert L.gdn_delta_rule_scratch_size(ctypes.byref(s), n) > gl.GDN_NOALLOC_SCRATCH_BYTES
     buf = torch.zeros(16, dtype=torch.float32, device=DEV)
     r = L.gdn_delta_rule_noalloc(ctypes.byref(s), gl.ptr(buf), gl.ptr(buf), gl.ptr(buf), n, 0, gl.ptr(buf),
