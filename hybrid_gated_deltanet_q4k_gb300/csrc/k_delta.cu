@@ -356,7 +356,7 @@ struct StateSmem {
     static constexpr int E0 = R0 + 2 * SOP;        // Delta~^T [NV][DC]
     static constexpr int G0 = E0 + 2 * SOP;        // gate table [2][DC] x (gamma, e^gamma, b, e^{gamma_C-gamma})
     static constexpr int B0 = G0 + 2 * DC * 16;    // mbarriers
-    static constexpr int NBAR = 20;
+    static constexpr int NBAR = 17;
     static constexpr int MISC0 = B0 + NBAR * 8;    // TMEM base address, abort flag
     static constexpr int BYTES = MISC0 + 16;
     static_assert(BYTES + 1024 <= 227 * 1024, "state pass shared memory");
@@ -371,7 +371,6 @@ enum StateBar : int {
     F_QK, F_KT0, F_KT1, F_V, F_T, F_A,   // copies landed (tx bytes)
     E_QK, E_KT0, E_KT1, E_V, E_T, E_A,   // buffer free again
     M_XY, M_D, M_U, M_Z,                 // MMA groups complete (tcgen05.commit)
-    R_S, R_R, R_D,                       // operands written by the compute warps
     M_FIN,                               // every MMA of the CTA complete (shutdown)
 };
 
@@ -393,37 +392,49 @@ __device__ __forceinline__ bool state_wait(uint64_t* bar, uint32_t parity, volat
     }
 }
 
+// Named barriers between the compute warps (which write operands) and the
+// MMA warp (which then issues the products).  Both sides wait (bar.sync), so
+// no thread can reach a barrier a second time before it has completed.
+enum StateNamedBar : int { NB_S = 1, NB_R = 2, NB_D = 3 };
+__device__ __forceinline__ void nb_sync(int id) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(DELTA_THREADS + 32) : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_cta(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
-// Issue the k steps [k0, k1) of one MMA chain; a K step is 8 fp32 = 32 bytes,
+// Issue the k steps [0, NK) of one MMA chain; a K step is 8 fp32 = 32 bytes,
 // four per 128-byte swizzle row, then the next slab.
-template <int K0, int K1, int A_SLAB, int B_SLAB>
+template <int NK, int A_SLAB, int B_SLAB>
 __device__ __forceinline__ void mma_chain(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc) {
 #pragma unroll
-    for (int k = K0; k < K1; ++k)
+    for (int k = 0; k < NK; ++k)
         t5::mma_tf32(d_tmem, adesc + static_cast<uint64_t>((k >> 2) * (A_SLAB >> 4) + 2 * (k & 3)),
-                     bdesc + static_cast<uint64_t>((k >> 2) * (B_SLAB >> 4) + 2 * (k & 3)), idesc, k > K0 ? 1u : 0u);
+                     bdesc + static_cast<uint64_t>((k >> 2) * (B_SLAB >> 4) + 2 * (k & 3)), idesc, k > 0 ? 1u : 0u);
 }
 
 // One CTA per (value head, NV rows of S); 320 threads:
 //   warps 0-7  compute.  Warp w reads TMEM lanes 32*(w%4) .. +31 and columns
 //              16*(w/4) .. +15 of each 32-column accumulator.
 //   warp 8     producer: TMA boxes of Q, K, V; bulk copies of K^T, T, A, gates.
-//   warp 9     TMEM owner and MMA issuer (one thread).
+//   warp 9     TMEM owner and MMA issuer: meets the compute warps at a named
+//              barrier once they have written an operand, then issues (one
+//              thread).
 // Per chunk, with S the NV x D slice of the state (tf32 operands, fp32 sums):
 //   MMA  [Y; X] = [Q; K] S^T          (M = 128: Y in lanes 0-63, X in 64-127)
 //   warps 2,3,6,7 (lanes 64-127)  R = diag(b)(V - diag(e^gamma) X) -> R^T
 //   MMA  Delta = T R                  (M = 64: row j in lane 32*(j/16) + j%16)
-//   warps, lanes 0-15  Delta^T and Delta~^T = (diag(e^{gamma_C-gamma}) Delta)^T
+//   lanes 0-15  Delta^T and Delta~^T = (diag(e^{gamma_C-gamma}) Delta)^T
 //   MMA  U = K^T Delta~               (M = D: row d in lane d, or 32*(d/16)+d%16)
 //   MMA  [Z; 0] = [A; 0] Delta        (M = 128: Z in lanes 0-63, next to Y)
 //   warps  S <- e^{gamma_C} S + U in fp32 registers, its tf32 image -> S
-//   warps 0,1,4,5 (lanes 0-63)  O = diag(e^gamma) Y + Z, while the next chunk's
-//        [Q; K] S^T runs.
+//   MMA  next chunk's [Q; K] S^T
+//   warps 0,1,4,5 (lanes 0-63)  O = diag(e^gamma) Y + Z, while it runs.
 // The state's chain per chunk is four dependent steps (X, R, Delta, U); the
-// output products stay off it.
+// output products stay off it.  Every thread meets every named barrier of
+// every chunk, also after a wait ran out (it then skips the work, and the MMA
+// warp issues nothing more), so no barrier is ever left waiting.
 template <int D>
 __global__ void __launch_bounds__(STATE_THREADS, 1)
 delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
@@ -442,11 +453,7 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
         for (int i = F_QK; i <= F_A; ++i) mbar_init_cta(bars + i, 1);
         for (int i = E_QK; i <= E_A; ++i) mbar_init_cta(bars + i, 1);
         mbar_init_cta(bars + E_V, DELTA_THREADS);
-        for (int i = M_XY; i <= M_Z; ++i) mbar_init_cta(bars + i, 1);
-        mbar_init_cta(bars + R_S, DELTA_THREADS);
-        mbar_init_cta(bars + R_R, DELTA_THREADS / 2);
-        mbar_init_cta(bars + R_D, DELTA_THREADS);
-        mbar_init_cta(bars + M_FIN, 1);
+        for (int i = M_XY; i <= M_FIN; ++i) mbar_init_cta(bars + i, 1);
         mbar_init_fence();
         *abort = 0;
     }
@@ -497,41 +504,55 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
         }
     } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t ID64 = t5::idesc_tf32(64, NV);
-            constexpr uint32_t ID128 = t5::idesc_tf32(128, NV);
-            constexpr uint32_t IDU = t5::idesc_tf32(D, NV);
-            const uint64_t dQK = t5::desc_sw128(sbase + L::QK0), dS = t5::desc_sw128(sbase + L::S0);
-            const uint64_t dT = t5::desc_sw128(sbase + L::T0), dR = t5::desc_sw128(sbase + L::R0);
-            const uint64_t dA = t5::desc_sw128(sbase + L::A0), dE = t5::desc_sw128(sbase + L::E0);
-            const uint64_t dKT = t5::desc_sw128(sbase + L::KT0);
-            for (int c = 0; c < a.nchunks; ++c) {
-                const uint32_t ph = c & 1;
-                if (!state_wait(bars + R_S, ph, abort) || !state_wait(bars + F_QK, ph, abort)) break;
-                t5::fence_after();
-                mma_chain<0, D / 8, L::QK_SLAB, L::SOP>(tmem + TM_XY + 32 * ph, dQK, dS, ID128);
+        constexpr uint32_t ID64 = t5::idesc_tf32(64, NV);
+        constexpr uint32_t ID128 = t5::idesc_tf32(128, NV);
+        constexpr uint32_t IDU = t5::idesc_tf32(D, NV);
+        const uint64_t dQK = t5::desc_sw128(sbase + L::QK0), dS = t5::desc_sw128(sbase + L::S0);
+        const uint64_t dT = t5::desc_sw128(sbase + L::T0), dR = t5::desc_sw128(sbase + L::R0);
+        const uint64_t dA = t5::desc_sw128(sbase + L::A0), dE = t5::desc_sw128(sbase + L::E0);
+        const uint64_t dKT = t5::desc_sw128(sbase + L::KT0);
+        const bool leader = lane == 0;
+        // leader only: the copy has landed and nothing has failed
+        auto ready = [&](int bar, uint32_t parity) {
+            if (*abort || !state_wait(bars + bar, parity, abort)) return false;
+            t5::fence_after();
+            return true;
+        };
+        for (int c = 0; c < a.nchunks; ++c) {
+            const uint32_t ph = c & 1;
+            nb_sync(NB_S);                      // S of chunk c written
+            if (leader && ready(F_QK, ph)) {
+                mma_chain<D / 8, L::QK_SLAB, L::SOP>(tmem + TM_XY + 32 * ph, dQK, dS, ID128);
                 t5::commit(bars + M_XY);
                 t5::commit(bars + E_QK);
-                if (!state_wait(bars + R_R, ph, abort) || !state_wait(bars + F_T, ph, abort)) break;
-                t5::fence_after();
-                mma_chain<0, DC / 8, L::SLAB, L::SOP>(tmem + TM_D, dT, dR, ID64);
+            }
+            __syncwarp();
+            nb_sync(NB_R);                      // R^T written
+            if (leader && ready(F_T, ph)) {
+                mma_chain<DC / 8, L::SLAB, L::SOP>(tmem + TM_D, dT, dR, ID64);
                 t5::commit(bars + M_D);
                 t5::commit(bars + E_T);
-                if (!state_wait(bars + R_D, ph, abort) || !state_wait(bars + F_KT0 + ph, (c >> 1) & 1, abort)) break;
-                t5::fence_after();
-                mma_chain<0, DC / 8, L::KT_SLAB, L::SOP>(tmem + TM_U, dKT + ph * (L::KT_BYTES >> 4), dE, IDU);
+            }
+            __syncwarp();
+            nb_sync(NB_D);                      // Delta^T, Delta~^T written
+            if (leader && ready(F_KT0 + ph, (c >> 1) & 1)) {
+                mma_chain<DC / 8, L::KT_SLAB, L::SOP>(tmem + TM_U, dKT + ph * (L::KT_BYTES >> 4), dE, IDU);
                 t5::commit(bars + M_U);
                 t5::commit(bars + E_KT0 + ph);
-                if (!state_wait(bars + F_A, ph, abort)) break;
-                t5::fence_after();
-                mma_chain<0, DC / 8, L::QK_SLAB, L::SOP>(tmem + TM_Z, dA, dR, ID128);
-                t5::commit(bars + M_Z);
-                t5::commit(bars + E_A);
+                if (ready(F_A, ph)) {
+                    mma_chain<DC / 8, L::QK_SLAB, L::SOP>(tmem + TM_Z, dA, dR, ID128);
+                    t5::commit(bars + M_Z);
+                    t5::commit(bars + E_A);
+                }
             }
+            __syncwarp();
+        }
+        if (leader) {
             // every MMA issued above has completed before TMEM is released
             t5::commit(bars + M_FIN);
             mbar_wait_bounded(bars + M_FIN, 0, nullptr, 0, 200000000ull);
         }
+        __syncwarp();
     } else {
         // ------------------------------------------------------------ compute
         const int q = warp & 3, hc = warp >> 2;
@@ -544,6 +565,7 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
         // key-dimension row d of U owned by this thread (all lanes for D = 128, lanes 0-15 for D = 64)
         const bool own_d = D == 128 ? true : act;
         const int d = D == 128 ? 32 * q + lane : 16 * q + lane;
+
         float S[16];
 #pragma unroll
         for (int v = 0; v < 16; ++v)
@@ -562,32 +584,35 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
 #pragma unroll
             for (int v = 0; v < 16; ++v) *reinterpret_cast<float*>(cp + sw128_f32(v0 + v, t & 31)) = x[v];
         };
-        auto release = [&](int bar) {       // operands written by this thread -> the MMA issuer
+        // the operands this thread wrote go to the tensor cores
+        auto handover = [&](int id) {
             fence_proxy_async_smem();
             t5::fence_before();
-            mbar_arrive_cta(bars + bar);
+            nb_sync(id);
         };
-        write_s();
-        release(R_S);
-
-        bool ok = true;
-        auto wait_all = [&](int bar, uint32_t parity) {
-            ok = ok && state_wait(bars + bar, parity, abort);
+        // an MMA group has completed (warp-uniform; false once anything failed)
+        auto mma_done = [&](int bar, uint32_t parity) {
+            bool ok = !*abort && state_wait(bars + bar, parity, abort);
             ok = __all_sync(0xffffffffu, ok);
+            if (ok) t5::fence_after();
             return ok;
         };
+
+        write_s();
+        handover(NB_S);
         for (int c = 0; c < a.nchunks; ++c) {
             const uint32_t ph = c & 1;
             const float4* G = reinterpret_cast<const float4*>(base + L::G0 + ph * DC * 16);
-            if (!wait_all(F_V, ph)) break;
-            const float4 gt = G[tok];            // gates of this lane's token (M = 128 products)
-            const float sc = G[j].w;             // e^{gamma_C - gamma_j}
-            const float dec = G[DC - 1].y;       // e^{gamma_C}
+            float4 gt = make_float4(0.f, 0.f, 0.f, 0.f);
+            float sc = 0.f, dec = 0.f;
+            if (!*abort && state_wait(bars + F_V, ph, abort)) {
+                gt = G[tok];            // gates of this lane's token (M = 128 products)
+                sc = G[j].w;            // e^{gamma_C - gamma_j}
+                dec = G[DC - 1].y;      // e^{gamma_C}
+            }
 
             // ---- R = diag(b) (V - diag(e^gamma) X), stored as R^T (X rows: lanes 64-127)
-            if (xw) {
-                if (!wait_all(M_XY, ph)) break;
-                t5::fence_after();
+            if (xw && mma_done(M_XY, ph)) {
                 float x[16];
                 t5::ld16(tl + TM_XY + 32 * ph, x);
                 const unsigned char* vp = base + L::V0;
@@ -600,41 +625,39 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
                     x[4 * m + 3] = tf32f(gt.z * (vv.w - gt.y * x[4 * m + 3]));
                 }
                 write_col(L::R0, tok, x);
-                release(R_R);
             }
             mbar_arrive_cta(bars + E_V);         // V and this chunk's gate reads are done
+            handover(NB_R);
 
             // ---- Delta = T R -> Delta^T (over R^T) and Delta~^T
-            if (!wait_all(M_D, ph)) break;
-            t5::fence_after();
-            float dl[16];
-            t5::ld16(tl + TM_D, dl);
-            if (act) {
-                float de[16];
+            if (mma_done(M_D, ph)) {
+                float dl[16];
+                t5::ld16(tl + TM_D, dl);
+                if (act) {
+                    float de[16];
 #pragma unroll
-                for (int v = 0; v < 16; ++v) {
-                    de[v] = tf32f(dl[v] * sc);
-                    dl[v] = tf32f(dl[v]);
+                    for (int v = 0; v < 16; ++v) {
+                        de[v] = tf32f(dl[v] * sc);
+                        dl[v] = tf32f(dl[v]);
+                    }
+                    write_col(L::R0, j, dl);
+                    write_col(L::E0, j, de);
                 }
-                write_col(L::R0, j, dl);
-                write_col(L::E0, j, de);
             }
-            release(R_D);
+            handover(NB_D);
 
             // ---- S <- e^{gamma_C} S + U
-            if (!wait_all(M_U, ph)) break;
-            t5::fence_after();
-            float u[16];
-            t5::ld16(tl + TM_U, u);
+            if (mma_done(M_U, ph)) {
+                float u[16];
+                t5::ld16(tl + TM_U, u);
 #pragma unroll
-            for (int v = 0; v < 16; ++v) S[v] = fmaf(dec, S[v], u[v]);
-            write_s();
-            release(R_S);
+                for (int v = 0; v < 16; ++v) S[v] = fmaf(dec, S[v], u[v]);
+                write_s();
+            }
+            if (c + 1 < a.nchunks) handover(NB_S);
 
-            // ---- O = diag(e^gamma) Y + Z (Y rows: lanes 0-63)
-            if (!xw) {
-                if (!wait_all(M_Z, ph)) break;
-                t5::fence_after();
+            // ---- O = diag(e^gamma) Y + Z (Y rows: lanes 0-63), while the next X, Y run
+            if (!xw && mma_done(M_Z, ph)) {
                 float y[16], z[16];
                 t5::ld16x2(tl + TM_XY + 32 * ph, y, tl + TM_Z, z);
                 const int t = c * DC + tok;
@@ -648,7 +671,7 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
                 }
             }
         }
-        if (ok && own_d) {
+        if (!*abort && own_d) {
 #pragma unroll
             for (int v = 0; v < 16; ++v) a.state_out[(static_cast<int64_t>(h) * D + i0 + v0 + v) * D + d] = S[v];
         }
