@@ -202,6 +202,22 @@ __device__ __forceinline__ void store_group8(const GemmArgs& g, int row, int n, 
     }
 }
 
+// Tile order: groups of GROUP_N column tiles, and within a group the 148-odd
+// tiles in flight at a time span ~GROUP_N columns x ~10 row blocks.  The
+// group's B columns (GROUP_N * 256 rows of K codes, 32 MB at K = 4096) stay in
+// L2 while A streams through once per group; in plain row-major order every
+// row block sweeps all of B, which for a large B (the input projection's is
+// ~100 MB) falls out of L2 and is re-read from DRAM.
+constexpr int GROUP_N = 16;
+__device__ __forceinline__ void tile_origin(int tile, int num_m, int num_n, int& m0, int& n0) {
+    const int group = tile / (GROUP_N * num_m);
+    const int first = group * GROUP_N;
+    const int width = min(GROUP_N, num_n - first);
+    const int r = tile - group * GROUP_N * num_m;
+    m0 = (r / width) * tc::BM;
+    n0 = (first + r % width) * tc::BN;
+}
+
 __global__ void __launch_bounds__(tc::THREADS, 1)
 gemm_codes_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmArgs g) {
     using namespace tc;
@@ -253,7 +269,8 @@ gemm_codes_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             uint32_t armed_parity = 0;       // bit s: parity of its last fill
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                const int m0 = (tile / num_n) * BM, n0 = (tile % num_n) * BN;
+                int m0, n0;
+                tile_origin(tile, num_m, num_n, m0, n0);
                 for (int kb = 0; kb < nkb; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
                     uint8_t* sA = smem + stage * STAGE_BYTES;
@@ -317,7 +334,8 @@ gemm_codes_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         uint32_t acc_ctr = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-            const int m0 = (tile / num_n) * BM, n0 = (tile % num_n) * BN;
+            int m0, n0;
+            tile_origin(tile, num_m, num_n, m0, n0);
             int32_t acc[128];
 #pragma unroll
             for (int i = 0; i < 128; ++i) acc[i] = 0;
