@@ -18,32 +18,28 @@
 // All exponents are <= 0.  Tokens past N are padded with log a = 0, b = 0,
 // which leaves S unchanged.
 //
-// Two kernels:
-//   delta_prep   one CTA per (chunk, key head), all chunks in parallel: K K^T
-//                and Q K^T once on tensor cores, then per value head gamma,
-//                the masked A, and T by
-//                blocked inversion of the unit lower-triangular I + L (16x16
-//                diagonal blocks by substitution, off-diagonal blocks by
-//                block products).  Writes T and A (tf32-rounded) and a gate
-//                table (gamma, e^gamma, b, e^{gamma_C - gamma}) per token:
-//                33 KB per (chunk, head).
+// Two kernels, both on the fifth-generation tensor cores (tcgen05.mma
+// kind::tf32, accumulators in TMEM, operands staged by TMA):
+//   delta_prep   one CTA per (chunk, key head), all chunks in parallel: the
+//                Gram products Q K^T and K K^T once (the value heads of a key
+//                head share them), K^T for the state pass, then per value
+//                head gamma, the masked A, and T = (I + L)^{-1} by recursive
+//                doubling on the block-triangular structure.  Writes T, A and
+//                K^T (tf32, in the state pass's shared-memory operand image)
+//                and a gate table (gamma, e^gamma, b, e^{gamma_C - gamma}).
 //   delta_state  one CTA per (head, 32 rows of S): the chunks in order.  Rows
 //                of S evolve independently (row i only reads v[i]), so the
 //                rows split across CTAs with no communication.  The fp32 state
-//                stays in registers as the accumulator fragments of the
-//                update product.  Every operand of chunk c+1 is copied into
-//                shared memory by TMA (issued by a producer warp, completion
-//                on mbarriers) while chunk c computes: each copy is issued
-//                right after the operand's last use in chunk c (K and Q, used
-//                in the first phase, are double-buffered).  K, Q, V arrive as 2-D
-//                boxes of 64 tokens x 32 floats with the 128-byte swizzle; T
-//                and A are written by delta_prep in that same swizzled image,
-//                so a 1-D bulk copy lands them ready.
-// Products use mma.sync m16n8k8 with tf32 operands rounded to nearest (the
-// conv writes q, k, v already rounded; T, A, S, R, Delta are rounded where
-// they are produced) and fp32 accumulation; everything else is fp32.
-// Rounding every operand to tf32 keeps o and S within ~5e-4 (relative L2) of
-// the exact recurrence on the test workloads.
+//                stays in registers; its tf32 image is the B operand of the
+//                next chunk's products.  A producer warp copies every operand
+//                of chunk c+1 into shared memory (TMA boxes of 64 tokens x 32
+//                floats with the 128-byte swizzle for Q, K, V; bulk copies of
+//                the prep images) as soon as chunk c has released its buffer.
+// Products take tf32 operands rounded to nearest (the conv writes q, k, v
+// already rounded; T, A, S, R, Delta are rounded where they are produced) and
+// accumulate in fp32; everything else is fp32.  Rounding every operand to
+// tf32 keeps o and S within ~5e-4 (relative L2) of the exact recurrence on
+// the test workloads.
 #include "common.cuh"
 #include "tma.cuh"
 #include "tcgen05.cuh"
@@ -74,118 +70,105 @@ struct DeltaArgs {
     float* o;      // [n][c_v]
 };
 
-__device__ __forceinline__ uint32_t to_tf32(float x) { return tf32_bits(x); }
 __device__ __forceinline__ float tf32f(float x) { return round_tf32(x); }
-
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool valid) {
-    const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(s), "l"(gmem), "r"(valid ? 16 : 0) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
-// D += A(16x8, row) * B(8x8, col); fragments as in the PTX m16n8k8 .tf32 layout:
-// a0 (g, t) a1 (g+8, t) a2 (g, t+4) a3 (g+8, t+4); b0 (k=t, n=g) b1 (k=t+4, n=g);
-// c0 (g, 2t) c1 (g, 2t+1) c2 (g+8, 2t) c3 (g+8, 2t+1), g = lane/4, t = lane%4.
-__device__ __forceinline__ void mma_tf32(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint32_t lds_u32(const float* p) { return __float_as_uint(*p); }
-
-// ldmatrix on fp32 data: an 8x4 block of fp32 is an 8x8 block of b16 pairs, and
-// the b16 fragment of thread l (row l/4, elements 2(l%4), 2(l%4)+1) is exactly
-// fp32 element (l/4, l%4) -- the tf32 m16n8k8 fragment position.  Lane l passes
-// the address of row l%8 of matrix l/8.
-__device__ __forceinline__ void ldsm_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3, const float* p) {
-    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(a));
-}
-// A fragment (16x8 tile at row0, col0 of a row-major [m][k] array with pitch P).
-template <int P>
-__device__ __forceinline__ const float* a_frag_addr(const float* base, int row0, int col0, int lane) {
-    const int mat = lane >> 3, r = lane & 7;
-    return base + (row0 + r + 8 * (mat & 1)) * P + col0 + 4 * (mat >> 1);
-}
-// Two B fragments (n-tiles n0 and n0+8, k-block col0) of an [n][k] array with pitch P.
-template <int P>
-__device__ __forceinline__ const float* b2_frag_addr(const float* base, int n0, int col0, int lane) {
-    const int mat = lane >> 3, r = lane & 7;
-    return base + (n0 + r + 8 * (mat >> 1)) * P + col0 + 4 * (mat & 1);
-}
-
-// Float index of element (r, c) of a [DC][DC] matrix stored as the shared-memory
-// image the state pass reads: two slabs of DC rows x 32 floats (c / 32), each
-// with 128-byte rows and the 128-byte swizzle.
-__device__ __forceinline__ int swz64(int r, int c) {
-    return (c >> 5) * (DC * 32) + static_cast<int>(sw128_f32(r, c & 31) >> 2);
-}
 
 // ------------------------------------------------------------------ prep
 
 constexpr int PREP_MAX_RATIO = 8;  // value heads per key head handled by one CTA
+constexpr int PL = DC + 4;         // row pitch (floats) of L, T and the block temporaries
 
 template <int D>
 struct PrepSmem {
-    static constexpr int P = D + 4;    // K, Q row pitch (floats)
-    static constexpr int PL = DC + 4;  // KK, QK, L, T row pitch (floats)
-    static constexpr int K0 = 0;                      // Ks[DC][P]   (later: Ls, Ts)
-    static constexpr int Q0 = K0 + DC * P;            // Qs[DC][P]
-    static constexpr int L0 = K0;                     // Ls[DC][PL]  aliases Ks after the products
-    static constexpr int T0 = L0 + DC * PL;           // Ts[DC][PL]
-    static constexpr int KK0 = Q0 + DC * P;           // KK[DC][PL]  k_i . k_j (lower triangle)
-    static constexpr int QK0 = KK0 + DC * PL;         // QK[DC][PL]  q_i . k_j (lower triangle)
-    static constexpr int Z0 = QK0 + DC * PL;          // Zs[3][256]
-    static constexpr int GL0 = Z0 + 3 * 256;          // gamma[PREP_MAX_RATIO][DC]
-    static constexpr int BB0 = GL0 + PREP_MAX_RATIO * DC;  // b[PREP_MAX_RATIO][DC]
-    static constexpr int FLOATS = BB0 + PREP_MAX_RATIO * DC;
-    static_assert(2 * DC * PL <= 2 * DC * P, "L and T must fit in the K and Q region");
+    static constexpr int SLAB = DC * 128;          // 64 rows x 32 floats, 128-byte swizzle
+    static constexpr int NSLAB = D / 32;
+    static constexpr int QK0 = 0;                  // [Q; K] [2*DC][D]: NSLAB slabs of Q rows then K rows (TMA)
+    static constexpr int L0 = QK0 + NSLAB * 2 * SLAB;    // L  [DC][PL]
+    static constexpr int T0 = L0 + DC * PL * 4;          // T  [DC][PL]
+    static constexpr int W0 = T0 + DC * PL * 4;          // block temporaries [DC/2][PL]
+    static constexpr int GL0 = W0 + DC / 2 * PL * 4;     // gamma [PREP_MAX_RATIO][DC]
+    static constexpr int BB0 = GL0 + PREP_MAX_RATIO * DC * 4;  // b [PREP_MAX_RATIO][DC]
+    static constexpr int B0 = BB0 + PREP_MAX_RATIO * DC * 4;   // mbarriers: TMA, MMA
+    static constexpr int MISC0 = B0 + 16;                      // TMEM base address
+    static constexpr int BYTES = MISC0 + 16;
 };
 
-// One CTA per (chunk, key head): K K^T and Q K^T once (the value heads of a key
-// head share them), then for each of its value heads the gated L, T = (I+L)^-1,
-// the masked A and the gate table.
+// C = s * A B for blocks of the fp32 matrices in shared memory (row pitch PL):
+// A is R x KK at a, B is KK x Cc at b, C at c; one 2 x 2 output tile per
+// thread, threads `first` .. first + (R/2)(Cc/2) - 1 of the block take part.
+template <int R, int KK, int Cc>
+__device__ __forceinline__ void block_mm(const float* a, const float* b, float* c, float s, int t) {
+    constexpr int TC = Cc / 2;
+    if (t < 0 || t >= (R / 2) * TC) return;
+    const int r0 = 2 * (t / TC), c0 = 2 * (t % TC);
+    float c00 = 0.f, c01 = 0.f, c10 = 0.f, c11 = 0.f;
+#pragma unroll 8
+    for (int k = 0; k < KK; ++k) {
+        const float a0 = a[r0 * PL + k], a1 = a[(r0 + 1) * PL + k];
+        const float2 bv = *reinterpret_cast<const float2*>(b + k * PL + c0);
+        c00 = fmaf(a0, bv.x, c00);
+        c01 = fmaf(a0, bv.y, c01);
+        c10 = fmaf(a1, bv.x, c10);
+        c11 = fmaf(a1, bv.y, c11);
+    }
+    *reinterpret_cast<float2*>(c + r0 * PL + c0) = make_float2(s * c00, s * c01);
+    *reinterpret_cast<float2*>(c + (r0 + 1) * PL + c0) = make_float2(s * c10, s * c11);
+}
+
+// One CTA per (chunk, key head), 256 threads:
+//   - TMA loads the chunk's Q and K rows of the key head as one stacked
+//     [Q; K] operand; one tcgen05 product [Q; K] K^T (M = 128, N = 64) leaves
+//     q_i.k_j in TMEM lanes 0-63 and k_i.k_j in lanes 64-127 (all value heads
+//     of the key head share them).  Warp w then holds row 32(w%4) + lane,
+//     columns 32(w/4) .. +31, in registers.
+//   - K^T, in the state pass's operand image, straight from the K rows.
+//   - For each value head (gates differ): the gate prefix sums gamma; the
+//     masked A (rows of lanes 0-63) to global memory; L (rows of lanes 64-127)
+//     into shared memory; T = (I + L)^-1 by recursive doubling on the block
+//     triangular structure:
+//         16 x 16 diagonal blocks by substitution (one column per lane),
+//         inv [[A, 0], [C, B]] = [[A^-1, 0], [-B^-1 C A^-1, B^-1]]
+//     for 32 x 32 and then 64 x 64, every block product in fp32 on the CUDA
+//     cores; T (tf32-rounded) and the gate table to global memory.
 template <int D>
-__global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(DeltaArgs a) {
+__global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(const __grid_constant__ CUtensorMap qkv_map,
+                                                                      DeltaArgs a) {
     using L = PrepSmem<D>;
-    constexpr int P = L::P, PL = L::PL;
-    extern __shared__ __align__(16) float sm[];
-    float* Ks = sm + L::K0;
-    float* Qs = sm + L::Q0;
-    float* Ls = sm + L::L0;
-    float* Ts = sm + L::T0;
-    float* KK = sm + L::KK0;
-    float* QK = sm + L::QK0;
-    float* Zs = sm + L::Z0;
+    extern __shared__ __align__(1024) unsigned char smb[];
+    unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smb) + 1023) & ~uintptr_t(1023));
+    float* Ls = reinterpret_cast<float*>(base + L::L0);
+    float* Ts = reinterpret_cast<float*>(base + L::T0);
+    float* Ws = reinterpret_cast<float*>(base + L::W0);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(base + L::B0);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(base + L::MISC0);
 
     const int chunk = blockIdx.x, hk = blockIdx.y;
     const int t0 = chunk * DC;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int g = lane >> 2, tg = lane & 3;
     const int r = a.ratio;
 
-    // K and Q rows (tf32 values from the conv) by asynchronous copies; rows past n are zero.
-    for (int idx = tid; idx < 2 * DC * (D / 4); idx += DELTA_THREADS) {
-        const int which = idx / (DC * (D / 4)), rem = idx % (DC * (D / 4));
-        const int row = rem / (D / 4), c4 = rem % (D / 4), t = t0 + row;
-        const bool ok = t < a.n;
-        const int col = (which == 0 ? a.c_qk : 0) + hk * D + 4 * c4;
-        const float* src = ok ? a.qkv + static_cast<int64_t>(t) * a.c_conv + col : a.qkv;
-        cp_async16((which == 0 ? Ks : Qs) + row * P + 4 * c4, src, ok);
+    if (tid == 0) {
+        mbar_init_cta(bars + 0, 1);
+        mbar_init_cta(bars + 1, 1);
+        mbar_init_fence();
+        mbar_expect_tx(bars + 0, 2 * L::NSLAB * L::SLAB);
+        for (int sl = 0; sl < L::NSLAB; ++sl) {
+            unsigned char* dst = base + L::QK0 + sl * 2 * L::SLAB;
+            tma_load_2d_tile(dst, &qkv_map, bars + 0, hk * D + 32 * sl, t0);
+            tma_load_2d_tile(dst + L::SLAB, &qkv_map, bars + 0, a.c_qk + hk * D + 32 * sl, t0);
+        }
     }
-    cp_async_commit();
+    if (warp == 0) t5::alloc(tslot, 64);
+    // T's blocks (rows 0-15, cols 16-31) and (rows 32-47, cols 48-63) stay zero: the
+    // 32 x 32 diagonal blocks of T are read whole by the last doubling step
+    for (int idx = tid; idx < 2 * 16 * 16; idx += DELTA_THREADS) {
+        const int o = 32 * (idx >> 8), rr = (idx >> 4) & 15, cc = idx & 15;
+        Ts[(o + rr) * PL + o + 16 + cc] = 0.f;
+    }
     // gates of the value heads h = hk*r + j: log a -> inclusive prefix sum (one warp per head)
     for (int j = warp; j < r; j += DELTA_THREADS / 32) {
         const int h = hk * r + j;
-        float* gl = sm + L::GL0 + j * DC;
-        float* bb = sm + L::BB0 + j * DC;
+        float* gl = reinterpret_cast<float*>(base + L::GL0) + j * DC;
+        float* bb = reinterpret_cast<float*>(base + L::BB0) + j * DC;
         float x0 = 0.f, x1 = 0.f;
         const int ta = t0 + 2 * lane, tb = ta + 1;
         if (ta < a.n) x0 = a.log_a[static_cast<int64_t>(ta) * a.hv + h];
@@ -201,127 +184,147 @@ __global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(DeltaArgs 
         gl[2 * lane] = s - x1;
         gl[2 * lane + 1] = s;
     }
-    cp_async_wait<0>();
+    t5::fence_before();
     __syncthreads();
+    t5::fence_after();
+    const uint32_t tmem = *tslot;
 
-    // K K^T and Q K^T on the lower-triangular 16x8 tiles: warp -> m-tile warp/2,
-    // n-tiles 4*(warp%2) .. +3 (skipping tiles wholly above the diagonal).
-    {
-        const int mt = warp >> 1, nt0 = 4 * (warp & 1);
-        float ck[4][4] = {}, cq[4][4] = {};
-        const float* ka = a_frag_addr<P>(Ks, 16 * mt, 0, lane);
-        const float* qa = a_frag_addr<P>(Qs, 16 * mt, 0, lane);
-        const float* kb0 = b2_frag_addr<P>(Ks, 8 * nt0, 0, lane);
-        const float* kb1 = b2_frag_addr<P>(Ks, 8 * nt0 + 16, 0, lane);
-        const bool live01 = 8 * nt0 <= 16 * mt + 15, live23 = 8 * (nt0 + 2) <= 16 * mt + 15;
-#pragma unroll 4
-        for (int ks = 0; ks < D / 8; ++ks) {
-            const int c = 8 * ks;
-            uint32_t k0, k1, k2, k3, q0, q1, q2, q3, b0, b1, b2, b3;
-            ldsm_x4(k0, k1, k2, k3, ka + c);
-            ldsm_x4(q0, q1, q2, q3, qa + c);
-            if (live01) {
-                ldsm_x4(b0, b1, b2, b3, kb0 + c);
-                mma_tf32(ck[0], k0, k1, k2, k3, b0, b1);
-                mma_tf32(cq[0], q0, q1, q2, q3, b0, b1);
-                mma_tf32(ck[1], k0, k1, k2, k3, b2, b3);
-                mma_tf32(cq[1], q0, q1, q2, q3, b2, b3);
+    bool ok = true;
+    if (tid == 0) {
+        ok = mbar_wait_bounded(bars + 0, 0, &g_delta_error, ERR_WAIT_TIMEOUT);
+        if (ok) {
+            t5::fence_after();
+            const uint32_t sb = smem_addr(base);
+            const uint64_t dA = t5::desc_sw128(sb + L::QK0), dB = t5::desc_sw128(sb + L::QK0 + L::SLAB);
+            constexpr uint32_t ID = t5::idesc_tf32(128, DC);
+#pragma unroll
+            for (int k = 0; k < D / 8; ++k) {
+                const uint64_t off = static_cast<uint64_t>((k >> 2) * (2 * L::SLAB >> 4) + 2 * (k & 3));
+                t5::mma_tf32(tmem, dA + off, dB + off, ID, k > 0 ? 1u : 0u);
             }
-            if (live23) {
-                ldsm_x4(b0, b1, b2, b3, kb1 + c);
-                mma_tf32(ck[2], k0, k1, k2, k3, b0, b1);
-                mma_tf32(cq[2], q0, q1, q2, q3, b0, b1);
-                mma_tf32(ck[3], k0, k1, k2, k3, b2, b3);
-                mma_tf32(cq[3], q0, q1, q2, q3, b2, b3);
-            }
+            t5::commit(bars + 1);
         }
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int i = 16 * mt + g + (e >> 1) * 8, jj = 8 * (nt0 + j) + 2 * tg + (e & 1);
-                KK[i * PL + jj] = ck[j][e];
-                QK[i * PL + jj] = cq[j][e];
-            }
     }
-    // K^T of this (chunk, key head) for the state pass's update product, in its
-    // shared-memory operand image: two slabs (tokens 0-31, 32-63) of D rows of
-    // 32 floats with the 128-byte swizzle.  Lanes take consecutive d, so the
-    // column reads of Ks are conflict-free.
+    ok = __syncthreads_and(ok);
+    if (!ok) {
+        // the copy never landed: nothing was issued; give the copy (bounded) time to land
+        if (tid == 0) mbar_wait_bounded(bars + 0, 0, nullptr, 0, 20000000ull);
+        t5::fence_before();
+        __syncthreads();
+        if (warp == 0) t5::dealloc(tmem, 64);
+        return;
+    }
+
+    // ---- K^T image for the state pass: warp task (d-slab s, tokens 4g .. 4g+3), lane = d % 32
     {
         float* kt = a.KT + (static_cast<int64_t>(chunk) * gridDim.y + hk) * D * DC;
-        for (int idx = tid; idx < D * (DC / 4); idx += DELTA_THREADS) {
-            const int d = idx % D, t = 4 * (idx / D);
-            const float4 v = make_float4(Ks[t * P + d], Ks[(t + 1) * P + d], Ks[(t + 2) * P + d], Ks[(t + 3) * P + d]);
-            *reinterpret_cast<float4*>(kt + (t >> 5) * (D * 32) + (sw128_f32(d, t & 31) >> 2)) = v;
+        for (int task = warp; task < L::NSLAB * (DC / 4); task += DELTA_THREADS / 32) {
+            const int s = task / (DC / 4), g = task % (DC / 4), t = 4 * g;
+            const unsigned char* kp = base + L::QK0 + s * 2 * L::SLAB + L::SLAB;
+            const float4 v = make_float4(*reinterpret_cast<const float*>(kp + sw128_f32(t, lane)),
+                                         *reinterpret_cast<const float*>(kp + sw128_f32(t + 1, lane)),
+                                         *reinterpret_cast<const float*>(kp + sw128_f32(t + 2, lane)),
+                                         *reinterpret_cast<const float*>(kp + sw128_f32(t + 3, lane)));
+            *reinterpret_cast<float4*>(kt + (t >> 5) * (D * 32) + (sw128_f32(32 * s + lane, t & 31) >> 2)) = v;
         }
     }
-    __syncthreads();   // K and Q are no longer needed: L and T reuse their space
+
+    // ---- the Gram rows of this thread
+    const int q = warp & 3, half = warp >> 2;
+    const bool qrow = q < 2;                 // lanes 0-63: q_i.k_j; lanes 64-127: k_i.k_j
+    const int row = 32 * (q & 1) + lane;     // token i of this row
+    const int c0 = 32 * half;                // first column (token j)
+    float g[32];
+    if (!mbar_wait_bounded(bars + 1, 0, &g_delta_error, ERR_WAIT_TIMEOUT)) ok = false;
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+        t5::fence_after();
+        t5::ld32(tmem + (static_cast<uint32_t>(32 * q) << 16) + c0, g);
+    }
+    ok = __syncthreads_and(ok);
+    if (!ok) {
+        if (tid == 0) mbar_wait_bounded(bars + 1, 0, nullptr, 0, 200000000ull);
+        t5::fence_before();
+        __syncthreads();
+        if (warp == 0) t5::dealloc(tmem, 64);
+        return;
+    }
 
     for (int j = 0; j < r; ++j) {
         const int h = hk * r + j;
         const int64_t cb = static_cast<int64_t>(chunk) * a.hv + h;
-        const float* gl = sm + L::GL0 + j * DC;
-        const float* bb = sm + L::BB0 + j * DC;
-        float* aout = a.A + cb * DC * DC;
-        for (int idx = tid; idx < DC * DC; idx += DELTA_THREADS) {
-            const int i = idx / DC, jj = idx % DC;
-            const float dec = jj <= i ? expf(gl[i] - gl[jj]) : 0.f;
-            Ls[i * PL + jj] = jj < i ? bb[i] * dec * KK[i * PL + jj] : 0.f;
-            Ts[i * PL + jj] = 0.f;
-            aout[swz64(i, jj)] = tf32f(dec * QK[i * PL + jj]);
+        const float* gl = reinterpret_cast<const float*>(base + L::GL0) + j * DC;
+        const float* bb = reinterpret_cast<const float*>(base + L::BB0) + j * DC;
+        const float gi = gl[row];
+        if (qrow) {
+            // A_ij = e^{gamma_i - gamma_j} q_i.k_j (j <= i): one 128-byte row of the swizzled image
+            float* arow = a.A + cb * DC * DC + half * (DC * 32) + row * 32;
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                float v[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int c = c0 + 4 * m + e;
+                    v[e] = c <= row ? tf32f(__expf(gi - gl[c]) * g[4 * m + e]) : 0.f;
+                }
+                *reinterpret_cast<float4*>(arow + (((m ^ (row & 7)) & 7) << 2)) = make_float4(v[0], v[1], v[2], v[3]);
+            }
+        } else {
+            // L_ij = b_i e^{gamma_i - gamma_j} k_i.k_j (j < i)
+            const float bi = bb[row];
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                float v[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int c = c0 + 4 * m + e;
+                    v[e] = c < row ? bi * __expf(gi - gl[c]) * g[4 * m + e] : 0.f;
+                }
+                *reinterpret_cast<float4*>(Ls + row * PL + c0 + 4 * m) = make_float4(v[0], v[1], v[2], v[3]);
+            }
         }
         __syncthreads();
-        // T = (I + L)^{-1}: diagonal 16x16 blocks by substitution, one column per thread.
-        if (tid < 64) {
-            const int blk = tid >> 4, c = tid & 15, o = 16 * blk;
-            float col[16];
+        // 16 x 16 diagonal blocks of T: warp 0 blocks 0, 1; warp 1 blocks 2, 3; lane = column
+        if (warp < 2) {
+            const int blk = 2 * warp + (lane >> 4), cc = lane & 15, o = 16 * blk;
+            float t[16];
 #pragma unroll
             for (int rr = 0; rr < 16; ++rr) {
-                float v;
-                if (rr < c) {
-                    v = 0.f;
-                } else if (rr == c) {
-                    v = 1.f;
-                } else {
-                    float s = 0.f;
-#pragma unroll
-                    for (int k = 0; k < rr; ++k)
-                        if (k >= c) s = fmaf(Ls[(o + rr) * PL + o + k], col[k], s);
-                    v = -s;
-                }
-                col[rr] = v;
-            }
-#pragma unroll
-            for (int rr = 0; rr < 16; ++rr) Ts[(o + rr) * PL + o + c] = col[rr];
-        }
-        __syncthreads();
-        // Off-diagonal blocks, block row by block row:
-        //   T_IJ = -T_II * sum_{K=J}^{I-1} L_IK T_KJ   (J < I)
-        for (int I = 1; I < 4; ++I) {
-            for (int e = tid; e < I * 256; e += DELTA_THREADS) {
-                const int J = e >> 8, rr = (e >> 4) & 15, c = e & 15;
-                float z = 0.f;
-                for (int K = J; K < I; ++K)
-#pragma unroll
-                    for (int m = 0; m < 16; ++m)
-                        z = fmaf(Ls[(16 * I + rr) * PL + 16 * K + m], Ts[(16 * K + m) * PL + 16 * J + c], z);
-                Zs[J * 256 + rr * 16 + c] = z;
-            }
-            __syncthreads();
-            for (int e = tid; e < I * 256; e += DELTA_THREADS) {
-                const int J = e >> 8, rr = (e >> 4) & 15, c = e & 15;
                 float s = 0.f;
 #pragma unroll
-                for (int m = 0; m < 16; ++m) s = fmaf(Ts[(16 * I + rr) * PL + 16 * I + m], Zs[J * 256 + m * 16 + c], s);
-                Ts[(16 * I + rr) * PL + 16 * J + c] = -s;
+                for (int k = 0; k < rr; ++k) s = fmaf(Ls[(o + rr) * PL + o + k], t[k], s);
+                t[rr] = rr < cc ? 0.f : (rr == cc ? 1.f : -s);
             }
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr) Ts[(o + rr) * PL + o + cc] = t[rr];
+        }
+        __syncthreads();
+        // 32 x 32 blocks: T21 = -T22 (L21 T11), T43 = -T44 (L43 T33)
+        {
+            const int p = tid >> 6, o = 32 * p;   // threads 0-63: rows 16-31; 64-127: rows 48-63
+            block_mm<16, 16, 16>(Ls + (o + 16) * PL + o, Ts + o * PL + o, Ws + 16 * p * PL, 1.f, p < 2 ? (tid & 63) : -1);
+            __syncthreads();
+            block_mm<16, 16, 16>(Ts + (o + 16) * PL + o + 16, Ws + 16 * p * PL, Ts + (o + 16) * PL + o, -1.f,
+                                 p < 2 ? (tid & 63) : -1);
             __syncthreads();
         }
-        float* tout = a.T + cb * DC * DC;
-        for (int idx = tid; idx < DC * DC; idx += DELTA_THREADS) {
-            const int rr = idx / DC, c = idx % DC;
-            tout[swz64(rr, c)] = tf32f(Ts[rr * PL + c]);
+        // 64 x 64: T[32:64, 0:32] = -T[32:64, 32:64] (L[32:64, 0:32] T[0:32, 0:32])
+        block_mm<32, 32, 32>(Ls + 32 * PL, Ts, Ws, 1.f, tid);
+        __syncthreads();
+        block_mm<32, 32, 32>(Ts + 32 * PL + 32, Ws, Ts + 32 * PL, -1.f, tid);
+        __syncthreads();
+        // T (tf32) in the swizzled image: thread -> row tid/4, 16 columns; upper triangle zero
+        {
+            const int rr = tid >> 2, cq = 16 * (tid & 3);
+            float* trow = a.T + cb * DC * DC + (cq >> 5) * (DC * 32) + rr * 32;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const int c = cq + 4 * m;
+                float v[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) v[e] = c + e <= rr ? tf32f(Ts[rr * PL + c + e]) : 0.f;
+                *reinterpret_cast<float4*>(trow + (((((c & 31) >> 2) ^ (rr & 7)) & 7) << 2)) = make_float4(v[0], v[1], v[2], v[3]);
+            }
         }
         if (tid < DC) {
             const float gv = gl[tid];
@@ -329,6 +332,9 @@ __global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(DeltaArgs 
         }
         __syncthreads();   // before the next head overwrites L and T
     }
+    t5::fence_before();
+    __syncthreads();
+    if (warp == 0) t5::dealloc(tmem, 64);
 }
 
 // ------------------------------------------------------------------ state pass
@@ -732,7 +738,7 @@ int read_and_clear_delta_error() {
 
 template <int D>
 static cudaError_t launch_delta_d(DeltaArgs& a, cudaStream_t st) {
-    const size_t prep_smem = PrepSmem<D>::FLOATS * sizeof(float);
+    const size_t prep_smem = PrepSmem<D>::BYTES + 1024;
     const size_t state_smem = StateSmem<D>::BYTES + 1024;
     static bool attr = false;
     if (!attr) {
@@ -740,11 +746,11 @@ static cudaError_t launch_delta_d(DeltaArgs& a, cudaStream_t st) {
         cudaFuncSetAttribute(delta_state_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(state_smem));
         attr = true;
     }
-    delta_prep_kernel<D><<<dim3(a.nchunks, a.hv / a.ratio), DELTA_THREADS, prep_smem, st>>>(a);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
     CUtensorMap map;
     if (!make_qkv_map(&map, a.qkv, a.n, a.c_conv)) return cudaErrorInvalidValue;
+    delta_prep_kernel<D><<<dim3(a.nchunks, a.hv / a.ratio), DELTA_THREADS, prep_smem, st>>>(map, a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
     delta_state_kernel<D><<<dim3(a.hv, D / NV), STATE_THREADS, state_smem, st>>>(map, a);
     return cudaGetLastError();
 }
