@@ -87,9 +87,16 @@ struct PrepSmem {
     static constexpr int W0 = T0 + DC * PL * 4;          // block temporaries [DC/2][PL]
     static constexpr int GL0 = W0 + DC / 2 * PL * 4;     // gamma [PREP_MAX_RATIO][DC]
     static constexpr int BB0 = GL0 + PREP_MAX_RATIO * DC * 4;  // b [PREP_MAX_RATIO][DC]
-    static constexpr int B0 = BB0 + PREP_MAX_RATIO * DC * 4;   // mbarriers: TMA, MMA
+    // staging of the T image when the K rows cannot hold it (D = 64)
+    static constexpr int TX0 = BB0 + PREP_MAX_RATIO * DC * 4;
+    static constexpr int B0 = TX0 + (D == 64 ? 2 * SLAB : 0);  // mbarriers: TMA, MMA
     static constexpr int MISC0 = B0 + 16;                      // TMEM base address
     static constexpr int BYTES = MISC0 + 16;
+    // 8 KB staging pieces for the bulk stores, once the Gram product is done:
+    // K^T pieces in the Q rows of slab p; A (then T, for D = 128) in the K rows.
+    static __device__ __forceinline__ int kt_piece(int p) { return QK0 + p * 2 * SLAB; }
+    static __device__ __forceinline__ int a_piece(int p) { return QK0 + p * 2 * SLAB + SLAB; }
+    static __device__ __forceinline__ int t_piece(int p) { return D == 128 ? QK0 + (2 + p) * 2 * SLAB + SLAB : TX0 + p * SLAB; }
 };
 
 // C = s * A B for blocks of the fp32 matrices in shared memory (row pitch PL):
@@ -215,20 +222,6 @@ __global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(const __gr
         return;
     }
 
-    // ---- K^T image for the state pass: warp task (d-slab s, tokens 4g .. 4g+3), lane = d % 32
-    {
-        float* kt = a.KT + (static_cast<int64_t>(chunk) * gridDim.y + hk) * D * DC;
-        for (int task = warp; task < L::NSLAB * (DC / 4); task += DELTA_THREADS / 32) {
-            const int s = task / (DC / 4), g = task % (DC / 4), t = 4 * g;
-            const unsigned char* kp = base + L::QK0 + s * 2 * L::SLAB + L::SLAB;
-            const float4 v = make_float4(*reinterpret_cast<const float*>(kp + sw128_f32(t, lane)),
-                                         *reinterpret_cast<const float*>(kp + sw128_f32(t + 1, lane)),
-                                         *reinterpret_cast<const float*>(kp + sw128_f32(t + 2, lane)),
-                                         *reinterpret_cast<const float*>(kp + sw128_f32(t + 3, lane)));
-            *reinterpret_cast<float4*>(kt + (t >> 5) * (D * 32) + (sw128_f32(32 * s + lane, t & 31) >> 2)) = v;
-        }
-    }
-
     // ---- the Gram rows of this thread
     const int q = warp & 3, half = warp >> 2;
     const bool qrow = q < 2;                 // lanes 0-63: q_i.k_j; lanes 64-127: k_i.k_j
@@ -250,6 +243,32 @@ __global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(const __gr
         return;
     }
 
+    // ---- K^T image for the state pass, staged in the Q rows (free now) and
+    // written by bulk copies: piece (token slab ts, 64 key rows db) is 8 KB of
+    // the image.  Warp task (d-slab s, tokens 4g .. 4g+3), lane = d % 32.
+    {
+        for (int task = warp; task < L::NSLAB * (DC / 4); task += DELTA_THREADS / 32) {
+            const int s = task / (DC / 4), g4 = task % (DC / 4), t = 4 * g4;
+            const unsigned char* kp = base + L::QK0 + s * 2 * L::SLAB + L::SLAB;
+            const float4 v = make_float4(*reinterpret_cast<const float*>(kp + sw128_f32(t, lane)),
+                                         *reinterpret_cast<const float*>(kp + sw128_f32(t + 1, lane)),
+                                         *reinterpret_cast<const float*>(kp + sw128_f32(t + 2, lane)),
+                                         *reinterpret_cast<const float*>(kp + sw128_f32(t + 3, lane)));
+            const int d = 32 * s + lane, piece = (t >> 5) * (D / 64) + (d >> 6);
+            *reinterpret_cast<float4*>(base + L::kt_piece(piece) + sw128_f32(d & 63, t & 31)) = v;
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            float* kt = a.KT + (static_cast<int64_t>(chunk) * gridDim.y + hk) * D * DC;
+            for (int p = 0; p < L::NSLAB; ++p) {
+                const int ts = p / (D / 64), db = p % (D / 64);
+                bulk_store_1d(kt + ts * (D * 32) + db * (64 * 32), base + L::kt_piece(p), L::SLAB);
+            }
+            bulk_commit();
+        }
+    }
+
     for (int j = 0; j < r; ++j) {
         const int h = hk * r + j;
         const int64_t cb = static_cast<int64_t>(chunk) * a.hv + h;
@@ -258,7 +277,7 @@ __global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(const __gr
         const float gi = gl[row];
         if (qrow) {
             // A_ij = e^{gamma_i - gamma_j} q_i.k_j (j <= i): one 128-byte row of the swizzled image
-            float* arow = a.A + cb * DC * DC + half * (DC * 32) + row * 32;
+            unsigned char* arow = base + L::a_piece(half) + row * 128;
 #pragma unroll
             for (int m = 0; m < 8; ++m) {
                 float v[4];
@@ -267,7 +286,7 @@ __global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(const __gr
                     const int c = c0 + 4 * m + e;
                     v[e] = c <= row ? tf32f(__expf(gi - gl[c]) * g[4 * m + e]) : 0.f;
                 }
-                *reinterpret_cast<float4*>(arow + (((m ^ (row & 7)) & 7) << 2)) = make_float4(v[0], v[1], v[2], v[3]);
+                *reinterpret_cast<float4*>(arow + (((m ^ (row & 7)) & 7) << 4)) = make_float4(v[0], v[1], v[2], v[3]);
             }
         } else {
             // L_ij = b_i e^{gamma_i - gamma_j} k_i.k_j (j < i)
@@ -316,22 +335,34 @@ __global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(const __gr
         // T (tf32) in the swizzled image: thread -> row tid/4, 16 columns; upper triangle zero
         {
             const int rr = tid >> 2, cq = 16 * (tid & 3);
-            float* trow = a.T + cb * DC * DC + (cq >> 5) * (DC * 32) + rr * 32;
+            unsigned char* trow = base + L::t_piece(cq >> 5) + rr * 128;
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
                 const int c = cq + 4 * m;
                 float v[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) v[e] = c + e <= rr ? tf32f(Ts[rr * PL + c + e]) : 0.f;
-                *reinterpret_cast<float4*>(trow + (((((c & 31) >> 2) ^ (rr & 7)) & 7) << 2)) = make_float4(v[0], v[1], v[2], v[3]);
+                *reinterpret_cast<float4*>(trow + (((((c & 31) >> 2) ^ (rr & 7)) & 7) << 4)) = make_float4(v[0], v[1], v[2], v[3]);
             }
         }
         if (tid < DC) {
             const float gv = gl[tid];
             *reinterpret_cast<float4*>(a.G + (cb * DC + tid) * 4) = make_float4(gv, expf(gv), bb[tid], expf(gl[DC - 1] - gv));
         }
-        __syncthreads();   // before the next head overwrites L and T
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            // A and T images of this head, 2 x 8 KB each
+            for (int p = 0; p < 2; ++p) {
+                bulk_store_1d(a.A + cb * DC * DC + p * (DC * 32), base + L::a_piece(p), L::SLAB);
+                bulk_store_1d(a.T + cb * DC * DC + p * (DC * 32), base + L::t_piece(p), L::SLAB);
+            }
+            bulk_commit();
+            bulk_wait_read();      // the staging is rewritten by the next head
+        }
+        __syncthreads();   // before the next head overwrites L, T and the staging
     }
+    if (tid == 0) bulk_wait_all();
     t5::fence_before();
     __syncthreads();
     if (warp == 0) t5::dealloc(tmem, 64);

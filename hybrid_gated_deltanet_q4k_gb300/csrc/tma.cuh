@@ -81,6 +81,19 @@ __device__ __forceinline__ void bulk_load_1d(void* dst, const void* src, uint32_
                  : "memory");
 }
 
+// 1-D bulk copy shared -> global of `bytes` (a multiple of 16; both addresses
+// 16-byte aligned), tracked by this thread's bulk-async group.
+__device__ __forceinline__ void bulk_store_1d(void* dst, const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_addr(src)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// This thread's committed bulk stores have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// ... and have completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // Byte offset of fp32 element (r, c), c < 32, inside a 128-byte-swizzled slab
 // of 128-byte rows (the layout a 2-D TMA box with SWIZZLE_128B and a 32-float
 // inner extent writes): the 16-byte chunk index is XORed with r mod 8.
