@@ -23,10 +23,11 @@
 //   delta_prep   one CTA per (chunk, key head), all chunks in parallel: the
 //                Gram products Q K^T and K K^T once (the value heads of a key
 //                head share them), K^T for the state pass, then per value
-//                head gamma, the masked A, and T = (I + L)^{-1} by recursive
-//                doubling on the block-triangular structure.  Writes T, A and
-//                K^T (tf32, in the state pass's shared-memory operand image)
-//                and a gate table (gamma, e^gamma, b, e^{gamma_C - gamma}).
+//                head gamma, the masked A, T = (I + L)^{-1} by recursive
+//                doubling on the block-triangular structure, and A T.  Writes
+//                [A T; T] and K^T (tf32, in the state pass's shared-memory
+//                operand image) and a gate table (gamma, e^gamma, b,
+//                e^{gamma_C - gamma}).
 //   delta_state  one CTA per (head, 32 rows of S): the chunks in order.  Rows
 //                of S evolve independently (row i only reads v[i]), so the
 //                rows split across CTAs with no communication.  The fp32 state
@@ -61,8 +62,7 @@ struct DeltaArgs {
     const float* b;       // [n][hv]
     int n, hv, ratio, c_qk, c_conv, c_v;
     int nchunks;
-    float* T;      // [nchunks][hv][DC][DC]   tf32-rounded
-    float* A;      // [nchunks][hv][DC][DC]   tf32-rounded
+    float* TA;     // [nchunks][hv][2*DC][DC] [A T; T], tf32, in the swizzled operand image
     float* G;      // [nchunks][hv][DC][4]    gamma, e^gamma, b, e^{gamma_C - gamma}
     float* KT;     // [nchunks][hk][D][DC]    K^T, in the swizzled operand image
     const float* state_in;  // [hv][D][D] or null
@@ -87,16 +87,18 @@ struct PrepSmem {
     static constexpr int W0 = T0 + DC * PL * 4;          // block temporaries [DC/2][PL]
     static constexpr int GL0 = W0 + DC / 2 * PL * 4;     // gamma [PREP_MAX_RATIO][DC]
     static constexpr int BB0 = GL0 + PREP_MAX_RATIO * DC * 4;  // b [PREP_MAX_RATIO][DC]
-    // staging of the T image when the K rows cannot hold it (D = 64)
-    static constexpr int TX0 = BB0 + PREP_MAX_RATIO * DC * 4;
-    static constexpr int B0 = TX0 + (D == 64 ? 2 * SLAB : 0);  // mbarriers: TMA, MMA
+    // 8 KB pieces 0-7 of operand and output images once the Gram product is
+    // done: the [Q; K] region, extended for D = 64 by 32 KB of its own.
+    static constexpr int EX0 = BB0 + PREP_MAX_RATIO * DC * 4;
+    static constexpr int B0 = EX0 + (8 - 2 * NSLAB) * SLAB;    // mbarriers: TMA, MMA
     static constexpr int MISC0 = B0 + 16;                      // TMEM base address
     static constexpr int BYTES = MISC0 + 16;
-    // 8 KB staging pieces for the bulk stores, once the Gram product is done:
-    // K^T pieces in the Q rows of slab p; A (then T, for D = 128) in the K rows.
+    static __device__ __forceinline__ int piece(int p) { return p < 2 * NSLAB ? QK0 + p * SLAB : EX0 + (p - 2 * NSLAB) * SLAB; }
+    // K^T staging: the Q rows of slab p (pieces 0, 2, 4, 6), written while the K rows are read
     static __device__ __forceinline__ int kt_piece(int p) { return QK0 + p * 2 * SLAB; }
-    static __device__ __forceinline__ int a_piece(int p) { return QK0 + p * 2 * SLAB + SLAB; }
-    static __device__ __forceinline__ int t_piece(int p) { return D == 128 ? QK0 + (2 + p) * 2 * SLAB + SLAB : TX0 + p * SLAB; }
+    static constexpr int AI = 0;    // A operand [DC][DC] (pieces 0-1)
+    static constexpr int TTI = 2;   // T^T operand [DC][DC] (pieces 2-3)
+    static constexpr int OUTI = 4;  // [A T; T] output [2*DC][DC] (pieces 4-7: two 16 KB slabs)
 };
 
 // C = s * A B for blocks of the fp32 matrices in shared memory (row pitch PL):
@@ -164,7 +166,7 @@ __global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(const __gr
             tma_load_2d_tile(dst + L::SLAB, &qkv_map, bars + 0, a.c_qk + hk * D + 32 * sl, t0);
         }
     }
-    if (warp == 0) t5::alloc(tslot, 64);
+    if (warp == 0) t5::alloc(tslot, 128);
     // T's blocks (rows 0-15, cols 16-31) and (rows 32-47, cols 48-63) stay zero: the
     // 32 x 32 diagonal blocks of T are read whole by the last doubling step
     for (int idx = tid; idx < 2 * 16 * 16; idx += DELTA_THREADS) {
@@ -218,7 +220,7 @@ __global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(const __gr
         if (tid == 0) mbar_wait_bounded(bars + 0, 0, nullptr, 0, 20000000ull);
         t5::fence_before();
         __syncthreads();
-        if (warp == 0) t5::dealloc(tmem, 64);
+        if (warp == 0) t5::dealloc(tmem, 128);
         return;
     }
 
@@ -239,7 +241,7 @@ __global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(const __gr
         if (tid == 0) mbar_wait_bounded(bars + 1, 0, nullptr, 0, 200000000ull);
         t5::fence_before();
         __syncthreads();
-        if (warp == 0) t5::dealloc(tmem, 64);
+        if (warp == 0) t5::dealloc(tmem, 128);
         return;
     }
 
@@ -266,7 +268,9 @@ __global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(const __gr
                 bulk_store_1d(kt + ts * (D * 32) + db * (64 * 32), base + L::kt_piece(p), L::SLAB);
             }
             bulk_commit();
+            bulk_wait_read();      // the region becomes the per-head staging
         }
+        __syncthreads();
     }
 
     for (int j = 0; j < r; ++j) {
@@ -277,7 +281,7 @@ __global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(const __gr
         const float gi = gl[row];
         if (qrow) {
             // A_ij = e^{gamma_i - gamma_j} q_i.k_j (j <= i): one 128-byte row of the swizzled image
-            unsigned char* arow = base + L::a_piece(half) + row * 128;
+            unsigned char* arow = base + L::piece(L::AI + half) + row * 128;
 #pragma unroll
             for (int m = 0; m < 8; ++m) {
                 float v[4];
@@ -332,17 +336,24 @@ __global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(const __gr
         __syncthreads();
         block_mm<32, 32, 32>(Ts + 32 * PL + 32, Ws, Ts + 32 * PL, -1.f, tid);
         __syncthreads();
-        // T (tf32) in the swizzled image: thread -> row tid/4, 16 columns; upper triangle zero
+        // T^T operand image (row m, column j = T_jm) and the T rows of the output
+        // (rows 64-127 of [A T; T]), tf32; thread -> row tid/4, 16 columns
         {
             const int rr = tid >> 2, cq = 16 * (tid & 3);
-            unsigned char* trow = base + L::t_piece(cq >> 5) + rr * 128;
+            unsigned char* ttrow = base + L::piece(L::TTI + (cq >> 5)) + rr * 128;
+            unsigned char* orow = base + L::piece(L::OUTI + 2 * (cq >> 5)) + (DC + rr) * 128;
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
                 const int c = cq + 4 * m;
-                float v[4];
+                float v[4], w[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) v[e] = c + e <= rr ? tf32f(Ts[rr * PL + c + e]) : 0.f;
-                *reinterpret_cast<float4*>(trow + (((((c & 31) >> 2) ^ (rr & 7)) & 7) << 4)) = make_float4(v[0], v[1], v[2], v[3]);
+                for (int e = 0; e < 4; ++e) {
+                    v[e] = c + e <= rr ? tf32f(Ts[rr * PL + c + e]) : 0.f;
+                    w[e] = c + e >= rr ? tf32f(Ts[(c + e) * PL + rr]) : 0.f;
+                }
+                const int ch = ((((c & 31) >> 2) ^ (rr & 7)) & 7) << 4;
+                *reinterpret_cast<float4*>(orow + ch) = make_float4(v[0], v[1], v[2], v[3]);
+                *reinterpret_cast<float4*>(ttrow + ch) = make_float4(w[0], w[1], w[2], w[3]);
             }
         }
         if (tid < DC) {
@@ -350,22 +361,53 @@ __global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(const __gr
             *reinterpret_cast<float4*>(a.G + (cb * DC + tid) * 4) = make_float4(gv, expf(gv), bb[tid], expf(gl[DC - 1] - gv));
         }
         fence_proxy_async_smem();
+        t5::fence_before();
         __syncthreads();
+        // A T on the tensor cores (M = 64, N = 64, K = 64) into TMEM columns 64-127
+        bool mok = true;
         if (tid == 0) {
-            // A and T images of this head, 2 x 8 KB each
-            for (int p = 0; p < 2; ++p) {
-                bulk_store_1d(a.A + cb * DC * DC + p * (DC * 32), base + L::a_piece(p), L::SLAB);
-                bulk_store_1d(a.T + cb * DC * DC + p * (DC * 32), base + L::t_piece(p), L::SLAB);
+            t5::fence_after();
+            const uint32_t sb = smem_addr(base);
+            const uint64_t dA = t5::desc_sw128(sb + L::piece(L::AI)), dB = t5::desc_sw128(sb + L::piece(L::TTI));
+            constexpr uint32_t ID = t5::idesc_tf32(64, DC);
+#pragma unroll
+            for (int k = 0; k < DC / 8; ++k) {
+                const uint64_t off = static_cast<uint64_t>((k >> 2) * (L::SLAB >> 4) + 2 * (k & 3));
+                t5::mma_tf32(tmem + 64, dA + off, dB + off, ID, k > 0 ? 1u : 0u);
             }
+            t5::commit(bars + 1);
+        }
+        if (!mbar_wait_bounded(bars + 1, (j + 1) & 1, &g_delta_error, ERR_WAIT_TIMEOUT)) mok = false;
+        mok = __all_sync(0xffffffffu, mok);
+        if (mok) {
+            // rows 0-63 of the output: A T, row i in lane 32(i/16) + i%16 (M = 64)
+            t5::fence_after();
+            float at[32];
+            t5::ld32(tmem + (static_cast<uint32_t>(32 * q) << 16) + 64 + c0, at);
+            if (lane < 16) {
+                const int ri = 16 * q + lane;
+                unsigned char* orow = base + L::piece(L::OUTI + 2 * half) + ri * 128;
+#pragma unroll
+                for (int m = 0; m < 8; ++m)
+                    *reinterpret_cast<float4*>(orow + (((m ^ (ri & 7)) & 7) << 4)) =
+                        make_float4(tf32f(at[4 * m]), tf32f(at[4 * m + 1]), tf32f(at[4 * m + 2]), tf32f(at[4 * m + 3]));
+            }
+        }
+        fence_proxy_async_smem();
+        t5::fence_before();
+        mok = __syncthreads_and(mok);
+        if (tid == 0 && mok) {
+            bulk_store_1d(a.TA + cb * 2 * DC * DC, base + L::piece(L::OUTI), 4 * L::SLAB);
             bulk_commit();
             bulk_wait_read();      // the staging is rewritten by the next head
         }
         __syncthreads();   // before the next head overwrites L, T and the staging
+        if (!mok) break;
     }
     if (tid == 0) bulk_wait_all();
     t5::fence_before();
     __syncthreads();
-    if (warp == 0) t5::dealloc(tmem, 64);
+    if (warp == 0) t5::dealloc(tmem, 128);
 }
 
 // ------------------------------------------------------------------ state pass
@@ -385,15 +427,14 @@ struct StateSmem {
     static constexpr int KT_BYTES = 2 * KT_SLAB;   // one K^T [D][DC]
     static constexpr int QK0 = 0;                  // [Q; K] [2*DC][D]  (TMA)
     static constexpr int KT0 = QK0 + NSLAB * QK_SLAB;   // K^T [2][D][DC] (bulk copies)
-    static constexpr int T0 = KT0 + 2 * KT_BYTES;  // T [DC][DC]        (bulk copy)
-    static constexpr int A0 = T0 + 2 * SLAB;       // [A; 0] [2*DC][DC] (bulk copies into the upper rows)
-    static constexpr int V0 = A0 + 2 * QK_SLAB;    // V [DC][NV]        (TMA)
+    static constexpr int TA0 = KT0 + 2 * KT_BYTES; // [A T; T] [2*DC][DC] (bulk copy of the prep image)
+    static constexpr int V0 = TA0 + 2 * QK_SLAB;   // V [DC][NV]        (TMA)
     static constexpr int S0 = V0 + SLAB;           // S [NV][D]         tf32 operand of X, Y
-    static constexpr int R0 = S0 + NSLAB * SOP;    // R^T, then Delta^T [NV][DC]
+    static constexpr int R0 = S0 + NSLAB * SOP;    // R^T [NV][DC]
     static constexpr int E0 = R0 + 2 * SOP;        // Delta~^T [NV][DC]
     static constexpr int G0 = E0 + 2 * SOP;        // gate table [2][DC] x (gamma, e^gamma, b, e^{gamma_C-gamma})
     static constexpr int B0 = G0 + 2 * DC * 16;    // mbarriers
-    static constexpr int NBAR = 17;
+    static constexpr int NBAR = 14;
     static constexpr int MISC0 = B0 + NBAR * 8;    // TMEM base address, abort flag
     static constexpr int BYTES = MISC0 + 16;
     static_assert(BYTES + 1024 <= 227 * 1024, "state pass shared memory");
@@ -401,13 +442,13 @@ struct StateSmem {
 
 // TMEM columns (fp32 accumulators of NV = 32 columns).  [Q; K] S^T is
 // double-buffered: the output reads Y of chunk c while X, Y of chunk c+1 run.
-constexpr uint32_t TM_XY = 0, TM_D = 64, TM_U = 96, TM_Z = 128;
-constexpr uint32_t TM_COLS = 256;
+constexpr uint32_t TM_XY = 0, TM_DZ = 64, TM_U = 96;
+constexpr uint32_t TM_COLS = 128;
 
 enum StateBar : int {
-    F_QK, F_KT0, F_KT1, F_V, F_T, F_A,   // copies landed (tx bytes)
-    E_QK, E_KT0, E_KT1, E_V, E_T, E_A,   // buffer free again
-    M_XY, M_D, M_U, M_Z,                 // MMA groups complete (tcgen05.commit)
+    F_QK, F_KT0, F_KT1, F_V, F_TA,       // copies landed (tx bytes)
+    E_QK, E_KT0, E_KT1, E_V, E_TA,       // buffer free again
+    M_XY, M_DZ, M_U,                     // MMA groups complete (tcgen05.commit)
     M_FIN,                               // every MMA of the CTA complete (shutdown)
 };
 
@@ -461,15 +502,16 @@ __device__ __forceinline__ void mma_chain(uint32_t d_tmem, uint64_t adesc, uint6
 // Per chunk, with S the NV x D slice of the state (tf32 operands, fp32 sums):
 //   MMA  [Y; X] = [Q; K] S^T          (M = 128: Y in lanes 0-63, X in 64-127)
 //   warps 2,3,6,7 (lanes 64-127)  R = diag(b)(V - diag(e^gamma) X) -> R^T
-//   MMA  Delta = T R                  (M = 64: row j in lane 32*(j/16) + j%16)
-//   lanes 0-15  Delta^T and Delta~^T = (diag(e^{gamma_C-gamma}) Delta)^T
+//   MMA  [Z; Delta] = [A T; T] R      (M = 128: Z = A Delta in lanes 0-63,
+//        Delta in lanes 64-127; delta_prep folds A T, so A Delta costs no
+//        extra product)
+//   warps 2,3,6,7  Delta~^T = (diag(e^{gamma_C-gamma}) Delta)^T
 //   MMA  U = K^T Delta~               (M = D: row d in lane d, or 32*(d/16)+d%16)
-//   MMA  [Z; 0] = [A; 0] Delta        (M = 128: Z in lanes 0-63, next to Y)
 //   warps  S <- e^{gamma_C} S + U in fp32 registers, its tf32 image -> S
 //   MMA  next chunk's [Q; K] S^T
 //   warps 0,1,4,5 (lanes 0-63)  O = diag(e^gamma) Y + Z, while it runs.
 // The state's chain per chunk is four dependent steps (X, R, Delta, U); the
-// output products stay off it.  Every thread meets every named barrier of
+// output stays off it.  Every thread meets every named barrier of
 // every chunk, also after a wait ran out (it then skips the work, and the MMA
 // warp issues nothing more), so no barrier is ever left waiting.
 template <int D>
@@ -487,19 +529,13 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
     const uint32_t sbase = smem_addr(base);
 
     if (tid == 0) {
-        for (int i = F_QK; i <= F_A; ++i) mbar_init_cta(bars + i, 1);
-        for (int i = E_QK; i <= E_A; ++i) mbar_init_cta(bars + i, 1);
+        for (int i = F_QK; i <= F_TA; ++i) mbar_init_cta(bars + i, 1);
+        for (int i = E_QK; i <= E_TA; ++i) mbar_init_cta(bars + i, 1);
         mbar_init_cta(bars + E_V, DELTA_THREADS);
         for (int i = M_XY; i <= M_FIN; ++i) mbar_init_cta(bars + i, 1);
         mbar_init_fence();
         *abort = 0;
     }
-    // the zero rows 64-127 of the [A; 0] operand
-    for (int idx = tid; idx < 2 * L::SLAB / 16; idx += STATE_THREADS) {
-        const int sl = idx / (L::SLAB / 16), off = idx % (L::SLAB / 16);
-        *reinterpret_cast<uint4*>(base + L::A0 + sl * L::QK_SLAB + L::SLAB + 16 * off) = make_uint4(0u, 0u, 0u, 0u);
-    }
-    fence_proxy_async_smem();
     if (warp == 9) t5::alloc(tslot, TM_COLS);
     t5::fence_before();
     __syncthreads();
@@ -529,24 +565,18 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
                 mbar_expect_tx(bars + F_V, L::SLAB + DC * 16);
                 tma_load_2d_tile(base + L::V0, &qkv_map, bars + F_V, 2 * a.c_qk + h * D + i0, c * DC);
                 bulk_load_1d(base + L::G0 + (c & 1) * DC * 16, a.G + cb(c) * DC * 4, DC * 16, bars + F_V);
-                if (c >= 1 && !state_wait(bars + E_T, pp, abort)) break;
-                mbar_expect_tx(bars + F_T, 2 * L::SLAB);
-                bulk_load_1d(base + L::T0, a.T + cb(c) * DC * DC, 2 * L::SLAB, bars + F_T);
-                if (c >= 1 && !state_wait(bars + E_A, pp, abort)) break;
-                mbar_expect_tx(bars + F_A, 2 * L::SLAB);
-                for (int sl = 0; sl < 2; ++sl)
-                    bulk_load_1d(base + L::A0 + sl * L::QK_SLAB, a.A + cb(c) * DC * DC + sl * (DC * 32), L::SLAB,
-                                 bars + F_A);
+                if (c >= 1 && !state_wait(bars + E_TA, pp, abort)) break;
+                mbar_expect_tx(bars + F_TA, 2 * L::QK_SLAB);
+                bulk_load_1d(base + L::TA0, a.TA + cb(c) * 2 * DC * DC, 2 * L::QK_SLAB, bars + F_TA);
             }
         }
     } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
-        constexpr uint32_t ID64 = t5::idesc_tf32(64, NV);
         constexpr uint32_t ID128 = t5::idesc_tf32(128, NV);
         constexpr uint32_t IDU = t5::idesc_tf32(D, NV);
         const uint64_t dQK = t5::desc_sw128(sbase + L::QK0), dS = t5::desc_sw128(sbase + L::S0);
-        const uint64_t dT = t5::desc_sw128(sbase + L::T0), dR = t5::desc_sw128(sbase + L::R0);
-        const uint64_t dA = t5::desc_sw128(sbase + L::A0), dE = t5::desc_sw128(sbase + L::E0);
+        const uint64_t dTA = t5::desc_sw128(sbase + L::TA0), dR = t5::desc_sw128(sbase + L::R0);
+        const uint64_t dE = t5::desc_sw128(sbase + L::E0);
         const uint64_t dKT = t5::desc_sw128(sbase + L::KT0);
         const bool leader = lane == 0;
         // leader only: the copy has landed and nothing has failed
@@ -565,22 +595,17 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
             }
             __syncwarp();
             nb_sync(NB_R);                      // R^T written
-            if (leader && ready(F_T, ph)) {
-                mma_chain<DC / 8, L::SLAB, L::SOP>(tmem + TM_D, dT, dR, ID64);
-                t5::commit(bars + M_D);
-                t5::commit(bars + E_T);
+            if (leader && ready(F_TA, ph)) {
+                mma_chain<DC / 8, L::QK_SLAB, L::SOP>(tmem + TM_DZ, dTA, dR, ID128);
+                t5::commit(bars + M_DZ);
+                t5::commit(bars + E_TA);
             }
             __syncwarp();
-            nb_sync(NB_D);                      // Delta^T, Delta~^T written
+            nb_sync(NB_D);                      // Delta~^T written
             if (leader && ready(F_KT0 + ph, (c >> 1) & 1)) {
                 mma_chain<DC / 8, L::KT_SLAB, L::SOP>(tmem + TM_U, dKT + ph * (L::KT_BYTES >> 4), dE, IDU);
                 t5::commit(bars + M_U);
                 t5::commit(bars + E_KT0 + ph);
-                if (ready(F_A, ph)) {
-                    mma_chain<DC / 8, L::QK_SLAB, L::SOP>(tmem + TM_Z, dA, dR, ID128);
-                    t5::commit(bars + M_Z);
-                    t5::commit(bars + E_A);
-                }
             }
             __syncwarp();
         }
@@ -596,8 +621,7 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
         const int v0 = 16 * hc;
         const bool xw = q >= 2;                 // lanes 64-127: X rows; lanes 0-63: Y rows
         const int tok = 32 * (q & 1) + lane;    // token of this lane in the M = 128 products
-        const bool act = lane < 16;             // owns token j = 16q + lane of the M = 64 product
-        const int j = 16 * q + lane;
+        const bool act = lane < 16;             // lanes holding rows of an M = 64 product
         const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q) << 16) + v0;   // this warp's lanes, columns v0..
         // key-dimension row d of U owned by this thread (all lanes for D = 128, lanes 0-15 for D = 64)
         const bool own_d = D == 128 ? true : act;
@@ -641,10 +665,9 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
             const uint32_t ph = c & 1;
             const float4* G = reinterpret_cast<const float4*>(base + L::G0 + ph * DC * 16);
             float4 gt = make_float4(0.f, 0.f, 0.f, 0.f);
-            float sc = 0.f, dec = 0.f;
+            float dec = 0.f;
             if (!*abort && state_wait(bars + F_V, ph, abort)) {
-                gt = G[tok];            // gates of this lane's token (M = 128 products)
-                sc = G[j].w;            // e^{gamma_C - gamma_j}
+                gt = G[tok];            // gates of this lane's token: gamma, e^gamma, b, e^{gamma_C - gamma}
                 dec = G[DC - 1].y;      // e^{gamma_C}
             }
 
@@ -666,20 +689,13 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
             mbar_arrive_cta(bars + E_V);         // V and this chunk's gate reads are done
             handover(NB_R);
 
-            // ---- Delta = T R -> Delta^T (over R^T) and Delta~^T
-            if (mma_done(M_D, ph)) {
+            // ---- [Z; Delta] = [A T; T] R -> Delta~^T (Delta rows: lanes 64-127)
+            if (xw && mma_done(M_DZ, ph)) {
                 float dl[16];
-                t5::ld16(tl + TM_D, dl);
-                if (act) {
-                    float de[16];
+                t5::ld16(tl + TM_DZ, dl);
 #pragma unroll
-                    for (int v = 0; v < 16; ++v) {
-                        de[v] = tf32f(dl[v] * sc);
-                        dl[v] = tf32f(dl[v]);
-                    }
-                    write_col(L::R0, j, dl);
-                    write_col(L::E0, j, de);
-                }
+                for (int v = 0; v < 16; ++v) dl[v] = tf32f(dl[v] * gt.w);
+                write_col(L::E0, tok, dl);
             }
             handover(NB_D);
 
@@ -694,9 +710,9 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
             if (c + 1 < a.nchunks) handover(NB_S);
 
             // ---- O = diag(e^gamma) Y + Z (Y rows: lanes 0-63), while the next X, Y run
-            if (!xw && mma_done(M_Z, ph)) {
+            if (!xw && mma_done(M_DZ, ph)) {
                 float y[16], z[16];
-                t5::ld16x2(tl + TM_XY + 32 * ph, y, tl + TM_Z, z);
+                t5::ld16x2(tl + TM_XY + 32 * ph, y, tl + TM_DZ, z);
                 const int t = c * DC + tok;
                 if (t < a.n) {
                     float4* dst = reinterpret_cast<float4*>(a.o + static_cast<int64_t>(t) * a.c_v + h * D + i0 + v0);
@@ -717,7 +733,7 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
     if (*abort && tid == 0) {
         // A wait ran out.  Copies already issued land in their own time; let them
         // finish (bounded) before the CTA's shared memory is released.
-        for (int i = F_QK; i <= F_A; ++i)
+        for (int i = F_QK; i <= F_TA; ++i)
             for (uint32_t par = 0; par < 2; ++par) mbar_wait_bounded(bars + i, par, nullptr, 0, 20000000ull);
     }
     t5::fence_before();
@@ -802,9 +818,8 @@ cudaError_t launch_delta(const gdn_layer& L, const float* qkv, const float* log_
     a.nchunks = static_cast<int>((n + DC - 1) / DC);
     const int64_t nch = a.nchunks;
     float* base = static_cast<float*>(scratch);
-    a.T = base;
-    a.A = a.T + nch * a.hv * DC * DC;
-    a.G = a.A + nch * a.hv * DC * DC;
+    a.TA = base;
+    a.G = a.TA + nch * a.hv * 2 * DC * DC;
     a.KT = a.G + nch * a.hv * DC * 4;
     a.state_in = state_in;
     a.state_out = state_out;
