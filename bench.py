@@ -435,7 +435,7 @@ def run_stage(args, spec):
         work, unit = 2.0 * n * r_in * H / 1e12, "TFLOP"
     else:
         s = dl.struct()
-        qkv = torch.randn(n, spec.c_conv, device="cuda", generator=g) * 0.05
+        qkv = (torch.randn(n, spec.c_conv, device="cuda", generator=g) * 0.05).to(torch.float16)
         la = -0.5 * torch.rand(n, hv, device="cuda", generator=g)
         b = torch.rand(n, hv, device="cuda", generator=g)
         stt = torch.zeros(hv, d, d, device="cuda")

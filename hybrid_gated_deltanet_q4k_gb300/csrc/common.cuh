@@ -14,7 +14,7 @@ namespace gdn {
 // unit (`static __device__ int`, no relocatable device code): when a wait runs
 // out they record a code there and return early; gdn_sync_status() reads and
 // clears every such word through the unit's host accessor.
-enum : int { ERR_NONE = 0, ERR_WAIT_TIMEOUT = 1 };
+enum : int { ERR_NONE = 0, ERR_WAIT_TIMEOUT = 1, ERR_RANGE = 2 };
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -80,6 +80,12 @@ __device__ __forceinline__ float qcode_fast(float w, const QScale& q, bool& redo
     const float r = rintf(y);
     redo |= !(fabsf(y - r) <= 0.499f);
     return fminf(fmaxf(r, -127.0f), 127.0f) + 0.0f;
+}
+
+// Two floats as a pair of fp16 values (rounded to nearest), low half first.
+__device__ __forceinline__ uint32_t f16x2_bits(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 // Two codes (integer-valued floats) as a pair of fp16 values, low half first.

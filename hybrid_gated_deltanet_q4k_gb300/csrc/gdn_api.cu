@@ -27,15 +27,16 @@ cudaError_t launch_gemm_codes(const uint16_t*, const float*, const uint16_t*, co
 cudaError_t launch_gemm_f32(const float*, const float*, int64_t, int64_t, int64_t, uint16_t*, int64_t, int64_t, float*,
                             int64_t, cudaStream_t);
 cudaError_t launch_conv(const gdn_layer&, const uint16_t*, int64_t, int64_t, const float*, const float*, int64_t,
-                        float*, float*, float*, cudaStream_t);
+                        uint16_t*, float*, float*, cudaStream_t);
 cudaError_t launch_conv_state(const gdn_layer&, const uint16_t*, int64_t, int64_t, float*, cudaStream_t);
-cudaError_t launch_delta(const gdn_layer&, const float*, const float*, const float*, int64_t, const float*, float*,
+cudaError_t launch_delta(const gdn_layer&, const uint16_t*, const float*, const float*, int64_t, const float*, float*,
                          float*, void*, cudaStream_t);
 size_t delta_scratch_bytes(int hv, int hk, int d, int64_t n);
 cudaError_t launch_gated_norm(const gdn_layer&, const float*, const uint16_t*, int64_t, int64_t, uint16_t*, float*,
                               float*, cudaStream_t);
 int read_and_clear_gemm_error();
 int read_and_clear_delta_error();
+int read_and_clear_conv_error();
 }  // namespace gdn
 
 using namespace gdn;
@@ -116,7 +117,7 @@ struct Workspace {
     uint16_t* xc; float* sx;          // x codes [B][H], scales [B]
     uint16_t* qkvz;                   // projection, bf16 [B][n_bf16]
     float* ba;                        // projection, fp32 [B][2 hv]
-    float* qkv;                       // conv output, fp32 [B][c_conv]
+    uint16_t* qkv;                    // conv output, fp16 [B][c_conv]
     float* log_a; float* b;           // gates [B][hv]
     float* o;                         // recurrence output [B][c_v]
     uint16_t* oc; float* so;          // gated-norm codes [B][c_v], scales [B]  (Q4_K)
@@ -151,7 +152,7 @@ Workspace carve(const gdn_layer* L, const Sizes& s, int64_t B, void* base) {
     }
     w.qkvz = static_cast<uint16_t*>(take(B * s.n_bf16 * 2));
     w.ba = static_cast<float*>(take(B * 2 * s.hv * 4));
-    w.qkv = static_cast<float*>(take(B * s.c_conv * 4));
+    w.qkv = static_cast<uint16_t*>(take(B * s.c_conv * 2));
     w.log_a = static_cast<float*>(take(B * s.hv * 4));
     w.b = static_cast<float*>(take(B * s.hv * 4));
     w.o = static_cast<float*>(take(B * s.c_v * 4));
@@ -238,7 +239,7 @@ int gdn_gemm_f32(const float* a, const float* b, int64_t M, int64_t Nn, int64_t 
 }
 
 int gdn_conv(const gdn_layer* layer, const uint16_t* qkvz, int64_t ld_qkvz, int64_t n_tokens, const float* conv_state,
-             const float* ba, int64_t ld_ba, float* qkv, float* log_a, float* b, void* stream) {
+             const float* ba, int64_t ld_ba, uint16_t* qkv, float* log_a, float* b, void* stream) {
     Sizes s;
     int r = check_layer(layer, &s);
     if (r) return r;
@@ -269,7 +270,7 @@ size_t gdn_delta_rule_scratch_size(const gdn_layer* layer, int64_t n_tokens) {
     return delta_scratch_bytes(static_cast<int>(s.hv), static_cast<int>(s.hk), static_cast<int>(s.d), n_tokens);
 }
 
-int gdn_delta_rule(const gdn_layer* layer, const float* qkv, const float* log_a, const float* b, int64_t n_tokens,
+int gdn_delta_rule(const gdn_layer* layer, const uint16_t* qkv, const float* log_a, const float* b, int64_t n_tokens,
                    const float* state_in, float* state_out, float* o, void* scratch, size_t scratch_bytes, void* stream) {
     Sizes s;
     int r = check_layer(layer, &s);
@@ -389,7 +390,12 @@ int gdn_sync_status(void* stream) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "gdn_sync_status");
     if (read_and_clear_gemm_error()) return fail(GDN_ETIMEOUT, "a bounded wait in the projection kernel ran out");
-    if (read_and_clear_delta_error()) return fail(GDN_ETIMEOUT, "a bounded wait in the delta-rule kernel ran out");
+    const int dcode = read_and_clear_delta_error();
+    const int ccode = read_and_clear_conv_error();
+    if (dcode == ERR_WAIT_TIMEOUT) return fail(GDN_ETIMEOUT, "a bounded wait in the delta-rule kernel ran out");
+    if (ccode == ERR_RANGE || dcode == ERR_RANGE)
+        return fail(GDN_ERANGE, "a %s value exceeded the fp16 operand range (|x| > 65504)",
+                    ccode == ERR_RANGE ? "q, k or v" : "delta-rule intermediate (T, A T, S, R or Delta)");
     return GDN_OK;
 }
 
@@ -408,7 +414,7 @@ std::mutex g_noalloc_mutex;
 void* g_noalloc_addr[kMaxDevices] = {};
 }  // namespace
 
-extern "C" int gdn_delta_rule_noalloc(const gdn_layer* layer, const float* qkv, const float* log_a, const float* b,
+extern "C" int gdn_delta_rule_noalloc(const gdn_layer* layer, const uint16_t* qkv, const float* log_a, const float* b,
                                       int64_t n_tokens, const float* state_in, float* state_out, float* o,
                                       void* stream) {
     Sizes s;

@@ -12,11 +12,13 @@
 // its channels in registers, so each raw input is read from HBM once (plus a
 // three-token halo per run).  The L2 norm of a q or k head is a warp
 // reduction.  Inputs are the bf16 projection outputs; arithmetic is fp32 and
-// the outputs are fp32 values rounded to tf32 (nearest), the precision the
-// recurrence's tensor-core products consume, so that kernel can copy them
-// into shared memory untouched.  (bf16 outputs would move o by ~0.3%, which
-// the int8 re-quantisation of the gated-norm output amplifies about threefold
-// in y; tf32 keeps o within ~5e-4.)
+// the outputs are fp16 (rounded to nearest): the recurrence's tensor-core
+// products take fp16 operands, so that kernel copies them into shared memory
+// untouched.  fp16 keeps 11 significant bits, as tf32 does (bf16 keeps 8 and
+// would move o by ~0.3%, which the int8 re-quantisation of the gated-norm
+// output amplifies about threefold in y); its range ends at 65504, and a value
+// beyond it is reported (ERR_RANGE in this unit's error word), never stored as
+// infinity silently.
 //
 // Gates (when not drawn directly): log a = -exp(A_log) * softplus(alpha +
 // dt_bias), b = sigmoid(beta), from the fp32 beta | alpha columns of the
@@ -24,6 +26,8 @@
 #include "common.cuh"
 
 namespace gdn {
+
+static __device__ int g_conv_error;
 
 constexpr int CONV_WARPS = 8;
 constexpr int CONV_TOKENS = 16;
@@ -42,7 +46,7 @@ struct ConvArgs {
     float q_scale;
     const float* conv_w;   // [c_conv][4]
     const float* tail;     // [c_conv][3]
-    float* out;            // [n][c_conv]
+    uint16_t* out;         // [n][c_conv] fp16
     // gates
     const float* ba;
     int64_t ld_ba;
@@ -122,13 +126,16 @@ __device__ __forceinline__ void conv_head_run(const ConvArgs& a, int head, int t
             for (int i = 0; i < CPL; ++i) y[i] *= r;
         }
         if (t < t1) {
-            float* dst = a.out + static_cast<int64_t>(t) * a.c_conv + c0;
+            uint16_t* dst = a.out + static_cast<int64_t>(t) * a.c_conv + c0;
+            bool over = false;
 #pragma unroll
-            for (int i = 0; i < CPL; ++i) y[i] = round_tf32(y[i]);
+            for (int i = 0; i < CPL; ++i) over |= !(fabsf(y[i]) <= 65504.0f);
+            if (over) atomicCAS(&g_conv_error, 0, ERR_RANGE);
+            const uint32_t p0 = f16x2_bits(y[0], y[1 % CPL]);
             if (CPL == 4)
-                *reinterpret_cast<float4*>(dst) = make_float4(y[0], y[1 % CPL], y[2 % CPL], y[3 % CPL]);
+                *reinterpret_cast<uint2*>(dst) = make_uint2(p0, f16x2_bits(y[2 % CPL], y[3 % CPL]));
             else
-                *reinterpret_cast<float2*>(dst) = make_float2(y[0], y[1 % CPL]);
+                *reinterpret_cast<uint32_t*>(dst) = p0;
         }
     }
 }
@@ -155,7 +162,7 @@ __global__ void __launch_bounds__(CONV_WARPS * 32, 3) conv_kernel(ConvArgs a) {
 }
 
 cudaError_t launch_conv(const gdn_layer& L, const uint16_t* qkvz, int64_t ld_qkvz, int64_t n, const float* tail,
-                        const float* ba, int64_t ld_ba, float* out, float* log_a, float* b, cudaStream_t st) {
+                        const float* ba, int64_t ld_ba, uint16_t* out, float* log_a, float* b, cudaStream_t st) {
     ConvArgs a;
     a.qkvz = qkvz;
     a.ld_qkvz = ld_qkvz;
@@ -210,6 +217,13 @@ cudaError_t launch_conv_state(const gdn_layer& L, const uint16_t* qkvz, int64_t 
     const int c_conv = 2 * L.n_qk_heads * L.dk + L.n_v_heads * L.dv;
     conv_state_kernel<<<(c_conv + 255) / 256, 256, 0, st>>>(qkvz, ld, static_cast<int>(n), c_conv, state);
     return cudaGetLastError();
+}
+
+int read_and_clear_conv_error() {
+    int v = 0, z = 0;
+    cudaMemcpyFromSymbol(&v, g_conv_error, sizeof(int));
+    if (v) cudaMemcpyToSymbol(g_conv_error, &z, sizeof(int));
+    return v;
 }
 
 }  // namespace gdn

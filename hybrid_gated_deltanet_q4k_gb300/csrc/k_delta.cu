@@ -19,28 +19,32 @@
 // which leaves S unchanged.
 //
 // Two kernels, both on the fifth-generation tensor cores (tcgen05.mma
-// kind::tf32, accumulators in TMEM, operands staged by TMA):
+// kind::f16 with fp16 operands, fp32 accumulators in TMEM, operands staged by
+// TMA):
 //   delta_prep   one CTA per (chunk, key head), all chunks in parallel: the
 //                Gram products Q K^T and K K^T once (the value heads of a key
 //                head share them), K^T for the state pass, then per value
 //                head gamma, the masked A, T = (I + L)^{-1} by recursive
 //                doubling on the block-triangular structure, and A T.  Writes
-//                [A T; T] and K^T (tf32, in the state pass's shared-memory
+//                [A T; T] and K^T (fp16, in the state pass's shared-memory
 //                operand image) and a gate table (gamma, e^gamma, b,
 //                e^{gamma_C - gamma}).
 //   delta_state  one CTA per (head, 32 rows of S): the chunks in order.  Rows
 //                of S evolve independently (row i only reads v[i]), so the
 //                rows split across CTAs with no communication.  The fp32 state
-//                stays in registers; its tf32 image is the B operand of the
+//                stays in registers; its fp16 image is the B operand of the
 //                next chunk's products.  A producer warp copies every operand
-//                of chunk c+1 into shared memory (TMA boxes of 64 tokens x 32
-//                floats with the 128-byte swizzle for Q, K, V; bulk copies of
+//                of chunk c+1 into shared memory (TMA boxes of 64 tokens x 64
+//                halfs with the 128-byte swizzle for Q, K, V; bulk copies of
 //                the prep images) as soon as chunk c has released its buffer.
-// Products take tf32 operands rounded to nearest (the conv writes q, k, v
-// already rounded; T, A, S, R, Delta are rounded where they are produced) and
-// accumulate in fp32; everything else is fp32.  Rounding every operand to
-// tf32 keeps o and S within ~5e-4 (relative L2) of the exact recurrence on
-// the test workloads.
+// Products take fp16 operands rounded to nearest (the conv writes q, k, v in
+// fp16; T, A T, S, R, Delta are rounded where they are produced) and
+// accumulate in fp32; everything else is fp32.  fp16 keeps the 11 significant
+// bits tf32 keeps, so o and S stay within ~5e-4 (relative L2) of the exact
+// recurrence on the test workloads.  Its range ends at 65504: q and k are unit
+// or smaller and A is bounded by |q||k|, but T, A T, S, R and Delta are
+// checked where they are rounded, and a value out of range sets ERR_RANGE in
+// this unit's error word (the result is then not to be used).
 #include "common.cuh"
 #include "tma.cuh"
 #include "tcgen05.cuh"
@@ -55,50 +59,61 @@ constexpr int DC = GDN_CHUNK;  // 64
 constexpr int DELTA_THREADS = 256;            // prep; compute warps of the state pass
 constexpr int STATE_THREADS = DELTA_THREADS + 64;  // + TMA producer warp + MMA warp
 constexpr int NV = 32;         // rows of S per state CTA
+constexpr float F16_MAX = 65504.0f;
 
 struct DeltaArgs {
-    const float* qkv;     // [n][c_conv] fp32: q | k | v
+    const uint16_t* qkv;  // [n][c_conv] fp16: q | k | v
     const float* log_a;   // [n][hv]
     const float* b;       // [n][hv]
     int n, hv, ratio, c_qk, c_conv, c_v;
     int nchunks;
-    float* TA;     // [nchunks][hv][2*DC][DC] [A T; T], tf32, in the swizzled operand image
+    uint16_t* TA;  // [nchunks][hv][2*DC][DC] [A T; T], fp16, in the swizzled operand image
     float* G;      // [nchunks][hv][DC][4]    gamma, e^gamma, b, e^{gamma_C - gamma}
-    float* KT;     // [nchunks][hk][D][DC]    K^T, in the swizzled operand image
+    uint16_t* KT;  // [nchunks][hk][D][DC]    K^T, fp16, in the swizzled operand image
     const float* state_in;  // [hv][D][D] or null
     float* state_out;
     float* o;      // [n][c_v]
 };
 
-__device__ __forceinline__ float tf32f(float x) { return round_tf32(x); }
+__device__ __forceinline__ uint16_t f16_bits(float x) { return __half_as_ushort(__float2half_rn(x)); }
+
+// Eight floats as eight fp16 (16 bytes, first value in the lowest half).
+__device__ __forceinline__ uint4 f16x8(const float (&v)[8]) {
+    return make_uint4(f16x2_bits(v[0], v[1]), f16x2_bits(v[2], v[3]), f16x2_bits(v[4], v[5]), f16x2_bits(v[6], v[7]));
+}
+
+// true when x is not a finite value fp16 can hold
+__device__ __forceinline__ bool f16_out_of_range(float x) { return !(fabsf(x) <= F16_MAX); }
 
 // ------------------------------------------------------------------ prep
 
 constexpr int PREP_MAX_RATIO = 8;  // value heads per key head handled by one CTA
 constexpr int PL = DC + 4;         // row pitch (floats) of L, T and the block temporaries
 
+__host__ __device__ constexpr int align1k(int x) { return (x + 1023) & ~1023; }
+
 template <int D>
 struct PrepSmem {
-    static constexpr int SLAB = DC * 128;          // 64 rows x 32 floats, 128-byte swizzle
-    static constexpr int NSLAB = D / 32;
+    static constexpr int SLAB = DC * 128;          // 64 rows x 64 halfs, 128-byte swizzle
+    static constexpr int NSLAB = D / 64;
     static constexpr int QK0 = 0;                  // [Q; K] [2*DC][D]: NSLAB slabs of Q rows then K rows (TMA)
     static constexpr int L0 = QK0 + NSLAB * 2 * SLAB;    // L  [DC][PL]
     static constexpr int T0 = L0 + DC * PL * 4;          // T  [DC][PL]
     static constexpr int W0 = T0 + DC * PL * 4;          // block temporaries [DC/2][PL]
     static constexpr int GL0 = W0 + DC / 2 * PL * 4;     // gamma [PREP_MAX_RATIO][DC]
     static constexpr int BB0 = GL0 + PREP_MAX_RATIO * DC * 4;  // b [PREP_MAX_RATIO][DC]
-    // 8 KB pieces 0-7 of operand and output images once the Gram product is
-    // done: the [Q; K] region, extended for D = 64 by 32 KB of its own.
-    static constexpr int EX0 = BB0 + PREP_MAX_RATIO * DC * 4;
-    static constexpr int B0 = EX0 + (8 - 2 * NSLAB) * SLAB;    // mbarriers: TMA, MMA
+    // 8 KB pieces 0-3 of operand and output images once the Gram product is
+    // done: the [Q; K] region, extended for D = 64 by 16 KB of its own.
+    static constexpr int EX0 = align1k(BB0 + PREP_MAX_RATIO * DC * 4);
+    static constexpr int B0 = EX0 + (4 - 2 * NSLAB) * SLAB;    // mbarriers: TMA, MMA
     static constexpr int MISC0 = B0 + 16;                      // TMEM base address
     static constexpr int BYTES = MISC0 + 16;
     static __device__ __forceinline__ int piece(int p) { return p < 2 * NSLAB ? QK0 + p * SLAB : EX0 + (p - 2 * NSLAB) * SLAB; }
-    // K^T staging: the Q rows of slab p (pieces 0, 2, 4, 6), written while the K rows are read
+    // K^T staging: key rows 64p .. 64p+63 in the Q rows of slab p, written while the K rows are read
     static __device__ __forceinline__ int kt_piece(int p) { return QK0 + p * 2 * SLAB; }
-    static constexpr int AI = 0;    // A operand [DC][DC] (pieces 0-1)
-    static constexpr int TTI = 2;   // T^T operand [DC][DC] (pieces 2-3)
-    static constexpr int OUTI = 4;  // [A T; T] output [2*DC][DC] (pieces 4-7: two 16 KB slabs)
+    static constexpr int AI = 0;    // A operand [DC][DC] (piece 0)
+    static constexpr int TTI = 1;   // T^T operand [DC][DC] (piece 1)
+    static constexpr int OUTI = 2;  // [A T; T] output [2*DC][DC] (pieces 2-3, one 16 KB slab)
 };
 
 // C = s * A B for blocks of the fp32 matrices in shared memory (row pitch PL):
@@ -131,13 +146,14 @@ __device__ __forceinline__ void block_mm(const float* a, const float* b, float* 
 //     columns 32(w/4) .. +31, in registers.
 //   - K^T, in the state pass's operand image, straight from the K rows.
 //   - For each value head (gates differ): the gate prefix sums gamma; the
-//     masked A (rows of lanes 0-63) to global memory; L (rows of lanes 64-127)
-//     into shared memory; T = (I + L)^-1 by recursive doubling on the block
-//     triangular structure:
+//     masked A (rows of lanes 0-63) as an fp16 operand image; L (rows of
+//     lanes 64-127) into shared memory; T = (I + L)^-1 by recursive doubling
+//     on the block triangular structure:
 //         16 x 16 diagonal blocks by substitution (one column per lane),
 //         inv [[A, 0], [C, B]] = [[A^-1, 0], [-B^-1 C A^-1, B^-1]]
 //     for 32 x 32 and then 64 x 64, every block product in fp32 on the CUDA
-//     cores; T (tf32-rounded) and the gate table to global memory.
+//     cores; A T on the tensor cores; [A T; T] (fp16) and the gate table to
+//     global memory.
 template <int D>
 __global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(const __grid_constant__ CUtensorMap qkv_map,
                                                                       DeltaArgs a) {
@@ -162,8 +178,8 @@ __global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(const __gr
         mbar_expect_tx(bars + 0, 2 * L::NSLAB * L::SLAB);
         for (int sl = 0; sl < L::NSLAB; ++sl) {
             unsigned char* dst = base + L::QK0 + sl * 2 * L::SLAB;
-            tma_load_2d_tile(dst, &qkv_map, bars + 0, hk * D + 32 * sl, t0);
-            tma_load_2d_tile(dst + L::SLAB, &qkv_map, bars + 0, a.c_qk + hk * D + 32 * sl, t0);
+            tma_load_2d_tile(dst, &qkv_map, bars + 0, hk * D + 64 * sl, t0);
+            tma_load_2d_tile(dst + L::SLAB, &qkv_map, bars + 0, a.c_qk + hk * D + 64 * sl, t0);
         }
     }
     if (warp == 0) t5::alloc(tslot, 128);
@@ -205,11 +221,11 @@ __global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(const __gr
             t5::fence_after();
             const uint32_t sb = smem_addr(base);
             const uint64_t dA = t5::desc_sw128(sb + L::QK0), dB = t5::desc_sw128(sb + L::QK0 + L::SLAB);
-            constexpr uint32_t ID = t5::idesc_tf32(128, DC);
+            constexpr uint32_t ID = t5::idesc_f16(128, DC);
 #pragma unroll
-            for (int k = 0; k < D / 8; ++k) {
+            for (int k = 0; k < D / 16; ++k) {
                 const uint64_t off = static_cast<uint64_t>((k >> 2) * (2 * L::SLAB >> 4) + 2 * (k & 3));
-                t5::mma_tf32(tmem, dA + off, dB + off, ID, k > 0 ? 1u : 0u);
+                t5::mma_f16(tmem, dA + off, dB + off, ID, k > 0 ? 1u : 0u);
             }
             t5::commit(bars + 1);
         }
@@ -246,33 +262,34 @@ __global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(const __gr
     }
 
     // ---- K^T image for the state pass, staged in the Q rows (free now) and
-    // written by bulk copies: piece (token slab ts, 64 key rows db) is 8 KB of
-    // the image.  Warp task (d-slab s, tokens 4g .. 4g+3), lane = d % 32.
+    // written by bulk copies: staging piece p holds key rows 64p .. 64p+63
+    // (8 KB of the image).  Task (key row d, tokens 8g .. 8g+7) is one
+    // 16-byte store; consecutive threads take consecutive d.
     {
-        for (int task = warp; task < L::NSLAB * (DC / 4); task += DELTA_THREADS / 32) {
-            const int s = task / (DC / 4), g4 = task % (DC / 4), t = 4 * g4;
-            const unsigned char* kp = base + L::QK0 + s * 2 * L::SLAB + L::SLAB;
-            const float4 v = make_float4(*reinterpret_cast<const float*>(kp + sw128_f32(t, lane)),
-                                         *reinterpret_cast<const float*>(kp + sw128_f32(t + 1, lane)),
-                                         *reinterpret_cast<const float*>(kp + sw128_f32(t + 2, lane)),
-                                         *reinterpret_cast<const float*>(kp + sw128_f32(t + 3, lane)));
-            const int d = 32 * s + lane, piece = (t >> 5) * (D / 64) + (d >> 6);
-            *reinterpret_cast<float4*>(base + L::kt_piece(piece) + sw128_f32(d & 63, t & 31)) = v;
+        for (int task = tid; task < D * (DC / 8); task += DELTA_THREADS) {
+            const int d = task % D, g8 = task / D, dl = d & 63;
+            const unsigned char* kp = base + L::QK0 + (d >> 6) * 2 * L::SLAB + L::SLAB;
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const uint32_t lo = *reinterpret_cast<const uint16_t*>(kp + sw128_f16(8 * g8 + 2 * e, dl));
+                const uint32_t hi = *reinterpret_cast<const uint16_t*>(kp + sw128_f16(8 * g8 + 2 * e + 1, dl));
+                w[e] = lo | (hi << 16);
+            }
+            *reinterpret_cast<uint4*>(base + L::kt_piece(d >> 6) + sw128_f16(dl, 8 * g8)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
         fence_proxy_async_smem();
         __syncthreads();
         if (tid == 0) {
-            float* kt = a.KT + (static_cast<int64_t>(chunk) * gridDim.y + hk) * D * DC;
-            for (int p = 0; p < L::NSLAB; ++p) {
-                const int ts = p / (D / 64), db = p % (D / 64);
-                bulk_store_1d(kt + ts * (D * 32) + db * (64 * 32), base + L::kt_piece(p), L::SLAB);
-            }
+            uint16_t* kt = a.KT + (static_cast<int64_t>(chunk) * gridDim.y + hk) * D * DC;
+            for (int p = 0; p < L::NSLAB; ++p) bulk_store_1d(kt + p * (64 * DC), base + L::kt_piece(p), L::SLAB);
             bulk_commit();
             bulk_wait_read();      // the region becomes the per-head staging
         }
         __syncthreads();
     }
 
+    bool bad = false;   // a T or A T value outside the fp16 range
     for (int j = 0; j < r; ++j) {
         const int h = hk * r + j;
         const int64_t cb = static_cast<int64_t>(chunk) * a.hv + h;
@@ -280,17 +297,18 @@ __global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(const __gr
         const float* bb = reinterpret_cast<const float*>(base + L::BB0) + j * DC;
         const float gi = gl[row];
         if (qrow) {
-            // A_ij = e^{gamma_i - gamma_j} q_i.k_j (j <= i): one 128-byte row of the swizzled image
-            unsigned char* arow = base + L::piece(L::AI + half) + row * 128;
+            // A_ij = e^{gamma_i - gamma_j} q_i.k_j (j <= i), |A_ij| <= |q_i||k_j| <= 1:
+            // half of one 128-byte row of the swizzled image
+            unsigned char* arow = base + L::piece(L::AI) + row * 128;
 #pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                float v[4];
+            for (int m = 0; m < 4; ++m) {
+                float v[8];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int c = c0 + 4 * m + e;
-                    v[e] = c <= row ? tf32f(__expf(gi - gl[c]) * g[4 * m + e]) : 0.f;
+                for (int e = 0; e < 8; ++e) {
+                    const int c = c0 + 8 * m + e;
+                    v[e] = c <= row ? __expf(gi - gl[c]) * g[8 * m + e] : 0.f;
                 }
-                *reinterpret_cast<float4*>(arow + (((m ^ (row & 7)) & 7) << 4)) = make_float4(v[0], v[1], v[2], v[3]);
+                *reinterpret_cast<uint4*>(arow + ((((c0 >> 3) + m) ^ (row & 7)) << 4)) = f16x8(v);
             }
         } else {
             // L_ij = b_i e^{gamma_i - gamma_j} k_i.k_j (j < i)
@@ -337,23 +355,24 @@ __global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(const __gr
         block_mm<32, 32, 32>(Ts + 32 * PL + 32, Ws, Ts + 32 * PL, -1.f, tid);
         __syncthreads();
         // T^T operand image (row m, column j = T_jm) and the T rows of the output
-        // (rows 64-127 of [A T; T]), tf32; thread -> row tid/4, 16 columns
+        // (rows 64-127 of [A T; T]), fp16; thread -> row tid/4, 16 columns
         {
             const int rr = tid >> 2, cq = 16 * (tid & 3);
-            unsigned char* ttrow = base + L::piece(L::TTI + (cq >> 5)) + rr * 128;
-            unsigned char* orow = base + L::piece(L::OUTI + 2 * (cq >> 5)) + (DC + rr) * 128;
+            unsigned char* ttrow = base + L::piece(L::TTI) + rr * 128;
+            unsigned char* orow = base + L::piece(L::OUTI) + (DC + rr) * 128;
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const int c = cq + 4 * m;
-                float v[4], w[4];
+            for (int m = 0; m < 2; ++m) {
+                const int c = cq + 8 * m;
+                float v[8], w[8];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    v[e] = c + e <= rr ? tf32f(Ts[rr * PL + c + e]) : 0.f;
-                    w[e] = c + e >= rr ? tf32f(Ts[(c + e) * PL + rr]) : 0.f;
+                for (int e = 0; e < 8; ++e) {
+                    v[e] = c + e <= rr ? Ts[rr * PL + c + e] : 0.f;
+                    w[e] = c + e >= rr ? Ts[(c + e) * PL + rr] : 0.f;
+                    bad |= f16_out_of_range(v[e]);
                 }
-                const int ch = ((((c & 31) >> 2) ^ (rr & 7)) & 7) << 4;
-                *reinterpret_cast<float4*>(orow + ch) = make_float4(v[0], v[1], v[2], v[3]);
-                *reinterpret_cast<float4*>(ttrow + ch) = make_float4(w[0], w[1], w[2], w[3]);
+                const int ch = (((c >> 3) ^ (rr & 7)) & 7) << 4;
+                *reinterpret_cast<uint4*>(orow + ch) = f16x8(v);
+                *reinterpret_cast<uint4*>(ttrow + ch) = f16x8(w);
             }
         }
         if (tid < DC) {
@@ -369,12 +388,9 @@ __global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(const __gr
             t5::fence_after();
             const uint32_t sb = smem_addr(base);
             const uint64_t dA = t5::desc_sw128(sb + L::piece(L::AI)), dB = t5::desc_sw128(sb + L::piece(L::TTI));
-            constexpr uint32_t ID = t5::idesc_tf32(64, DC);
+            constexpr uint32_t ID = t5::idesc_f16(64, DC);
 #pragma unroll
-            for (int k = 0; k < DC / 8; ++k) {
-                const uint64_t off = static_cast<uint64_t>((k >> 2) * (L::SLAB >> 4) + 2 * (k & 3));
-                t5::mma_tf32(tmem + 64, dA + off, dB + off, ID, k > 0 ? 1u : 0u);
-            }
+            for (int k = 0; k < DC / 16; ++k) t5::mma_f16(tmem + 64, dA + 2 * k, dB + 2 * k, ID, k > 0 ? 1u : 0u);
             t5::commit(bars + 1);
         }
         if (!mbar_wait_bounded(bars + 1, (j + 1) & 1, &g_delta_error, ERR_WAIT_TIMEOUT)) mok = false;
@@ -386,24 +402,31 @@ __global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(const __gr
             t5::ld32(tmem + (static_cast<uint32_t>(32 * q) << 16) + 64 + c0, at);
             if (lane < 16) {
                 const int ri = 16 * q + lane;
-                unsigned char* orow = base + L::piece(L::OUTI + 2 * half) + ri * 128;
+                unsigned char* orow = base + L::piece(L::OUTI) + ri * 128;
 #pragma unroll
-                for (int m = 0; m < 8; ++m)
-                    *reinterpret_cast<float4*>(orow + (((m ^ (ri & 7)) & 7) << 4)) =
-                        make_float4(tf32f(at[4 * m]), tf32f(at[4 * m + 1]), tf32f(at[4 * m + 2]), tf32f(at[4 * m + 3]));
+                for (int m = 0; m < 4; ++m) {
+                    float v[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        v[e] = at[8 * m + e];
+                        bad |= f16_out_of_range(v[e]);
+                    }
+                    *reinterpret_cast<uint4*>(orow + ((((c0 >> 3) + m) ^ (ri & 7)) << 4)) = f16x8(v);
+                }
             }
         }
         fence_proxy_async_smem();
         t5::fence_before();
         mok = __syncthreads_and(mok);
         if (tid == 0 && mok) {
-            bulk_store_1d(a.TA + cb * 2 * DC * DC, base + L::piece(L::OUTI), 4 * L::SLAB);
+            bulk_store_1d(a.TA + cb * 2 * DC * DC, base + L::piece(L::OUTI), 2 * L::SLAB);
             bulk_commit();
             bulk_wait_read();      // the staging is rewritten by the next head
         }
         __syncthreads();   // before the next head overwrites L, T and the staging
         if (!mok) break;
     }
+    if (bad) atomicCAS(&g_delta_error, 0, ERR_RANGE);
     if (tid == 0) bulk_wait_all();
     t5::fence_before();
     __syncthreads();
@@ -414,25 +437,24 @@ __global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(const __gr
 
 // Shared-memory layout of the state pass (byte offsets; every operand base is
 // 1024-byte aligned, as the 128-byte swizzle requires).  Operands are slabs of
-// rows of 32 fp32 (128 bytes) with the 128-byte swizzle, K-major for the
+// rows of 64 fp16 (128 bytes) with the 128-byte swizzle, K-major for the
 // tensor cores: the image a 2-D TMA box with SWIZZLE_128B writes, and the one
-// delta_prep writes for T, A and K^T.
+// delta_prep writes for [A T; T] and K^T.
 template <int D>
 struct StateSmem {
-    static constexpr int SLAB = DC * 128;          // 64 rows x 32 floats
-    static constexpr int NSLAB = D / 32;
+    static constexpr int SLAB = DC * 128;          // 64 rows x 64 halfs
+    static constexpr int NSLAB = D / 64;
     static constexpr int QK_SLAB = 2 * SLAB;       // Q rows 0-63, K rows 64-127
-    static constexpr int SOP = NV * 128;           // 32 rows x 32 floats
-    static constexpr int KT_SLAB = D * 128;        // D rows x 32 floats
-    static constexpr int KT_BYTES = 2 * KT_SLAB;   // one K^T [D][DC]
+    static constexpr int SOP = NV * 128;           // 32 rows x 64 halfs
+    static constexpr int KT_BYTES = D * 128;       // one K^T [D][DC]
     static constexpr int QK0 = 0;                  // [Q; K] [2*DC][D]  (TMA)
     static constexpr int KT0 = QK0 + NSLAB * QK_SLAB;   // K^T [2][D][DC] (bulk copies)
     static constexpr int TA0 = KT0 + 2 * KT_BYTES; // [A T; T] [2*DC][DC] (bulk copy of the prep image)
-    static constexpr int V0 = TA0 + 2 * QK_SLAB;   // V [DC][NV]        (TMA)
-    static constexpr int S0 = V0 + SLAB;           // S [NV][D]         tf32 operand of X, Y
+    static constexpr int V0 = TA0 + QK_SLAB;       // V [DC][64]        (TMA; this CTA's NV columns at i0 % 64)
+    static constexpr int S0 = V0 + SLAB;           // S [NV][D]         fp16 operand of X, Y
     static constexpr int R0 = S0 + NSLAB * SOP;    // R^T [NV][DC]
-    static constexpr int E0 = R0 + 2 * SOP;        // Delta~^T [NV][DC]
-    static constexpr int G0 = E0 + 2 * SOP;        // gate table [2][DC] x (gamma, e^gamma, b, e^{gamma_C-gamma})
+    static constexpr int E0 = R0 + SOP;            // Delta~^T [NV][DC]
+    static constexpr int G0 = E0 + SOP;            // gate table [2][DC] x (gamma, e^gamma, b, e^{gamma_C-gamma})
     static constexpr int B0 = G0 + 2 * DC * 16;    // mbarriers
     static constexpr int NBAR = 14;
     static constexpr int MISC0 = B0 + NBAR * 8;    // TMEM base address, abort flag
@@ -482,24 +504,25 @@ __device__ __forceinline__ void mbar_arrive_cta(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
-// Issue the k steps [0, NK) of one MMA chain; a K step is 8 fp32 = 32 bytes,
+// Issue the k steps [0, NK) of one MMA chain; a K step is 16 fp16 = 32 bytes,
 // four per 128-byte swizzle row, then the next slab.
 template <int NK, int A_SLAB, int B_SLAB>
 __device__ __forceinline__ void mma_chain(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc) {
 #pragma unroll
     for (int k = 0; k < NK; ++k)
-        t5::mma_tf32(d_tmem, adesc + static_cast<uint64_t>((k >> 2) * (A_SLAB >> 4) + 2 * (k & 3)),
-                     bdesc + static_cast<uint64_t>((k >> 2) * (B_SLAB >> 4) + 2 * (k & 3)), idesc, k > 0 ? 1u : 0u);
+        t5::mma_f16(d_tmem, adesc + static_cast<uint64_t>((k >> 2) * (A_SLAB >> 4) + 2 * (k & 3)),
+                    bdesc + static_cast<uint64_t>((k >> 2) * (B_SLAB >> 4) + 2 * (k & 3)), idesc, k > 0 ? 1u : 0u);
 }
 
 // One CTA per (value head, NV rows of S); 320 threads:
 //   warps 0-7  compute.  Warp w reads TMEM lanes 32*(w%4) .. +31 and columns
 //              16*(w/4) .. +15 of each 32-column accumulator.
-//   warp 8     producer: TMA boxes of Q, K, V; bulk copies of K^T, T, A, gates.
+//   warp 8     producer: TMA boxes of Q, K, V; bulk copies of K^T, [A T; T],
+//              gates.
 //   warp 9     TMEM owner and MMA issuer: meets the compute warps at a named
 //              barrier once they have written an operand, then issues (one
 //              thread).
-// Per chunk, with S the NV x D slice of the state (tf32 operands, fp32 sums):
+// Per chunk, with S the NV x D slice of the state (fp16 operands, fp32 sums):
 //   MMA  [Y; X] = [Q; K] S^T          (M = 128: Y in lanes 0-63, X in 64-127)
 //   warps 2,3,6,7 (lanes 64-127)  R = diag(b)(V - diag(e^gamma) X) -> R^T
 //   MMA  [Z; Delta] = [A T; T] R      (M = 128: Z = A Delta in lanes 0-63,
@@ -507,7 +530,7 @@ __device__ __forceinline__ void mma_chain(uint32_t d_tmem, uint64_t adesc, uint6
 //        extra product)
 //   warps 2,3,6,7  Delta~^T = (diag(e^{gamma_C-gamma}) Delta)^T
 //   MMA  U = K^T Delta~               (M = D: row d in lane d, or 32*(d/16)+d%16)
-//   warps  S <- e^{gamma_C} S + U in fp32 registers, its tf32 image -> S
+//   warps  S <- e^{gamma_C} S + U in fp32 registers, its fp16 image -> S
 //   MMA  next chunk's [Q; K] S^T
 //   warps 0,1,4,5 (lanes 0-63)  O = diag(e^gamma) Y + Z, while it runs.
 // The state's chain per chunk is four dependent steps (X, R, Delta, U); the
@@ -552,8 +575,8 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
                 mbar_expect_tx(bars + F_QK, 2 * L::NSLAB * L::SLAB);
                 for (int sl = 0; sl < L::NSLAB; ++sl) {
                     unsigned char* dst = base + L::QK0 + sl * L::QK_SLAB;
-                    tma_load_2d_tile(dst, &qkv_map, bars + F_QK, hk * D + 32 * sl, c * DC);
-                    tma_load_2d_tile(dst + L::SLAB, &qkv_map, bars + F_QK, a.c_qk + hk * D + 32 * sl, c * DC);
+                    tma_load_2d_tile(dst, &qkv_map, bars + F_QK, hk * D + 64 * sl, c * DC);
+                    tma_load_2d_tile(dst + L::SLAB, &qkv_map, bars + F_QK, a.c_qk + hk * D + 64 * sl, c * DC);
                 }
                 const int kb = c & 1;
                 if (c >= 2 && !state_wait(bars + E_KT0 + kb, ((c - 2) >> 1) & 1, abort)) break;
@@ -563,17 +586,17 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
                              bars + F_KT0 + kb);
                 if (c >= 1 && !state_wait(bars + E_V, pp, abort)) break;
                 mbar_expect_tx(bars + F_V, L::SLAB + DC * 16);
-                tma_load_2d_tile(base + L::V0, &qkv_map, bars + F_V, 2 * a.c_qk + h * D + i0, c * DC);
+                tma_load_2d_tile(base + L::V0, &qkv_map, bars + F_V, 2 * a.c_qk + h * D + (i0 & ~63), c * DC);
                 bulk_load_1d(base + L::G0 + (c & 1) * DC * 16, a.G + cb(c) * DC * 4, DC * 16, bars + F_V);
                 if (c >= 1 && !state_wait(bars + E_TA, pp, abort)) break;
-                mbar_expect_tx(bars + F_TA, 2 * L::QK_SLAB);
-                bulk_load_1d(base + L::TA0, a.TA + cb(c) * 2 * DC * DC, 2 * L::QK_SLAB, bars + F_TA);
+                mbar_expect_tx(bars + F_TA, L::QK_SLAB);
+                bulk_load_1d(base + L::TA0, a.TA + cb(c) * 2 * DC * DC, L::QK_SLAB, bars + F_TA);
             }
         }
     } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
-        constexpr uint32_t ID128 = t5::idesc_tf32(128, NV);
-        constexpr uint32_t IDU = t5::idesc_tf32(D, NV);
+        constexpr uint32_t ID128 = t5::idesc_f16(128, NV);
+        constexpr uint32_t IDU = t5::idesc_f16(D, NV);
         const uint64_t dQK = t5::desc_sw128(sbase + L::QK0), dS = t5::desc_sw128(sbase + L::S0);
         const uint64_t dTA = t5::desc_sw128(sbase + L::TA0), dR = t5::desc_sw128(sbase + L::R0);
         const uint64_t dE = t5::desc_sw128(sbase + L::E0);
@@ -589,21 +612,21 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
             const uint32_t ph = c & 1;
             nb_sync(NB_S);                      // S of chunk c written
             if (leader && ready(F_QK, ph)) {
-                mma_chain<D / 8, L::QK_SLAB, L::SOP>(tmem + TM_XY + 32 * ph, dQK, dS, ID128);
+                mma_chain<D / 16, L::QK_SLAB, L::SOP>(tmem + TM_XY + 32 * ph, dQK, dS, ID128);
                 t5::commit(bars + M_XY);
                 t5::commit(bars + E_QK);
             }
             __syncwarp();
             nb_sync(NB_R);                      // R^T written
             if (leader && ready(F_TA, ph)) {
-                mma_chain<DC / 8, L::QK_SLAB, L::SOP>(tmem + TM_DZ, dTA, dR, ID128);
+                mma_chain<DC / 16, L::QK_SLAB, L::SOP>(tmem + TM_DZ, dTA, dR, ID128);
                 t5::commit(bars + M_DZ);
                 t5::commit(bars + E_TA);
             }
             __syncwarp();
             nb_sync(NB_D);                      // Delta~^T written
             if (leader && ready(F_KT0 + ph, (c >> 1) & 1)) {
-                mma_chain<DC / 8, L::KT_SLAB, L::SOP>(tmem + TM_U, dKT + ph * (L::KT_BYTES >> 4), dE, IDU);
+                mma_chain<DC / 16, L::KT_BYTES, L::SOP>(tmem + TM_U, dKT + ph * (L::KT_BYTES >> 4), dE, IDU);
                 t5::commit(bars + M_U);
                 t5::commit(bars + E_KT0 + ph);
             }
@@ -626,6 +649,8 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
         // key-dimension row d of U owned by this thread (all lanes for D = 128, lanes 0-15 for D = 64)
         const bool own_d = D == 128 ? true : act;
         const int d = D == 128 ? 32 * q + lane : 16 * q + lane;
+        const int vc = (i0 & 63) + v0;          // first V column of this warp in the 64-column V box
+        bool bad = false;                       // an S, R or Delta~ value outside the fp16 range
 
         float S[16];
 #pragma unroll
@@ -633,17 +658,22 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
             S[v] = (own_d && a.state_in) ? a.state_in[(static_cast<int64_t>(h) * D + i0 + v0 + v) * D + d] : 0.f;
         auto write_s = [&]() {
             if (own_d) {
-                unsigned char* sp = base + L::S0 + (d >> 5) * L::SOP;
+                unsigned char* sp = base + L::S0 + (d >> 6) * L::SOP;
 #pragma unroll
-                for (int v = 0; v < 16; ++v)
-                    *reinterpret_cast<float*>(sp + sw128_f32(v0 + v, d & 31)) = tf32f(S[v]);
+                for (int v = 0; v < 16; ++v) {
+                    bad |= f16_out_of_range(S[v]);
+                    *reinterpret_cast<uint16_t*>(sp + sw128_f16(v0 + v, d & 63)) = f16_bits(S[v]);
+                }
             }
         };
-        // column t of an [NV][DC] operand (R^T, Delta^T, Delta~^T), rows v0 .. v0+15
+        // column t of an [NV][DC] operand (R^T, Delta~^T), rows v0 .. v0+15
         auto write_col = [&](int off, int t, const float (&x)[16]) {
-            unsigned char* cp = base + off + (t >> 5) * L::SOP;
+            unsigned char* cp = base + off;
 #pragma unroll
-            for (int v = 0; v < 16; ++v) *reinterpret_cast<float*>(cp + sw128_f32(v0 + v, t & 31)) = x[v];
+            for (int v = 0; v < 16; ++v) {
+                bad |= f16_out_of_range(x[v]);
+                *reinterpret_cast<uint16_t*>(cp + sw128_f16(v0 + v, t)) = f16_bits(x[v]);
+            }
         };
         // the operands this thread wrote go to the tensor cores
         auto handover = [&](int id) {
@@ -677,12 +707,16 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
                 t5::ld16(tl + TM_XY + 32 * ph, x);
                 const unsigned char* vp = base + L::V0;
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const float4 vv = *reinterpret_cast<const float4*>(vp + sw128_f32(tok, v0 + 4 * m));
-                    x[4 * m + 0] = tf32f(gt.z * (vv.x - gt.y * x[4 * m + 0]));
-                    x[4 * m + 1] = tf32f(gt.z * (vv.y - gt.y * x[4 * m + 1]));
-                    x[4 * m + 2] = tf32f(gt.z * (vv.z - gt.y * x[4 * m + 2]));
-                    x[4 * m + 3] = tf32f(gt.z * (vv.w - gt.y * x[4 * m + 3]));
+                for (int m = 0; m < 2; ++m) {
+                    const uint4 raw = *reinterpret_cast<const uint4*>(vp + sw128_f16(tok, vc + 8 * m));
+                    const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 vv = __half22float2(*reinterpret_cast<const __half2*>(&w4[e]));
+                        const int i = 8 * m + 2 * e;
+                        x[i] = gt.z * (vv.x - gt.y * x[i]);
+                        x[i + 1] = gt.z * (vv.y - gt.y * x[i + 1]);
+                    }
                 }
                 write_col(L::R0, tok, x);
             }
@@ -694,7 +728,7 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
                 float dl[16];
                 t5::ld16(tl + TM_DZ, dl);
 #pragma unroll
-                for (int v = 0; v < 16; ++v) dl[v] = tf32f(dl[v] * gt.w);
+                for (int v = 0; v < 16; ++v) dl[v] *= gt.w;
                 write_col(L::E0, tok, dl);
             }
             handover(NB_D);
@@ -728,6 +762,7 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
 #pragma unroll
             for (int v = 0; v < 16; ++v) a.state_out[(static_cast<int64_t>(h) * D + i0 + v0 + v) * D + d] = S[v];
         }
+        if (bad) atomicCAS(&g_delta_error, 0, ERR_RANGE);
     }
 
     if (*abort && tid == 0) {
@@ -744,10 +779,12 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
     }
 }
 
+// Scratch per chunk: [A T; T] (fp16) and the gate table per value head, K^T
+// (fp16) per key head; every piece is a multiple of 1 KB.
 size_t delta_scratch_bytes(int hv, int hk, int d, int64_t n) {
     const int64_t nch = (n + DC - 1) / DC;
-    const int64_t per = static_cast<int64_t>(hv) * DC * (2 * DC + 4) + static_cast<int64_t>(hk) * d * DC;
-    return static_cast<size_t>(nch * per) * sizeof(float);
+    const int64_t per = static_cast<int64_t>(hv) * (2 * DC * DC * 2 + DC * 16) + static_cast<int64_t>(hk) * d * DC * 2;
+    return static_cast<size_t>(nch * per);
 }
 
 static PFN_cuTensorMapEncodeTiled_v12000 delta_map_encoder() {
@@ -763,15 +800,15 @@ static PFN_cuTensorMapEncodeTiled_v12000 delta_map_encoder() {
     return fn;
 }
 
-// fp32 qkv [n][c_conv]: boxes of DC tokens x 32 floats, 128-byte swizzle, zero fill.
-static bool make_qkv_map(CUtensorMap* map, const float* qkv, int64_t n, int c_conv) {
+// fp16 qkv [n][c_conv]: boxes of DC tokens x 64 halfs, 128-byte swizzle, zero fill.
+static bool make_qkv_map(CUtensorMap* map, const uint16_t* qkv, int64_t n, int c_conv) {
     auto enc = delta_map_encoder();
     if (!enc) return false;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(c_conv), static_cast<cuuint64_t>(n)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(c_conv) * 4};
-    cuuint32_t box[2] = {32, static_cast<cuuint32_t>(DC)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(c_conv) * 2};
+    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(DC)};
     cuuint32_t estr[2] = {1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(qkv), dims, strides, box, estr,
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(qkv), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -802,7 +839,7 @@ static cudaError_t launch_delta_d(DeltaArgs& a, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_delta(const gdn_layer& L, const float* qkv, const float* log_a, const float* b, int64_t n,
+cudaError_t launch_delta(const gdn_layer& L, const uint16_t* qkv, const float* log_a, const float* b, int64_t n,
                          const float* state_in, float* state_out, float* o, void* scratch, cudaStream_t st) {
     DeltaArgs a;
     const int d = L.dk;
@@ -817,10 +854,10 @@ cudaError_t launch_delta(const gdn_layer& L, const float* qkv, const float* log_
     a.c_conv = 2 * a.c_qk + a.c_v;
     a.nchunks = static_cast<int>((n + DC - 1) / DC);
     const int64_t nch = a.nchunks;
-    float* base = static_cast<float*>(scratch);
-    a.TA = base;
-    a.G = a.TA + nch * a.hv * 2 * DC * DC;
-    a.KT = a.G + nch * a.hv * DC * 4;
+    unsigned char* base = static_cast<unsigned char*>(scratch);
+    a.TA = reinterpret_cast<uint16_t*>(base);
+    a.G = reinterpret_cast<float*>(base + nch * a.hv * 2 * DC * DC * 2);
+    a.KT = reinterpret_cast<uint16_t*>(base + nch * a.hv * (2 * DC * DC * 2 + DC * 16));
     a.state_in = state_in;
     a.state_out = state_out;
     a.o = o;

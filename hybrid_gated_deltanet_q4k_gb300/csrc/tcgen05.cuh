@@ -31,12 +31,19 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int m, int n) {
            (static_cast<uint32_t>(m >> 4) << 24);
 }
 
+// Instruction descriptor for kind::f16 with fp16 A and B: D fp32 (bits 4-5 =
+// 1), A and B fp16 (bits 7-9 and 10-12 = 0), both K-major, N>>3 at bits
+// 17-22, M>>4 at bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_f16(int m, int n) {
+    return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+}
+
 // Shared-memory descriptor of a K-major operand stored with the 128-byte
 // swizzle (rows of 128 bytes, 8-row groups 1024 bytes apart): start address
 // >> 4 (bits 0-13), leading offset 16 B (unused for this layout), stride
 // 1024 B >> 4 (bits 32-45), descriptor version 1 (bit 46), swizzle mode 2
 // (bits 61-63).  A K step of 32 bytes inside the swizzle row adds 2 to the
-// start field.
+// start field (8 fp32 or 16 fp16: one MMA K step of either kind).
 __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
     return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(1) << 16) |
            (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
@@ -50,6 +57,18 @@ __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// D[tmem] (+)= A * B^T with fp16 operands (K = 16 per instruction), one
+// elected thread.
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }

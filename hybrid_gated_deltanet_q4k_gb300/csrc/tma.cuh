@@ -101,4 +101,10 @@ __host__ __device__ __forceinline__ uint32_t sw128_f32(int r, int c) {
     return static_cast<uint32_t>(r * 128 + ((((c >> 2) ^ (r & 7)) & 7) << 4) + ((c & 3) << 2));
 }
 
+// Byte offset of fp16 element (r, c), c < 64, in an image of 128-byte rows
+// (64 halfs) written with the 128-byte swizzle.
+__host__ __device__ __forceinline__ uint32_t sw128_f16(int r, int c) {
+    return static_cast<uint32_t>(r * 128 + ((((c >> 3) ^ (r & 7)) & 7) << 4) + ((c & 7) << 1));
+}
+
 }  // namespace gdn

@@ -15,7 +15,7 @@ from . import build as _build
 
 c_int32, c_int64, c_float, c_void_p, c_size_t = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
 
-GDN_OK, GDN_EINVAL, GDN_ENOMEM, GDN_ECUDA, GDN_ETIMEOUT = 0, -1, -2, -3, -4
+GDN_OK, GDN_EINVAL, GDN_ENOMEM, GDN_ECUDA, GDN_ETIMEOUT, GDN_ERANGE = 0, -1, -2, -3, -4, -5
 GDN_W_Q4K, GDN_W_F32 = 0, 1
 GDN_CHUNK = 64
 GDN_N_STAGE_EVENTS = 8

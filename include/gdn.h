@@ -54,6 +54,7 @@ extern "C" {
 #define GDN_ENOMEM (-2)   /* workspace smaller than one ubatch of tokens needs */
 #define GDN_ECUDA (-3)    /* a CUDA call or kernel launch failed */
 #define GDN_ETIMEOUT (-4) /* a bounded device-side wait ran out; the kernel returned early */
+#define GDN_ERANGE (-5)   /* a value beyond the fp16 operand range (|x| > 65504) reached the recurrence */
 
 #define GDN_W_Q4K 0 /* weights are GGUF Q4_K superblocks, activations bf16 */
 #define GDN_W_F32 1 /* weights and activations fp32, no quantisation anywhere */
@@ -151,8 +152,10 @@ int gdn_prefill(const gdn_layer *layer, const void *x, int64_t n_tokens, const f
 
 /*
  * gdn_sync_status -- wait for `stream`, then report (and clear) the device
- * error word the kernels set when a bounded wait runs out: GDN_OK,
- * GDN_ETIMEOUT or GDN_ECUDA (a CUDA error from the stream).
+ * error words the kernels set: GDN_OK, GDN_ETIMEOUT (a bounded wait ran out),
+ * GDN_ERANGE (a value beyond the fp16 operand range of the recurrence: the
+ * results of that call are not valid) or GDN_ECUDA (a CUDA error from the
+ * stream).
  */
 int gdn_sync_status(void *stream);
 
@@ -218,15 +221,16 @@ int gdn_gemm_f32(const float *a, const float *b, int64_t M, int64_t Nn, int64_t 
 /*
  * gdn_conv -- step 2: causal 4-tap depthwise conv over the q|k|v channels of
  * the projection (qkvz: bf16 [N][ld_qkvz], channel c at column c), SiLU, L2
- * norm of each q and k head (q then scaled by q_scale), written as fp32
- * values rounded to tf32 (nearest; the precision gdn_delta_rule's tensor
- * cores consume) into qkv [N][C_conv] (16-byte aligned).  conv_state [C_conv][3] holds the raw inputs before token 0
+ * norm of each q and k head (q then scaled by q_scale), written as fp16
+ * (rounded to nearest; the operand type of gdn_delta_rule's tensor cores)
+ * into qkv [N][C_conv] (16-byte aligned); a value beyond the fp16 range is
+ * reported as GDN_ERANGE by gdn_sync_status.  conv_state [C_conv][3] holds the raw inputs before token 0
  * (read only here).  When gates are not drawn (layer gate pointers NULL) it
  * also writes log_a, b [N][Hv] from beta | alpha (ba: fp32 [N][ld_ba],
  * beta at column h, alpha at column Hv + h); otherwise ba, log_a, b unused.
  */
 int gdn_conv(const gdn_layer *layer, const uint16_t *qkvz, int64_t ld_qkvz, int64_t n_tokens,
-             const float *conv_state, const float *ba, int64_t ld_ba, float *qkv, float *log_a,
+             const float *conv_state, const float *ba, int64_t ld_ba, uint16_t *qkv, float *log_a,
              float *b, void *stream);
 
 /*
@@ -241,13 +245,15 @@ int gdn_conv_state_update(const gdn_layer *layer, const uint16_t *qkvz, int64_t 
  * gdn_delta_rule -- step 3: the gated delta rule
  *     S_t = a_t S_{t-1} (I - b_t k_t k_t^T) + b_t v_t k_t^T,   o_t = S_t q_t
  * per value head, in chunks of GDN_CHUNK tokens (WY/UT form), products on
- * tensor cores with tf32 operands and fp32 accumulation; the state stays
- * fp32.  qkv: fp32 [N][C_conv] as written by gdn_conv (q, k and v are read at
- * tf32 precision: pass them rounded to tf32, as gdn_conv writes them); log_a, b: fp32 [N][Hv]; state_in /
- * state_out fp32 [Hv][dv][dk] (state_in NULL = zero; may alias); o: fp32
- * [N][C_v].  scratch: device bytes >= gdn_delta_rule_scratch_size(layer, N).
+ * tensor cores with fp16 operands and fp32 accumulation; the state stays
+ * fp32.  qkv: fp16 [N][C_conv] as written by gdn_conv (16-byte aligned);
+ * log_a, b: fp32 [N][Hv]; state_in / state_out fp32 [Hv][dv][dk] (state_in
+ * NULL = zero; may alias); o: fp32 [N][C_v].  scratch: 16-byte aligned device
+ * bytes >= gdn_delta_rule_scratch_size(layer, N).  An intermediate outside
+ * the fp16 range (T, A T, the state's fp16 image, R or Delta) is reported as
+ * GDN_ERANGE by gdn_sync_status; o and the state are then not to be used.
  */
-int gdn_delta_rule(const gdn_layer *layer, const float *qkv, const float *log_a, const float *b,
+int gdn_delta_rule(const gdn_layer *layer, const uint16_t *qkv, const float *log_a, const float *b,
                    int64_t n_tokens, const float *state_in, float *state_out, float *o,
                    void *scratch, size_t scratch_bytes, void *stream);
 size_t gdn_delta_rule_scratch_size(const gdn_layer *layer, int64_t n_tokens);
@@ -264,7 +270,7 @@ size_t gdn_delta_rule_scratch_size(const gdn_layer *layer, int64_t n_tokens);
  *     library holds until the process exits.  The call itself allocates
  *     nothing (no cudaMalloc, no cudaFree, no allocating library routine).
  *   - A call whose gdn_delta_rule_scratch_size(layer, n_tokens) exceeds that
- *     size returns GDN_EINVAL with a message (e.g. at most 1984 tokens, 31
+ *     size returns GDN_EINVAL with a message (e.g. at most 3904 tokens, 61
  *     chunks of 64, for 32 value heads over 16 key heads of d = 128).
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
@@ -276,7 +282,7 @@ size_t gdn_delta_rule_scratch_size(const gdn_layer *layer, int64_t n_tokens);
  * Arguments, layouts and results are those of gdn_delta_rule.
  */
 #define GDN_NOALLOC_SCRATCH_BYTES (48u << 20)
-int gdn_delta_rule_noalloc(const gdn_layer *layer, const float *qkv, const float *log_a, const float *b,
+int gdn_delta_rule_noalloc(const gdn_layer *layer, const uint16_t *qkv, const float *log_a, const float *b,
                            int64_t n_tokens, const float *state_in, float *state_out, float *o,
                            void *stream);
 

@@ -40,12 +40,14 @@ def oracle_params(spec, layer: dict, eps=1e-6) -> dict:
     return p
 
 
-def tf32_round(x) -> np.ndarray:
-    """float32 values rounded to tf32 (10 explicit mantissa bits), nearest, ties away from zero."""
-    u = np.array(x, dtype=np.float32, copy=True).view(np.uint32)
-    u += np.uint32(0x1000)
-    u &= np.uint32(0xFFFFE000)
-    return u.view(np.float32)
+def f16_round(x) -> np.ndarray:
+    """Values rounded to IEEE fp16 (nearest even), returned as float32 (exact)."""
+    return np.asarray(x).astype(np.float16).astype(np.float32)
+
+
+def f16_dev(a: np.ndarray) -> torch.Tensor:
+    """fp16 device tensor of the values (rounded to nearest even)."""
+    return torch.from_numpy(np.ascontiguousarray(np.asarray(a).astype(np.float16))).to(DEV)
 
 
 def rel_l2(a, b) -> float:

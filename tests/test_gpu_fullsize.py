@@ -60,7 +60,7 @@ def test_h4096_n32768_prefill():
     L.gdn_gemm_codes(gl.ptr(xc), gl.ptr(sx), gl.ptr(wc_in), gl.ptr(ws_in), n, r_in, H, gl.ptr(qkvz), nbf, nbf,
                      gl.ptr(ba), 2 * hv, st)
     conv2 = torch.zeros(c_conv, 3, dtype=torch.float32, device=DEV)
-    qkv = torch.empty(n, c_conv, dtype=torch.float32, device=DEV)
+    qkv = torch.empty(n, c_conv, dtype=torch.float16, device=DEV)
     L.gdn_conv(sp, gl.ptr(qkvz), nbf, n, gl.ptr(conv2), gl.ptr(ba), 2 * hv, gl.ptr(qkv), 0, 0, st)
     L.gdn_conv_state_update(sp, gl.ptr(qkvz), nbf, n, gl.ptr(conv2), st)
     nbytes = L.gdn_delta_rule_scratch_size(sp, n)

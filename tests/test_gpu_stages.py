@@ -25,7 +25,7 @@ from hybrid_gated_deltanet_q4k_gb300 import synth
 from oracle import layer as OL
 from oracle import q4k, quant
 
-from gpu_util import DEV, bf16_dev, bf16_host_f32, f16_codes, f32_dev, rel_l2, stream, sync, tf32_round
+from gpu_util import DEV, bf16_dev, bf16_host_f32, f16_codes, f16_dev, f16_round, f32_dev, rel_l2, stream, sync
 
 pytestmark = pytest.mark.gpu
 
@@ -178,7 +178,7 @@ def test_conv_stage(L, spec, n):
     tail = synth.bf16_bits_to_f32(synth._to_bf16_bits(rng.normal(0, 1.3, size=(spec.c_conv, 3)).astype(np.float32)))
     ba = rng.normal(0, 1, size=(n, 2 * spec.n_v_heads)).astype(np.float32)
     qkvz, taild, bad = bf16_dev(bits), f32_dev(tail), f32_dev(ba)
-    qkv = torch.empty(n, spec.c_conv, dtype=torch.float32, device=DEV)
+    qkv = torch.empty(n, spec.c_conv, dtype=torch.float16, device=DEV)
     la = torch.empty(n, spec.n_v_heads, dtype=torch.float32, device=DEV)
     bb = torch.empty_like(la)
     L.gdn_conv(ctypes.byref(s), gl.ptr(qkvz), nb, n, gl.ptr(taild), gl.ptr(bad), 2 * spec.n_v_heads, gl.ptr(qkv),
@@ -189,13 +189,43 @@ def test_conv_stage(L, spec, n):
              eps_l2=1e-6, q_scale=spec.dk ** -0.5, wtype=spec.wtype, hidden=spec.hidden)
     q, k, v, new_tail = OL.conv_stage(p, raw[:, :spec.c_conv], tail)
     ref = np.concatenate([q.reshape(n, -1), k.reshape(n, -1), v.reshape(n, -1)], axis=1)
-    got = qkv.cpu().numpy()
+    got = qkv.float().cpu().numpy()
+    # fp16 rounding (half an ulp: 2^-11 relative, 2^-25 absolute below the normal
+    # range) on top of the fp32 arithmetic
     bound = (2 ** -11 + 3e-5) * np.abs(ref) + 1e-6 * np.abs(ref).max()
     assert np.all(np.abs(got - ref) <= bound)
     assert np.array_equal(taild.cpu().numpy(), new_tail.astype(np.float32))
     rla, rb = OL.gates(ba[:, spec.n_v_heads:], ba[:, :spec.n_v_heads], layer["A_log"], layer["dt_bias"])
     assert rel_l2(la.cpu().numpy(), rla) < 1e-5
     assert rel_l2(bb.cpu().numpy(), rb) < 1e-6
+
+
+def test_conv_reports_fp16_overflow(L):
+    """A conv output beyond the fp16 range (|y| > 65504) is reported once as
+    GDN_ERANGE by the next status read, which also clears it."""
+    spec = CONV_SPECS[2]
+    layer, dev, s = _layer(spec, L)
+    n = 70
+    rng = np.random.default_rng(5)
+    nb = 2 * spec.c_qk + 2 * spec.c_v
+    x = rng.normal(0, 1.0, size=(n, nb)).astype(np.float32)
+    # the v channel whose filter taps sum furthest from zero, driven with a constant
+    # of that sum's sign: SiLU(conv) = 3e6 |sum| once all taps see it, far above 65504
+    vch = 2 * spec.c_qk + np.arange(spec.c_v)
+    wsum = np.asarray(layer["conv_w"], np.float64).reshape(spec.c_conv, -1)[vch].sum(axis=1)
+    c = int(np.argmax(np.abs(wsum)))
+    assert abs(wsum[c]) > 0.05
+    x[:, vch[c]] = 3.0e6 * np.sign(wsum[c])
+    qkvz, taild = bf16_dev(synth._to_bf16_bits(x)), f32_dev(np.zeros((spec.c_conv, 3), np.float32))
+    bad = f32_dev(np.zeros((n, 2 * spec.n_v_heads), np.float32))
+    qkv = torch.empty(n, spec.c_conv, dtype=torch.float16, device=DEV)
+    la = torch.empty(n, spec.n_v_heads, dtype=torch.float32, device=DEV)
+    bb = torch.empty_like(la)
+    L.gdn_conv(ctypes.byref(s), gl.ptr(qkvz), nb, n, gl.ptr(taild), gl.ptr(bad), 2 * spec.n_v_heads, gl.ptr(qkv),
+               gl.ptr(la), gl.ptr(bb), stream())
+    assert L.gdn_sync_status(stream(), check=False) == gl.GDN_ERANGE
+    assert "fp16" in L.last_error() or "range" in L.last_error()
+    assert L.gdn_sync_status(stream(), check=False) == gl.GDN_OK
 
 
 # ------------------------------------------------------------------ step 3
@@ -205,8 +235,8 @@ def _delta_inputs(spec, n, rng):
     q = OL.l2norm_heads(rng.normal(size=(n, hk, d)), 1e-6) * d ** -0.5
     k = OL.l2norm_heads(rng.normal(size=(n, hk, d)), 1e-6)
     v = OL.silu(rng.normal(0, 1, size=(n, hv, d)))
-    # the recurrence consumes q, k, v at tf32 precision, as gdn_conv writes them
-    qkv = tf32_round(np.concatenate([q.reshape(n, -1), k.reshape(n, -1), v.reshape(n, -1)], axis=1))
+    # the recurrence consumes q, k, v in fp16, as gdn_conv writes them
+    qkv = f16_round(np.concatenate([q.reshape(n, -1), k.reshape(n, -1), v.reshape(n, -1)], axis=1))
     vals = qkv.astype(np.float64)
     c = spec.c_qk
     qe = OL.expand_kv_heads(vals[:, :c].reshape(n, hk, d), hv)
@@ -232,7 +262,7 @@ def test_delta_rule_stage(L, spec, n, with_state):
     rng = np.random.default_rng(1000 + n)
     qkv_h, qe, ke, ve, la, b = _delta_inputs(spec, n, rng)
     S0 = rng.normal(0, 0.3, size=(spec.n_v_heads, spec.dv, spec.dk)).astype(np.float32) if with_state else None
-    qkv, lad, bd = f32_dev(qkv_h), f32_dev(la), f32_dev(b)
+    qkv, lad, bd = f16_dev(qkv_h), f32_dev(la), f32_dev(b)
     sin = f32_dev(S0) if with_state else None
     sout = torch.empty(spec.n_v_heads, spec.dv, spec.dk, dtype=torch.float32, device=DEV)
     o = torch.empty(n, spec.c_v, dtype=torch.float32, device=DEV)
@@ -254,7 +284,7 @@ def test_delta_rule_state_aliasing(L):
     n = 150
     qkv_h, qe, ke, ve, la, b = _delta_inputs(spec, n, rng)
     S0 = rng.normal(0, 0.3, size=(spec.n_v_heads, spec.dv, spec.dk)).astype(np.float32)
-    qkv, lad, bd, st = f32_dev(qkv_h), f32_dev(la), f32_dev(b), f32_dev(S0)
+    qkv, lad, bd, st = f16_dev(qkv_h), f32_dev(la), f32_dev(b), f32_dev(S0)
     o = torch.empty(n, spec.c_v, dtype=torch.float32, device=DEV)
     nbytes = L.gdn_delta_rule_scratch_size(ctypes.byref(s), n)
     scratch = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
@@ -264,6 +294,25 @@ def test_delta_rule_state_aliasing(L):
     ro, rS = OL.gated_delta_rule(qe, ke, ve, la, b, S0)
     assert rel_l2(st.cpu().numpy(), rS) <= 2e-3
     assert rel_l2(o.cpu().numpy(), ro.reshape(n, -1)) <= 2e-3
+
+
+def test_delta_rule_reports_fp16_overflow(L):
+    """A state whose fp16 operand image would overflow (|S| > 65504) is
+    reported as GDN_ERANGE; the next call with a state in range is clean."""
+    spec = DELTA_SPECS[1]
+    _, dev, s = _layer(spec, L)
+    rng = np.random.default_rng(78)
+    n = 100
+    qkv_h, qe, ke, ve, la, b = _delta_inputs(spec, n, rng)
+    qkv, lad, bd = f16_dev(qkv_h), f32_dev(la), f32_dev(b)
+    o = torch.empty(n, spec.c_v, dtype=torch.float32, device=DEV)
+    nbytes = L.gdn_delta_rule_scratch_size(ctypes.byref(s), n)
+    scratch = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    for scale, want in ((1.0e5, gl.GDN_ERANGE), (0.3, gl.GDN_OK)):
+        st = f32_dev(rng.normal(0, scale, size=(spec.n_v_heads, spec.dv, spec.dk)))
+        L.gdn_delta_rule(ctypes.byref(s), gl.ptr(qkv), gl.ptr(lad), gl.ptr(bd), n, gl.ptr(st), gl.ptr(st), gl.ptr(o),
+                         gl.ptr(scratch), nbytes, stream())
+        assert L.gdn_sync_status(stream(), check=False) == want
 
 
 # ------------------------------------------------------------------ step 4

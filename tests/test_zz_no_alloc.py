@@ -14,7 +14,7 @@ from hybrid_gated_deltanet_q4k_gb300 import lib as gl
 from hybrid_gated_deltanet_q4k_gb300 import synth
 from oracle import layer as OL
 
-from gpu_util import DEV, f32_dev, rel_l2, stream, sync, tf32_round
+from gpu_util import DEV, f16_dev, f32_dev, rel_l2, stream, sync
 
 pytestmark = pytest.mark.gpu
 
@@ -25,11 +25,11 @@ def _inputs(spec, n, seed):
     q = OL.l2norm_heads(rng.normal(size=(n, hk, d)), 1e-6) * d ** -0.5
     k = OL.l2norm_heads(rng.normal(size=(n, hk, d)), 1e-6)
     v = OL.silu(rng.normal(size=(n, hv, d)))
-    qkv = tf32_round(np.concatenate([q.reshape(n, -1), k.reshape(n, -1), v.reshape(n, -1)], axis=1))
+    qkv = np.concatenate([q.reshape(n, -1), k.reshape(n, -1), v.reshape(n, -1)], axis=1)
     la = rng.uniform(-0.5, 0, size=(n, hv)).astype(np.float32)
     b = (1 / (1 + np.exp(-rng.normal(size=(n, hv))))).astype(np.float32)
     s0 = rng.normal(0, 0.3, size=(hv, d, d)).astype(np.float32)
-    return f32_dev(qkv), f32_dev(la), f32_dev(b), f32_dev(s0)
+    return f16_dev(qkv), f32_dev(la), f32_dev(b), f32_dev(s0)
 
 
 def _layer_struct(spec):
@@ -67,10 +67,10 @@ def test_noalloc_rejects_more_tokens_than_its_scratch():
     L = gl.load(build=True)
     spec = synth.SPECS["h4096"]
     s, _keep = _layer_struct(spec)
-    n = 1985                                       # 32 chunks of 64 > the 31 that fit in 48 MiB
+    n = 3905                                       # 62 chunks of 64 > the 61 that fit in 48 MiB
     assert L.gdn_delta_rule_scratch_size(ctypes.byref(s), n) > gl.GDN_NOALLOC_SCRATCH_BYTES
     buf = torch.zeros(16, dtype=torch.float32, device=DEV)
     r = L.gdn_delta_rule_noalloc(ctypes.byref(s), gl.ptr(buf), gl.ptr(buf), gl.ptr(buf), n, 0, gl.ptr(buf),
                                  gl.ptr(buf), stream(), check=False)
     assert r == gl.GDN_EINVAL
-    assert "at most 1984 tokens" in L.last_error()
+    assert "at most 3904 tokens" in L.last_error()
