@@ -30,7 +30,7 @@ cudaError_t launch_conv(const gdn_layer&, const uint16_t*, int64_t, int64_t, con
                         uint16_t*, float*, float*, cudaStream_t);
 cudaError_t launch_conv_state(const gdn_layer&, const uint16_t*, int64_t, int64_t, float*, cudaStream_t);
 cudaError_t launch_delta(const gdn_layer&, const uint16_t*, const float*, const float*, int64_t, const float*, float*,
-                         float*, void*, cudaStream_t);
+                         float*, void*, cudaStream_t, bool overlap);
 size_t delta_scratch_bytes(int hv, int hk, int d, int64_t n);
 cudaError_t launch_gated_norm(const gdn_layer&, const float*, const uint16_t*, int64_t, int64_t, uint16_t*, float*,
                               float*, cudaStream_t);
@@ -280,7 +280,8 @@ int gdn_delta_rule(const gdn_layer* layer, const uint16_t* qkv, const float* log
     if (!aligned(qkv, 16) || !aligned(scratch, 16) || !aligned(o, 8)) return fail(GDN_EINVAL, "gdn_delta_rule: qkv and scratch 16-byte, o 8-byte alignment required");
     if (scratch_bytes < delta_scratch_bytes(static_cast<int>(s.hv), static_cast<int>(s.hk), static_cast<int>(s.d), n_tokens))
         return fail(GDN_ENOMEM, "gdn_delta_rule: scratch too small");
-    GDN_LAUNCH(launch_delta(*layer, qkv, log_a, b, n_tokens, state_in, state_out, o, scratch, static_cast<cudaStream_t>(stream)),
+    GDN_LAUNCH(launch_delta(*layer, qkv, log_a, b, n_tokens, state_in, state_out, o, scratch, static_cast<cudaStream_t>(stream),
+                            true),
                "gdn_delta_rule");
     return GDN_OK;
 }
@@ -363,7 +364,7 @@ int gdn_prefill(const gdn_layer* layer, const void* x, int64_t n_tokens, const f
         GDN_LAUNCH(mark(4, first, st), "stage event");
         const float* la = lu.gate_log_a ? lu.gate_log_a : w.log_a;
         const float* bb = lu.gate_b ? lu.gate_b : w.b;
-        GDN_LAUNCH(launch_delta(lu, w.qkv, la, bb, nb, first ? state_in : state_out, state_out, w.o, w.delta, st),
+        GDN_LAUNCH(launch_delta(lu, w.qkv, la, bb, nb, first ? state_in : state_out, state_out, w.o, w.delta, st, true),
                    "delta rule");
         GDN_LAUNCH(mark(5, first, st), "stage event");
         const uint16_t* z = w.qkvz + s.c_conv;
@@ -448,7 +449,7 @@ extern "C" int gdn_delta_rule_noalloc(const gdn_layer* layer, const uint16_t* qk
         scratch = g_noalloc_addr[dev];
     }
     GDN_LAUNCH(launch_delta(*layer, qkv, log_a, b, n_tokens, state_in, state_out, o, scratch,
-                            static_cast<cudaStream_t>(stream)),
+                            static_cast<cudaStream_t>(stream), false),
                "gdn_delta_rule_noalloc");
     return GDN_OK;
 }

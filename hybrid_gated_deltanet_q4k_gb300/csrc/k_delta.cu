@@ -66,7 +66,7 @@ struct DeltaArgs {
     const float* log_a;   // [n][hv]
     const float* b;       // [n][hv]
     int n, hv, ratio, c_qk, c_conv, c_v;
-    int nchunks;
+    int chunk0, nchunks;  // the chunks [chunk0, chunk0 + nchunks) of this launch (indices are absolute)
     uint16_t* TA;  // [nchunks][hv][2*DC][DC] [A T; T], fp16, in the swizzled operand image
     float* G;      // [nchunks][hv][DC][4]    gamma, e^gamma, b, e^{gamma_C - gamma}
     uint16_t* KT;  // [nchunks][hk][D][DC]    K^T, fp16, in the swizzled operand image
@@ -102,23 +102,26 @@ struct PrepSmem {
     static constexpr int W0 = T0 + DC * PL * 4;          // block temporaries [DC/2][PL]
     static constexpr int GL0 = W0 + DC / 2 * PL * 4;     // gamma [PREP_MAX_RATIO][DC]
     static constexpr int BB0 = GL0 + PREP_MAX_RATIO * DC * 4;  // b [PREP_MAX_RATIO][DC]
-    // 8 KB pieces 0-3 of operand and output images once the Gram product is
-    // done: the [Q; K] region, extended for D = 64 by 16 KB of its own.
+    // 8 KB pieces 0-5 of operand and output images once the Gram product is
+    // done: the [Q; K] region, extended by a region of its own.
+    static constexpr int NPIECE = 6;
     static constexpr int EX0 = align1k(BB0 + PREP_MAX_RATIO * DC * 4);
-    static constexpr int B0 = EX0 + (4 - 2 * NSLAB) * SLAB;    // mbarriers: TMA, MMA
-    static constexpr int MISC0 = B0 + 16;                      // TMEM base address
+    static constexpr int B0 = EX0 + (NPIECE - 2 * NSLAB) * SLAB;   // mbarriers: TMA, MMA
+    static constexpr int MISC0 = B0 + 16;                          // TMEM base address
     static constexpr int BYTES = MISC0 + 16;
     static __device__ __forceinline__ int piece(int p) { return p < 2 * NSLAB ? QK0 + p * SLAB : EX0 + (p - 2 * NSLAB) * SLAB; }
-    // K^T staging: key rows 64p .. 64p+63 in the Q rows of slab p, written while the K rows are read
-    static __device__ __forceinline__ int kt_piece(int p) { return QK0 + p * 2 * SLAB; }
     static constexpr int AI = 0;    // A operand [DC][DC] (piece 0)
     static constexpr int TTI = 1;   // T^T operand [DC][DC] (piece 1)
-    static constexpr int OUTI = 2;  // [A T; T] output [2*DC][DC] (pieces 2-3, one 16 KB slab)
+    // [A T; T] output staging [2*DC][DC], two buffers (pieces 2-3 and 4-5, one
+    // 16 KB slab each) used by alternate value heads; the second buffer first
+    // stages K^T (key rows 64p .. 64p+63 in piece 4 + p).
+    static __device__ __forceinline__ int out(int j) { return piece(2 + 2 * (j & 1)); }
+    static __device__ __forceinline__ int kt_stage(int p) { return piece(4 + p); }
 };
 
 // C = s * A B for blocks of the fp32 matrices in shared memory (row pitch PL):
 // A is R x KK at a, B is KK x Cc at b, C at c; one 2 x 2 output tile per
-// thread, threads `first` .. first + (R/2)(Cc/2) - 1 of the block take part.
+// thread, threads 0 .. (R/2)(Cc/2) - 1 of the range given by t take part.
 template <int R, int KK, int Cc>
 __device__ __forceinline__ void block_mm(const float* a, const float* b, float* c, float s, int t) {
     constexpr int TC = Cc / 2;
@@ -138,13 +141,42 @@ __device__ __forceinline__ void block_mm(const float* a, const float* b, float* 
     *reinterpret_cast<float2*>(c + (r0 + 1) * PL + c0) = make_float2(s * c10, s * c11);
 }
 
+// The same with one 2 x 4 output tile per thread (threads 0 .. (R/2)(Cc/4) - 1):
+// per k a warp reads four rows of A and 128 contiguous bytes of B, half the
+// shared-memory wavefronts of the 2 x 2 tiling for the same products.
+template <int R, int KK, int Cc>
+__device__ __forceinline__ void block_mm24(const float* a, const float* b, float* c, float s, int t) {
+    constexpr int TC = Cc / 4;
+    if (t < 0 || t >= (R / 2) * TC) return;
+    const int r0 = 2 * (t / TC), c0 = 4 * (t % TC);
+    float x[2][4] = {};
+#pragma unroll 8
+    for (int k = 0; k < KK; ++k) {
+        const float a0 = a[r0 * PL + k], a1 = a[(r0 + 1) * PL + k];
+        const float4 bv = *reinterpret_cast<const float4*>(b + k * PL + c0);
+        x[0][0] = fmaf(a0, bv.x, x[0][0]);
+        x[0][1] = fmaf(a0, bv.y, x[0][1]);
+        x[0][2] = fmaf(a0, bv.z, x[0][2]);
+        x[0][3] = fmaf(a0, bv.w, x[0][3]);
+        x[1][0] = fmaf(a1, bv.x, x[1][0]);
+        x[1][1] = fmaf(a1, bv.y, x[1][1]);
+        x[1][2] = fmaf(a1, bv.z, x[1][2]);
+        x[1][3] = fmaf(a1, bv.w, x[1][3]);
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+        *reinterpret_cast<float4*>(c + (r0 + i) * PL + c0) =
+            make_float4(s * x[i][0], s * x[i][1], s * x[i][2], s * x[i][3]);
+}
+
 // One CTA per (chunk, key head), 256 threads:
 //   - TMA loads the chunk's Q and K rows of the key head as one stacked
 //     [Q; K] operand; one tcgen05 product [Q; K] K^T (M = 128, N = 64) leaves
 //     q_i.k_j in TMEM lanes 0-63 and k_i.k_j in lanes 64-127 (all value heads
 //     of the key head share them).  Warp w then holds row 32(w%4) + lane,
 //     columns 32(w/4) .. +31, in registers.
-//   - K^T, in the state pass's operand image, straight from the K rows.
+//   - K^T, in the state pass's operand image, by 8 x 8 transposes of the K
+//     rows (ldmatrix.trans, stmatrix).
 //   - For each value head (gates differ): the gate prefix sums gamma; the
 //     masked A (rows of lanes 0-63) as an fp16 operand image; L (rows of
 //     lanes 64-127) into shared memory; T = (I + L)^-1 by recursive doubling
@@ -153,10 +185,15 @@ __device__ __forceinline__ void block_mm(const float* a, const float* b, float* 
 //         inv [[A, 0], [C, B]] = [[A^-1, 0], [-B^-1 C A^-1, B^-1]]
 //     for 32 x 32 and then 64 x 64, every block product in fp32 on the CUDA
 //     cores; A T on the tensor cores; [A T; T] (fp16) and the gate table to
-//     global memory.
+//     global memory.  Alternate heads stage their output in alternate
+//     buffers, so a head never waits for the previous head's store.
+// 88 registers a thread: a prep CTA then fits on an SM beside a state CTA,
+// so the prep of the next token segment runs in the shadow of the state
+// pass.  Registers are allocated per SM sub-partition (16K each, warps spread
+// over the four): three state warps (112 registers a thread once rounded)
+// leave 5632 registers, two prep warps of 88.
 template <int D>
-__global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(const __grid_constant__ CUtensorMap qkv_map,
-                                                                      DeltaArgs a) {
+__global__ void __maxnreg__(88) delta_prep_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
     using L = PrepSmem<D>;
     extern __shared__ __align__(1024) unsigned char smb[];
     unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smb) + 1023) & ~uintptr_t(1023));
@@ -166,7 +203,7 @@ __global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(const __gr
     uint64_t* bars = reinterpret_cast<uint64_t*>(base + L::B0);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(base + L::MISC0);
 
-    const int chunk = blockIdx.x, hk = blockIdx.y;
+    const int chunk = a.chunk0 + blockIdx.x, hk = blockIdx.y;
     const int t0 = chunk * DC;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int r = a.ratio;
@@ -240,11 +277,26 @@ __global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(const __gr
         return;
     }
 
+    // ---- K^T image for the state pass: warp task = tokens 8tb .. 8tb+7 x key
+    // rows 32dq .. 32dq+31, four 8 x 8 blocks transposed; written to its staging
+    // while the Gram product runs, then by bulk copies.  Every thread observes
+    // the copy's completion itself (it has completed: this returns at once).
+    mbar_wait_bounded(bars + 0, 0, &g_delta_error, ERR_WAIT_TIMEOUT);
+    for (int task = warp; task < (DC / 8) * (D / 32); task += DELTA_THREADS / 32) {
+        const int tb = task % (DC / 8), dq = task / (DC / 8);
+        const int d = 32 * dq + 8 * (lane >> 3), rr = lane & 7;   // block of this lane's address, row rr of it
+        uint32_t f[4];
+        ldsm_x4_trans(smem_addr(base + L::QK0 + (d >> 6) * 2 * L::SLAB + L::SLAB + sw128_f16(8 * tb + rr, d & 63)), f);
+        const int dr = d + rr;
+        stsm_x4(smem_addr(base + L::kt_stage(dr >> 6) + sw128_f16(dr & 63, 8 * tb)), f);
+    }
+
     // ---- the Gram rows of this thread
     const int q = warp & 3, half = warp >> 2;
     const bool qrow = q < 2;                 // lanes 0-63: q_i.k_j; lanes 64-127: k_i.k_j
     const int row = 32 * (q & 1) + lane;     // token i of this row
     const int c0 = 32 * half;                // first column (token j)
+    const bool upper = (q & 1) == 0 && half == 1;   // rows 0-31 x columns 32-63: every j > i, masked
     float g[32];
     if (!mbar_wait_bounded(bars + 1, 0, &g_delta_error, ERR_WAIT_TIMEOUT)) ok = false;
     ok = __all_sync(0xffffffffu, ok);
@@ -252,6 +304,7 @@ __global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(const __gr
         t5::fence_after();
         t5::ld32(tmem + (static_cast<uint32_t>(32 * q) << 16) + c0, g);
     }
+    fence_proxy_async_smem();               // the K^T staging goes to the bulk copies
     ok = __syncthreads_and(ok);
     if (!ok) {
         if (tid == 0) mbar_wait_bounded(bars + 1, 0, nullptr, 0, 200000000ull);
@@ -260,33 +313,10 @@ __global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(const __gr
         if (warp == 0) t5::dealloc(tmem, 128);
         return;
     }
-
-    // ---- K^T image for the state pass, staged in the Q rows (free now) and
-    // written by bulk copies: staging piece p holds key rows 64p .. 64p+63
-    // (8 KB of the image).  Task (key row d, tokens 8g .. 8g+7) is one
-    // 16-byte store; consecutive threads take consecutive d.
-    {
-        for (int task = tid; task < D * (DC / 8); task += DELTA_THREADS) {
-            const int d = task % D, g8 = task / D, dl = d & 63;
-            const unsigned char* kp = base + L::QK0 + (d >> 6) * 2 * L::SLAB + L::SLAB;
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const uint32_t lo = *reinterpret_cast<const uint16_t*>(kp + sw128_f16(8 * g8 + 2 * e, dl));
-                const uint32_t hi = *reinterpret_cast<const uint16_t*>(kp + sw128_f16(8 * g8 + 2 * e + 1, dl));
-                w[e] = lo | (hi << 16);
-            }
-            *reinterpret_cast<uint4*>(base + L::kt_piece(d >> 6) + sw128_f16(dl, 8 * g8)) = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-        fence_proxy_async_smem();
-        __syncthreads();
-        if (tid == 0) {
-            uint16_t* kt = a.KT + (static_cast<int64_t>(chunk) * gridDim.y + hk) * D * DC;
-            for (int p = 0; p < L::NSLAB; ++p) bulk_store_1d(kt + p * (64 * DC), base + L::kt_piece(p), L::SLAB);
-            bulk_commit();
-            bulk_wait_read();      // the region becomes the per-head staging
-        }
-        __syncthreads();
+    if (tid == 0) {
+        uint16_t* kt = a.KT + (static_cast<int64_t>(chunk) * gridDim.y + hk) * D * DC;
+        for (int p = 0; p < L::NSLAB; ++p) bulk_store_1d(kt + p * (64 * DC), base + L::kt_stage(p), L::SLAB);
+        bulk_commit();
     }
 
     bool bad = false;   // a T or A T value outside the fp16 range
@@ -296,6 +326,9 @@ __global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(const __gr
         const float* gl = reinterpret_cast<const float*>(base + L::GL0) + j * DC;
         const float* bb = reinterpret_cast<const float*>(base + L::BB0) + j * DC;
         const float gi = gl[row];
+        // this head's output buffer was last read by the store two heads back
+        // (or, for head 1, by the K^T store): let that read finish first
+        if (tid == 0 && j >= 1) bulk_wait_read_but_last();
         if (qrow) {
             // A_ij = e^{gamma_i - gamma_j} q_i.k_j (j <= i), |A_ij| <= |q_i||k_j| <= 1:
             // half of one 128-byte row of the swizzled image
@@ -306,7 +339,7 @@ __global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(const __gr
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const int c = c0 + 8 * m + e;
-                    v[e] = c <= row ? __expf(gi - gl[c]) * g[8 * m + e] : 0.f;
+                    v[e] = (!upper && c <= row) ? __expf(gi - gl[c]) * g[8 * m + e] : 0.f;
                 }
                 *reinterpret_cast<uint4*>(arow + ((((c0 >> 3) + m) ^ (row & 7)) << 4)) = f16x8(v);
             }
@@ -319,22 +352,25 @@ __global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(const __gr
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int c = c0 + 4 * m + e;
-                    v[e] = c < row ? bi * __expf(gi - gl[c]) * g[4 * m + e] : 0.f;
+                    v[e] = (!upper && c < row) ? bi * __expf(gi - gl[c]) * g[4 * m + e] : 0.f;
                 }
                 *reinterpret_cast<float4*>(Ls + row * PL + c0 + 4 * m) = make_float4(v[0], v[1], v[2], v[3]);
             }
         }
         __syncthreads();
-        // 16 x 16 diagonal blocks of T: warp 0 blocks 0, 1; warp 1 blocks 2, 3; lane = column
+        // 16 x 16 diagonal blocks of T: warp 0 blocks 0, 1; warp 1 blocks 2, 3; lane = column.
+        // Right-looking: once t_k is final it is folded into the sums of the rows below,
+        // so each step waits on one product, not on a sum over k.
         if (warp < 2) {
             const int blk = 2 * warp + (lane >> 4), cc = lane & 15, o = 16 * blk;
-            float t[16];
+            float t[16], sum[16];
 #pragma unroll
-            for (int rr = 0; rr < 16; ++rr) {
-                float s = 0.f;
+            for (int i = 0; i < 16; ++i) sum[i] = 0.f;
 #pragma unroll
-                for (int k = 0; k < rr; ++k) s = fmaf(Ls[(o + rr) * PL + o + k], t[k], s);
-                t[rr] = rr < cc ? 0.f : (rr == cc ? 1.f : -s);
+            for (int k = 0; k < 16; ++k) {
+                t[k] = k < cc ? 0.f : (k == cc ? 1.f : -sum[k]);
+#pragma unroll
+                for (int i = k + 1; i < 16; ++i) sum[i] = fmaf(Ls[(o + i) * PL + o + k], t[k], sum[i]);
             }
 #pragma unroll
             for (int rr = 0; rr < 16; ++rr) Ts[(o + rr) * PL + o + cc] = t[rr];
@@ -350,23 +386,26 @@ __global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(const __gr
             __syncthreads();
         }
         // 64 x 64: T[32:64, 0:32] = -T[32:64, 32:64] (L[32:64, 0:32] T[0:32, 0:32])
-        block_mm<32, 32, 32>(Ls + 32 * PL, Ts, Ws, 1.f, tid);
+        block_mm24<32, 32, 32>(Ls + 32 * PL, Ts, Ws, 1.f, tid);
         __syncthreads();
-        block_mm<32, 32, 32>(Ts + 32 * PL + 32, Ws, Ts + 32 * PL, -1.f, tid);
+        block_mm24<32, 32, 32>(Ts + 32 * PL + 32, Ws, Ts + 32 * PL, -1.f, tid);
         __syncthreads();
         // T^T operand image (row m, column j = T_jm) and the T rows of the output
-        // (rows 64-127 of [A T; T]), fp16; thread -> row tid/4, 16 columns
+        // (rows 64-127 of [A T; T]), fp16; thread -> row tid%64, columns 16(tid/64) ..
         {
-            const int rr = tid >> 2, cq = 16 * (tid & 3);
+            const int rr = tid & 63, cq = 16 * (tid >> 6);
             unsigned char* ttrow = base + L::piece(L::TTI) + rr * 128;
-            unsigned char* orow = base + L::piece(L::OUTI) + (DC + rr) * 128;
+            unsigned char* orow = base + L::out(j) + (DC + rr) * 128;
 #pragma unroll
             for (int m = 0; m < 2; ++m) {
                 const int c = cq + 8 * m;
+                const float4 r0 = *reinterpret_cast<const float4*>(Ts + rr * PL + c);
+                const float4 r1 = *reinterpret_cast<const float4*>(Ts + rr * PL + c + 4);
+                const float rv[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
                 float v[8], w[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    v[e] = c + e <= rr ? Ts[rr * PL + c + e] : 0.f;
+                    v[e] = c + e <= rr ? rv[e] : 0.f;
                     w[e] = c + e >= rr ? Ts[(c + e) * PL + rr] : 0.f;
                     bad |= f16_out_of_range(v[e]);
                 }
@@ -402,7 +441,7 @@ __global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(const __gr
             t5::ld32(tmem + (static_cast<uint32_t>(32 * q) << 16) + 64 + c0, at);
             if (lane < 16) {
                 const int ri = 16 * q + lane;
-                unsigned char* orow = base + L::piece(L::OUTI) + ri * 128;
+                unsigned char* orow = base + L::out(j) + ri * 128;
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
                     float v[8];
@@ -417,13 +456,11 @@ __global__ void __launch_bounds__(DELTA_THREADS, 2) delta_prep_kernel(const __gr
         }
         fence_proxy_async_smem();
         t5::fence_before();
-        mok = __syncthreads_and(mok);
+        mok = __syncthreads_and(mok);   // also: A, T^T and L are free for the next head
         if (tid == 0 && mok) {
-            bulk_store_1d(a.TA + cb * 2 * DC * DC, base + L::piece(L::OUTI), 2 * L::SLAB);
+            bulk_store_1d(a.TA + cb * 2 * DC * DC, base + L::out(j), 2 * L::SLAB);
             bulk_commit();
-            bulk_wait_read();      // the staging is rewritten by the next head
         }
-        __syncthreads();   // before the next head overwrites L, T and the staging
         if (!mok) break;
     }
     if (bad) atomicCAS(&g_delta_error, 0, ERR_RANGE);
@@ -569,26 +606,27 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             auto cb = [&](int c) { return static_cast<int64_t>(c) * a.hv + h; };
-            for (int c = 0; c < a.nchunks; ++c) {
-                const uint32_t pp = (c - 1) & 1;   // phase of the previous chunk's release
-                if (c >= 1 && !state_wait(bars + E_QK, pp, abort)) break;
+            for (int j = 0; j < a.nchunks; ++j) {
+                const int c = a.chunk0 + j;
+                const uint32_t pp = (j - 1) & 1;   // phase of the previous chunk's release
+                if (j >= 1 && !state_wait(bars + E_QK, pp, abort)) break;
                 mbar_expect_tx(bars + F_QK, 2 * L::NSLAB * L::SLAB);
                 for (int sl = 0; sl < L::NSLAB; ++sl) {
                     unsigned char* dst = base + L::QK0 + sl * L::QK_SLAB;
                     tma_load_2d_tile(dst, &qkv_map, bars + F_QK, hk * D + 64 * sl, c * DC);
                     tma_load_2d_tile(dst + L::SLAB, &qkv_map, bars + F_QK, a.c_qk + hk * D + 64 * sl, c * DC);
                 }
-                const int kb = c & 1;
-                if (c >= 2 && !state_wait(bars + E_KT0 + kb, ((c - 2) >> 1) & 1, abort)) break;
+                const int kb = j & 1;
+                if (j >= 2 && !state_wait(bars + E_KT0 + kb, ((j - 2) >> 1) & 1, abort)) break;
                 mbar_expect_tx(bars + F_KT0 + kb, L::KT_BYTES);
                 bulk_load_1d(base + L::KT0 + kb * L::KT_BYTES,
                              a.KT + (static_cast<int64_t>(c) * (a.hv / a.ratio) + hk) * D * DC, L::KT_BYTES,
                              bars + F_KT0 + kb);
-                if (c >= 1 && !state_wait(bars + E_V, pp, abort)) break;
+                if (j >= 1 && !state_wait(bars + E_V, pp, abort)) break;
                 mbar_expect_tx(bars + F_V, L::SLAB + DC * 16);
                 tma_load_2d_tile(base + L::V0, &qkv_map, bars + F_V, 2 * a.c_qk + h * D + (i0 & ~63), c * DC);
-                bulk_load_1d(base + L::G0 + (c & 1) * DC * 16, a.G + cb(c) * DC * 4, DC * 16, bars + F_V);
-                if (c >= 1 && !state_wait(bars + E_TA, pp, abort)) break;
+                bulk_load_1d(base + L::G0 + (j & 1) * DC * 16, a.G + cb(c) * DC * 4, DC * 16, bars + F_V);
+                if (j >= 1 && !state_wait(bars + E_TA, pp, abort)) break;
                 mbar_expect_tx(bars + F_TA, L::QK_SLAB);
                 bulk_load_1d(base + L::TA0, a.TA + cb(c) * 2 * DC * DC, L::QK_SLAB, bars + F_TA);
             }
@@ -608,9 +646,9 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
             t5::fence_after();
             return true;
         };
-        for (int c = 0; c < a.nchunks; ++c) {
-            const uint32_t ph = c & 1;
-            nb_sync(NB_S);                      // S of chunk c written
+        for (int j = 0; j < a.nchunks; ++j) {
+            const uint32_t ph = j & 1;
+            nb_sync(NB_S);                      // S of chunk j written
             if (leader && ready(F_QK, ph)) {
                 mma_chain<D / 16, L::QK_SLAB, L::SOP>(tmem + TM_XY + 32 * ph, dQK, dS, ID128);
                 t5::commit(bars + M_XY);
@@ -625,7 +663,7 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
             }
             __syncwarp();
             nb_sync(NB_D);                      // Delta~^T written
-            if (leader && ready(F_KT0 + ph, (c >> 1) & 1)) {
+            if (leader && ready(F_KT0 + ph, (j >> 1) & 1)) {
                 mma_chain<DC / 16, L::KT_BYTES, L::SOP>(tmem + TM_U, dKT + ph * (L::KT_BYTES >> 4), dE, IDU);
                 t5::commit(bars + M_U);
                 t5::commit(bars + E_KT0 + ph);
@@ -691,8 +729,9 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
 
         write_s();
         handover(NB_S);
-        for (int c = 0; c < a.nchunks; ++c) {
-            const uint32_t ph = c & 1;
+        for (int j = 0; j < a.nchunks; ++j) {
+            const int c = a.chunk0 + j;
+            const uint32_t ph = j & 1;
             const float4* G = reinterpret_cast<const float4*>(base + L::G0 + ph * DC * 16);
             float4 gt = make_float4(0.f, 0.f, 0.f, 0.f);
             float dec = 0.f;
@@ -741,7 +780,7 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
                 for (int v = 0; v < 16; ++v) S[v] = fmaf(dec, S[v], u[v]);
                 write_s();
             }
-            if (c + 1 < a.nchunks) handover(NB_S);
+            if (j + 1 < a.nchunks) handover(NB_S);
 
             // ---- O = diag(e^gamma) Y + Z (Y rows: lanes 0-63), while the next X, Y run
             if (!xw && mma_done(M_DZ, ph)) {
@@ -820,27 +859,104 @@ int read_and_clear_delta_error() {
     return v;
 }
 
+// Token segments of DELTA_SEG_CHUNKS chunks.  With more than one, the prep
+// of segment i+1 runs on a low-priority stream while the state pass of
+// segment i runs on a high-priority one (the state is carried between
+// segments in state_out, fp32, so the results are those of one launch).  The
+// two library streams are forked from the caller's stream and joined back to
+// it, so the call stays ordered on that stream and can be captured in a CUDA
+// graph.
+constexpr int DELTA_SEG_CHUNKS = 64;
+constexpr int DELTA_MAX_DEVICES = 64;
+
+struct DeltaStreams {
+    cudaStream_t prep = nullptr, state = nullptr;
+    cudaEvent_t fork = nullptr, seg = nullptr;
+};
+static std::mutex g_delta_streams_mu;   // guards the table and each enqueue sequence
+static DeltaStreams g_delta_streams[DELTA_MAX_DEVICES];
+
+static cudaError_t delta_streams(DeltaStreams** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= DELTA_MAX_DEVICES) return cudaErrorInvalidDevice;
+    DeltaStreams& s = g_delta_streams[dev];
+    if (!s.seg) {
+        int least = 0, greatest = 0;
+        if ((e = cudaDeviceGetStreamPriorityRange(&least, &greatest)) != cudaSuccess) return e;
+        if (!s.prep && (e = cudaStreamCreateWithPriority(&s.prep, cudaStreamNonBlocking, least)) != cudaSuccess) return e;
+        if (!s.state && (e = cudaStreamCreateWithPriority(&s.state, cudaStreamNonBlocking, greatest)) != cudaSuccess)
+            return e;
+        if (!s.fork && (e = cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&s.seg, cudaEventDisableTiming)) != cudaSuccess) return e;
+    }
+    *out = &s;
+    return cudaSuccess;
+}
+
 template <int D>
-static cudaError_t launch_delta_d(DeltaArgs& a, cudaStream_t st) {
-    const size_t prep_smem = PrepSmem<D>::BYTES + 1024;
-    const size_t state_smem = StateSmem<D>::BYTES + 1024;
+static void launch_prep(const CUtensorMap& map, const DeltaArgs& a, cudaStream_t st) {
+    delta_prep_kernel<D><<<dim3(a.nchunks, a.hv / a.ratio), DELTA_THREADS, PrepSmem<D>::BYTES + 1024, st>>>(map, a);
+}
+template <int D>
+static void launch_state(const CUtensorMap& map, const DeltaArgs& a, cudaStream_t st) {
+    delta_state_kernel<D><<<dim3(a.hv, D / NV), STATE_THREADS, StateSmem<D>::BYTES + 1024, st>>>(map, a);
+}
+
+template <int D>
+static cudaError_t launch_delta_d(DeltaArgs& a, cudaStream_t st, bool overlap) {
     static bool attr = false;
     if (!attr) {
-        cudaFuncSetAttribute(delta_prep_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(prep_smem));
-        cudaFuncSetAttribute(delta_state_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(state_smem));
+        cudaFuncSetAttribute(delta_prep_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, PrepSmem<D>::BYTES + 1024);
+        cudaFuncSetAttribute(delta_state_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, StateSmem<D>::BYTES + 1024);
+        // the whole unified L1 as shared memory, so that a state CTA and a prep CTA fit on one SM
+        cudaFuncSetAttribute(delta_prep_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+        cudaFuncSetAttribute(delta_state_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
         attr = true;
     }
     CUtensorMap map;
     if (!make_qkv_map(&map, a.qkv, a.n, a.c_conv)) return cudaErrorInvalidValue;
-    delta_prep_kernel<D><<<dim3(a.nchunks, a.hv / a.ratio), DELTA_THREADS, prep_smem, st>>>(map, a);
-    cudaError_t e = cudaGetLastError();
+    const int nch = a.nchunks;
+    a.chunk0 = 0;
+    if (!overlap || nch <= DELTA_SEG_CHUNKS) {
+        launch_prep<D>(map, a, st);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        launch_state<D>(map, a, st);
+        return cudaGetLastError();
+    }
+    std::lock_guard<std::mutex> lock(g_delta_streams_mu);
+    DeltaStreams* ds = nullptr;
+    cudaError_t e = delta_streams(&ds);
     if (e != cudaSuccess) return e;
-    delta_state_kernel<D><<<dim3(a.hv, D / NV), STATE_THREADS, state_smem, st>>>(map, a);
-    return cudaGetLastError();
+    if ((e = cudaEventRecord(ds->fork, st)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(ds->prep, ds->fork, 0)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(ds->state, ds->fork, 0)) != cudaSuccess) return e;
+    cudaError_t first = cudaSuccess;
+    for (int c0 = 0; c0 < nch && first == cudaSuccess; c0 += DELTA_SEG_CHUNKS) {
+        DeltaArgs s = a;
+        s.chunk0 = c0;
+        s.nchunks = nch - c0 < DELTA_SEG_CHUNKS ? nch - c0 : DELTA_SEG_CHUNKS;
+        if (c0 > 0) s.state_in = a.state_out;
+        launch_prep<D>(map, s, ds->prep);
+        if ((first = cudaGetLastError()) != cudaSuccess) break;
+        if ((first = cudaEventRecord(ds->seg, ds->prep)) != cudaSuccess) break;
+        if ((first = cudaStreamWaitEvent(ds->state, ds->seg, 0)) != cudaSuccess) break;
+        launch_state<D>(map, s, ds->state);
+        first = cudaGetLastError();
+    }
+    // join both library streams back to the caller's stream, also after a failure
+    e = cudaEventRecord(ds->seg, ds->prep);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(ds->state, ds->seg, 0);
+    if (e == cudaSuccess) e = cudaEventRecord(ds->fork, ds->state);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ds->fork, 0);
+    return first != cudaSuccess ? first : e;
 }
 
 cudaError_t launch_delta(const gdn_layer& L, const uint16_t* qkv, const float* log_a, const float* b, int64_t n,
-                         const float* state_in, float* state_out, float* o, void* scratch, cudaStream_t st) {
+                         const float* state_in, float* state_out, float* o, void* scratch, cudaStream_t st,
+                         bool overlap) {
     DeltaArgs a;
     const int d = L.dk;
     a.qkv = qkv;
@@ -852,6 +968,7 @@ cudaError_t launch_delta(const gdn_layer& L, const uint16_t* qkv, const float* l
     a.c_qk = L.n_qk_heads * d;
     a.c_v = L.n_v_heads * d;
     a.c_conv = 2 * a.c_qk + a.c_v;
+    a.chunk0 = 0;
     a.nchunks = static_cast<int>((n + DC - 1) / DC);
     const int64_t nch = a.nchunks;
     unsigned char* base = static_cast<unsigned char*>(scratch);
@@ -861,7 +978,7 @@ cudaError_t launch_delta(const gdn_layer& L, const uint16_t* qkv, const float* l
     a.state_in = state_in;
     a.state_out = state_out;
     a.o = o;
-    return d == 128 ? launch_delta_d<128>(a, st) : launch_delta_d<64>(a, st);
+    return d == 128 ? launch_delta_d<128>(a, st, overlap) : launch_delta_d<64>(a, st, overlap);
 }
 
 }  // namespace gdn

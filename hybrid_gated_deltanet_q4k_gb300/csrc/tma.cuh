@@ -93,6 +93,25 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 // ... and have completed.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// All but this thread's most recent committed bulk store have finished reading.
+__device__ __forceinline__ void bulk_wait_read_but_last() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+
+// Whole warp: four 8 x 8 matrices of 16-bit values loaded transposed (lanes
+// 8i .. 8i+7 give the shared addresses of the rows of matrix i; register i
+// of each lane receives its part of matrix i, transposed).
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+// Whole warp: the inverse of a plain (non-transposing) ldmatrix: four 8 x 8
+// matrices stored at the row addresses lanes 8i .. 8i+7 give for matrix i.
+__device__ __forceinline__ void stsm_x4(uint32_t addr, const uint32_t (&r)[4]) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(r[0]), "r"(r[1]),
+                 "r"(r[2]), "r"(r[3])
+                 : "memory");
+}
 
 // Byte offset of fp32 element (r, c), c < 32, inside a 128-byte-swizzled slab
 // of 128-byte rows (the layout a 2-D TMA box with SWIZZLE_128B and a 32-float

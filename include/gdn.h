@@ -26,6 +26,11 @@
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Device
  *     work is enqueued asynchronously on it; the call returns when the work is
  *     enqueued.  A fault inside a kernel shows up at gdn_sync_status().
+ *     gdn_delta_rule and gdn_prefill run the delta rule of long inputs (more
+ *     than 64 chunks) on two streams of the library, forked from `stream`
+ *     and joined back to it within the call, so the work stays ordered on
+ *     `stream` and a stream capture records it; the first such call on a
+ *     device creates the two streams and two events, kept until exit.
  *   - Return value: GDN_OK (0) or a negative GDN_E* code; the message of the
  *     last failure on the calling thread is gdn_last_error().  A failing call
  *     enqueues nothing unless the code is GDN_ECUDA (a launch that failed).

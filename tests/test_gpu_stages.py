@@ -256,7 +256,7 @@ DELTA_SPECS = [synth.SPECS["tiny_f32"], synth.LayerSpec("d4", 512, 2, 4, 128, 12
 
 @pytest.mark.parametrize("spec", DELTA_SPECS, ids=lambda s: s.name)
 @pytest.mark.parametrize("n,with_state", [(1, True), (63, False), (64, True), (65, True), (200, False),
-                                          (513, True), (2000, True)])
+                                          (513, True), (2000, True), (8300, True)])
 def test_delta_rule_stage(L, spec, n, with_state):
     _, dev, s = _layer(spec, L)
     rng = np.random.default_rng(1000 + n)
@@ -275,6 +275,41 @@ def test_delta_rule_stage(L, spec, n, with_state):
     ro, rS = OL.gated_delta_rule(qe, ke, ve, la, b, S0r)
     assert rel_l2(o.cpu().numpy(), ro.reshape(n, -1)) <= 2e-3
     assert rel_l2(sout.cpu().numpy(), rS) <= 2e-3
+
+
+def test_delta_rule_segments_bitwise(L):
+    """Inputs longer than 64 chunks run as token segments (the prep of the next
+    segment beside the state pass of the current one) with the fp32 state
+    carried between them: one call over 8300 tokens (three segments) gives the
+    same bits as a call over the first 4096 tokens (one segment) followed by
+    one over the rest (two segments)."""
+    spec = DELTA_SPECS[1]
+    _, dev, s = _layer(spec, L)
+    rng = np.random.default_rng(79)
+    n, n1 = 8300, 4096
+    qkv_h, qe, ke, ve, la, b = _delta_inputs(spec, n, rng)
+    S0 = rng.normal(0, 0.3, size=(spec.n_v_heads, spec.dv, spec.dk)).astype(np.float32)
+    qkv, lad, bd = f16_dev(qkv_h), f32_dev(la), f32_dev(b)
+
+    def run(lo, hi, sin, sout, o):
+        m = hi - lo
+        nbytes = L.gdn_delta_rule_scratch_size(ctypes.byref(s), m)
+        scratch = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+        L.gdn_delta_rule(ctypes.byref(s), gl.ptr(qkv[lo:hi]), gl.ptr(lad[lo:hi]), gl.ptr(bd[lo:hi]), m, gl.ptr(sin),
+                         gl.ptr(sout), gl.ptr(o[lo:hi]), gl.ptr(scratch), nbytes, stream())
+        sync(L)
+
+    o_one = torch.empty(n, spec.c_v, dtype=torch.float32, device=DEV)
+    st_one = torch.empty(spec.n_v_heads, spec.dv, spec.dk, dtype=torch.float32, device=DEV)
+    run(0, n, f32_dev(S0), st_one, o_one)
+    o_two = torch.empty_like(o_one)
+    st_two = f32_dev(S0)
+    run(0, n1, st_two, st_two, o_two)
+    run(n1, n, st_two, st_two, o_two)
+    assert torch.equal(o_one, o_two) and torch.equal(st_one, st_two)
+    ro, rS = OL.gated_delta_rule(qe, ke, ve, la, b, S0)
+    assert rel_l2(o_one.cpu().numpy(), ro.reshape(n, -1)) <= 2e-3
+    assert rel_l2(st_one.cpu().numpy(), rS) <= 2e-3
 
 
 def test_delta_rule_state_aliasing(L):
