@@ -439,7 +439,7 @@ def run_stage(args, spec):
         la = -0.5 * torch.rand(n, hv, device="cuda", generator=g)
         b = torch.rand(n, hv, device="cuda", generator=g)
         stt = torch.zeros(hv, d, d, device="cuda")
-        o = torch.empty(n, spec.c_v, device="cuda")
+        o = torch.empty(n, spec.c_v, dtype=torch.float16, device="cuda")
         nbytes = L.gdn_delta_rule_scratch_size(ctypes.byref(s), n)
         scratch = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
         fn = lambda: L.gdn_delta_rule(ctypes.byref(s), gl.ptr(qkv), gl.ptr(la), gl.ptr(b), n, 0, gl.ptr(stt),  # noqa: E731

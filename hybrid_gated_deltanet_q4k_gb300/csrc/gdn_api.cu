@@ -30,9 +30,9 @@ cudaError_t launch_conv(const gdn_layer&, const uint16_t*, int64_t, int64_t, con
                         uint16_t*, float*, float*, cudaStream_t);
 cudaError_t launch_conv_state(const gdn_layer&, const uint16_t*, int64_t, int64_t, float*, cudaStream_t);
 cudaError_t launch_delta(const gdn_layer&, const uint16_t*, const float*, const float*, int64_t, const float*, float*,
-                         float*, void*, cudaStream_t, bool overlap);
+                         uint16_t*, void*, cudaStream_t, bool overlap);
 size_t delta_scratch_bytes(int hv, int hk, int d, int64_t n);
-cudaError_t launch_gated_norm(const gdn_layer&, const float*, const uint16_t*, int64_t, int64_t, uint16_t*, float*,
+cudaError_t launch_gated_norm(const gdn_layer&, const uint16_t*, const uint16_t*, int64_t, int64_t, uint16_t*, float*,
                               float*, cudaStream_t);
 int read_and_clear_gemm_error();
 int read_and_clear_delta_error();
@@ -119,7 +119,7 @@ struct Workspace {
     float* ba;                        // projection, fp32 [B][2 hv]
     uint16_t* qkv;                    // conv output, fp16 [B][c_conv]
     float* log_a; float* b;           // gates [B][hv]
-    float* o;                         // recurrence output [B][c_v]
+    uint16_t* o;                      // recurrence output, fp16 [B][c_v]
     uint16_t* oc; float* so;          // gated-norm codes [B][c_v], scales [B]  (Q4_K)
     float* ohat;                      // gated-norm output [B][c_v]               (F32)
     void* delta; size_t delta_bytes;  // chunked delta-rule scratch
@@ -155,7 +155,7 @@ Workspace carve(const gdn_layer* L, const Sizes& s, int64_t B, void* base) {
     w.qkv = static_cast<uint16_t*>(take(B * s.c_conv * 2));
     w.log_a = static_cast<float*>(take(B * s.hv * 4));
     w.b = static_cast<float*>(take(B * s.hv * 4));
-    w.o = static_cast<float*>(take(B * s.c_v * 4));
+    w.o = static_cast<uint16_t*>(take(B * s.c_v * 2));
     w.delta_bytes = delta_scratch_bytes(static_cast<int>(s.hv), static_cast<int>(s.hk), static_cast<int>(s.d), B);
     w.delta = take(w.delta_bytes);
     w.total = off;
@@ -271,13 +271,13 @@ size_t gdn_delta_rule_scratch_size(const gdn_layer* layer, int64_t n_tokens) {
 }
 
 int gdn_delta_rule(const gdn_layer* layer, const uint16_t* qkv, const float* log_a, const float* b, int64_t n_tokens,
-                   const float* state_in, float* state_out, float* o, void* scratch, size_t scratch_bytes, void* stream) {
+                   const float* state_in, float* state_out, uint16_t* o, void* scratch, size_t scratch_bytes, void* stream) {
     Sizes s;
     int r = check_layer(layer, &s);
     if (r) return r;
     if (n_tokens < 1 || n_tokens > 0x7fffffff) return fail(GDN_EINVAL, "gdn_delta_rule: n_tokens >= 1 required");
     if (!qkv || !log_a || !b || !state_out || !o || !scratch) return fail(GDN_EINVAL, "gdn_delta_rule: NULL pointer");
-    if (!aligned(qkv, 16) || !aligned(scratch, 16) || !aligned(o, 8)) return fail(GDN_EINVAL, "gdn_delta_rule: qkv and scratch 16-byte, o 8-byte alignment required");
+    if (!aligned(qkv, 16) || !aligned(scratch, 16) || !aligned(o, 16)) return fail(GDN_EINVAL, "gdn_delta_rule: qkv, scratch and o 16-byte alignment required");
     if (scratch_bytes < delta_scratch_bytes(static_cast<int>(s.hv), static_cast<int>(s.hk), static_cast<int>(s.d), n_tokens))
         return fail(GDN_ENOMEM, "gdn_delta_rule: scratch too small");
     GDN_LAUNCH(launch_delta(*layer, qkv, log_a, b, n_tokens, state_in, state_out, o, scratch, static_cast<cudaStream_t>(stream),
@@ -286,13 +286,13 @@ int gdn_delta_rule(const gdn_layer* layer, const uint16_t* qkv, const float* log
     return GDN_OK;
 }
 
-int gdn_gated_norm(const gdn_layer* layer, const float* o, const uint16_t* z, int64_t ld_z, int64_t n_tokens,
+int gdn_gated_norm(const gdn_layer* layer, const uint16_t* o, const uint16_t* z, int64_t ld_z, int64_t n_tokens,
                    uint16_t* codes, float* scale, float* out_f32, void* stream) {
     Sizes s;
     int r = check_layer(layer, &s);
     if (r) return r;
     if (n_tokens < 1 || n_tokens > 0x7fffffff || !o || !z) return fail(GDN_EINVAL, "gdn_gated_norm: arguments");
-    if (ld_z < s.c_v || ld_z % 4 || !aligned(z, 8) || !aligned(o, 16)) return fail(GDN_EINVAL, "gdn_gated_norm: layout");
+    if (ld_z < s.c_v || ld_z % 4 || !aligned(z, 8) || !aligned(o, 8)) return fail(GDN_EINVAL, "gdn_gated_norm: layout");
     if (layer->wtype == GDN_W_Q4K && (!codes || !scale || !aligned(codes, 8))) return fail(GDN_EINVAL, "gdn_gated_norm: codes");
     if (layer->wtype == GDN_W_F32 && !out_f32) return fail(GDN_EINVAL, "gdn_gated_norm: out_f32");
     GDN_LAUNCH(launch_gated_norm(*layer, o, z, ld_z, n_tokens, codes, scale, out_f32, static_cast<cudaStream_t>(stream)),
@@ -416,14 +416,14 @@ void* g_noalloc_addr[kMaxDevices] = {};
 }  // namespace
 
 extern "C" int gdn_delta_rule_noalloc(const gdn_layer* layer, const uint16_t* qkv, const float* log_a, const float* b,
-                                      int64_t n_tokens, const float* state_in, float* state_out, float* o,
+                                      int64_t n_tokens, const float* state_in, float* state_out, uint16_t* o,
                                       void* stream) {
     Sizes s;
     int r = check_layer(layer, &s);
     if (r) return r;
     if (n_tokens < 1 || n_tokens > 0x7fffffff) return fail(GDN_EINVAL, "gdn_delta_rule_noalloc: n_tokens >= 1 required");
     if (!qkv || !log_a || !b || !state_out || !o) return fail(GDN_EINVAL, "gdn_delta_rule_noalloc: NULL pointer");
-    if (!aligned(qkv, 16) || !aligned(o, 8)) return fail(GDN_EINVAL, "gdn_delta_rule_noalloc: qkv 16-byte, o 8-byte alignment required");
+    if (!aligned(qkv, 16) || !aligned(o, 16)) return fail(GDN_EINVAL, "gdn_delta_rule_noalloc: qkv and o 16-byte alignment required");
     const size_t need = delta_scratch_bytes(static_cast<int>(s.hv), static_cast<int>(s.hk), static_cast<int>(s.d), n_tokens);
     if (need > GDN_NOALLOC_SCRATCH_BYTES) {
         const size_t per_chunk = delta_scratch_bytes(static_cast<int>(s.hv), static_cast<int>(s.hk), static_cast<int>(s.d), 1);

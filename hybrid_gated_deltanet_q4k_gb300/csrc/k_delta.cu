@@ -43,8 +43,9 @@
 // bits tf32 keeps, so o and S stay within ~5e-4 (relative L2) of the exact
 // recurrence on the test workloads.  Its range ends at 65504: q and k are unit
 // or smaller and A is bounded by |q||k|, but T, A T, S, R and Delta are
-// checked where they are rounded, and a value out of range sets ERR_RANGE in
-// this unit's error word (the result is then not to be used).
+// checked where they are rounded, as is the output o (written in fp16), and a
+// value out of range sets ERR_RANGE in this unit's error word (the result is
+// then not to be used).
 #include "common.cuh"
 #include "tma.cuh"
 #include "tcgen05.cuh"
@@ -72,7 +73,7 @@ struct DeltaArgs {
     uint16_t* KT;  // [nchunks][hk][D][DC]    K^T, fp16, in the swizzled operand image
     const float* state_in;  // [hv][D][D] or null
     float* state_out;
-    float* o;      // [n][c_v]
+    uint16_t* o;   // [n][c_v] fp16
 };
 
 __device__ __forceinline__ uint16_t f16_bits(float x) { return __half_as_ushort(__float2half_rn(x)); }
@@ -688,7 +689,7 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
         const bool own_d = D == 128 ? true : act;
         const int d = D == 128 ? 32 * q + lane : 16 * q + lane;
         const int vc = (i0 & 63) + v0;          // first V column of this warp in the 64-column V box
-        bool bad = false;                       // an S, R or Delta~ value outside the fp16 range
+        bool bad = false;                       // an S, R, Delta~ or o value outside the fp16 range
 
         float S[16];
 #pragma unroll
@@ -782,18 +783,22 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
             }
             if (j + 1 < a.nchunks) handover(NB_S);
 
-            // ---- O = diag(e^gamma) Y + Z (Y rows: lanes 0-63), while the next X, Y run
+            // ---- O = diag(e^gamma) Y + Z (Y rows: lanes 0-63), while the next X, Y run;
+            // written in fp16 (|o_i| <= max|S| |q|_1 <= 65504 for |q| <= d^-1/2; checked)
             if (!xw && mma_done(M_DZ, ph)) {
                 float y[16], z[16];
                 t5::ld16x2(tl + TM_XY + 32 * ph, y, tl + TM_DZ, z);
                 const int t = c * DC + tok;
                 if (t < a.n) {
-                    float4* dst = reinterpret_cast<float4*>(a.o + static_cast<int64_t>(t) * a.c_v + h * D + i0 + v0);
+                    float ov[2][8];
 #pragma unroll
-                    for (int m = 0; m < 4; ++m)
-                        dst[m] = make_float4(fmaf(gt.y, y[4 * m], z[4 * m]), fmaf(gt.y, y[4 * m + 1], z[4 * m + 1]),
-                                             fmaf(gt.y, y[4 * m + 2], z[4 * m + 2]),
-                                             fmaf(gt.y, y[4 * m + 3], z[4 * m + 3]));
+                    for (int v = 0; v < 16; ++v) {
+                        ov[v >> 3][v & 7] = fmaf(gt.y, y[v], z[v]);
+                        bad |= f16_out_of_range(ov[v >> 3][v & 7]);
+                    }
+                    uint4* dst = reinterpret_cast<uint4*>(a.o + static_cast<int64_t>(t) * a.c_v + h * D + i0 + v0);
+                    dst[0] = f16x8(ov[0]);
+                    dst[1] = f16x8(ov[1]);
                 }
             }
         }
@@ -955,7 +960,7 @@ static cudaError_t launch_delta_d(DeltaArgs& a, cudaStream_t st, bool overlap) {
 }
 
 cudaError_t launch_delta(const gdn_layer& L, const uint16_t* qkv, const float* log_a, const float* b, int64_t n,
-                         const float* state_in, float* state_out, float* o, void* scratch, cudaStream_t st,
+                         const float* state_in, float* state_out, uint16_t* o, void* scratch, cudaStream_t st,
                          bool overlap) {
     DeltaArgs a;
     const int d = L.dk;

@@ -14,11 +14,13 @@
 namespace gdn {
 
 constexpr int NORM_THREADS = 256;
-constexpr int NORM_MAX_HEADS_PER_WARP = 8;  // Hv <= 64
 
-template <int CPL, bool QUANT>
-__global__ void __launch_bounds__(NORM_THREADS)
-gated_norm_kernel(const float* __restrict__ o, const uint16_t* __restrict__ z, int64_t ld_z, int hv,
+// HPW heads per warp (Hv <= 8 HPW): the row's share of a thread lives in
+// registers sized for exactly that many heads, which keeps the kernel small
+// enough for 6 CTAs per SM and so enough loads in flight to cover HBM latency.
+template <int CPL, bool QUANT, int HPW>
+__global__ void __launch_bounds__(NORM_THREADS, HPW <= 4 ? 6 : 4)
+gated_norm_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ z, int64_t ld_z, int hv,
                   const float* __restrict__ norm_w, float eps, uint16_t* __restrict__ codes,
                   float* __restrict__ scale, float* __restrict__ out_f32) {
     __shared__ float red[32];
@@ -29,30 +31,33 @@ gated_norm_kernel(const float* __restrict__ o, const uint16_t* __restrict__ z, i
     float wv[CPL];
 #pragma unroll
     for (int i = 0; i < CPL; ++i) wv[i] = norm_w[lane * CPL + i];
-    // All of the warp's loads first (o as fp32, z as bf16 pairs), then the math:
+    // All of the warp's loads first (o as fp16 pairs, z as bf16 pairs), then the math:
     // a warp keeps its whole share of the row in flight.
-    float v[NORM_MAX_HEADS_PER_WARP][CPL];
-    uint32_t zb[NORM_MAX_HEADS_PER_WARP][CPL / 2];
+    float v[HPW][CPL];
+    uint32_t zb[HPW][CPL / 2];
 #pragma unroll
-    for (int hh = 0; hh < NORM_MAX_HEADS_PER_WARP; ++hh) {
+    for (int hh = 0; hh < HPW; ++hh) {
         const int h = warp + 8 * hh;
         if (h < hv) {
             const int c0 = h * D + lane * CPL;
             if (CPL == 4) {
-                const float4 f = __ldg(reinterpret_cast<const float4*>(o + t * c_v + c0));
-                v[hh][0] = f.x; v[hh][1 % CPL] = f.y; v[hh][2 % CPL] = f.z; v[hh][3 % CPL] = f.w;
+                const uint2 f = __ldg(reinterpret_cast<const uint2*>(o + t * c_v + c0));
+                const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&f.x));
+                const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&f.y));
+                v[hh][0] = f0.x; v[hh][1 % CPL] = f0.y; v[hh][2 % CPL] = f1.x; v[hh][3 % CPL] = f1.y;
                 const uint2 u = __ldg(reinterpret_cast<const uint2*>(z + t * ld_z + c0));
                 zb[hh][0] = u.x; zb[hh][1 % (CPL / 2)] = u.y;
             } else {
-                const float2 f = __ldg(reinterpret_cast<const float2*>(o + t * c_v + c0));
-                v[hh][0] = f.x; v[hh][1 % CPL] = f.y;
+                const uint32_t f = __ldg(reinterpret_cast<const uint32_t*>(o + t * c_v + c0));
+                const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&f));
+                v[hh][0] = f0.x; v[hh][1 % CPL] = f0.y;
                 zb[hh][0] = __ldg(reinterpret_cast<const uint32_t*>(z + t * ld_z + c0));
             }
         }
     }
     float amax = 0.0f;
 #pragma unroll
-    for (int hh = 0; hh < NORM_MAX_HEADS_PER_WARP; ++hh) {
+    for (int hh = 0; hh < HPW; ++hh) {
         const int h = warp + 8 * hh;
         if (h < hv) {
             const int c0 = h * D + lane * CPL;
@@ -79,7 +84,7 @@ gated_norm_kernel(const float* __restrict__ o, const uint16_t* __restrict__ z, i
     const QScale qsc = make_qscale(amax);
     if (threadIdx.x == 0) scale[t] = qsc.s;
 #pragma unroll
-    for (int hh = 0; hh < NORM_MAX_HEADS_PER_WARP; ++hh) {
+    for (int hh = 0; hh < HPW; ++hh) {
         const int h = warp + 8 * hh;
         if (h < hv) {
             const int c0 = h * D + lane * CPL;
@@ -102,20 +107,34 @@ gated_norm_kernel(const float* __restrict__ o, const uint16_t* __restrict__ z, i
     }
 }
 
-cudaError_t launch_gated_norm(const gdn_layer& L, const float* o, const uint16_t* z, int64_t ld_z, int64_t n,
+template <int CPL, bool QUANT>
+static void launch_norm_hpw(const gdn_layer& L, const uint16_t* o, const uint16_t* z, int64_t ld_z, unsigned grid,
+                            uint16_t* codes, float* scale, float* out_f32, cudaStream_t st) {
+    const int hpw = (L.n_v_heads + 7) / 8;
+    if (hpw <= 1)
+        gated_norm_kernel<CPL, QUANT, 1><<<grid, NORM_THREADS, 0, st>>>(o, z, ld_z, L.n_v_heads, L.norm_w, L.eps_rms, codes, scale, out_f32);
+    else if (hpw <= 2)
+        gated_norm_kernel<CPL, QUANT, 2><<<grid, NORM_THREADS, 0, st>>>(o, z, ld_z, L.n_v_heads, L.norm_w, L.eps_rms, codes, scale, out_f32);
+    else if (hpw <= 4)
+        gated_norm_kernel<CPL, QUANT, 4><<<grid, NORM_THREADS, 0, st>>>(o, z, ld_z, L.n_v_heads, L.norm_w, L.eps_rms, codes, scale, out_f32);
+    else
+        gated_norm_kernel<CPL, QUANT, 8><<<grid, NORM_THREADS, 0, st>>>(o, z, ld_z, L.n_v_heads, L.norm_w, L.eps_rms, codes, scale, out_f32);
+}
+
+cudaError_t launch_gated_norm(const gdn_layer& L, const uint16_t* o, const uint16_t* z, int64_t ld_z, int64_t n,
                               uint16_t* codes, float* scale, float* out_f32, cudaStream_t st) {
     const bool quant = L.wtype == GDN_W_Q4K;
     const unsigned grid = static_cast<unsigned>(n);
     if (L.dv == 128) {
         if (quant)
-            gated_norm_kernel<4, true><<<grid, NORM_THREADS, 0, st>>>(o, z, ld_z, L.n_v_heads, L.norm_w, L.eps_rms, codes, scale, out_f32);
+            launch_norm_hpw<4, true>(L, o, z, ld_z, grid, codes, scale, out_f32, st);
         else
-            gated_norm_kernel<4, false><<<grid, NORM_THREADS, 0, st>>>(o, z, ld_z, L.n_v_heads, L.norm_w, L.eps_rms, codes, scale, out_f32);
+            launch_norm_hpw<4, false>(L, o, z, ld_z, grid, codes, scale, out_f32, st);
     } else {
         if (quant)
-            gated_norm_kernel<2, true><<<grid, NORM_THREADS, 0, st>>>(o, z, ld_z, L.n_v_heads, L.norm_w, L.eps_rms, codes, scale, out_f32);
+            launch_norm_hpw<2, true>(L, o, z, ld_z, grid, codes, scale, out_f32, st);
         else
-            gated_norm_kernel<2, false><<<grid, NORM_THREADS, 0, st>>>(o, z, ld_z, L.n_v_heads, L.norm_w, L.eps_rms, codes, scale, out_f32);
+            launch_norm_hpw<2, false>(L, o, z, ld_z, grid, codes, scale, out_f32, st);
     }
     return cudaGetLastError();
 }

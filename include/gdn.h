@@ -253,13 +253,15 @@ int gdn_conv_state_update(const gdn_layer *layer, const uint16_t *qkvz, int64_t 
  * tensor cores with fp16 operands and fp32 accumulation; the state stays
  * fp32.  qkv: fp16 [N][C_conv] as written by gdn_conv (16-byte aligned);
  * log_a, b: fp32 [N][Hv]; state_in / state_out fp32 [Hv][dv][dk] (state_in
- * NULL = zero; may alias); o: fp32 [N][C_v].  scratch: 16-byte aligned device
- * bytes >= gdn_delta_rule_scratch_size(layer, N).  An intermediate outside
- * the fp16 range (T, A T, the state's fp16 image, R or Delta) is reported as
- * GDN_ERANGE by gdn_sync_status; o and the state are then not to be used.
+ * NULL = zero; may alias); o: fp16 [N][C_v] (16-byte aligned; rounded to
+ * nearest; |o| <= max|S| for |q| <= dk^-1/2).  scratch: 16-byte aligned device
+ * bytes >= gdn_delta_rule_scratch_size(layer, N).  An intermediate or output
+ * outside the fp16 range (T, A T, the state's fp16 image, R, Delta or o) is
+ * reported as GDN_ERANGE by gdn_sync_status; o and the state are then not to
+ * be used.
  */
 int gdn_delta_rule(const gdn_layer *layer, const uint16_t *qkv, const float *log_a, const float *b,
-                   int64_t n_tokens, const float *state_in, float *state_out, float *o,
+                   int64_t n_tokens, const float *state_in, float *state_out, uint16_t *o,
                    void *scratch, size_t scratch_bytes, void *stream);
 size_t gdn_delta_rule_scratch_size(const gdn_layer *layer, int64_t n_tokens);
 
@@ -288,17 +290,17 @@ size_t gdn_delta_rule_scratch_size(const gdn_layer *layer, int64_t n_tokens);
  */
 #define GDN_NOALLOC_SCRATCH_BYTES (48u << 20)
 int gdn_delta_rule_noalloc(const gdn_layer *layer, const uint16_t *qkv, const float *log_a, const float *b,
-                           int64_t n_tokens, const float *state_in, float *state_out, float *o,
+                           int64_t n_tokens, const float *state_in, float *state_out, uint16_t *o,
                            void *stream);
 
 /*
  * gdn_gated_norm -- step 4: per token and value head
- * o_hat = o / sqrt(mean(o^2) + eps_rms) * norm_w * SiLU(z), z bf16 at
- * z[t*ld_z + h*dv + i].  Q4_K layers: each token row of o_hat (all C_v
+ * o_hat = o / sqrt(mean(o^2) + eps_rms) * norm_w * SiLU(z), o fp16 [N][C_v]
+ * (8-byte aligned) as gdn_delta_rule writes it, z bf16 at z[t*ld_z + h*dv + i].  Q4_K layers: each token row of o_hat (all C_v
  * values) is quantised like gdn_quant_rows into codes [N][C_v] + scale [N]
  * (out_f32 unused).  F32 layers: o_hat is written to out_f32 [N][C_v].
  */
-int gdn_gated_norm(const gdn_layer *layer, const float *o, const uint16_t *z, int64_t ld_z,
+int gdn_gated_norm(const gdn_layer *layer, const uint16_t *o, const uint16_t *z, int64_t ld_z,
                    int64_t n_tokens, uint16_t *codes, float *scale, float *out_f32, void *stream);
 
 #ifdef __cplusplus

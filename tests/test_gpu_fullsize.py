@@ -66,7 +66,7 @@ def test_h4096_n32768_prefill():
     nbytes = L.gdn_delta_rule_scratch_size(sp, n)
     scratch = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
     state2 = torch.empty_like(state)
-    o = torch.empty(n, c_v, dtype=torch.float32, device=DEV)
+    o = torch.empty(n, c_v, dtype=torch.float16, device=DEV)
     L.gdn_delta_rule(sp, gl.ptr(qkv), gl.ptr(la), gl.ptr(bb), n, 0, gl.ptr(state2), gl.ptr(o), gl.ptr(scratch), nbytes, st)
     del scratch
     oc = torch.empty(n, c_v, dtype=torch.float16, device=DEV)
@@ -111,10 +111,10 @@ def test_h4096_n32768_prefill():
         kh = qkv_h[:, c_qk + hk * d:c_qk + (hk + 1) * d][:, None, :]
         vh = qkv_h[:, 2 * c_qk + h * d:2 * c_qk + (h + 1) * d][:, None, :]
         ro, rS = OL.gated_delta_rule(qh, kh, vh, tok["log_a"][:, h:h + 1], tok["b"][:, h:h + 1], np.zeros((1, d, d)))
-        assert rel_l2(o[:, h * d:(h + 1) * d].cpu().numpy(), ro[:, 0]) <= 2e-3
+        assert rel_l2(o[:, h * d:(h + 1) * d].float().cpu().numpy(), ro[:, 0]) <= 2e-3
         assert rel_l2(state[h].cpu().numpy(), rS[0]) <= 2e-3
     # 4: gated norm on sampled tokens
-    o_s = o[rows].cpu().numpy().reshape(len(rows), hv, d)
+    o_s = o[rows].float().cpu().numpy().reshape(len(rows), hv, d)
     z_s = bf16_host_f32(qkvz[rows, c_conv:]).reshape(len(rows), hv, d)
     oh = OL.gated_rmsnorm(o_s, z_s, layer["norm_w"], 1e-6).reshape(len(rows), -1)
     rqo, rso = quant.quant_rows_i8(oh.astype(np.float32))

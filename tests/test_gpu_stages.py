@@ -265,7 +265,7 @@ def test_delta_rule_stage(L, spec, n, with_state):
     qkv, lad, bd = f16_dev(qkv_h), f32_dev(la), f32_dev(b)
     sin = f32_dev(S0) if with_state else None
     sout = torch.empty(spec.n_v_heads, spec.dv, spec.dk, dtype=torch.float32, device=DEV)
-    o = torch.empty(n, spec.c_v, dtype=torch.float32, device=DEV)
+    o = torch.empty(n, spec.c_v, dtype=torch.float16, device=DEV)
     nbytes = L.gdn_delta_rule_scratch_size(ctypes.byref(s), n)
     scratch = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
     L.gdn_delta_rule(ctypes.byref(s), gl.ptr(qkv), gl.ptr(lad), gl.ptr(bd), n, gl.ptr(sin), gl.ptr(sout), gl.ptr(o),
@@ -273,7 +273,7 @@ def test_delta_rule_stage(L, spec, n, with_state):
     sync(L)
     S0r = S0 if with_state else np.zeros((spec.n_v_heads, spec.dv, spec.dk))
     ro, rS = OL.gated_delta_rule(qe, ke, ve, la, b, S0r)
-    assert rel_l2(o.cpu().numpy(), ro.reshape(n, -1)) <= 2e-3
+    assert rel_l2(o.float().cpu().numpy(), ro.reshape(n, -1)) <= 2e-3
     assert rel_l2(sout.cpu().numpy(), rS) <= 2e-3
 
 
@@ -299,7 +299,7 @@ def test_delta_rule_segments_bitwise(L):
                          gl.ptr(sout), gl.ptr(o[lo:hi]), gl.ptr(scratch), nbytes, stream())
         sync(L)
 
-    o_one = torch.empty(n, spec.c_v, dtype=torch.float32, device=DEV)
+    o_one = torch.empty(n, spec.c_v, dtype=torch.float16, device=DEV)
     st_one = torch.empty(spec.n_v_heads, spec.dv, spec.dk, dtype=torch.float32, device=DEV)
     run(0, n, f32_dev(S0), st_one, o_one)
     o_two = torch.empty_like(o_one)
@@ -308,7 +308,7 @@ def test_delta_rule_segments_bitwise(L):
     run(n1, n, st_two, st_two, o_two)
     assert torch.equal(o_one, o_two) and torch.equal(st_one, st_two)
     ro, rS = OL.gated_delta_rule(qe, ke, ve, la, b, S0)
-    assert rel_l2(o_one.cpu().numpy(), ro.reshape(n, -1)) <= 2e-3
+    assert rel_l2(o_one.float().cpu().numpy(), ro.reshape(n, -1)) <= 2e-3
     assert rel_l2(st_one.cpu().numpy(), rS) <= 2e-3
 
 
@@ -320,7 +320,7 @@ def test_delta_rule_state_aliasing(L):
     qkv_h, qe, ke, ve, la, b = _delta_inputs(spec, n, rng)
     S0 = rng.normal(0, 0.3, size=(spec.n_v_heads, spec.dv, spec.dk)).astype(np.float32)
     qkv, lad, bd, st = f16_dev(qkv_h), f32_dev(la), f32_dev(b), f32_dev(S0)
-    o = torch.empty(n, spec.c_v, dtype=torch.float32, device=DEV)
+    o = torch.empty(n, spec.c_v, dtype=torch.float16, device=DEV)
     nbytes = L.gdn_delta_rule_scratch_size(ctypes.byref(s), n)
     scratch = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
     L.gdn_delta_rule(ctypes.byref(s), gl.ptr(qkv), gl.ptr(lad), gl.ptr(bd), n, gl.ptr(st), gl.ptr(st), gl.ptr(o),
@@ -328,7 +328,7 @@ def test_delta_rule_state_aliasing(L):
     sync(L)
     ro, rS = OL.gated_delta_rule(qe, ke, ve, la, b, S0)
     assert rel_l2(st.cpu().numpy(), rS) <= 2e-3
-    assert rel_l2(o.cpu().numpy(), ro.reshape(n, -1)) <= 2e-3
+    assert rel_l2(o.float().cpu().numpy(), ro.reshape(n, -1)) <= 2e-3
 
 
 def test_delta_rule_reports_fp16_overflow(L):
@@ -340,7 +340,7 @@ def test_delta_rule_reports_fp16_overflow(L):
     n = 100
     qkv_h, qe, ke, ve, la, b = _delta_inputs(spec, n, rng)
     qkv, lad, bd = f16_dev(qkv_h), f32_dev(la), f32_dev(b)
-    o = torch.empty(n, spec.c_v, dtype=torch.float32, device=DEV)
+    o = torch.empty(n, spec.c_v, dtype=torch.float16, device=DEV)
     nbytes = L.gdn_delta_rule_scratch_size(ctypes.byref(s), n)
     scratch = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
     for scale, want in ((1.0e5, gl.GDN_ERANGE), (0.3, gl.GDN_OK)):
@@ -358,10 +358,11 @@ def test_delta_rule_reports_fp16_overflow(L):
 def test_gated_norm_stage(L, spec, n):
     layer, dev, s = _layer(spec, L)
     rng = np.random.default_rng(n + 5)
-    o = rng.normal(0, 0.05, size=(n, spec.c_v)).astype(np.float32)
+    # o in fp16, as gdn_delta_rule writes it
+    o = f16_round(rng.normal(0, 0.05, size=(n, spec.c_v)))
     zbits = synth._to_bf16_bits(rng.normal(0, 1, size=(n, spec.c_v)).astype(np.float32))
     z = synth.bf16_bits_to_f32(zbits)
-    od, zd = f32_dev(o), bf16_dev(zbits)
+    od, zd = f16_dev(o), bf16_dev(zbits)
     ref = OL.gated_rmsnorm(o.reshape(n, spec.n_v_heads, spec.dv), z.reshape(n, spec.n_v_heads, spec.dv),
                            layer["norm_w"], 1e-6).reshape(n, -1)
     if spec.wtype == "f32":
