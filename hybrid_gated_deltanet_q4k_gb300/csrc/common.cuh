@@ -99,6 +99,27 @@ __device__ __forceinline__ uint32_t codes_to_f16x2(float c0, float c1) {
 // e^-u = inf and the quotient -0.
 __device__ __forceinline__ float silu_f(float u) { return __fdividef(u, 1.0f + __expf(-u)); }
 
+// The causal depthwise conv of one channel at token t (taps w.x .. w.w on
+// x_{t-3} .. x_t) followed by SiLU.  Every kernel that evaluates the conv calls
+// this one function, so their results agree bit for bit.
+__device__ __forceinline__ float conv4_silu(const float4 w, float xm3, float xm2, float xm1, float x) {
+    float u = w.x * xm3;
+    u = fmaf(w.y, xm2, u);
+    u = fmaf(w.z, xm1, u);
+    u = fmaf(w.w, x, u);
+    return silu_f(u);
+}
+
+// Gates of one value head from the projection's beta and alpha columns:
+// log a = -exp(A_log) * softplus(alpha + dt_bias), b = sigmoid(beta).
+__device__ __forceinline__ void gate_values(float beta, float alpha, float A_log, float dt_bias, float& log_a,
+                                            float& b) {
+    const float u = alpha + dt_bias;
+    const float sp = fmaxf(u, 0.0f) + log1pf(expf(-fabsf(u)));
+    log_a = -expf(A_log) * sp;
+    b = 1.0f / (1.0f + expf(-beta));
+}
+
 // fp32 -> tf32 (10 explicit mantissa bits), round to nearest with ties away
 // from zero, as fp32 bits: half a tf32 unit (0x1000) is added to the
 // magnitude bits and the 13 low bits cleared; a carry into the exponent rounds

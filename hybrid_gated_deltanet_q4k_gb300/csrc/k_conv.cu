@@ -58,52 +58,23 @@ struct ConvArgs {
     int conv_blocks_y;     // gridDim.y slices that run the conv; the rest run gates
 };
 
-template <int CPL>
-__device__ __forceinline__ void conv_head_run(const ConvArgs& a, int head, int t0) {
+// Tokens t0 .. t0+NT-1 (those below t1 are written) of one head, one warp,
+// CPL channels per lane: xr holds the raw inputs of the tokens (packed bf16
+// pairs), h0, h1, h2 the three raw inputs before t0.  The conv, SiLU, the L2
+// norm of q and k heads (a warp reduction) and the fp16 store.
+template <int CPL, int NT>
+__device__ __forceinline__ void conv_head_tokens(const ConvArgs& a, int head, int t0, int t1,
+                                                 const uint32_t (&xr)[NT][CPL / 2], float (&h0)[CPL], float (&h1)[CPL],
+                                                 float (&h2)[CPL]) {
     const int lane = threadIdx.x & 31;
     const int c0 = head * a.d + lane * CPL;
-    float w[CPL][4];
-    float h0[CPL], h1[CPL], h2[CPL];  // x_{t-3}, x_{t-2}, x_{t-1}
+    float4 w[CPL];
 #pragma unroll
-    for (int i = 0; i < CPL; ++i) {
-        const float4 wv = *reinterpret_cast<const float4*>(a.conv_w + static_cast<int64_t>(c0 + i) * 4);
-        w[i][0] = wv.x; w[i][1] = wv.y; w[i][2] = wv.z; w[i][3] = wv.w;
-    }
-    auto raw = [&](int t, int i) -> float {
-        // raw input x_t of channel c0+i; t < 0 reads the conv state (oldest first)
-        if (t >= 0) return bf16_bits_to_float(a.qkvz[static_cast<int64_t>(t) * a.ld_qkvz + c0 + i]);
-        return a.tail[static_cast<int64_t>(c0 + i) * 3 + (3 + t)];
-    };
-#pragma unroll
-    for (int i = 0; i < CPL; ++i) {
-        h0[i] = raw(t0 - 3, i);
-        h1[i] = raw(t0 - 2, i);
-        h2[i] = raw(t0 - 1, i);
-    }
+    for (int i = 0; i < CPL; ++i) w[i] = *reinterpret_cast<const float4*>(a.conv_w + static_cast<int64_t>(c0 + i) * 4);
     const bool norm = head < a.n_qk_norm;
     const float mul = head < a.n_q ? a.q_scale : 1.0f;
-    const int t1 = min(a.n, t0 + CONV_TOKENS);
-    // All CONV_TOKENS rows of the run are loaded (packed bf16 pairs) before the
-    // first is used, so each warp keeps the whole run in flight.
-    uint32_t xr[CONV_TOKENS][CPL / 2];
 #pragma unroll
-    for (int k = 0; k < CONV_TOKENS; ++k) {
-        const int t = t0 + k;
-        if (t < t1) {
-            const uint16_t* src = a.qkvz + static_cast<int64_t>(t) * a.ld_qkvz + c0;
-            if (CPL == 4) {
-                const uint2 u = __ldg(reinterpret_cast<const uint2*>(src));
-                xr[k][0] = u.x; xr[k][1 % (CPL / 2)] = u.y;
-            } else {
-                xr[k][0] = __ldg(reinterpret_cast<const uint32_t*>(src));
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < CPL / 2; ++i) xr[k][i] = 0u;
-        }
-    }
-#pragma unroll
-    for (int k = 0; k < CONV_TOKENS; ++k) {
+    for (int k = 0; k < NT; ++k) {
         const int t = t0 + k;
         float y[CPL];
         float ss = 0.0f;
@@ -111,11 +82,7 @@ __device__ __forceinline__ void conv_head_run(const ConvArgs& a, int head, int t
         for (int i = 0; i < CPL; ++i) {
             const uint32_t xw = xr[k][i >> 1];
             const float x = __uint_as_float((i & 1) ? (xw & 0xffff0000u) : (xw << 16));
-            float u = w[i][0] * h0[i];
-            u = fmaf(w[i][1], h1[i], u);
-            u = fmaf(w[i][2], h2[i], u);
-            u = fmaf(w[i][3], x, u);
-            y[i] = silu_f(u);
+            y[i] = conv4_silu(w[i], h0[i], h1[i], h2[i], x);
             ss = fmaf(y[i], y[i], ss);
             h0[i] = h1[i]; h1[i] = h2[i]; h2[i] = x;
         }
@@ -140,6 +107,50 @@ __device__ __forceinline__ void conv_head_run(const ConvArgs& a, int head, int t
     }
 }
 
+// CPL raw inputs of a bf16 row at channel c0, as packed pairs.
+template <int CPL>
+__device__ __forceinline__ void load_raw(const uint16_t* src, uint32_t (&x)[CPL / 2]) {
+    if (CPL == 4) {
+        const uint2 u = __ldg(reinterpret_cast<const uint2*>(src));
+        x[0] = u.x; x[1 % (CPL / 2)] = u.y;
+    } else {
+        x[0] = __ldg(reinterpret_cast<const uint32_t*>(src));
+    }
+}
+
+template <int CPL>
+__device__ __forceinline__ void conv_head_run(const ConvArgs& a, int head, int t0) {
+    const int lane = threadIdx.x & 31;
+    const int c0 = head * a.d + lane * CPL;
+    float h0[CPL], h1[CPL], h2[CPL];  // x_{t-3}, x_{t-2}, x_{t-1}
+    auto raw = [&](int t, int i) -> float {
+        // raw input x_t of channel c0+i; t < 0 reads the conv state (oldest first)
+        if (t >= 0) return bf16_bits_to_float(a.qkvz[static_cast<int64_t>(t) * a.ld_qkvz + c0 + i]);
+        return a.tail[static_cast<int64_t>(c0 + i) * 3 + (3 + t)];
+    };
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+        h0[i] = raw(t0 - 3, i);
+        h1[i] = raw(t0 - 2, i);
+        h2[i] = raw(t0 - 1, i);
+    }
+    const int t1 = min(a.n, t0 + CONV_TOKENS);
+    // All CONV_TOKENS rows of the run are loaded (packed bf16 pairs) before the
+    // first is used, so each warp keeps the whole run in flight.
+    uint32_t xr[CONV_TOKENS][CPL / 2];
+#pragma unroll
+    for (int k = 0; k < CONV_TOKENS; ++k) {
+        const int t = t0 + k;
+        if (t < t1) {
+            load_raw<CPL>(a.qkvz + static_cast<int64_t>(t) * a.ld_qkvz + c0, xr[k]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < CPL / 2; ++i) xr[k][i] = 0u;
+        }
+    }
+    conv_head_tokens<CPL, CONV_TOKENS>(a, head, t0, t1, xr, h0, h1, h2);
+}
+
 template <int CPL>
 __global__ void __launch_bounds__(CONV_WARPS * 32, 3) conv_kernel(ConvArgs a) {
     const int t0 = blockIdx.x * CONV_TOKENS;
@@ -154,15 +165,13 @@ __global__ void __launch_bounds__(CONV_WARPS * 32, 3) conv_kernel(ConvArgs a) {
         const int t = t0 + i / a.hv, h = i % a.hv;
         const float beta = a.ba[static_cast<int64_t>(t) * a.ld_ba + h];
         const float alpha = a.ba[static_cast<int64_t>(t) * a.ld_ba + a.hv + h];
-        const float u = alpha + a.dt_bias[h];
-        const float sp = fmaxf(u, 0.0f) + log1pf(expf(-fabsf(u)));
-        a.log_a[static_cast<int64_t>(t) * a.hv + h] = -expf(a.A_log[h]) * sp;
-        a.b[static_cast<int64_t>(t) * a.hv + h] = 1.0f / (1.0f + expf(-beta));
+        gate_values(beta, alpha, a.A_log[h], a.dt_bias[h], a.log_a[static_cast<int64_t>(t) * a.hv + h],
+                    a.b[static_cast<int64_t>(t) * a.hv + h]);
     }
 }
 
-cudaError_t launch_conv(const gdn_layer& L, const uint16_t* qkvz, int64_t ld_qkvz, int64_t n, const float* tail,
-                        const float* ba, int64_t ld_ba, uint16_t* out, float* log_a, float* b, cudaStream_t st) {
+static ConvArgs conv_args(const gdn_layer& L, const uint16_t* qkvz, int64_t ld_qkvz, int64_t n, const float* tail,
+                          const float* ba, int64_t ld_ba, uint16_t* out, float* log_a, float* b) {
     ConvArgs a;
     a.qkvz = qkvz;
     a.ld_qkvz = ld_qkvz;
@@ -186,6 +195,12 @@ cudaError_t launch_conv(const gdn_layer& L, const uint16_t* qkvz, int64_t ld_qkv
     a.log_a = log_a;
     a.b = b;
     a.conv_blocks_y = (a.n_heads + CONV_WARPS - 1) / CONV_WARPS;
+    return a;
+}
+
+cudaError_t launch_conv(const gdn_layer& L, const uint16_t* qkvz, int64_t ld_qkvz, int64_t n, const float* tail,
+                        const float* ba, int64_t ld_ba, uint16_t* out, float* log_a, float* b, cudaStream_t st) {
+    const ConvArgs a = conv_args(L, qkvz, ld_qkvz, n, tail, ba, ld_ba, out, log_a, b);
     const bool gates = L.gate_log_a == nullptr;
     dim3 grid(static_cast<unsigned>((n + CONV_TOKENS - 1) / CONV_TOKENS), static_cast<unsigned>(a.conv_blocks_y + (gates ? 1 : 0)));
     if (L.dk == 128)

@@ -174,3 +174,85 @@ def test_errors_are_statuses_not_fallbacks():
     assert dl.prefill(bf16_dev(tok["x_bits"]), None, state, conv, y, small, check=False) == -2
     ws = dl.new_workspace(10)
     assert dl.prefill(bf16_dev(tok["x_bits"])[:0], None, state, conv, y, ws, check=False) == -1
+
+
+def _stage_by_stage(dl, spec, x, la, bb, state_in, conv_state):
+    """The layer through the stage entry points one by one (the conv as its own
+    kernel on the projection's bf16 output); returns y, the state and the conv
+    state.  la, bb = None: gates computed from the projection."""
+    import ctypes
+
+    from hybrid_gated_deltanet_q4k_gb300 import lib as gl
+
+    L = dl.lib
+    n, H, hv = x.shape[0], spec.hidden, spec.n_v_heads
+    c_v, c_conv, r_in = spec.c_v, spec.c_conv, spec.r_in
+    nbf = spec.c_conv + spec.c_v
+    s = dl.struct(la, bb)
+    sp = ctypes.byref(s)
+    st = gl.stream_handle()
+    wc_in = torch.empty(r_in, H, dtype=torch.float16, device=DEV)
+    ws_in = torch.empty(r_in, dtype=torch.float32, device=DEV)
+    wc_out = torch.empty(H, c_v, dtype=torch.float16, device=DEV)
+    ws_out = torch.empty(H, dtype=torch.float32, device=DEV)
+    L.gdn_q4k_deq_codes(gl.ptr(dl.dev["w_in"]), r_in, H, gl.ptr(wc_in), gl.ptr(ws_in), st)
+    L.gdn_q4k_deq_codes(gl.ptr(dl.dev["w_out"]), H, c_v, gl.ptr(wc_out), gl.ptr(ws_out), st)
+    xc = torch.empty(n, H, dtype=torch.float16, device=DEV)
+    sx = torch.empty(n, dtype=torch.float32, device=DEV)
+    L.gdn_quant_rows(gl.ptr(x), n, H, gl.ptr(xc), gl.ptr(sx), st)
+    qkvz = torch.empty(n, nbf, dtype=torch.bfloat16, device=DEV)
+    ba = torch.empty(n, 2 * hv, dtype=torch.float32, device=DEV)
+    L.gdn_gemm_codes(gl.ptr(xc), gl.ptr(sx), gl.ptr(wc_in), gl.ptr(ws_in), n, r_in, H, gl.ptr(qkvz), nbf, nbf,
+                     gl.ptr(ba), 2 * hv, st)
+    qkv = torch.empty(n, c_conv, dtype=torch.float16, device=DEV)
+    la_c = torch.empty(n, hv, dtype=torch.float32, device=DEV)
+    b_c = torch.empty(n, hv, dtype=torch.float32, device=DEV)
+    L.gdn_conv(sp, gl.ptr(qkvz), nbf, n, gl.ptr(conv_state), gl.ptr(ba), 2 * hv, gl.ptr(qkv), gl.ptr(la_c),
+               gl.ptr(b_c), st)
+    L.gdn_conv_state_update(sp, gl.ptr(qkvz), nbf, n, gl.ptr(conv_state), st)
+    nbytes = L.gdn_delta_rule_scratch_size(sp, n)
+    scratch = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    state = torch.empty_like(state_in)
+    o = torch.empty(n, c_v, dtype=torch.float16, device=DEV)
+    ga, gb = (la, bb) if la is not None else (la_c, b_c)
+    L.gdn_delta_rule(sp, gl.ptr(qkv), gl.ptr(ga), gl.ptr(gb), n, gl.ptr(state_in), gl.ptr(state), gl.ptr(o),
+                     gl.ptr(scratch), nbytes, st)
+    oc = torch.empty(n, c_v, dtype=torch.float16, device=DEV)
+    so = torch.empty(n, dtype=torch.float32, device=DEV)
+    z = qkvz[:, c_conv:]
+    L.gdn_gated_norm(sp, gl.ptr(o), gl.ptr(z), nbf, n, gl.ptr(oc), gl.ptr(so), 0, st)
+    y = torch.empty(n, H, dtype=torch.bfloat16, device=DEV)
+    L.gdn_gemm_codes(gl.ptr(oc), gl.ptr(so), gl.ptr(wc_out), gl.ptr(ws_out), n, H, c_v, gl.ptr(y), H, H, 0, 0, st)
+    torch.cuda.synchronize()
+    return y, state, conv_state
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 127, 128, 130, 300, 515])
+@pytest.mark.parametrize("gates", ["drawn", "computed"])
+def test_prefill_equals_stage_calls(n, gates):
+    """gdn_prefill runs the conv in the input projection's epilogue (one thread
+    holds a token's head; the three tokens before it come from the lanes below,
+    the previous quarter of the tile, or the conv state) and fixes up the first
+    three tokens of every 128-token tile after the first in a separate pass.
+    It must give the same bits as the stage entry points called one by one,
+    whose conv is its own kernel: for lengths around the tile and quarter
+    boundaries, a nonzero initial conv state (not bf16-exact), drawn and
+    computed gates."""
+    spec = SMALL
+    layer = synth.make_layer(spec)
+    tok = synth.make_tokens(spec, n, seed=40 + n)
+    dl = DeviceLayer(spec, layer)
+    rng = np.random.default_rng(n)
+    x = _x_dev(spec, tok)
+    la, bb = (f32_dev(tok["log_a"]), f32_dev(tok["b"])) if gates == "drawn" else (None, None)
+    s0 = f32_dev(rng.normal(0, 0.3, size=(spec.n_v_heads, spec.dv, spec.dk)))
+    c0 = f32_dev(rng.normal(0, 1.0, size=(spec.c_conv, 3)))
+    state, conv = s0.clone(), c0.clone()
+    y = _new_y(spec, n)
+    ws = dl.new_workspace(n)
+    dl.prefill(x, state, state, conv, y, ws, gate_log_a=la, gate_b=bb)
+    torch.cuda.synchronize()
+    y2, state2, conv2 = _stage_by_stage(dl, spec, x, la, bb, s0, c0.clone())
+    assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
+    assert torch.equal(state, state2)
+    assert torch.equal(conv, conv2)
