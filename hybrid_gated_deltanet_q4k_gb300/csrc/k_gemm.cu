@@ -12,21 +12,33 @@
 // segment to int32 and sums the segments in registers.  The result is the
 // exact integer product whatever the data.
 //
-// Kernel structure (one persistent CTA per SM, 320 threads):
-//   warp 0      TMA producer: 128x64 A tile + 256x64 B tile per stage into
-//               128-byte-swizzled shared memory, 4 stages (48 KB each);
-//   warp 1      TMEM allocator and MMA issuer: tcgen05.mma kind::f16,
-//               M=128 N=256 K=16, one elected thread, fp32 accumulators in
-//               two 256-column TMEM buffers (one per K segment, ping-pong);
-//   warps 2-9   epilogue: tcgen05.ld of each finished segment (warp w reads
-//               TMEM lanes 32*(w%4).., half (w-2)/4 of the 256 columns), int32
-//               running sums in registers, then the fp32 rescale and the
-//               stores.  The buffer is released right after it is read, so
+// Kernel structure: persistent pairs of CTAs (thread-block clusters of 2, one
+// CTA per SM, 320 threads each) on the fifth-generation tensor cores' two-SM
+// mode (tcgen05 .cta_group::2).  A pair computes 256 x 256 output tiles: each
+// CTA stages its 128 rows of A and its half (128 rows) of B, and one
+// instruction of the even CTA multiplies M = 256 (both CTAs' A rows) by
+// N = 256 (both B halves), each CTA's TMEM receiving its own 128 rows.  Per
+// output element a CTA stages and reads a third less shared memory than a
+// one-SM M = 128, N = 256 product, whose operand traffic (TMA writes plus
+// tensor reads) is what bounds it.
+//   warp 0      TMA producer (both CTAs): 128x64 A tile + 128x64 B half per
+//               stage, 6 stages of 32 KB, 128-byte swizzle; every copy of the
+//               pair completes on the even CTA's stage barrier;
+//   warp 1      TMEM allocator (both CTAs, one collective pair allocation of
+//               512 columns) and, in the even CTA, the MMA issuer:
+//               tcgen05.mma.cta_group::2 kind::f16 M=256 N=256 K=16, fp32
+//               accumulators in two 256-column buffers (one per K segment,
+//               ping-pong); its commits signal both CTAs' barriers;
+//   warps 2-9   epilogue (both CTAs): tcgen05.ld of each finished segment of
+//               the CTA's 128 rows (warp w reads TMEM lanes 32*(w%4).., half
+//               (w-2)/4 of the 256 columns), int32 running sums in registers,
+//               then the fp32 rescale and the stores.  Each warp releases the
+//               buffer right after reading it (to the even CTA's barrier), so
 //               the next segment's MMAs overlap the conversion and stores.
 // Every wait is bounded (about two seconds); a wait that runs out records
 // ERR_WAIT_TIMEOUT in this unit's error word and the CTA winds down: it waits
-// (bounded) for its own TMA copies and MMAs in flight, frees its TMEM and
-// returns.
+// (bounded) for the copies and MMAs in flight, meets its peer at the closing
+// cluster barrier, frees the TMEM and returns.
 #include "common.cuh"
 
 #include <cuda.h>
@@ -39,13 +51,13 @@ namespace gdn {
 static __device__ int g_gemm_error;
 
 namespace tc {
-constexpr int BM = 128;
-constexpr int BN = 256;
+constexpr int BM = 128;              // A rows per CTA (a pair covers 2 * BM)
+constexpr int BN = 256;              // output columns per tile (each CTA stages BN / 2 rows of B)
 constexpr int BK = 64;               // fp16 elements = 128 bytes = one swizzle row
-constexpr int STAGES = 4;
+constexpr int STAGES = 6;
 constexpr int SEG_KB = 16;           // k-blocks per exact fp32 segment (16 * 64 = 1024)
 constexpr int A_BYTES = BM * BK * 2; // 16 KB
-constexpr int B_BYTES = BN * BK * 2; // 32 KB
+constexpr int B_BYTES = BN / 2 * BK * 2; // 16 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int THREADS = 64 + NUM_EPI_WARPS * 32;
@@ -58,7 +70,8 @@ constexpr uint64_t DRAIN_LIMIT_NS = 20000000ull;
 // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B fp16
 // (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0), N>>3 at bits 17-22,
 // M>>4 at bits 24-28.
-constexpr uint32_t IDESC = (1u << 4) | (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
+// The pair instruction: M = 2 * BM.
+constexpr uint32_t IDESC = (1u << 4) | (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>((2 * BM) >> 4) << 24);
 }  // namespace tc
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -114,12 +127,36 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
 }
 
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
+// TMA into this CTA's shared memory; completion is counted on the mbarrier at
+// shared::cluster address `bar` (the even CTA's, for either CTA of the pair).
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
             smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
         : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// shared::cluster address of this CTA's shared variable at `p` in CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// arrive once on the mbarrier at shared::cluster address `bar` (possibly the peer's)
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -136,18 +173,25 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
            (static_cast<uint64_t>(2) << 61);
 }
 
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+// The pair product: descriptors address this (even) CTA's tiles; the odd CTA's
+// tiles sit at the same offsets of its shared memory.
+__device__ __forceinline__ void mma_f16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(tc::IDESC), "r"(accumulate)
         : "memory");
 }
 
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-                 : "memory");
+// Arrive on the mbarrier at this offset in both CTAs of the pair once the MMAs
+// issued so far have completed.
+__device__ __forceinline__ void mma_commit_pair(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(static_cast<uint16_t>(3))
+        : "memory");
 }
 
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
@@ -202,8 +246,8 @@ __device__ __forceinline__ void store_group8(const GemmArgs& g, int row, int n, 
     }
 }
 
-// Tile order: groups of GROUP_N column tiles, and within a group the 148-odd
-// tiles in flight at a time span ~GROUP_N columns x ~10 row blocks.  The
+// Tile order: groups of GROUP_N column tiles, and within a group the ~76 pair
+// tiles in flight at a time span ~GROUP_N columns x ~5 row blocks of 256.  The
 // group's B columns (GROUP_N * 256 rows of K codes, 32 MB at K = 4096) stay in
 // L2 while A streams through once per group; in plain row-major order every
 // row block sweeps all of B, which for a large B (the input projection's is
@@ -214,11 +258,11 @@ __device__ __forceinline__ void tile_origin(int tile, int num_m, int num_n, int&
     const int first = group * GROUP_N;
     const int width = min(GROUP_N, num_n - first);
     const int r = tile - group * GROUP_N * num_m;
-    m0 = (r / width) * tc::BM;
+    m0 = (r / width) * (2 * tc::BM);
     n0 = (first + r % width) * tc::BN;
 }
 
-__global__ void __launch_bounds__(tc::THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
 gemm_codes_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmArgs g) {
     using namespace tc;
     extern __shared__ uint8_t smem_raw[];
@@ -231,71 +275,78 @@ gemm_codes_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int num_m = (g.M + BM - 1) / BM, num_n = (g.N + BN - 1) / BN;
+    const uint32_t rank = cluster_rank();
+    const bool leader = rank == 0;
+    const int pair = blockIdx.x >> 1, num_pairs = gridDim.x >> 1;
+    const int num_m = (g.M + 2 * BM - 1) / (2 * BM), num_n = (g.N + BN - 1) / BN;
     const int num_tiles = num_m * num_n;
     const int nkb = g.K / BK;
     const int nseg = (nkb + SEG_KB - 1) / SEG_KB;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&full[s], 1);     // even CTA: its producer's arrive (+ both CTAs' bytes)
+            mbar_init(&empty[s], 1);    // the pair's commit
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&acc_full[b], 1);
-            mbar_init(&acc_empty[b], NUM_EPI_WARPS * 32);
+            mbar_init(&acc_full[b], 1);                     // the pair's commit
+            mbar_init(&acc_empty[b], 2 * NUM_EPI_WARPS);    // even CTA: one arrival per epilogue warp of the pair
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                      "r"(TMEM_COLS)
                      : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
     }
     tc_fence_before();
-    __syncthreads();
+    // both CTAs' barriers are initialised before either signals the other's
+    cluster_sync();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
     if (warp == 0) {
         if (lane == 0) {
-            // ------------------------------------------------ TMA producer
+            // ------------------------------------------------ TMA producer (both CTAs)
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+            const uint32_t full0 = cluster_addr(&full[0], 0);   // the even CTA's stage barriers
             uint32_t stage = 0, phase = 0;
-            uint32_t armed = 0;              // bit s: stage s has been filled at least once
+            uint32_t armed = 0;              // bit s: stage s has been filled at least once (even CTA)
             uint32_t armed_parity = 0;       // bit s: parity of its last fill
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            for (int tile = pair; ok && tile < num_tiles; tile += num_pairs) {
                 int m0, n0;
                 tile_origin(tile, num_m, num_n, m0, n0);
                 for (int kb = 0; kb < nkb; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
                     uint8_t* sA = smem + stage * STAGE_BYTES;
-                    mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
-                    tma_load_2d(sA, &tmA, &full[stage], kb * BK, m0);
-                    tma_load_2d(sA + A_BYTES, &tmB, &full[stage], kb * BK, n0);
+                    if (leader) mbar_arrive_expect_tx(&full[stage], 2 * STAGE_BYTES);
+                    tma_load_2d_pair(sA, &tmA, full0 + 8 * stage, kb * BK, m0 + static_cast<int>(rank) * BM);
+                    tma_load_2d_pair(sA + A_BYTES, &tmB, full0 + 8 * stage, kb * BK, n0 + static_cast<int>(rank) * (BN / 2));
                     armed |= 1u << stage;
                     armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
             }
-            // Let every copy this thread issued land before the CTA exits.
-            for (int s = 0; s < STAGES; ++s)
-                if (armed & (1u << s)) {
-                    int dummy = 0;
-                    mbar_wait(&full[s], (armed_parity >> s) & 1u, reinterpret_cast<volatile int*>(&dummy), DRAIN_LIMIT_NS);
-                }
+            // Let every copy of the pair land before the CTAs exit (the even CTA's
+            // barriers count the odd CTA's copies too).
+            if (leader)
+                for (int s = 0; s < STAGES; ++s)
+                    if (armed & (1u << s)) {
+                        int dummy = 0;
+                        mbar_wait(&full[s], (armed_parity >> s) & 1u, reinterpret_cast<volatile int*>(&dummy), DRAIN_LIMIT_NS);
+                    }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            // ------------------------------------------------ MMA issuer
+        if (lane == 0 && leader) {
+            // ------------------------------------------------ MMA issuer (even CTA)
             uint32_t stage = 0, phase = 0, acc_ctr = 0;
             bool ok = true, committed = false;
             uint32_t last_buf = 0, last_par = 0;
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            for (int tile = pair; ok && tile < num_tiles; tile += num_pairs) {
                 for (int seg = 0; ok && seg < nseg; ++seg) {
                     const uint32_t buf = acc_ctr & 1u, par = (acc_ctr >> 1) & 1u;
                     if (!mbar_wait(&acc_empty[buf], par ^ 1u, abort_flag)) { ok = false; break; }
@@ -310,11 +361,11 @@ gemm_codes_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         const uint64_t bdesc = sw128_desc(sa_addr + A_BYTES);
 #pragma unroll
                         for (int kk = 0; kk < BK / 16; ++kk)
-                            mma_f16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, (kb > kb0 || kk > 0) ? 1u : 0u);
-                        mma_commit(&empty[stage]);
+                            mma_f16_pair(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, (kb > kb0 || kk > 0) ? 1u : 0u);
+                        mma_commit_pair(&empty[stage]);
                         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                     }
-                    mma_commit(&acc_full[buf]);
+                    mma_commit_pair(&acc_full[buf]);
                     committed = true;
                     last_buf = buf;
                     last_par = par;
@@ -328,14 +379,16 @@ gemm_codes_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             }
         }
     } else {
-        // ---------------------------------------------------- epilogue
+        // ---------------------------------------------------- epilogue (both CTAs)
         const int quarter = warp & 3;
         const int half = (warp - 2) >> 2;
+        const uint32_t acc_empty0 = cluster_addr(&acc_empty[0], 0);
         uint32_t acc_ctr = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        for (int tile = pair; ok && tile < num_tiles; tile += num_pairs) {
             int m0, n0;
             tile_origin(tile, num_m, num_n, m0, n0);
+            m0 += static_cast<int>(rank) * BM;
             int32_t acc[128];
 #pragma unroll
             for (int i = 0; i < 128; ++i) acc[i] = 0;
@@ -354,7 +407,8 @@ gemm_codes_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     for (int j = 0; j < 32; ++j) acc[c * 32 + j] += __float2int_rn(__uint_as_float(r[j]));
                 }
                 tc_fence_before();
-                mbar_arrive(&acc_empty[buf]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(acc_empty0 + 8 * buf);
                 ++acc_ctr;
             }
             if (!ok) break;
@@ -381,9 +435,12 @@ gemm_codes_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 
     tc_fence_before();
     __syncthreads();
+    // neither CTA frees its shared memory or TMEM while the pair's MMAs may
+    // still read the one or write the other
+    cluster_sync();
     if (warp == 1) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS) : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS) : "memory");
     }
 }
 
@@ -424,13 +481,39 @@ static int sm_count() {
     return n > 0 ? n : 1;
 }
 
+// Clusters of 2 CTAs of the projection kernel that fit on the device at once.
+static int resident_pairs() {
+    static int cached = 0;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(sm_count()), 1, 1);
+        cfg.blockDim = dim3(tc::THREADS, 1, 1);
+        cfg.dynamicSmemBytes = tc::SMEM_BYTES;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = 2;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, gemm_codes_kernel, &cfg) != cudaSuccess || n < 1) {
+            cudaGetLastError();
+            n = sm_count() / 2;
+        }
+        cached = n;
+    });
+    return cached;
+}
+
 // Returns cudaErrorInvalidValue when a tensor map cannot be built (caller
 // validated shapes and alignment first).
 cudaError_t launch_gemm_codes(const uint16_t* a, const float* sa, const uint16_t* b, const float* sb, int64_t M,
                               int64_t N, int64_t K, uint16_t* out_bf16, int64_t ld_bf16, int64_t n_bf16,
                               float* out_f32, int64_t ld_f32, cudaStream_t st) {
     CUtensorMap ma, mb;
-    if (!make_map(&ma, a, M, K, tc::BM) || !make_map(&mb, b, N, K, tc::BN)) return cudaErrorInvalidValue;
+    if (!make_map(&ma, a, M, K, tc::BM) || !make_map(&mb, b, N, K, tc::BN / 2)) return cudaErrorInvalidValue;
     static std::once_flag attr_once;
     std::call_once(attr_once, [] {
         cudaFuncSetAttribute(gemm_codes_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_BYTES);
@@ -450,8 +533,12 @@ cudaError_t launch_gemm_codes(const uint16_t* a, const float* sa, const uint16_t
     const bool f_ok = out_f32 == nullptr ||
                       ((reinterpret_cast<uintptr_t>(out_f32) & 15) == 0 && ld_f32 % 4 == 0 && n_bf16 % 4 == 0);
     g.vec_ok = (bf_ok && f_ok) ? 1 : 0;
-    const int64_t tiles = ((M + tc::BM - 1) / tc::BM) * ((N + tc::BN - 1) / tc::BN);
-    const int grid = static_cast<int>(tiles < sm_count() ? tiles : sm_count());
+    // pairs of CTAs (clusters of 2): as many as can be resident at once (a
+    // cluster stays within one GPC), at most one per tile
+    const int64_t tiles = ((M + 2 * tc::BM - 1) / (2 * tc::BM)) * ((N + tc::BN - 1) / tc::BN);
+    const int max_pairs = resident_pairs();
+    const int pairs = static_cast<int>(tiles < max_pairs ? tiles : max_pairs);
+    const int grid = 2 * (pairs > 0 ? pairs : 1);
     gemm_codes_kernel<<<grid, tc::THREADS, tc::SMEM_BYTES, st>>>(ma, mb, g);
     return cudaGetLastError();
 }
