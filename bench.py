@@ -385,7 +385,13 @@ def run_ours(args, dist, spec):
                          f"projections as fp64 matmuls on the exact int8 operands, recurrence one token at a time)"}
 
     passes = 1
-    launches = (1 + 8 * passes) * K   # one weight-dequant launch, eight per token pass
+    # per step: weight decode (one launch, both matrices); per token pass: x
+    # quantisation, input projection, conv, conv state, the delta rule's prep
+    # and state pass per token segment of 64 chunks (one segment up to 64
+    # chunks), gated norm, output projection
+    nch = (n + 63) // 64
+    segments = 1 if nch <= 64 else (nch + 63) // 64
+    launches = (1 + (1 + 1 + 2 + 2 * segments + 2) * passes) * K
     if dist.rank == 0:
         print(json.dumps({
             "metric": METRIC, "value": n * dist.world / (ms_max / 1e3), "unit": UNIT, "n_gpus": dist.world,

@@ -49,6 +49,7 @@
 #include "common.cuh"
 #include "tma.cuh"
 #include "tcgen05.cuh"
+#include "streams.h"
 
 #include <mutex>
 
@@ -865,41 +866,11 @@ int read_and_clear_delta_error() {
 }
 
 // Token segments of DELTA_SEG_CHUNKS chunks.  With more than one, the prep
-// of segment i+1 runs on a low-priority stream while the state pass of
-// segment i runs on a high-priority one (the state is carried between
-// segments in state_out, fp32, so the results are those of one launch).  The
-// two library streams are forked from the caller's stream and joined back to
-// it, so the call stays ordered on that stream and can be captured in a CUDA
-// graph.
+// of segment i+1 runs on the library's low-priority stream while the state
+// pass of segment i runs on its high-priority one (the state is carried
+// between segments in state_out, fp32, so the results are those of one
+// launch).  Both are forked from the caller's stream and joined back to it.
 constexpr int DELTA_SEG_CHUNKS = 64;
-constexpr int DELTA_MAX_DEVICES = 64;
-
-struct DeltaStreams {
-    cudaStream_t prep = nullptr, state = nullptr;
-    cudaEvent_t fork = nullptr, seg = nullptr;
-};
-static std::mutex g_delta_streams_mu;   // guards the table and each enqueue sequence
-static DeltaStreams g_delta_streams[DELTA_MAX_DEVICES];
-
-static cudaError_t delta_streams(DeltaStreams** out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= DELTA_MAX_DEVICES) return cudaErrorInvalidDevice;
-    DeltaStreams& s = g_delta_streams[dev];
-    if (!s.seg) {
-        int least = 0, greatest = 0;
-        if ((e = cudaDeviceGetStreamPriorityRange(&least, &greatest)) != cudaSuccess) return e;
-        if (!s.prep && (e = cudaStreamCreateWithPriority(&s.prep, cudaStreamNonBlocking, least)) != cudaSuccess) return e;
-        if (!s.state && (e = cudaStreamCreateWithPriority(&s.state, cudaStreamNonBlocking, greatest)) != cudaSuccess)
-            return e;
-        if (!s.fork && (e = cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
-        if ((e = cudaEventCreateWithFlags(&s.seg, cudaEventDisableTiming)) != cudaSuccess) return e;
-    }
-    *out = &s;
-    return cudaSuccess;
-}
-
 template <int D>
 static void launch_prep(const CUtensorMap& map, const DeltaArgs& a, cudaStream_t st) {
     delta_prep_kernel<D><<<dim3(a.nchunks, a.hv / a.ratio), DELTA_THREADS, PrepSmem<D>::BYTES + 1024, st>>>(map, a);
@@ -931,31 +902,32 @@ static cudaError_t launch_delta_d(DeltaArgs& a, cudaStream_t st, bool overlap) {
         launch_state<D>(map, a, st);
         return cudaGetLastError();
     }
-    std::lock_guard<std::mutex> lock(g_delta_streams_mu);
-    DeltaStreams* ds = nullptr;
-    cudaError_t e = delta_streams(&ds);
+    std::lock_guard<std::mutex> lock(lib_streams_mutex());
+    LibStreams* ls = nullptr;
+    cudaError_t e = lib_streams(&ls);
     if (e != cudaSuccess) return e;
-    if ((e = cudaEventRecord(ds->fork, st)) != cudaSuccess) return e;
-    if ((e = cudaStreamWaitEvent(ds->prep, ds->fork, 0)) != cudaSuccess) return e;
-    if ((e = cudaStreamWaitEvent(ds->state, ds->fork, 0)) != cudaSuccess) return e;
+    cudaStream_t prep_st = ls->lo, state_st = ls->hi;
+    if ((e = cudaEventRecord(ls->ev_a, st)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(prep_st, ls->ev_a, 0)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(state_st, ls->ev_a, 0)) != cudaSuccess) return e;
     cudaError_t first = cudaSuccess;
     for (int c0 = 0; c0 < nch && first == cudaSuccess; c0 += DELTA_SEG_CHUNKS) {
         DeltaArgs s = a;
         s.chunk0 = c0;
         s.nchunks = nch - c0 < DELTA_SEG_CHUNKS ? nch - c0 : DELTA_SEG_CHUNKS;
         if (c0 > 0) s.state_in = a.state_out;
-        launch_prep<D>(map, s, ds->prep);
+        launch_prep<D>(map, s, prep_st);
         if ((first = cudaGetLastError()) != cudaSuccess) break;
-        if ((first = cudaEventRecord(ds->seg, ds->prep)) != cudaSuccess) break;
-        if ((first = cudaStreamWaitEvent(ds->state, ds->seg, 0)) != cudaSuccess) break;
-        launch_state<D>(map, s, ds->state);
+        if ((first = cudaEventRecord(ls->ev_b, prep_st)) != cudaSuccess) break;
+        if ((first = cudaStreamWaitEvent(state_st, ls->ev_b, 0)) != cudaSuccess) break;
+        launch_state<D>(map, s, state_st);
         first = cudaGetLastError();
     }
     // join both library streams back to the caller's stream, also after a failure
-    e = cudaEventRecord(ds->seg, ds->prep);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(ds->state, ds->seg, 0);
-    if (e == cudaSuccess) e = cudaEventRecord(ds->fork, ds->state);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ds->fork, 0);
+    e = cudaEventRecord(ls->ev_b, prep_st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(state_st, ls->ev_b, 0);
+    if (e == cudaSuccess) e = cudaEventRecord(ls->ev_a, state_st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ls->ev_a, 0);
     return first != cudaSuccess ? first : e;
 }
 

@@ -1,0 +1,33 @@
+#include "streams.h"
+
+namespace gdn {
+
+namespace {
+constexpr int kMaxDevices = 64;
+LibStreams g_streams[kMaxDevices];
+}  // namespace
+
+std::mutex& lib_streams_mutex() {
+    static std::mutex mu;
+    return mu;
+}
+
+cudaError_t lib_streams(LibStreams** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    LibStreams& s = g_streams[dev];
+    if (!s.ev_b) {
+        int least = 0, greatest = 0;
+        if ((e = cudaDeviceGetStreamPriorityRange(&least, &greatest)) != cudaSuccess) return e;
+        if (!s.lo && (e = cudaStreamCreateWithPriority(&s.lo, cudaStreamNonBlocking, least)) != cudaSuccess) return e;
+        if (!s.hi && (e = cudaStreamCreateWithPriority(&s.hi, cudaStreamNonBlocking, greatest)) != cudaSuccess) return e;
+        if (!s.ev_a && (e = cudaEventCreateWithFlags(&s.ev_a, cudaEventDisableTiming)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&s.ev_b, cudaEventDisableTiming)) != cudaSuccess) return e;
+    }
+    *out = &s;
+    return cudaSuccess;
+}
+
+}  // namespace gdn

@@ -1,0 +1,26 @@
+// Two streams and two events of the library per device, for work that runs
+// beside the caller's stream within one call: forked from the caller's stream
+// and joined back to it before the call returns, so the call stays ordered on
+// that stream and a stream capture records it.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+namespace gdn {
+
+struct LibStreams {
+    cudaStream_t lo = nullptr;   // least priority
+    cudaStream_t hi = nullptr;   // greatest priority
+    cudaEvent_t ev_a = nullptr, ev_b = nullptr;   // timing disabled
+};
+
+// Guards the table and every enqueue sequence that uses the streams and events.
+std::mutex& lib_streams_mutex();
+
+// The current device's streams and events, created on first use (call with
+// lib_streams_mutex() held).
+cudaError_t lib_streams(LibStreams** out);
+
+}  // namespace gdn
