@@ -37,6 +37,7 @@ cudaError_t launch_gated_norm(const gdn_layer&, const uint16_t*, const uint16_t*
 int read_and_clear_gemm_error();
 int read_and_clear_delta_error();
 int read_and_clear_conv_error();
+int read_and_clear_norm_error();
 }  // namespace gdn
 
 using namespace gdn;
@@ -393,6 +394,8 @@ int gdn_sync_status(void* stream) {
     if (read_and_clear_gemm_error()) return fail(GDN_ETIMEOUT, "a bounded wait in the projection kernel ran out");
     const int dcode = read_and_clear_delta_error();
     const int ccode = read_and_clear_conv_error();
+    if (read_and_clear_norm_error() == ERR_WAIT_TIMEOUT)
+        return fail(GDN_ETIMEOUT, "a bounded wait in the gated-norm kernel ran out");
     if (dcode == ERR_WAIT_TIMEOUT) return fail(GDN_ETIMEOUT, "a bounded wait in the delta-rule kernel ran out");
     if (ccode == ERR_RANGE || dcode == ERR_RANGE)
         return fail(GDN_ERANGE, "a %s value exceeded the fp16 operand range (|x| > 65504)",

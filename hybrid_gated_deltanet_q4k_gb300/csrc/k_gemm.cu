@@ -63,7 +63,10 @@ constexpr int NUM_EPI_WARPS = 8;
 constexpr int THREADS = 64 + NUM_EPI_WARPS * 32;
 constexpr uint32_t TMEM_COLS = 512;  // two accumulator buffers of BN columns
 constexpr int BAR_BYTES = 256;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;  // + alignment slack
+// epilogue staging: one 32-row x 64-column bf16 tile (4 KB, 128-byte swizzle) per epilogue warp
+constexpr int EPI_TILE_BYTES = 32 * 64 * 2;
+constexpr int EPI_BYTES = NUM_EPI_WARPS * EPI_TILE_BYTES;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES + 1024;  // + alignment slack
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 constexpr uint64_t DRAIN_LIMIT_NS = 20000000ull;
 
@@ -136,6 +139,17 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
         : "memory");
 }
+
+// Tensor store of a shared-memory tile (bulk async group of this thread).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(smem_u32(src))
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_group_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
@@ -217,7 +231,8 @@ struct GemmArgs {
     int n_bf16;
     float* out_f32;
     int64_t ld_f32;
-    int vec_ok;  // 16-byte vector stores are aligned
+    int vec_ok;     // 16-byte vector stores are aligned
+    int tma_store;  // bf16 output through shared memory and TMA tensor stores (the third tensor map)
 };
 
 __device__ __forceinline__ void store_group8(const GemmArgs& g, int row, int n, const float* y) {
@@ -263,11 +278,13 @@ __device__ __forceinline__ void tile_origin(int tile, int num_m, int num_n, int&
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(tc::THREADS, 1)
-gemm_codes_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmArgs g) {
+gemm_codes_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                  const __grid_constant__ CUtensorMap tmC, GemmArgs g) {
     using namespace tc;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    uint8_t* epi = smem + STAGES * STAGE_BYTES;   // epilogue staging, 1024-byte aligned
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES + EPI_BYTES);
     uint64_t* empty = full + STAGES;
     uint64_t* acc_full = empty + STAGES;
     uint64_t* acc_empty = acc_full + 2;
@@ -413,26 +430,59 @@ gemm_codes_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             }
             if (!ok) break;
             const int row = m0 + quarter * 32 + lane;
-            if (row < g.M) {
-                const float srow = g.sa[row];
-                const int nbase = n0 + half * 128;
+            const bool valid = row < g.M;
+            const float srow = valid ? g.sa[row] : 0.0f;
+            const int nbase = n0 + half * 128;
+            uint8_t* ebuf = epi + (warp - 2) * EPI_TILE_BYTES;
 #pragma unroll
-                for (int grp = 0; grp < 16; ++grp) {
-                    const int n = nbase + grp * 8;
-                    if (n < g.N) {
-                        float y[8];
+            for (int c = 0; c < 2; ++c) {
+                const int n = nbase + 64 * c;
+                if (g.tma_store && n + 64 <= g.n_bf16) {
+                    if (m0 + quarter * 32 >= g.M) continue;   // every row of this warp's box is past M
+                    // bf16 rows of 64 columns into this warp's staging tile (lane = row,
+                    // 128-byte swizzle), then one tensor store; the TMA clips rows past M
+                    uint32_t w[32];
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const float scol = (n + j < g.N) ? __ldg(g.sb + n + j) : 0.0f;
-                            y[j] = __fmul_rn(__fmul_rn(__int2float_rn(acc[grp * 8 + j]), srow), scol);
+                    for (int j = 0; j < 32; ++j) {
+                        const float y0 = __fmul_rn(__fmul_rn(__int2float_rn(acc[64 * c + 2 * j]), srow), __ldg(g.sb + n + 2 * j));
+                        const float y1 =
+                            __fmul_rn(__fmul_rn(__int2float_rn(acc[64 * c + 2 * j + 1]), srow), __ldg(g.sb + n + 2 * j + 1));
+                        w[j] = static_cast<uint32_t>(float_to_bf16_bits(y0)) |
+                               (static_cast<uint32_t>(float_to_bf16_bits(y1)) << 16);
+                    }
+                    if (lane == 0) bulk_wait_group_read0();   // the previous store has read the tile
+                    __syncwarp();
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        *reinterpret_cast<uint4*>(ebuf + lane * 128 + ((q ^ (lane & 7)) << 4)) =
+                            make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmC, ebuf, n, m0 + quarter * 32);
+                        bulk_commit_group();
+                    }
+                } else if (valid) {
+#pragma unroll
+                    for (int grp = 0; grp < 8; ++grp) {
+                        const int nn = n + grp * 8;
+                        if (nn < g.N) {
+                            float y[8];
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const float scol = (nn + j < g.N) ? __ldg(g.sb + nn + j) : 0.0f;
+                                y[j] = __fmul_rn(__fmul_rn(__int2float_rn(acc[64 * c + grp * 8 + j]), srow), scol);
+                            }
+                            store_group8(g, row, nn, y);
                         }
-                        store_group8(g, row, n, y);
                     }
                 }
             }
         }
     }
 
+    // this warp's tensor stores have completed before the shared memory goes
+    if (warp >= 2 && lane == 0) bulk_wait_group0();
     tc_fence_before();
     __syncthreads();
     // neither CTA frees its shared memory or TMEM while the pair's MMAs may
@@ -479,6 +529,21 @@ static int sm_count() {
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
     return n > 0 ? n : 1;
+}
+
+// bf16 output [rows][n_cols] with row pitch ld (elements): boxes of 32 rows x
+// 64 columns, 128-byte swizzle, for the epilogue's tensor stores.
+static bool make_store_map(CUtensorMap* map, const void* base, int64_t rows, int64_t n_cols, int64_t ld) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(n_cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+    cuuint32_t box[2] = {64, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
 }
 
 // Clusters of 2 CTAs of the projection kernel that fit on the device at once.
@@ -533,13 +598,17 @@ cudaError_t launch_gemm_codes(const uint16_t* a, const float* sa, const uint16_t
     const bool f_ok = out_f32 == nullptr ||
                       ((reinterpret_cast<uintptr_t>(out_f32) & 15) == 0 && ld_f32 % 4 == 0 && n_bf16 % 4 == 0);
     g.vec_ok = (bf_ok && f_ok) ? 1 : 0;
+    // bf16 output through TMA tensor stores when it is 16-byte aligned with a
+    // row pitch of a multiple of 8 elements
+    CUtensorMap mc = ma;
+    g.tma_store = (out_bf16 != nullptr && bf_ok && n_bf16 >= 64 && make_store_map(&mc, out_bf16, M, n_bf16, ld_bf16)) ? 1 : 0;
     // pairs of CTAs (clusters of 2): as many as can be resident at once (a
     // cluster stays within one GPC), at most one per tile
     const int64_t tiles = ((M + 2 * tc::BM - 1) / (2 * tc::BM)) * ((N + tc::BN - 1) / tc::BN);
     const int max_pairs = resident_pairs();
     const int pairs = static_cast<int>(tiles < max_pairs ? tiles : max_pairs);
     const int grid = 2 * (pairs > 0 ? pairs : 1);
-    gemm_codes_kernel<<<grid, tc::THREADS, tc::SMEM_BYTES, st>>>(ma, mb, g);
+    gemm_codes_kernel<<<grid, tc::THREADS, tc::SMEM_BYTES, st>>>(ma, mb, mc, g);
     return cudaGetLastError();
 }
 
