@@ -10,6 +10,7 @@
 // sized per ubatch of tokens: when it holds fewer than N tokens the call runs
 // in passes, each an exact extend of the previous one.
 #include "common.cuh"
+#include "streams.h"
 
 #include <cstdarg>
 #include <cstdio>
@@ -30,7 +31,7 @@ cudaError_t launch_conv(const gdn_layer&, const uint16_t*, int64_t, int64_t, con
                         uint16_t*, float*, float*, cudaStream_t);
 cudaError_t launch_conv_state(const gdn_layer&, const uint16_t*, int64_t, int64_t, float*, cudaStream_t);
 cudaError_t launch_delta(const gdn_layer&, const uint16_t*, const float*, const float*, int64_t, const float*, float*,
-                         uint16_t*, void*, cudaStream_t, bool overlap);
+                         uint16_t*, void*, cudaStream_t, bool overlap, const TokenRangeHook* after_state);
 size_t delta_scratch_bytes(int hv, int hk, int d, int64_t n);
 cudaError_t launch_gated_norm(const gdn_layer&, const uint16_t*, const uint16_t*, int64_t, int64_t, uint16_t*, float*,
                               float*, cudaStream_t);
@@ -282,7 +283,7 @@ int gdn_delta_rule(const gdn_layer* layer, const uint16_t* qkv, const float* log
     if (scratch_bytes < delta_scratch_bytes(static_cast<int>(s.hv), static_cast<int>(s.hk), static_cast<int>(s.d), n_tokens))
         return fail(GDN_ENOMEM, "gdn_delta_rule: scratch too small");
     GDN_LAUNCH(launch_delta(*layer, qkv, log_a, b, n_tokens, state_in, state_out, o, scratch, static_cast<cudaStream_t>(stream),
-                            true),
+                            true, nullptr),
                "gdn_delta_rule");
     return GDN_OK;
 }
@@ -365,11 +366,18 @@ int gdn_prefill(const gdn_layer* layer, const void* x, int64_t n_tokens, const f
         GDN_LAUNCH(mark(4, first, st), "stage event");
         const float* la = lu.gate_log_a ? lu.gate_log_a : w.log_a;
         const float* bb = lu.gate_b ? lu.gate_b : w.b;
-        GDN_LAUNCH(launch_delta(lu, w.qkv, la, bb, nb, first ? state_in : state_out, state_out, w.o, w.delta, st, true),
-                   "delta rule");
-        GDN_LAUNCH(mark(5, first, st), "stage event");
+        // The gated norm of each token segment of the delta rule runs as soon as
+        // that segment's state pass is done, beside the later segments.
         const uint16_t* z = w.qkvz + s.c_conv;
-        GDN_LAUNCH(launch_gated_norm(lu, w.o, z, s.n_bf16, nb, w.oc, w.so, w.ohat, st), "gated norm");
+        const TokenRangeHook norm_hook = [&](int64_t t0, int64_t t1, cudaStream_t cs) {
+            return launch_gated_norm(lu, w.o + t0 * s.c_v, z + t0 * s.n_bf16, s.n_bf16, t1 - t0,
+                                     w.oc ? w.oc + t0 * s.c_v : nullptr, w.so ? w.so + t0 : nullptr,
+                                     w.ohat ? w.ohat + t0 * s.c_v : nullptr, cs);
+        };
+        GDN_LAUNCH(launch_delta(lu, w.qkv, la, bb, nb, first ? state_in : state_out, state_out, w.o, w.delta, st, true,
+                                &norm_hook),
+                   "delta rule and gated norm");
+        GDN_LAUNCH(mark(5, first, st), "stage event");
         GDN_LAUNCH(mark(6, first, st), "stage event");
         if (q4k) {
             uint16_t* ys = static_cast<uint16_t*>(y) + u0 * s.H;
@@ -452,7 +460,7 @@ extern "C" int gdn_delta_rule_noalloc(const gdn_layer* layer, const uint16_t* qk
         scratch = g_noalloc_addr[dev];
     }
     GDN_LAUNCH(launch_delta(*layer, qkv, log_a, b, n_tokens, state_in, state_out, o, scratch,
-                            static_cast<cudaStream_t>(stream), false),
+                            static_cast<cudaStream_t>(stream), false, nullptr),
                "gdn_delta_rule_noalloc");
     return GDN_OK;
 }

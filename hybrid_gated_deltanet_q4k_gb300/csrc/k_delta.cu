@@ -51,6 +51,7 @@
 #include "tcgen05.cuh"
 #include "streams.h"
 
+#include <algorithm>
 #include <mutex>
 
 namespace gdn {
@@ -880,8 +881,12 @@ static void launch_state(const CUtensorMap& map, const DeltaArgs& a, cudaStream_
     delta_state_kernel<D><<<dim3(a.hv, D / NV), STATE_THREADS, StateSmem<D>::BYTES + 1024, st>>>(map, a);
 }
 
+// after_state (may be null): work on each segment's output tokens, enqueued on
+// the low-priority stream once that segment's state pass is done (after all
+// the preps, so it never delays one), so that it too runs beside the later
+// state segments; without segments it runs on st after the state pass.
 template <int D>
-static cudaError_t launch_delta_d(DeltaArgs& a, cudaStream_t st, bool overlap) {
+static cudaError_t launch_delta_d(DeltaArgs& a, cudaStream_t st, bool overlap, const TokenRangeHook* after_state) {
     static bool attr = false;
     if (!attr) {
         cudaFuncSetAttribute(delta_prep_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, PrepSmem<D>::BYTES + 1024);
@@ -900,7 +905,8 @@ static cudaError_t launch_delta_d(DeltaArgs& a, cudaStream_t st, bool overlap) {
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         launch_state<D>(map, a, st);
-        return cudaGetLastError();
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        return after_state ? (*after_state)(0, a.n, st) : cudaSuccess;
     }
     std::lock_guard<std::mutex> lock(lib_streams_mutex());
     LibStreams* ls = nullptr;
@@ -911,6 +917,7 @@ static cudaError_t launch_delta_d(DeltaArgs& a, cudaStream_t st, bool overlap) {
     if ((e = cudaStreamWaitEvent(prep_st, ls->ev_a, 0)) != cudaSuccess) return e;
     if ((e = cudaStreamWaitEvent(state_st, ls->ev_a, 0)) != cudaSuccess) return e;
     cudaError_t first = cudaSuccess;
+    int nseg = 0;
     for (int c0 = 0; c0 < nch && first == cudaSuccess; c0 += DELTA_SEG_CHUNKS) {
         DeltaArgs s = a;
         s.chunk0 = c0;
@@ -921,7 +928,20 @@ static cudaError_t launch_delta_d(DeltaArgs& a, cudaStream_t st, bool overlap) {
         if ((first = cudaEventRecord(ls->ev_b, prep_st)) != cudaSuccess) break;
         if ((first = cudaStreamWaitEvent(state_st, ls->ev_b, 0)) != cudaSuccess) break;
         launch_state<D>(map, s, state_st);
-        first = cudaGetLastError();
+        if ((first = cudaGetLastError()) != cudaSuccess) break;
+        if (after_state && nseg < LIB_EVENT_POOL) first = cudaEventRecord(ls->pool[nseg], state_st);
+        ++nseg;
+    }
+    if (after_state && first == cudaSuccess) {
+        // segments past the event pool wait for the last state segment
+        if (nseg > LIB_EVENT_POOL) first = cudaEventRecord(ls->ev_a, state_st);
+        for (int i = 0; i < nseg && first == cudaSuccess; ++i) {
+            first = cudaStreamWaitEvent(prep_st, i < LIB_EVENT_POOL ? ls->pool[i] : ls->ev_a, 0);
+            if (first != cudaSuccess) break;
+            const int64_t tb = static_cast<int64_t>(i) * DELTA_SEG_CHUNKS * DC;
+            const int64_t te = std::min<int64_t>(a.n, tb + static_cast<int64_t>(DELTA_SEG_CHUNKS) * DC);
+            first = (*after_state)(tb, te, prep_st);
+        }
     }
     // join both library streams back to the caller's stream, also after a failure
     e = cudaEventRecord(ls->ev_b, prep_st);
@@ -933,7 +953,7 @@ static cudaError_t launch_delta_d(DeltaArgs& a, cudaStream_t st, bool overlap) {
 
 cudaError_t launch_delta(const gdn_layer& L, const uint16_t* qkv, const float* log_a, const float* b, int64_t n,
                          const float* state_in, float* state_out, uint16_t* o, void* scratch, cudaStream_t st,
-                         bool overlap) {
+                         bool overlap, const TokenRangeHook* after_state) {
     DeltaArgs a;
     const int d = L.dk;
     a.qkv = qkv;
@@ -955,7 +975,7 @@ cudaError_t launch_delta(const gdn_layer& L, const uint16_t* qkv, const float* l
     a.state_in = state_in;
     a.state_out = state_out;
     a.o = o;
-    return d == 128 ? launch_delta_d<128>(a, st, overlap) : launch_delta_d<64>(a, st, overlap);
+    return d == 128 ? launch_delta_d<128>(a, st, overlap, after_state) : launch_delta_d<64>(a, st, overlap, after_state);
 }
 
 }  // namespace gdn

@@ -24,6 +24,8 @@ cudaError_t lib_streams(LibStreams** out) {
         if (!s.lo && (e = cudaStreamCreateWithPriority(&s.lo, cudaStreamNonBlocking, least)) != cudaSuccess) return e;
         if (!s.hi && (e = cudaStreamCreateWithPriority(&s.hi, cudaStreamNonBlocking, greatest)) != cudaSuccess) return e;
         if (!s.ev_a && (e = cudaEventCreateWithFlags(&s.ev_a, cudaEventDisableTiming)) != cudaSuccess) return e;
+        for (int i = 0; i < LIB_EVENT_POOL; ++i)
+            if (!s.pool[i] && (e = cudaEventCreateWithFlags(&s.pool[i], cudaEventDisableTiming)) != cudaSuccess) return e;
         if ((e = cudaEventCreateWithFlags(&s.ev_b, cudaEventDisableTiming)) != cudaSuccess) return e;
     }
     *out = &s;

@@ -6,14 +6,23 @@
 
 #include <cuda_runtime.h>
 
+#include <stdint.h>
+
+#include <functional>
 #include <mutex>
 
 namespace gdn {
+
+// Work over the token range [t_begin, t_end) enqueued on a given stream.
+using TokenRangeHook = std::function<cudaError_t(int64_t t_begin, int64_t t_end, cudaStream_t)>;
+
+constexpr int LIB_EVENT_POOL = 64;
 
 struct LibStreams {
     cudaStream_t lo = nullptr;   // least priority
     cudaStream_t hi = nullptr;   // greatest priority
     cudaEvent_t ev_a = nullptr, ev_b = nullptr;   // timing disabled
+    cudaEvent_t pool[LIB_EVENT_POOL] = {};         // one per pending dependency of a call
 };
 
 // Guards the table and every enqueue sequence that uses the streams and events.
