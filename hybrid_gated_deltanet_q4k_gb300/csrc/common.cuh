@@ -74,12 +74,13 @@ __device__ __forceinline__ QScale make_qscale(float amax) {
 // other; rounding to nearest can tell them apart only when they straddle a
 // half-integer.  When y is within 1e-3 of one (or is not a number), `redo` is
 // set and the caller recomputes with qcode_exact, so the result always equals
-// qcode_exact(w, s).
+// qcode_exact(w, s).  No clamp is needed: |w| <= amax and s = fl(amax/127)
+// give |y| <= 127 (1 + 2^-22) < 127.5, so |rint(y)| <= 127.
 __device__ __forceinline__ float qcode_fast(float w, const QScale& q, bool& redo) {
     const float y = w * q.rs;
     const float r = rintf(y);
     redo |= !(fabsf(y - r) <= 0.499f);
-    return fminf(fmaxf(r, -127.0f), 127.0f) + 0.0f;
+    return r + 0.0f;
 }
 
 // Two floats as a pair of fp16 values (rounded to nearest), low half first.
