@@ -66,3 +66,21 @@ class DeviceLayer:
         return self.lib.gdn_prefill(ctypes.byref(s), gl.ptr(x), x.shape[0], gl.ptr(state_in), gl.ptr(state_out),
                                     gl.ptr(conv_state), gl.ptr(y), gl.ptr(workspace), workspace.numel(),
                                     gl.stream_handle(stream), check=check)
+
+    def host_workspace_bytes(self, pass_tokens: int, gates: bool = False) -> int:
+        """Device workspace of ``prefill_host`` for passes of ``pass_tokens`` (with or without drawn gates)."""
+        s = self.struct()
+        if gates:                   # only whether gates are drawn matters for the size
+            s.gate_log_a = s.gate_b = 16
+        return self.lib.gdn_host_workspace_size(ctypes.byref(s), int(pass_tokens))
+
+    def new_host_workspace(self, pass_tokens: int, gates: bool = False) -> torch.Tensor:
+        return torch.empty(self.host_workspace_bytes(pass_tokens, gates), dtype=torch.uint8, device=self.device)
+
+    def prefill_host(self, x_host: torch.Tensor, state_in, state_out, conv_state, y_host: torch.Tensor, workspace,
+                     pass_tokens: int = 0, gate_log_a=None, gate_b=None, stream=None, check=True) -> int:
+        """Enqueue gdn_prefill_host: x_host, y_host (and the gates, if given) are pinned host tensors."""
+        s = self.struct(gate_log_a, gate_b)
+        return self.lib.gdn_prefill_host(ctypes.byref(s), gl.ptr(x_host), x_host.shape[0], gl.ptr(state_in),
+                                         gl.ptr(state_out), gl.ptr(conv_state), gl.ptr(y_host), int(pass_tokens),
+                                         gl.ptr(workspace), workspace.numel(), gl.stream_handle(stream), check=check)

@@ -164,6 +164,99 @@ Workspace carve(const gdn_layer* L, const Sizes& s, int64_t B, void* base) {
     return w;
 }
 
+// One pass of nb tokens (steps 1b to 5) on device buffers: x [nb][H] -> y
+// [nb][H], the state read from st_in and written to state_out, the conv tail
+// carried in place.  gla / gb: this pass's drawn gates (device [nb][hv]) or
+// NULL.  The weight codes in w must already be decoded.
+int run_pass(const gdn_layer* layer, const Sizes& s, const Workspace& w, const void* x, int64_t nb, const float* gla,
+             const float* gb, const float* st_in, float* state_out, float* conv_state, void* y, bool first,
+             cudaStream_t st) {
+    const bool q4k = layer->wtype == GDN_W_Q4K;
+    if (q4k) {
+        GDN_LAUNCH(launch_quant_rows(static_cast<const uint16_t*>(x), nb, s.H, w.xc, w.sx, st), "quantise x");
+        GDN_LAUNCH(mark(2, first, st), "stage event");
+        cudaError_t e = launch_gemm_codes(w.xc, w.sx, w.wc_in, w.ws_in, nb, s.r_in, s.H, w.qkvz, s.n_bf16, s.n_bf16,
+                                          w.ba, 2 * s.hv, st);
+        if (e != cudaSuccess) return cuda_fail(e, "input projection");
+    } else {
+        GDN_LAUNCH(mark(2, first, st), "stage event");
+        GDN_LAUNCH(launch_gemm_f32(static_cast<const float*>(x), static_cast<const float*>(layer->w_in), nb, s.r_in, s.H,
+                                   w.qkvz, s.n_bf16, s.n_bf16, w.ba, 2 * s.hv, st),
+                   "input projection");
+    }
+    GDN_LAUNCH(mark(3, first, st), "stage event");
+    gdn_layer lu = *layer;
+    lu.gate_log_a = gla;
+    lu.gate_b = gb;
+    GDN_LAUNCH(launch_conv(lu, w.qkvz, s.n_bf16, nb, conv_state, w.ba, 2 * s.hv, w.qkv, w.log_a, w.b, st), "conv");
+    GDN_LAUNCH(launch_conv_state(lu, w.qkvz, s.n_bf16, nb, conv_state, st), "conv state");
+    GDN_LAUNCH(mark(4, first, st), "stage event");
+    const float* la = gla ? gla : w.log_a;
+    const float* bb = gb ? gb : w.b;
+    // The gated norm of each token segment of the delta rule runs as soon as
+    // that segment's state pass is done, beside the later segments.
+    const uint16_t* z = w.qkvz + s.c_conv;
+    const TokenRangeHook norm_hook = [&](int64_t t0, int64_t t1, cudaStream_t cs) {
+        return launch_gated_norm(lu, w.o + t0 * s.c_v, z + t0 * s.n_bf16, s.n_bf16, t1 - t0,
+                                 w.oc ? w.oc + t0 * s.c_v : nullptr, w.so ? w.so + t0 : nullptr,
+                                 w.ohat ? w.ohat + t0 * s.c_v : nullptr, cs);
+    };
+    GDN_LAUNCH(launch_delta(lu, w.qkv, la, bb, nb, st_in, state_out, w.o, w.delta, st, true, &norm_hook),
+               "delta rule and gated norm");
+    GDN_LAUNCH(mark(5, first, st), "stage event");
+    GDN_LAUNCH(mark(6, first, st), "stage event");
+    if (q4k) {
+        cudaError_t e = launch_gemm_codes(w.oc, w.so, w.wc_out, w.ws_out, nb, s.H, s.c_v, static_cast<uint16_t*>(y), s.H,
+                                          s.H, nullptr, 0, st);
+        if (e != cudaSuccess) return cuda_fail(e, "output projection");
+    } else {
+        GDN_LAUNCH(launch_gemm_f32(w.ohat, static_cast<const float*>(layer->w_out), nb, s.H, s.c_v, nullptr, 0, 0,
+                                   static_cast<float*>(y), s.H, st),
+                   "output projection");
+    }
+    GDN_LAUNCH(mark(7, first, st), "stage event");
+    return GDN_OK;
+}
+
+// Tokens per pass for a workspace of ws_bytes: all n if they fit, else the
+// largest count that fits, rounded down to whole chunks when at least one
+// chunk fits.  0 if not even one token fits.
+int64_t pass_tokens_for(const gdn_layer* layer, const Sizes& s, int64_t n, size_t ws_bytes,
+                        size_t (*extra)(const gdn_layer*, const Sizes&, int64_t)) {
+    auto need = [&](int64_t B) { return carve(layer, s, B, nullptr).total + (extra ? extra(layer, s, B) : 0); };
+    if (need(1) > ws_bytes) return 0;
+    if (need(n) <= ws_bytes) return n;
+    int64_t lo = 1, hi = n;  // need(lo) fits, need(hi) does not
+    while (hi - lo > 1) {
+        const int64_t mid = lo + (hi - lo) / 2;
+        if (need(mid) <= ws_bytes) lo = mid; else hi = mid;
+    }
+    return lo >= GDN_CHUNK ? lo - lo % GDN_CHUNK : lo;
+}
+
+// Device staging of gdn_prefill_host beyond the pass workspace: two slots each
+// of x, y and (when the gates are drawn) log a and b.
+size_t host_stage_bytes(const gdn_layer* L, const Sizes& s, int64_t B) {
+    const size_t esz = L->wtype == GDN_W_Q4K ? 2 : 4;
+    size_t t = 4 * up256(B * s.H * esz);
+    if (L->gate_log_a) t += 4 * up256(B * s.hv * 4);
+    return t;
+}
+
+// GDN_OK if p is page-locked host memory (cudaHostAlloc or cudaHostRegister).
+int check_pinned(const void* p, const char* what) {
+    cudaPointerAttributes a{};
+    cudaError_t e = cudaPointerGetAttributes(&a, p);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return fail(GDN_EINVAL, "gdn_prefill_host: %s: %s", what, cudaGetErrorString(e));
+    }
+    if (a.type != cudaMemoryTypeHost)
+        return fail(GDN_EINVAL, "gdn_prefill_host: %s must be page-locked host memory (cudaHostAlloc or cudaHostRegister)",
+                    what);
+    return GDN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -318,17 +411,10 @@ int gdn_prefill(const gdn_layer* layer, const void* x, int64_t n_tokens, const f
     if (!aligned(x, 16) || !aligned(y, 16) || !aligned(workspace, 256)) return fail(GDN_EINVAL, "gdn_prefill: x, y 16-byte and workspace 256-byte alignment required");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     // Largest pass that fits: the workspace grows linearly in B.
-    const size_t w1 = carve(layer, s, 1, nullptr).total;
-    if (ws_bytes < w1) return fail(GDN_ENOMEM, "gdn_prefill: workspace %zu B < %zu B needed for one token", ws_bytes, w1);
-    int64_t B = n_tokens;
-    if (carve(layer, s, B, nullptr).total > ws_bytes) {
-        int64_t lo = 1, hi = n_tokens;  // carve(lo) fits, carve(hi) does not
-        while (hi - lo > 1) {
-            const int64_t mid = lo + (hi - lo) / 2;
-            if (carve(layer, s, mid, nullptr).total <= ws_bytes) lo = mid; else hi = mid;
-        }
-        B = lo >= GDN_CHUNK ? lo - lo % GDN_CHUNK : lo;
-    }
+    const int64_t B = pass_tokens_for(layer, s, n_tokens, ws_bytes, nullptr);
+    if (B < 1)
+        return fail(GDN_ENOMEM, "gdn_prefill: workspace %zu B < %zu B needed for one token", ws_bytes,
+                    carve(layer, s, 1, nullptr).total);
     Workspace w = carve(layer, s, B, workspace);
     const bool q4k = layer->wtype == GDN_W_Q4K;
     GDN_LAUNCH(mark(0, true, st), "stage event");
@@ -340,57 +426,122 @@ int gdn_prefill(const gdn_layer* layer, const void* x, int64_t n_tokens, const f
     GDN_LAUNCH(mark(1, true, st), "stage event");
     for (int64_t u0 = 0; u0 < n_tokens; u0 += B) {
         const int64_t nb = (n_tokens - u0) < B ? (n_tokens - u0) : B;
-        const bool first = u0 == 0;
-        if (q4k) {
-            const uint16_t* xs = static_cast<const uint16_t*>(x) + u0 * s.H;
-            GDN_LAUNCH(launch_quant_rows(xs, nb, s.H, w.xc, w.sx, st), "quantise x");
-            GDN_LAUNCH(mark(2, first, st), "stage event");
-            cudaError_t e = launch_gemm_codes(w.xc, w.sx, w.wc_in, w.ws_in, nb, s.r_in, s.H, w.qkvz, s.n_bf16, s.n_bf16,
-                                              w.ba, 2 * s.hv, st);
-            if (e != cudaSuccess) return cuda_fail(e, "input projection");
-        } else {
-            GDN_LAUNCH(mark(2, first, st), "stage event");
-            const float* xs = static_cast<const float*>(x) + u0 * s.H;
-            GDN_LAUNCH(launch_gemm_f32(xs, static_cast<const float*>(layer->w_in), nb, s.r_in, s.H, w.qkvz, s.n_bf16,
-                                       s.n_bf16, w.ba, 2 * s.hv, st),
-                       "input projection");
-        }
-        GDN_LAUNCH(mark(3, first, st), "stage event");
-        gdn_layer lu = *layer;
-        if (layer->gate_log_a) {
-            lu.gate_log_a = layer->gate_log_a + u0 * s.hv;
-            lu.gate_b = layer->gate_b + u0 * s.hv;
-        }
-        GDN_LAUNCH(launch_conv(lu, w.qkvz, s.n_bf16, nb, conv_state, w.ba, 2 * s.hv, w.qkv, w.log_a, w.b, st), "conv");
-        GDN_LAUNCH(launch_conv_state(lu, w.qkvz, s.n_bf16, nb, conv_state, st), "conv state");
-        GDN_LAUNCH(mark(4, first, st), "stage event");
-        const float* la = lu.gate_log_a ? lu.gate_log_a : w.log_a;
-        const float* bb = lu.gate_b ? lu.gate_b : w.b;
-        // The gated norm of each token segment of the delta rule runs as soon as
-        // that segment's state pass is done, beside the later segments.
-        const uint16_t* z = w.qkvz + s.c_conv;
-        const TokenRangeHook norm_hook = [&](int64_t t0, int64_t t1, cudaStream_t cs) {
-            return launch_gated_norm(lu, w.o + t0 * s.c_v, z + t0 * s.n_bf16, s.n_bf16, t1 - t0,
-                                     w.oc ? w.oc + t0 * s.c_v : nullptr, w.so ? w.so + t0 : nullptr,
-                                     w.ohat ? w.ohat + t0 * s.c_v : nullptr, cs);
-        };
-        GDN_LAUNCH(launch_delta(lu, w.qkv, la, bb, nb, first ? state_in : state_out, state_out, w.o, w.delta, st, true,
-                                &norm_hook),
-                   "delta rule and gated norm");
-        GDN_LAUNCH(mark(5, first, st), "stage event");
-        GDN_LAUNCH(mark(6, first, st), "stage event");
-        if (q4k) {
-            uint16_t* ys = static_cast<uint16_t*>(y) + u0 * s.H;
-            cudaError_t e = launch_gemm_codes(w.oc, w.so, w.wc_out, w.ws_out, nb, s.H, s.c_v, ys, s.H, s.H, nullptr, 0, st);
-            if (e != cudaSuccess) return cuda_fail(e, "output projection");
-        } else {
-            float* ys = static_cast<float*>(y) + u0 * s.H;
-            GDN_LAUNCH(launch_gemm_f32(w.ohat, static_cast<const float*>(layer->w_out), nb, s.H, s.c_v, nullptr, 0, 0, ys,
-                                       s.H, st),
-                       "output projection");
-        }
-        GDN_LAUNCH(mark(7, first, st), "stage event");
+        const size_t esz = q4k ? 2 : 4;
+        const float* gla = layer->gate_log_a ? layer->gate_log_a + u0 * s.hv : nullptr;
+        const float* gb = layer->gate_b ? layer->gate_b + u0 * s.hv : nullptr;
+        r = run_pass(layer, s, w, static_cast<const uint8_t*>(x) + u0 * s.H * esz, nb, gla, gb,
+                     u0 == 0 ? state_in : state_out, state_out, conv_state, static_cast<uint8_t*>(y) + u0 * s.H * esz,
+                     u0 == 0, st);
+        if (r) return r;
     }
+    return GDN_OK;
+}
+
+size_t gdn_host_workspace_size(const gdn_layer* layer, int64_t pass_tokens) {
+    Sizes s;
+    if (check_layer(layer, &s) || pass_tokens < 1) return 0;
+    return carve(layer, s, pass_tokens, nullptr).total + host_stage_bytes(layer, s, pass_tokens);
+}
+
+int gdn_prefill_host(const gdn_layer* layer, const void* x_host, int64_t n_tokens, const float* state_in,
+                     float* state_out, float* conv_state, void* y_host, int64_t pass_tokens, void* workspace,
+                     size_t ws_bytes, void* stream) {
+    Sizes s;
+    int r = check_layer(layer, &s);
+    if (r) return r;
+    if (n_tokens < 1 || n_tokens > 0x7fffffff)
+        return fail(GDN_EINVAL, "gdn_prefill_host: n_tokens >= 1 required (got %lld)", (long long)n_tokens);
+    if (pass_tokens < 0) return fail(GDN_EINVAL, "gdn_prefill_host: pass_tokens >= 0 required");
+    if (!x_host || !state_out || !conv_state || !y_host || !workspace) return fail(GDN_EINVAL, "gdn_prefill_host: NULL pointer");
+    if (!aligned(workspace, 256)) return fail(GDN_EINVAL, "gdn_prefill_host: workspace 256-byte alignment required");
+    if ((r = check_pinned(x_host, "x_host")) || (r = check_pinned(y_host, "y_host"))) return r;
+    const bool gates = layer->gate_log_a != nullptr;
+    if (gates && ((r = check_pinned(layer->gate_log_a, "gate_log_a")) || (r = check_pinned(layer->gate_b, "gate_b"))))
+        return r;
+    int64_t B = pass_tokens_for(layer, s, n_tokens, ws_bytes, host_stage_bytes);
+    if (B < 1)
+        return fail(GDN_ENOMEM, "gdn_prefill_host: workspace %zu B < %zu B needed for one token", ws_bytes,
+                    carve(layer, s, 1, nullptr).total + host_stage_bytes(layer, s, 1));
+    if (pass_tokens > 0 && pass_tokens < B) B = pass_tokens >= GDN_CHUNK ? pass_tokens - pass_tokens % GDN_CHUNK : pass_tokens;
+    const bool q4k = layer->wtype == GDN_W_Q4K;
+    const size_t esz = q4k ? 2 : 4;
+    Workspace w = carve(layer, s, B, workspace);
+    uint8_t* stage = static_cast<uint8_t*>(workspace) + w.total;
+    const size_t xb = up256(B * s.H * esz), gbytes = up256(B * s.hv * 4);
+    uint8_t* xs[2] = {stage, stage + xb};
+    uint8_t* ys[2] = {stage + 2 * xb, stage + 3 * xb};
+    float* gas[2] = {nullptr, nullptr};
+    float* gbs[2] = {nullptr, nullptr};
+    if (gates)
+        for (int i = 0; i < 2; ++i) {
+            gas[i] = reinterpret_cast<float*>(stage + 4 * xb + (2 * i) * gbytes);
+            gbs[i] = reinterpret_cast<float*>(stage + 4 * xb + (2 * i + 1) * gbytes);
+        }
+    const int64_t np = (n_tokens + B - 1) / B;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    std::lock_guard<std::mutex> lock(copy_streams_mutex());
+    CopyStreams* cs = nullptr;
+    cudaError_t e = copy_streams(&cs);
+    if (e != cudaSuccess) return cuda_fail(e, "gdn_prefill_host: copy streams");
+    GDN_LAUNCH(cudaEventRecord(cs->fork, st), "gdn_prefill_host: fork");
+    GDN_LAUNCH(cudaStreamWaitEvent(cs->h2d, cs->fork, 0), "gdn_prefill_host: fork");
+    GDN_LAUNCH(cudaStreamWaitEvent(cs->d2h, cs->fork, 0), "gdn_prefill_host: fork");
+
+    // Host-to-device copy of pass p into slot p % 2, once pass p - 2 (the
+    // previous user of the slot) is done with it.
+    auto copy_in = [&](int64_t p) -> int {
+        const int64_t u0 = p * B, nb = (n_tokens - u0) < B ? (n_tokens - u0) : B;
+        const int slot = static_cast<int>(p & 1);
+        if (p >= 2) GDN_LAUNCH(cudaStreamWaitEvent(cs->h2d, cs->pass_done[slot], 0), "gdn_prefill_host: slot wait");
+        GDN_LAUNCH(cudaMemcpyAsync(xs[slot], static_cast<const uint8_t*>(x_host) + u0 * s.H * esz, nb * s.H * esz,
+                                   cudaMemcpyHostToDevice, cs->h2d),
+                   "gdn_prefill_host: copy x");
+        if (gates) {
+            GDN_LAUNCH(cudaMemcpyAsync(gas[slot], layer->gate_log_a + u0 * s.hv, nb * s.hv * 4, cudaMemcpyHostToDevice,
+                                       cs->h2d),
+                       "gdn_prefill_host: copy gate_log_a");
+            GDN_LAUNCH(cudaMemcpyAsync(gbs[slot], layer->gate_b + u0 * s.hv, nb * s.hv * 4, cudaMemcpyHostToDevice,
+                                       cs->h2d),
+                       "gdn_prefill_host: copy gate_b");
+        }
+        GDN_LAUNCH(cudaEventRecord(cs->in_ready[slot], cs->h2d), "gdn_prefill_host: event");
+        return GDN_OK;
+    };
+    auto pipeline = [&]() -> int {
+        GDN_LAUNCH(mark(0, true, st), "stage event");
+        if (q4k)
+            GDN_LAUNCH(launch_q4k_deq_codes2(layer->w_in, s.r_in, s.H, w.wc_in, w.ws_in, layer->w_out, s.H, s.c_v,
+                                             w.wc_out, w.ws_out, st),
+                       "dequant W_in, W_out");
+        GDN_LAUNCH(mark(1, true, st), "stage event");
+        int rr = copy_in(0);
+        if (rr) return rr;
+        for (int64_t p = 0; p < np; ++p) {
+            const int64_t u0 = p * B, nb = (n_tokens - u0) < B ? (n_tokens - u0) : B;
+            const int slot = static_cast<int>(p & 1);
+            if (p + 1 < np && (rr = copy_in(p + 1))) return rr;
+            GDN_LAUNCH(cudaStreamWaitEvent(st, cs->in_ready[slot], 0), "gdn_prefill_host: input wait");
+            if (p >= 2) GDN_LAUNCH(cudaStreamWaitEvent(st, cs->out_free[slot], 0), "gdn_prefill_host: output wait");
+            rr = run_pass(layer, s, w, xs[slot], nb, gas[slot], gbs[slot], p == 0 ? state_in : state_out, state_out,
+                          conv_state, ys[slot], p == 0, st);
+            if (rr) return rr;
+            GDN_LAUNCH(cudaEventRecord(cs->pass_done[slot], st), "gdn_prefill_host: event");
+            GDN_LAUNCH(cudaStreamWaitEvent(cs->d2h, cs->pass_done[slot], 0), "gdn_prefill_host: output wait");
+            GDN_LAUNCH(cudaMemcpyAsync(static_cast<uint8_t*>(y_host) + u0 * s.H * esz, ys[slot], nb * s.H * esz,
+                                       cudaMemcpyDeviceToHost, cs->d2h),
+                       "gdn_prefill_host: copy y");
+            GDN_LAUNCH(cudaEventRecord(cs->out_free[slot], cs->d2h), "gdn_prefill_host: event");
+        }
+        return GDN_OK;
+    };
+    r = pipeline();
+    // Join both copy streams back into the caller's stream on every path.
+    const cudaError_t j[4] = {cudaEventRecord(cs->join_h2d, cs->h2d), cudaStreamWaitEvent(st, cs->join_h2d, 0),
+                              cudaEventRecord(cs->join_d2h, cs->d2h), cudaStreamWaitEvent(st, cs->join_d2h, 0)};
+    if (r) return r;
+    for (cudaError_t je : j)
+        if (je != cudaSuccess) return cuda_fail(je, "gdn_prefill_host: join");
     return GDN_OK;
 }
 

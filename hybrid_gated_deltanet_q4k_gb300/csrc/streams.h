@@ -32,4 +32,20 @@ std::mutex& lib_streams_mutex();
 // lib_streams_mutex() held).
 cudaError_t lib_streams(LibStreams** out);
 
+// Copy streams of a host-fed prefill: one for host-to-device copies, one for
+// device-to-host copies, and the events that pace two staging slots between
+// them and the compute stream (timing disabled).
+struct CopyStreams {
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+    cudaEvent_t fork = nullptr, join_h2d = nullptr, join_d2h = nullptr;
+    cudaEvent_t in_ready[2] = {}, pass_done[2] = {}, out_free[2] = {};
+};
+
+// Guards the copy-stream table and every enqueue sequence that uses it.
+std::mutex& copy_streams_mutex();
+
+// The current device's copy streams and events, created on first use (call
+// with copy_streams_mutex() held).
+cudaError_t copy_streams(CopyStreams** out);
+
 }  // namespace gdn

@@ -156,6 +156,40 @@ int gdn_prefill(const gdn_layer *layer, const void *x, int64_t n_tokens, const f
                 void *stream);
 
 /*
+ * gdn_prefill_host -- gdn_prefill fed from, and writing to, host memory: the
+ * prompt arrives from the host and the layer output goes back to it, as for
+ * an engine whose activations live in host memory between layers.  The
+ * tokens run in passes of B tokens; the host-to-device copy of pass p+1 and
+ * the device-to-host copy of pass p-1 run on two copy streams of the library
+ * while pass p computes (two device staging slots each of x, y and the
+ * drawn gates), so the copies hide behind the compute except for the first
+ * input and the last output.  Results are bitwise those of gdn_prefill run
+ * with passes of the same B.
+ *   x_host     page-locked host memory (cudaHostAlloc / cudaHostRegister):
+ *              bf16 (Q4_K) or fp32 (F32) [N][hidden]
+ *   y_host     page-locked host memory, same type and shape as x_host;
+ *              complete once `stream` has reached the end of the call
+ *   layer->gate_log_a, gate_b   when given: page-locked HOST memory [N][Hv]
+ *   state_in, state_out, conv_state   device memory, as in gdn_prefill
+ *   pass_tokens  tokens per pass (rounded down to whole chunks of GDN_CHUNK
+ *              when at least one chunk); 0 = as many as the workspace holds;
+ *              never more than the workspace holds
+ *   workspace  device, 256-byte aligned, ws_bytes >=
+ *              gdn_host_workspace_size(layer, 1); gdn_host_workspace_size(
+ *              layer, B) holds passes of B tokens
+ * Host buffers that are not page-locked are rejected (GDN_EINVAL): pageable
+ * copies would serialise with the host thread and defeat the overlap.  The
+ * first call on a device creates two copy streams and nine events, kept
+ * until exit; the copy streams are forked from `stream` and joined back to
+ * it within the call.  Calls from several host threads are serialised while
+ * they enqueue.
+ */
+size_t gdn_host_workspace_size(const gdn_layer *layer, int64_t pass_tokens);
+int gdn_prefill_host(const gdn_layer *layer, const void *x_host, int64_t n_tokens, const float *state_in,
+                     float *state_out, float *conv_state, void *y_host, int64_t pass_tokens, void *workspace,
+                     size_t ws_bytes, void *stream);
+
+/*
  * gdn_sync_status -- wait for `stream`, then report (and clear) the device
  * error words the kernels set: GDN_OK, GDN_ETIMEOUT (a bounded wait ran out),
  * GDN_ERANGE (a value beyond the fp16 operand range of the recurrence: the

@@ -256,3 +256,77 @@ def test_prefill_equals_stage_calls(n, gates):
     assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
     assert torch.equal(state, state2)
     assert torch.equal(conv, conv2)
+
+
+def _pinned(a: np.ndarray, dtype=None) -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    return (t.view(dtype) if dtype is not None else t).pin_memory()
+
+
+@pytest.mark.parametrize("name,n,pass_tokens", [("h2560", 1000, 256), ("h2560", 4096, 1024), ("tiny_f32", 64, 0),
+                                                ("h1024", 513, 128)])
+def test_prefill_host_equals_device_prefill(name, n, pass_tokens):
+    """gdn_prefill_host (pinned host x, y and gates, copies overlapped with the
+    passes) gives bit for bit what gdn_prefill gives with passes of the same
+    size, and stays within the oracle's tolerance."""
+    spec = synth.SPECS[name]
+    layer = synth.make_layer(spec)
+    tok = synth.make_tokens(spec, n, seed=spec.seed + 30)
+    dl = DeviceLayer(spec, layer)
+    B = pass_tokens or n
+    yd, sd, cd = _run(dl, spec, tok, ws_tokens=B)
+    q4k = spec.wtype == "q4k"
+    xh = _pinned(tok["x_bits"].view(np.int16)) if q4k else _pinned(tok["x"].astype(np.float32))
+    yh = torch.empty(n, spec.hidden, dtype=torch.int16 if q4k else torch.float32).pin_memory()
+    lah, bh = _pinned(tok["log_a"].astype(np.float32)), _pinned(tok["b"].astype(np.float32))
+    state, conv = dl.new_state()
+    ws = dl.new_host_workspace(B, gates=True)
+    for _ in range(2):     # a second call reuses the copy streams, events and staging slots
+        state.zero_()
+        conv.zero_()
+        yh.zero_()
+        dl.prefill_host(xh, None, state, conv, yh, ws, pass_tokens=pass_tokens, gate_log_a=lah, gate_b=bh)
+        torch.cuda.current_stream().synchronize()
+        yv = yh.view(torch.int16) if q4k else yh
+        assert torch.equal(yv, yd.cpu().view(torch.int16) if q4k else yd.cpu())
+        assert torch.equal(state, sd) and torch.equal(conv, cd)
+    if n <= 1024:
+        yy = synth.bf16_bits_to_f32(yh.numpy().view(np.uint16)) if q4k else yh.numpy()
+        ref = OL.layer_forward(oracle_params(spec, layer), tok["x"], gate_log_a=tok["log_a"], gate_b=tok["b"])
+        assert rel_l2(yy, ref["y"]) <= 1e-2
+
+
+def test_prefill_host_computed_gates_and_extend():
+    """Without drawn gates, and extending a saved state: two host-fed calls
+    (2 passes, then 3) equal one device call over the concatenation."""
+    spec = SMALL
+    layer = synth.make_layer(spec)
+    tok = synth.make_tokens(spec, 640, seed=21)
+    dl = DeviceLayer(spec, layer)
+    state, conv = dl.new_state()
+    y = _new_y(spec, 640)
+    dl.prefill(bf16_dev(tok["x_bits"]), None, state, conv, y, dl.new_workspace(128))
+    xh = _pinned(tok["x_bits"].view(np.int16))
+    yh = torch.empty(640, spec.hidden, dtype=torch.int16).pin_memory()
+    s2, c2 = dl.new_state()
+    ws = dl.new_host_workspace(128)
+    dl.prefill_host(xh[:256], None, s2, c2, yh[:256], ws, pass_tokens=128)
+    dl.prefill_host(xh[256:], s2, s2, c2, yh[256:], ws, pass_tokens=128)
+    torch.cuda.current_stream().synchronize()
+    assert torch.equal(yh, y.cpu().view(torch.int16))
+    assert torch.equal(s2, state) and torch.equal(c2, conv)
+
+
+def test_prefill_host_rejects_pageable_memory():
+    from hybrid_gated_deltanet_q4k_gb300 import lib as gl
+    spec = SMALL
+    layer = synth.make_layer(spec)
+    dl = DeviceLayer(spec, layer)
+    state, conv = dl.new_state()
+    xh = torch.zeros(64, spec.hidden, dtype=torch.int16)          # pageable
+    yh = torch.zeros(64, spec.hidden, dtype=torch.int16).pin_memory()
+    ws = dl.new_host_workspace(64)
+    r = dl.prefill_host(xh, None, state, conv, yh, ws, check=False)
+    assert r == gl.GDN_EINVAL and "page-locked" in dl.lib.last_error()
+    r = dl.prefill_host(yh, None, state, conv, yh, ws[: dl.host_workspace_bytes(1) - 256], check=False)
+    assert r == gl.GDN_ENOMEM
