@@ -484,8 +484,74 @@ def run_stage(args, spec):
                       "rate": work / (ms / 1e3), "rate_unit": unit + "/s"}), flush=True)
 
 
+def run_extend(args, spec):
+    """Session-extend workload (8 sequences of the h2560 layer, each extending a
+    saved 2048-token state by U[1, 4096] tokens): the extensions in one
+    gdn_prefill_batch call against one gdn_prefill call per sequence, both
+    timed with CUDA events, inputs resident.  A secondary measurement, not the
+    headline metric."""
+    import torch
+
+    from hybrid_gated_deltanet_q4k_gb300 import lib as gl
+    from hybrid_gated_deltanet_q4k_gb300 import synth
+    from hybrid_gated_deltanet_q4k_gb300.api import DeviceLayer
+
+    L = gl.load(build=True)
+    layer = synth.make_layer(spec)
+    dl = DeviceLayer(spec, layer)
+    cases = synth.make_extend_case(spec)
+    n = len(cases)
+    pre, ext = cases[0]["prefix"], [c["extension"] for c in cases]
+    cu = np.concatenate([[0], np.cumsum(ext)]).astype(np.int64)
+    T = int(cu[-1])
+    x = torch.from_numpy(np.concatenate([c["x_bits"][pre:] for c in cases]).view(np.int16)).cuda().view(torch.bfloat16)
+    la = torch.from_numpy(np.concatenate([c["log_a"][pre:] for c in cases])).cuda()
+    bb = torch.from_numpy(np.concatenate([c["b"][pre:] for c in cases])).cuda()
+    rng = np.random.default_rng(7)
+    s_saved = torch.from_numpy((0.05 * rng.standard_normal((n, spec.n_v_heads, spec.dv, spec.dk))).astype(np.float32)).cuda()
+    c_saved = torch.from_numpy(rng.standard_normal((n, spec.c_conv, 3)).astype(np.float32)).cuda()
+    st, cv = s_saved.clone(), c_saved.clone()
+    y = torch.empty(T, spec.hidden, dtype=torch.bfloat16, device="cuda")
+    wsb = dl.new_batch_workspace(T, n)
+    wss = dl.new_workspace(max(ext))
+    stream = torch.cuda.current_stream()
+
+    def batch():
+        dl.prefill_batch(x, cu, s_saved, st, cv, y, wsb, gate_log_a=la, gate_b=bb)
+
+    def sequential():
+        for i in range(n):
+            a, b = int(cu[i]), int(cu[i + 1])
+            dl.prefill(x[a:b], s_saved[i], st[i], cv[i], y[a:b], wss, gate_log_a=la[a:b], gate_b=bb[a:b])
+
+    res = {}
+    for name, fn in (("batch", batch), ("per_sequence", sequential)):
+        for _ in range(max(args.warmup, 3)):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        assert L.gdn_sync_status(stream.cuda_stream, check=False) == 0, L.last_error()
+        ms = e0.elapsed_time(e1) / args.steps
+        res[name] = {"ms_per_step": ms, "value": T / (ms / 1e3)}
+    print(json.dumps({"metric": "GDN-layer extend tokens/s, 8 sequences (1 GB300)", "unit": UNIT,
+                      "value": res["batch"]["value"], "ms_per_step": res["batch"]["ms_per_step"],
+                      "per_sequence_calls": res["per_sequence"], "steps": args.steps, "warmup": max(args.warmup, 3),
+                      "dtype": "int8", "data": "synthetic",
+                      "config": {"workload": "extend_h2560_8seq", "hidden": spec.hidden, "prefix": pre,
+                                 "extensions": ext, "tokens": T, "call": "gdn_prefill_batch"}}), flush=True)
+
+
 def main():
     args = parse()
+    if args.config == "extend" and args.impl == "ours" and not args.stage:
+        from hybrid_gated_deltanet_q4k_gb300 import synth
+        run_extend(args, synth.SPECS["extend"])
+        return
     if args.stage:
         from hybrid_gated_deltanet_q4k_gb300 import synth
         run_stage(args, synth.SPECS[args.config])

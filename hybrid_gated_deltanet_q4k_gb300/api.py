@@ -84,3 +84,26 @@ class DeviceLayer:
         return self.lib.gdn_prefill_host(ctypes.byref(s), gl.ptr(x_host), x_host.shape[0], gl.ptr(state_in),
                                          gl.ptr(state_out), gl.ptr(conv_state), gl.ptr(y_host), int(pass_tokens),
                                          gl.ptr(workspace), workspace.numel(), gl.stream_handle(stream), check=check)
+
+    def batch_workspace_bytes(self, n_tokens: int, n_seqs: int) -> int:
+        s = self.struct()
+        return self.lib.gdn_batch_workspace_size(ctypes.byref(s), int(n_tokens), int(n_seqs))
+
+    def new_batch_workspace(self, n_tokens: int, n_seqs: int) -> torch.Tensor:
+        return torch.empty(self.batch_workspace_bytes(n_tokens, n_seqs), dtype=torch.uint8, device=self.device)
+
+    def new_batch_state(self, n_seqs: int) -> tuple:
+        sp = self.spec
+        state = torch.zeros(n_seqs, sp.n_v_heads, sp.dv, sp.dk, dtype=torch.float32, device=self.device)
+        conv = torch.zeros(n_seqs, sp.c_conv, 3, dtype=torch.float32, device=self.device)
+        return state, conv
+
+    def prefill_batch(self, x: torch.Tensor, cu_seqlens, state_in, state_out, conv_state, y, workspace,
+                      gate_log_a=None, gate_b=None, stream=None, check=True) -> int:
+        """Enqueue gdn_prefill_batch: x holds the sequences' tokens back to back, cu_seqlens (host, n_seqs + 1)
+        their offsets; states [n_seqs][Hv][dv][dk] and conv tails [n_seqs][C_conv][3] are per sequence."""
+        cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int64))
+        s = self.struct(gate_log_a, gate_b)
+        return self.lib.gdn_prefill_batch(ctypes.byref(s), gl.ptr(x), gl.ptr(cu), len(cu) - 1, gl.ptr(state_in),
+                                          gl.ptr(state_out), gl.ptr(conv_state), gl.ptr(y), gl.ptr(workspace),
+                                          workspace.numel(), gl.stream_handle(stream), check=check)

@@ -16,6 +16,45 @@ namespace gdn {
 // clears every such word through the unit's host accessor.
 enum : int { ERR_NONE = 0, ERR_WAIT_TIMEOUT = 1, ERR_RANGE = 2 };
 
+// The sequences of one call, passed to kernels as a __grid_constant__
+// parameter (2 KB, no device memory): sequence s holds tokens [tok[s],
+// tok[s+1]) of the call's token rows and the work units [unit[s], unit[s+1])
+// of the kernel that reads it (chunks of the delta rule, token runs of the
+// conv), numbered across all sequences in order.  One sequence of n tokens is
+// {1, {0, n}, {0, units(n)}}.
+struct SeqTable {
+    int n;
+    int tok[GDN_MAX_SEQS + 1];
+    int unit[GDN_MAX_SEQS + 1];
+};
+
+// The sequence holding work unit u: the last s with unit[s] <= u (an empty
+// sequence owns no unit, so it is passed over).
+__device__ __forceinline__ int seq_of_unit(const SeqTable& t, int u) {
+    int lo = 0, hi = t.n - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (t.unit[mid] <= u) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// Host: the table of the sequences cu[0..n_seqs] (token offsets) with units
+// of `per` tokens.
+inline SeqTable make_seq_table(const int64_t* cu, int n_seqs, int per) {
+    SeqTable t{};
+    t.n = n_seqs;
+    for (int s = 0; s <= n_seqs; ++s) {
+        t.tok[s] = static_cast<int>(cu[s]);
+        t.unit[s] = s == 0 ? 0 : t.unit[s - 1] + static_cast<int>((cu[s] - cu[s - 1] + per - 1) / per);
+    }
+    return t;
+}
+inline SeqTable one_seq_table(int64_t n, int per) {
+    const int64_t cu[2] = {0, n};
+    return make_seq_table(cu, 1, per);
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

@@ -28,10 +28,12 @@ cudaError_t launch_gemm_codes(const uint16_t*, const float*, const uint16_t*, co
 cudaError_t launch_gemm_f32(const float*, const float*, int64_t, int64_t, int64_t, uint16_t*, int64_t, int64_t, float*,
                             int64_t, cudaStream_t);
 cudaError_t launch_conv(const gdn_layer&, const uint16_t*, int64_t, int64_t, const float*, const float*, int64_t,
-                        uint16_t*, float*, float*, cudaStream_t);
-cudaError_t launch_conv_state(const gdn_layer&, const uint16_t*, int64_t, int64_t, float*, cudaStream_t);
+                        uint16_t*, float*, float*, cudaStream_t, const int64_t* cu_seqlens = nullptr, int n_seqs = 1);
+cudaError_t launch_conv_state(const gdn_layer&, const uint16_t*, int64_t, int64_t, float*, cudaStream_t,
+                              const int64_t* cu_seqlens = nullptr, int n_seqs = 1);
 cudaError_t launch_delta(const gdn_layer&, const uint16_t*, const float*, const float*, int64_t, const float*, float*,
-                         uint16_t*, void*, cudaStream_t, bool overlap, const TokenRangeHook* after_state);
+                         uint16_t*, void*, cudaStream_t, bool overlap, const TokenRangeHook* after_state,
+                         const int64_t* cu_seqlens = nullptr, int n_seqs = 1);
 size_t delta_scratch_bytes(int hv, int hk, int d, int64_t n);
 cudaError_t launch_gated_norm(const gdn_layer&, const uint16_t*, const uint16_t*, int64_t, int64_t, uint16_t*, float*,
                               float*, cudaStream_t);
@@ -130,7 +132,9 @@ struct Workspace {
 
 size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-Workspace carve(const gdn_layer* L, const Sizes& s, int64_t B, void* base) {
+// delta_chunks: chunks the delta-rule scratch holds (default: those of B
+// tokens in one sequence).
+Workspace carve(const gdn_layer* L, const Sizes& s, int64_t B, void* base, int64_t delta_chunks = -1) {
     Workspace w{};
     uint8_t* p = static_cast<uint8_t*>(base);
     size_t off = 0;
@@ -158,7 +162,8 @@ Workspace carve(const gdn_layer* L, const Sizes& s, int64_t B, void* base) {
     w.log_a = static_cast<float*>(take(B * s.hv * 4));
     w.b = static_cast<float*>(take(B * s.hv * 4));
     w.o = static_cast<uint16_t*>(take(B * s.c_v * 2));
-    w.delta_bytes = delta_scratch_bytes(static_cast<int>(s.hv), static_cast<int>(s.hk), static_cast<int>(s.d), B);
+    w.delta_bytes = delta_scratch_bytes(static_cast<int>(s.hv), static_cast<int>(s.hk), static_cast<int>(s.d),
+                                        delta_chunks < 0 ? B : delta_chunks * GDN_CHUNK);
     w.delta = take(w.delta_bytes);
     w.total = off;
     return w;
@@ -542,6 +547,111 @@ int gdn_prefill_host(const gdn_layer* layer, const void* x_host, int64_t n_token
     if (r) return r;
     for (cudaError_t je : j)
         if (je != cudaSuccess) return cuda_fail(je, "gdn_prefill_host: join");
+    return GDN_OK;
+}
+
+size_t gdn_batch_workspace_size(const gdn_layer* layer, int64_t n_tokens, int n_seqs) {
+    Sizes s;
+    if (check_layer(layer, &s) || n_tokens < 0 || n_seqs < 1 || n_seqs > GDN_MAX_SEQS) return 0;
+    // every sequence's last chunk may be partial: at most n/64 + n_seqs chunks
+    return carve(layer, s, n_tokens > 0 ? n_tokens : 1, nullptr, n_tokens / GDN_CHUNK + n_seqs).total;
+}
+
+int gdn_prefill_batch(const gdn_layer* layer, const void* x, const int64_t* cu_seqlens, int n_seqs,
+                      const float* state_in, float* state_out, float* conv_state, void* y, void* workspace,
+                      size_t ws_bytes, void* stream) {
+    Sizes s;
+    int r = check_layer(layer, &s);
+    if (r) return r;
+    if (n_seqs < 1 || n_seqs > GDN_MAX_SEQS)
+        return fail(GDN_EINVAL, "gdn_prefill_batch: 1 <= n_seqs <= %d required (got %d)", GDN_MAX_SEQS, n_seqs);
+    if (!cu_seqlens) return fail(GDN_EINVAL, "gdn_prefill_batch: cu_seqlens is NULL");
+    if (cu_seqlens[0] != 0) return fail(GDN_EINVAL, "gdn_prefill_batch: cu_seqlens[0] must be 0");
+    int64_t n_chunks = 0;
+    for (int i = 0; i < n_seqs; ++i) {
+        if (cu_seqlens[i + 1] < cu_seqlens[i])
+            return fail(GDN_EINVAL, "gdn_prefill_batch: cu_seqlens must not decrease (sequence %d)", i);
+        n_chunks += (cu_seqlens[i + 1] - cu_seqlens[i] + GDN_CHUNK - 1) / GDN_CHUNK;
+    }
+    const int64_t T = cu_seqlens[n_seqs];
+    if (T > 0x7fffffff) return fail(GDN_EINVAL, "gdn_prefill_batch: more than 2^31 - 1 tokens");
+    if (!state_out || !conv_state || !workspace) return fail(GDN_EINVAL, "gdn_prefill_batch: NULL pointer");
+    if (T > 0 && (!x || !y)) return fail(GDN_EINVAL, "gdn_prefill_batch: NULL x or y");
+    if ((x && !aligned(x, 16)) || (y && !aligned(y, 16)) || !aligned(workspace, 256))
+        return fail(GDN_EINVAL, "gdn_prefill_batch: x, y 16-byte and workspace 256-byte alignment required");
+    const size_t need = carve(layer, s, T > 0 ? T : 1, nullptr, n_chunks).total;
+    if (ws_bytes < need)
+        return fail(GDN_ENOMEM, "gdn_prefill_batch: workspace %zu B < %zu B for %lld tokens in %d sequences", ws_bytes,
+                    need, (long long)T, n_seqs);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // An empty sequence passes its state through unchanged (its conv state is
+    // left as it is by the conv-state kernel).
+    const size_t sbytes = static_cast<size_t>(s.hv) * s.d * s.d * 4;
+    for (int i = 0; i < n_seqs; ++i) {
+        if (cu_seqlens[i + 1] != cu_seqlens[i]) continue;
+        float* so = state_out + static_cast<size_t>(i) * sbytes / 4;
+        if (!state_in)
+            GDN_LAUNCH(cudaMemsetAsync(so, 0, sbytes, st), "gdn_prefill_batch: zero state");
+        else if (state_in != state_out)
+            GDN_LAUNCH(cudaMemcpyAsync(so, state_in + static_cast<size_t>(i) * sbytes / 4, sbytes,
+                                       cudaMemcpyDeviceToDevice, st),
+                       "gdn_prefill_batch: copy state");
+    }
+    if (T == 0) return GDN_OK;
+
+    Workspace w = carve(layer, s, T, workspace, n_chunks);
+    const bool q4k = layer->wtype == GDN_W_Q4K;
+    GDN_LAUNCH(mark(0, true, st), "stage event");
+    if (q4k)
+        GDN_LAUNCH(launch_q4k_deq_codes2(layer->w_in, s.r_in, s.H, w.wc_in, w.ws_in, layer->w_out, s.H, s.c_v, w.wc_out,
+                                         w.ws_out, st),
+                   "dequant W_in, W_out");
+    GDN_LAUNCH(mark(1, true, st), "stage event");
+    // steps 1b, 1c: all tokens of all sequences in one product
+    if (q4k) {
+        GDN_LAUNCH(launch_quant_rows(static_cast<const uint16_t*>(x), T, s.H, w.xc, w.sx, st), "quantise x");
+        GDN_LAUNCH(mark(2, true, st), "stage event");
+        cudaError_t e = launch_gemm_codes(w.xc, w.sx, w.wc_in, w.ws_in, T, s.r_in, s.H, w.qkvz, s.n_bf16, s.n_bf16,
+                                          w.ba, 2 * s.hv, st);
+        if (e != cudaSuccess) return cuda_fail(e, "input projection");
+    } else {
+        GDN_LAUNCH(mark(2, true, st), "stage event");
+        GDN_LAUNCH(launch_gemm_f32(static_cast<const float*>(x), static_cast<const float*>(layer->w_in), T, s.r_in, s.H,
+                                   w.qkvz, s.n_bf16, s.n_bf16, w.ba, 2 * s.hv, st),
+                   "input projection");
+    }
+    GDN_LAUNCH(mark(3, true, st), "stage event");
+    // step 2 per sequence (its own conv state), in one launch
+    GDN_LAUNCH(launch_conv(*layer, w.qkvz, s.n_bf16, T, conv_state, w.ba, 2 * s.hv, w.qkv, w.log_a, w.b, st, cu_seqlens,
+                           n_seqs),
+               "conv");
+    GDN_LAUNCH(launch_conv_state(*layer, w.qkvz, s.n_bf16, T, conv_state, st, cu_seqlens, n_seqs), "conv state");
+    GDN_LAUNCH(mark(4, true, st), "stage event");
+    // step 3: every sequence chunked from its first token, all in parallel; step 4 after it
+    const float* la = layer->gate_log_a ? layer->gate_log_a : w.log_a;
+    const float* bb = layer->gate_b ? layer->gate_b : w.b;
+    const uint16_t* z = w.qkvz + s.c_conv;
+    const TokenRangeHook norm_hook = [&](int64_t t0, int64_t t1, cudaStream_t cs) {
+        return launch_gated_norm(*layer, w.o + t0 * s.c_v, z + t0 * s.n_bf16, s.n_bf16, t1 - t0,
+                                 w.oc ? w.oc + t0 * s.c_v : nullptr, w.so ? w.so + t0 : nullptr,
+                                 w.ohat ? w.ohat + t0 * s.c_v : nullptr, cs);
+    };
+    GDN_LAUNCH(launch_delta(*layer, w.qkv, la, bb, T, state_in, state_out, w.o, w.delta, st, true, &norm_hook, cu_seqlens,
+                            n_seqs),
+               "delta rule and gated norm");
+    GDN_LAUNCH(mark(5, true, st), "stage event");
+    GDN_LAUNCH(mark(6, true, st), "stage event");
+    // step 5
+    if (q4k) {
+        cudaError_t e = launch_gemm_codes(w.oc, w.so, w.wc_out, w.ws_out, T, s.H, s.c_v, static_cast<uint16_t*>(y), s.H,
+                                          s.H, nullptr, 0, st);
+        if (e != cudaSuccess) return cuda_fail(e, "output projection");
+    } else {
+        GDN_LAUNCH(launch_gemm_f32(w.ohat, static_cast<const float*>(layer->w_out), T, s.H, s.c_v, nullptr, 0, 0,
+                                   static_cast<float*>(y), s.H, st),
+                   "output projection");
+    }
+    GDN_LAUNCH(mark(7, true, st), "stage event");
     return GDN_OK;
 }
 

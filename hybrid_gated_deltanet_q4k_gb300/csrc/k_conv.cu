@@ -45,7 +45,7 @@ struct ConvArgs {
     float eps;
     float q_scale;
     const float* conv_w;   // [c_conv][4]
-    const float* tail;     // [c_conv][3]
+    const float* tail;     // [n_seqs][c_conv][3]: per sequence, the raw inputs before its first token
     uint16_t* out;         // [n][c_conv] fp16
     // gates
     const float* ba;
@@ -118,15 +118,18 @@ __device__ __forceinline__ void load_raw(const uint16_t* src, uint32_t (&x)[CPL 
     }
 }
 
+// Tokens t0 .. t1-1 (at most CONV_TOKENS) of one head, of a sequence whose
+// first token is ts and whose conv state is tail [c_conv][3].
 template <int CPL>
-__device__ __forceinline__ void conv_head_run(const ConvArgs& a, int head, int t0) {
+__device__ __forceinline__ void conv_head_run(const ConvArgs& a, int head, int t0, int t1, int ts, const float* tail) {
     const int lane = threadIdx.x & 31;
     const int c0 = head * a.d + lane * CPL;
     float h0[CPL], h1[CPL], h2[CPL];  // x_{t-3}, x_{t-2}, x_{t-1}
     auto raw = [&](int t, int i) -> float {
-        // raw input x_t of channel c0+i; t < 0 reads the conv state (oldest first)
-        if (t >= 0) return bf16_bits_to_float(a.qkvz[static_cast<int64_t>(t) * a.ld_qkvz + c0 + i]);
-        return a.tail[static_cast<int64_t>(c0 + i) * 3 + (3 + t)];
+        // raw input x_t of channel c0+i; a token before the sequence's first
+        // reads its conv state (oldest first)
+        if (t >= ts) return bf16_bits_to_float(a.qkvz[static_cast<int64_t>(t) * a.ld_qkvz + c0 + i]);
+        return tail[static_cast<int64_t>(c0 + i) * 3 + (3 + t - ts)];
     };
 #pragma unroll
     for (int i = 0; i < CPL; ++i) {
@@ -134,7 +137,6 @@ __device__ __forceinline__ void conv_head_run(const ConvArgs& a, int head, int t
         h1[i] = raw(t0 - 2, i);
         h2[i] = raw(t0 - 1, i);
     }
-    const int t1 = min(a.n, t0 + CONV_TOKENS);
     // All CONV_TOKENS rows of the run are loaded (packed bf16 pairs) before the
     // first is used, so each warp keeps the whole run in flight.
     uint32_t xr[CONV_TOKENS][CPL / 2];
@@ -151,16 +153,20 @@ __device__ __forceinline__ void conv_head_run(const ConvArgs& a, int head, int t
     conv_head_tokens<CPL, CONV_TOKENS>(a, head, t0, t1, xr, h0, h1, h2);
 }
 
+// Block x: run blockIdx.x of the runs of CONV_TOKENS tokens that tile each
+// sequence from its first token (sq: runs as units).
 template <int CPL>
-__global__ void __launch_bounds__(CONV_WARPS * 32, 3) conv_kernel(ConvArgs a) {
-    const int t0 = blockIdx.x * CONV_TOKENS;
+__global__ void __launch_bounds__(CONV_WARPS * 32, 3) conv_kernel(ConvArgs a, const __grid_constant__ SeqTable sq) {
+    const int r = blockIdx.x, s = seq_of_unit(sq, r);
+    const int ts = sq.tok[s];
+    const int t0 = ts + (r - sq.unit[s]) * CONV_TOKENS;
+    const int t1 = min(sq.tok[s + 1], t0 + CONV_TOKENS);
     if (static_cast<int>(blockIdx.y) < a.conv_blocks_y) {
         const int head = blockIdx.y * CONV_WARPS + (threadIdx.x >> 5);
-        if (head < a.n_heads) conv_head_run<CPL>(a, head, t0);
+        if (head < a.n_heads) conv_head_run<CPL>(a, head, t0, t1, ts, a.tail + static_cast<int64_t>(s) * a.c_conv * 3);
         return;
     }
-    // gate block: tokens t0 .. t0+CONV_TOKENS-1, all value heads
-    const int t1 = min(a.n, t0 + CONV_TOKENS);
+    // gate block: tokens t0 .. t1-1, all value heads
     for (int i = threadIdx.x; i < (t1 - t0) * a.hv; i += blockDim.x) {
         const int t = t0 + i / a.hv, h = i % a.hv;
         const float beta = a.ba[static_cast<int64_t>(t) * a.ld_ba + h];
@@ -198,39 +204,50 @@ static ConvArgs conv_args(const gdn_layer& L, const uint16_t* qkvz, int64_t ld_q
     return a;
 }
 
+// cu_seqlens: host token offsets [n_seqs + 1] of the call's sequences (null:
+// one sequence of n tokens); tail then holds one conv state per sequence.
 cudaError_t launch_conv(const gdn_layer& L, const uint16_t* qkvz, int64_t ld_qkvz, int64_t n, const float* tail,
-                        const float* ba, int64_t ld_ba, uint16_t* out, float* log_a, float* b, cudaStream_t st) {
+                        const float* ba, int64_t ld_ba, uint16_t* out, float* log_a, float* b, cudaStream_t st,
+                        const int64_t* cu_seqlens, int n_seqs) {
     const ConvArgs a = conv_args(L, qkvz, ld_qkvz, n, tail, ba, ld_ba, out, log_a, b);
     const bool gates = L.gate_log_a == nullptr;
-    dim3 grid(static_cast<unsigned>((n + CONV_TOKENS - 1) / CONV_TOKENS), static_cast<unsigned>(a.conv_blocks_y + (gates ? 1 : 0)));
+    const SeqTable sq = cu_seqlens ? make_seq_table(cu_seqlens, n_seqs, CONV_TOKENS) : one_seq_table(n, CONV_TOKENS);
+    if (sq.unit[sq.n] == 0) return cudaSuccess;
+    dim3 grid(static_cast<unsigned>(sq.unit[sq.n]), static_cast<unsigned>(a.conv_blocks_y + (gates ? 1 : 0)));
     if (L.dk == 128)
-        conv_kernel<4><<<grid, CONV_WARPS * 32, 0, st>>>(a);
+        conv_kernel<4><<<grid, CONV_WARPS * 32, 0, st>>>(a, sq);
     else
-        conv_kernel<2><<<grid, CONV_WARPS * 32, 0, st>>>(a);
+        conv_kernel<2><<<grid, CONV_WARPS * 32, 0, st>>>(a, sq);
     return cudaGetLastError();
 }
 
-// conv_state <- the last three raw inputs per channel (x_{N-3}, x_{N-2}, x_{N-1}),
-// from the projection, or from the old state for N < 3.  One thread per channel
+// conv_state of sequence blockIdx.y <- its last three raw inputs per channel
+// (x_{N-3}, x_{N-2}, x_{N-1} of its N tokens), from the projection, or from the
+// old state for N < 3 (an empty sequence keeps it).  One thread per channel
 // reads its three old values before writing, so the update is in place.
-__global__ void conv_state_kernel(const uint16_t* __restrict__ qkvz, int64_t ld, int n, int c_conv, float* state) {
+__global__ void conv_state_kernel(const uint16_t* __restrict__ qkvz, int64_t ld, int c_conv, float* state,
+                                  const __grid_constant__ SeqTable sq) {
     const int c = blockIdx.x * blockDim.x + threadIdx.x;
     if (c >= c_conv) return;
-    float old[3] = {state[c * 3 + 0], state[c * 3 + 1], state[c * 3 + 2]};
+    const int s = blockIdx.y, ts = sq.tok[s], n = sq.tok[s + 1] - ts;
+    float* st = state + static_cast<int64_t>(s) * c_conv * 3;
+    float old[3] = {st[c * 3 + 0], st[c * 3 + 1], st[c * 3 + 2]};
     float nw[3];
 #pragma unroll
     for (int j = 0; j < 3; ++j) {
         const int t = n - 3 + j;
-        nw[j] = t >= 0 ? bf16_bits_to_float(qkvz[static_cast<int64_t>(t) * ld + c]) : old[3 + t];
+        nw[j] = t >= 0 ? bf16_bits_to_float(qkvz[static_cast<int64_t>(ts + t) * ld + c]) : old[3 + t];
     }
 #pragma unroll
-    for (int j = 0; j < 3; ++j) state[c * 3 + j] = nw[j];
+    for (int j = 0; j < 3; ++j) st[c * 3 + j] = nw[j];
 }
 
+// cu_seqlens: as for launch_conv; state then holds one conv state per sequence.
 cudaError_t launch_conv_state(const gdn_layer& L, const uint16_t* qkvz, int64_t ld, int64_t n, float* state,
-                              cudaStream_t st) {
+                              cudaStream_t st, const int64_t* cu_seqlens, int n_seqs) {
     const int c_conv = 2 * L.n_qk_heads * L.dk + L.n_v_heads * L.dv;
-    conv_state_kernel<<<(c_conv + 255) / 256, 256, 0, st>>>(qkvz, ld, static_cast<int>(n), c_conv, state);
+    const SeqTable sq = cu_seqlens ? make_seq_table(cu_seqlens, n_seqs, 1) : one_seq_table(n, 1);
+    conv_state_kernel<<<dim3((c_conv + 255) / 256, sq.n), 256, 0, st>>>(qkvz, ld, c_conv, state, sq);
     return cudaGetLastError();
 }
 

@@ -196,7 +196,8 @@ __device__ __forceinline__ void block_mm24(const float* a, const float* b, float
 // over the four): three state warps (112 registers a thread once rounded)
 // leave 5632 registers, two prep warps of 88.
 template <int D>
-__global__ void __maxnreg__(88) delta_prep_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
+__global__ void __maxnreg__(88) delta_prep_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a,
+                                                   const __grid_constant__ SeqTable sq) {
     using L = PrepSmem<D>;
     extern __shared__ __align__(1024) unsigned char smb[];
     unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smb) + 1023) & ~uintptr_t(1023));
@@ -206,8 +207,11 @@ __global__ void __maxnreg__(88) delta_prep_kernel(const __grid_constant__ CUtens
     uint64_t* bars = reinterpret_cast<uint64_t*>(base + L::B0);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(base + L::MISC0);
 
-    const int chunk = a.chunk0 + blockIdx.x, hk = blockIdx.y;
-    const int t0 = chunk * DC;
+    // chunk chunk0 + blockIdx.x of sequence blockIdx.z (none past its end)
+    const int sq_i = blockIdx.z, local = a.chunk0 + blockIdx.x;
+    if (local >= sq.unit[sq_i + 1] - sq.unit[sq_i]) return;
+    const int chunk = sq.unit[sq_i] + local, hk = blockIdx.y;
+    const int t0 = sq.tok[sq_i] + local * DC, t_end = sq.tok[sq_i + 1];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int r = a.ratio;
 
@@ -236,10 +240,10 @@ __global__ void __maxnreg__(88) delta_prep_kernel(const __grid_constant__ CUtens
         float* bb = reinterpret_cast<float*>(base + L::BB0) + j * DC;
         float x0 = 0.f, x1 = 0.f;
         const int ta = t0 + 2 * lane, tb = ta + 1;
-        if (ta < a.n) x0 = a.log_a[static_cast<int64_t>(ta) * a.hv + h];
-        if (tb < a.n) x1 = a.log_a[static_cast<int64_t>(tb) * a.hv + h];
-        bb[2 * lane] = ta < a.n ? a.b[static_cast<int64_t>(ta) * a.hv + h] : 0.f;
-        bb[2 * lane + 1] = tb < a.n ? a.b[static_cast<int64_t>(tb) * a.hv + h] : 0.f;
+        if (ta < t_end) x0 = a.log_a[static_cast<int64_t>(ta) * a.hv + h];
+        if (tb < t_end) x1 = a.log_a[static_cast<int64_t>(tb) * a.hv + h];
+        bb[2 * lane] = ta < t_end ? a.b[static_cast<int64_t>(ta) * a.hv + h] : 0.f;
+        bb[2 * lane + 1] = tb < t_end ? a.b[static_cast<int64_t>(tb) * a.hv + h] : 0.f;
         float s = x0 + x1;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -579,7 +583,7 @@ __device__ __forceinline__ void mma_chain(uint32_t d_tmem, uint64_t adesc, uint6
 // warp issues nothing more), so no barrier is ever left waiting.
 template <int D>
 __global__ void __launch_bounds__(STATE_THREADS, 1)
-delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
+delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a, const __grid_constant__ SeqTable sq) {
     using L = StateSmem<D>;
     extern __shared__ __align__(1024) unsigned char smb[];
     unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smb) + 1023) & ~uintptr_t(1023));
@@ -590,6 +594,18 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
     const int h = blockIdx.x, i0 = blockIdx.y * NV, hk = h / a.ratio;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t sbase = smem_addr(base);
+    // chunks chunk0 .. chunk0 + nchunks - 1 of sequence blockIdx.z, those it has
+    const int sq_i = blockIdx.z;
+    const int nch = min(a.nchunks, sq.unit[sq_i + 1] - sq.unit[sq_i] - a.chunk0);
+    if (nch <= 0) return;
+    const int cg0 = sq.unit[sq_i] + a.chunk0;            // global index of the first (scratch tables)
+    const int tc0 = sq.tok[sq_i] + a.chunk0 * DC;        // its first token
+    const int t_end = sq.tok[sq_i + 1];
+    const int64_t sq_off = static_cast<int64_t>(sq_i) * a.hv * D * D;
+    // the sequence's state before the first chunk: the caller's (or zero) at
+    // its start, else what the previous token segment left in state_out
+    const float* st_in = a.chunk0 == 0 ? (a.state_in ? a.state_in + sq_off : nullptr) : a.state_out + sq_off;
+    float* st_out = a.state_out + sq_off;
 
     if (tid == 0) {
         for (int i = F_QK; i <= F_TA; ++i) mbar_init_cta(bars + i, 1);
@@ -609,15 +625,15 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             auto cb = [&](int c) { return static_cast<int64_t>(c) * a.hv + h; };
-            for (int j = 0; j < a.nchunks; ++j) {
-                const int c = a.chunk0 + j;
+            for (int j = 0; j < nch; ++j) {
+                const int c = cg0 + j, tc = tc0 + j * DC;
                 const uint32_t pp = (j - 1) & 1;   // phase of the previous chunk's release
                 if (j >= 1 && !state_wait(bars + E_QK, pp, abort)) break;
                 mbar_expect_tx(bars + F_QK, 2 * L::NSLAB * L::SLAB);
                 for (int sl = 0; sl < L::NSLAB; ++sl) {
                     unsigned char* dst = base + L::QK0 + sl * L::QK_SLAB;
-                    tma_load_2d_tile(dst, &qkv_map, bars + F_QK, hk * D + 64 * sl, c * DC);
-                    tma_load_2d_tile(dst + L::SLAB, &qkv_map, bars + F_QK, a.c_qk + hk * D + 64 * sl, c * DC);
+                    tma_load_2d_tile(dst, &qkv_map, bars + F_QK, hk * D + 64 * sl, tc);
+                    tma_load_2d_tile(dst + L::SLAB, &qkv_map, bars + F_QK, a.c_qk + hk * D + 64 * sl, tc);
                 }
                 const int kb = j & 1;
                 if (j >= 2 && !state_wait(bars + E_KT0 + kb, ((j - 2) >> 1) & 1, abort)) break;
@@ -627,7 +643,7 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
                              bars + F_KT0 + kb);
                 if (j >= 1 && !state_wait(bars + E_V, pp, abort)) break;
                 mbar_expect_tx(bars + F_V, L::SLAB + DC * 16);
-                tma_load_2d_tile(base + L::V0, &qkv_map, bars + F_V, 2 * a.c_qk + h * D + (i0 & ~63), c * DC);
+                tma_load_2d_tile(base + L::V0, &qkv_map, bars + F_V, 2 * a.c_qk + h * D + (i0 & ~63), tc);
                 bulk_load_1d(base + L::G0 + (j & 1) * DC * 16, a.G + cb(c) * DC * 4, DC * 16, bars + F_V);
                 if (j >= 1 && !state_wait(bars + E_TA, pp, abort)) break;
                 mbar_expect_tx(bars + F_TA, L::QK_SLAB);
@@ -649,7 +665,7 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
             t5::fence_after();
             return true;
         };
-        for (int j = 0; j < a.nchunks; ++j) {
+        for (int j = 0; j < nch; ++j) {
             const uint32_t ph = j & 1;
             nb_sync(NB_S);                      // S of chunk j written
             if (leader && ready(F_QK, ph)) {
@@ -696,7 +712,7 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
         float S[16];
 #pragma unroll
         for (int v = 0; v < 16; ++v)
-            S[v] = (own_d && a.state_in) ? a.state_in[(static_cast<int64_t>(h) * D + i0 + v0 + v) * D + d] : 0.f;
+            S[v] = (own_d && st_in) ? st_in[(static_cast<int64_t>(h) * D + i0 + v0 + v) * D + d] : 0.f;
         auto write_s = [&]() {
             if (own_d) {
                 unsigned char* sp = base + L::S0 + (d >> 6) * L::SOP;
@@ -732,8 +748,8 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
 
         write_s();
         handover(NB_S);
-        for (int j = 0; j < a.nchunks; ++j) {
-            const int c = a.chunk0 + j;
+        for (int j = 0; j < nch; ++j) {
+            const int tc = tc0 + j * DC;
             const uint32_t ph = j & 1;
             const float4* G = reinterpret_cast<const float4*>(base + L::G0 + ph * DC * 16);
             float4 gt = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -783,15 +799,15 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
                 for (int v = 0; v < 16; ++v) S[v] = fmaf(dec, S[v], u[v]);
                 write_s();
             }
-            if (j + 1 < a.nchunks) handover(NB_S);
+            if (j + 1 < nch) handover(NB_S);
 
             // ---- O = diag(e^gamma) Y + Z (Y rows: lanes 0-63), while the next X, Y run;
             // written in fp16 (|o_i| <= max|S| |q|_1 <= 65504 for |q| <= d^-1/2; checked)
             if (!xw && mma_done(M_DZ, ph)) {
                 float y[16], z[16];
                 t5::ld16x2(tl + TM_XY + 32 * ph, y, tl + TM_DZ, z);
-                const int t = c * DC + tok;
-                if (t < a.n) {
+                const int t = tc + tok;
+                if (t < t_end) {
                     float ov[2][8];
 #pragma unroll
                     for (int v = 0; v < 16; ++v) {
@@ -806,7 +822,7 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a) {
         }
         if (!*abort && own_d) {
 #pragma unroll
-            for (int v = 0; v < 16; ++v) a.state_out[(static_cast<int64_t>(h) * D + i0 + v0 + v) * D + d] = S[v];
+            for (int v = 0; v < 16; ++v) st_out[(static_cast<int64_t>(h) * D + i0 + v0 + v) * D + d] = S[v];
         }
         if (bad) atomicCAS(&g_delta_error, 0, ERR_RANGE);
     }
@@ -866,27 +882,32 @@ int read_and_clear_delta_error() {
     return v;
 }
 
-// Token segments of DELTA_SEG_CHUNKS chunks.  With more than one, the prep
-// of segment i+1 runs on the library's low-priority stream while the state
-// pass of segment i runs on its high-priority one (the state is carried
-// between segments in state_out, fp32, so the results are those of one
-// launch).  Both are forked from the caller's stream and joined back to it.
+// Token segments of DELTA_SEG_CHUNKS chunks of every sequence.  With more
+// than one, the prep of segment i+1 runs on the library's low-priority stream
+// while the state pass of segment i runs on its high-priority one (the state
+// is carried between segments in state_out, fp32, so the results are those of
+// one launch).  Both are forked from the caller's stream and joined back to
+// it.  Each launch covers all sequences (grid z); a CTA past the end of its
+// sequence returns at once.
 constexpr int DELTA_SEG_CHUNKS = 64;
 template <int D>
-static void launch_prep(const CUtensorMap& map, const DeltaArgs& a, cudaStream_t st) {
-    delta_prep_kernel<D><<<dim3(a.nchunks, a.hv / a.ratio), DELTA_THREADS, PrepSmem<D>::BYTES + 1024, st>>>(map, a);
+static void launch_prep(const CUtensorMap& map, const DeltaArgs& a, const SeqTable& sq, cudaStream_t st) {
+    delta_prep_kernel<D><<<dim3(a.nchunks, a.hv / a.ratio, sq.n), DELTA_THREADS, PrepSmem<D>::BYTES + 1024, st>>>(map, a, sq);
 }
 template <int D>
-static void launch_state(const CUtensorMap& map, const DeltaArgs& a, cudaStream_t st) {
-    delta_state_kernel<D><<<dim3(a.hv, D / NV), STATE_THREADS, StateSmem<D>::BYTES + 1024, st>>>(map, a);
+static void launch_state(const CUtensorMap& map, const DeltaArgs& a, const SeqTable& sq, cudaStream_t st) {
+    delta_state_kernel<D><<<dim3(a.hv, D / NV, sq.n), STATE_THREADS, StateSmem<D>::BYTES + 1024, st>>>(map, a, sq);
 }
 
 // after_state (may be null): work on each segment's output tokens, enqueued on
 // the low-priority stream once that segment's state pass is done (after all
 // the preps, so it never delays one), so that it too runs beside the later
-// state segments; without segments it runs on st after the state pass.
+// state segments; without segments it runs on st after the state pass.  With
+// several sequences a segment's tokens are not contiguous, and the hook runs
+// once over all tokens after the last state segment.
 template <int D>
-static cudaError_t launch_delta_d(DeltaArgs& a, cudaStream_t st, bool overlap, const TokenRangeHook* after_state) {
+static cudaError_t launch_delta_d(DeltaArgs& a, const SeqTable& sq, cudaStream_t st, bool overlap,
+                                  const TokenRangeHook* after_state) {
     static bool attr = false;
     if (!attr) {
         cudaFuncSetAttribute(delta_prep_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, PrepSmem<D>::BYTES + 1024);
@@ -898,16 +919,20 @@ static cudaError_t launch_delta_d(DeltaArgs& a, cudaStream_t st, bool overlap, c
     }
     CUtensorMap map;
     if (!make_qkv_map(&map, a.qkv, a.n, a.c_conv)) return cudaErrorInvalidValue;
-    const int nch = a.nchunks;
+    int nch = 0;  // chunks of the longest sequence
+    for (int i = 0; i < sq.n; ++i) nch = std::max(nch, sq.unit[i + 1] - sq.unit[i]);
     a.chunk0 = 0;
+    a.nchunks = nch;
+    if (nch == 0) return cudaSuccess;
     if (!overlap || nch <= DELTA_SEG_CHUNKS) {
-        launch_prep<D>(map, a, st);
+        launch_prep<D>(map, a, sq, st);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
-        launch_state<D>(map, a, st);
+        launch_state<D>(map, a, sq, st);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         return after_state ? (*after_state)(0, a.n, st) : cudaSuccess;
     }
+    const bool per_segment_hook = after_state && sq.n == 1;
     std::lock_guard<std::mutex> lock(lib_streams_mutex());
     LibStreams* ls = nullptr;
     cudaError_t e = lib_streams(&ls);
@@ -922,17 +947,16 @@ static cudaError_t launch_delta_d(DeltaArgs& a, cudaStream_t st, bool overlap, c
         DeltaArgs s = a;
         s.chunk0 = c0;
         s.nchunks = nch - c0 < DELTA_SEG_CHUNKS ? nch - c0 : DELTA_SEG_CHUNKS;
-        if (c0 > 0) s.state_in = a.state_out;
-        launch_prep<D>(map, s, prep_st);
+        launch_prep<D>(map, s, sq, prep_st);
         if ((first = cudaGetLastError()) != cudaSuccess) break;
         if ((first = cudaEventRecord(ls->ev_b, prep_st)) != cudaSuccess) break;
         if ((first = cudaStreamWaitEvent(state_st, ls->ev_b, 0)) != cudaSuccess) break;
-        launch_state<D>(map, s, state_st);
+        launch_state<D>(map, s, sq, state_st);
         if ((first = cudaGetLastError()) != cudaSuccess) break;
-        if (after_state && nseg < LIB_EVENT_POOL) first = cudaEventRecord(ls->pool[nseg], state_st);
+        if (per_segment_hook && nseg < LIB_EVENT_POOL) first = cudaEventRecord(ls->pool[nseg], state_st);
         ++nseg;
     }
-    if (after_state && first == cudaSuccess) {
+    if (per_segment_hook && first == cudaSuccess) {
         // segments past the event pool wait for the last state segment
         if (nseg > LIB_EVENT_POOL) first = cudaEventRecord(ls->ev_a, state_st);
         for (int i = 0; i < nseg && first == cudaSuccess; ++i) {
@@ -948,14 +972,18 @@ static cudaError_t launch_delta_d(DeltaArgs& a, cudaStream_t st, bool overlap, c
     if (e == cudaSuccess) e = cudaStreamWaitEvent(state_st, ls->ev_b, 0);
     if (e == cudaSuccess) e = cudaEventRecord(ls->ev_a, state_st);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ls->ev_a, 0);
+    if (first == cudaSuccess && e == cudaSuccess && after_state && !per_segment_hook) first = (*after_state)(0, a.n, st);
     return first != cudaSuccess ? first : e;
 }
 
 cudaError_t launch_delta(const gdn_layer& L, const uint16_t* qkv, const float* log_a, const float* b, int64_t n,
                          const float* state_in, float* state_out, uint16_t* o, void* scratch, cudaStream_t st,
-                         bool overlap, const TokenRangeHook* after_state) {
+                         bool overlap, const TokenRangeHook* after_state, const int64_t* cu_seqlens, int n_seqs) {
     DeltaArgs a;
     const int d = L.dk;
+    // the call's sequences (host token offsets; null: one sequence of n tokens),
+    // each chunked from its first token; the states are [n_seqs][hv][D][D]
+    const SeqTable sq = cu_seqlens ? make_seq_table(cu_seqlens, n_seqs, DC) : one_seq_table(n, DC);
     a.qkv = qkv;
     a.log_a = log_a;
     a.b = b;
@@ -966,8 +994,8 @@ cudaError_t launch_delta(const gdn_layer& L, const uint16_t* qkv, const float* l
     a.c_v = L.n_v_heads * d;
     a.c_conv = 2 * a.c_qk + a.c_v;
     a.chunk0 = 0;
-    a.nchunks = static_cast<int>((n + DC - 1) / DC);
-    const int64_t nch = a.nchunks;
+    a.nchunks = 0;
+    const int64_t nch = sq.unit[sq.n];   // chunks of all sequences: the scratch tables' extent
     unsigned char* base = static_cast<unsigned char*>(scratch);
     a.TA = reinterpret_cast<uint16_t*>(base);
     a.G = reinterpret_cast<float*>(base + nch * a.hv * 2 * DC * DC * 2);
@@ -975,7 +1003,8 @@ cudaError_t launch_delta(const gdn_layer& L, const uint16_t* qkv, const float* l
     a.state_in = state_in;
     a.state_out = state_out;
     a.o = o;
-    return d == 128 ? launch_delta_d<128>(a, st, overlap, after_state) : launch_delta_d<64>(a, st, overlap, after_state);
+    return d == 128 ? launch_delta_d<128>(a, sq, st, overlap, after_state)
+                    : launch_delta_d<64>(a, sq, st, overlap, after_state);
 }
 
 }  // namespace gdn

@@ -18,6 +18,7 @@ c_int32, c_int64, c_float, c_void_p, c_size_t = ctypes.c_int32, ctypes.c_int64, 
 GDN_OK, GDN_EINVAL, GDN_ENOMEM, GDN_ECUDA, GDN_ETIMEOUT, GDN_ERANGE = 0, -1, -2, -3, -4, -5
 GDN_W_Q4K, GDN_W_F32 = 0, 1
 GDN_CHUNK = 64
+GDN_MAX_SEQS = 256
 GDN_N_STAGE_EVENTS = 8
 GDN_NOALLOC_SCRATCH_BYTES = 48 << 20
 STAGE_NAMES = ["dequant", "act_quant", "in_proj", "conv", "delta_rule", "gated_norm", "out_proj"]
@@ -40,6 +41,8 @@ _SIGNATURES = {
     "q4k_deq_i8": (c_int32, [_P, c_int64, c_int64, _P, _P, _P]),
     "gdn_workspace_size": (c_size_t, [_P, c_int64]),
     "gdn_prefill": (c_int32, [_P, _P, c_int64, _P, _P, _P, _P, _P, c_size_t, _P]),
+    "gdn_batch_workspace_size": (c_size_t, [_P, c_int64, c_int32]),
+    "gdn_prefill_batch": (c_int32, [_P, _P, _P, c_int32, _P, _P, _P, _P, _P, c_size_t, _P]),
     "gdn_host_workspace_size": (c_size_t, [_P, c_int64]),
     "gdn_prefill_host": (c_int32, [_P, _P, c_int64, _P, _P, _P, _P, c_int64, _P, c_size_t, _P]),
     "gdn_sync_status": (c_int32, [_P]),

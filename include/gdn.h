@@ -65,6 +65,7 @@ extern "C" {
 #define GDN_W_F32 1 /* weights and activations fp32, no quantisation anywhere */
 
 #define GDN_CHUNK 64 /* tokens per chunk of the chunked delta rule */
+#define GDN_MAX_SEQS 256 /* sequences per gdn_prefill_batch call */
 
 /*
  * One GDN layer.  Sizes: Hk = n_qk_heads, Hv = n_v_heads (a multiple of Hk,
@@ -154,6 +155,34 @@ size_t gdn_workspace_size(const gdn_layer *layer, int64_t ubatch_tokens);
 int gdn_prefill(const gdn_layer *layer, const void *x, int64_t n_tokens, const float *state_in,
                 float *state_out, float *conv_state, void *y, void *workspace, size_t ws_bytes,
                 void *stream);
+
+/*
+ * gdn_prefill_batch -- the whole layer over several independent sequences in
+ * one call (variable lengths, each with its own recurrent state and conv
+ * tail): the projections run once over the tokens of all sequences, and the
+ * state passes of the sequences run side by side (the pages' decode kernels
+ * put heads x sequences on the grid: "CRUX parity spike" #4220, technique
+ * table row 1).  Each sequence is chunked from its own first token, so its
+ * results are bitwise those of a gdn_prefill call on that sequence alone.
+ *   x           bf16 (Q4_K) or fp32 (F32) [T][hidden]: the sequences' tokens
+ *               one after another, T = cu_seqlens[n_seqs]
+ *   cu_seqlens  HOST int64 [n_seqs + 1]: cu_seqlens[0] = 0, non-decreasing;
+ *               sequence i holds tokens [cu_seqlens[i], cu_seqlens[i+1]).  A
+ *               sequence may be empty: its state is passed through.
+ *   n_seqs      1 .. GDN_MAX_SEQS
+ *   state_in    fp32 [n_seqs][Hv][dv][dk] or NULL (all zero)
+ *   state_out   fp32 [n_seqs][Hv][dv][dk]; may equal state_in
+ *   conv_state  fp32 [n_seqs][C_conv][3], in/out, one tail per sequence
+ *   y           as x
+ *   layer->gate_log_a, gate_b   when given: device [T][Hv]
+ *   workspace   device, 256-byte aligned, ws_bytes >=
+ *               gdn_batch_workspace_size(layer, T, n_seqs); the call runs in
+ *               one pass (GDN_ENOMEM when the workspace is smaller)
+ */
+size_t gdn_batch_workspace_size(const gdn_layer *layer, int64_t n_tokens, int n_seqs);
+int gdn_prefill_batch(const gdn_layer *layer, const void *x, const int64_t *cu_seqlens, int n_seqs,
+                      const float *state_in, float *state_out, float *conv_state, void *y, void *workspace,
+                      size_t ws_bytes, void *stream);
 
 /*
  * gdn_prefill_host -- gdn_prefill fed from, and writing to, host memory: the
