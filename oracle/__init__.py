@@ -12,6 +12,9 @@ threads on Qwen3.5 prefill speed):
 * ``q4k``    the GGUF Q4_K superblock (256 values, 8 sub-blocks of 32, 6-bit
   scales and mins, fp16 d/dmin), its decode to exact fp32, and a plain
   min-max encoder;
+* ``q6k``    the GGUF Q6_K superblock (256 values, 16 sub-blocks of 16, int8
+  scales, fp16 d, 6-bit codes split into 4 + 2 bits), its exact decode and a
+  plain absmax encoder;
 * ``quant``  int8 row quantisation with one fp32 scale per row, the exact
   integer product of two int8 matrices and its fp32 rescale, bf16 rounding;
 * ``layer``  the causal 4-tap conv with SiLU, per-head L2 norm, the gates,
@@ -28,4 +31,4 @@ has no worked example on the pages, so its end-to-end values are pinned only
 through the pinned stages and the layer-level invariants (extend equals
 re-prefill, chunked equals sequential).
 """
-from . import q4k, quant, layer  # noqa: F401
+from . import q4k, q6k, quant, layer  # noqa: F401
