@@ -56,7 +56,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-pass", type=int, default=8192, help="tokens per pass of the host-fed call")
-    ap.add_argument("--stage", choices=["in_proj", "delta_rule"], default=None,
+    ap.add_argument("--stage", choices=["in_proj", "delta_rule", "q6k_deq", "q4k_deq"], default=None,
                     help="time one stage kernel alone through its stage entry point (profiling case)")
     ap.add_argument("--tokens", type=int, default=None,
                     help="tokens per step (default: the workload's N); a smaller N is a profiling case, not the metric")
@@ -457,6 +457,17 @@ def run_stage(args, spec):
         fn = lambda: L.gdn_gemm_codes(gl.ptr(xc), gl.ptr(sx), gl.ptr(wc), gl.ptr(ws), n, r_in, H, gl.ptr(out), nbf,  # noqa: E731
                                       nbf, gl.ptr(ba), 2 * hv, st)
         work, unit = 2.0 * n * r_in * H / 1e12, "TFLOP"
+    elif args.stage in ("q6k_deq", "q4k_deq"):
+        # step 1a alone on the input-projection matrix [R_in][H], each format:
+        # HBM bytes = blocks read + int8 codes and fp32 scales written
+        from hybrid_gated_deltanet_q4k_gb300.api import pack_q4k, pack_q6k
+        q6 = args.stage == "q6k_deq"
+        blocks = torch.from_numpy((pack_q6k if q6 else pack_q4k)(layer["w_in"])).cuda()
+        q8 = torch.empty(r_in, H, dtype=torch.int8, device="cuda")
+        sc = torch.empty(r_in, dtype=torch.float32, device="cuda")
+        dec = L.q6k_deq_i8 if q6 else L.q4k_deq_i8
+        fn = lambda: dec(gl.ptr(blocks), r_in, H, gl.ptr(q8), gl.ptr(sc), st)  # noqa: E731
+        work, unit = (blocks.numel() + q8.numel() + 4 * r_in) / 1e9, "GB"
     else:
         s = dl.struct()
         qkv = (torch.randn(n, spec.c_conv, device="cuda", generator=g) * 0.05).to(torch.float16)

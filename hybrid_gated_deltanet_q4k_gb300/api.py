@@ -22,18 +22,29 @@ def pack_q4k(w: np.ndarray) -> np.ndarray:
     return out
 
 
+def pack_q6k(w: np.ndarray) -> np.ndarray:
+    """Host Q6_K encoding through the library (``q6k_pack``)."""
+    w = np.ascontiguousarray(w, np.float32)
+    out = np.zeros((w.shape[0], w.shape[1] // 256 * 210), np.uint8)
+    gl.load().q6k_pack(gl.ptr(w), w.shape[0], w.shape[1], gl.ptr(out))
+    return out
+
+
 class DeviceLayer:
     """One GDN layer's parameters in device memory, in the layouts ``gdn_layer`` names."""
 
     def __init__(self, spec, params: dict, device: str = "cuda", eps_l2: float = 1e-6, eps_rms: float = 1e-6,
-                 q_scale: float | None = None, blocks: dict | None = None):
+                 q_scale: float | None = None, blocks: dict | None = None, q6k: tuple = ()):
+        """q6k: names of the matrices ("w_in", "w_out") to hold in Q6_K instead of Q4_K."""
         self.spec = spec
         self.device = device
         self.lib = gl.load()
+        self.q6k_mask = (1 if "w_in" in q6k else 0) | (2 if "w_out" in q6k else 0)
         t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)  # noqa: E731
         if spec.wtype == "q4k":
-            b_in = blocks["w_in"] if blocks else pack_q4k(params["w_in"])
-            b_out = blocks["w_out"] if blocks else pack_q4k(params["w_out"])
+            enc = {k: (pack_q6k if k in q6k else pack_q4k) for k in ("w_in", "w_out")}
+            b_in = blocks["w_in"] if blocks else enc["w_in"](params["w_in"])
+            b_out = blocks["w_out"] if blocks else enc["w_out"](params["w_out"])
             self.host_blocks = {"w_in": b_in, "w_out": b_out}
             self.dev = {"w_in": t(b_in), "w_out": t(b_out)}
         else:
@@ -44,7 +55,9 @@ class DeviceLayer:
         self.q_scale = spec.dk ** -0.5 if q_scale is None else q_scale
 
     def struct(self, gate_log_a=None, gate_b=None) -> gl.GdnLayer:
-        return gl.make_layer_struct(self.spec, self.dev, self.eps_l2, self.eps_rms, self.q_scale, gate_log_a, gate_b)
+        L = gl.make_layer_struct(self.spec, self.dev, self.eps_l2, self.eps_rms, self.q_scale, gate_log_a, gate_b)
+        L.q6k_mask = self.q6k_mask
+        return L
 
     def workspace_bytes(self, ubatch_tokens: int) -> int:
         s = self.struct()

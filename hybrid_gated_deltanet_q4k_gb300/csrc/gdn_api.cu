@@ -20,6 +20,8 @@
 namespace gdn {
 cudaError_t launch_q4k_deq_i8(const void*, int64_t, int64_t, int8_t*, float*, cudaStream_t);
 cudaError_t launch_q4k_deq_codes(const void*, int64_t, int64_t, uint16_t*, float*, cudaStream_t);
+cudaError_t launch_q6k_deq_i8(const void*, int64_t, int64_t, int8_t*, float*, cudaStream_t);
+cudaError_t launch_q6k_deq_codes(const void*, int64_t, int64_t, uint16_t*, float*, cudaStream_t);
 cudaError_t launch_q4k_deq_codes2(const void*, int64_t, int64_t, uint16_t*, float*, const void*, int64_t, int64_t,
                                   uint16_t*, float*, cudaStream_t);
 cudaError_t launch_quant_rows(const uint16_t*, int64_t, int64_t, uint16_t*, float*, cudaStream_t);
@@ -110,7 +112,8 @@ int check_layer(const gdn_layer* L, Sizes* s) {
     if ((L->gate_log_a == nullptr) != (L->gate_b == nullptr)) return fail(GDN_EINVAL, "gate_log_a and gate_b: both or neither");
     if (!aligned(L->w_in, 16) || !aligned(L->w_out, 16) || !aligned(L->conv_w, 16))
         return fail(GDN_EINVAL, "w_in, w_out and conv_w must be 16-byte aligned");
-    if (L->reserved0 != 0) return fail(GDN_EINVAL, "reserved0 must be 0");
+    if (L->q6k_mask & ~3) return fail(GDN_EINVAL, "q6k_mask: only bits 0 (w_in) and 1 (w_out) are defined");
+    if (L->q6k_mask && L->wtype != GDN_W_Q4K) return fail(GDN_EINVAL, "q6k_mask needs a quantised (GDN_W_Q4K) layer");
     return GDN_OK;
 }
 
@@ -239,6 +242,26 @@ int64_t pass_tokens_for(const gdn_layer* layer, const Sizes& s, int64_t n, size_
     return lo >= GDN_CHUNK ? lo - lo % GDN_CHUNK : lo;
 }
 
+// Step 1a for both weight matrices: each decoded from its own format (Q4_K,
+// or Q6_K where the layer's q6k_mask says so) to int8 codes + row scales.
+// Two Q4_K matrices share one launch.
+int decode_weights(const gdn_layer* L, const Sizes& s, const Workspace& w, cudaStream_t st) {
+    const bool in6 = L->q6k_mask & 1, out6 = L->q6k_mask & 2;
+    if (!in6 && !out6) {
+        GDN_LAUNCH(launch_q4k_deq_codes2(L->w_in, s.r_in, s.H, w.wc_in, w.ws_in, L->w_out, s.H, s.c_v, w.wc_out,
+                                         w.ws_out, st),
+                   "dequant W_in, W_out");
+        return GDN_OK;
+    }
+    GDN_LAUNCH(in6 ? launch_q6k_deq_codes(L->w_in, s.r_in, s.H, w.wc_in, w.ws_in, st)
+                   : launch_q4k_deq_codes(L->w_in, s.r_in, s.H, w.wc_in, w.ws_in, st),
+               "dequant W_in");
+    GDN_LAUNCH(out6 ? launch_q6k_deq_codes(L->w_out, s.H, s.c_v, w.wc_out, w.ws_out, st)
+                    : launch_q4k_deq_codes(L->w_out, s.H, s.c_v, w.wc_out, w.ws_out, st),
+               "dequant W_out");
+    return GDN_OK;
+}
+
 // Device staging of gdn_prefill_host beyond the pass workspace: two slots each
 // of x, y and (when the gates are drawn) log a and b.
 size_t host_stage_bytes(const gdn_layer* L, const Sizes& s, int64_t B) {
@@ -297,6 +320,25 @@ int gdn_q4k_deq_codes(const void* blocks, int64_t rows, int64_t cols, uint16_t* 
         return fail(GDN_EINVAL, "gdn_q4k_deq_codes: rows >= 1 and cols a multiple of 256 in [256, 16384] required");
     if (!aligned(blocks, 16) || !aligned(codes, 16)) return fail(GDN_EINVAL, "gdn_q4k_deq_codes: 16-byte alignment required");
     GDN_LAUNCH(launch_q4k_deq_codes(blocks, rows, cols, codes, row_scale, static_cast<cudaStream_t>(stream)), "gdn_q4k_deq_codes");
+    return GDN_OK;
+}
+
+int q6k_deq_i8(const void* blocks, int64_t rows, int64_t cols, int8_t* q, float* row_scale, void* stream) {
+    if (!blocks || !q || !row_scale) return fail(GDN_EINVAL, "q6k_deq_i8: NULL pointer");
+    if (rows < 1 || rows > 0x7fffffff || cols < 256 || cols > 16384 || cols % 256)
+        return fail(GDN_EINVAL, "q6k_deq_i8: rows >= 1 and cols a multiple of 256 in [256, 16384] required");
+    if (!aligned(blocks, 16) || !aligned(q, 8)) return fail(GDN_EINVAL, "q6k_deq_i8: blocks 16-byte and q 8-byte alignment required");
+    GDN_LAUNCH(launch_q6k_deq_i8(blocks, rows, cols, q, row_scale, static_cast<cudaStream_t>(stream)), "q6k_deq_i8");
+    return GDN_OK;
+}
+
+int gdn_q6k_deq_codes(const void* blocks, int64_t rows, int64_t cols, uint16_t* codes, float* row_scale, void* stream) {
+    if (!blocks || !codes || !row_scale) return fail(GDN_EINVAL, "gdn_q6k_deq_codes: NULL pointer");
+    if (rows < 1 || rows > 0x7fffffff || cols < 256 || cols > 16384 || cols % 256)
+        return fail(GDN_EINVAL, "gdn_q6k_deq_codes: rows >= 1 and cols a multiple of 256 in [256, 16384] required");
+    if (!aligned(blocks, 16) || !aligned(codes, 16)) return fail(GDN_EINVAL, "gdn_q6k_deq_codes: 16-byte alignment required");
+    GDN_LAUNCH(launch_q6k_deq_codes(blocks, rows, cols, codes, row_scale, static_cast<cudaStream_t>(stream)),
+               "gdn_q6k_deq_codes");
     return GDN_OK;
 }
 
@@ -423,11 +465,7 @@ int gdn_prefill(const gdn_layer* layer, const void* x, int64_t n_tokens, const f
     Workspace w = carve(layer, s, B, workspace);
     const bool q4k = layer->wtype == GDN_W_Q4K;
     GDN_LAUNCH(mark(0, true, st), "stage event");
-    if (q4k) {
-        GDN_LAUNCH(launch_q4k_deq_codes2(layer->w_in, s.r_in, s.H, w.wc_in, w.ws_in, layer->w_out, s.H, s.c_v,
-                                         w.wc_out, w.ws_out, st),
-                   "dequant W_in, W_out");
-    }
+    if (q4k && (r = decode_weights(layer, s, w, st))) return r;
     GDN_LAUNCH(mark(1, true, st), "stage event");
     for (int64_t u0 = 0; u0 < n_tokens; u0 += B) {
         const int64_t nb = (n_tokens - u0) < B ? (n_tokens - u0) : B;
@@ -515,13 +553,10 @@ int gdn_prefill_host(const gdn_layer* layer, const void* x_host, int64_t n_token
     };
     auto pipeline = [&]() -> int {
         GDN_LAUNCH(mark(0, true, st), "stage event");
-        if (q4k)
-            GDN_LAUNCH(launch_q4k_deq_codes2(layer->w_in, s.r_in, s.H, w.wc_in, w.ws_in, layer->w_out, s.H, s.c_v,
-                                             w.wc_out, w.ws_out, st),
-                       "dequant W_in, W_out");
-        GDN_LAUNCH(mark(1, true, st), "stage event");
-        int rr = copy_in(0);
+        int rr = q4k ? decode_weights(layer, s, w, st) : GDN_OK;
         if (rr) return rr;
+        GDN_LAUNCH(mark(1, true, st), "stage event");
+        if ((rr = copy_in(0))) return rr;
         for (int64_t p = 0; p < np; ++p) {
             const int64_t u0 = p * B, nb = (n_tokens - u0) < B ? (n_tokens - u0) : B;
             const int slot = static_cast<int>(p & 1);
@@ -602,10 +637,7 @@ int gdn_prefill_batch(const gdn_layer* layer, const void* x, const int64_t* cu_s
     Workspace w = carve(layer, s, T, workspace, n_chunks);
     const bool q4k = layer->wtype == GDN_W_Q4K;
     GDN_LAUNCH(mark(0, true, st), "stage event");
-    if (q4k)
-        GDN_LAUNCH(launch_q4k_deq_codes2(layer->w_in, s.r_in, s.H, w.wc_in, w.ws_in, layer->w_out, s.H, s.c_v, w.wc_out,
-                                         w.ws_out, st),
-                   "dequant W_in, W_out");
+    if (q4k && (r = decode_weights(layer, s, w, st))) return r;
     GDN_LAUNCH(mark(1, true, st), "stage event");
     // steps 1b, 1c: all tokens of all sequences in one product
     if (q4k) {

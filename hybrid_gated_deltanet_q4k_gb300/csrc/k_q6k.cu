@@ -1,0 +1,139 @@
+// Step 1a for Q6_K weights: superblocks -> int8 rows with one fp32 scale per row.
+//
+// sparkinfer PR #464 ("fused Q4K/Q6K->int8 dequant + token-parallel GDN conv
+// ..."), Summary, "Fused Q4_K/Q6_K -> int8-row dequant": the same fused
+// decode-and-quantise as for Q4_K, for the Q6_K tensors that Q4_K_M files
+// carry; the quantisation starts from the exact fp32 decode.
+//
+// Layout of one 210-byte superblock (GGUF Q6_K): ql[128] | qh[64] | int8
+// scales[16] | fp16 d.  Weight v (half h = v / 128, group g = (v % 128) / 32,
+// lane l = v % 32) has the 6-bit code c = low | high << 4 with low = nibble
+// g / 2 of ql[64h + 32(g % 2) + l] and high = bits 2g, 2g+1 of qh[32h + l];
+// it decodes to d * scales[v / 16] * (c - 32).  |d| has 11 significant bits,
+// |scale| <= 128 and |c - 32| <= 32, so the product is exact in fp32 in any
+// order of evaluation.
+//
+// One warp per weight row.  In iteration i the warp decodes superblock i,
+// lane L the 8 consecutive weights 8L .. 8L+7: they share h, g and one scale,
+// and their codes sit in 8 consecutive ql bytes (one nibble each) and 8
+// consecutive qh bytes (one bit pair each).  Superblocks are only 2-byte
+// aligned (210 = 2 * 105), so the lane reads 16-bit words.  Pass 1 finds the
+// row amax from each lane's largest |c - 32| (one multiply per lane and
+// superblock); pass 2 decodes, quantises with the row scale and writes the 8
+// codes as one vector (int8: 8 bytes, fp16 carriers: 16 bytes).
+#include "common.cuh"
+
+namespace gdn {
+
+constexpr int Q6_THREADS = 256;
+constexpr int Q6_BLOCK = 210;
+
+template <typename OutT>
+struct Q6Job {
+    const uint8_t* blocks;
+    int64_t rows;
+    int cols;
+    OutT* codes;
+    float* scale;
+};
+
+// The 8 six-bit codes of lane L's weights in superblock blk, as signed q = c - 32,
+// and the lane's d * scale (exact).
+__device__ __forceinline__ void q6k_lane(const uint8_t* blk, int lane, int (&q)[8], float& ds) {
+    const int v0 = 8 * lane, h = v0 >> 7, g = (v0 & 127) >> 5, l0 = v0 & 31;
+    const uint16_t* ql = reinterpret_cast<const uint16_t*>(blk + 64 * h + 32 * (g & 1) + l0);
+    const uint16_t* qh = reinterpret_cast<const uint16_t*>(blk + 128 + 32 * h + l0);
+    const int nsh = 4 * (g >> 1), hsh = 2 * g;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t lw = __ldg(ql + k), hw = __ldg(qh + k);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const uint32_t lo = (lw >> (8 * e + nsh)) & 15u;
+            const uint32_t hi = (hw >> (8 * e + hsh)) & 3u;
+            q[2 * k + e] = static_cast<int>(lo | (hi << 4)) - 32;
+        }
+    }
+    const int8_t sc = static_cast<int8_t>(__ldg(blk + 192 + (v0 >> 4)));
+    const float d = __half2float(__ushort_as_half(__ldg(reinterpret_cast<const uint16_t*>(blk + 208))));
+    ds = __fmul_rn(d, static_cast<float>(sc));
+}
+
+template <typename OutT>
+__device__ __forceinline__ void store_codes8(OutT* dst, const float (&c)[8]);
+
+template <>
+__device__ __forceinline__ void store_codes8<uint16_t>(uint16_t* dst, const float (&c)[8]) {
+    *reinterpret_cast<uint4*>(dst) = make_uint4(codes_to_f16x2(c[0], c[1]), codes_to_f16x2(c[2], c[3]),
+                                                codes_to_f16x2(c[4], c[5]), codes_to_f16x2(c[6], c[7]));
+}
+
+template <>
+__device__ __forceinline__ void store_codes8<int8_t>(int8_t* dst, const float (&c)[8]) {
+    uint32_t w[2] = {0u, 0u};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) w[e >> 2] |= (static_cast<uint32_t>(static_cast<int>(c[e])) & 0xffu) << (8 * (e & 3));
+    *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+}
+
+template <typename OutT>
+__global__ void __launch_bounds__(Q6_THREADS, 4) q6k_deq_rows_warp_kernel(Q6Job<OutT> j) {
+    const int lane = threadIdx.x & 31;
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * (Q6_THREADS / 32) + (threadIdx.x >> 5);
+    if (row >= j.rows) return;
+    const int nsb = j.cols >> 8;
+    const uint8_t* rb = j.blocks + row * static_cast<int64_t>(nsb) * Q6_BLOCK;
+
+    float amax = 0.0f;
+#pragma unroll 4
+    for (int i = 0; i < nsb; ++i) {
+        int q[8];
+        float ds;
+        q6k_lane(rb + i * Q6_BLOCK, lane, q, ds);
+        int m = 0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) m = max(m, abs(q[e]));
+        amax = fmaxf(amax, fabsf(ds * static_cast<float>(m)));   // exact: the largest |w| of the 8
+    }
+    amax = warp_max(amax);
+    const QScale qsc = make_qscale(amax);
+    if (lane == 0) j.scale[row] = qsc.s;
+    OutT* out = j.codes + row * static_cast<int64_t>(j.cols) + lane * 8;
+#pragma unroll 4
+    for (int i = 0; i < nsb; ++i) {
+        int q[8];
+        float ds;
+        q6k_lane(rb + i * Q6_BLOCK, lane, q, ds);
+        float w[8], c[8];
+        bool redo = !qsc.fast;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            w[e] = ds * static_cast<float>(q[e]);
+            c[e] = qcode_fast(w[e], qsc, redo);
+        }
+        if (redo) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) c[e] = qcode_exact(w[e], qsc.s);
+        }
+        store_codes8<OutT>(out + i * 256, c);
+    }
+}
+
+template <typename OutT>
+static cudaError_t launch_q6k(const void* blocks, int64_t rows, int64_t cols, OutT* q, float* s, cudaStream_t st) {
+    const Q6Job<OutT> j{static_cast<const uint8_t*>(blocks), rows, static_cast<int>(cols), q, s};
+    const int64_t wpb = Q6_THREADS / 32;
+    q6k_deq_rows_warp_kernel<OutT><<<static_cast<unsigned>((rows + wpb - 1) / wpb), Q6_THREADS, 0, st>>>(j);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_q6k_deq_i8(const void* blocks, int64_t rows, int64_t cols, int8_t* q, float* s, cudaStream_t st) {
+    return launch_q6k<int8_t>(blocks, rows, cols, q, s, st);
+}
+
+cudaError_t launch_q6k_deq_codes(const void* blocks, int64_t rows, int64_t cols, uint16_t* q, float* s,
+                                 cudaStream_t st) {
+    return launch_q6k<uint16_t>(blocks, rows, cols, q, s, st);
+}
+
+}  // namespace gdn

@@ -1,5 +1,7 @@
-// q4k_pack: fp32 weights -> GGUF Q4_K superblocks (host, plain min-max encoder).
+// q4k_pack, q6k_pack: fp32 weights -> GGUF Q4_K / Q6_K superblocks (host,
+// plain encoders).
 //
+// Q4_K (plain min-max):
 // The pages only ever decode Q4_K (sparkinfer PR #464, "Fused Q4_K/Q6_K ->
 // int8-row dequant"); the weights here are synthetic, so they are encoded with
 // the simplest encoder the format admits.  Per 32-weight sub-block j the range
@@ -18,6 +20,15 @@
 // and m_4..7; bytes 8-11 hold the low nibbles of sc_4..7 (bits 0-3) and of
 // m_4..7 (bits 4-7).  Code byte 32p + l holds weight 64p + l in its low nibble
 // and weight 64p + 32 + l in its high nibble.
+//
+// Q6_K (plain absmax; the pages name Q6_K beside Q4_K in the same summary):
+// per 16-weight sub-block j, step_j = max|w| / 31; d = max_j step_j / 127
+// rounded to fp16 (+0 for a zero); scale_j = clamp(rne(step_j / d), 0, 127);
+// q = clamp(rne(w / (d * scale_j)), -32, 31), a zero divisor giving 0.
+// Block layout (210 bytes): ql[128] | qh[64] | int8 scales[16] | fp16 d.  The
+// 6-bit code c = q + 32 of weight v (half h = v / 128, group g = (v % 128) /
+// 32, lane l = v % 32) keeps its low 4 bits in nibble g / 2 of ql[64h +
+// 32(g % 2) + l] and its high 2 bits in bits 2g, 2g+1 of qh[32h + l].
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -125,7 +136,48 @@ void pack_superblock(const float* x, uint8_t* out) {
             qs[32 * p + l] = static_cast<uint8_t>(q[64 * p + l] | (q[64 * p + 32 + l] << 4));
 }
 
+void pack_q6k_superblock(const float* x, uint8_t* out) {
+    float step[16];
+    for (int j = 0; j < 16; ++j) {
+        float amax = 0.0f;
+        for (int i = 0; i < 16; ++i) {
+            const float a = std::fabs(x[16 * j + i]);
+            if (a > amax) amax = a;
+        }
+        step[j] = amax / 31.0f;
+    }
+    float max_step = step[0];
+    for (int j = 1; j < 16; ++j)
+        if (step[j] > max_step) max_step = step[j];
+    uint16_t d16 = f32_to_f16_rne(max_step / 127.0f);
+    if ((d16 & 0x7fffu) == 0) d16 = 0;
+    const float d = f16_to_f32(d16);
+    int sc[16];
+    for (int j = 0; j < 16; ++j) sc[j] = d > 0.0f ? clamp_rne(step[j] / d, 0, 127) : 0;
+    uint8_t* ql = out;
+    uint8_t* qh = out + 128;
+    std::memset(out, 0, 192);
+    for (int v = 0; v < 256; ++v) {
+        const float ds = d * static_cast<float>(sc[v / 16]);
+        const int q = ds > 0.0f ? clamp_rne(x[v] / ds, -32, 31) : 0;
+        const int c = q + 32, h = v / 128, g = (v % 128) / 32, l = v % 32;
+        ql[64 * h + 32 * (g % 2) + l] |= static_cast<uint8_t>((c & 15) << (4 * (g / 2)));
+        qh[32 * h + l] |= static_cast<uint8_t>((c >> 4) << (2 * g));
+    }
+    for (int j = 0; j < 16; ++j) out[192 + j] = static_cast<uint8_t>(static_cast<int8_t>(sc[j]));
+    std::memcpy(out + 208, &d16, 2);
+}
+
 }  // namespace
+
+extern "C" int q6k_pack(const float* w, int64_t rows, int64_t cols, void* blocks) {
+    if (w == nullptr || blocks == nullptr || rows < 0 || cols <= 0 || cols % 256 != 0) return GDN_EINVAL;
+    const int64_t nsb = cols / 256;
+    uint8_t* out = static_cast<uint8_t*>(blocks);
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t b = 0; b < nsb; ++b) pack_q6k_superblock(w + r * cols + b * 256, out + (r * nsb + b) * 210);
+    return GDN_OK;
+}
 
 extern "C" int q4k_pack(const float* w, int64_t rows, int64_t cols, void* blocks) {
     if (w == nullptr || blocks == nullptr || rows < 0 || cols <= 0 || cols % 256 != 0) return GDN_EINVAL;

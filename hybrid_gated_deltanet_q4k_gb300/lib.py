@@ -28,7 +28,7 @@ class GdnLayer(ctypes.Structure):
     """Mirror of ``struct gdn_layer``."""
     _fields_ = [
         ("hidden", c_int32), ("n_qk_heads", c_int32), ("n_v_heads", c_int32), ("dk", c_int32), ("dv", c_int32),
-        ("conv_taps", c_int32), ("wtype", c_int32), ("reserved0", c_int32),
+        ("conv_taps", c_int32), ("wtype", c_int32), ("q6k_mask", c_int32),
         ("w_in", c_void_p), ("w_out", c_void_p), ("conv_w", c_void_p), ("A_log", c_void_p), ("dt_bias", c_void_p),
         ("norm_w", c_void_p), ("gate_log_a", c_void_p), ("gate_b", c_void_p),
         ("eps_l2", c_float), ("eps_rms", c_float), ("q_scale", c_float), ("reserved1", c_float),
@@ -39,6 +39,9 @@ _P = c_void_p
 _SIGNATURES = {
     "q4k_pack": (c_int32, [_P, c_int64, c_int64, _P]),
     "q4k_deq_i8": (c_int32, [_P, c_int64, c_int64, _P, _P, _P]),
+    "q6k_pack": (c_int32, [_P, c_int64, c_int64, _P]),
+    "q6k_deq_i8": (c_int32, [_P, c_int64, c_int64, _P, _P, _P]),
+    "gdn_q6k_deq_codes": (c_int32, [_P, c_int64, c_int64, _P, _P, _P]),
     "gdn_workspace_size": (c_size_t, [_P, c_int64]),
     "gdn_prefill": (c_int32, [_P, _P, c_int64, _P, _P, _P, _P, _P, c_size_t, _P]),
     "gdn_batch_workspace_size": (c_size_t, [_P, c_int64, c_int32]),

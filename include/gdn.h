@@ -83,9 +83,11 @@ typedef struct gdn_layer {
     int32_t dv;
     int32_t conv_taps; /* must be 4 */
     int32_t wtype;     /* GDN_W_Q4K or GDN_W_F32 */
-    int32_t reserved0; /* must be 0 */
-    const void *w_in;  /* Q4_K: [R_in][hidden/256] blocks of 144 B (16-byte aligned); F32: fp32 [R_in][hidden] */
-    const void *w_out; /* Q4_K: [hidden][C_v/256] blocks; F32: fp32 [hidden][C_v] */
+    int32_t q6k_mask;  /* GDN_W_Q4K layers: bit 0 set = w_in is Q6_K, bit 1 set = w_out is
+                          Q6_K (210-byte blocks, see q6k_pack); 0 = both Q4_K.  0 for F32. */
+    const void *w_in;  /* Q4_K: [R_in][hidden/256] blocks of 144 B (210 B if Q6_K), 16-byte aligned;
+                          F32: fp32 [R_in][hidden] */
+    const void *w_out; /* Q4_K: [hidden][C_v/256] blocks (Q6_K likewise); F32: fp32 [hidden][C_v] */
     const float *conv_w;  /* [C_conv][4]; tap 3 multiplies the current token */
     const float *A_log;   /* [Hv] */
     const float *dt_bias; /* [Hv] */
@@ -126,6 +128,30 @@ int q4k_pack(const float *w, int64_t rows, int64_t cols, void *blocks);
  * 256 <= cols <= 16384, cols % 256 == 0, rows >= 1.
  */
 int q4k_deq_i8(const void *blocks, int64_t rows, int64_t cols, int8_t *q, float *row_scale, void *stream);
+
+/*
+ * q6k_pack -- encode fp32 weights into GGUF Q6_K blocks (host only, no GPU),
+ * the second weight format of the fused dequant (sparkinfer PR #464,
+ * Summary, "Fused Q4_K/Q6_K -> int8-row dequant").  w: host fp32
+ * [rows][cols], cols a multiple of 256.  blocks: host output, rows *
+ * cols/256 * 210 bytes, each ql[128] | qh[64] | int8 scales[16] | fp16 d.
+ * Per 16-weight sub-block step = max|w| / 31; d = the largest step / 127
+ * rounded to fp16; scale = clamp(rne(step / d), 0, 127); 6-bit codes q + 32
+ * with q = clamp(rne(w / (d*scale)), -32, 31), all in IEEE fp32.  The pages
+ * give no encoder; this is the plain absmax one.
+ * Returns GDN_EINVAL for null pointers, rows < 0 or cols % 256 != 0.
+ */
+int q6k_pack(const float *w, int64_t rows, int64_t cols, void *blocks);
+
+/*
+ * q6k_deq_i8 -- q4k_deq_i8 for Q6_K rows: decode in registers (the exact
+ * fp32 value d*scale*(c - 32)) and quantise each row straight to int8 with one
+ * fp32 scale, row_scale = amax/127 and q = clamp(rne(w/row_scale), -127, 127)
+ * in IEEE fp32.  blocks: device [rows][cols/256][210 B], 16-byte aligned base.
+ * q: device int8 [rows][cols], 8-byte aligned.  row_scale: device fp32 [rows].
+ * 256 <= cols <= 16384, cols % 256 == 0, rows >= 1.
+ */
+int q6k_deq_i8(const void *blocks, int64_t rows, int64_t cols, int8_t *q, float *row_scale, void *stream);
 
 /*
  * gdn_workspace_size -- bytes of device workspace gdn_prefill needs to run
@@ -254,6 +280,10 @@ int gdn_set_stage_events(void *const *events, int n_events);
  * 16-byte aligned), the operand form of the tensor-core product.
  */
 int gdn_q4k_deq_codes(const void *blocks, int64_t rows, int64_t cols, uint16_t *codes,
+                      float *row_scale, void *stream);
+
+/* gdn_q6k_deq_codes -- gdn_q4k_deq_codes for Q6_K rows (q6k_deq_i8's codes as fp16 patterns). */
+int gdn_q6k_deq_codes(const void *blocks, int64_t rows, int64_t cols, uint16_t *codes,
                       float *row_scale, void *stream);
 
 /*

@@ -34,6 +34,7 @@ from __future__ import annotations
 import numpy as np
 
 from . import q4k as _q4k
+from . import q6k as _q6k
 from . import quant as _quant
 
 f64 = np.float64
@@ -168,6 +169,15 @@ def layer_sizes(p):
             "r_in": 2 * c_qk + 2 * c_v + 2 * hv}
 
 
+def unpack_weights(p, name, rows, cols):
+    """Decode a quantised weight matrix: Q4_K, or Q6_K when p[name + "_fmt"] is
+    "q6k" (the pages' fused dequant takes both formats: sparkinfer PR #464,
+    Summary, "Fused Q4_K/Q6_K -> int8-row dequant")."""
+    if p.get(name + "_fmt", "q4k") == "q6k":
+        return _q6k.unpack_q6k(p[name], rows, cols)
+    return _q4k.unpack_q4k(p[name], rows, cols)
+
+
 def project_in(p, x32):
     """Fused input projection P = x W_in^T split into bf16 q|k|v|z and fp32 beta|alpha.
 
@@ -175,7 +185,7 @@ def project_in(p, x32):
     rescale (sparkinfer PR #464, Summary).  fp32 layers: plain product."""
     sz = layer_sizes(p)
     if p["wtype"] == "q4k":
-        wf = _q4k.unpack_q4k(p["w_in"], sz["r_in"], p["hidden"])
+        wf = unpack_weights(p, "w_in", sz["r_in"], p["hidden"])
         qw, sw = _quant.quant_rows_i8(wf)
         qx, sx = _quant.quant_rows_i8(x32)
         P = _quant.gemm_q8(qx, sx, qw, sw)
@@ -189,7 +199,7 @@ def project_out(p, o_hat):
     """Output projection y = o_hat W_out^T; Q4_K layers quantise o_hat (fp32) per token row."""
     sz = layer_sizes(p)
     if p["wtype"] == "q4k":
-        wf = _q4k.unpack_q4k(p["w_out"], p["hidden"], sz["c_v"])
+        wf = unpack_weights(p, "w_out", p["hidden"], sz["c_v"])
         qw, sw = _quant.quant_rows_i8(wf)
         qo, so = _quant.quant_rows_i8(np.asarray(o_hat, f64).astype(np.float32))
         return _quant.bf16_round(_quant.gemm_q8(qo, so, qw, sw))

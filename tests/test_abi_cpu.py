@@ -50,6 +50,21 @@ def test_q4k_pack_matches_oracle_on_layer_weights(L):
     assert np.array_equal(_pack(L, w), q4k.pack_q4k(w))
 
 
+@pytest.mark.parametrize("seed", [0, 1])
+def test_q6k_pack_matches_oracle_bytes(L, seed):
+    from oracle import q6k
+    rng = np.random.default_rng(seed + 100)
+    w = rng.normal(0, 0.02, size=(21, 768)).astype(np.float32)
+    w[2] = 0.0
+    w[3] = -np.abs(w[3])
+    w[4, :16] = 3.0                 # constant sub-block
+    w[5, :256] = 1e-7 * w[5, :256]  # fp16 subnormal super-scale
+    out = np.zeros((21, 3 * 210), np.uint8)
+    L.q6k_pack(gl.ptr(w), 21, 768, gl.ptr(out))
+    assert np.array_equal(out, q6k.pack_q6k(w))
+    assert L.q6k_pack(gl.ptr(w), 21, 700, gl.ptr(out), check=False) == gl.GDN_EINVAL
+
+
 def test_q4k_pack_rejects_bad_shapes(L):
     w = np.zeros((2, 300), np.float32)
     out = np.zeros(1000, np.uint8)

@@ -330,3 +330,23 @@ def test_prefill_host_rejects_pageable_memory():
     assert r == gl.GDN_EINVAL and "page-locked" in dl.lib.last_error()
     r = dl.prefill_host(yh, None, state, conv, yh, ws[: dl.host_workspace_bytes(1) - 256], check=False)
     assert r == gl.GDN_ENOMEM
+
+
+@pytest.mark.parametrize("q6k", [("w_out",), ("w_in", "w_out"), ("w_in",)])
+def test_prefill_with_q6k_matrices(q6k):
+    """Q4_K_M files hold some matrices in Q6_K: the layer decodes each from its
+    own format and matches the oracle doing the same."""
+    spec = SMALL
+    layer = synth.make_layer(spec)
+    tok = synth.make_tokens(spec, 200, seed=len(q6k) + 50)
+    dl = DeviceLayer(spec, layer, q6k=q6k)
+    y, state, conv = _run(dl, spec, tok)
+    p = oracle_params(spec, layer)
+    from oracle import q6k as O6
+    for name in q6k:
+        p[name] = O6.pack_q6k(layer[name])
+        p[name + "_fmt"] = "q6k"
+        assert np.array_equal(dl.host_blocks[name], p[name])
+    ref = OL.layer_forward(p, tok["x"], gate_log_a=tok["log_a"], gate_b=tok["b"])
+    assert rel_l2(_y_host(spec, y), ref["y"]) <= 1e-2
+    assert rel_l2(state.cpu().numpy(), ref["state"]) <= 1e-2

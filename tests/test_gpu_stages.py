@@ -23,7 +23,7 @@ import torch
 from hybrid_gated_deltanet_q4k_gb300 import lib as gl
 from hybrid_gated_deltanet_q4k_gb300 import synth
 from oracle import layer as OL
-from oracle import q4k, quant
+from oracle import q4k, q6k, quant
 
 from gpu_util import DEV, bf16_dev, bf16_host_f32, f16_codes, f16_dev, f16_round, f32_dev, rel_l2, stream, sync
 
@@ -61,6 +61,59 @@ def test_q4k_deq_bit_exact(L, rows, cols):
     assert np.array_equal(s.cpu().numpy().view(np.uint32), ref_s.view(np.uint32))
     assert np.array_equal(f16_codes(codes), ref_q.astype(np.int64))
     assert np.array_equal(s2.cpu().numpy().view(np.uint32), ref_s.view(np.uint32))
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 256), (7, 512), (1024, 2048), (4096, 4096), (3, 16384), (12352, 256)])
+def test_q6k_deq_bit_exact(L, rows, cols):
+    """Q6_K rows (the fused dequant's second format) decode and quantise to
+    the oracle's int8 codes and row scales byte for byte."""
+    rng = np.random.default_rng(rows * 5 + cols)
+    w = rng.normal(0, 0.02, size=(rows, cols)).astype(np.float32)
+    if rows > 4:
+        w[1] = 0.0
+        w[2] = -0.37
+        w[3, ::5] *= 60.0
+    blocks = q6k.pack_q6k(w)
+    ref_q, ref_s = quant.quant_rows_i8(q6k.unpack_q6k(blocks, rows, cols))
+    b = torch.from_numpy(blocks).to(DEV)
+    q = torch.empty(rows, cols, dtype=torch.int8, device=DEV)
+    s = torch.empty(rows, dtype=torch.float32, device=DEV)
+    L.q6k_deq_i8(gl.ptr(b), rows, cols, gl.ptr(q), gl.ptr(s), stream())
+    codes = torch.empty(rows, cols, dtype=torch.float16, device=DEV)
+    s2 = torch.empty(rows, dtype=torch.float32, device=DEV)
+    L.gdn_q6k_deq_codes(gl.ptr(b), rows, cols, gl.ptr(codes), gl.ptr(s2), stream())
+    sync(L)
+    assert np.array_equal(q.cpu().numpy(), ref_q)
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), ref_s.view(np.uint32))
+    assert np.array_equal(f16_codes(codes), ref_q.astype(np.int64))
+    assert np.array_equal(s2.cpu().numpy().view(np.uint32), ref_s.view(np.uint32))
+
+
+def test_q6k_deq_extreme_codes(L):
+    """Blocks with every code at -32 or 31 and scales at -128 / 127 (the ends
+    of both fields) and a row holding one nonzero weight."""
+    rng = np.random.default_rng(2)
+    rows, cols = 6, 1024
+    raw = rng.integers(0, 256, size=(rows, cols // 256, 210), dtype=np.uint8)
+    raw[:, :, 208:210] = np.array([2.0 ** -9], np.float16).view(np.uint8)   # finite d everywhere
+    raw[0, :, :192] = 0                                                     # codes 0: q = -32
+    raw[0, :, 192:208] = np.uint8(0x80)                                     # scales -128
+    raw[1, :, :192] = 0xFF                                                  # codes 63: q = 31
+    raw[1, :, 192:208] = 127
+    raw[2, :, 128:192] = 0xAA                                               # q = 0 except one weight
+    raw[2, :, :128] = 0
+    raw[2, 1, 5] = 3                                                        # weight 5 of superblock 1: q = 3
+    raw[2, 1, 192] = 5                                                      # its scale
+    blocks = raw.reshape(rows, -1)
+    ref_q, ref_s = quant.quant_rows_i8(q6k.unpack_q6k(blocks, rows, cols))
+    b = torch.from_numpy(blocks.copy()).to(DEV)
+    q = torch.empty(rows, cols, dtype=torch.int8, device=DEV)
+    s = torch.empty(rows, dtype=torch.float32, device=DEV)
+    L.q6k_deq_i8(gl.ptr(b), rows, cols, gl.ptr(q), gl.ptr(s), stream())
+    sync(L)
+    assert np.array_equal(q.cpu().numpy(), ref_q)
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), ref_s.view(np.uint32))
+    assert np.count_nonzero(ref_q[2]) == 1
 
 
 # ------------------------------------------------------------------ step 1b
