@@ -557,8 +557,59 @@ def run_extend(args, spec):
                                  "extensions": ext, "tokens": T, "call": "gdn_prefill_batch"}}), flush=True)
 
 
+def run_decode(args, spec):
+    """Decode step of the 32k layer (h4096): one token for each of B sequences
+    with saved states, every step through gdn_decode; inputs resident, timed
+    with CUDA events.  HBM roofline: the Q4_K bytes of both weight matrices plus
+    the states read and written, per step.  A secondary measurement."""
+    import torch
+
+    from hybrid_gated_deltanet_q4k_gb300 import lib as gl
+    from hybrid_gated_deltanet_q4k_gb300 import synth
+    from hybrid_gated_deltanet_q4k_gb300.api import DeviceLayer
+
+    L = gl.load(build=True)
+    layer = synth.make_layer(spec)
+    dl = DeviceLayer(spec, layer)
+    stream = torch.cuda.current_stream()
+    pk = peaks()
+    rows = []
+    for B in (1, 8, 32):
+        tok = synth.make_tokens(spec, B, seed=90 + B)
+        x = torch.from_numpy(tok["x_bits"].view(np.int16)).cuda().view(torch.bfloat16)
+        la, bb = torch.from_numpy(tok["log_a"]).cuda(), torch.from_numpy(tok["b"]).cuda()
+        st, cv = dl.new_batch_state(B)
+        st.normal_(0, 0.05)
+        y = torch.empty(B, spec.hidden, dtype=torch.bfloat16, device="cuda")
+        ws = dl.new_decode_workspace(B)
+        fn = lambda: dl.decode(x, st, cv, y, ws, gate_log_a=la, gate_b=bb)  # noqa: E731
+        for _ in range(max(args.warmup, 3)):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        assert L.gdn_sync_status(stream.cuda_stream, check=False) == 0, L.last_error()
+        us = e0.elapsed_time(e1) / args.steps * 1e3
+        wbytes = dl.dev["w_in"].numel() + dl.dev["w_out"].numel()
+        sbytes = 2 * st.numel() * 4
+        gbs = (wbytes + sbytes) / (us * 1e-6) / 1e9
+        rows.append({"n_seqs": B, "us_per_step": us, "tokens_per_s": B / (us * 1e-6), "hbm_bytes": wbytes + sbytes,
+                     "achieved_gbs": gbs, "frac": gbs / pk["hbm"]})
+    print(json.dumps({"metric": "GDN-layer decode step (1 GB300)", "workload": spec.workload, "steps": args.steps,
+                      "peak_gbs": pk["hbm"], "peak_source": pk["src"], "rows": rows, "dtype": "int8",
+                      "data": "synthetic", "call": "gdn_decode"}), flush=True)
+
+
 def main():
     args = parse()
+    if args.config == "decode" and args.impl == "ours":
+        from hybrid_gated_deltanet_q4k_gb300 import synth
+        run_decode(args, synth.SPECS["h4096"])
+        return
     if args.config == "extend" and args.impl == "ours" and not args.stage:
         from hybrid_gated_deltanet_q4k_gb300 import synth
         run_extend(args, synth.SPECS["extend"])

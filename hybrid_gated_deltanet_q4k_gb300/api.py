@@ -120,3 +120,19 @@ class DeviceLayer:
         return self.lib.gdn_prefill_batch(ctypes.byref(s), gl.ptr(x), gl.ptr(cu), len(cu) - 1, gl.ptr(state_in),
                                           gl.ptr(state_out), gl.ptr(conv_state), gl.ptr(y), gl.ptr(workspace),
                                           workspace.numel(), gl.stream_handle(stream), check=check)
+
+    def decode_workspace_bytes(self, n_seqs: int) -> int:
+        s = self.struct()
+        return self.lib.gdn_decode_workspace_size(ctypes.byref(s), int(n_seqs))
+
+    def new_decode_workspace(self, n_seqs: int) -> torch.Tensor:
+        return torch.empty(self.decode_workspace_bytes(n_seqs), dtype=torch.uint8, device=self.device)
+
+    def decode(self, x: torch.Tensor, state, conv_state, y, workspace, gate_log_a=None, gate_b=None, stream=None,
+               check=True) -> int:
+        """Enqueue gdn_decode: one token per sequence (x [n_seqs][H]), states [n_seqs][Hv][dv][dk] and
+        conv tails [n_seqs][C_conv][3] updated in place."""
+        s = self.struct(gate_log_a, gate_b)
+        return self.lib.gdn_decode(ctypes.byref(s), gl.ptr(x), x.shape[0], gl.ptr(state), gl.ptr(conv_state),
+                                   gl.ptr(y), gl.ptr(workspace), workspace.numel(), gl.stream_handle(stream),
+                                   check=check)

@@ -16,6 +16,7 @@
 #include <cstdio>
 #include <mutex>
 #include <string>
+#include <vector>
 
 namespace gdn {
 cudaError_t launch_q4k_deq_i8(const void*, int64_t, int64_t, int8_t*, float*, cudaStream_t);
@@ -39,6 +40,11 @@ cudaError_t launch_delta(const gdn_layer&, const uint16_t*, const float*, const 
 size_t delta_scratch_bytes(int hv, int hk, int d, int64_t n);
 cudaError_t launch_gated_norm(const gdn_layer&, const uint16_t*, const uint16_t*, int64_t, int64_t, uint16_t*, float*,
                               float*, cudaStream_t);
+cudaError_t launch_gemv_codes(const void*, bool, int64_t, int64_t, const uint16_t*, const float*, int64_t, uint16_t*,
+                              int64_t, int64_t, float*, int64_t, cudaStream_t);
+cudaError_t launch_decode_rule(const gdn_layer&, const uint16_t*, const float*, const float*, int64_t, float*, uint16_t*,
+                               cudaStream_t);
+int read_and_clear_decode_error();
 int read_and_clear_gemm_error();
 int read_and_clear_delta_error();
 int read_and_clear_conv_error();
@@ -269,6 +275,45 @@ size_t host_stage_bytes(const gdn_layer* L, const Sizes& s, int64_t B) {
     size_t t = 4 * up256(B * s.H * esz);
     if (L->gate_log_a) t += 4 * up256(B * s.hv * 4);
     return t;
+}
+
+// Workspace of one decode step of B tokens (one per sequence).
+struct DecodeWs {
+    uint16_t* xc; float* sx;          // x codes [B][H], scales [B]         (Q4_K)
+    uint16_t* qkvz; float* ba;        // projection [B][n_bf16] bf16, [B][2 hv] fp32
+    uint16_t* qkv;                    // conv output [B][c_conv] fp16
+    float* log_a; float* b;           // gates [B][hv]
+    uint16_t* o;                      // recurrence output [B][c_v] fp16
+    uint16_t* oc; float* so;          // gated-norm codes [B][c_v], scales [B] (Q4_K)
+    float* ohat;                      // gated-norm output [B][c_v]          (F32)
+    size_t total;
+};
+
+DecodeWs carve_decode(const gdn_layer* L, const Sizes& s, int64_t B, void* base) {
+    DecodeWs w{};
+    uint8_t* p = static_cast<uint8_t*>(base);
+    size_t off = 0;
+    auto take = [&](size_t bytes) -> void* {
+        void* r = p ? static_cast<void*>(p + off) : nullptr;
+        off += up256(bytes);
+        return r;
+    };
+    if (L->wtype == GDN_W_Q4K) {
+        w.xc = static_cast<uint16_t*>(take(B * s.H * 2));
+        w.sx = static_cast<float*>(take(B * 4));
+        w.oc = static_cast<uint16_t*>(take(B * s.c_v * 2));
+        w.so = static_cast<float*>(take(B * 4));
+    } else {
+        w.ohat = static_cast<float*>(take(B * s.c_v * 4));
+    }
+    w.qkvz = static_cast<uint16_t*>(take(B * s.n_bf16 * 2));
+    w.ba = static_cast<float*>(take(B * 2 * s.hv * 4));
+    w.qkv = static_cast<uint16_t*>(take(B * s.c_conv * 2));
+    w.log_a = static_cast<float*>(take(B * s.hv * 4));
+    w.b = static_cast<float*>(take(B * s.hv * 4));
+    w.o = static_cast<uint16_t*>(take(B * s.c_v * 2));
+    w.total = off;
+    return w;
 }
 
 // GDN_OK if p is page-locked host memory (cudaHostAlloc or cudaHostRegister).
@@ -687,6 +732,83 @@ int gdn_prefill_batch(const gdn_layer* layer, const void* x, const int64_t* cu_s
     return GDN_OK;
 }
 
+size_t gdn_decode_workspace_size(const gdn_layer* layer, int n_seqs) {
+    Sizes s;
+    if (check_layer(layer, &s) || n_seqs < 1 || n_seqs > GDN_MAX_SEQS) return 0;
+    return carve_decode(layer, s, n_seqs, nullptr).total;
+}
+
+int gdn_decode(const gdn_layer* layer, const void* x, int n_seqs, float* state, float* conv_state, void* y,
+               void* workspace, size_t ws_bytes, void* stream) {
+    Sizes s;
+    int r = check_layer(layer, &s);
+    if (r) return r;
+    if (n_seqs < 1 || n_seqs > GDN_MAX_SEQS)
+        return fail(GDN_EINVAL, "gdn_decode: 1 <= n_seqs <= %d required (got %d)", GDN_MAX_SEQS, n_seqs);
+    if (!x || !state || !conv_state || !y || !workspace) return fail(GDN_EINVAL, "gdn_decode: NULL pointer");
+    if (!aligned(x, 16) || !aligned(y, 16) || !aligned(state, 16) || !aligned(workspace, 256))
+        return fail(GDN_EINVAL, "gdn_decode: x, y, state 16-byte and workspace 256-byte alignment required");
+    const DecodeWs w = carve_decode(layer, s, n_seqs, workspace);
+    if (ws_bytes < w.total) return fail(GDN_ENOMEM, "gdn_decode: workspace %zu B < %zu B", ws_bytes, w.total);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const bool q4k = layer->wtype == GDN_W_Q4K;
+    const int64_t B = n_seqs;
+    // steps 1b, 1c: int8 codes of the tokens, then the weight rows decoded in
+    // registers against them
+    if (q4k) {
+        GDN_LAUNCH(launch_quant_rows(static_cast<const uint16_t*>(x), B, s.H, w.xc, w.sx, st), "decode: quantise x");
+        GDN_LAUNCH(launch_gemv_codes(layer->w_in, layer->q6k_mask & 1, s.r_in, s.H, w.xc, w.sx, B, w.qkvz, s.n_bf16,
+                                     s.n_bf16, w.ba, 2 * s.hv, st),
+                   "decode: input projection");
+    } else {
+        GDN_LAUNCH(launch_gemm_f32(static_cast<const float*>(x), static_cast<const float*>(layer->w_in), B, s.r_in, s.H,
+                                   w.qkvz, s.n_bf16, s.n_bf16, w.ba, 2 * s.hv, st),
+                   "decode: input projection");
+    }
+    // step 2: every token is a one-token sequence with its own conv tail
+    std::vector<int64_t> cu(static_cast<size_t>(B) + 1);
+    for (int64_t i = 0; i <= B; ++i) cu[static_cast<size_t>(i)] = i;
+    GDN_LAUNCH(launch_conv(*layer, w.qkvz, s.n_bf16, B, conv_state, w.ba, 2 * s.hv, w.qkv, w.log_a, w.b, st, cu.data(),
+                           n_seqs),
+               "decode: conv");
+    GDN_LAUNCH(launch_conv_state(*layer, w.qkvz, s.n_bf16, B, conv_state, st, cu.data(), n_seqs), "decode: conv state");
+    // step 3: one token of the recurrence per sequence, in fp32
+    const float* la = layer->gate_log_a ? layer->gate_log_a : w.log_a;
+    const float* bb = layer->gate_b ? layer->gate_b : w.b;
+    GDN_LAUNCH(launch_decode_rule(*layer, w.qkv, la, bb, B, state, w.o, st), "decode: recurrence");
+    // steps 4, 5
+    GDN_LAUNCH(launch_gated_norm(*layer, w.o, w.qkvz + s.c_conv, s.n_bf16, B, w.oc, w.so, w.ohat, st),
+               "decode: gated norm");
+    if (q4k) {
+        GDN_LAUNCH(launch_gemv_codes(layer->w_out, layer->q6k_mask & 2, s.H, s.c_v, w.oc, w.so, B,
+                                     static_cast<uint16_t*>(y), s.H, s.H, nullptr, 0, st),
+                   "decode: output projection");
+    } else {
+        GDN_LAUNCH(launch_gemm_f32(w.ohat, static_cast<const float*>(layer->w_out), B, s.H, s.c_v, nullptr, 0, 0,
+                                   static_cast<float*>(y), s.H, st),
+                   "decode: output projection");
+    }
+    return GDN_OK;
+}
+
+int gdn_gemv_codes(const void* blocks, int q6k, int64_t rows, int64_t cols, const uint16_t* xc, const float* sx,
+                   int64_t n, uint16_t* out_bf16, int64_t ld_bf16, int64_t n_bf16, float* out_f32, int64_t ld_f32,
+                   void* stream) {
+    if (!blocks || !xc || !sx) return fail(GDN_EINVAL, "gdn_gemv_codes: NULL operand");
+    if (q6k != 0 && q6k != 1) return fail(GDN_EINVAL, "gdn_gemv_codes: q6k must be 0 or 1");
+    if (rows < 1 || rows > 0x7fffffff || cols < 256 || cols > 16384 || cols % 256 || n < 1 || n > GDN_MAX_SEQS)
+        return fail(GDN_EINVAL, "gdn_gemv_codes: rows >= 1, cols a multiple of 256 in [256, 16384], 1 <= n <= %d",
+                    GDN_MAX_SEQS);
+    if (n_bf16 < 0) return fail(GDN_EINVAL, "gdn_gemv_codes: n_bf16 < 0");
+    if (n_bf16 > 0 && (!out_bf16 || ld_bf16 < (n_bf16 < rows ? n_bf16 : rows))) return fail(GDN_EINVAL, "gdn_gemv_codes: bf16 output");
+    if (n_bf16 < rows && (!out_f32 || ld_f32 < rows - n_bf16)) return fail(GDN_EINVAL, "gdn_gemv_codes: fp32 output");
+    if (!aligned(blocks, 16) || !aligned(xc, 16)) return fail(GDN_EINVAL, "gdn_gemv_codes: 16-byte alignment required");
+    GDN_LAUNCH(launch_gemv_codes(blocks, q6k == 1, rows, cols, xc, sx, n, out_bf16, ld_bf16, n_bf16, out_f32, ld_f32,
+                                 static_cast<cudaStream_t>(stream)),
+               "gdn_gemv_codes");
+    return GDN_OK;
+}
+
 int gdn_sync_status(void* stream) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "gdn_sync_status");
@@ -694,10 +816,12 @@ int gdn_sync_status(void* stream) {
     if (e != cudaSuccess) return cuda_fail(e, "gdn_sync_status");
     if (read_and_clear_gemm_error()) return fail(GDN_ETIMEOUT, "a bounded wait in the projection kernel ran out");
     const int dcode = read_and_clear_delta_error();
+    const int rcode = read_and_clear_decode_error();
     const int ccode = read_and_clear_conv_error();
     if (read_and_clear_norm_error() == ERR_WAIT_TIMEOUT)
         return fail(GDN_ETIMEOUT, "a bounded wait in the gated-norm kernel ran out");
     if (dcode == ERR_WAIT_TIMEOUT) return fail(GDN_ETIMEOUT, "a bounded wait in the delta-rule kernel ran out");
+    if (rcode == ERR_RANGE) return fail(GDN_ERANGE, "a decode-step output o exceeded the fp16 range (|x| > 65504)");
     if (ccode == ERR_RANGE || dcode == ERR_RANGE)
         return fail(GDN_ERANGE, "a %s value exceeded the fp16 operand range (|x| > 65504)",
                     ccode == ERR_RANGE ? "q, k or v" : "delta-rule intermediate (T, A T, S, R or Delta)");

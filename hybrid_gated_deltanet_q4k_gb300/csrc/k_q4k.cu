@@ -19,6 +19,7 @@
 // quantisation: HBM traffic is the 144 B/256 weights read plus the codes
 // written, nothing else.
 #include "common.cuh"
+#include "qk_decode.cuh"
 
 namespace gdn {
 
@@ -26,23 +27,6 @@ constexpr int DEQ_THREADS = 256;
 constexpr int DEQ_MAX_COLS = 16384;                              // 64 superblocks
 constexpr int DEQ_MAX_GROUPS = DEQ_MAX_COLS / 16 / DEQ_THREADS;  // 16-weight groups per thread
 
-// Byte i (0..11) of the 12 scale bytes, held in three little-endian words.
-__device__ __forceinline__ int scale_byte(uint32_t y, uint32_t z, uint32_t w, int i) {
-    const uint32_t word = i < 4 ? y : (i < 8 ? z : w);
-    return static_cast<int>((word >> (8 * (i & 3))) & 0xffu);
-}
-
-// 6-bit scale and min of sub-block j.
-__device__ __forceinline__ void q4k_scale_min(uint32_t y, uint32_t z, uint32_t w, int j, int& sc, int& m) {
-    if (j < 4) {
-        sc = scale_byte(y, z, w, j) & 63;
-        m = scale_byte(y, z, w, j + 4) & 63;
-    } else {
-        const int hi = scale_byte(y, z, w, j + 4);
-        sc = (hi & 15) | ((scale_byte(y, z, w, j - 4) >> 6) << 4);
-        m = (hi >> 4) | ((scale_byte(y, z, w, j) >> 6) << 4);
-    }
-}
 
 template <typename OutT>
 __device__ __forceinline__ void store8(OutT* dst, const int* q);
@@ -148,17 +132,6 @@ struct DeqJob {
     uint16_t* codes;
     float* scale;
 };
-
-// d*sc and dmin*m of sub-block `sub` of a superblock header; both products are
-// exact in fp32 (11-bit x 6-bit significands).
-__device__ __forceinline__ void q4k_sub_affine(const uint4& hdr, int sub, float& ds, float& dm) {
-    const float d = __half2float(__ushort_as_half(static_cast<uint16_t>(hdr.x & 0xffffu)));
-    const float dmin = __half2float(__ushort_as_half(static_cast<uint16_t>(hdr.x >> 16)));
-    int sc, m;
-    q4k_scale_min(hdr.y, hdr.z, hdr.w, sub, sc, m);
-    ds = __fmul_rn(d, static_cast<float>(sc));
-    dm = __fmul_rn(dmin, static_cast<float>(m));
-}
 
 __global__ void __launch_bounds__(DEQ_WARP_THREADS, 4)
 q4k_deq_rows_warp_kernel(DeqJob j0, DeqJob j1) {

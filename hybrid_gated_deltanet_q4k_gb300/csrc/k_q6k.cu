@@ -22,6 +22,7 @@
 // superblock); pass 2 decodes, quantises with the row scale and writes the 8
 // codes as one vector (int8: 8 bytes, fp16 carriers: 16 bytes).
 #include "common.cuh"
+#include "qk_decode.cuh"
 
 namespace gdn {
 
@@ -36,28 +37,6 @@ struct Q6Job {
     OutT* codes;
     float* scale;
 };
-
-// The 8 six-bit codes of lane L's weights in superblock blk, as signed q = c - 32,
-// and the lane's d * scale (exact).
-__device__ __forceinline__ void q6k_lane(const uint8_t* blk, int lane, int (&q)[8], float& ds) {
-    const int v0 = 8 * lane, h = v0 >> 7, g = (v0 & 127) >> 5, l0 = v0 & 31;
-    const uint16_t* ql = reinterpret_cast<const uint16_t*>(blk + 64 * h + 32 * (g & 1) + l0);
-    const uint16_t* qh = reinterpret_cast<const uint16_t*>(blk + 128 + 32 * h + l0);
-    const int nsh = 4 * (g >> 1), hsh = 2 * g;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const uint32_t lw = __ldg(ql + k), hw = __ldg(qh + k);
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const uint32_t lo = (lw >> (8 * e + nsh)) & 15u;
-            const uint32_t hi = (hw >> (8 * e + hsh)) & 3u;
-            q[2 * k + e] = static_cast<int>(lo | (hi << 4)) - 32;
-        }
-    }
-    const int8_t sc = static_cast<int8_t>(__ldg(blk + 192 + (v0 >> 4)));
-    const float d = __half2float(__ushort_as_half(__ldg(reinterpret_cast<const uint16_t*>(blk + 208))));
-    ds = __fmul_rn(d, static_cast<float>(sc));
-}
 
 template <typename OutT>
 __device__ __forceinline__ void store_codes8(OutT* dst, const float (&c)[8]);
@@ -86,35 +65,16 @@ __global__ void __launch_bounds__(Q6_THREADS, 4) q6k_deq_rows_warp_kernel(Q6Job<
 
     float amax = 0.0f;
 #pragma unroll 4
-    for (int i = 0; i < nsb; ++i) {
-        int q[8];
-        float ds;
-        q6k_lane(rb + i * Q6_BLOCK, lane, q, ds);
-        int m = 0;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) m = max(m, abs(q[e]));
-        amax = fmaxf(amax, fabsf(ds * static_cast<float>(m)));   // exact: the largest |w| of the 8
-    }
+    for (int i = 0; i < nsb; ++i) amax = fmaxf(amax, Q6KLane::amax(rb + i * Q6_BLOCK, lane));
     amax = warp_max(amax);
     const QScale qsc = make_qscale(amax);
     if (lane == 0) j.scale[row] = qsc.s;
     OutT* out = j.codes + row * static_cast<int64_t>(j.cols) + lane * 8;
 #pragma unroll 4
     for (int i = 0; i < nsb; ++i) {
-        int q[8];
-        float ds;
-        q6k_lane(rb + i * Q6_BLOCK, lane, q, ds);
         float w[8], c[8];
-        bool redo = !qsc.fast;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            w[e] = ds * static_cast<float>(q[e]);
-            c[e] = qcode_fast(w[e], qsc, redo);
-        }
-        if (redo) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) c[e] = qcode_exact(w[e], qsc.s);
-        }
+        Q6KLane::decode(rb + i * Q6_BLOCK, lane, w);
+        quantise8(w, qsc, c);
         store_codes8<OutT>(out + i * 256, c);
     }
 }

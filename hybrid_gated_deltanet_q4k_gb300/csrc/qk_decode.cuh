@@ -1,0 +1,141 @@
+// Decoding of GGUF Q4_K and Q6_K superblocks, shared by the kernels that
+// read them (step 1a to int8 codes, and the fused decode-and-dot of the
+// decode step), so that every path yields the same codes bit for bit.
+//
+// Q4_K (144 B): fp16 d | fp16 dmin | 12 bytes of 6-bit scales/mins | 128 bytes
+// of 4-bit codes; sub-block j (32 weights) decodes as d*sc_j*q - dmin*m_j.
+// Lane l of a warp takes the 8 weights 8l .. 8l+7 of a superblock: sub-block
+// l/4, the low (even sub-block) or high (odd) nibbles of code bytes
+// 32(l/8) + 8(l%4) .. +7.
+//
+// Q6_K (210 B): ql[128] | qh[64] | int8 scales[16] | fp16 d; weight v decodes
+// as d*scales[v/16]*(c - 32) with c's low 4 bits in nibble g/2 of
+// ql[64h + 32(g%2) + l] and its high 2 bits in bits 2g, 2g+1 of qh[32h + l]
+// (h = v/128, g = (v%128)/32, l = v%32).  Lane L takes the 8 weights 8L .. 8L+7:
+// they share h, g and one scale.
+#pragma once
+
+#include "common.cuh"
+
+namespace gdn {
+
+// Byte i (0..11) of the 12 Q4_K scale bytes, held in three little-endian words.
+__device__ __forceinline__ int scale_byte(uint32_t y, uint32_t z, uint32_t w, int i) {
+    const uint32_t word = i < 4 ? y : (i < 8 ? z : w);
+    return static_cast<int>((word >> (8 * (i & 3))) & 0xffu);
+}
+
+// 6-bit scale and min of Q4_K sub-block j.
+__device__ __forceinline__ void q4k_scale_min(uint32_t y, uint32_t z, uint32_t w, int j, int& sc, int& m) {
+    if (j < 4) {
+        sc = scale_byte(y, z, w, j) & 63;
+        m = scale_byte(y, z, w, j + 4) & 63;
+    } else {
+        const int hi = scale_byte(y, z, w, j + 4);
+        sc = (hi & 15) | ((scale_byte(y, z, w, j - 4) >> 6) << 4);
+        m = (hi >> 4) | ((scale_byte(y, z, w, j) >> 6) << 4);
+    }
+}
+
+// d*sc and dmin*m of Q4_K sub-block `sub` of a superblock header; both products
+// are exact in fp32 (11-bit x 6-bit significands).
+__device__ __forceinline__ void q4k_sub_affine(const uint4& hdr, int sub, float& ds, float& dm) {
+    const float d = __half2float(__ushort_as_half(static_cast<uint16_t>(hdr.x & 0xffffu)));
+    const float dmin = __half2float(__ushort_as_half(static_cast<uint16_t>(hdr.x >> 16)));
+    int sc, m;
+    q4k_scale_min(hdr.y, hdr.z, hdr.w, sub, sc, m);
+    ds = __fmul_rn(d, static_cast<float>(sc));
+    dm = __fmul_rn(dmin, static_cast<float>(m));
+}
+
+// Q4_K: lane's 8 weights of the superblock at blk (16-byte aligned), exact
+// single roundings of d*sc*q - dmin*m; amax_only: just their largest magnitude
+// (at the smallest or largest code: the decode is monotonic in q).
+struct Q4KLane {
+    static constexpr int BYTES = 144;
+    __device__ __forceinline__ static float amax(const uint8_t* blk, int lane) {
+        const int sub = lane >> 2, p = sub >> 1, l0 = (lane & 3) * 8, shift = (sub & 1) * 4;
+        const uint4 hdr = __ldg(reinterpret_cast<const uint4*>(blk));
+        const uint2 qs = __ldg(reinterpret_cast<const uint2*>(blk + 16 + 32 * p + l0));
+        float ds, dm;
+        q4k_sub_affine(hdr, sub, ds, dm);
+        const uint32_t n0 = (qs.x >> shift) & 0x0f0f0f0fu, n1 = (qs.y >> shift) & 0x0f0f0f0fu;
+        uint32_t mn = __vminu4(n0, n1), mx = __vmaxu4(n0, n1);
+        mn = __vminu4(mn, mn >> 16);
+        mx = __vmaxu4(mx, mx >> 16);
+        mn = __vminu4(mn, mn >> 8) & 0xffu;
+        mx = __vmaxu4(mx, mx >> 8) & 0xffu;
+        const float w0 = __fmaf_rn(ds, static_cast<float>(mn), -dm);
+        const float w1 = __fmaf_rn(ds, static_cast<float>(mx), -dm);
+        return fmaxf(fabsf(w0), fabsf(w1));
+    }
+    __device__ __forceinline__ static void decode(const uint8_t* blk, int lane, float (&w)[8]) {
+        const int sub = lane >> 2, p = sub >> 1, l0 = (lane & 3) * 8, shift = (sub & 1) * 4;
+        const uint4 hdr = __ldg(reinterpret_cast<const uint4*>(blk));
+        const uint2 qs = __ldg(reinterpret_cast<const uint2*>(blk + 16 + 32 * p + l0));
+        float ds, dm;
+        q4k_sub_affine(hdr, sub, ds, dm);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const uint32_t q = ((e < 4 ? qs.x : qs.y) >> (8 * (e & 3) + shift)) & 15u;
+            w[e] = __fmaf_rn(ds, static_cast<float>(q), -dm);
+        }
+    }
+};
+
+// Q6_K: the lane's 8 signed codes q = c - 32 and its d * scale (exact); the
+// superblock is only 2-byte aligned (210 = 2 * 105), so it is read in 16-bit words.
+__device__ __forceinline__ void q6k_lane(const uint8_t* blk, int lane, int (&q)[8], float& ds) {
+    const int v0 = 8 * lane, h = v0 >> 7, g = (v0 & 127) >> 5, l0 = v0 & 31;
+    const uint16_t* ql = reinterpret_cast<const uint16_t*>(blk + 64 * h + 32 * (g & 1) + l0);
+    const uint16_t* qh = reinterpret_cast<const uint16_t*>(blk + 128 + 32 * h + l0);
+    const int nsh = 4 * (g >> 1), hsh = 2 * g;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t lw = __ldg(ql + k), hw = __ldg(qh + k);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const uint32_t lo = (lw >> (8 * e + nsh)) & 15u;
+            const uint32_t hi = (hw >> (8 * e + hsh)) & 3u;
+            q[2 * k + e] = static_cast<int>(lo | (hi << 4)) - 32;
+        }
+    }
+    const int8_t sc = static_cast<int8_t>(__ldg(blk + 192 + (v0 >> 4)));
+    const float d = __half2float(__ushort_as_half(__ldg(reinterpret_cast<const uint16_t*>(blk + 208))));
+    ds = __fmul_rn(d, static_cast<float>(sc));
+}
+
+struct Q6KLane {
+    static constexpr int BYTES = 210;
+    __device__ __forceinline__ static float amax(const uint8_t* blk, int lane) {
+        int q[8];
+        float ds;
+        q6k_lane(blk, lane, q, ds);
+        int m = 0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) m = max(m, abs(q[e]));
+        return fabsf(ds * static_cast<float>(m));   // exact: the largest |w| of the 8
+    }
+    __device__ __forceinline__ static void decode(const uint8_t* blk, int lane, float (&w)[8]) {
+        int q[8];
+        float ds;
+        q6k_lane(blk, lane, q, ds);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) w[e] = ds * static_cast<float>(q[e]);
+    }
+};
+
+// The int8 codes of 8 decoded weights for the row's scale: the fast quantiser,
+// with the exact fallback where it may round differently (results equal
+// qcode_exact for every weight).
+__device__ __forceinline__ void quantise8(const float (&w)[8], const QScale& qsc, float (&c)[8]) {
+    bool redo = !qsc.fast;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) c[e] = qcode_fast(w[e], qsc, redo);
+    if (redo) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) c[e] = qcode_exact(w[e], qsc.s);
+    }
+}
+
+}  // namespace gdn

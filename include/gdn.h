@@ -65,7 +65,8 @@ extern "C" {
 #define GDN_W_F32 1 /* weights and activations fp32, no quantisation anywhere */
 
 #define GDN_CHUNK 64 /* tokens per chunk of the chunked delta rule */
-#define GDN_MAX_SEQS 256 /* sequences per gdn_prefill_batch call */
+#define GDN_MAX_SEQS 256 /* sequences per gdn_prefill_batch or gdn_decode call */
+#define GDN_DECODE_GEMV_TOKENS 8 /* tokens per launch of the decode step's fused weight-decode GEMV */
 
 /*
  * One GDN layer.  Sizes: Hk = n_qk_heads, Hv = n_v_heads (a multiple of Hk,
@@ -209,6 +210,46 @@ size_t gdn_batch_workspace_size(const gdn_layer *layer, int64_t n_tokens, int n_
 int gdn_prefill_batch(const gdn_layer *layer, const void *x, const int64_t *cu_seqlens, int n_seqs,
                       const float *state_in, float *state_out, float *conv_state, void *y, void *workspace,
                       size_t ws_bytes, void *stream);
+
+/*
+ * gdn_decode -- the decode step: one new token for each of n_seqs sequences,
+ * each with its own state and conv tail, updated in place ("Qwen3.5 speed:
+ * prefill and decode parity with llama.cpp" #5305, the decode side of the
+ * same layer; the state layout is gdn_prefill's, so a sequence prefills and
+ * then decodes on the same buffers).
+ *   x          bf16 (Q4_K) or fp32 (F32) [n_seqs][hidden], token s of sequence s
+ *   state      fp32 [n_seqs][Hv][dv][dk], in/out
+ *   conv_state fp32 [n_seqs][C_conv][3], in/out
+ *   y          as x
+ *   layer->gate_log_a, gate_b   when given: device [n_seqs][Hv]
+ *   workspace  device, 256-byte aligned, ws_bytes >= gdn_decode_workspace_size(
+ *              layer, n_seqs)
+ * The projections decode the Q4_K / Q6_K weight rows in registers and take
+ * exact integer dot products with the tokens' int8 codes (no int8 weight copy
+ * in memory): bit for bit the projections gdn_prefill computes for the same
+ * tokens.  The conv is gdn_prefill's.  The recurrence takes the token in fp32
+ * (S <- a S (I - b k k^T) + b v k^T, o = S q), not through the chunked
+ * fp16-operand form, so o and the state agree with a prefill of the same
+ * token within the recurrence tolerance, not bit for bit.
+ * 1 <= n_seqs <= GDN_MAX_SEQS.  An out-of-range o is reported as GDN_ERANGE by
+ * gdn_sync_status.
+ */
+size_t gdn_decode_workspace_size(const gdn_layer *layer, int n_seqs);
+int gdn_decode(const gdn_layer *layer, const void *x, int n_seqs, float *state, float *conv_state, void *y,
+               void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * gdn_gemv_codes -- the decode step's projection as its own call: out[t][r] =
+ * ((float)sum_k codes(W)[r][k] * xc[t][k] * sx[t]) * s_w[r], W given as Q4_K
+ * (q6k = 0) or Q6_K (q6k = 1) blocks [rows][cols/256], its codes and row scale
+ * s_w those of gdn_q4k_deq_codes / gdn_q6k_deq_codes; xc: int8 codes of n
+ * tokens as fp16 patterns [n][cols] (16-byte aligned), sx [n].  Rows r <
+ * n_bf16 go to out_bf16[t*ld_bf16 + r] (bf16), the others to out_f32[t*ld_f32 +
+ * r - n_bf16].  256 <= cols <= 16384, cols % 256 == 0, 1 <= n <= GDN_MAX_SEQS.
+ */
+int gdn_gemv_codes(const void *blocks, int q6k, int64_t rows, int64_t cols, const uint16_t *xc, const float *sx,
+                   int64_t n, uint16_t *out_bf16, int64_t ld_bf16, int64_t n_bf16, float *out_f32, int64_t ld_f32,
+                   void *stream);
 
 /*
  * gdn_prefill_host -- gdn_prefill fed from, and writing to, host memory: the
