@@ -178,30 +178,39 @@ def unpack_weights(p, name, rows, cols):
     return _q4k.unpack_q4k(p[name], rows, cols)
 
 
-def project_in(p, x32):
+def project_in(p, x32, decode=False):
     """Fused input projection P = x W_in^T split into bf16 q|k|v|z and fp32 beta|alpha.
 
     Q4_K layers: both operands int8 row-quantised, exact integer product, fp32
-    rescale (sparkinfer PR #464, Summary).  fp32 layers: plain product."""
+    rescale (sparkinfer PR #464, Summary).  decode: the decode step's product
+    of the int8 activation rows with the exactly decoded weights
+    (quant.matvec_exact_weights), rounded once to fp32.  fp32 layers: plain
+    product."""
     sz = layer_sizes(p)
     if p["wtype"] == "q4k":
         wf = unpack_weights(p, "w_in", sz["r_in"], p["hidden"])
-        qw, sw = _quant.quant_rows_i8(wf)
         qx, sx = _quant.quant_rows_i8(x32)
-        P = _quant.gemm_q8(qx, sx, qw, sw)
+        if decode:
+            P = _quant.matvec_exact_weights(qx, sx, wf).astype(np.float32)
+        else:
+            qw, sw = _quant.quant_rows_i8(wf)
+            P = _quant.gemm_q8(qx, sx, qw, sw)
     else:
         P = (np.asarray(x32, f64) @ np.asarray(p["w_in"], f64).T).astype(np.float32)
     nb = sz["n_bf16"]
     return _quant.bf16_round(P[:, :nb]), P[:, nb:].copy()
 
 
-def project_out(p, o_hat):
-    """Output projection y = o_hat W_out^T; Q4_K layers quantise o_hat (fp32) per token row."""
+def project_out(p, o_hat, decode=False):
+    """Output projection y = o_hat W_out^T; Q4_K layers quantise o_hat (fp32) per
+    token row (decode: against the exactly decoded weights, as project_in)."""
     sz = layer_sizes(p)
     if p["wtype"] == "q4k":
         wf = unpack_weights(p, "w_out", p["hidden"], sz["c_v"])
-        qw, sw = _quant.quant_rows_i8(wf)
         qo, so = _quant.quant_rows_i8(np.asarray(o_hat, f64).astype(np.float32))
+        if decode:
+            return _quant.bf16_round(_quant.matvec_exact_weights(qo, so, wf).astype(np.float32))
+        qw, sw = _quant.quant_rows_i8(wf)
         return _quant.bf16_round(_quant.gemm_q8(qo, so, qw, sw))
     return (np.asarray(o_hat, f64) @ np.asarray(p["w_out"], f64).T).astype(np.float32)
 
@@ -219,7 +228,8 @@ def conv_stage(p, qkv_raw, tail):
     return q, k, v, new_tail
 
 
-def layer_forward(p, x32, S0=None, conv_tail=None, gate_log_a=None, gate_b=None, sequential=True, chunk=64):
+def layer_forward(p, x32, S0=None, conv_tail=None, gate_log_a=None, gate_b=None, sequential=True, chunk=64,
+                  decode=False):
     """Whole layer: projections, conv, gates, gated delta rule, gated RMSNorm, output projection.
 
     x32 [N, hidden] float32 (the exact values of the bf16 input for Q4_K layers);
@@ -232,7 +242,7 @@ def layer_forward(p, x32, S0=None, conv_tail=None, gate_log_a=None, gate_b=None,
         S0 = np.zeros((hv, dv, dk))
     if conv_tail is None:
         conv_tail = np.zeros((sz["c_conv"], p["conv_w"].shape[1] - 1))
-    qkvz, ba = project_in(p, x32)
+    qkvz, ba = project_in(p, x32, decode=decode)
     q, k, v, new_tail = conv_stage(p, qkvz[:, :sz["c_conv"]], conv_tail)
     z = qkvz[:, sz["c_conv"]:].reshape(n, hv, dv)
     if gate_log_a is not None:
@@ -243,6 +253,6 @@ def layer_forward(p, x32, S0=None, conv_tail=None, gate_log_a=None, gate_b=None,
     rec = gated_delta_rule if sequential else (lambda *a: gated_delta_rule_chunked(*a, chunk=chunk))
     o, S = rec(qe, ke, v, log_a, b, S0)
     o_hat = gated_rmsnorm(o, z, p["norm_w"], p["eps_rms"])
-    y = project_out(p, o_hat.reshape(n, sz["c_v"]))
+    y = project_out(p, o_hat.reshape(n, sz["c_v"]), decode=decode)
     return {"qkvz": qkvz, "ba": ba, "q": q, "k": k, "v": v, "z": z, "log_a": log_a, "b": b,
             "o": o, "state": S, "o_hat": o_hat, "y": y, "conv_tail": new_tail}

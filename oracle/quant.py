@@ -54,6 +54,19 @@ def gemm_q8(qa, sa, qb, sb) -> np.ndarray:
     return rescale(int_matmul_exact(qa, qb), sa, sb)
 
 
+def matvec_exact_weights(qa: np.ndarray, sa: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """The decode step's projection: int8 row codes qa [M, K] with scales sa [M]
+    against the exactly decoded weights w [N, K] (no re-quantisation of the
+    weights), y = sa[m] * sum_k qa[m, k] w[n, k], in float64.
+
+    This is the quantised-activation product of a decode GEMV that reads the
+    4-bit or 6-bit weight codes directly ("Qwen3.5 speed: prefill and decode
+    parity with llama.cpp" #5305, child ticket #5221, against llama.cpp's
+    quantised GEMV); the pages fix no rounding, so the oracle gives the exact
+    value and the GPU's fp32 sums are compared within a tolerance."""
+    return np.asarray(sa, np.float64)[:, None] * (qa.astype(np.float64) @ np.asarray(w, np.float64).T)
+
+
 def bf16_round(x: np.ndarray) -> np.ndarray:
     """Round float32 values to the nearest bf16 (ties to even); returned as float32."""
     u = np.ascontiguousarray(x, np.float32).view(np.uint32).astype(np.uint64)

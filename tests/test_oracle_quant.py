@@ -104,3 +104,42 @@ def test_bf16_round_closed_forms():
     assert r[5] == 1.0
     # every result has its low 16 bits clear
     assert np.all((r.view(np.uint32) & 0xFFFF) == 0)
+
+
+# ------------------------------------------------- decode-step product (exact weights)
+
+def test_matvec_exact_weights_brute_force():
+    """Element by element against Python's exact rationals on a tiny case,
+    with Q4_K-decoded weights (fp32 values, exact as fractions)."""
+    from fractions import Fraction
+    from oracle import q4k
+    rng = np.random.default_rng(4)
+    w = q4k.unpack_q4k(q4k.pack_q4k(rng.normal(0, 0.02, size=(3, 256)).astype(np.float32)), 3, 256)
+    qa, sa = quant.quant_rows_i8(rng.normal(0, 1, size=(2, 256)).astype(np.float32))
+    got = quant.matvec_exact_weights(qa, sa, w)
+    for m in range(2):
+        for n in range(3):
+            exact = Fraction(float(sa[m])) * sum(Fraction(int(qa[m, k])) * Fraction(float(w[n, k])) for k in range(256))
+            assert abs(Fraction(float(got[m, n])) - exact) <= abs(exact) * Fraction(1, 2 ** 50) + Fraction(1, 2 ** 80)
+
+
+def test_matvec_exact_weights_closed_form_and_bound():
+    """Constant weight rows give s * c * sum(q); against the prefill's product
+    (weights re-quantised to int8 rows) the difference is bounded by the
+    weights' half-step: |y_exact - y_q8| <= s_x * sum|q_x| * s_w / 2 (+ fp32 rounding)."""
+    rng = np.random.default_rng(8)
+    qa, sa = quant.quant_rows_i8(rng.normal(0, 1, size=(4, 512)).astype(np.float32))
+    w = np.full((2, 512), 0.375, np.float32)
+    w[1] = -0.0625
+    y = quant.matvec_exact_weights(qa, sa, w)
+    for m in range(4):
+        tot = int(qa[m].astype(np.int64).sum())
+        assert y[m, 0] == float(sa[m]) * 0.375 * tot
+        assert y[m, 1] == float(sa[m]) * -0.0625 * tot
+    wr = rng.normal(0, 0.02, size=(64, 512)).astype(np.float32)
+    qw, sw = quant.quant_rows_i8(wr)
+    ye = quant.matvec_exact_weights(qa, sa, wr)
+    yq = quant.gemm_q8(qa, sa, qw, sw).astype(np.float64)
+    bound = sa[:, None].astype(np.float64) * np.abs(qa).astype(np.float64).sum(1)[:, None] * sw[None, :] / 2
+    assert np.all(np.abs(ye - yq) <= bound * (1 + 1e-6) + 1e-6 * np.abs(ye))
+    assert np.any(ye != yq)        # the two products really differ
