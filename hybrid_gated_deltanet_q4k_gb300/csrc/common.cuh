@@ -87,13 +87,28 @@ __device__ __forceinline__ int quant_code(float w, float s) {
     return max(-127, min(127, q));
 }
 
-// The same code as a float (an integer value, +0 for zero), by the IEEE divide.
+// Codes are carried between the quantiser and the stores as "magic" floats
+// t = q + QCODE_MAGIC (q the integer code).  QCODE_MAGIC = 1.5 * 2^23 + 0x6480
+// puts t in [2^23, 2^24), where consecutive fp32 values are the integers, so
+// the one addition that forms t rounds to the nearest integer with ties to
+// even (QCODE_MAGIC is even), exactly as rint; and since fp32 bit patterns
+// grow by one per integer there, the low 16 bits of t are 0x6480 + q, the fp16
+// pattern of 1152 + q, and its low byte is (0x80 + q) mod 256.  The stores
+// take the code from those bits with byte permutes and one packed fp16
+// subtraction, so no instruction converts between integer and float.
+constexpr float QCODE_MAGIC = 12608640.0f;
+
+// The code of w by the IEEE divide, clamp(rne(w / s), -127, 127) (s == 0 or a
+// NaN quotient: 0), as a magic float.
 __device__ __forceinline__ float qcode_exact(float w, float s) {
-    if (s == 0.0f) return 0.0f;
+    if (s == 0.0f) return QCODE_MAGIC;
     const float r = rintf(__fdiv_rn(w, s));
-    if (r != r) return 0.0f;
-    return fminf(fmaxf(r, -127.0f), 127.0f) + 0.0f;
+    if (r != r) return QCODE_MAGIC;
+    return __fadd_rn(fminf(fmaxf(r, -127.0f), 127.0f), QCODE_MAGIC);
 }
+
+// The integer value of a magic-float code.
+__device__ __forceinline__ float qcode_value(float t) { return __fsub_rn(t, QCODE_MAGIC); }
 
 // Row scale s = amax/127 with its reciprocal for the fast quantiser.
 struct QScale {
@@ -114,12 +129,14 @@ __device__ __forceinline__ QScale make_qscale(float amax) {
 // half-integer.  When y is within 1e-3 of one (or is not a number), `redo` is
 // set and the caller recomputes with qcode_exact, so the result always equals
 // qcode_exact(w, s).  No clamp is needed: |w| <= amax and s = fl(amax/127)
-// give |y| <= 127 (1 + 2^-22) < 127.5, so |rint(y)| <= 127.
+// give |y| <= 127 (1 + 2^-22) < 127.5, so |rint(y)| <= 127.  Returns the
+// magic float of rint(y); every step is an explicitly rounded fp32 operation
+// (no contraction), and none is a conversion.
 __device__ __forceinline__ float qcode_fast(float w, const QScale& q, bool& redo) {
-    const float y = w * q.rs;
-    const float r = rintf(y);
-    redo |= !(fabsf(y - r) <= 0.499f);
-    return r + 0.0f;
+    const float y = __fmul_rn(w, q.rs);
+    const float t = __fadd_rn(y, QCODE_MAGIC);
+    redo |= !(fabsf(__fsub_rn(y, qcode_value(t))) <= 0.499f);
+    return t;
 }
 
 // Two floats as a pair of fp16 values (rounded to nearest), low half first.
@@ -128,10 +145,26 @@ __device__ __forceinline__ uint32_t f16x2_bits(float lo, float hi) {
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// Two codes (integer-valued floats) as a pair of fp16 values, low half first.
-__device__ __forceinline__ uint32_t codes_to_f16x2(float c0, float c1) {
-    const __half2 h = __floats2half2_rn(c0, c1);
+// Two magic-float codes as a pair of fp16 values, low half first: the fp16
+// patterns of 1152 + q (the low halves of the magic floats) minus 1152, exact.
+__device__ __forceinline__ uint32_t codes_to_f16x2(float t0, float t1) {
+    const uint32_t b = __byte_perm(__float_as_uint(t0), __float_as_uint(t1), 0x5410);
+    const __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&b), __half2half2(__ushort_as_half(0x6480)));
     return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Four magic-float codes as four int8 bytes, the first in the lowest byte:
+// the low bytes (0x80 + q) mod 256 of the magic floats, with the top bit flipped.
+__device__ __forceinline__ uint32_t codes_to_i8x4(float t0, float t1, float t2, float t3) {
+    const uint32_t lo = __byte_perm(__float_as_uint(t0), __float_as_uint(t1), 0x0040);
+    const uint32_t hi = __byte_perm(__float_as_uint(t2), __float_as_uint(t3), 0x0040);
+    return __byte_perm(lo, hi, 0x5410) ^ 0x80808080u;
+}
+
+// An integer 0 <= v < 2^23 as a float, exactly, without a conversion
+// instruction: 2^23 + v has the pattern 0x4B000000 | v.
+__device__ __forceinline__ float small_uint_to_float(uint32_t v) {
+    return __fsub_rn(__uint_as_float(0x4B000000u | v), 8388608.0f);
 }
 
 // SiLU(u) = u / (1 + e^-u) with the hardware exponential and reciprocal

@@ -40,7 +40,7 @@ cudaError_t launch_delta(const gdn_layer&, const uint16_t*, const float*, const 
 size_t delta_scratch_bytes(int hv, int hk, int d, int64_t n);
 cudaError_t launch_gated_norm(const gdn_layer&, const uint16_t*, const uint16_t*, int64_t, int64_t, uint16_t*, float*,
                               float*, cudaStream_t);
-cudaError_t launch_gemv_codes(const void*, bool, int64_t, int64_t, const uint16_t*, const float*, int64_t, uint16_t*,
+cudaError_t launch_gemv_dot(const void*, bool, int64_t, int64_t, const uint16_t*, const float*, int64_t, uint16_t*,
                               int64_t, int64_t, float*, int64_t, cudaStream_t);
 cudaError_t launch_decode_rule(const gdn_layer&, const uint16_t*, const float*, const float*, int64_t, float*, uint16_t*,
                                cudaStream_t);
@@ -757,7 +757,7 @@ int gdn_decode(const gdn_layer* layer, const void* x, int n_seqs, float* state, 
     // registers against them
     if (q4k) {
         GDN_LAUNCH(launch_quant_rows(static_cast<const uint16_t*>(x), B, s.H, w.xc, w.sx, st), "decode: quantise x");
-        GDN_LAUNCH(launch_gemv_codes(layer->w_in, layer->q6k_mask & 1, s.r_in, s.H, w.xc, w.sx, B, w.qkvz, s.n_bf16,
+        GDN_LAUNCH(launch_gemv_dot(layer->w_in, layer->q6k_mask & 1, s.r_in, s.H, w.xc, w.sx, B, w.qkvz, s.n_bf16,
                                      s.n_bf16, w.ba, 2 * s.hv, st),
                    "decode: input projection");
     } else {
@@ -780,7 +780,7 @@ int gdn_decode(const gdn_layer* layer, const void* x, int n_seqs, float* state, 
     GDN_LAUNCH(launch_gated_norm(*layer, w.o, w.qkvz + s.c_conv, s.n_bf16, B, w.oc, w.so, w.ohat, st),
                "decode: gated norm");
     if (q4k) {
-        GDN_LAUNCH(launch_gemv_codes(layer->w_out, layer->q6k_mask & 2, s.H, s.c_v, w.oc, w.so, B,
+        GDN_LAUNCH(launch_gemv_dot(layer->w_out, layer->q6k_mask & 2, s.H, s.c_v, w.oc, w.so, B,
                                      static_cast<uint16_t*>(y), s.H, s.H, nullptr, 0, st),
                    "decode: output projection");
     } else {
@@ -791,21 +791,21 @@ int gdn_decode(const gdn_layer* layer, const void* x, int n_seqs, float* state, 
     return GDN_OK;
 }
 
-int gdn_gemv_codes(const void* blocks, int q6k, int64_t rows, int64_t cols, const uint16_t* xc, const float* sx,
+int gdn_decode_gemv(const void* blocks, int q6k, int64_t rows, int64_t cols, const uint16_t* xc, const float* sx,
                    int64_t n, uint16_t* out_bf16, int64_t ld_bf16, int64_t n_bf16, float* out_f32, int64_t ld_f32,
                    void* stream) {
-    if (!blocks || !xc || !sx) return fail(GDN_EINVAL, "gdn_gemv_codes: NULL operand");
-    if (q6k != 0 && q6k != 1) return fail(GDN_EINVAL, "gdn_gemv_codes: q6k must be 0 or 1");
+    if (!blocks || !xc || !sx) return fail(GDN_EINVAL, "gdn_decode_gemv: NULL operand");
+    if (q6k != 0 && q6k != 1) return fail(GDN_EINVAL, "gdn_decode_gemv: q6k must be 0 or 1");
     if (rows < 1 || rows > 0x7fffffff || cols < 256 || cols > 16384 || cols % 256 || n < 1 || n > GDN_MAX_SEQS)
-        return fail(GDN_EINVAL, "gdn_gemv_codes: rows >= 1, cols a multiple of 256 in [256, 16384], 1 <= n <= %d",
+        return fail(GDN_EINVAL, "gdn_decode_gemv: rows >= 1, cols a multiple of 256 in [256, 16384], 1 <= n <= %d",
                     GDN_MAX_SEQS);
-    if (n_bf16 < 0) return fail(GDN_EINVAL, "gdn_gemv_codes: n_bf16 < 0");
-    if (n_bf16 > 0 && (!out_bf16 || ld_bf16 < (n_bf16 < rows ? n_bf16 : rows))) return fail(GDN_EINVAL, "gdn_gemv_codes: bf16 output");
-    if (n_bf16 < rows && (!out_f32 || ld_f32 < rows - n_bf16)) return fail(GDN_EINVAL, "gdn_gemv_codes: fp32 output");
-    if (!aligned(blocks, 16) || !aligned(xc, 16)) return fail(GDN_EINVAL, "gdn_gemv_codes: 16-byte alignment required");
-    GDN_LAUNCH(launch_gemv_codes(blocks, q6k == 1, rows, cols, xc, sx, n, out_bf16, ld_bf16, n_bf16, out_f32, ld_f32,
+    if (n_bf16 < 0) return fail(GDN_EINVAL, "gdn_decode_gemv: n_bf16 < 0");
+    if (n_bf16 > 0 && (!out_bf16 || ld_bf16 < (n_bf16 < rows ? n_bf16 : rows))) return fail(GDN_EINVAL, "gdn_decode_gemv: bf16 output");
+    if (n_bf16 < rows && (!out_f32 || ld_f32 < rows - n_bf16)) return fail(GDN_EINVAL, "gdn_decode_gemv: fp32 output");
+    if (!aligned(blocks, 16) || !aligned(xc, 16)) return fail(GDN_EINVAL, "gdn_decode_gemv: 16-byte alignment required");
+    GDN_LAUNCH(launch_gemv_dot(blocks, q6k == 1, rows, cols, xc, sx, n, out_bf16, ld_bf16, n_bf16, out_f32, ld_f32,
                                  static_cast<cudaStream_t>(stream)),
-               "gdn_gemv_codes");
+               "gdn_decode_gemv");
     return GDN_OK;
 }
 

@@ -3,19 +3,21 @@
 // Two kernels of its own, beside the prefill kernels it shares (activation
 // quantisation, conv with one token per sequence, gated norm):
 //
-// gemv_codes_kernel -- the projections for a few tokens.  Decoding a whole
-//   weight matrix to int8 codes in HBM (step 1a of the prefill) would move
-//   3.5x the Q4_K bytes for one token; here each warp decodes one weight row
-//   in registers (the same per-lane decode and quantiser as step 1a, so the
-//   codes and the row scale are bit for bit the prefill's), and takes the
-//   exact integer dot products with the tokens' int8 codes (dp4a, int32).
-//   The epilogue ((float)acc * s_x) * s_w is the prefill GEMM's, so the
-//   projections equal the prefill's bit for bit.  A decode GEMV is bound by
-//   reading the quantised weights once ("Qwen3.5 speed: prefill and decode
-//   parity with llama.cpp" #5305, child ticket #5221: decode GEMV bandwidth
-//   against llama.cpp's quantised-activation GEMV, Q4_K and Q6_K).  Row pass 1 finds the amax (the row stays in L1), pass 2 decodes,
-//   quantises and accumulates.  The tokens' codes sit in shared memory as
-//   packed int8.
+// gemv_dot_kernel -- the projections for a few tokens.  Decoding a whole
+//   weight matrix to int8 rows in HBM (step 1a of the prefill) would move 3.5x
+//   the Q4_K bytes for one token, and re-quantising each weight costs more
+//   instructions than reading it; a decode GEMV is bound by reading the
+//   quantised weights once ("Qwen3.5 speed: prefill and decode parity with
+//   llama.cpp" #5305, child ticket #5221: decode GEMV bandwidth against
+//   llama.cpp's quantised GEMV, Q4_K and Q6_K).  So the tokens keep the int8
+//   row codes the prefill gives them (scale s_x per token), and each weight
+//   sub-block meets them as integers: for a Q4_K sub-block
+//       sum_k w_k x_k = d*sc * sum q_k x_k - dmin*m * sum x_k,
+//   for a Q6_K sub-block d*scale * (sum c_k x_k - 32 sum x_k), the integer
+//   sums by dp4a on the packed 4-bit / 6-bit codes, the rest in fp32; the
+//   token's total is then multiplied by s_x.  Weight tiles of 8 rows (one per
+//   warp) arrive in shared memory by bulk copies through a ring of stages, so
+//   each row is read from HBM once with many bytes in flight.
 //
 // decode_rule_kernel -- one token of the gated delta rule per sequence, in
 //   fp32, the state read and written once:
@@ -31,18 +33,24 @@
 //   type); a value beyond its range sets ERR_RANGE.
 #include "common.cuh"
 #include "qk_decode.cuh"
+#include "tma.cuh"
 
 namespace gdn {
 
 static __device__ int g_decode_error;
 
 constexpr int GEMV_THREADS = 256;
-constexpr int GEMV_WARPS = GEMV_THREADS / 32;
+constexpr int GEMV_WARPS = GEMV_THREADS / 32;          // = rows per tile: one row per warp
 constexpr int GEMV_TOKENS = GDN_DECODE_GEMV_TOKENS;   // tokens per launch (codes in shared memory)
+constexpr int GEMV_MAX_STAGES = 4;
+constexpr int GEMV_SMEM_BUDGET = 112 * 1024;          // two CTAs per SM when the tiles allow
 
 struct GemvArgs {
     const uint8_t* blocks;   // [rows][cols/256] superblocks
     int rows, cols;
+    int64_t row_bytes;       // cols/256 superblocks of the format's size
+    int ntiles, stages;      // tiles of GEMV_WARPS rows; shared-memory ring depth
+    int64_t total_bytes;     // rows * row_bytes
     const uint16_t* xc;      // [g][cols] int8 codes as fp16 patterns
     const float* sx;         // [g]
     int g;                   // tokens of this launch, 1 .. GEMV_TOKENS
@@ -53,113 +61,243 @@ struct GemvArgs {
     int64_t ld_f32;
 };
 
-__device__ __forceinline__ uint32_t pack_i8x4(float c0, float c1, float c2, float c3) {
-    return (static_cast<uint32_t>(static_cast<int>(c0)) & 0xffu) | ((static_cast<uint32_t>(static_cast<int>(c1)) & 0xffu) << 8) |
-           ((static_cast<uint32_t>(static_cast<int>(c2)) & 0xffu) << 16) | (static_cast<uint32_t>(static_cast<int>(c3)) << 24);
+// Shared memory: the tokens' codes (g * cols bytes), their sums over blocks
+// of 16 (g * cols/16 ints), then `stages` tiles of GEMV_WARPS weight rows,
+// then one mbarrier per stage.
+__host__ __device__ inline int64_t gemv_tile_bytes(int64_t row_bytes) { return GEMV_WARPS * row_bytes; }
+__host__ __device__ inline int64_t gemv_xsum_offset(int g, int cols) { return (static_cast<int64_t>(g) * cols + 127) & ~127LL; }
+__host__ __device__ inline int64_t gemv_ring_offset(int g, int cols) {
+    return (gemv_xsum_offset(g, cols) + static_cast<int64_t>(g) * (cols / 16) * 4 + 127) & ~127LL;
+}
+__host__ __device__ inline int64_t gemv_smem_bytes(int g, int cols, int64_t row_bytes, int stages) {
+    return gemv_ring_offset(g, cols) + stages * gemv_tile_bytes(row_bytes) + 8 * GEMV_MAX_STAGES;
 }
 
-__device__ __forceinline__ int warp_sum_i(int v) {
+// Copy tile `tile` into stage `s`: the whole bytes by one bulk copy (a tile
+// starts on 16 bytes: 8 rows of 144 or 210 bytes per superblock are a multiple
+// of 16), a ragged end of the last tile (< 16 bytes) by plain loads.  Thread 0.
+__device__ __forceinline__ void gemv_issue(const GemvArgs& a, unsigned char* ring, uint64_t* full, int tile, int s) {
+    if (tile >= a.ntiles) return;
+    const int64_t tb = gemv_tile_bytes(a.row_bytes);
+    const int64_t off = static_cast<int64_t>(tile) * tb;
+    const int64_t bytes = (a.total_bytes - off) < tb ? (a.total_bytes - off) : tb;
+    const int64_t b16 = bytes & ~15LL;
+    unsigned char* dst = ring + s * tb;
+    for (int64_t i = b16; i < bytes; ++i) dst[i] = a.blocks[off + i];
+    mbar_expect_tx(full + s, static_cast<uint32_t>(b16));
+    if (b16) bulk_load_1d(dst, a.blocks + off, static_cast<uint32_t>(b16), full + s);
+}
+
+// One lane takes one 32-weight span of a superblock (a Q4_K sub-block; two
+// 16-weight Q6_K sub-blocks): lane l of a warp step works on superblock
+// step*4 + l/8, span l%8, so a warp covers 4 superblocks per step and each
+// lane decodes its scales once per 32 weights.  Its codes come as 8 words of
+// 4 packed bytes (weights 32j .. 32j+31 of the superblock, in order), and
+//   sum_k w_k x_k = mul0 * dot(codes[0..15], x) + mul1 * dot(codes[16..31], x)
+//                 + add0 * sum(x[0..15]) + add1 * sum(x[16..31]).
+template <bool Q6>
+__device__ __forceinline__ void span_codes(const uint8_t* blk, int j, uint32_t (&c)[8], float& mul0, float& mul1,
+                                           float& add0, float& add1) {
+    if constexpr (!Q6) {
+        const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
+        const int k = j & 3;
+        const uint32_t yk = __byte_perm(hdr.y, 0u, 0x4440 + k), zk = __byte_perm(hdr.z, 0u, 0x4440 + k);
+        const uint32_t wk = __byte_perm(hdr.w, 0u, 0x4440 + k);
+        const uint32_t sc = j < 4 ? (yk & 63u) : ((wk & 15u) | ((yk >> 2) & 0x30u));
+        const uint32_t m = j < 4 ? (zk & 63u) : ((wk >> 4) | ((zk >> 2) & 0x30u));
+        const float d = __half2float(__ushort_as_half(static_cast<uint16_t>(hdr.x & 0xffffu)));
+        const float dmin = __half2float(__ushort_as_half(static_cast<uint16_t>(hdr.x >> 16)));
+        const float ds = __fmul_rn(d, small_uint_to_float(sc)), dm = __fmul_rn(dmin, small_uint_to_float(m));
+        const uint4* q = reinterpret_cast<const uint4*>(blk + 16 + 32 * (j >> 1));
+        const uint4 a = q[0], b = q[1];
+        const int sh = 4 * (j & 1);
+        c[0] = (a.x >> sh) & 0x0f0f0f0fu; c[1] = (a.y >> sh) & 0x0f0f0f0fu;
+        c[2] = (a.z >> sh) & 0x0f0f0f0fu; c[3] = (a.w >> sh) & 0x0f0f0f0fu;
+        c[4] = (b.x >> sh) & 0x0f0f0f0fu; c[5] = (b.y >> sh) & 0x0f0f0f0fu;
+        c[6] = (b.z >> sh) & 0x0f0f0f0fu; c[7] = (b.w >> sh) & 0x0f0f0f0fu;
+        mul0 = mul1 = ds;
+        add0 = add1 = -dm;
+    } else {
+        const int h = j >> 2, g = j & 3;
+        const uint16_t* ql = reinterpret_cast<const uint16_t*>(blk + 64 * h + 32 * (g & 1));
+        const uint16_t* qh = reinterpret_cast<const uint16_t*>(blk + 128 + 32 * h);
+        const int nsh = 4 * (g >> 1), hsh = 2 * g;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
+        for (int e = 0; e < 8; ++e) {
+            const uint32_t lw = ql[2 * e] | (static_cast<uint32_t>(ql[2 * e + 1]) << 16);
+            const uint32_t hw = qh[2 * e] | (static_cast<uint32_t>(qh[2 * e + 1]) << 16);
+            c[e] = ((lw >> nsh) & 0x0f0f0f0fu) | (((hw >> hsh) & 0x03030303u) << 4);
+        }
+        const float d = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(blk + 208)));
+        const int8_t s0 = static_cast<int8_t>(blk[192 + 2 * j]), s1 = static_cast<int8_t>(blk[193 + 2 * j]);
+        mul0 = __fmul_rn(d, static_cast<float>(s0));
+        mul1 = __fmul_rn(d, static_cast<float>(s1));
+        add0 = -32.0f * mul0;
+        add1 = -32.0f * mul1;
+    }
 }
 
-template <class Fmt>
-__global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_codes_kernel(GemvArgs a) {
-    extern __shared__ __align__(16) uint32_t xs[];   // [g][cols / 4] packed int8
-    const int kw = a.cols >> 2;
-    for (int i = threadIdx.x; i < a.g * kw; i += GEMV_THREADS) {
-        const int t = i / kw, k4 = i - t * kw;
-        const uint2 h = __ldg(reinterpret_cast<const uint2*>(a.xc + static_cast<int64_t>(t) * a.cols + 4 * k4));
-        const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&h.x));
-        const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&h.y));
-        xs[i] = pack_i8x4(f0.x, f0.y, f1.x, f1.y);
+template <bool Q6>
+__global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_dot_kernel(GemvArgs a) {
+    constexpr int BYTES = Q6 ? 210 : 144;
+    extern __shared__ __align__(128) unsigned char gsm[];
+    uint32_t* xs = reinterpret_cast<uint32_t*>(gsm);                 // [g][cols / 4] packed int8
+    int* xsum = reinterpret_cast<int*>(gsm + gemv_xsum_offset(a.g, a.cols));   // [g][cols / 16] block sums
+    unsigned char* ring = gsm + gemv_ring_offset(a.g, a.cols);
+    const int64_t tb = gemv_tile_bytes(a.row_bytes);
+    uint64_t* full = reinterpret_cast<uint64_t*>(ring + a.stages * tb);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    if (tid == 0) {
+        for (int i = 0; i < a.stages; ++i) mbar_init_cta(full + i, 1);
+        mbar_init_fence();
+        for (int i = 0; i < a.stages; ++i) gemv_issue(a, ring, full, blockIdx.x + i * gridDim.x, i);
+    }
+    // the tokens' codes as packed int8, and their sums over every 16 codes
+    const int kw = a.cols >> 2, k16 = a.cols >> 4;
+    for (int i = tid; i < a.g * k16; i += GEMV_THREADS) {
+        const int t = i / k16, b = i - t * k16;
+        const uint4 h0 = __ldg(reinterpret_cast<const uint4*>(a.xc + static_cast<int64_t>(t) * a.cols + 16 * b));
+        const uint4 h1 = __ldg(reinterpret_cast<const uint4*>(a.xc + static_cast<int64_t>(t) * a.cols + 16 * b + 8));
+        const uint32_t hw[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+        int sum = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&hw[2 * q]));
+            const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&hw[2 * q + 1]));
+            const uint32_t packed = codes_to_i8x4(__fadd_rn(f0.x, QCODE_MAGIC), __fadd_rn(f0.y, QCODE_MAGIC),
+                                                  __fadd_rn(f1.x, QCODE_MAGIC), __fadd_rn(f1.y, QCODE_MAGIC));
+            xs[t * kw + 4 * b + q] = packed;
+            sum = __dp4a(static_cast<int>(packed), 0x01010101, sum);
+        }
+        xsum[i] = sum;
     }
     __syncthreads();
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nsb = a.cols >> 8;
-    for (int row = blockIdx.x * GEMV_WARPS + warp; row < a.rows; row += gridDim.x * GEMV_WARPS) {
-        const uint8_t* rb = a.blocks + static_cast<int64_t>(row) * nsb * Fmt::BYTES;
-        float amax = 0.0f;
-#pragma unroll 4
-        for (int i = 0; i < nsb; ++i) amax = fmaxf(amax, Fmt::amax(rb + i * Fmt::BYTES, lane));
-        amax = warp_max(amax);
-        const QScale qsc = make_qscale(amax);
-        int acc[GEMV_TOKENS];
+    const int j = lane & 7, sbl = lane >> 3;       // the lane's span and superblock within a step of 4
+    bool aborted = false;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x, ++it) {
+        const int s = it % a.stages;
+        const bool ok = mbar_wait_bounded(full + s, (it / a.stages) & 1, &g_decode_error, ERR_WAIT_TIMEOUT);
+        if (!__syncthreads_and(ok)) {
+            aborted = true;
+            break;
+        }
+        const int row = tile * GEMV_WARPS + warp;
+        if (row < a.rows) {
+            const uint8_t* rb = ring + s * tb + static_cast<int64_t>(warp) * a.row_bytes;
+            float acc[GEMV_TOKENS];
 #pragma unroll
-        for (int t = 0; t < GEMV_TOKENS; ++t) acc[t] = 0;
-#pragma unroll 2
-        for (int i = 0; i < nsb; ++i) {
-            float w[8], c[8];
-            Fmt::decode(rb + i * Fmt::BYTES, lane, w);
-            quantise8(w, qsc, c);
-            const int lo = static_cast<int>(pack_i8x4(c[0], c[1], c[2], c[3]));
-            const int hi = static_cast<int>(pack_i8x4(c[4], c[5], c[6], c[7]));
-            const uint32_t* xw = xs + 64 * i + 2 * lane;
+            for (int t = 0; t < GEMV_TOKENS; ++t) acc[t] = 0.0f;
+            for (int i = sbl; i < nsb; i += 4) {
+                uint32_t c[8];
+                float mul0, mul1, add0, add1;
+                span_codes<Q6>(rb + i * BYTES, j, c, mul0, mul1, add0, add1);
+                const int w0 = 64 * i + 8 * j;           // first x word of the span (256 i + 32 j bytes)
+#pragma unroll
+                for (int t = 0; t < GEMV_TOKENS; ++t) {
+                    if (t < a.g) {
+                        const uint4 xa = *reinterpret_cast<const uint4*>(xs + t * kw + w0);
+                        const uint4 xb = *reinterpret_cast<const uint4*>(xs + t * kw + w0 + 4);
+                        const int2 sx = *reinterpret_cast<const int2*>(xsum + t * k16 + 16 * i + 2 * j);
+                        int d0 = __dp4a(static_cast<int>(c[0]), static_cast<int>(xa.x), 0);
+                        d0 = __dp4a(static_cast<int>(c[1]), static_cast<int>(xa.y), d0);
+                        d0 = __dp4a(static_cast<int>(c[2]), static_cast<int>(xa.z), d0);
+                        d0 = __dp4a(static_cast<int>(c[3]), static_cast<int>(xa.w), d0);
+                        int d1 = __dp4a(static_cast<int>(c[4]), static_cast<int>(xb.x), 0);
+                        d1 = __dp4a(static_cast<int>(c[5]), static_cast<int>(xb.y), d1);
+                        d1 = __dp4a(static_cast<int>(c[6]), static_cast<int>(xb.z), d1);
+                        d1 = __dp4a(static_cast<int>(c[7]), static_cast<int>(xb.w), d1);
+                        float r = fmaf(mul0, static_cast<float>(d0), fmaf(add0, static_cast<float>(sx.x), acc[t]));
+                        acc[t] = fmaf(mul1, static_cast<float>(d1), fmaf(add1, static_cast<float>(sx.y), r));
+                    }
+                }
+            }
+            float mine = 0.0f;
 #pragma unroll
             for (int t = 0; t < GEMV_TOKENS; ++t) {
                 if (t < a.g) {
-                    const uint2 xv = *reinterpret_cast<const uint2*>(xw + t * kw);
-                    acc[t] = __dp4a(lo, static_cast<int>(xv.x), acc[t]);
-                    acc[t] = __dp4a(hi, static_cast<int>(xv.y), acc[t]);
+                    const float sum = warp_sum(acc[t]);
+                    if (lane == t) mine = sum;
                 }
             }
-        }
-        int mine = 0;
-#pragma unroll
-        for (int t = 0; t < GEMV_TOKENS; ++t) {
-            if (t < a.g) {
-                const int s = warp_sum_i(acc[t]);   // exact: |sum| <= 16384 * 127^2 < 2^31
-                if (lane == t) mine = s;
+            if (lane < a.g) {
+                const float y = mine * a.sx[lane];
+                if (row < a.n_bf16)
+                    a.out_bf16[lane * a.ld_bf16 + row] = float_to_bf16_bits(y);
+                else
+                    a.out_f32[lane * a.ld_f32 + (row - a.n_bf16)] = y;
             }
         }
-        if (lane < a.g) {
-            const float y = __fmul_rn(__fmul_rn(static_cast<float>(mine), a.sx[lane]), qsc.s);
-            if (row < a.n_bf16)
-                a.out_bf16[lane * a.ld_bf16 + row] = float_to_bf16_bits(y);
-            else
-                a.out_f32[lane * a.ld_f32 + (row - a.n_bf16)] = y;
+        __syncthreads();   // every warp is done with stage s
+        if (tid == 0) {
+            fence_proxy_async_smem();
+            gemv_issue(a, ring, full, tile + a.stages * gridDim.x, s);
         }
+    }
+    if (aborted && tid == 0) {
+        // a wait ran out: let copies already issued land (bounded) before the
+        // shared memory is released
+        for (int i = 0; i < a.stages; ++i)
+            for (uint32_t par = 0; par < 2; ++par) mbar_wait_bounded(full + i, par, nullptr, 0, 20000000ull);
     }
 }
 
-// out = codes(x) . codes(W)^T rescaled, for n tokens in launches of at most
-// GEMV_TOKENS; W in Q4_K (q6k false) or Q6_K.
-cudaError_t launch_gemv_codes(const void* blocks, bool q6k, int64_t rows, int64_t cols, const uint16_t* xc,
+// out[t][r] = s_x[t] * sum_k xc[t][k] W[r][k] (W exactly decoded), for n tokens in launches of at most
+// GEMV_TOKENS (fewer when a token's codes and the tiles would not fit shared
+// memory); W in Q4_K (q6k false) or Q6_K.  A persistent grid of at most two
+// CTAs per SM walks the tiles.
+cudaError_t launch_gemv_dot(const void* blocks, bool q6k, int64_t rows, int64_t cols, const uint16_t* xc,
                               const float* sx, int64_t n, uint16_t* out_bf16, int64_t ld_bf16, int64_t n_bf16,
                               float* out_f32, int64_t ld_f32, cudaStream_t st) {
-    static int sms = 0;
+    static int sms = 0, max_optin = 0;
     if (!sms) {
         int dev = 0;
         cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        cudaFuncSetAttribute(gemv_dot_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_optin);
+        cudaFuncSetAttribute(gemv_dot_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_optin);
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        const int max_smem = GEMV_TOKENS * 16384;
-        cudaFuncSetAttribute(gemv_codes_kernel<Q4KLane>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-        cudaFuncSetAttribute(gemv_codes_kernel<Q6KLane>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
     }
-    const int64_t need_ctas = (rows + GEMV_WARPS - 1) / GEMV_WARPS;
-    const unsigned grid = static_cast<unsigned>(need_ctas < 4LL * sms ? need_ctas : 4LL * sms);
-    for (int64_t t0 = 0; t0 < n; t0 += GEMV_TOKENS) {
+    const int64_t row_bytes = (cols / 256) * (q6k ? 210 : 144);
+    const int64_t tb = gemv_tile_bytes(row_bytes);
+    // tokens per launch: what fits beside one stage
+    int64_t gmax = GEMV_TOKENS;
+    while (gmax > 1 && gemv_smem_bytes(static_cast<int>(gmax), static_cast<int>(cols), row_bytes, 1) > max_optin) --gmax;
+    if (gemv_smem_bytes(1, static_cast<int>(cols), row_bytes, 1) > max_optin) return cudaErrorInvalidValue;
+    const int ntiles = static_cast<int>((rows + GEMV_WARPS - 1) / GEMV_WARPS);
+    for (int64_t t0 = 0; t0 < n; t0 += gmax) {
         GemvArgs a;
         a.blocks = static_cast<const uint8_t*>(blocks);
         a.rows = static_cast<int>(rows);
         a.cols = static_cast<int>(cols);
+        a.row_bytes = row_bytes;
+        a.ntiles = ntiles;
+        a.total_bytes = rows * row_bytes;
         a.xc = xc + t0 * cols;
         a.sx = sx + t0;
-        a.g = static_cast<int>(n - t0 < GEMV_TOKENS ? n - t0 : GEMV_TOKENS);
+        a.g = static_cast<int>(n - t0 < gmax ? n - t0 : gmax);
         a.out_bf16 = out_bf16 ? out_bf16 + t0 * ld_bf16 : nullptr;
         a.ld_bf16 = ld_bf16;
         a.n_bf16 = static_cast<int>(n_bf16);
         a.out_f32 = out_f32 ? out_f32 + t0 * ld_f32 : nullptr;
         a.ld_f32 = ld_f32;
-        const size_t smem = static_cast<size_t>(a.g) * cols;
+        // ring depth: as many stages as fit the two-CTA budget (at least one)
+        int stages = GEMV_MAX_STAGES;
+        while (stages > 1 && gemv_smem_bytes(a.g, a.cols, row_bytes, stages) > GEMV_SMEM_BUDGET) --stages;
+        a.stages = stages;
+        const size_t smem = static_cast<size_t>(gemv_smem_bytes(a.g, a.cols, row_bytes, stages));
+        const int per_sm = smem <= GEMV_SMEM_BUDGET ? 2 : 1;
+        const unsigned grid = static_cast<unsigned>(ntiles < per_sm * sms ? ntiles : per_sm * sms);
         if (q6k)
-            gemv_codes_kernel<Q6KLane><<<grid, GEMV_THREADS, smem, st>>>(a);
+            gemv_dot_kernel<true><<<grid, GEMV_THREADS, smem, st>>>(a);
         else
-            gemv_codes_kernel<Q4KLane><<<grid, GEMV_THREADS, smem, st>>>(a);
+            gemv_dot_kernel<false><<<grid, GEMV_THREADS, smem, st>>>(a);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
+    (void)tb;
     return cudaSuccess;
 }
 

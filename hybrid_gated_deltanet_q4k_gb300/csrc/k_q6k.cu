@@ -39,23 +39,6 @@ struct Q6Job {
 };
 
 template <typename OutT>
-__device__ __forceinline__ void store_codes8(OutT* dst, const float (&c)[8]);
-
-template <>
-__device__ __forceinline__ void store_codes8<uint16_t>(uint16_t* dst, const float (&c)[8]) {
-    *reinterpret_cast<uint4*>(dst) = make_uint4(codes_to_f16x2(c[0], c[1]), codes_to_f16x2(c[2], c[3]),
-                                                codes_to_f16x2(c[4], c[5]), codes_to_f16x2(c[6], c[7]));
-}
-
-template <>
-__device__ __forceinline__ void store_codes8<int8_t>(int8_t* dst, const float (&c)[8]) {
-    uint32_t w[2] = {0u, 0u};
-#pragma unroll
-    for (int e = 0; e < 8; ++e) w[e >> 2] |= (static_cast<uint32_t>(static_cast<int>(c[e])) & 0xffu) << (8 * (e & 3));
-    *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
-}
-
-template <typename OutT>
 __global__ void __launch_bounds__(Q6_THREADS, 4) q6k_deq_rows_warp_kernel(Q6Job<OutT> j) {
     const int lane = threadIdx.x & 31;
     const int64_t row = static_cast<int64_t>(blockIdx.x) * (Q6_THREADS / 32) + (threadIdx.x >> 5);

@@ -48,15 +48,24 @@ __device__ __forceinline__ void q4k_sub_affine(const uint4& hdr, int sub, float&
     dm = __fmul_rn(dmin, static_cast<float>(m));
 }
 
-// Q4_K: lane's 8 weights of the superblock at blk (16-byte aligned), exact
-// single roundings of d*sc*q - dmin*m; amax_only: just their largest magnitude
-// (at the smallest or largest code: the decode is monotonic in q).
-struct Q4KLane {
+// Loads of the decoders: read-only global loads (G = true) or plain loads (G =
+// false, e.g. from shared memory).
+template <bool G, typename T>
+__device__ __forceinline__ T ldq(const T* p) {
+    if constexpr (G) return __ldg(p);
+    else return *p;
+}
+
+// Q4_K: the lane's 8 weights of the superblock at blk (16-byte aligned), exact
+// single roundings of d*sc*q - dmin*m; amax: just their largest magnitude (at
+// the smallest or largest code: the decode is monotonic in q).
+template <bool G>
+struct Q4KLaneT {
     static constexpr int BYTES = 144;
     __device__ __forceinline__ static float amax(const uint8_t* blk, int lane) {
         const int sub = lane >> 2, p = sub >> 1, l0 = (lane & 3) * 8, shift = (sub & 1) * 4;
-        const uint4 hdr = __ldg(reinterpret_cast<const uint4*>(blk));
-        const uint2 qs = __ldg(reinterpret_cast<const uint2*>(blk + 16 + 32 * p + l0));
+        const uint4 hdr = ldq<G>(reinterpret_cast<const uint4*>(blk));
+        const uint2 qs = ldq<G>(reinterpret_cast<const uint2*>(blk + 16 + 32 * p + l0));
         float ds, dm;
         q4k_sub_affine(hdr, sub, ds, dm);
         const uint32_t n0 = (qs.x >> shift) & 0x0f0f0f0fu, n1 = (qs.y >> shift) & 0x0f0f0f0fu;
@@ -65,69 +74,77 @@ struct Q4KLane {
         mx = __vmaxu4(mx, mx >> 16);
         mn = __vminu4(mn, mn >> 8) & 0xffu;
         mx = __vmaxu4(mx, mx >> 8) & 0xffu;
-        const float w0 = __fmaf_rn(ds, static_cast<float>(mn), -dm);
-        const float w1 = __fmaf_rn(ds, static_cast<float>(mx), -dm);
+        const float w0 = __fmaf_rn(ds, small_uint_to_float(mn), -dm);
+        const float w1 = __fmaf_rn(ds, small_uint_to_float(mx), -dm);
         return fmaxf(fabsf(w0), fabsf(w1));
     }
     __device__ __forceinline__ static void decode(const uint8_t* blk, int lane, float (&w)[8]) {
         const int sub = lane >> 2, p = sub >> 1, l0 = (lane & 3) * 8, shift = (sub & 1) * 4;
-        const uint4 hdr = __ldg(reinterpret_cast<const uint4*>(blk));
-        const uint2 qs = __ldg(reinterpret_cast<const uint2*>(blk + 16 + 32 * p + l0));
+        const uint4 hdr = ldq<G>(reinterpret_cast<const uint4*>(blk));
+        const uint2 qs = ldq<G>(reinterpret_cast<const uint2*>(blk + 16 + 32 * p + l0));
         float ds, dm;
         q4k_sub_affine(hdr, sub, ds, dm);
+        // the lane's 8 nibbles, one per byte, then each byte as 2^23 + q (byte permutes)
+        const uint32_t n0 = (qs.x >> shift) & 0x0f0f0f0fu, n1 = (qs.y >> shift) & 0x0f0f0f0fu;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            const uint32_t q = ((e < 4 ? qs.x : qs.y) >> (8 * (e & 3) + shift)) & 15u;
-            w[e] = __fmaf_rn(ds, static_cast<float>(q), -dm);
+            const uint32_t bits = __byte_perm(e < 4 ? n0 : n1, 0x4B000000u, 0x7440 + (e & 3));
+            w[e] = __fmaf_rn(ds, __fsub_rn(__uint_as_float(bits), 8388608.0f), -dm);
         }
     }
 };
+using Q4KLane = Q4KLaneT<true>;
 
-// Q6_K: the lane's 8 signed codes q = c - 32 and its d * scale (exact); the
-// superblock is only 2-byte aligned (210 = 2 * 105), so it is read in 16-bit words.
-__device__ __forceinline__ void q6k_lane(const uint8_t* blk, int lane, int (&q)[8], float& ds) {
+// Q6_K: the lane's 8 six-bit codes c (0..63, weight = d*scale*(c - 32)) and its
+// d * scale (exact); the superblock is only 2-byte aligned (210 = 2 * 105),
+// so it is read in 16-bit words.
+template <bool G>
+__device__ __forceinline__ void q6k_lane(const uint8_t* blk, int lane, uint32_t (&c)[8], float& ds) {
     const int v0 = 8 * lane, h = v0 >> 7, g = (v0 & 127) >> 5, l0 = v0 & 31;
     const uint16_t* ql = reinterpret_cast<const uint16_t*>(blk + 64 * h + 32 * (g & 1) + l0);
     const uint16_t* qh = reinterpret_cast<const uint16_t*>(blk + 128 + 32 * h + l0);
     const int nsh = 4 * (g >> 1), hsh = 2 * g;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        const uint32_t lw = __ldg(ql + k), hw = __ldg(qh + k);
+        const uint32_t lw = ldq<G>(ql + k), hw = ldq<G>(qh + k);
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             const uint32_t lo = (lw >> (8 * e + nsh)) & 15u;
             const uint32_t hi = (hw >> (8 * e + hsh)) & 3u;
-            q[2 * k + e] = static_cast<int>(lo | (hi << 4)) - 32;
+            c[2 * k + e] = lo | (hi << 4);
         }
     }
-    const int8_t sc = static_cast<int8_t>(__ldg(blk + 192 + (v0 >> 4)));
-    const float d = __half2float(__ushort_as_half(__ldg(reinterpret_cast<const uint16_t*>(blk + 208))));
+    const int8_t sc = static_cast<int8_t>(ldq<G>(blk + 192 + (v0 >> 4)));
+    const float d = __half2float(__ushort_as_half(ldq<G>(reinterpret_cast<const uint16_t*>(blk + 208))));
     ds = __fmul_rn(d, static_cast<float>(sc));
 }
 
-struct Q6KLane {
+template <bool G>
+struct Q6KLaneT {
     static constexpr int BYTES = 210;
     __device__ __forceinline__ static float amax(const uint8_t* blk, int lane) {
-        int q[8];
+        uint32_t c[8];
         float ds;
-        q6k_lane(blk, lane, q, ds);
+        q6k_lane<G>(blk, lane, c, ds);
         int m = 0;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) m = max(m, abs(q[e]));
-        return fabsf(ds * static_cast<float>(m));   // exact: the largest |w| of the 8
+        for (int e = 0; e < 8; ++e) m = max(m, abs(static_cast<int>(c[e]) - 32));
+        return fabsf(__fmul_rn(ds, small_uint_to_float(static_cast<uint32_t>(m))));   // the largest |w| of the 8, exact
     }
     __device__ __forceinline__ static void decode(const uint8_t* blk, int lane, float (&w)[8]) {
-        int q[8];
+        uint32_t c[8];
         float ds;
-        q6k_lane(blk, lane, q, ds);
+        q6k_lane<G>(blk, lane, c, ds);
+        // c - 32 exactly: (2^23 + c) - (2^23 + 32); the product with d*scale is exact
 #pragma unroll
-        for (int e = 0; e < 8; ++e) w[e] = ds * static_cast<float>(q[e]);
+        for (int e = 0; e < 8; ++e) w[e] = __fmul_rn(ds, __fsub_rn(__uint_as_float(0x4B000000u | c[e]), 8388640.0f));
     }
 };
+using Q6KLane = Q6KLaneT<true>;
 
-// The int8 codes of 8 decoded weights for the row's scale: the fast quantiser,
-// with the exact fallback where it may round differently (results equal
-// qcode_exact for every weight).
+// The int8 codes of 8 decoded weights for the row's scale, as magic floats:
+// the fast quantiser, with the exact fallback where it may round differently
+// (results equal qcode_exact for every weight).
 __device__ __forceinline__ void quantise8(const float (&w)[8], const QScale& qsc, float (&c)[8]) {
     bool redo = !qsc.fast;
 #pragma unroll
@@ -136,6 +153,21 @@ __device__ __forceinline__ void quantise8(const float (&w)[8], const QScale& qsc
 #pragma unroll
         for (int e = 0; e < 8; ++e) c[e] = qcode_exact(w[e], qsc.s);
     }
+}
+
+// 8 magic-float codes stored as fp16 patterns (16 bytes) or int8 (8 bytes).
+template <typename OutT>
+__device__ __forceinline__ void store_codes8(OutT* dst, const float (&c)[8]);
+
+template <>
+__device__ __forceinline__ void store_codes8<uint16_t>(uint16_t* dst, const float (&c)[8]) {
+    *reinterpret_cast<uint4*>(dst) = make_uint4(codes_to_f16x2(c[0], c[1]), codes_to_f16x2(c[2], c[3]),
+                                                codes_to_f16x2(c[4], c[5]), codes_to_f16x2(c[6], c[7]));
+}
+
+template <>
+__device__ __forceinline__ void store_codes8<int8_t>(int8_t* dst, const float (&c)[8]) {
+    *reinterpret_cast<uint2*>(dst) = make_uint2(codes_to_i8x4(c[0], c[1], c[2], c[3]), codes_to_i8x4(c[4], c[5], c[6], c[7]));
 }
 
 }  // namespace gdn

@@ -48,7 +48,7 @@ _SIGNATURES = {
     "gdn_prefill_batch": (c_int32, [_P, _P, _P, c_int32, _P, _P, _P, _P, _P, c_size_t, _P]),
     "gdn_decode_workspace_size": (c_size_t, [_P, c_int32]),
     "gdn_decode": (c_int32, [_P, _P, c_int32, _P, _P, _P, _P, c_size_t, _P]),
-    "gdn_gemv_codes": (c_int32, [_P, c_int32, c_int64, c_int64, _P, _P, c_int64, _P, c_int64, c_int64, _P, c_int64, _P]),
+    "gdn_decode_gemv": (c_int32, [_P, c_int32, c_int64, c_int64, _P, _P, c_int64, _P, c_int64, c_int64, _P, c_int64, _P]),
     "gdn_host_workspace_size": (c_size_t, [_P, c_int64]),
     "gdn_prefill_host": (c_int32, [_P, _P, c_int64, _P, _P, _P, _P, c_int64, _P, c_size_t, _P]),
     "gdn_sync_status": (c_int32, [_P]),

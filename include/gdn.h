@@ -224,13 +224,16 @@ int gdn_prefill_batch(const gdn_layer *layer, const void *x, const int64_t *cu_s
  *   layer->gate_log_a, gate_b   when given: device [n_seqs][Hv]
  *   workspace  device, 256-byte aligned, ws_bytes >= gdn_decode_workspace_size(
  *              layer, n_seqs)
- * The projections decode the Q4_K / Q6_K weight rows in registers and take
- * exact integer dot products with the tokens' int8 codes (no int8 weight copy
- * in memory): bit for bit the projections gdn_prefill computes for the same
- * tokens.  The conv is gdn_prefill's.  The recurrence takes the token in fp32
- * (S <- a S (I - b k k^T) + b v k^T, o = S q), not through the chunked
- * fp16-operand form, so o and the state agree with a prefill of the same
- * token within the recurrence tolerance, not bit for bit.
+ * The tokens are quantised to int8 rows as in gdn_prefill; the projections
+ * read the Q4_K / Q6_K weights once and take, per weight sub-block, integer
+ * dot products of the 4- or 6-bit codes with the tokens' codes, scaled by the
+ * sub-block's d*sc (and dmin*m) in fp32: the product of the int8 activations
+ * with the exactly decoded weights (no re-quantisation of the weights, unlike
+ * the prefill's int8 weight rows), within fp32 rounding.  The conv is
+ * gdn_prefill's.  The recurrence takes the token in fp32 (S <- a S (I - b k
+ * k^T) + b v k^T, o = S q), not through the chunked fp16-operand form.  So a
+ * decoded token agrees with a prefill of it within the stated tolerances, not
+ * bit for bit.
  * 1 <= n_seqs <= GDN_MAX_SEQS.  An out-of-range o is reported as GDN_ERANGE by
  * gdn_sync_status.
  */
@@ -239,17 +242,17 @@ int gdn_decode(const gdn_layer *layer, const void *x, int n_seqs, float *state, 
                void *workspace, size_t ws_bytes, void *stream);
 
 /*
- * gdn_gemv_codes -- the decode step's projection as its own call: out[t][r] =
- * ((float)sum_k codes(W)[r][k] * xc[t][k] * sx[t]) * s_w[r], W given as Q4_K
- * (q6k = 0) or Q6_K (q6k = 1) blocks [rows][cols/256], its codes and row scale
- * s_w those of gdn_q4k_deq_codes / gdn_q6k_deq_codes; xc: int8 codes of n
- * tokens as fp16 patterns [n][cols] (16-byte aligned), sx [n].  Rows r <
+ * gdn_decode_gemv -- the decode step's projection as its own call:
+ * out[t][r] = sx[t] * sum_k xc[t][k] * W[r][k], W the exactly decoded Q4_K
+ * (q6k = 0) or Q6_K (q6k = 1) rows [rows][cols/256 blocks] (16-byte aligned),
+ * xc the int8 codes of n tokens as fp16 patterns [n][cols] (16-byte aligned),
+ * sx [n]; integer dot products per weight sub-block, fp32 sums.  Rows r <
  * n_bf16 go to out_bf16[t*ld_bf16 + r] (bf16), the others to out_f32[t*ld_f32 +
  * r - n_bf16].  256 <= cols <= 16384, cols % 256 == 0, 1 <= n <= GDN_MAX_SEQS.
  */
-int gdn_gemv_codes(const void *blocks, int q6k, int64_t rows, int64_t cols, const uint16_t *xc, const float *sx,
-                   int64_t n, uint16_t *out_bf16, int64_t ld_bf16, int64_t n_bf16, float *out_f32, int64_t ld_f32,
-                   void *stream);
+int gdn_decode_gemv(const void *blocks, int q6k, int64_t rows, int64_t cols, const uint16_t *xc, const float *sx,
+                    int64_t n, uint16_t *out_bf16, int64_t ld_bf16, int64_t n_bf16, float *out_f32, int64_t ld_f32,
+                    void *stream);
 
 /*
  * gdn_prefill_host -- gdn_prefill fed from, and writing to, host memory: the

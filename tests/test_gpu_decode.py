@@ -1,15 +1,18 @@
 """The decode step (gdn_decode): one token per sequence, states and conv tails
 updated in place.
 
-* Its projection (weights decoded in registers, integer dot products) is
-  bit-exact against the oracle's int8 product, for Q4_K and Q6_K weights and
-  any number of tokens (several launches past 8).
+* Its projection (int8 activation rows against the exactly decoded Q4_K /
+  Q6_K weights, integer dot products per sub-block, fp32 sums) matches the
+  oracle's exact product within fp32 rounding (relative L2 1e-6 on fp32
+  outputs, one bf16 rounding on bf16 outputs), for any number of tokens
+  (several launches past 8).
 * One step on sequences with saved states matches the oracle's layer on that
-  token (y within 1e-2 relative L2, the int8-projection tolerance; the state
-  within 2e-3, the recurrence tolerance; the conv tail exactly).
-* A prefill followed by tokens decoded one at a time matches the oracle's
-  prefill of the whole prompt, and a batch of sequences decodes bit for bit
-  as each sequence alone.
+  token with the same projections (y within 1e-2 relative L2, the
+  int8-projection tolerance; the state within 2e-3, the recurrence tolerance;
+  the conv tail exactly).
+* A prefill followed by tokens decoded one at a time matches the oracle doing
+  the same, and a batch of sequences decodes bit for bit as each sequence
+  alone.
 """
 import numpy as np
 import pytest
@@ -36,31 +39,40 @@ def L():
 @pytest.mark.parametrize("fmt,rows,cols,n,n_bf16", [("q4k", 300, 1024, 1, 300), ("q4k", 1000, 4096, 8, 700),
                                                      ("q6k", 517, 2048, 9, 0), ("q6k", 64, 16384, 3, 40),
                                                      ("q4k", 12352, 4096, 1, 12288)])
-def test_gemv_codes_bit_exact(L, fmt, rows, cols, n, n_bf16):
+def test_decode_gemv_matches_oracle(L, fmt, rows, cols, n, n_bf16):
     rng = np.random.default_rng(rows + cols + n)
     w = rng.normal(0, 0.02, size=(rows, cols)).astype(np.float32)
     w[0] = 0.0
     blocks = (q6k.pack_q6k if fmt == "q6k" else q4k.pack_q4k)(w)
     wf = (q6k.unpack_q6k if fmt == "q6k" else q4k.unpack_q4k)(blocks, rows, cols)
-    qw, sw = quant.quant_rows_i8(wf)
     x = (rng.normal(0, 1, size=(n, cols)) * 10.0 ** rng.uniform(-2, 2, size=(n, 1))).astype(np.float32)
     qx, sx = quant.quant_rows_i8(x)
-    ref = quant.gemm_q8(qx, sx, qw, sw)                       # fp32 [n][rows]
+    ref = quant.matvec_exact_weights(qx, sx, wf)               # fp64 [n][rows]
     xc = torch.from_numpy(qx.astype(np.float16)).to(DEV)
     sxd = f32_dev(sx)
     b = torch.from_numpy(blocks).to(DEV)
     ob = torch.zeros(n, max(n_bf16, 1), dtype=torch.int16, device=DEV)
     of = torch.zeros(n, max(rows - n_bf16, 1), dtype=torch.float32, device=DEV)
-    L.gdn_gemv_codes(gl.ptr(b), int(fmt == "q6k"), rows, cols, gl.ptr(xc), gl.ptr(sxd), n, gl.ptr(ob), ob.shape[1],
-                     n_bf16, gl.ptr(of), of.shape[1], stream())
+    L.gdn_decode_gemv(gl.ptr(b), int(fmt == "q6k"), rows, cols, gl.ptr(xc), gl.ptr(sxd), n, gl.ptr(ob), ob.shape[1],
+                      n_bf16, gl.ptr(of), of.shape[1], stream())
     sync(L)
     if n_bf16:
-        want = quant.bf16_round(ref[:, :n_bf16]).astype(np.float32)
-        got = synth.bf16_bits_to_f32(ob.cpu().numpy().view(np.uint16)[:, :n_bf16])
-        assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+        # one bf16 rounding of an fp32 value within ~1e-6 of the exact sum: at most one bf16 step apart
+        got = synth.bf16_bits_to_f32(ob.cpu().numpy().view(np.uint16)[:, :n_bf16]).astype(np.float64)
+        want = ref[:, :n_bf16]
+        assert np.all(np.abs(got - want) <= 2.0 ** -8 * np.abs(want) + 1e-6 * np.abs(want).max())
+        assert rel_l2(got, want) <= 2.0 ** -8
     if rows > n_bf16:
-        assert np.array_equal(of.cpu().numpy()[:, : rows - n_bf16].view(np.uint32),
-                              ref[:, n_bf16:].astype(np.float32).view(np.uint32))
+        got = of.cpu().numpy()[:, : rows - n_bf16]
+        assert rel_l2(got, ref[:, n_bf16:]) <= 1e-6
+
+
+def _tail_close(got, want):
+    """Conv tails of decoded tokens: raw projection outputs rounded to bf16 from
+    an fp32 (GPU) or fp64 (oracle) sum can straddle a rounding boundary: one
+    bf16 step at most."""
+    want = np.asarray(want, np.float64)
+    return np.all(np.abs(np.asarray(got, np.float64) - want) <= 2.0 ** -7 * np.abs(want) + 1e-30)
 
 
 def _saved_states(spec, n, seed):
@@ -97,16 +109,20 @@ def test_decode_step_matches_oracle(name, n, gates, q6):
     for s in range(n):
         ref = OL.layer_forward(p, tok["x"][s:s + 1], S0=st0[s].astype(np.float64), conv_tail=cv0[s],
                                gate_log_a=tok["log_a"][s:s + 1] if gates else None,
-                               gate_b=tok["b"][s:s + 1] if gates else None)
+                               gate_b=tok["b"][s:s + 1] if gates else None, decode=True)
         assert rel_l2(yh[s:s + 1], ref["y"]) <= 1e-2, s
         assert rel_l2(state[s].cpu().numpy(), ref["state"]) <= 2e-3, s
         if q4:
-            assert np.array_equal(conv[s].cpu().numpy(), ref["conv_tail"].astype(np.float32)), s
+            c = conv[s].cpu().numpy()
+            assert np.array_equal(c[:, :2], cv0[s][:, 1:]), s          # the older inputs move up, exactly
+            assert _tail_close(c[:, 2], ref["conv_tail"][:, 2]), s
 
 
 def test_prefill_then_decode_matches_oracle_prefill():
     """Prefill 200 tokens, then decode 40 more one at a time on the same state
-    and conv tail: against the oracle's prefill of all 240."""
+    and conv tail: against the oracle doing the same (its prefill of the 200,
+    then its decode step per token), and within the recurrence tolerance of
+    the oracle's prefill of all 240."""
     spec = SMALL
     layer = synth.make_layer(spec)
     n0, m = 200, 40
@@ -125,11 +141,23 @@ def test_prefill_then_decode_matches_oracle_prefill():
                   gate_b=f32_dev(tok["b"][t:t + 1]))
         ys.append(y)
     sync(dl.lib)
-    ref = OL.layer_forward(oracle_params(spec, layer), tok["x"], gate_log_a=tok["log_a"], gate_b=tok["b"])
+    p = oracle_params(spec, layer)
+    r0 = OL.layer_forward(p, tok["x"][:n0], gate_log_a=tok["log_a"][:n0], gate_b=tok["b"][:n0])
+    S, tail, yr = r0["state"], r0["conv_tail"], []
+    for t in range(n0, n0 + m):
+        r = OL.layer_forward(p, tok["x"][t:t + 1], S0=S, conv_tail=tail, gate_log_a=tok["log_a"][t:t + 1],
+                             gate_b=tok["b"][t:t + 1], decode=True)
+        S, tail = r["state"], r["conv_tail"]
+        yr.append(r["y"])
     yd = bf16_host_f32(torch.cat(ys))
-    assert rel_l2(yd, ref["y"][n0:]) <= 1e-2
-    assert rel_l2(state.cpu().numpy(), ref["state"]) <= 2e-3
-    assert np.array_equal(conv.cpu().numpy(), ref["conv_tail"].astype(np.float32))
+    assert rel_l2(yd, np.concatenate(yr)) <= 1e-2
+    assert rel_l2(state.cpu().numpy(), S) <= 2e-3
+    assert _tail_close(conv.cpu().numpy(), tail)
+    # against the oracle's prefill of all 240 tokens: the decode projections use
+    # the exact weights where the prefill's use int8 weight rows (a half step
+    # of the row scale per weight), which moves this state by about 1%
+    full = OL.layer_forward(p, tok["x"], gate_log_a=tok["log_a"], gate_b=tok["b"])
+    assert rel_l2(state.cpu().numpy(), full["state"]) <= 3e-2
 
 
 def test_decode_batch_equals_each_sequence_alone():
