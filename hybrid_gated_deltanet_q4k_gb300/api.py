@@ -136,3 +136,13 @@ class DeviceLayer:
         return self.lib.gdn_decode(ctypes.byref(s), gl.ptr(x), x.shape[0], gl.ptr(state), gl.ptr(conv_state),
                                    gl.ptr(y), gl.ptr(workspace), workspace.numel(), gl.stream_handle(stream),
                                    check=check)
+
+    def prefill_ckpt(self, x: torch.Tensor, state_in, state_out, conv_state, y, workspace, ckpt_every: int,
+                     ckpt_state, ckpt_conv, gate_log_a=None, gate_b=None, stream=None, check=True) -> int:
+        """Enqueue gdn_prefill_ckpt: as prefill, plus snapshots of the state [N // every][Hv][dv][dk] and conv
+        state [N // every][C_conv][3] every ckpt_every tokens."""
+        s = self.struct(gate_log_a, gate_b)
+        return self.lib.gdn_prefill_ckpt(ctypes.byref(s), gl.ptr(x), x.shape[0], gl.ptr(state_in), gl.ptr(state_out),
+                                         gl.ptr(conv_state), gl.ptr(y), int(ckpt_every), gl.ptr(ckpt_state),
+                                         gl.ptr(ckpt_conv), gl.ptr(workspace), workspace.numel(),
+                                         gl.stream_handle(stream), check=check)

@@ -28,6 +28,16 @@ struct SeqTable {
     int unit[GDN_MAX_SEQS + 1];
 };
 
+// Recurrent-state snapshots taken during a prefill: after every `every_chunks`
+// chunks (counted from the start of the prompt, of which this call's first
+// chunk is number chunk_base), the state S goes to
+// state[(chunks done) / every_chunks - 1], each [Hv][dv][dk] fp32.
+struct DeltaCkpt {
+    float* state;
+    int every_chunks;
+    int chunk_base;
+};
+
 // The sequence holding work unit u: the last s with unit[s] <= u (an empty
 // sequence owns no unit, so it is passed over).
 __device__ __forceinline__ int seq_of_unit(const SeqTable& t, int u) {

@@ -36,7 +36,8 @@ cudaError_t launch_conv_state(const gdn_layer&, const uint16_t*, int64_t, int64_
                               const int64_t* cu_seqlens = nullptr, int n_seqs = 1);
 cudaError_t launch_delta(const gdn_layer&, const uint16_t*, const float*, const float*, int64_t, const float*, float*,
                          uint16_t*, void*, cudaStream_t, bool overlap, const TokenRangeHook* after_state,
-                         const int64_t* cu_seqlens = nullptr, int n_seqs = 1);
+                         const int64_t* cu_seqlens = nullptr, int n_seqs = 1, const DeltaCkpt* ckpt = nullptr);
+cudaError_t launch_conv_ckpt(const gdn_layer&, const uint16_t*, int64_t, int64_t, int64_t, int64_t, float*, cudaStream_t);
 size_t delta_scratch_bytes(int hv, int hk, int d, int64_t n);
 cudaError_t launch_gated_norm(const gdn_layer&, const uint16_t*, const uint16_t*, int64_t, int64_t, uint16_t*, float*,
                               float*, cudaStream_t);
@@ -182,9 +183,19 @@ Workspace carve(const gdn_layer* L, const Sizes& s, int64_t B, void* base, int64
 // [nb][H], the state read from st_in and written to state_out, the conv tail
 // carried in place.  gla / gb: this pass's drawn gates (device [nb][hv]) or
 // NULL.  The weight codes in w must already be decoded.
+// Snapshots of a prefill with checkpoints: every `every` tokens (a multiple
+// of GDN_CHUNK) of the prompt, the state and the conv state.
+struct Ckpt {
+    int64_t every;
+    float* state;   // [n/every][hv][d][d]
+    float* conv;    // [n/every][c_conv][3]
+};
+
+// u0: the pass's first token within the prompt (for the snapshots; a
+// multiple of GDN_CHUNK when ck is given).
 int run_pass(const gdn_layer* layer, const Sizes& s, const Workspace& w, const void* x, int64_t nb, const float* gla,
              const float* gb, const float* st_in, float* state_out, float* conv_state, void* y, bool first,
-             cudaStream_t st) {
+             cudaStream_t st, const Ckpt* ck = nullptr, int64_t u0 = 0) {
     const bool q4k = layer->wtype == GDN_W_Q4K;
     if (q4k) {
         GDN_LAUNCH(launch_quant_rows(static_cast<const uint16_t*>(x), nb, s.H, w.xc, w.sx, st), "quantise x");
@@ -204,6 +215,7 @@ int run_pass(const gdn_layer* layer, const Sizes& s, const Workspace& w, const v
     lu.gate_b = gb;
     GDN_LAUNCH(launch_conv(lu, w.qkvz, s.n_bf16, nb, conv_state, w.ba, 2 * s.hv, w.qkv, w.log_a, w.b, st), "conv");
     GDN_LAUNCH(launch_conv_state(lu, w.qkvz, s.n_bf16, nb, conv_state, st), "conv state");
+    if (ck) GDN_LAUNCH(launch_conv_ckpt(lu, w.qkvz, s.n_bf16, u0, nb, ck->every, ck->conv, st), "conv-state snapshots");
     GDN_LAUNCH(mark(4, first, st), "stage event");
     const float* la = gla ? gla : w.log_a;
     const float* bb = gb ? gb : w.b;
@@ -215,7 +227,10 @@ int run_pass(const gdn_layer* layer, const Sizes& s, const Workspace& w, const v
                                  w.oc ? w.oc + t0 * s.c_v : nullptr, w.so ? w.so + t0 : nullptr,
                                  w.ohat ? w.ohat + t0 * s.c_v : nullptr, cs);
     };
-    GDN_LAUNCH(launch_delta(lu, w.qkv, la, bb, nb, st_in, state_out, w.o, w.delta, st, true, &norm_hook),
+    const DeltaCkpt dck{ck ? ck->state : nullptr, ck ? static_cast<int>(ck->every / GDN_CHUNK) : 1,
+                        static_cast<int>(u0 / GDN_CHUNK)};
+    GDN_LAUNCH(launch_delta(lu, w.qkv, la, bb, nb, st_in, state_out, w.o, w.delta, st, true, &norm_hook, nullptr, 1,
+                            ck ? &dck : nullptr),
                "delta rule and gated norm");
     GDN_LAUNCH(mark(5, first, st), "stage event");
     GDN_LAUNCH(mark(6, first, st), "stage event");
@@ -493,8 +508,8 @@ size_t gdn_workspace_size(const gdn_layer* layer, int64_t ubatch_tokens) {
     return carve(layer, s, ubatch_tokens, nullptr).total;
 }
 
-int gdn_prefill(const gdn_layer* layer, const void* x, int64_t n_tokens, const float* state_in, float* state_out,
-                float* conv_state, void* y, void* workspace, size_t ws_bytes, void* stream) {
+static int prefill_impl(const gdn_layer* layer, const void* x, int64_t n_tokens, const float* state_in, float* state_out,
+                        float* conv_state, void* y, void* workspace, size_t ws_bytes, void* stream, const Ckpt* ck) {
     Sizes s;
     int r = check_layer(layer, &s);
     if (r) return r;
@@ -507,6 +522,9 @@ int gdn_prefill(const gdn_layer* layer, const void* x, int64_t n_tokens, const f
     if (B < 1)
         return fail(GDN_ENOMEM, "gdn_prefill: workspace %zu B < %zu B needed for one token", ws_bytes,
                     carve(layer, s, 1, nullptr).total);
+    if (ck && B < n_tokens && B % GDN_CHUNK)
+        return fail(GDN_ENOMEM, "gdn_prefill_ckpt: with snapshots the workspace must hold %d tokens or all of them",
+                    GDN_CHUNK);
     Workspace w = carve(layer, s, B, workspace);
     const bool q4k = layer->wtype == GDN_W_Q4K;
     GDN_LAUNCH(mark(0, true, st), "stage event");
@@ -519,10 +537,29 @@ int gdn_prefill(const gdn_layer* layer, const void* x, int64_t n_tokens, const f
         const float* gb = layer->gate_b ? layer->gate_b + u0 * s.hv : nullptr;
         r = run_pass(layer, s, w, static_cast<const uint8_t*>(x) + u0 * s.H * esz, nb, gla, gb,
                      u0 == 0 ? state_in : state_out, state_out, conv_state, static_cast<uint8_t*>(y) + u0 * s.H * esz,
-                     u0 == 0, st);
+                     u0 == 0, st, ck, u0);
         if (r) return r;
     }
     return GDN_OK;
+}
+
+int gdn_prefill(const gdn_layer* layer, const void* x, int64_t n_tokens, const float* state_in, float* state_out,
+                float* conv_state, void* y, void* workspace, size_t ws_bytes, void* stream) {
+    return prefill_impl(layer, x, n_tokens, state_in, state_out, conv_state, y, workspace, ws_bytes, stream, nullptr);
+}
+
+int gdn_prefill_ckpt(const gdn_layer* layer, const void* x, int64_t n_tokens, const float* state_in, float* state_out,
+                     float* conv_state, void* y, int64_t ckpt_every, float* ckpt_state, float* ckpt_conv,
+                     void* workspace, size_t ws_bytes, void* stream) {
+    if (ckpt_every < GDN_CHUNK || ckpt_every % GDN_CHUNK)
+        return fail(GDN_EINVAL, "gdn_prefill_ckpt: ckpt_every must be a positive multiple of %d (got %lld)", GDN_CHUNK,
+                    (long long)ckpt_every);
+    if (n_tokens >= ckpt_every && (!ckpt_state || !ckpt_conv)) return fail(GDN_EINVAL, "gdn_prefill_ckpt: NULL snapshot buffer");
+    if ((ckpt_state && !aligned(ckpt_state, 16)) || (ckpt_conv && !aligned(ckpt_conv, 4)))
+        return fail(GDN_EINVAL, "gdn_prefill_ckpt: snapshot buffers misaligned");
+    const Ckpt ck{ckpt_every, ckpt_state, ckpt_conv};
+    return prefill_impl(layer, x, n_tokens, state_in, state_out, conv_state, y, workspace, ws_bytes, stream,
+                        n_tokens >= ckpt_every ? &ck : nullptr);
 }
 
 size_t gdn_host_workspace_size(const gdn_layer* layer, int64_t pass_tokens) {

@@ -251,6 +251,31 @@ cudaError_t launch_conv_state(const gdn_layer& L, const uint16_t* qkvz, int64_t 
     return cudaGetLastError();
 }
 
+// Conv-state snapshots of a prefill pass whose first token is number t0 of
+// the prompt (t0 a multiple of 64): for every position p = k * every with t0 <
+// p <= t0 + n (every a multiple of 64), snapshot k - 1 gets the raw inputs of
+// tokens p-3, p-2, p-1 per channel, oldest first -- the conv state a prefill
+// of the first p tokens leaves.  They lie in this pass (p - t0 >= 64).
+__global__ void conv_ckpt_kernel(const uint16_t* __restrict__ qkvz, int64_t ld, int c_conv, int64_t t0, int64_t every,
+                                 float* __restrict__ ckpt) {
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= c_conv) return;
+    const int64_t k = t0 / every + 1 + blockIdx.y, p = k * every;
+    float* dst = ckpt + (k - 1) * c_conv * 3 + static_cast<int64_t>(c) * 3;
+#pragma unroll
+    for (int j = 0; j < 3; ++j) dst[j] = bf16_bits_to_float(qkvz[(p - 3 + j - t0) * ld + c]);
+}
+
+cudaError_t launch_conv_ckpt(const gdn_layer& L, const uint16_t* qkvz, int64_t ld, int64_t t0, int64_t n, int64_t every,
+                             float* ckpt, cudaStream_t st) {
+    const int c_conv = 2 * L.n_qk_heads * L.dk + L.n_v_heads * L.dv;
+    const int64_t first = t0 / every + 1, last = (t0 + n) / every;   // snapshots k in [first, last]
+    if (last < first) return cudaSuccess;
+    conv_ckpt_kernel<<<dim3((c_conv + 255) / 256, static_cast<unsigned>(last - first + 1)), 256, 0, st>>>(
+        qkvz, ld, c_conv, t0, every, ckpt);
+    return cudaGetLastError();
+}
+
 int read_and_clear_conv_error() {
     int v = 0, z = 0;
     cudaMemcpyFromSymbol(&v, g_conv_error, sizeof(int));

@@ -76,6 +76,7 @@ struct DeltaArgs {
     const float* state_in;  // [hv][D][D] or null
     float* state_out;
     uint16_t* o;   // [n][c_v] fp16
+    DeltaCkpt ckpt;  // state snapshots (ckpt.state null: none); one sequence only
 };
 
 __device__ __forceinline__ uint16_t f16_bits(float x) { return __half_as_ushort(__float2half_rn(x)); }
@@ -798,6 +799,13 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a, con
 #pragma unroll
                 for (int v = 0; v < 16; ++v) S[v] = fmaf(dec, S[v], u[v]);
                 write_s();
+                // a snapshot of the state after a whole chunk that ends on a multiple of the interval
+                const int done = a.ckpt.chunk_base + a.chunk0 + j + 1;
+                if (a.ckpt.state && own_d && tc + DC <= t_end && done % a.ckpt.every_chunks == 0) {
+                    float* cp = a.ckpt.state + static_cast<int64_t>(done / a.ckpt.every_chunks - 1) * a.hv * D * D;
+#pragma unroll
+                    for (int v = 0; v < 16; ++v) cp[(static_cast<int64_t>(h) * D + i0 + v0 + v) * D + d] = S[v];
+                }
             }
             if (j + 1 < nch) handover(NB_S);
 
@@ -978,7 +986,8 @@ static cudaError_t launch_delta_d(DeltaArgs& a, const SeqTable& sq, cudaStream_t
 
 cudaError_t launch_delta(const gdn_layer& L, const uint16_t* qkv, const float* log_a, const float* b, int64_t n,
                          const float* state_in, float* state_out, uint16_t* o, void* scratch, cudaStream_t st,
-                         bool overlap, const TokenRangeHook* after_state, const int64_t* cu_seqlens, int n_seqs) {
+                         bool overlap, const TokenRangeHook* after_state, const int64_t* cu_seqlens, int n_seqs,
+                         const DeltaCkpt* ckpt) {
     DeltaArgs a;
     const int d = L.dk;
     // the call's sequences (host token offsets; null: one sequence of n tokens),
@@ -1003,6 +1012,7 @@ cudaError_t launch_delta(const gdn_layer& L, const uint16_t* qkv, const float* l
     a.state_in = state_in;
     a.state_out = state_out;
     a.o = o;
+    a.ckpt = ckpt && !cu_seqlens ? *ckpt : DeltaCkpt{nullptr, 1, 0};
     return d == 128 ? launch_delta_d<128>(a, sq, st, overlap, after_state)
                     : launch_delta_d<64>(a, sq, st, overlap, after_state);
 }

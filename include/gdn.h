@@ -289,6 +289,28 @@ int gdn_prefill_host(const gdn_layer *layer, const void *x_host, int64_t n_token
                      size_t ws_bytes, void *stream);
 
 /*
+ * gdn_prefill_ckpt -- gdn_prefill that also keeps recurrent-state checkpoints:
+ * every ckpt_every tokens of the prompt, the state and conv state a prefill
+ * of that prefix would leave, so that a later prompt sharing the prefix (a
+ * second turn, a retried request) resumes from it instead of prefilling it
+ * again ("Qwen3.5 on CPU prefills one token at a time" #5475: a prompt that
+ * extends the held tokens prefills only the suffix, and the same page's "Not
+ * in scope here" names cross-request reuse of the state as its own issue).
+ *   ckpt_every  a positive multiple of GDN_CHUNK
+ *   ckpt_state  fp32 [N / ckpt_every][Hv][dv][dk]: snapshot k holds S after
+ *               token (k+1)*ckpt_every - 1
+ *   ckpt_conv   fp32 [N / ckpt_every][C_conv][3]: the conv state at the same
+ *               point (raw inputs of tokens p-3, p-2, p-1, p = (k+1)*ckpt_every)
+ * Both may be NULL when N < ckpt_every.  Snapshots are bitwise the state_out and
+ * conv_state of gdn_prefill over that prefix (the same chunks, the same
+ * arithmetic).  Other arguments as gdn_prefill; the workspace must hold at
+ * least GDN_CHUNK tokens unless it holds all N.
+ */
+int gdn_prefill_ckpt(const gdn_layer *layer, const void *x, int64_t n_tokens, const float *state_in, float *state_out,
+                     float *conv_state, void *y, int64_t ckpt_every, float *ckpt_state, float *ckpt_conv,
+                     void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * gdn_sync_status -- wait for `stream`, then report (and clear) the device
  * error words the kernels set: GDN_OK, GDN_ETIMEOUT (a bounded wait ran out),
  * GDN_ERANGE (a value beyond the fp16 operand range of the recurrence: the
