@@ -26,6 +26,7 @@ cudaError_t launch_q6k_deq_codes(const void*, int64_t, int64_t, uint16_t*, float
 cudaError_t launch_q4k_deq_codes2(const void*, int64_t, int64_t, uint16_t*, float*, const void*, int64_t, int64_t,
                                   uint16_t*, float*, cudaStream_t);
 cudaError_t launch_quant_rows(const uint16_t*, int64_t, int64_t, uint16_t*, float*, cudaStream_t);
+cudaError_t launch_quant_rows_f32(const float*, int64_t, int64_t, uint16_t*, float*, cudaStream_t);
 cudaError_t launch_gemm_codes(const uint16_t*, const float*, const uint16_t*, const float*, int64_t, int64_t, int64_t,
                               uint16_t*, int64_t, int64_t, float*, int64_t, cudaStream_t);
 cudaError_t launch_gemm_f32(const float*, const float*, int64_t, int64_t, int64_t, uint16_t*, int64_t, int64_t, float*,
@@ -42,9 +43,11 @@ size_t delta_scratch_bytes(int hv, int hk, int d, int64_t n);
 cudaError_t launch_gated_norm(const gdn_layer&, const uint16_t*, const uint16_t*, int64_t, int64_t, uint16_t*, float*,
                               float*, cudaStream_t);
 cudaError_t launch_gemv_dot(const void*, bool, int64_t, int64_t, const uint16_t*, const float*, int64_t, uint16_t*,
-                              int64_t, int64_t, float*, int64_t, cudaStream_t);
-cudaError_t launch_decode_rule(const gdn_layer&, const uint16_t*, const float*, const float*, int64_t, float*, uint16_t*,
-                               cudaStream_t);
+                              int64_t, int64_t, float*, int64_t, cudaStream_t, int in_mode = 0, const void* xraw = nullptr,
+                              float* cs_state = nullptr, const uint16_t* cs_qkvz = nullptr, int64_t cs_ld = 0,
+                              int cs_c_conv = 0, int cs_n = 0);
+cudaError_t launch_decode_mid(const gdn_layer&, const uint16_t*, int64_t, const float*, int64_t, const float*, int64_t,
+                              float*, float*, cudaStream_t);
 int read_and_clear_decode_error();
 int read_and_clear_gemm_error();
 int read_and_clear_delta_error();
@@ -294,13 +297,10 @@ size_t host_stage_bytes(const gdn_layer* L, const Sizes& s, int64_t B) {
 
 // Workspace of one decode step of B tokens (one per sequence).
 struct DecodeWs {
-    uint16_t* xc; float* sx;          // x codes [B][H], scales [B]         (Q4_K)
     uint16_t* qkvz; float* ba;        // projection [B][n_bf16] bf16, [B][2 hv] fp32
-    uint16_t* qkv;                    // conv output [B][c_conv] fp16
-    float* log_a; float* b;           // gates [B][hv]
-    uint16_t* o;                      // recurrence output [B][c_v] fp16
-    uint16_t* oc; float* so;          // gated-norm codes [B][c_v], scales [B] (Q4_K)
-    float* ohat;                      // gated-norm output [B][c_v]          (F32)
+    float* ohat;                      // gated-norm output [B][c_v] fp32
+    uint16_t* xc; float* sx;          // codes of x [B][H] and of o_hat [B][c_v], with row scales,
+    uint16_t* oc; float* so;          // when B > GDN_DECODE_GEMV_TOKENS (quantised once, not per CTA)
     size_t total;
 };
 
@@ -313,20 +313,15 @@ DecodeWs carve_decode(const gdn_layer* L, const Sizes& s, int64_t B, void* base)
         off += up256(bytes);
         return r;
     };
-    if (L->wtype == GDN_W_Q4K) {
+    w.qkvz = static_cast<uint16_t*>(take(B * s.n_bf16 * 2));
+    w.ba = static_cast<float*>(take(B * 2 * s.hv * 4));
+    w.ohat = static_cast<float*>(take(B * s.c_v * 4));
+    if (L->wtype == GDN_W_Q4K && B > GDN_DECODE_GEMV_TOKENS) {
         w.xc = static_cast<uint16_t*>(take(B * s.H * 2));
         w.sx = static_cast<float*>(take(B * 4));
         w.oc = static_cast<uint16_t*>(take(B * s.c_v * 2));
         w.so = static_cast<float*>(take(B * 4));
-    } else {
-        w.ohat = static_cast<float*>(take(B * s.c_v * 4));
     }
-    w.qkvz = static_cast<uint16_t*>(take(B * s.n_bf16 * 2));
-    w.ba = static_cast<float*>(take(B * 2 * s.hv * 4));
-    w.qkv = static_cast<uint16_t*>(take(B * s.c_conv * 2));
-    w.log_a = static_cast<float*>(take(B * s.hv * 4));
-    w.b = static_cast<float*>(take(B * s.hv * 4));
-    w.o = static_cast<uint16_t*>(take(B * s.c_v * 2));
     w.total = off;
     return w;
 }
@@ -790,37 +785,45 @@ int gdn_decode(const gdn_layer* layer, const void* x, int n_seqs, float* state, 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const bool q4k = layer->wtype == GDN_W_Q4K;
     const int64_t B = n_seqs;
-    // steps 1b, 1c: int8 codes of the tokens, then the weight rows decoded in
-    // registers against them
-    if (q4k) {
+    // K1, steps 1b + 1c: each CTA quantises the tokens to int8 rows, then
+    // reads the weight rows once (Q4_K layers); F32 layers: plain product
+    // (more tokens than one projection launch takes: quantised once beforehand)
+    const bool once = B > GDN_DECODE_GEMV_TOKENS;
+    if (q4k && once) {
         GDN_LAUNCH(launch_quant_rows(static_cast<const uint16_t*>(x), B, s.H, w.xc, w.sx, st), "decode: quantise x");
         GDN_LAUNCH(launch_gemv_dot(layer->w_in, layer->q6k_mask & 1, s.r_in, s.H, w.xc, w.sx, B, w.qkvz, s.n_bf16,
-                                     s.n_bf16, w.ba, 2 * s.hv, st),
+                                   s.n_bf16, w.ba, 2 * s.hv, st),
+                   "decode: input projection");
+    } else if (q4k) {
+        GDN_LAUNCH(launch_gemv_dot(layer->w_in, layer->q6k_mask & 1, s.r_in, s.H, nullptr, nullptr, B, w.qkvz, s.n_bf16,
+                                   s.n_bf16, w.ba, 2 * s.hv, st, 1, x),
                    "decode: input projection");
     } else {
         GDN_LAUNCH(launch_gemm_f32(static_cast<const float*>(x), static_cast<const float*>(layer->w_in), B, s.r_in, s.H,
                                    w.qkvz, s.n_bf16, s.n_bf16, w.ba, 2 * s.hv, st),
                    "decode: input projection");
     }
-    // step 2: every token is a one-token sequence with its own conv tail
-    std::vector<int64_t> cu(static_cast<size_t>(B) + 1);
-    for (int64_t i = 0; i <= B; ++i) cu[static_cast<size_t>(i)] = i;
-    GDN_LAUNCH(launch_conv(*layer, w.qkvz, s.n_bf16, B, conv_state, w.ba, 2 * s.hv, w.qkv, w.log_a, w.b, st, cu.data(),
-                           n_seqs),
-               "decode: conv");
-    GDN_LAUNCH(launch_conv_state(*layer, w.qkvz, s.n_bf16, B, conv_state, st, cu.data(), n_seqs), "decode: conv state");
-    // step 3: one token of the recurrence per sequence, in fp32
-    const float* la = layer->gate_log_a ? layer->gate_log_a : w.log_a;
-    const float* bb = layer->gate_b ? layer->gate_b : w.b;
-    GDN_LAUNCH(launch_decode_rule(*layer, w.qkv, la, bb, B, state, w.o, st), "decode: recurrence");
-    // steps 4, 5
-    GDN_LAUNCH(launch_gated_norm(*layer, w.o, w.qkvz + s.c_conv, s.n_bf16, B, w.oc, w.so, w.ohat, st),
-               "decode: gated norm");
-    if (q4k) {
+    // K2, steps 2-4 per (value head, sequence): conv, norms, gates, one token of
+    // the recurrence, gated RMSNorm -> o_hat (fp32)
+    GDN_LAUNCH(launch_decode_mid(*layer, w.qkvz, s.n_bf16, w.ba, 2 * s.hv, conv_state, B, state, w.ohat, st),
+               "decode: conv, recurrence and gated norm");
+    // K3, step 5: the conv tails move up by one token, o_hat is quantised to
+    // int8 rows in each CTA and meets the output weights (Q4_K layers)
+    if (q4k && once) {
+        GDN_LAUNCH(launch_quant_rows_f32(w.ohat, B, s.c_v, w.oc, w.so, st), "decode: quantise o_hat");
         GDN_LAUNCH(launch_gemv_dot(layer->w_out, layer->q6k_mask & 2, s.H, s.c_v, w.oc, w.so, B,
-                                     static_cast<uint16_t*>(y), s.H, s.H, nullptr, 0, st),
-                   "decode: output projection");
+                                   static_cast<uint16_t*>(y), s.H, s.H, nullptr, 0, st, 0, nullptr, conv_state, w.qkvz,
+                                   s.n_bf16, static_cast<int>(s.c_conv), n_seqs),
+                   "decode: conv state and output projection");
+    } else if (q4k) {
+        GDN_LAUNCH(launch_gemv_dot(layer->w_out, layer->q6k_mask & 2, s.H, s.c_v, nullptr, nullptr, B,
+                                   static_cast<uint16_t*>(y), s.H, s.H, nullptr, 0, st, 2, w.ohat, conv_state, w.qkvz,
+                                   s.n_bf16, static_cast<int>(s.c_conv), n_seqs),
+                   "decode: conv state and output projection");
     } else {
+        std::vector<int64_t> cu(static_cast<size_t>(B) + 1);
+        for (int64_t i = 0; i <= B; ++i) cu[static_cast<size_t>(i)] = i;
+        GDN_LAUNCH(launch_conv_state(*layer, w.qkvz, s.n_bf16, B, conv_state, st, cu.data(), n_seqs), "decode: conv state");
         GDN_LAUNCH(launch_gemm_f32(w.ohat, static_cast<const float*>(layer->w_out), B, s.H, s.c_v, nullptr, 0, 0,
                                    static_cast<float*>(y), s.H, st),
                    "decode: output projection");

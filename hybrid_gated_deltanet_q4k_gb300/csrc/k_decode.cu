@@ -59,7 +59,41 @@ struct GemvArgs {
     int n_bf16;
     float* out_f32;          // r >= n_bf16: at t * ld_f32 + r - n_bf16
     int64_t ld_f32;
+    // in_mode 0: xc / sx hold the tokens' int8 codes and scales.  1, 2: xraw
+    // holds the tokens' rows [g][cols] in bf16 (1) or fp32 (2), quantised here
+    // per row exactly as step 1b does (scale amax/127, the same codes).
+    int in_mode;
+    const void* xraw;
+    // optional (cs_state non-null): shift the conv tails of cs_n sequences by
+    // one token, [x_{t-2}, x_{t-1}, x_t] from the raw projection row cs_qkvz
+    float* cs_state;         // [cs_n][cs_c_conv][3]
+    const uint16_t* cs_qkvz; // [cs_n][cs_ld] bf16
+    int64_t cs_ld;
+    int cs_c_conv, cs_n;
 };
+
+// Elements 16b .. 16b+15 of raw input row t as floats.
+__device__ __forceinline__ void gemv_raw16(const GemvArgs& a, int t, int b, float (&w)[16]) {
+    if (a.in_mode == 1) {
+        const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.xraw) +
+                                                        static_cast<int64_t>(t) * a.cols + 16 * b);
+        const uint4 u0 = __ldg(p), u1 = __ldg(p + 1);
+        const uint32_t u[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            w[2 * e] = __uint_as_float(u[e] << 16);
+            w[2 * e + 1] = __uint_as_float(u[e] & 0xffff0000u);
+        }
+    } else {
+        const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(a.xraw) +
+                                                          static_cast<int64_t>(t) * a.cols + 16 * b);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float4 v = __ldg(p + e);
+            w[4 * e] = v.x; w[4 * e + 1] = v.y; w[4 * e + 2] = v.z; w[4 * e + 3] = v.w;
+        }
+    }
+}
 
 // Shared memory: the tokens' codes (g * cols bytes), their sums over blocks
 // of 16 (g * cols/16 ints), then `stages` tiles of GEMV_WARPS weight rows,
@@ -153,9 +187,68 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_dot_kernel(GemvArgs a) {
         mbar_init_fence();
         for (int i = 0; i < a.stages; ++i) gemv_issue(a, ring, full, blockIdx.x + i * gridDim.x, i);
     }
+    static_assert(GEMV_TOKENS <= GEMV_WARPS, "one warp quantises each token");
+    __shared__ float sxs[GEMV_TOKENS], wmax[GEMV_WARPS];
+    if (a.cs_state) {
+        // conv tails move up by one token (the readers of the old tails have finished)
+        const int64_t total = static_cast<int64_t>(a.cs_n) * a.cs_c_conv;
+        for (int64_t i = static_cast<int64_t>(blockIdx.x) * GEMV_THREADS + tid; i < total;
+             i += static_cast<int64_t>(gridDim.x) * GEMV_THREADS) {
+            const int64_t sq = i / a.cs_c_conv, c = i - sq * a.cs_c_conv;
+            float* t3 = a.cs_state + i * 3;
+            const float x1 = t3[1], x2 = t3[2];
+            t3[0] = x1;
+            t3[1] = x2;
+            t3[2] = bf16_bits_to_float(a.cs_qkvz[sq * a.cs_ld + c]);
+        }
+    }
     // the tokens' codes as packed int8, and their sums over every 16 codes
     const int kw = a.cols >> 2, k16 = a.cols >> 4;
-    for (int i = tid; i < a.g * k16; i += GEMV_THREADS) {
+    if (a.in_mode != 0) {
+        // the warps split evenly over the tokens (wpt warps each): the row
+        // amax (warp maxima combined through shared memory), then the codes
+        const int wpt = GEMV_WARPS / a.g, t = warp / wpt, gl = (warp - t * wpt) * 32 + lane, gs = wpt * 32;
+        float amax = 0.0f;
+        if (t < a.g) {
+            for (int b = gl; b < k16; b += gs) {
+                float w[16];
+                gemv_raw16(a, t, b, w);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fabsf(w[e]));
+            }
+        }
+        amax = warp_max(amax);
+        if (lane == 0) wmax[warp] = amax;
+        __syncthreads();
+        if (t < a.g) {
+            amax = 0.0f;
+            for (int w = 0; w < wpt; ++w) amax = fmaxf(amax, wmax[t * wpt + w]);
+            const QScale qsc = make_qscale(amax);
+            if (gl == 0) sxs[t] = qsc.s;
+            for (int b = gl; b < k16; b += gs) {
+                float w[16], c[16];
+                gemv_raw16(a, t, b, w);
+                bool redo = !qsc.fast;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) c[e] = qcode_fast(w[e], qsc, redo);
+                if (redo) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) c[e] = qcode_exact(w[e], qsc.s);
+                }
+                int sum = 0;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t packed = codes_to_i8x4(c[4 * q], c[4 * q + 1], c[4 * q + 2], c[4 * q + 3]);
+                    xs[t * kw + 4 * b + q] = packed;
+                    sum = __dp4a(static_cast<int>(packed), 0x01010101, sum);
+                }
+                xsum[t * k16 + b] = sum;
+            }
+        }
+    } else {
+        if (tid < a.g) sxs[tid] = a.sx[tid];
+    }
+    for (int i = tid; a.in_mode == 0 && i < a.g * k16; i += GEMV_THREADS) {
         const int t = i / k16, b = i - t * k16;
         const uint4 h0 = __ldg(reinterpret_cast<const uint4*>(a.xc + static_cast<int64_t>(t) * a.cols + 16 * b));
         const uint4 h1 = __ldg(reinterpret_cast<const uint4*>(a.xc + static_cast<int64_t>(t) * a.cols + 16 * b + 8));
@@ -223,7 +316,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_dot_kernel(GemvArgs a) {
                 }
             }
             if (lane < a.g) {
-                const float y = mine * a.sx[lane];
+                const float y = mine * sxs[lane];
                 if (row < a.n_bf16)
                     a.out_bf16[lane * a.ld_bf16 + row] = float_to_bf16_bits(y);
                 else
@@ -248,14 +341,22 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_dot_kernel(GemvArgs a) {
 // GEMV_TOKENS (fewer when a token's codes and the tiles would not fit shared
 // memory); W in Q4_K (q6k false) or Q6_K.  A persistent grid of at most two
 // CTAs per SM walks the tiles.
+// in_mode 1 / 2: the tokens come as raw bf16 / fp32 rows xraw [n][cols] and
+// are quantised in each CTA (xc, sx unused).  cs_state non-null: the first
+// launch also shifts the conv tails of cs_n sequences (see GemvArgs).
 cudaError_t launch_gemv_dot(const void* blocks, bool q6k, int64_t rows, int64_t cols, const uint16_t* xc,
                               const float* sx, int64_t n, uint16_t* out_bf16, int64_t ld_bf16, int64_t n_bf16,
-                              float* out_f32, int64_t ld_f32, cudaStream_t st) {
+                              float* out_f32, int64_t ld_f32, cudaStream_t st, int in_mode, const void* xraw,
+                              float* cs_state, const uint16_t* cs_qkvz, int64_t cs_ld, int cs_c_conv, int cs_n) {
     static int sms = 0, max_optin = 0;
     if (!sms) {
         int dev = 0;
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        // dynamic shared memory: the opt-in maximum less the kernels' static arrays
+        cudaFuncAttributes fa{};
+        cudaFuncGetAttributes(&fa, gemv_dot_kernel<true>);
+        max_optin -= static_cast<int>(fa.sharedSizeBytes);
         cudaFuncSetAttribute(gemv_dot_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_optin);
         cudaFuncSetAttribute(gemv_dot_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_optin);
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -275,8 +376,15 @@ cudaError_t launch_gemv_dot(const void* blocks, bool q6k, int64_t rows, int64_t 
         a.row_bytes = row_bytes;
         a.ntiles = ntiles;
         a.total_bytes = rows * row_bytes;
-        a.xc = xc + t0 * cols;
-        a.sx = sx + t0;
+        a.xc = xc ? xc + t0 * cols : nullptr;
+        a.sx = sx ? sx + t0 : nullptr;
+        a.in_mode = in_mode;
+        a.xraw = xraw ? static_cast<const uint8_t*>(xraw) + t0 * cols * (in_mode == 1 ? 2 : 4) : nullptr;
+        a.cs_state = t0 == 0 ? cs_state : nullptr;
+        a.cs_qkvz = cs_qkvz;
+        a.cs_ld = cs_ld;
+        a.cs_c_conv = cs_c_conv;
+        a.cs_n = cs_n;
         a.g = static_cast<int>(n - t0 < gmax ? n - t0 : gmax);
         a.out_bf16 = out_bf16 ? out_bf16 + t0 * ld_bf16 : nullptr;
         a.ld_bf16 = ld_bf16;
@@ -301,94 +409,177 @@ cudaError_t launch_gemv_dot(const void* blocks, bool q6k, int64_t rows, int64_t 
     return cudaSuccess;
 }
 
-// ------------------------------------------------------------ recurrence
+// ------------------------------------------------------------ conv, recurrence, gated norm
 
-struct DecodeArgs {
-    const uint16_t* qkv;   // [B][c_conv] fp16: q | k | v
-    const float* log_a;    // [B][hv]
-    const float* b;        // [B][hv]
-    float* state;          // [B][hv][D][D], in place
-    uint16_t* o;           // [B][c_v] fp16
+struct MidArgs {
+    const uint16_t* qkvz;    // [B][ld] bf16 projection: q | k | v | z
+    int64_t ld;
+    const float* ba;         // [B][ld_ba] fp32 beta | alpha (gates from the projection)
+    int64_t ld_ba;
+    const float* gate_log_a; // [B][hv] drawn gates, or null
+    const float* gate_b;
+    const float* conv_w;     // [c_conv][4]
+    const float* conv_state; // [B][c_conv][3], read only here
+    const float* A_log;
+    const float* dt_bias;
+    const float* norm_w;     // [D]
+    float* state;            // [B][hv][D][D], in place
+    float* o_hat;            // [B][c_v] fp32 gated-norm output
     int hv, ratio, c_qk, c_conv, c_v;
+    float eps_l2, eps_rms, q_scale;
 };
 
-constexpr int DEC_WARPS = 8;
+constexpr int MID_THREADS = 256;
+constexpr int MID_WARPS = MID_THREADS / 32;
 
-template <int D>
-__global__ void __launch_bounds__(DEC_WARPS * 32) decode_rule_kernel(DecodeArgs a) {
-    constexpr int E = D / 32;   // entries per lane
-    const int lane = threadIdx.x & 31;
-    const int gr = blockIdx.x * DEC_WARPS + (threadIdx.x >> 5);   // row of all heads: h * D + i
-    const int sq = blockIdx.y;
-    if (gr >= a.hv * D) return;
-    const int h = gr / D, i = gr - h * D, hk = h / a.ratio;
-    const uint16_t* tok = a.qkv + static_cast<int64_t>(sq) * a.c_conv;
-    float q[E], k[E], s[E];
-    {
-        const uint16_t* qp = tok + hk * D + E * lane;
-        const uint16_t* kp = tok + a.c_qk + hk * D + E * lane;
+// Block sum of one value per thread; every thread gets the total.
+__device__ __forceinline__ float mid_block_sum(float v, float* red) {
+    v = warp_sum(v);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    float r = 0.0f;
 #pragma unroll
-        for (int e = 0; e < E; e += 2) {
-            const float2 qv = __half22float2(*reinterpret_cast<const __half2*>(qp + e));
-            const float2 kv = __half22float2(*reinterpret_cast<const __half2*>(kp + e));
-            q[e] = qv.x; q[e + 1] = qv.y;
-            k[e] = kv.x; k[e + 1] = kv.y;
-        }
-    }
-    float* sp = a.state + ((static_cast<int64_t>(sq) * a.hv + h) * D + i) * D + E * lane;
-    if (E == 4) {
-        const float4 v4 = *reinterpret_cast<const float4*>(sp);
-        s[0] = v4.x; s[1 % E] = v4.y; s[2 % E] = v4.z; s[3 % E] = v4.w;
-    } else {
-        const float2 v2 = *reinterpret_cast<const float2*>(sp);
-        s[0] = v2.x; s[1 % E] = v2.y;
-    }
-    float sk = 0.f, sq_ = 0.f, kq = 0.f;
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-        sk = fmaf(s[e], k[e], sk);
-        sq_ = fmaf(s[e], q[e], sq_);
-        kq = fmaf(k[e], q[e], kq);
-    }
-    sk = warp_sum(sk);
-    sq_ = warp_sum(sq_);
-    kq = warp_sum(kq);
-    const int64_t gi = static_cast<int64_t>(sq) * a.hv + h;
-    const float dec = expf(a.log_a[gi]), beta = a.b[gi];
-    const float v = __half2float(__ushort_as_half(tok[2 * a.c_qk + h * D + i]));
-    const float u = beta * (v - dec * sk);   // b (v_i - a S_i.k)
-#pragma unroll
-    for (int e = 0; e < E; ++e) s[e] = fmaf(u, k[e], dec * s[e]);
-    if (E == 4)
-        *reinterpret_cast<float4*>(sp) = make_float4(s[0], s[1 % E], s[2 % E], s[3 % E]);
-    else
-        *reinterpret_cast<float2*>(sp) = make_float2(s[0], s[1 % E]);
-    if (lane == 0) {
-        const float ov = fmaf(u, kq, dec * sq_);   // S_new . q
-        if (!(fabsf(ov) <= 65504.0f)) atomicCAS(&g_decode_error, 0, ERR_RANGE);
-        a.o[static_cast<int64_t>(sq) * a.c_v + h * D + i] = __half_as_ushort(__float2half_rn(ov));
-    }
+    for (int w = 0; w < MID_WARPS; ++w) r += red[w];
+    return r;
 }
 
-cudaError_t launch_decode_rule(const gdn_layer& L, const uint16_t* qkv, const float* log_a, const float* b,
-                               int64_t n_seqs, float* state, uint16_t* o, cudaStream_t st) {
-    DecodeArgs a;
+// One CTA per (value head h, sequence): the conv of its key head's q and k
+// channels and of its own v channels (SiLU, L2 norm of q and k, q scale), the
+// gates, one token of the recurrence on the head's D rows (a warp per row;
+// S_i.k, S_i.q and k.q are warp sums of the old row, o_i = a S_i.q + u k.q
+// with u = b (v_i - a S_i.k)), and the gated RMSNorm of o; everything in fp32.
+template <int D>
+__global__ void __launch_bounds__(MID_THREADS) decode_mid_kernel(MidArgs a) {
+    constexpr int E = D / 32;   // state entries per lane
+    __shared__ float qs[D], ks[D], vs[D], gz[D], os[D], red[MID_WARPS];
+    __shared__ float gate[2];
+    const int h = blockIdx.x, sq = blockIdx.y, hk = h / a.ratio;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint16_t* row = a.qkvz + static_cast<int64_t>(sq) * a.ld;
+    const float* tail = a.conv_state + static_cast<int64_t>(sq) * a.c_conv * 3;
+    // conv + SiLU of the 3D channels: q (key head), k (key head), v (this head)
+    for (int i = tid; i < 3 * D; i += MID_THREADS) {
+        const int part = i / D, e = i - part * D;
+        const int c = part == 0 ? hk * D + e : (part == 1 ? a.c_qk + hk * D + e : 2 * a.c_qk + h * D + e);
+        const float4 w = *reinterpret_cast<const float4*>(a.conv_w + static_cast<int64_t>(c) * 4);
+        const float y = conv4_silu(w, tail[c * 3 + 0], tail[c * 3 + 1], tail[c * 3 + 2], bf16_bits_to_float(row[c]));
+        (part == 0 ? qs : (part == 1 ? ks : vs))[e] = y;
+    }
+    for (int e = tid; e < D; e += MID_THREADS) {
+        const float z = bf16_bits_to_float(row[a.c_conv + h * D + e]);
+        gz[e] = silu_f(z) * a.norm_w[e];
+    }
+    if (tid == 0) {
+        const int64_t gi = static_cast<int64_t>(sq) * a.hv + h;
+        float la, b;
+        if (a.gate_log_a) {
+            la = a.gate_log_a[gi];
+            b = a.gate_b[gi];
+        } else {
+            const float* bar = a.ba + static_cast<int64_t>(sq) * a.ld_ba;
+            gate_values(bar[h], bar[a.hv + h], a.A_log[h], a.dt_bias[h], la, b);
+        }
+        gate[0] = expf(la);
+        gate[1] = b;
+    }
+    __syncthreads();
+    // L2 norms of q and k (q then scaled)
+    float q2 = 0.0f, k2 = 0.0f;
+    for (int e = tid; e < D; e += MID_THREADS) {
+        q2 = fmaf(qs[e], qs[e], q2);
+        k2 = fmaf(ks[e], ks[e], k2);
+    }
+    q2 = mid_block_sum(q2, red);
+    k2 = mid_block_sum(k2, red);
+    const float rq = rsqrtf(q2 + a.eps_l2) * a.q_scale, rk = rsqrtf(k2 + a.eps_l2);
+    float q[E], k[E];
+    float kq = 0.0f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        q[e] = qs[E * lane + e] * rq;
+        k[e] = ks[E * lane + e] * rk;
+        kq = fmaf(k[e], q[e], kq);
+    }
+    kq = warp_sum(kq);
+    const float dec = gate[0], beta = gate[1];
+    float* sbase = a.state + (static_cast<int64_t>(sq) * a.hv + h) * D * D + E * lane;
+    // the warp's rows i = warp + MID_WARPS * r, all loaded before the first is used
+    constexpr int R = D / MID_WARPS;
+    float sr[R][E];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const float* sp = sbase + static_cast<int64_t>(warp + MID_WARPS * r) * D;
+        if (E == 4) {
+            const float4 v4 = *reinterpret_cast<const float4*>(sp);
+            sr[r][0] = v4.x; sr[r][1 % E] = v4.y; sr[r][2 % E] = v4.z; sr[r][3 % E] = v4.w;
+        } else {
+            const float2 v2 = *reinterpret_cast<const float2*>(sp);
+            sr[r][0] = v2.x; sr[r][1 % E] = v2.y;
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int i = warp + MID_WARPS * r;
+        float* sp = sbase + static_cast<int64_t>(i) * D;
+        float (&s)[E] = sr[r];
+        float sk = 0.0f, sqv = 0.0f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            sk = fmaf(s[e], k[e], sk);
+            sqv = fmaf(s[e], q[e], sqv);
+        }
+        sk = warp_sum(sk);
+        sqv = warp_sum(sqv);
+        const float u = beta * (vs[i] - dec * sk);   // b (v_i - a S_i.k)
+#pragma unroll
+        for (int e = 0; e < E; ++e) s[e] = fmaf(u, k[e], dec * s[e]);
+        if (E == 4)
+            *reinterpret_cast<float4*>(sp) = make_float4(s[0], s[1 % E], s[2 % E], s[3 % E]);
+        else
+            *reinterpret_cast<float2*>(sp) = make_float2(s[0], s[1 % E]);
+        if (lane == 0) os[i] = fmaf(u, kq, dec * sqv);   // S_new . q
+    }
+    __syncthreads();
+    // gated RMSNorm: o / sqrt(mean o^2 + eps) * norm_w * SiLU(z)
+    float o2 = 0.0f;
+    for (int e = tid; e < D; e += MID_THREADS) o2 = fmaf(os[e], os[e], o2);
+    o2 = mid_block_sum(o2, red);
+    const float r = rsqrtf(o2 / static_cast<float>(D) + a.eps_rms);
+    for (int e = tid; e < D; e += MID_THREADS)
+        a.o_hat[static_cast<int64_t>(sq) * a.c_v + h * D + e] = os[e] * r * gz[e];
+}
+
+cudaError_t launch_decode_mid(const gdn_layer& L, const uint16_t* qkvz, int64_t ld, const float* ba, int64_t ld_ba,
+                              const float* conv_state, int64_t n_seqs, float* state, float* o_hat, cudaStream_t st) {
+    MidArgs a;
     const int d = L.dk;
-    a.qkv = qkv;
-    a.log_a = log_a;
-    a.b = b;
+    a.qkvz = qkvz;
+    a.ld = ld;
+    a.ba = ba;
+    a.ld_ba = ld_ba;
+    a.gate_log_a = L.gate_log_a;
+    a.gate_b = L.gate_b;
+    a.conv_w = L.conv_w;
+    a.conv_state = conv_state;
+    a.A_log = L.A_log;
+    a.dt_bias = L.dt_bias;
+    a.norm_w = L.norm_w;
     a.state = state;
-    a.o = o;
+    a.o_hat = o_hat;
     a.hv = L.n_v_heads;
     a.ratio = L.n_v_heads / L.n_qk_heads;
     a.c_qk = L.n_qk_heads * d;
     a.c_v = L.n_v_heads * d;
     a.c_conv = 2 * a.c_qk + a.c_v;
-    const dim3 grid(static_cast<unsigned>((a.hv * d + DEC_WARPS - 1) / DEC_WARPS), static_cast<unsigned>(n_seqs));
+    a.eps_l2 = L.eps_l2;
+    a.eps_rms = L.eps_rms;
+    a.q_scale = L.q_scale;
+    const dim3 grid(static_cast<unsigned>(a.hv), static_cast<unsigned>(n_seqs));
     if (d == 128)
-        decode_rule_kernel<128><<<grid, DEC_WARPS * 32, 0, st>>>(a);
+        decode_mid_kernel<128><<<grid, MID_THREADS, 0, st>>>(a);
     else
-        decode_rule_kernel<64><<<grid, DEC_WARPS * 32, 0, st>>>(a);
+        decode_mid_kernel<64><<<grid, MID_THREADS, 0, st>>>(a);
     return cudaGetLastError();
 }
 

@@ -229,13 +229,15 @@ int gdn_prefill_batch(const gdn_layer *layer, const void *x, const int64_t *cu_s
  * dot products of the 4- or 6-bit codes with the tokens' codes, scaled by the
  * sub-block's d*sc (and dmin*m) in fp32: the product of the int8 activations
  * with the exactly decoded weights (no re-quantisation of the weights, unlike
- * the prefill's int8 weight rows), within fp32 rounding.  The conv is
- * gdn_prefill's.  The recurrence takes the token in fp32 (S <- a S (I - b k
- * k^T) + b v k^T, o = S q), not through the chunked fp16-operand form.  So a
- * decoded token agrees with a prefill of it within the stated tolerances, not
- * bit for bit.
- * 1 <= n_seqs <= GDN_MAX_SEQS.  An out-of-range o is reported as GDN_ERANGE by
- * gdn_sync_status.
+ * the prefill's int8 weight rows), within fp32 rounding.  The conv, SiLU,
+ * L2 norms, gates, one token of the recurrence (S <- a S (I - b k k^T) +
+ * b v k^T, o = S q) and the gated RMSNorm run in fp32 in one kernel per
+ * (value head, sequence), with none of the prefill's fp16 operand roundings;
+ * the quantisation of each token (before the input projection) and of its
+ * gated-norm output (before the output projection) happens inside the
+ * projection kernels.  Three launches in all.  A decoded token therefore
+ * agrees with a prefill of it within the stated tolerances, not bit for bit.
+ * 1 <= n_seqs <= GDN_MAX_SEQS.
  */
 size_t gdn_decode_workspace_size(const gdn_layer *layer, int n_seqs);
 int gdn_decode(const gdn_layer *layer, const void *x, int n_seqs, float *state, float *conv_state, void *y,
