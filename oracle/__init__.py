@@ -17,6 +17,8 @@ threads on Qwen3.5 prefill speed):
   plain absmax encoder;
 * ``quant``  int8 row quantisation with one fp32 scale per row, the exact
   integer product of two int8 matrices and its fp32 rescale, bf16 rounding;
+* ``attention``  causal grouped-query softmax attention (the prefill of the
+  hybrid model's full-attention layers), in float64;
 * ``layer``  the causal 4-tap conv with SiLU, per-head L2 norm, the gates,
   the gated delta rule one token at a time (and, to pin the algebra a chunked
   kernel uses, its chunked WY/UT form), the gated RMSNorm and the whole layer.
@@ -31,4 +33,4 @@ has no worked example on the pages, so its end-to-end values are pinned only
 through the pinned stages and the layer-level invariants (extend equals
 re-prefill, chunked equals sequential).
 """
-from . import q4k, q6k, quant, layer  # noqa: F401
+from . import q4k, q6k, quant, layer, attention  # noqa: F401
