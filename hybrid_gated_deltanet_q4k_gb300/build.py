@@ -20,7 +20,7 @@ OUT_DIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT_DIR, "libgdn.so")
 INCLUDE = os.path.join(ROOT, "include")
 
-CU_SOURCES = ["k_q4k.cu", "k_q6k.cu", "k_quant.cu", "k_gemm.cu", "k_conv.cu", "k_delta.cu", "k_norm.cu", "k_decode.cu", "streams.cu", "gdn_api.cu"]
+CU_SOURCES = ["k_q4k.cu", "k_q6k.cu", "k_quant.cu", "k_gemm.cu", "k_conv.cu", "k_delta.cu", "k_norm.cu", "k_decode.cu", "k_attn.cu", "streams.cu", "gdn_api.cu"]
 CPP_SOURCES = ["kquant_pack.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

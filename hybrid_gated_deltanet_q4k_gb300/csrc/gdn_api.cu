@@ -12,6 +12,7 @@
 #include "common.cuh"
 #include "streams.h"
 
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <mutex>
@@ -49,6 +50,10 @@ cudaError_t launch_gemv_dot(const void*, bool, int64_t, int64_t, const uint16_t*
 cudaError_t launch_decode_mid(const gdn_layer&, const uint16_t*, int64_t, const float*, int64_t, const float*, int64_t,
                               float*, float*, cudaStream_t);
 int read_and_clear_decode_error();
+cudaError_t launch_attn(const uint16_t*, const uint16_t*, const uint16_t*, int64_t, int64_t, int, int, int, float, uint16_t*,
+                        void*, cudaStream_t);
+size_t attn_workspace_bytes(int64_t nk, int hkv, int d);
+int read_and_clear_attn_error();
 int read_and_clear_gemm_error();
 int read_and_clear_delta_error();
 int read_and_clear_conv_error();
@@ -849,12 +854,43 @@ int gdn_decode_gemv(const void* blocks, int q6k, int64_t rows, int64_t cols, con
     return GDN_OK;
 }
 
+size_t gdn_attn_workspace_size(int64_t nk, int n_kv_heads, int head_dim) {
+    if (nk < 1 || n_kv_heads < 1 || (head_dim != 64 && head_dim != 128 && head_dim != 256)) return 0;
+    return attn_workspace_bytes(nk, n_kv_heads, head_dim);
+}
+
+int gdn_attn_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v, int64_t nq, int64_t nk, int n_q_heads,
+                     int n_kv_heads, int head_dim, float scale, uint16_t* o, void* workspace, size_t ws_bytes,
+                     void* stream) {
+    if (!q || !k || !v || !o || !workspace) return fail(GDN_EINVAL, "gdn_attn_prefill: NULL pointer");
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256)
+        return fail(GDN_EINVAL, "gdn_attn_prefill: head_dim must be 64, 128 or 256 (got %d)", head_dim);
+    if (n_q_heads < 1 || n_kv_heads < 1 || n_q_heads % n_kv_heads || n_q_heads > 256)
+        return fail(GDN_EINVAL, "gdn_attn_prefill: n_q_heads a multiple of n_kv_heads, at most 256 (got %d, %d)",
+                    n_q_heads, n_kv_heads);
+    if (nq < 1 || nk < nq || nk > 0x7fffffff)
+        return fail(GDN_EINVAL, "gdn_attn_prefill: 1 <= nq <= nk < 2^31 required (got %lld, %lld)", (long long)nq,
+                    (long long)nk);
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(workspace, 16))
+        return fail(GDN_EINVAL, "gdn_attn_prefill: 16-byte alignment required");
+    if (ws_bytes < attn_workspace_bytes(nk, n_kv_heads, head_dim))
+        return fail(GDN_ENOMEM, "gdn_attn_prefill: workspace %zu B < %zu B", ws_bytes,
+                    attn_workspace_bytes(nk, n_kv_heads, head_dim));
+    const float sc = scale > 0.0f ? scale : 1.0f / sqrtf(static_cast<float>(head_dim));
+    cudaError_t e = launch_attn(q, k, v, nq, nk, n_q_heads, n_kv_heads, head_dim, sc, o, workspace,
+                                static_cast<cudaStream_t>(stream));
+    if (e == cudaErrorInvalidValue) return fail(GDN_EINVAL, "gdn_attn_prefill: tensor map rejected");
+    if (e != cudaSuccess) return cuda_fail(e, "gdn_attn_prefill");
+    return GDN_OK;
+}
+
 int gdn_sync_status(void* stream) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "gdn_sync_status");
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "gdn_sync_status");
     if (read_and_clear_gemm_error()) return fail(GDN_ETIMEOUT, "a bounded wait in the projection kernel ran out");
+    if (read_and_clear_attn_error()) return fail(GDN_ETIMEOUT, "a bounded wait in the attention kernel ran out");
     const int dcode = read_and_clear_delta_error();
     const int rcode = read_and_clear_decode_error();
     const int ccode = read_and_clear_conv_error();

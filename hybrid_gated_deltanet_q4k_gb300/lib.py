@@ -52,6 +52,8 @@ _SIGNATURES = {
     "gdn_host_workspace_size": (c_size_t, [_P, c_int64]),
     "gdn_prefill_host": (c_int32, [_P, _P, c_int64, _P, _P, _P, _P, c_int64, _P, c_size_t, _P]),
     "gdn_prefill_ckpt": (c_int32, [_P, _P, c_int64, _P, _P, _P, _P, c_int64, _P, _P, _P, c_size_t, _P]),
+    "gdn_attn_workspace_size": (c_size_t, [c_int64, c_int32, c_int32]),
+    "gdn_attn_prefill": (c_int32, [_P, _P, _P, c_int64, c_int64, c_int32, c_int32, c_int32, c_float, _P, _P, c_size_t, _P]),
     "gdn_sync_status": (c_int32, [_P]),
     "gdn_last_error": (ctypes.c_char_p, []),
     "gdn_set_stage_events": (c_int32, [ctypes.POINTER(c_void_p), c_int32]),

@@ -166,3 +166,19 @@ def make_extend_case(spec: LayerSpec, n_seqs: int = 8, prefix: int = 2048, max_e
         toks["extension"] = int(ext[i])
         cases.append(toks)
     return cases
+
+
+def make_attention(nq: int, nk: int, hq: int, hkv: int, d: int, seed: int, q_gain: float = 1.0) -> dict:
+    """Inputs of the full-attention prefill: q [nq, hq, d], k and v [nk, hkv, d]
+    ~ N(0, 1) (q times q_gain: a larger gain makes the softmax peakier), rounded
+    to bf16; returned as bit patterns (``*_bits``) and their exact float32
+    values."""
+    rng = np.random.default_rng(seed)
+    out = {}
+    for name, shape, gain in (("q", (nq, hq, d), q_gain), ("k", (nk, hkv, d), 1.0), ("v", (nk, hkv, d), 1.0)):
+        x = rng.standard_normal(shape, dtype=np.float32)
+        if gain != 1.0:
+            x *= np.float32(gain)
+        out[name + "_bits"] = _round_bf16_inplace(x)
+        out[name] = x
+    return out

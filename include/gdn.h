@@ -313,6 +313,29 @@ int gdn_prefill_ckpt(const gdn_layer *layer, const void *x, int64_t n_tokens, co
                      void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * gdn_attn_prefill -- prefill of the hybrid model's full-attention layers:
+ * causal softmax attention with grouped key/value heads (the pages' flash
+ * attention for those layers, "Qwen3.5 speed: prefill and decode parity with
+ * llama.cpp" #5305, sub-ticket #4442: at 32k tokens the prefill falls because
+ * they run "cuBLAS f32 with a materialised score matrix", "CRUX parity spike"
+ * #4220, long-context finding 2).  For query head h (key/value head h /
+ * (n_q_heads / n_kv_heads)) and query i at position nk - nq + i:
+ *     o_i = sum_{j <= nk - nq + i} softmax_j(scale * q_i . k_j) v_j
+ * (nq = nk: a fresh prefill; nq < nk: queries extending held keys).
+ *   q  bf16 [nq][n_q_heads][head_dim], k and v bf16 [nk][n_kv_heads][head_dim],
+ *      o bf16 [nq][n_q_heads][head_dim], all 16-byte aligned
+ *   head_dim 64, 128 or 256; scale <= 0 means head_dim^-1/2
+ *   workspace >= gdn_attn_workspace_size(nk, n_kv_heads, head_dim) bytes (V^T)
+ * Products on tcgen05 tensor cores with bf16 operands and fp32 accumulation;
+ * the probabilities enter the second product rounded to bf16; the softmax is
+ * fp32.  A bounded wait that runs out is reported as GDN_ETIMEOUT.
+ */
+size_t gdn_attn_workspace_size(int64_t nk, int n_kv_heads, int head_dim);
+int gdn_attn_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, int64_t nq, int64_t nk, int n_q_heads,
+                     int n_kv_heads, int head_dim, float scale, uint16_t *o, void *workspace, size_t ws_bytes,
+                     void *stream);
+
+/*
  * gdn_sync_status -- wait for `stream`, then report (and clear) the device
  * error words the kernels set: GDN_OK, GDN_ETIMEOUT (a bounded wait ran out),
  * GDN_ERANGE (a value beyond the fp16 operand range of the recurrence: the
