@@ -56,6 +56,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-pass", type=int, default=8192, help="tokens per pass of the host-fed call")
+    ap.add_argument("--seqs", type=int, default=None, help="--config decode: one batch size only (a profiling case)")
     ap.add_argument("--stage", choices=["in_proj", "delta_rule", "q6k_deq", "q4k_deq"], default=None,
                     help="time one stage kernel alone through its stage entry point (profiling case)")
     ap.add_argument("--tokens", type=int, default=None,
@@ -574,7 +575,7 @@ def run_decode(args, spec):
     stream = torch.cuda.current_stream()
     pk = peaks()
     rows = []
-    for B in (1, 8, 32):
+    for B in ((args.seqs,) if args.seqs else (1, 8, 32)):
         tok = synth.make_tokens(spec, B, seed=90 + B)
         x = torch.from_numpy(tok["x_bits"].view(np.int16)).cuda().view(torch.bfloat16)
         la, bb = torch.from_numpy(tok["log_a"]).cuda(), torch.from_numpy(tok["b"]).cuda()
@@ -604,8 +605,59 @@ def run_decode(args, spec):
                       "data": "synthetic", "call": "gdn_decode"}), flush=True)
 
 
+def run_attn(args):
+    """Prefill of a full-attention layer of the 9B-like hybrid (16 query heads
+    over 4 key/value heads of 256; the pages give no sizes for these layers, so
+    the GQA ratio and head size are a reading), N = 32768 causal, through
+    gdn_attn_prefill; inputs resident, CUDA events.  Tensor roofline: the causal
+    FLOPs 4 d Hq N (N + 1) / 2 against the bf16 peak (burst: the kernel timed
+    alone).  A secondary measurement."""
+    import torch
+
+    from hybrid_gated_deltanet_q4k_gb300 import lib as gl
+    from hybrid_gated_deltanet_q4k_gb300 import synth
+
+    L = gl.load(build=True)
+    n = args.tokens or 32768
+    hq, hkv, d = 16, 4, 256
+    inp = synth.make_attention(n, n, hq, hkv, d, seed=11)
+    dev = lambda b: torch.from_numpy(b.view(np.int16)).cuda().view(torch.bfloat16)  # noqa: E731
+    q, k, v = dev(inp["q_bits"]), dev(inp["k_bits"]), dev(inp["v_bits"])
+    o = torch.empty(n, hq, d, dtype=torch.bfloat16, device="cuda")
+    nbytes = L.gdn_attn_workspace_size(n, hkv, d)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    fn = lambda: L.gdn_attn_prefill(gl.ptr(q), gl.ptr(k), gl.ptr(v), n, n, hq, hkv, d, 0.0, gl.ptr(o), gl.ptr(ws),  # noqa: E731
+                                    nbytes, stream.cuda_stream)
+    for _ in range(max(args.warmup, 3)):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    assert L.gdn_sync_status(stream.cuda_stream, check=False) == 0, L.last_error()
+    ms = e0.elapsed_time(e1) / args.steps
+    flops = 4.0 * d * hq * n * (n + 1) / 2
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    peak = json.load(open(path))["bf16_tflops"] if os.path.exists(path) else 1900.0
+    tf = flops / (ms / 1e3) / 1e12
+    print(json.dumps({"metric": "full-attention layer prefill tokens/s (1 GB300)", "unit": "tokens/s",
+                      "value": n / (ms / 1e3), "ms_per_step": ms, "steps": args.steps,
+                      "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
+                                   "peak_source": "of measured (MEASURED_PEAKS.json bf16_tflops, burst)"},
+                      "dtype": "bf16", "data": "synthetic",
+                      "config": {"workload": f"attn_causal_n{n}_hq{hq}_hkv{hkv}_d{d}", "call": "gdn_attn_prefill"}}),
+          flush=True)
+
+
 def main():
     args = parse()
+    if args.config == "attn" and args.impl == "ours":
+        run_attn(args)
+        return
     if args.config == "decode" and args.impl == "ours":
         from hybrid_gated_deltanet_q4k_gb300 import synth
         run_decode(args, synth.SPECS["h4096"])

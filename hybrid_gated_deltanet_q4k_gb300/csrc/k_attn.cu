@@ -17,9 +17,11 @@
 //   S_j = Q K_j^T            tcgen05.mma kind::f16 (bf16), M = 128, N = 64, K = D,
 //                            into one of two TMEM buffers (S_{j+1} runs while
 //                            the softmax works on S_j)
-//   softmax warps            one query row per thread: the row's 64 scores from
-//                            TMEM, causal mask, the running maximum m, P_j =
-//                            2^(s log2e - m) in bf16 to shared memory, l += sum P
+//   softmax warps            two threads per query row, 32 scores each from
+//                            TMEM, causal mask on diagonal blocks, the running
+//                            maximum m (the halves swap their block maxima),
+//                            P_j = 2^(s scale log2e - m) in bf16 to shared
+//                            memory, l += sum P
 //   O += P_j V_j             M = 128, N = D, K = 64, O accumulated in TMEM
 // The maximum is raised only when a row's block maximum exceeds it by more
 // than 2^8 (so P <= 256, fine for bf16); then the warp's O rows are scaled by
@@ -28,8 +30,8 @@
 // V is read through its transpose V^T [Hkv][D][nk], written by a transpose
 // kernel first, so both operands of both products are K-major.
 // Warps: 0 TMA (lane 0 loads K blocks, lane 1 V^T blocks, two stages each; Q
-// once), 1 TMEM owner and MMA issuer, 2-5 softmax (warp w reads TMEM lanes
-// 32 (w % 4) .. +31).  Every wait is bounded; after a wait runs out the CTA
+// once), 1 TMEM owner and MMA issuer, 2-9 softmax (warp w reads TMEM lanes
+// 32 (w % 4) .. +31; warps 2-5 and 6-9 take the two halves of those rows).  Every wait is bounded; after a wait runs out the CTA
 // stops issuing, lets its copies and products finish and returns with an error
 // word set (GDN_ETIMEOUT).
 #include "common.cuh"
@@ -44,7 +46,8 @@ static __device__ int g_attn_error;
 
 constexpr int ATT_BM = 128;   // queries per CTA
 constexpr int ATT_BN = 64;    // keys per block
-constexpr int ATT_THREADS = 192;
+constexpr int ATT_SM_WARPS = 8;   // softmax warps: two per row quadrant, each half of a row's scores
+constexpr int ATT_THREADS = 64 + 32 * ATT_SM_WARPS;
 constexpr float ATT_RESCALE_LOG2 = 8.0f;   // raise the maximum only past this margin
 
 template <int D>
@@ -61,7 +64,9 @@ struct AttSmem {
     static constexpr int B0 = P0 + ATT_BM * 128;         // mbarriers
     // barrier indices
     static constexpr int QF = 0, KF = 1, KE = 3, VF = 5, VE = 7, SF = 9, PF = 11, PV = 12, FIN = 13, NBAR = 14;
-    static constexpr int MISC0 = B0 + 8 * NBAR;          // TMEM base, abort flag
+    static constexpr int X0 = B0 + 8 * NBAR;             // row maxima of each half, two rounds: [2][2][128] fp32
+    static constexpr int LS0 = X0 + 2 * 2 * ATT_BM * 4;  // row sums of each half: [2][128] fp32
+    static constexpr int MISC0 = LS0 + 2 * ATT_BM * 4;   // TMEM base, abort flag
     static constexpr int BYTES = MISC0 + 16;
 };
 
@@ -115,7 +120,7 @@ attn_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUte
     const int nb = last_pos / ATT_BN + 1;                     // key blocks it needs
 
     if (tid == 0) {
-        for (int i = 0; i < L::NBAR; ++i) mbar_init_cta(bars + i, i == L::PF ? 128 : 1);
+        for (int i = 0; i < L::NBAR; ++i) mbar_init_cta(bars + i, i == L::PF ? 32 * ATT_SM_WARPS : 1);
         mbar_init_fence();
         *abort = 0;
     }
@@ -193,29 +198,40 @@ attn_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUte
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------------------ softmax, one row per thread
-        const int quad = warp & 3, r = 32 * quad + lane, pos = off + q0 + r;
+        // ------------------------------------------------------------ softmax
+        // Warp w reads TMEM lanes 32 (w % 4) .. +31 (rows r); warps 2-5 take the
+        // scores 0-31 of their rows' block and the O columns 0 .. D/2-1, warps
+        // 6-9 the scores 32-63 and O columns D/2 .. D-1; the two halves of a row
+        // swap their block maxima through shared memory (two rounds of buffers)
+        // and keep partial sums, added at the end.
+        const int quad = warp & 3, half = (warp - 2) >> 2, r = 32 * quad + lane, pos = off + q0 + r;
         const uint32_t trow = tmem + (static_cast<uint32_t>(32 * quad) << 16);
+        float* xmax = reinterpret_cast<float*>(base + L::X0);
+        float* lsum = reinterpret_cast<float*>(base + L::LS0);
+        const int pos_min = off + q0;   // every query of the tile sees keys <= pos_min
         float m = 0.0f, l = 0.0f;
         bool ok = true;
         for (int j = 0; j < nb; ++j) {
             const int st = j & 1;
             ok = __all_sync(0xffffffffu, ok && att_wait(bars + L::SF + st, (j >> 1) & 1, abort));
-            float x[64];
+            float x[32];
             float bm = -INFINITY;
             if (ok) {
                 t5::fence_after();
-                float s0[32], s1[32];
-                t5::ld32(trow + st * ATT_BN, s0);
-                t5::ld32(trow + st * ATT_BN + 32, s1);
+                t5::ld32(trow + st * ATT_BN + 32 * half, x);
+                const int key0 = j * ATT_BN + 32 * half;
+                if (key0 + 31 > pos_min || key0 + 31 >= a.nk) {   // a block on the diagonal or past the keys
 #pragma unroll
-                for (int c = 0; c < 64; ++c) {
-                    const int key = j * ATT_BN + c;
-                    const float sv = c < 32 ? s0[c] : s1[c - 32];
-                    x[c] = (key <= pos && key < a.nk) ? sv * a.sl2 : -INFINITY;
-                    bm = fmaxf(bm, x[c]);
+                    for (int c = 0; c < 32; ++c)
+                        if (!(key0 + c <= pos && key0 + c < a.nk)) x[c] = -INFINITY;
                 }
+#pragma unroll
+                for (int c = 0; c < 32; ++c) bm = fmaxf(bm, x[c]);
             }
+            // the row's maximum over both halves (raw scores; the scale is positive)
+            xmax[(st * 2 + half) * ATT_BM + r] = bm;
+            asm volatile("bar.sync 1, %0;" ::"n"(32 * ATT_SM_WARPS) : "memory");
+            bm = fmaxf(bm, xmax[(st * 2 + (half ^ 1)) * ATT_BM + r]) * a.sl2;
             // the previous product must be done before P is rewritten or O rescaled
             if (j > 0) ok = __all_sync(0xffffffffu, ok && att_wait(bars + L::PV, (j - 1) & 1, abort));
             if (!ok) {
@@ -230,7 +246,7 @@ attn_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUte
                 l *= alpha;
                 t5::fence_after();
 #pragma unroll 1
-                for (int c0 = 0; c0 < D; c0 += 32) {
+                for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 32) {
                     float ov[32];
                     t5::ld32(trow + 2 * ATT_BN + c0, ov);
 #pragma unroll
@@ -238,31 +254,35 @@ attn_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUte
                     t5::st32(trow + 2 * ATT_BN + c0, ov);
                 }
             }
-            // P_j in bf16 (the 128-byte-swizzled K-major image), l from the rounded values
+            // P = 2^(s scale log2e - m) in bf16 (the 128-byte-swizzled K-major image)
             float sum = 0.0f;
 #pragma unroll
-            for (int c = 0; c < 64; c += 8) {
-                uint32_t w[4];
+            for (int c = 0; c < 32; c += 8) {
+                float p[8];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    w[e] = bf16x2_bits(ex2_approx(x[c + 2 * e] - m), ex2_approx(x[c + 2 * e + 1] - m));
-                    sum += __uint_as_float(w[e] << 16) + __uint_as_float(w[e] & 0xffff0000u);
+                for (int e = 0; e < 8; ++e) {
+                    p[e] = ex2_approx(fmaf(x[c + e], a.sl2, -m));
+                    sum += p[e];
                 }
-                *reinterpret_cast<uint4*>(base + L::P0 + sw128_f16(r, c)) = make_uint4(w[0], w[1], w[2], w[3]);
+                *reinterpret_cast<uint4*>(base + L::P0 + sw128_f16(r, 32 * half + c)) =
+                    make_uint4(bf16x2_bits(p[0], p[1]), bf16x2_bits(p[2], p[3]), bf16x2_bits(p[4], p[5]),
+                               bf16x2_bits(p[6], p[7]));
             }
             l += sum;
             fence_proxy_async_smem();
             t5::fence_before();
             att_arrive(bars + L::PF);
         }
+        lsum[half * ATT_BM + r] = l;
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * ATT_SM_WARPS) : "memory");
         ok = __all_sync(0xffffffffu, ok && att_wait(bars + L::PV, (nb - 1) & 1, abort));
         if (ok) {
             t5::fence_after();
-            const float inv = 1.0f / l;
+            const float inv = 1.0f / (lsum[r] + lsum[ATT_BM + r]);
             const bool store = q0 + r < a.nq;
             uint16_t* orow = a.o + (static_cast<int64_t>(q0 + r) * a.hq + h) * D;
 #pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
+            for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 32) {
                 float ov[32];
                 t5::ld32(trow + 2 * ATT_BN + c0, ov);
                 if (store) {
