@@ -602,7 +602,28 @@ int gdn_prefill_host(const gdn_layer* layer, const void* x_host, int64_t n_token
             gas[i] = reinterpret_cast<float*>(stage + 4 * xb + (2 * i) * gbytes);
             gbs[i] = reinterpret_cast<float*>(stage + 4 * xb + (2 * i + 1) * gbytes);
         }
-    const int64_t np = (n_tokens + B - 1) / B;
+    // Pass boundaries: passes of B tokens, except that the first and the last
+    // are a quarter of B when B is a whole number of 4 chunks and there is more
+    // than one pass -- the copy-in of the first pass and the copy-out of the
+    // last are the ones nothing hides.  Every boundary is a chunk boundary.
+    std::vector<int64_t> bounds{0};
+    {
+        const int64_t qb = B / 4;
+        const bool short_ends = n_tokens > B && B % (4 * GDN_CHUNK) == 0;
+        int64_t t = short_ends ? qb : (B < n_tokens ? B : n_tokens);
+        bounds.push_back(t);
+        while (t < n_tokens) {
+            int64_t next = t + B < n_tokens ? t + B : n_tokens;
+            if (short_ends && next == n_tokens && n_tokens - t > qb) {
+                // a short last pass, split on a chunk boundary
+                const int64_t split = t + (n_tokens - t - qb) / GDN_CHUNK * GDN_CHUNK;
+                if (split > t) next = split;
+            }
+            t = next;
+            bounds.push_back(t);
+        }
+    }
+    const int64_t np = static_cast<int64_t>(bounds.size()) - 1;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
     std::lock_guard<std::mutex> lock(copy_streams_mutex());
@@ -616,7 +637,7 @@ int gdn_prefill_host(const gdn_layer* layer, const void* x_host, int64_t n_token
     // Host-to-device copy of pass p into slot p % 2, once pass p - 2 (the
     // previous user of the slot) is done with it.
     auto copy_in = [&](int64_t p) -> int {
-        const int64_t u0 = p * B, nb = (n_tokens - u0) < B ? (n_tokens - u0) : B;
+        const int64_t u0 = bounds[p], nb = bounds[p + 1] - bounds[p];
         const int slot = static_cast<int>(p & 1);
         if (p >= 2) GDN_LAUNCH(cudaStreamWaitEvent(cs->h2d, cs->pass_done[slot], 0), "gdn_prefill_host: slot wait");
         GDN_LAUNCH(cudaMemcpyAsync(xs[slot], static_cast<const uint8_t*>(x_host) + u0 * s.H * esz, nb * s.H * esz,
@@ -640,7 +661,7 @@ int gdn_prefill_host(const gdn_layer* layer, const void* x_host, int64_t n_token
         GDN_LAUNCH(mark(1, true, st), "stage event");
         if ((rr = copy_in(0))) return rr;
         for (int64_t p = 0; p < np; ++p) {
-            const int64_t u0 = p * B, nb = (n_tokens - u0) < B ? (n_tokens - u0) : B;
+            const int64_t u0 = bounds[p], nb = bounds[p + 1] - bounds[p];
             const int slot = static_cast<int>(p & 1);
             if (p + 1 < np && (rr = copy_in(p + 1))) return rr;
             GDN_LAUNCH(cudaStreamWaitEvent(st, cs->in_ready[slot], 0), "gdn_prefill_host: input wait");

@@ -264,8 +264,10 @@ int gdn_decode_gemv(const void *blocks, int q6k, int64_t rows, int64_t cols, con
  * the device-to-host copy of pass p-1 run on two copy streams of the library
  * while pass p computes (two device staging slots each of x, y and the
  * drawn gates), so the copies hide behind the compute except for the first
- * input and the last output.  Results are bitwise those of gdn_prefill run
- * with passes of the same B.
+ * input and the last output; those two passes are B/4 tokens when B is a
+ * multiple of 4 * GDN_CHUNK and N > B.  Every pass boundary is a chunk
+ * boundary (an exact extend), so the results are bitwise those of
+ * gdn_prefill.
  *   x_host     page-locked host memory (cudaHostAlloc / cudaHostRegister):
  *              bf16 (Q4_K) or fp32 (F32) [N][hidden]
  *   y_host     page-locked host memory, same type and shape as x_host;
