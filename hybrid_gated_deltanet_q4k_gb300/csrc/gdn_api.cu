@@ -46,9 +46,12 @@ cudaError_t launch_gated_norm(const gdn_layer&, const uint16_t*, const uint16_t*
 cudaError_t launch_gemv_dot(const void*, bool, int64_t, int64_t, const uint16_t*, const float*, int64_t, uint16_t*,
                               int64_t, int64_t, float*, int64_t, cudaStream_t, int in_mode = 0, const void* xraw = nullptr,
                               float* cs_state = nullptr, const uint16_t* cs_qkvz = nullptr, int64_t cs_ld = 0,
-                              int cs_c_conv = 0, int cs_n = 0);
+                              int cs_c_conv = 0, int cs_n = 0, const float* rms_psum = nullptr, int rms_hv = 0,
+                              int rms_d = 0, int rms_split = 0, float rms_eps = 0.0f);
 cudaError_t launch_decode_mid(const gdn_layer&, const uint16_t*, int64_t, const float*, int64_t, const float*, int64_t,
-                              float*, float*, cudaStream_t);
+                              float*, float*, float*, cudaStream_t);
+cudaError_t launch_decode_rms_apply(const gdn_layer&, float*, const float*, int64_t, cudaStream_t);
+constexpr int DECODE_MID_SPLIT = 4;   // row blocks per value head in the decode step's middle kernel
 int read_and_clear_decode_error();
 cudaError_t launch_attn(const uint16_t*, const uint16_t*, const uint16_t*, int64_t, int64_t, int, int, int, float, uint16_t*,
                         void*, cudaStream_t);
@@ -303,7 +306,8 @@ size_t host_stage_bytes(const gdn_layer* L, const Sizes& s, int64_t B) {
 // Workspace of one decode step of B tokens (one per sequence).
 struct DecodeWs {
     uint16_t* qkvz; float* ba;        // projection [B][n_bf16] bf16, [B][2 hv] fp32
-    float* ohat;                      // gated-norm output [B][c_v] fp32
+    float* ohat;                      // gated output [B][c_v] fp32 (RMS applied by the output projection)
+    float* psum;                      // partial sums of o^2 [B][hv][DECODE_MID_SPLIT]
     uint16_t* xc; float* sx;          // codes of x [B][H] and of o_hat [B][c_v], with row scales,
     uint16_t* oc; float* so;          // when B > GDN_DECODE_GEMV_TOKENS (quantised once, not per CTA)
     size_t total;
@@ -321,6 +325,7 @@ DecodeWs carve_decode(const gdn_layer* L, const Sizes& s, int64_t B, void* base)
     w.qkvz = static_cast<uint16_t*>(take(B * s.n_bf16 * 2));
     w.ba = static_cast<float*>(take(B * 2 * s.hv * 4));
     w.ohat = static_cast<float*>(take(B * s.c_v * 4));
+    w.psum = static_cast<float*>(take(B * s.hv * DECODE_MID_SPLIT * 4));
     if (L->wtype == GDN_W_Q4K && B > GDN_DECODE_GEMV_TOKENS) {
         w.xc = static_cast<uint16_t*>(take(B * s.H * 2));
         w.sx = static_cast<float*>(take(B * 4));
@@ -831,10 +836,11 @@ int gdn_decode(const gdn_layer* layer, const void* x, int n_seqs, float* state, 
     }
     // K2, steps 2-4 per (value head, sequence): conv, norms, gates, one token of
     // the recurrence, gated RMSNorm -> o_hat (fp32)
-    GDN_LAUNCH(launch_decode_mid(*layer, w.qkvz, s.n_bf16, w.ba, 2 * s.hv, conv_state, B, state, w.ohat, st),
+    GDN_LAUNCH(launch_decode_mid(*layer, w.qkvz, s.n_bf16, w.ba, 2 * s.hv, conv_state, B, state, w.ohat, w.psum, st),
                "decode: conv, recurrence and gated norm");
     // K3, step 5: the conv tails move up by one token, o_hat is quantised to
     // int8 rows in each CTA and meets the output weights (Q4_K layers)
+    if (!q4k || once) GDN_LAUNCH(launch_decode_rms_apply(*layer, w.ohat, w.psum, B, st), "decode: gated-norm RMS");
     if (q4k && once) {
         GDN_LAUNCH(launch_quant_rows_f32(w.ohat, B, s.c_v, w.oc, w.so, st), "decode: quantise o_hat");
         GDN_LAUNCH(launch_gemv_dot(layer->w_out, layer->q6k_mask & 2, s.H, s.c_v, w.oc, w.so, B,
@@ -844,7 +850,8 @@ int gdn_decode(const gdn_layer* layer, const void* x, int n_seqs, float* state, 
     } else if (q4k) {
         GDN_LAUNCH(launch_gemv_dot(layer->w_out, layer->q6k_mask & 2, s.H, s.c_v, nullptr, nullptr, B,
                                    static_cast<uint16_t*>(y), s.H, s.H, nullptr, 0, st, 2, w.ohat, conv_state, w.qkvz,
-                                   s.n_bf16, static_cast<int>(s.c_conv), n_seqs),
+                                   s.n_bf16, static_cast<int>(s.c_conv), n_seqs, w.psum, static_cast<int>(s.hv),
+                                   static_cast<int>(s.d), DECODE_MID_SPLIT, layer->eps_rms),
                    "decode: conv state and output projection");
     } else {
         std::vector<int64_t> cu(static_cast<size_t>(B) + 1);

@@ -70,10 +70,18 @@ struct GemvArgs {
     const uint16_t* cs_qkvz; // [cs_n][cs_ld] bf16
     int64_t cs_ld;
     int cs_c_conv, cs_n;
+    // optional with in_mode 2 (rms_psum non-null): the rows are gated but not yet
+    // RMS-normalised; head h of token t is multiplied by rsqrt(sum_p
+    // rms_psum[(t*rms_hv + h)*rms_split + p] / rms_d + rms_eps) first (the
+    // partial sums of o^2 over the head's row blocks, added in order)
+    const float* rms_psum;
+    int rms_hv, rms_d, rms_split;
+    float rms_eps;
 };
 
-// Elements 16b .. 16b+15 of raw input row t as floats.
-__device__ __forceinline__ void gemv_raw16(const GemvArgs& a, int t, int b, float (&w)[16]) {
+// Elements 16b .. 16b+15 of raw input row t as floats (rh: per token and head
+// scale of in_mode 2 with rms_psum, else unused).
+__device__ __forceinline__ void gemv_raw16(const GemvArgs& a, int t, int b, float (&w)[16], const float* rh) {
     if (a.in_mode == 1) {
         const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.xraw) +
                                                         static_cast<int64_t>(t) * a.cols + 16 * b);
@@ -87,10 +95,11 @@ __device__ __forceinline__ void gemv_raw16(const GemvArgs& a, int t, int b, floa
     } else {
         const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(a.xraw) +
                                                           static_cast<int64_t>(t) * a.cols + 16 * b);
+        const float sc = a.rms_psum ? rh[t * 64 + (16 * b) / a.rms_d] : 1.0f;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const float4 v = __ldg(p + e);
-            w[4 * e] = v.x; w[4 * e + 1] = v.y; w[4 * e + 2] = v.z; w[4 * e + 3] = v.w;
+            w[4 * e] = v.x * sc; w[4 * e + 1] = v.y * sc; w[4 * e + 2] = v.z * sc; w[4 * e + 3] = v.w * sc;
         }
     }
 }
@@ -188,7 +197,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_dot_kernel(GemvArgs a) {
         for (int i = 0; i < a.stages; ++i) gemv_issue(a, ring, full, blockIdx.x + i * gridDim.x, i);
     }
     static_assert(GEMV_TOKENS <= GEMV_WARPS, "one warp quantises each token");
-    __shared__ float sxs[GEMV_TOKENS], wmax[GEMV_WARPS];
+    __shared__ float sxs[GEMV_TOKENS], wmax[GEMV_WARPS], rh[GEMV_TOKENS * 64];
     if (a.cs_state) {
         // conv tails move up by one token (the readers of the old tails have finished)
         const int64_t total = static_cast<int64_t>(a.cs_n) * a.cs_c_conv;
@@ -205,6 +214,16 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_dot_kernel(GemvArgs a) {
     // the tokens' codes as packed int8, and their sums over every 16 codes
     const int kw = a.cols >> 2, k16 = a.cols >> 4;
     if (a.in_mode != 0) {
+        if (a.rms_psum) {
+            for (int i = tid; i < a.g * a.rms_hv; i += GEMV_THREADS) {
+                const int t = i / a.rms_hv, hh = i - t * a.rms_hv;
+                const float* ps = a.rms_psum + (static_cast<int64_t>(t) * a.rms_hv + hh) * a.rms_split;
+                float sum = 0.0f;
+                for (int p = 0; p < a.rms_split; ++p) sum += ps[p];
+                rh[t * 64 + hh] = rsqrtf(sum / static_cast<float>(a.rms_d) + a.rms_eps);
+            }
+            __syncthreads();
+        }
         // the warps split evenly over the tokens (wpt warps each): the row
         // amax (warp maxima combined through shared memory), then the codes
         const int wpt = GEMV_WARPS / a.g, t = warp / wpt, gl = (warp - t * wpt) * 32 + lane, gs = wpt * 32;
@@ -212,7 +231,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_dot_kernel(GemvArgs a) {
         if (t < a.g) {
             for (int b = gl; b < k16; b += gs) {
                 float w[16];
-                gemv_raw16(a, t, b, w);
+                gemv_raw16(a, t, b, w, rh);
 #pragma unroll
                 for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fabsf(w[e]));
             }
@@ -227,7 +246,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_dot_kernel(GemvArgs a) {
             if (gl == 0) sxs[t] = qsc.s;
             for (int b = gl; b < k16; b += gs) {
                 float w[16], c[16];
-                gemv_raw16(a, t, b, w);
+                gemv_raw16(a, t, b, w, rh);
                 bool redo = !qsc.fast;
 #pragma unroll
                 for (int e = 0; e < 16; ++e) c[e] = qcode_fast(w[e], qsc, redo);
@@ -347,7 +366,8 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_dot_kernel(GemvArgs a) {
 cudaError_t launch_gemv_dot(const void* blocks, bool q6k, int64_t rows, int64_t cols, const uint16_t* xc,
                               const float* sx, int64_t n, uint16_t* out_bf16, int64_t ld_bf16, int64_t n_bf16,
                               float* out_f32, int64_t ld_f32, cudaStream_t st, int in_mode, const void* xraw,
-                              float* cs_state, const uint16_t* cs_qkvz, int64_t cs_ld, int cs_c_conv, int cs_n) {
+                              float* cs_state, const uint16_t* cs_qkvz, int64_t cs_ld, int cs_c_conv, int cs_n,
+                              const float* rms_psum, int rms_hv, int rms_d, int rms_split, float rms_eps) {
     static int sms = 0, max_optin = 0;
     if (!sms) {
         int dev = 0;
@@ -385,6 +405,11 @@ cudaError_t launch_gemv_dot(const void* blocks, bool q6k, int64_t rows, int64_t 
         a.cs_ld = cs_ld;
         a.cs_c_conv = cs_c_conv;
         a.cs_n = cs_n;
+        a.rms_psum = rms_psum ? rms_psum + t0 * rms_hv * rms_split : nullptr;
+        a.rms_hv = rms_hv;
+        a.rms_d = rms_d > 0 ? rms_d : 1;
+        a.rms_split = rms_split;
+        a.rms_eps = rms_eps;
         a.g = static_cast<int>(n - t0 < gmax ? n - t0 : gmax);
         a.out_bf16 = out_bf16 ? out_bf16 + t0 * ld_bf16 : nullptr;
         a.ld_bf16 = ld_bf16;
@@ -424,7 +449,8 @@ struct MidArgs {
     const float* dt_bias;
     const float* norm_w;     // [D]
     float* state;            // [B][hv][D][D], in place
-    float* o_hat;            // [B][c_v] fp32 gated-norm output
+    float* o_hat;            // [B][c_v] fp32 gated output, not yet RMS-normalised
+    float* o_psum;           // [B][hv][MID_SPLIT] partial sums of o^2
     int hv, ratio, c_qk, c_conv, c_v;
     float eps_l2, eps_rms, q_scale;
 };
@@ -444,31 +470,40 @@ __device__ __forceinline__ float mid_block_sum(float v, float* red) {
     return r;
 }
 
-// One CTA per (value head h, sequence): the conv of its key head's q and k
-// channels and of its own v channels (SiLU, L2 norm of q and k, q scale), the
-// gates, one token of the recurrence on the head's D rows (a warp per row;
-// S_i.k, S_i.q and k.q are warp sums of the old row, o_i = a S_i.q + u k.q
-// with u = b (v_i - a S_i.k)), and the gated RMSNorm of o; everything in fp32.
+// One CTA per (value head h, block of D / MID_SPLIT of its state rows,
+// sequence): the conv of its key head's q and k channels and of its own v
+// channels (SiLU, L2 norm of q and k, q scale), the gates, one token of the
+// recurrence on its rows (a warp per row; S_i.k, S_i.q and k.q are warp sums
+// of the old row, o_i = a S_i.q + u k.q with u = b (v_i - a S_i.k)), and the
+// gated output o_i * norm_w_i * SiLU(z_i) with the block's partial sum of o^2
+// (the RMS of the head is applied by the output projection, which adds the
+// partial sums in order); everything in fp32.
+constexpr int MID_SPLIT = 4;
+
 template <int D>
 __global__ void __launch_bounds__(MID_THREADS) decode_mid_kernel(MidArgs a) {
-    constexpr int E = D / 32;   // state entries per lane
-    __shared__ float qs[D], ks[D], vs[D], gz[D], os[D], red[MID_WARPS];
+    constexpr int E = D / 32;                        // state entries per lane
+    constexpr int NR = D / MID_SPLIT;                // rows of this CTA
+    constexpr int R = NR / MID_WARPS;                // rows per warp
+    __shared__ float qs[D], ks[D], vs[NR], gz[NR], red[MID_WARPS];
     __shared__ float gate[2];
-    const int h = blockIdx.x, sq = blockIdx.y, hk = h / a.ratio;
+    const int h = blockIdx.x / MID_SPLIT, part = blockIdx.x % MID_SPLIT, sq = blockIdx.y, hk = h / a.ratio;
+    const int i0 = part * NR;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint16_t* row = a.qkvz + static_cast<int64_t>(sq) * a.ld;
     const float* tail = a.conv_state + static_cast<int64_t>(sq) * a.c_conv * 3;
-    // conv + SiLU of the 3D channels: q (key head), k (key head), v (this head)
-    for (int i = tid; i < 3 * D; i += MID_THREADS) {
-        const int part = i / D, e = i - part * D;
-        const int c = part == 0 ? hk * D + e : (part == 1 ? a.c_qk + hk * D + e : 2 * a.c_qk + h * D + e);
+    // conv + SiLU: q and k of the key head (all D), v of this CTA's rows
+    for (int i = tid; i < 2 * D + NR; i += MID_THREADS) {
+        const int part2 = i < D ? 0 : (i < 2 * D ? 1 : 2);
+        const int e = i - part2 * D;
+        const int c = part2 == 0 ? hk * D + e : (part2 == 1 ? a.c_qk + hk * D + e : 2 * a.c_qk + h * D + i0 + e);
         const float4 w = *reinterpret_cast<const float4*>(a.conv_w + static_cast<int64_t>(c) * 4);
         const float y = conv4_silu(w, tail[c * 3 + 0], tail[c * 3 + 1], tail[c * 3 + 2], bf16_bits_to_float(row[c]));
-        (part == 0 ? qs : (part == 1 ? ks : vs))[e] = y;
+        (part2 == 0 ? qs : (part2 == 1 ? ks : vs))[e] = y;
     }
-    for (int e = tid; e < D; e += MID_THREADS) {
-        const float z = bf16_bits_to_float(row[a.c_conv + h * D + e]);
-        gz[e] = silu_f(z) * a.norm_w[e];
+    for (int e = tid; e < NR; e += MID_THREADS) {
+        const float z = bf16_bits_to_float(row[a.c_conv + h * D + i0 + e]);
+        gz[e] = silu_f(z) * a.norm_w[i0 + e];
     }
     if (tid == 0) {
         const int64_t gi = static_cast<int64_t>(sq) * a.hv + h;
@@ -504,12 +539,12 @@ __global__ void __launch_bounds__(MID_THREADS) decode_mid_kernel(MidArgs a) {
     kq = warp_sum(kq);
     const float dec = gate[0], beta = gate[1];
     float* sbase = a.state + (static_cast<int64_t>(sq) * a.hv + h) * D * D + E * lane;
-    // the warp's rows i = warp + MID_WARPS * r, all loaded before the first is used
-    constexpr int R = D / MID_WARPS;
+    float* ohat = a.o_hat + static_cast<int64_t>(sq) * a.c_v + h * D + i0;
+    // the warp's rows i0 + warp + MID_WARPS * r, all loaded before the first is used
     float sr[R][E];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-        const float* sp = sbase + static_cast<int64_t>(warp + MID_WARPS * r) * D;
+        const float* sp = sbase + static_cast<int64_t>(i0 + warp + MID_WARPS * r) * D;
         if (E == 4) {
             const float4 v4 = *reinterpret_cast<const float4*>(sp);
             sr[r][0] = v4.x; sr[r][1 % E] = v4.y; sr[r][2 % E] = v4.z; sr[r][3 % E] = v4.w;
@@ -518,10 +553,11 @@ __global__ void __launch_bounds__(MID_THREADS) decode_mid_kernel(MidArgs a) {
             sr[r][0] = v2.x; sr[r][1 % E] = v2.y;
         }
     }
+    float o2 = 0.0f;   // lane 0: this warp's share of the sum of o^2
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-        const int i = warp + MID_WARPS * r;
-        float* sp = sbase + static_cast<int64_t>(i) * D;
+        const int il = warp + MID_WARPS * r;      // row within the CTA's block
+        float* sp = sbase + static_cast<int64_t>(i0 + il) * D;
         float (&s)[E] = sr[r];
         float sk = 0.0f, sqv = 0.0f;
 #pragma unroll
@@ -531,27 +567,46 @@ __global__ void __launch_bounds__(MID_THREADS) decode_mid_kernel(MidArgs a) {
         }
         sk = warp_sum(sk);
         sqv = warp_sum(sqv);
-        const float u = beta * (vs[i] - dec * sk);   // b (v_i - a S_i.k)
+        const float u = beta * (vs[il] - dec * sk);   // b (v_i - a S_i.k)
 #pragma unroll
         for (int e = 0; e < E; ++e) s[e] = fmaf(u, k[e], dec * s[e]);
         if (E == 4)
             *reinterpret_cast<float4*>(sp) = make_float4(s[0], s[1 % E], s[2 % E], s[3 % E]);
         else
             *reinterpret_cast<float2*>(sp) = make_float2(s[0], s[1 % E]);
-        if (lane == 0) os[i] = fmaf(u, kq, dec * sqv);   // S_new . q
+        if (lane == 0) {
+            const float o = fmaf(u, kq, dec * sqv);   // S_new . q
+            o2 = fmaf(o, o, o2);
+            ohat[il] = o * gz[il];
+        }
     }
-    __syncthreads();
-    // gated RMSNorm: o / sqrt(mean o^2 + eps) * norm_w * SiLU(z)
-    float o2 = 0.0f;
-    for (int e = tid; e < D; e += MID_THREADS) o2 = fmaf(os[e], os[e], o2);
-    o2 = mid_block_sum(o2, red);
-    const float r = rsqrtf(o2 / static_cast<float>(D) + a.eps_rms);
-    for (int e = tid; e < D; e += MID_THREADS)
-        a.o_hat[static_cast<int64_t>(sq) * a.c_v + h * D + e] = os[e] * r * gz[e];
+    o2 = mid_block_sum(lane == 0 ? o2 : 0.0f, red);
+    if (tid == 0) a.o_psum[(static_cast<int64_t>(sq) * a.hv + h) * MID_SPLIT + part] = o2;
+}
+
+// o_hat *= rsqrt(mean o^2 + eps) per token and head, from the partial sums
+// (the decode step's path for more tokens than one projection launch takes).
+__global__ void decode_rms_apply_kernel(float* o_hat, const float* psum, int hv, int d, int c_v, float eps) {
+    const int sq = blockIdx.y;
+    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < c_v; e += gridDim.x * blockDim.x) {
+        const int h = e / d;
+        const float* ps = psum + (static_cast<int64_t>(sq) * hv + h) * MID_SPLIT;
+        float sum = 0.0f;
+        for (int p = 0; p < MID_SPLIT; ++p) sum += ps[p];
+        o_hat[static_cast<int64_t>(sq) * c_v + e] *= rsqrtf(sum / static_cast<float>(d) + eps);
+    }
+}
+
+cudaError_t launch_decode_rms_apply(const gdn_layer& L, float* o_hat, const float* psum, int64_t n_seqs, cudaStream_t st) {
+    const int c_v = L.n_v_heads * L.dv;
+    decode_rms_apply_kernel<<<dim3(static_cast<unsigned>((c_v + 255) / 256), static_cast<unsigned>(n_seqs)), 256, 0, st>>>(
+        o_hat, psum, L.n_v_heads, L.dv, c_v, L.eps_rms);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_decode_mid(const gdn_layer& L, const uint16_t* qkvz, int64_t ld, const float* ba, int64_t ld_ba,
-                              const float* conv_state, int64_t n_seqs, float* state, float* o_hat, cudaStream_t st) {
+                              const float* conv_state, int64_t n_seqs, float* state, float* o_hat, float* o_psum,
+                              cudaStream_t st) {
     MidArgs a;
     const int d = L.dk;
     a.qkvz = qkvz;
@@ -567,6 +622,7 @@ cudaError_t launch_decode_mid(const gdn_layer& L, const uint16_t* qkvz, int64_t 
     a.norm_w = L.norm_w;
     a.state = state;
     a.o_hat = o_hat;
+    a.o_psum = o_psum;
     a.hv = L.n_v_heads;
     a.ratio = L.n_v_heads / L.n_qk_heads;
     a.c_qk = L.n_qk_heads * d;
@@ -575,7 +631,7 @@ cudaError_t launch_decode_mid(const gdn_layer& L, const uint16_t* qkvz, int64_t 
     a.eps_l2 = L.eps_l2;
     a.eps_rms = L.eps_rms;
     a.q_scale = L.q_scale;
-    const dim3 grid(static_cast<unsigned>(a.hv), static_cast<unsigned>(n_seqs));
+    const dim3 grid(static_cast<unsigned>(a.hv * MID_SPLIT), static_cast<unsigned>(n_seqs));
     if (d == 128)
         decode_mid_kernel<128><<<grid, MID_THREADS, 0, st>>>(a);
     else
