@@ -89,14 +89,6 @@ __device__ __forceinline__ uint16_t code_to_f16_bits(int q) {
     return __half_as_ushort(__int2half_rn(q));
 }
 
-// int8 quantisation code of w for the row scale s (s = amax/127):
-// clamp(rne(w / s), -127, 127) with an IEEE-correct fp32 divide; s == 0 -> 0.
-__device__ __forceinline__ int quant_code(float w, float s) {
-    if (s == 0.0f) return 0;
-    int q = __float2int_rn(__fdiv_rn(w, s));
-    return max(-127, min(127, q));
-}
-
 // Codes are carried between the quantiser and the stores as "magic" floats
 // t = q + QCODE_MAGIC (q the integer code).  QCODE_MAGIC = 1.5 * 2^23 + 0x6480
 // puts t in [2^23, 2^24), where consecutive fp32 values are the integers, so

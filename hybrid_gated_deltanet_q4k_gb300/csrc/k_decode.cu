@@ -1,7 +1,5 @@
-// The decode step of the layer: one new token for each of B sequences.
-//
-// Two kernels of its own, beside the prefill kernels it shares (activation
-// quantisation, conv with one token per sequence, gated norm):
+// The decode step of the layer: one new token for each of B sequences, in
+// three launches:
 //
 // gemv_dot_kernel -- the projections for a few tokens.  Decoding a whole
 //   weight matrix to int8 rows in HBM (step 1a of the prefill) would move 3.5x
@@ -19,18 +17,20 @@
 //   warp) arrive in shared memory by bulk copies through a ring of stages, so
 //   each row is read from HBM once with many bytes in flight.
 //
-// decode_rule_kernel -- one token of the gated delta rule per sequence, in
-//   fp32, the state read and written once:
+// decode_mid_kernel -- per (value head, block of its state rows, sequence):
+//   the conv, SiLU and L2 norms of the token's q, k, v, the gates, and one
+//   token of the gated delta rule in fp32, the state read and written once:
 //     S_i <- a S_i + b (v_i - a S_i.k) k^T,   o_i = S_i.q
-//   for every row i of every value head (rows are independent).  One warp per
-//   row: each lane holds D/32 consecutive entries; S_i.k, S_i.q and k.q are
-//   warp sums of the old row, and o_i = a S_i.q + b (v_i - a S_i.k) (k.q)
-//   needs no second pass.  The pages measure this step per decode call
-//   (#5305, child ticket #5222: the GDN recurrence at 44.7 us per call against
-//   llama.cpp's 2.5 us) and name llama.cpp's form as prior art (a token loop
-//   with the state in registers, "CRUX parity spike" #4220, technique table
-//   row 1).  o is written in fp16 (the gated norm's input
-//   type); a value beyond its range sets ERR_RANGE.
+//   for every row i (rows are independent).  One warp per row: each lane holds
+//   D/32 consecutive entries; S_i.k, S_i.q and k.q are warp sums of the old
+//   row, and o_i = a S_i.q + b (v_i - a S_i.k) (k.q) needs no second pass.
+//   The pages measure this step per decode call (#5305, child ticket #5222:
+//   the GDN recurrence at 44.7 us per call against llama.cpp's 2.5 us) and
+//   name llama.cpp's form as prior art (a token loop with the state in
+//   registers, "CRUX parity spike" #4220, technique table row 1).  It writes
+//   the gated output o * norm_w * SiLU(z) and partial sums of o^2; the
+//   output projection's kernel applies the RMS of each head, quantises the
+//   row and shifts the conv tails (the readers of the old tails are done).
 #include "common.cuh"
 #include "qk_decode.cuh"
 #include "tma.cuh"
