@@ -13,27 +13,33 @@
 // p_i = nk - nq + i:  o_i = sum_{j <= p_i} softmax_j(scale q_i.k_j) v_j.
 //
 // One CTA per (tile of 128 queries, query head), the tiles with the most keys
-// first.  Keys come in blocks of 64.  Per block j:
-//   S_j = Q K_j^T            tcgen05.mma kind::f16 (bf16), M = 128, N = 64, K = D,
-//                            into one of two TMEM buffers (S_{j+1} runs while
-//                            the softmax works on S_j)
-//   softmax warps            two threads per query row, 32 scores each from
+// first.  Keys come in blocks of 128.  Per block j:
+//   S_j = Q K_j^T            tcgen05.mma kind::f16 (bf16), M = 128, N = 128,
+//                            K = D, into one of two TMEM buffers (S_{j+1} may
+//                            run while the softmax works on S_j)
+//   softmax warps            two threads per query row, 64 scores each from
 //                            TMEM, causal mask on diagonal blocks, the running
 //                            maximum m (the halves swap their block maxima),
 //                            P_j = 2^(s scale log2e - m) in bf16 to shared
 //                            memory, l += sum P
-//   O += P_j V_j             M = 128, N = D, K = 64, O accumulated in TMEM
+//   O += P_j V_j             M = 128, K = 128, N = D in instructions of at
+//                            most 128 columns, O accumulated in TMEM
+// Blocks of 128 keys halve the instructions per key of the score product
+// against blocks of 64 (an M = 128 instruction costs about the same issue time
+// at N = 64 as at N = 128), and the tensor pipe is bound by that issue rate.
 // The maximum is raised only when a row's block maximum exceeds it by more
-// than 2^8 (so P <= 256, fine for bf16); then the warp's O rows are scaled by
-// 2^(m_old - m_new) in TMEM (tcgen05.ld / st) after the previous product has
-// finished.  O / l at the end is the softmax exactly, whatever maxima were used.
-// V is read through its transpose V^T [Hkv][D][nk], written by a transpose
-// kernel first, so both operands of both products are K-major.
-// Warps: 0 TMA (lane 0 loads K blocks, lane 1 V^T blocks, two stages each; Q
-// once), 1 TMEM owner and MMA issuer, 2-9 softmax (warp w reads TMEM lanes
-// 32 (w % 4) .. +31; warps 2-5 and 6-9 take the two halves of those rows).  Every wait is bounded; after a wait runs out the CTA
-// stops issuing, lets its copies and products finish and returns with an error
-// word set (GDN_ETIMEOUT).
+// than 2^8 (so P <= 256, fine for bf16); then the warp's O columns are scaled
+// by 2^(m_old - m_new) in TMEM (tcgen05.ld / st) after the previous product
+// has finished.  O / l at the end is the softmax exactly, whatever maxima were
+// used.  V is read through its transpose V^T [Hkv][D][nk], written by a
+// transpose kernel first, so both operands of both products are K-major.
+// Warps: 0 TMA (lane 0 loads K blocks, lane 1 V^T blocks, one stage each at
+// D = 256 and two below; Q once), 1 TMEM owner and MMA issuer (it issues S_j
+// and P_j V_j in whichever order they become ready), 2-9 softmax (warp w reads
+// TMEM lanes 32 (w % 4) .. +31; warps 2-5 and 6-9 take the two halves of those
+// rows).  Every wait is bounded; after a wait runs out the CTA stops issuing,
+// lets its copies and products finish and returns with an error word set
+// (GDN_ETIMEOUT).
 #include "common.cuh"
 #include "tma.cuh"
 #include "tcgen05.cuh"
@@ -45,30 +51,37 @@ namespace gdn {
 static __device__ int g_attn_error;
 
 constexpr int ATT_BM = 128;   // queries per CTA
-constexpr int ATT_BN = 64;    // keys per block
+constexpr int ATT_BN = 128;   // keys per block
 constexpr int ATT_SM_WARPS = 8;   // softmax warps: two per row quadrant, each half of a row's scores
 constexpr int ATT_THREADS = 64 + 32 * ATT_SM_WARPS;
 constexpr float ATT_RESCALE_LOG2 = 8.0f;   // raise the maximum only past this margin
 
+// Shared memory.  K and V^T hold one key block each at D = 256 (no room for
+// two), two at smaller D.
 template <int D>
 struct AttSmem {
     static constexpr int NS = D / 64;                    // 64-element slabs of a row
-    static constexpr int Q0 = 0;                         // Q: NS slabs of [128][64] bf16 (16 KB)
+    static constexpr int ST = D == 256 ? 1 : 2;          // key blocks held at once
+    static constexpr int Q0 = 0;                         // Q: NS slabs of [128 rows][64] bf16 (16 KB)
     static constexpr int QSLAB = ATT_BM * 128;
-    static constexpr int K0 = Q0 + NS * QSLAB;           // K: 2 stages x NS slabs of [64][64] (8 KB)
+    static constexpr int K0 = Q0 + NS * QSLAB;           // K: ST blocks x NS slabs of [128 keys][64] (16 KB)
     static constexpr int KSLAB = ATT_BN * 128;
     static constexpr int KSTAGE = NS * KSLAB;
-    static constexpr int V0 = K0 + 2 * KSTAGE;           // V^T: 2 stages of [D][64] (D x 128 B)
-    static constexpr int VSTAGE = D * 128;
-    static constexpr int P0 = V0 + 2 * VSTAGE;           // P: [128][64] bf16, one slab
-    static constexpr int B0 = P0 + ATT_BM * 128;         // mbarriers
-    // barrier indices
+    static constexpr int V0 = K0 + ST * KSTAGE;          // V^T: ST blocks x 2 slabs of [D rows][64 keys]
+    static constexpr int VSLAB = D * 128;
+    static constexpr int VSTAGE = 2 * VSLAB;
+    static constexpr int P0 = V0 + ST * VSTAGE;          // P: 2 slabs of [128 rows][64 keys] bf16
+    static constexpr int PSLAB = ATT_BM * 128;
+    static constexpr int B0 = P0 + 2 * PSLAB;            // mbarriers
+    // barrier indices: K/V full and empty per block slot, S full per TMEM buffer
     static constexpr int QF = 0, KF = 1, KE = 3, VF = 5, VE = 7, SF = 9, PF = 11, PV = 12, FIN = 13, NBAR = 14;
-    static constexpr int X0 = B0 + 8 * NBAR;             // row maxima of each half, two rounds: [2][2][128] fp32
-    static constexpr int LS0 = X0 + 2 * 2 * ATT_BM * 4;  // row sums of each half: [2][128] fp32
-    static constexpr int MISC0 = LS0 + 2 * ATT_BM * 4;   // TMEM base, abort flag
+    static constexpr int X0 = (B0 + 8 * NBAR + 15) & ~15;    // row maxima of each half: [2][128] fp32
+    static constexpr int LS0 = P0;                            // row sums of each half, after the last product
+    static constexpr int MISC0 = X0 + 2 * ATT_BM * 4;        // TMEM base, abort flag
     static constexpr int BYTES = MISC0 + 16;
 };
+
+static_assert(AttSmem<256>::BYTES + 1024 <= 227 * 1024, "d = 256 tiles must fit the shared memory of a CTA");
 
 struct AttArgs {
     int nq, nk, hq, hkv, ratio;
@@ -96,6 +109,20 @@ __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// Non-blocking test of a phase (the MMA issuer polls two kinds of work and
+// must not be suspended on one while the other is ready).
+__device__ __forceinline__ bool att_ready(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ void att_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
@@ -105,6 +132,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
 attn_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
             const __grid_constant__ CUtensorMap mv, AttArgs a) {
     using L = AttSmem<D>;
+    constexpr int ST = L::ST;
     extern __shared__ __align__(1024) unsigned char smb[];
     unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smb) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(base + L::B0);
@@ -130,6 +158,7 @@ attn_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUte
     t5::fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t sbase = smem_addr(base);
+    constexpr uint32_t OCOL = 2 * ATT_BN;   // TMEM: S in columns 0-127 and 128-255, O from 256
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA
@@ -138,59 +167,81 @@ attn_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUte
             for (int s = 0; s < L::NS; ++s)
                 tma_load_2d_tile(base + L::Q0 + s * L::QSLAB, &mq, bars + L::QF, h * D + 64 * s, q0);
             for (int j = 0; j < nb; ++j) {
-                const int st = j & 1;
-                if (j >= 2 && !att_wait(bars + L::KE + st, ((j >> 1) - 1) & 1, abort)) break;
-                mbar_expect_tx(bars + L::KF + st, L::KSTAGE);
+                const int sl = j % ST, use = j / ST;
+                if (j >= ST && !att_wait(bars + L::KE + sl, (use - 1) & 1, abort)) break;
+                mbar_expect_tx(bars + L::KF + sl, L::KSTAGE);
                 for (int s = 0; s < L::NS; ++s)
-                    tma_load_2d_tile(base + L::K0 + st * L::KSTAGE + s * L::KSLAB, &mk, bars + L::KF + st, g * D + 64 * s,
+                    tma_load_2d_tile(base + L::K0 + sl * L::KSTAGE + s * L::KSLAB, &mk, bars + L::KF + sl, g * D + 64 * s,
                                      j * ATT_BN);
             }
         } else if (lane == 1) {
             for (int j = 0; j < nb; ++j) {
-                const int st = j & 1;
-                if (j >= 2 && !att_wait(bars + L::VE + st, ((j >> 1) - 1) & 1, abort)) break;
-                mbar_expect_tx(bars + L::VF + st, L::VSTAGE);
-                tma_load_2d_tile(base + L::V0 + st * L::VSTAGE, &mv, bars + L::VF + st, j * ATT_BN, g * D);
+                const int sl = j % ST, use = j / ST;
+                if (j >= ST && !att_wait(bars + L::VE + sl, (use - 1) & 1, abort)) break;
+                mbar_expect_tx(bars + L::VF + sl, L::VSTAGE);
+                for (int s = 0; s < 2; ++s)
+                    tma_load_2d_tile(base + L::V0 + sl * L::VSTAGE + s * L::VSLAB, &mv, bars + L::VF + sl,
+                                     j * ATT_BN + 64 * s, g * D);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        // Two kinds of work, issued in whichever order they become ready: S_j
+        // (its K block has landed; S_j may run ahead of P_{j-1} V_{j-1} by one
+        // block) and P_j V_j (the softmax has written P_j, its V^T block has
+        // landed).  One thread polls both; a stall past 2 s sets the error word.
         if (lane == 0) {
-            constexpr uint32_t IDS = t5::idesc_bf16(ATT_BM, ATT_BN), IDO = t5::idesc_bf16(ATT_BM, D);
-            auto issue_s = [&](int j) {   // S_j = Q K_j^T into TMEM columns 64 (j & 1)
-                const int st = j & 1;
-                if (!att_wait(bars + L::KF + st, (j >> 1) & 1, abort)) return false;
-                t5::fence_after();
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const int s = kk >> 2, w = kk & 3;
-                    const uint64_t da = t5::desc_sw128(sbase + L::Q0 + s * L::QSLAB + w * 32);
-                    const uint64_t db = t5::desc_sw128(sbase + L::K0 + st * L::KSTAGE + s * L::KSLAB + w * 32);
-                    t5::mma_f16(tmem + st * ATT_BN, da, db, IDS, kk > 0 ? 1u : 0u);
-                }
-                t5::commit(bars + L::SF + st);
-                t5::commit(bars + L::KE + st);
-                return true;
-            };
+            constexpr int NO = D < 128 ? D : 128;   // N of one PV instruction (O in halves at D = 256)
+            constexpr uint32_t IDS = t5::idesc_bf16(ATT_BM, ATT_BN), IDO = t5::idesc_bf16(ATT_BM, NO);
             bool ok = att_wait(bars + L::QF, 0, abort);
-            if (ok) {
-                t5::fence_after();
-                ok = issue_s(0);
-            }
-            if (ok && nb > 1) ok = issue_s(1);
-            for (int j = 0; ok && j < nb; ++j) {
-                const int st = j & 1;
-                if (!att_wait(bars + L::PF, j & 1, abort) || !att_wait(bars + L::VF + st, (j >> 1) & 1, abort)) break;
-                t5::fence_after();
+            if (ok) t5::fence_after();
+            int ns = 0, np = 0;   // the next S and PV to issue
+            uint64_t t_last = globaltimer_ns();
+            while (ok && np < nb) {
+                bool did = false;
+                if (ns < nb && ns <= np + 1 && att_ready(bars + L::KF + ns % ST, (ns / ST) & 1)) {
+                    // S_ns = Q K_ns^T into TMEM columns 128 (ns & 1); that buffer's
+                    // previous scores (block ns - 2) were read before P_{ns-2}
+                    t5::fence_after();
+                    const int sl = ns % ST;
 #pragma unroll
-                for (int kk = 0; kk < ATT_BN / 16; ++kk) {   // O += P_j V_j  (columns 128 ..)
-                    const uint64_t da = t5::desc_sw128(sbase + L::P0 + kk * 32);
-                    const uint64_t db = t5::desc_sw128(sbase + L::V0 + st * L::VSTAGE + kk * 32);
-                    t5::mma_f16(tmem + 2 * ATT_BN, da, db, IDO, (j > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const int s = kk >> 2, w = kk & 3;
+                        const uint64_t da = t5::desc_sw128(sbase + L::Q0 + s * L::QSLAB + w * 32);
+                        const uint64_t db = t5::desc_sw128(sbase + L::K0 + sl * L::KSTAGE + s * L::KSLAB + w * 32);
+                        t5::mma_f16(tmem + (ns & 1) * ATT_BN, da, db, IDS, kk > 0 ? 1u : 0u);
+                    }
+                    t5::commit(bars + L::SF + (ns & 1));
+                    t5::commit(bars + L::KE + sl);
+                    ++ns;
+                    did = true;
+                } else if (np < ns && att_ready(bars + L::PF, np & 1) && att_ready(bars + L::VF + np % ST, (np / ST) & 1)) {
+                    // O += P_np V_np over 8 key steps of 16
+                    t5::fence_after();
+                    const int sl = np % ST;
+#pragma unroll
+                    for (int kk = 0; kk < ATT_BN / 16; ++kk) {
+                        const int s = kk >> 2, w = kk & 3;
+                        const uint64_t da = t5::desc_sw128(sbase + L::P0 + s * L::PSLAB + w * 32);
+#pragma unroll
+                        for (int nh = 0; nh < D / NO; ++nh) {
+                            const uint64_t db = t5::desc_sw128(sbase + L::V0 + sl * L::VSTAGE + s * L::VSLAB +
+                                                               nh * NO * 128 + w * 32);
+                            t5::mma_f16(tmem + OCOL + nh * NO, da, db, IDO, (np > 0 || kk > 0) ? 1u : 0u);
+                        }
+                    }
+                    t5::commit(bars + L::PV);
+                    t5::commit(bars + L::VE + sl);
+                    ++np;
+                    did = true;
                 }
-                t5::commit(bars + L::PV);
-                t5::commit(bars + L::VE + st);
-                if (j + 2 < nb) ok = issue_s(j + 2);
+                if (did) {
+                    t_last = globaltimer_ns();
+                } else if (*abort || globaltimer_ns() - t_last > 2000000000ull) {
+                    if (!*abort) atomicCAS(&g_attn_error, 0, ERR_WAIT_TIMEOUT);
+                    *abort = 1;
+                    ok = false;
+                }
             }
             // every product issued has completed before TMEM is released
             t5::commit(bars + L::FIN);
@@ -200,10 +251,10 @@ attn_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUte
     } else {
         // ------------------------------------------------------------ softmax
         // Warp w reads TMEM lanes 32 (w % 4) .. +31 (rows r); warps 2-5 take the
-        // scores 0-31 of their rows' block and the O columns 0 .. D/2-1, warps
-        // 6-9 the scores 32-63 and O columns D/2 .. D-1; the two halves of a row
-        // swap their block maxima through shared memory (two rounds of buffers)
-        // and keep partial sums, added at the end.
+        // scores 0-63 of their rows' block and the O columns 0 .. D/2-1, warps
+        // 6-9 the scores 64-127 and O columns D/2 .. D-1; the two halves of a
+        // row swap their block maxima through shared memory and keep partial
+        // sums, added at the end.
         const int quad = warp & 3, half = (warp - 2) >> 2, r = 32 * quad + lane, pos = off + q0 + r;
         const uint32_t trow = tmem + (static_cast<uint32_t>(32 * quad) << 16);
         float* xmax = reinterpret_cast<float*>(base + L::X0);
@@ -212,26 +263,35 @@ attn_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUte
         float m = 0.0f, l = 0.0f;
         bool ok = true;
         for (int j = 0; j < nb; ++j) {
-            const int st = j & 1;
-            ok = __all_sync(0xffffffffu, ok && att_wait(bars + L::SF + st, (j >> 1) & 1, abort));
-            float x[32];
+            const int sb = j & 1;
+            ok = __all_sync(0xffffffffu, ok && att_wait(bars + L::SF + sb, (j >> 1) & 1, abort));
+            float x[64];
             float bm = -INFINITY;
             if (ok) {
                 t5::fence_after();
-                t5::ld32(trow + st * ATT_BN + 32 * half, x);
-                const int key0 = j * ATT_BN + 32 * half;
-                if (key0 + 31 > pos_min || key0 + 31 >= a.nk) {   // a block on the diagonal or past the keys
+                float s0[32], s1[32];
+                t5::ld32(trow + sb * ATT_BN + 64 * half, s0);
+                t5::ld32(trow + sb * ATT_BN + 64 * half + 32, s1);
 #pragma unroll
-                    for (int c = 0; c < 32; ++c)
+                for (int c = 0; c < 32; ++c) {
+                    x[c] = s0[c];
+                    x[32 + c] = s1[c];
+                }
+                const int key0 = j * ATT_BN + 64 * half;
+                if (key0 + 63 > pos_min || key0 + 63 >= a.nk) {   // a block on the diagonal or past the keys
+#pragma unroll
+                    for (int c = 0; c < 64; ++c)
                         if (!(key0 + c <= pos && key0 + c < a.nk)) x[c] = -INFINITY;
                 }
 #pragma unroll
-                for (int c = 0; c < 32; ++c) bm = fmaxf(bm, x[c]);
+                for (int c = 0; c < 64; ++c) bm = fmaxf(bm, x[c]);
             }
-            // the row's maximum over both halves (raw scores; the scale is positive)
-            xmax[(st * 2 + half) * ATT_BM + r] = bm;
+            // the row's maximum over both halves (raw scores; the scale is positive);
+            // the second barrier keeps the next block's write after both reads
+            xmax[half * ATT_BM + r] = bm;
             asm volatile("bar.sync 1, %0;" ::"n"(32 * ATT_SM_WARPS) : "memory");
-            bm = fmaxf(bm, xmax[(st * 2 + (half ^ 1)) * ATT_BM + r]) * a.sl2;
+            bm = fmaxf(bm, xmax[(half ^ 1) * ATT_BM + r]) * a.sl2;
+            asm volatile("bar.sync 1, %0;" ::"n"(32 * ATT_SM_WARPS) : "memory");
             // the previous product must be done before P is rewritten or O rescaled
             if (j > 0) ok = __all_sync(0xffffffffu, ok && att_wait(bars + L::PV, (j - 1) & 1, abort));
             if (!ok) {
@@ -248,23 +308,23 @@ attn_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUte
 #pragma unroll 1
                 for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 32) {
                     float ov[32];
-                    t5::ld32(trow + 2 * ATT_BN + c0, ov);
+                    t5::ld32(trow + OCOL + c0, ov);
 #pragma unroll
                     for (int e = 0; e < 32; ++e) ov[e] *= alpha;
-                    t5::st32(trow + 2 * ATT_BN + c0, ov);
+                    t5::st32(trow + OCOL + c0, ov);
                 }
             }
-            // P = 2^(s scale log2e - m) in bf16 (the 128-byte-swizzled K-major image)
+            // P = 2^(s scale log2e - m) in bf16 (slab `half` of the 128-byte-swizzled K-major image)
             float sum = 0.0f;
 #pragma unroll
-            for (int c = 0; c < 32; c += 8) {
+            for (int c = 0; c < 64; c += 8) {
                 float p[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     p[e] = ex2_approx(fmaf(x[c + e], a.sl2, -m));
                     sum += p[e];
                 }
-                *reinterpret_cast<uint4*>(base + L::P0 + sw128_f16(r, 32 * half + c)) =
+                *reinterpret_cast<uint4*>(base + L::P0 + half * L::PSLAB + sw128_f16(r, c)) =
                     make_uint4(bf16x2_bits(p[0], p[1]), bf16x2_bits(p[2], p[3]), bf16x2_bits(p[4], p[5]),
                                bf16x2_bits(p[6], p[7]));
             }
@@ -273,9 +333,9 @@ attn_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUte
             t5::fence_before();
             att_arrive(bars + L::PF);
         }
-        lsum[half * ATT_BM + r] = l;
-        asm volatile("bar.sync 1, %0;" ::"n"(32 * ATT_SM_WARPS) : "memory");
         ok = __all_sync(0xffffffffu, ok && att_wait(bars + L::PV, (nb - 1) & 1, abort));
+        lsum[half * ATT_BM + r] = l;   // the P area is free: the last product has finished
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * ATT_SM_WARPS) : "memory");
         if (ok) {
             t5::fence_after();
             const float inv = 1.0f / (lsum[r] + lsum[ATT_BM + r]);
@@ -284,7 +344,7 @@ attn_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUte
 #pragma unroll 1
             for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 32) {
                 float ov[32];
-                t5::ld32(trow + 2 * ATT_BN + c0, ov);
+                t5::ld32(trow + OCOL + c0, ov);
                 if (store) {
 #pragma unroll
                     for (int e = 0; e < 32; e += 8)
