@@ -15,31 +15,32 @@
 // One CTA per (tile of 128 queries, query head), the tiles with the most keys
 // first.  Keys come in blocks of 128.  Per block j:
 //   S_j = Q K_j^T            tcgen05.mma kind::f16 (bf16), M = 128, N = 128,
-//                            K = D, into one of two TMEM buffers (S_{j+1} may
-//                            run while the softmax works on S_j)
+//                            K = D, A and B from shared memory, into TMEM
 //   softmax warps            two threads per query row, 64 scores each from
-//                            TMEM, causal mask on diagonal blocks, the running
+//                            TMEM (once read, S_{j+1} may overwrite them),
+//                            causal mask on diagonal blocks, the running
 //                            maximum m (the halves swap their block maxima),
-//                            P_j = 2^(s scale log2e - m) in bf16 to shared
-//                            memory, l += sum P
-//   O += P_j V_j             M = 128, K = 128, N = D in instructions of at
-//                            most 128 columns, O accumulated in TMEM
-// Blocks of 128 keys halve the instructions per key of the score product
-// against blocks of 64 (an M = 128 instruction costs about the same issue time
-// at N = 64 as at N = 128), and the tensor pipe is bound by that issue rate.
+//                            P_j = 2^(s scale log2e - m) in bf16 back into
+//                            TMEM (two buffers), l += sum P
+//   O += P_j V_j             M = 128, K = 128, N = D, A (P) from TMEM, B (V^T)
+//                            from shared memory, O accumulated in TMEM
+// An M = 128, N = 128 instruction with both operands in shared memory reads
+// about as many bytes per cycle as shared memory delivers, so shared-memory
+// traffic (operand reads, TMA writes of K and V^T) bounds the kernel with the
+// tensor math: P kept in TMEM takes its writes and the second product's A
+// reads off shared memory.
 // The maximum is raised only when a row's block maximum exceeds it by more
 // than 2^8 (so P <= 256, fine for bf16); then the warp's O columns are scaled
 // by 2^(m_old - m_new) in TMEM (tcgen05.ld / st) after the previous product
 // has finished.  O / l at the end is the softmax exactly, whatever maxima were
 // used.  V is read through its transpose V^T [Hkv][D][nk], written by a
-// transpose kernel first, so both operands of both products are K-major.
-// Warps: 0 TMA (lane 0 loads K blocks, lane 1 V^T blocks, one stage each at
-// D = 256 and two below; Q once), 1 TMEM owner and MMA issuer (it issues S_j
-// and P_j V_j in whichever order they become ready), 2-9 softmax (warp w reads
-// TMEM lanes 32 (w % 4) .. +31; warps 2-5 and 6-9 take the two halves of those
-// rows).  Every wait is bounded; after a wait runs out the CTA stops issuing,
-// lets its copies and products finish and returns with an error word set
-// (GDN_ETIMEOUT).
+// transpose kernel first, so the B operands of both products are K-major.
+// Warps: 0 TMA for Q and K, 10 TMA for V^T (one block each at D = 256, two
+// below), 1 TMEM owner and MMA issuer (it issues S_j and P_j V_j in whichever
+// order they become ready), 2-9 softmax (warp w reads TMEM lanes 32 (w % 4)
+// .. +31; warps 2-5 and 6-9 take the two halves of those rows).  Every wait is
+// bounded; after a wait runs out the CTA stops issuing, lets its copies and
+// products finish and returns with an error word set (GDN_ETIMEOUT).
 #include "common.cuh"
 #include "tma.cuh"
 #include "tcgen05.cuh"
@@ -53,11 +54,12 @@ static __device__ int g_attn_error;
 constexpr int ATT_BM = 128;   // queries per CTA
 constexpr int ATT_BN = 128;   // keys per block
 constexpr int ATT_SM_WARPS = 8;   // softmax warps: two per row quadrant, each half of a row's scores
-constexpr int ATT_THREADS = 64 + 32 * ATT_SM_WARPS;
+constexpr int ATT_THREADS = 96 + 32 * ATT_SM_WARPS;
+constexpr int ATT_VWARP = 2 + ATT_SM_WARPS;
 constexpr float ATT_RESCALE_LOG2 = 8.0f;   // raise the maximum only past this margin
 
 // Shared memory.  K and V^T hold one key block each at D = 256 (no room for
-// two), two at smaller D.
+// two), two at smaller D.  P lives in TMEM, not here.
 template <int D>
 struct AttSmem {
     static constexpr int NS = D / 64;                    // 64-element slabs of a row
@@ -70,14 +72,14 @@ struct AttSmem {
     static constexpr int V0 = K0 + ST * KSTAGE;          // V^T: ST blocks x 2 slabs of [D rows][64 keys]
     static constexpr int VSLAB = D * 128;
     static constexpr int VSTAGE = 2 * VSLAB;
-    static constexpr int P0 = V0 + ST * VSTAGE;          // P: 2 slabs of [128 rows][64 keys] bf16
-    static constexpr int PSLAB = ATT_BM * 128;
-    static constexpr int B0 = P0 + 2 * PSLAB;            // mbarriers
-    // barrier indices: K/V full and empty per block slot, S full per TMEM buffer
-    static constexpr int QF = 0, KF = 1, KE = 3, VF = 5, VE = 7, SF = 9, PF = 11, PV = 12, FIN = 13, NBAR = 14;
-    static constexpr int X0 = (B0 + 8 * NBAR + 15) & ~15;    // row maxima of each half: [2][128] fp32
-    static constexpr int LS0 = P0;                            // row sums of each half, after the last product
-    static constexpr int MISC0 = X0 + 2 * ATT_BM * 4;        // TMEM base, abort flag
+    static constexpr int B0 = V0 + ST * VSTAGE;          // mbarriers
+    // barrier indices: Q full; K and V^T full / empty per block slot; S full;
+    // S consumed (the softmax has read it); P full and P V done per P buffer
+    static constexpr int QF = 0, KF = 1, KE = 3, VF = 5, VE = 7, SF = 9, SC = 10, PF = 11, PV = 13, FIN = 15,
+                         NBAR = 16;
+    static constexpr int X0 = (B0 + 8 * NBAR + 15) & ~15;    // row maxima: [2 rounds][2 halves][128] fp32
+    static constexpr int LS0 = X0 + 4 * ATT_BM * 4;          // row sums of each half: [2][128] fp32
+    static constexpr int MISC0 = LS0 + 2 * ATT_BM * 4;       // TMEM base, abort flag
     static constexpr int BYTES = MISC0 + 16;
 };
 
@@ -148,7 +150,8 @@ attn_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUte
     const int nb = last_pos / ATT_BN + 1;                     // key blocks it needs
 
     if (tid == 0) {
-        for (int i = 0; i < L::NBAR; ++i) mbar_init_cta(bars + i, i == L::PF ? 32 * ATT_SM_WARPS : 1);
+        for (int i = 0; i < L::NBAR; ++i)
+            mbar_init_cta(bars + i, (i == L::SC || i == L::PF || i == L::PF + 1) ? 32 * ATT_SM_WARPS : 1);
         mbar_init_fence();
         *abort = 0;
     }
@@ -158,10 +161,11 @@ attn_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUte
     t5::fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t sbase = smem_addr(base);
-    constexpr uint32_t OCOL = 2 * ATT_BN;   // TMEM: S in columns 0-127 and 128-255, O from 256
+    // TMEM columns: S 0-127 (fp32), P_j 128 + 64 (j & 1) .. +63 (bf16 pairs), O from 256
+    constexpr uint32_t PCOL = ATT_BN, OCOL = 2 * ATT_BN;
 
     if (warp == 0) {
-        // ------------------------------------------------------------ TMA
+        // ------------------------------------------------------------ TMA: Q, K
         if (lane == 0) {
             mbar_expect_tx(bars + L::QF, L::NS * L::QSLAB);
             for (int s = 0; s < L::NS; ++s)
@@ -174,7 +178,10 @@ attn_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUte
                     tma_load_2d_tile(base + L::K0 + sl * L::KSTAGE + s * L::KSLAB, &mk, bars + L::KF + sl, g * D + 64 * s,
                                      j * ATT_BN);
             }
-        } else if (lane == 1) {
+        }
+    } else if (warp == ATT_VWARP) {
+        // ------------------------------------------------------------ TMA: V^T
+        if (lane == 0) {
             for (int j = 0; j < nb; ++j) {
                 const int sl = j % ST, use = j / ST;
                 if (j >= ST && !att_wait(bars + L::VE + sl, (use - 1) & 1, abort)) break;
@@ -187,21 +194,21 @@ attn_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUte
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         // Two kinds of work, issued in whichever order they become ready: S_j
-        // (its K block has landed; S_j may run ahead of P_{j-1} V_{j-1} by one
-        // block) and P_j V_j (the softmax has written P_j, its V^T block has
-        // landed).  One thread polls both; a stall past 2 s sets the error word.
+        // (its K block has landed and the softmax has read S_{j-1}; S_j may
+        // run ahead of P_{j-1} V_{j-1} by one block) and P_j V_j (the softmax
+        // has written P_j, its V^T block has landed).  One thread polls both;
+        // a stall past 2 s sets the error word.
         if (lane == 0) {
-            constexpr int NO = D < 128 ? D : 128;   // N of one PV instruction (O in halves at D = 256)
-            constexpr uint32_t IDS = t5::idesc_bf16(ATT_BM, ATT_BN), IDO = t5::idesc_bf16(ATT_BM, NO);
+            constexpr uint32_t IDS = t5::idesc_bf16(ATT_BM, ATT_BN), IDO = t5::idesc_bf16(ATT_BM, D);
             bool ok = att_wait(bars + L::QF, 0, abort);
             if (ok) t5::fence_after();
             int ns = 0, np = 0;   // the next S and PV to issue
             uint64_t t_last = globaltimer_ns();
             while (ok && np < nb) {
                 bool did = false;
-                if (ns < nb && ns <= np + 1 && att_ready(bars + L::KF + ns % ST, (ns / ST) & 1)) {
-                    // S_ns = Q K_ns^T into TMEM columns 128 (ns & 1); that buffer's
-                    // previous scores (block ns - 2) were read before P_{ns-2}
+                if (ns < nb && ns <= np + 1 && (ns == 0 || att_ready(bars + L::SC, (ns - 1) & 1)) &&
+                    att_ready(bars + L::KF + ns % ST, (ns / ST) & 1)) {
+                    // S_ns = Q K_ns^T into TMEM columns 0-127
                     t5::fence_after();
                     const int sl = ns % ST;
 #pragma unroll
@@ -209,28 +216,25 @@ attn_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUte
                         const int s = kk >> 2, w = kk & 3;
                         const uint64_t da = t5::desc_sw128(sbase + L::Q0 + s * L::QSLAB + w * 32);
                         const uint64_t db = t5::desc_sw128(sbase + L::K0 + sl * L::KSTAGE + s * L::KSLAB + w * 32);
-                        t5::mma_f16(tmem + (ns & 1) * ATT_BN, da, db, IDS, kk > 0 ? 1u : 0u);
+                        t5::mma_f16(tmem, da, db, IDS, kk > 0 ? 1u : 0u);
                     }
-                    t5::commit(bars + L::SF + (ns & 1));
+                    t5::commit(bars + L::SF);
                     t5::commit(bars + L::KE + sl);
                     ++ns;
                     did = true;
-                } else if (np < ns && att_ready(bars + L::PF, np & 1) && att_ready(bars + L::VF + np % ST, (np / ST) & 1)) {
-                    // O += P_np V_np over 8 key steps of 16
+                } else if (np < ns && att_ready(bars + L::PF + (np & 1), (np >> 1) & 1) &&
+                           att_ready(bars + L::VF + np % ST, (np / ST) & 1)) {
+                    // O += P_np V_np over 8 key steps of 16, P from TMEM, N = D
                     t5::fence_after();
                     const int sl = np % ST;
+                    const uint32_t pa = tmem + PCOL + (np & 1) * (ATT_BN / 2);
 #pragma unroll
                     for (int kk = 0; kk < ATT_BN / 16; ++kk) {
                         const int s = kk >> 2, w = kk & 3;
-                        const uint64_t da = t5::desc_sw128(sbase + L::P0 + s * L::PSLAB + w * 32);
-#pragma unroll
-                        for (int nh = 0; nh < D / NO; ++nh) {
-                            const uint64_t db = t5::desc_sw128(sbase + L::V0 + sl * L::VSTAGE + s * L::VSLAB +
-                                                               nh * NO * 128 + w * 32);
-                            t5::mma_f16(tmem + OCOL + nh * NO, da, db, IDO, (np > 0 || kk > 0) ? 1u : 0u);
-                        }
+                        const uint64_t db = t5::desc_sw128(sbase + L::V0 + sl * L::VSTAGE + s * L::VSLAB + w * 32);
+                        t5::mma_f16_ts(tmem + OCOL, pa + kk * 8, db, IDO, (np > 0 || kk > 0) ? 1u : 0u);
                     }
-                    t5::commit(bars + L::PV);
+                    t5::commit(bars + L::PV + (np & 1));
                     t5::commit(bars + L::VE + sl);
                     ++np;
                     did = true;
@@ -253,8 +257,8 @@ attn_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUte
         // Warp w reads TMEM lanes 32 (w % 4) .. +31 (rows r); warps 2-5 take the
         // scores 0-63 of their rows' block and the O columns 0 .. D/2-1, warps
         // 6-9 the scores 64-127 and O columns D/2 .. D-1; the two halves of a
-        // row swap their block maxima through shared memory and keep partial
-        // sums, added at the end.
+        // row swap their block maxima through shared memory (two rounds of
+        // buffers) and keep partial sums, added at the end.
         const int quad = warp & 3, half = (warp - 2) >> 2, r = 32 * quad + lane, pos = off + q0 + r;
         const uint32_t trow = tmem + (static_cast<uint32_t>(32 * quad) << 16);
         float* xmax = reinterpret_cast<float*>(base + L::X0);
@@ -263,20 +267,24 @@ attn_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUte
         float m = 0.0f, l = 0.0f;
         bool ok = true;
         for (int j = 0; j < nb; ++j) {
-            const int sb = j & 1;
-            ok = __all_sync(0xffffffffu, ok && att_wait(bars + L::SF + sb, (j >> 1) & 1, abort));
+            ok = __all_sync(0xffffffffu, ok && att_wait(bars + L::SF, j & 1, abort));
             float x[64];
             float bm = -INFINITY;
             if (ok) {
                 t5::fence_after();
                 float s0[32], s1[32];
-                t5::ld32(trow + sb * ATT_BN + 64 * half, s0);
-                t5::ld32(trow + sb * ATT_BN + 64 * half + 32, s1);
+                t5::ld32(trow + 64 * half, s0);
+                t5::ld32(trow + 64 * half + 32, s1);
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
                     x[c] = s0[c];
                     x[32 + c] = s1[c];
                 }
+            }
+            // S_j is in registers: S_{j+1} may overwrite it
+            t5::fence_before();
+            att_arrive(bars + L::SC);
+            if (ok) {
                 const int key0 = j * ATT_BN + 64 * half;
                 if (key0 + 63 > pos_min || key0 + 63 >= a.nk) {   // a block on the diagonal or past the keys
 #pragma unroll
@@ -286,21 +294,25 @@ attn_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUte
 #pragma unroll
                 for (int c = 0; c < 64; ++c) bm = fmaxf(bm, x[c]);
             }
-            // the row's maximum over both halves (raw scores; the scale is positive);
-            // the second barrier keeps the next block's write after both reads
-            xmax[half * ATT_BM + r] = bm;
+            // the row's maximum over both halves (raw scores; the scale is positive)
+            xmax[((j & 1) * 2 + half) * ATT_BM + r] = bm;
             asm volatile("bar.sync 1, %0;" ::"n"(32 * ATT_SM_WARPS) : "memory");
-            bm = fmaxf(bm, xmax[(half ^ 1) * ATT_BM + r]) * a.sl2;
-            asm volatile("bar.sync 1, %0;" ::"n"(32 * ATT_SM_WARPS) : "memory");
-            // the previous product must be done before P is rewritten or O rescaled
-            if (j > 0) ok = __all_sync(0xffffffffu, ok && att_wait(bars + L::PV, (j - 1) & 1, abort));
+            bm = fmaxf(bm, xmax[((j & 1) * 2 + (half ^ 1)) * ATT_BM + r]) * a.sl2;
+            // P buffer j & 1 is free once P_{j-2} V_{j-2} has finished
+            if (j >= 2) ok = __all_sync(0xffffffffu, ok && att_wait(bars + L::PV + (j & 1), ((j - 2) >> 1) & 1, abort));
             if (!ok) {
-                att_arrive(bars + L::PF);
+                att_arrive(bars + L::PF + (j & 1));
                 continue;
             }
             if (j == 0) {
                 m = bm;   // finite: key 0 is visible to every query
             } else if (__any_sync(0xffffffffu, bm > m + ATT_RESCALE_LOG2)) {
+                // O is rescaled once P_{j-1} V_{j-1} has finished
+                ok = __all_sync(0xffffffffu, att_wait(bars + L::PV + ((j - 1) & 1), ((j - 1) >> 1) & 1, abort));
+                if (!ok) {
+                    att_arrive(bars + L::PF + (j & 1));
+                    continue;
+                }
                 const float mn = fmaxf(m, bm), alpha = ex2_approx(m - mn);
                 m = mn;
                 l *= alpha;
@@ -314,27 +326,25 @@ attn_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUte
                     t5::st32(trow + OCOL + c0, ov);
                 }
             }
-            // P = 2^(s scale log2e - m) in bf16 (slab `half` of the 128-byte-swizzled K-major image)
+            // P = 2^(s scale log2e - m) in bf16 pairs, this half's 64 keys into
+            // 32 TMEM columns of P buffer j & 1
             float sum = 0.0f;
+            uint32_t pk[32];
 #pragma unroll
-            for (int c = 0; c < 64; c += 8) {
-                float p[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    p[e] = ex2_approx(fmaf(x[c + e], a.sl2, -m));
-                    sum += p[e];
-                }
-                *reinterpret_cast<uint4*>(base + L::P0 + half * L::PSLAB + sw128_f16(r, c)) =
-                    make_uint4(bf16x2_bits(p[0], p[1]), bf16x2_bits(p[2], p[3]), bf16x2_bits(p[4], p[5]),
-                               bf16x2_bits(p[6], p[7]));
+            for (int c = 0; c < 32; ++c) {
+                const float p0 = ex2_approx(fmaf(x[2 * c], a.sl2, -m));
+                const float p1 = ex2_approx(fmaf(x[2 * c + 1], a.sl2, -m));
+                sum += p0 + p1;
+                pk[c] = bf16x2_bits(p0, p1);
             }
             l += sum;
-            fence_proxy_async_smem();
+            t5::fence_after();   // after the wait for P_{j-2} V_{j-2}
+            t5::st32u(trow + PCOL + (j & 1) * (ATT_BN / 2) + 32 * half, pk);
             t5::fence_before();
-            att_arrive(bars + L::PF);
+            att_arrive(bars + L::PF + (j & 1));
         }
-        ok = __all_sync(0xffffffffu, ok && att_wait(bars + L::PV, (nb - 1) & 1, abort));
-        lsum[half * ATT_BM + r] = l;   // the P area is free: the last product has finished
+        ok = __all_sync(0xffffffffu, ok && att_wait(bars + L::PV + ((nb - 1) & 1), ((nb - 1) >> 1) & 1, abort));
+        lsum[half * ATT_BM + r] = l;
         asm volatile("bar.sync 1, %0;" ::"n"(32 * ATT_SM_WARPS) : "memory");
         if (ok) {
             t5::fence_after();
