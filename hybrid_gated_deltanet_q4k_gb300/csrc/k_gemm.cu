@@ -40,6 +40,7 @@
 // (bounded) for the copies and MMAs in flight, meets its peer at the closing
 // cluster barrier, frees the TMEM and returns.
 #include "common.cuh"
+#include "tcgen05.cuh"
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -130,16 +131,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
 }
 
-// TMA into this CTA's shared memory; completion is counted on the mbarrier at
-// shared::cluster address `bar` (the even CTA's, for either CTA of the pair).
-__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-            smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
-
 // Tensor store of a shared-memory tile (bulk async group of this thread).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
@@ -150,28 +141,6 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void*
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_group_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-// shared::cluster address of this CTA's shared variable at `p` in CTA `rank`.
-__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
-    return r;
-}
-
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// arrive once on the mbarrier at shared::cluster address `bar` (possibly the peer's)
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
-}
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -190,23 +159,12 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
 // The pair product: descriptors address this (even) CTA's tiles; the odd CTA's
 // tiles sit at the same offsets of its shared memory.
 __device__ __forceinline__ void mma_f16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(tc::IDESC), "r"(accumulate)
-        : "memory");
+    t5::mma_f16_pair(d_tmem, adesc, bdesc, tc::IDESC, accumulate);
 }
 
 // Arrive on the mbarrier at this offset in both CTAs of the pair once the MMAs
 // issued so far have completed.
-__device__ __forceinline__ void mma_commit_pair(uint64_t* bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"(static_cast<uint16_t>(3))
-        : "memory");
-}
+__device__ __forceinline__ void mma_commit_pair(uint64_t* bar) { t5::commit_pair(bar); }
 
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
@@ -313,10 +271,7 @@ gemm_codes_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                     "r"(TMEM_COLS)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+        t5::alloc_pair(tmem_slot, TMEM_COLS);
     }
     tc_fence_before();
     // both CTAs' barriers are initialised before either signals the other's
@@ -490,7 +445,7 @@ gemm_codes_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     cluster_sync();
     if (warp == 1) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS) : "memory");
+        t5::dealloc_pair(tmem_base, TMEM_COLS);
     }
 }
 

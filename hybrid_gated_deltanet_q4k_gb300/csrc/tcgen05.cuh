@@ -100,6 +100,42 @@ __device__ __forceinline__ void commit(uint64_t* bar) {
                  : "memory");
 }
 
+// ---- the two-SM mode (CTA pairs, tcgen05 .cta_group::2): one instruction of
+// the even CTA multiplies M = 256 rows (each CTA's A rows: shared memory at the
+// same offsets in both, or each CTA's TMEM lanes) by N columns whose B rows
+// are split in halves between the two CTAs' shared memory; each CTA's TMEM
+// receives its own 128 rows.
+
+// Whole warp of each CTA of the pair: allocate `cols` TMEM columns in both.
+__device__ __forceinline__ void alloc_pair(uint32_t* slot, uint32_t cols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(slot)), "r"(cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void dealloc_pair(uint32_t base, uint32_t cols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(base), "r"(cols) : "memory");
+}
+
+__device__ __forceinline__ void mma_f16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive on the mbarrier at this offset in both CTAs of the pair once the pair
+// MMAs issued so far have completed.
+__device__ __forceinline__ void commit_pair(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_addr(bar)),
+        "h"(static_cast<uint16_t>(3))
+        : "memory");
+}
+
 // Whole warp: 16 consecutive 32-bit columns of this thread's TMEM lane.  The
 // load and its wait are one asm statement, so no use of the values can be
 // scheduled before the data has arrived.
