@@ -65,6 +65,11 @@ inline SeqTable one_seq_table(int64_t n, int per) {
     return make_seq_table(cu, 1, per);
 }
 
+// Let the next kernel in the stream, when it is launched as a programmatic
+// dependent, start now (its CTAs wait with griddepcontrol.wait before they
+// read anything this kernel writes); no effect otherwise.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

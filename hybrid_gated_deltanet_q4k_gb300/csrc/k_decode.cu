@@ -43,7 +43,7 @@ constexpr int GEMV_THREADS = 256;
 constexpr int GEMV_WARPS = GEMV_THREADS / 32;          // = rows per tile: one row per warp
 constexpr int GEMV_TOKENS = GDN_DECODE_GEMV_TOKENS;   // tokens per launch (codes in shared memory)
 constexpr int GEMV_MAX_STAGES = 4;
-constexpr int GEMV_SMEM_BUDGET = 112 * 1024;          // two CTAs per SM when the tiles allow
+constexpr int GEMV_SM_SMEM = 227 * 1024;              // shared memory of an SM for the CTAs it holds
 
 struct GemvArgs {
     const uint8_t* blocks;   // [rows][cols/256] superblocks
@@ -112,8 +112,9 @@ __host__ __device__ inline int64_t gemv_xsum_offset(int g, int cols) { return (s
 __host__ __device__ inline int64_t gemv_ring_offset(int g, int cols) {
     return (gemv_xsum_offset(g, cols) + static_cast<int64_t>(g) * (cols / 16) * 4 + 127) & ~127LL;
 }
+// ... then per stage a count of the warps done with it, and an abort flag.
 __host__ __device__ inline int64_t gemv_smem_bytes(int g, int cols, int64_t row_bytes, int stages) {
-    return gemv_ring_offset(g, cols) + stages * gemv_tile_bytes(row_bytes) + 8 * GEMV_MAX_STAGES;
+    return gemv_ring_offset(g, cols) + stages * gemv_tile_bytes(row_bytes) + 12 * GEMV_MAX_STAGES + 4;
 }
 
 // Copy tile `tile` into stage `s`: the whole bytes by one bulk copy (a tile
@@ -180,24 +181,46 @@ __device__ __forceinline__ void span_codes(const uint8_t* blk, int j, uint32_t (
     }
 }
 
-template <bool Q6>
-__global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_dot_kernel(GemvArgs a) {
+// Bounded wait of one warp on a stage: gives up at once after any earlier
+// wait of the CTA ran out.
+__device__ __forceinline__ bool gemv_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+    if (*abort) return false;
+    if (mbar_wait_bounded(bar, parity, &g_decode_error, ERR_WAIT_TIMEOUT)) return true;
+    *abort = 1;
+    return false;
+}
+
+// G: tokens the kernel computes (a power of two >= a.g; the codes of tokens
+// a.g .. G-1 are zero and their sums are not stored).
+template <bool Q6, int G>
+__global__ void __launch_bounds__(GEMV_THREADS, G <= 2 ? 4 : 2) gemv_dot_kernel(GemvArgs a) {
     constexpr int BYTES = Q6 ? 210 : 144;
     extern __shared__ __align__(128) unsigned char gsm[];
-    uint32_t* xs = reinterpret_cast<uint32_t*>(gsm);                 // [g][cols / 4] packed int8
-    int* xsum = reinterpret_cast<int*>(gsm + gemv_xsum_offset(a.g, a.cols));   // [g][cols / 16] block sums
-    unsigned char* ring = gsm + gemv_ring_offset(a.g, a.cols);
+    uint32_t* xs = reinterpret_cast<uint32_t*>(gsm);                 // [G][cols / 4] packed int8
+    int* xsum = reinterpret_cast<int*>(gsm + gemv_xsum_offset(G, a.cols));   // [G][cols / 16] block sums
+    unsigned char* ring = gsm + gemv_ring_offset(G, a.cols);
     const int64_t tb = gemv_tile_bytes(a.row_bytes);
     uint64_t* full = reinterpret_cast<uint64_t*>(ring + a.stages * tb);
+    int* done = reinterpret_cast<int*>(full + GEMV_MAX_STAGES);      // warps done with each stage
+    volatile int* abort = reinterpret_cast<volatile int*>(done + GEMV_MAX_STAGES);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
     if (tid == 0) {
-        for (int i = 0; i < a.stages; ++i) mbar_init_cta(full + i, 1);
+        for (int i = 0; i < a.stages; ++i) {
+            mbar_init_cta(full + i, 1);
+            done[i] = 0;
+        }
+        *abort = 0;
         mbar_init_fence();
         for (int i = 0; i < a.stages; ++i) gemv_issue(a, ring, full, blockIdx.x + i * gridDim.x, i);
     }
-    static_assert(GEMV_TOKENS <= GEMV_WARPS, "one warp quantises each token");
+    static_assert(GEMV_TOKENS <= GEMV_WARPS, "each token has at least one warp");
     __shared__ float sxs[GEMV_TOKENS], wmax[GEMV_WARPS], rh[GEMV_TOKENS * 64];
+    // launched as a dependent of the previous kernel in the stream (programmatic
+    // launch): the weight copies above read only the weights; everything the
+    // previous kernels write (the inputs, the conv tails, the outputs' readers)
+    // is touched only after that kernel has completed
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (a.cs_state) {
         // conv tails move up by one token (the readers of the old tails have finished)
         const int64_t total = static_cast<int64_t>(a.cs_n) * a.cs_c_conv;
@@ -213,6 +236,11 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_dot_kernel(GemvArgs a) {
     }
     // the tokens' codes as packed int8, and their sums over every 16 codes
     const int kw = a.cols >> 2, k16 = a.cols >> 4;
+    for (int i = a.g * k16 + tid; i < G * k16; i += GEMV_THREADS) {
+        const int t = i / k16, b = i - t * k16;
+        *reinterpret_cast<uint4*>(xs + t * kw + 4 * b) = make_uint4(0u, 0u, 0u, 0u);
+        xsum[i] = 0;
+    }
     if (a.in_mode != 0) {
         if (a.rms_psum) {
             for (int i = tid; i < a.g * a.rms_hv; i += GEMV_THREADS) {
@@ -266,73 +294,68 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_dot_kernel(GemvArgs a) {
         }
     } else {
         if (tid < a.g) sxs[tid] = a.sx[tid];
-    }
-    for (int i = tid; a.in_mode == 0 && i < a.g * k16; i += GEMV_THREADS) {
-        const int t = i / k16, b = i - t * k16;
-        const uint4 h0 = __ldg(reinterpret_cast<const uint4*>(a.xc + static_cast<int64_t>(t) * a.cols + 16 * b));
-        const uint4 h1 = __ldg(reinterpret_cast<const uint4*>(a.xc + static_cast<int64_t>(t) * a.cols + 16 * b + 8));
-        const uint32_t hw[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-        int sum = 0;
+        for (int i = tid; i < a.g * k16; i += GEMV_THREADS) {
+            const int t = i / k16, b = i - t * k16;
+            const uint4 h0 = __ldg(reinterpret_cast<const uint4*>(a.xc + static_cast<int64_t>(t) * a.cols + 16 * b));
+            const uint4 h1 = __ldg(reinterpret_cast<const uint4*>(a.xc + static_cast<int64_t>(t) * a.cols + 16 * b + 8));
+            const uint32_t hw[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+            int sum = 0;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&hw[2 * q]));
-            const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&hw[2 * q + 1]));
-            const uint32_t packed = codes_to_i8x4(__fadd_rn(f0.x, QCODE_MAGIC), __fadd_rn(f0.y, QCODE_MAGIC),
-                                                  __fadd_rn(f1.x, QCODE_MAGIC), __fadd_rn(f1.y, QCODE_MAGIC));
-            xs[t * kw + 4 * b + q] = packed;
-            sum = __dp4a(static_cast<int>(packed), 0x01010101, sum);
+            for (int q = 0; q < 4; ++q) {
+                const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&hw[2 * q]));
+                const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&hw[2 * q + 1]));
+                const uint32_t packed = codes_to_i8x4(__fadd_rn(f0.x, QCODE_MAGIC), __fadd_rn(f0.y, QCODE_MAGIC),
+                                                      __fadd_rn(f1.x, QCODE_MAGIC), __fadd_rn(f1.y, QCODE_MAGIC));
+                xs[t * kw + 4 * b + q] = packed;
+                sum = __dp4a(static_cast<int>(packed), 0x01010101, sum);
+            }
+            xsum[i] = sum;
         }
-        xsum[i] = sum;
     }
     __syncthreads();
+    // Each warp takes its row of every tile the CTA walks, waiting on the
+    // tile's stage by itself; the last warp done with a stage refills it with
+    // the CTA's tile `stages` steps ahead (no CTA-wide barrier per tile).
     const int nsb = a.cols >> 8;
     const int j = lane & 7, sbl = lane >> 3;       // the lane's span and superblock within a step of 4
-    bool aborted = false;
     int it = 0;
     for (int tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x, ++it) {
         const int s = it % a.stages;
-        const bool ok = mbar_wait_bounded(full + s, (it / a.stages) & 1, &g_decode_error, ERR_WAIT_TIMEOUT);
-        if (!__syncthreads_and(ok)) {
-            aborted = true;
-            break;
-        }
+        if (!__all_sync(0xffffffffu, gemv_wait(full + s, (it / a.stages) & 1, abort))) break;
         const int row = tile * GEMV_WARPS + warp;
         if (row < a.rows) {
             const uint8_t* rb = ring + s * tb + static_cast<int64_t>(warp) * a.row_bytes;
-            float acc[GEMV_TOKENS];
+            float acc[G];
 #pragma unroll
-            for (int t = 0; t < GEMV_TOKENS; ++t) acc[t] = 0.0f;
+            for (int t = 0; t < G; ++t) acc[t] = 0.0f;
+#pragma unroll 4
             for (int i = sbl; i < nsb; i += 4) {
                 uint32_t c[8];
                 float mul0, mul1, add0, add1;
                 span_codes<Q6>(rb + i * BYTES, j, c, mul0, mul1, add0, add1);
                 const int w0 = 64 * i + 8 * j;           // first x word of the span (256 i + 32 j bytes)
 #pragma unroll
-                for (int t = 0; t < GEMV_TOKENS; ++t) {
-                    if (t < a.g) {
-                        const uint4 xa = *reinterpret_cast<const uint4*>(xs + t * kw + w0);
-                        const uint4 xb = *reinterpret_cast<const uint4*>(xs + t * kw + w0 + 4);
-                        const int2 sx = *reinterpret_cast<const int2*>(xsum + t * k16 + 16 * i + 2 * j);
-                        int d0 = __dp4a(static_cast<int>(c[0]), static_cast<int>(xa.x), 0);
-                        d0 = __dp4a(static_cast<int>(c[1]), static_cast<int>(xa.y), d0);
-                        d0 = __dp4a(static_cast<int>(c[2]), static_cast<int>(xa.z), d0);
-                        d0 = __dp4a(static_cast<int>(c[3]), static_cast<int>(xa.w), d0);
-                        int d1 = __dp4a(static_cast<int>(c[4]), static_cast<int>(xb.x), 0);
-                        d1 = __dp4a(static_cast<int>(c[5]), static_cast<int>(xb.y), d1);
-                        d1 = __dp4a(static_cast<int>(c[6]), static_cast<int>(xb.z), d1);
-                        d1 = __dp4a(static_cast<int>(c[7]), static_cast<int>(xb.w), d1);
-                        float r = fmaf(mul0, static_cast<float>(d0), fmaf(add0, static_cast<float>(sx.x), acc[t]));
-                        acc[t] = fmaf(mul1, static_cast<float>(d1), fmaf(add1, static_cast<float>(sx.y), r));
-                    }
+                for (int t = 0; t < G; ++t) {
+                    const uint4 xa = *reinterpret_cast<const uint4*>(xs + t * kw + w0);
+                    const uint4 xb = *reinterpret_cast<const uint4*>(xs + t * kw + w0 + 4);
+                    const int2 sx = *reinterpret_cast<const int2*>(xsum + t * k16 + 16 * i + 2 * j);
+                    int d0 = __dp4a(static_cast<int>(c[0]), static_cast<int>(xa.x), 0);
+                    d0 = __dp4a(static_cast<int>(c[1]), static_cast<int>(xa.y), d0);
+                    d0 = __dp4a(static_cast<int>(c[2]), static_cast<int>(xa.z), d0);
+                    d0 = __dp4a(static_cast<int>(c[3]), static_cast<int>(xa.w), d0);
+                    int d1 = __dp4a(static_cast<int>(c[4]), static_cast<int>(xb.x), 0);
+                    d1 = __dp4a(static_cast<int>(c[5]), static_cast<int>(xb.y), d1);
+                    d1 = __dp4a(static_cast<int>(c[6]), static_cast<int>(xb.z), d1);
+                    d1 = __dp4a(static_cast<int>(c[7]), static_cast<int>(xb.w), d1);
+                    const float r = fmaf(mul0, static_cast<float>(d0), fmaf(add0, static_cast<float>(sx.x), acc[t]));
+                    acc[t] = fmaf(mul1, static_cast<float>(d1), fmaf(add1, static_cast<float>(sx.y), r));
                 }
             }
             float mine = 0.0f;
 #pragma unroll
-            for (int t = 0; t < GEMV_TOKENS; ++t) {
-                if (t < a.g) {
-                    const float sum = warp_sum(acc[t]);
-                    if (lane == t) mine = sum;
-                }
+            for (int t = 0; t < G; ++t) {
+                const float sum = warp_sum(acc[t]);
+                if (lane == t) mine = sum;
             }
             if (lane < a.g) {
                 const float y = mine * sxs[lane];
@@ -342,18 +365,59 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_dot_kernel(GemvArgs a) {
                     a.out_f32[lane * a.ld_f32 + (row - a.n_bf16)] = y;
             }
         }
-        __syncthreads();   // every warp is done with stage s
-        if (tid == 0) {
-            fence_proxy_async_smem();
-            gemv_issue(a, ring, full, tile + a.stages * gridDim.x, s);
+        // this warp is done reading stage s (its loads have been consumed)
+        __syncwarp();
+        if (lane == 0) {
+            __threadfence_block();
+            if (atomicAdd(done + s, 1) == GEMV_WARPS - 1) {
+                done[s] = 0;
+                __threadfence_block();
+                fence_proxy_async_smem();
+                gemv_issue(a, ring, full, tile + a.stages * gridDim.x, s);
+            }
         }
     }
-    if (aborted && tid == 0) {
+    __syncthreads();
+    if (*abort && tid == 0) {
         // a wait ran out: let copies already issued land (bounded) before the
         // shared memory is released
         for (int i = 0; i < a.stages; ++i)
             for (uint32_t par = 0; par < 2; ++par) mbar_wait_bounded(full + i, par, nullptr, 0, 20000000ull);
     }
+}
+
+template <bool Q6>
+static void gemv_set_smem(int bytes) {
+    cudaFuncSetAttribute(gemv_dot_kernel<Q6, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    cudaFuncSetAttribute(gemv_dot_kernel<Q6, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    cudaFuncSetAttribute(gemv_dot_kernel<Q6, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    cudaFuncSetAttribute(gemv_dot_kernel<Q6, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+// A programmatic dependent launch: the CTAs may start while the previous
+// kernel in the stream finishes (it signals when; see griddepcontrol in the
+// kernel), so the weight copies start before the inputs exist.
+template <bool Q6, int G>
+static cudaError_t gemv_launch_g(unsigned grid, size_t smem, cudaStream_t st, const GemvArgs& a) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(GEMV_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at;
+    at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemv_dot_kernel<Q6, G>, a);
+}
+
+template <bool Q6>
+static cudaError_t gemv_launch(int G, unsigned grid, size_t smem, cudaStream_t st, const GemvArgs& a) {
+    if (G == 1) return gemv_launch_g<Q6, 1>(grid, smem, st, a);
+    if (G == 2) return gemv_launch_g<Q6, 2>(grid, smem, st, a);
+    if (G == 4) return gemv_launch_g<Q6, 4>(grid, smem, st, a);
+    return gemv_launch_g<Q6, 8>(grid, smem, st, a);
 }
 
 // out[t][r] = s_x[t] * sum_k xc[t][k] W[r][k] (W exactly decoded), for n tokens in launches of at most
@@ -368,24 +432,25 @@ cudaError_t launch_gemv_dot(const void* blocks, bool q6k, int64_t rows, int64_t 
                               float* out_f32, int64_t ld_f32, cudaStream_t st, int in_mode, const void* xraw,
                               float* cs_state, const uint16_t* cs_qkvz, int64_t cs_ld, int cs_c_conv, int cs_n,
                               const float* rms_psum, int rms_hv, int rms_d, int rms_split, float rms_eps) {
-    static int sms = 0, max_optin = 0;
+    static int sms = 0, max_optin = 0, fa_static = 0;
     if (!sms) {
         int dev = 0;
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
         // dynamic shared memory: the opt-in maximum less the kernels' static arrays
         cudaFuncAttributes fa{};
-        cudaFuncGetAttributes(&fa, gemv_dot_kernel<true>);
-        max_optin -= static_cast<int>(fa.sharedSizeBytes);
-        cudaFuncSetAttribute(gemv_dot_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_optin);
-        cudaFuncSetAttribute(gemv_dot_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_optin);
+        cudaFuncGetAttributes(&fa, gemv_dot_kernel<true, 8>);
+        fa_static = static_cast<int>(fa.sharedSizeBytes);
+        max_optin -= fa_static;
+        gemv_set_smem<false>(max_optin);
+        gemv_set_smem<true>(max_optin);
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     }
     const int64_t row_bytes = (cols / 256) * (q6k ? 210 : 144);
     const int64_t tb = gemv_tile_bytes(row_bytes);
-    // tokens per launch: what fits beside one stage
+    // tokens per launch (a power of two): what fits beside one stage
     int64_t gmax = GEMV_TOKENS;
-    while (gmax > 1 && gemv_smem_bytes(static_cast<int>(gmax), static_cast<int>(cols), row_bytes, 1) > max_optin) --gmax;
+    while (gmax > 1 && gemv_smem_bytes(static_cast<int>(gmax), static_cast<int>(cols), row_bytes, 1) > max_optin) gmax /= 2;
     if (gemv_smem_bytes(1, static_cast<int>(cols), row_bytes, 1) > max_optin) return cudaErrorInvalidValue;
     const int ntiles = static_cast<int>((rows + GEMV_WARPS - 1) / GEMV_WARPS);
     for (int64_t t0 = 0; t0 < n; t0 += gmax) {
@@ -416,18 +481,25 @@ cudaError_t launch_gemv_dot(const void* blocks, bool q6k, int64_t rows, int64_t 
         a.n_bf16 = static_cast<int>(n_bf16);
         a.out_f32 = out_f32 ? out_f32 + t0 * ld_f32 : nullptr;
         a.ld_f32 = ld_f32;
-        // ring depth: as many stages as fit the two-CTA budget (at least one)
-        int stages = GEMV_MAX_STAGES;
-        while (stages > 1 && gemv_smem_bytes(a.g, a.cols, row_bytes, stages) > GEMV_SMEM_BUDGET) --stages;
+        // tokens computed: a power of two >= g; CTAs per SM and ring depth:
+        // the most CTAs (up to 4 at G <= 2, where registers allow them, else
+        // 2) whose shared memory holds at least two stages each, then as many
+        // stages as fit (one stage when nothing else fits)
+        const int G = a.g <= 1 ? 1 : a.g <= 2 ? 2 : a.g <= 4 ? 4 : 8;
+        int per_sm = G <= 2 ? 4 : 2, stages = 1;
+        for (; per_sm >= 1; --per_sm) {
+            const int64_t budget = GEMV_SM_SMEM / per_sm - 1024 - static_cast<int64_t>(fa_static);
+            stages = GEMV_MAX_STAGES;
+            while (stages > 1 && gemv_smem_bytes(G, a.cols, row_bytes, stages) > budget) --stages;
+            if (stages >= 2 || per_sm == 1) break;
+        }
+        if (per_sm < 1) per_sm = 1;
         a.stages = stages;
-        const size_t smem = static_cast<size_t>(gemv_smem_bytes(a.g, a.cols, row_bytes, stages));
-        const int per_sm = smem <= GEMV_SMEM_BUDGET ? 2 : 1;
+        const size_t smem = static_cast<size_t>(gemv_smem_bytes(G, a.cols, row_bytes, stages));
+        if (smem > static_cast<size_t>(max_optin)) return cudaErrorInvalidValue;
         const unsigned grid = static_cast<unsigned>(ntiles < per_sm * sms ? ntiles : per_sm * sms);
-        if (q6k)
-            gemv_dot_kernel<true><<<grid, GEMV_THREADS, smem, st>>>(a);
-        else
-            gemv_dot_kernel<false><<<grid, GEMV_THREADS, smem, st>>>(a);
-        cudaError_t e = cudaGetLastError();
+        cudaError_t e = q6k ? gemv_launch<true>(G, grid, smem, st, a) : gemv_launch<false>(G, grid, smem, st, a);
+        if (e == cudaSuccess) e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     (void)tb;
@@ -487,6 +559,7 @@ __global__ void __launch_bounds__(MID_THREADS) decode_mid_kernel(MidArgs a) {
     constexpr int R = NR / MID_WARPS;                // rows per warp
     __shared__ float qs[D], ks[D], vs[NR], gz[NR], red[MID_WARPS];
     __shared__ float gate[2];
+    pdl_trigger();
     const int h = blockIdx.x / MID_SPLIT, part = blockIdx.x % MID_SPLIT, sq = blockIdx.y, hk = h / a.ratio;
     const int i0 = part * NR;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -587,6 +660,7 @@ __global__ void __launch_bounds__(MID_THREADS) decode_mid_kernel(MidArgs a) {
 // o_hat *= rsqrt(mean o^2 + eps) per token and head, from the partial sums
 // (the decode step's path for more tokens than one projection launch takes).
 __global__ void decode_rms_apply_kernel(float* o_hat, const float* psum, int hv, int d, int c_v, float eps) {
+    pdl_trigger();
     const int sq = blockIdx.y;
     for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < c_v; e += gridDim.x * blockDim.x) {
         const int h = e / d;

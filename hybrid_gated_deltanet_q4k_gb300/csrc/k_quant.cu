@@ -19,6 +19,7 @@ template <int THREADS>
 __global__ void __launch_bounds__(THREADS)
 quant_rows_bf16_kernel(const uint16_t* __restrict__ x, int cols, uint16_t* __restrict__ codes,
                        float* __restrict__ scale) {
+    pdl_trigger();
     __shared__ float red[32];
     const int64_t row = blockIdx.x;
     const int nvec = cols >> 3;
@@ -73,6 +74,7 @@ quant_rows_bf16_kernel(const uint16_t* __restrict__ x, int cols, uint16_t* __res
 // one CTA per row, 8 values a thread per pass, the row read twice (L1).
 __global__ void __launch_bounds__(256) quant_rows_f32_kernel(const float* __restrict__ x, int cols,
                                                              uint16_t* __restrict__ codes, float* __restrict__ scale) {
+    pdl_trigger();
     __shared__ float red[32];
     const int64_t row = blockIdx.x;
     const float4* src = reinterpret_cast<const float4*>(x + row * cols);
