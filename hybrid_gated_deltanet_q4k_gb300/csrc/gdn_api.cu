@@ -27,7 +27,6 @@ cudaError_t launch_q6k_deq_codes(const void*, int64_t, int64_t, uint16_t*, float
 cudaError_t launch_q4k_deq_codes2(const void*, int64_t, int64_t, uint16_t*, float*, const void*, int64_t, int64_t,
                                   uint16_t*, float*, cudaStream_t);
 cudaError_t launch_quant_rows(const uint16_t*, int64_t, int64_t, uint16_t*, float*, cudaStream_t);
-cudaError_t launch_quant_rows_f32(const float*, int64_t, int64_t, uint16_t*, float*, cudaStream_t);
 cudaError_t launch_gemm_codes(const uint16_t*, const float*, const uint16_t*, const float*, int64_t, int64_t, int64_t,
                               uint16_t*, int64_t, int64_t, float*, int64_t, cudaStream_t);
 cudaError_t launch_gemm_f32(const float*, const float*, int64_t, int64_t, int64_t, uint16_t*, int64_t, int64_t, float*,
@@ -43,11 +42,12 @@ cudaError_t launch_conv_ckpt(const gdn_layer&, const uint16_t*, int64_t, int64_t
 size_t delta_scratch_bytes(int hv, int hk, int d, int64_t n);
 cudaError_t launch_gated_norm(const gdn_layer&, const uint16_t*, const uint16_t*, int64_t, int64_t, uint16_t*, float*,
                               float*, cudaStream_t);
-cudaError_t launch_gemv_dot(const void*, bool, int64_t, int64_t, const uint16_t*, const float*, int64_t, uint16_t*,
-                              int64_t, int64_t, float*, int64_t, cudaStream_t, int in_mode = 0, const void* xraw = nullptr,
-                              float* cs_state = nullptr, const uint16_t* cs_qkvz = nullptr, int64_t cs_ld = 0,
-                              int cs_c_conv = 0, int cs_n = 0, const float* rms_psum = nullptr, int rms_hv = 0,
-                              int rms_d = 0, int rms_split = 0, float rms_eps = 0.0f);
+cudaError_t launch_gemv_dot(const void*, bool, int64_t, int64_t, const uint16_t*, const uint32_t*, int64_t, const float*,
+                            int64_t, uint16_t*, int64_t, int64_t, float*, int64_t, cudaStream_t, float*, const uint16_t*,
+                            int64_t, int, int);
+cudaError_t launch_decode_pack(const void*, bool, int64_t, int64_t, const float*, int, int, int, float, uint32_t*, float*,
+                               cudaStream_t);
+int64_t decode_pack_stride(int64_t);
 cudaError_t launch_decode_mid(const gdn_layer&, const uint16_t*, int64_t, const float*, int64_t, const float*, int64_t,
                               float*, float*, float*, cudaStream_t);
 cudaError_t launch_decode_rms_apply(const gdn_layer&, float*, const float*, int64_t, cudaStream_t);
@@ -306,10 +306,10 @@ size_t host_stage_bytes(const gdn_layer* L, const Sizes& s, int64_t B) {
 // Workspace of one decode step of B tokens (one per sequence).
 struct DecodeWs {
     uint16_t* qkvz; float* ba;        // projection [B][n_bf16] bf16, [B][2 hv] fp32
-    float* ohat;                      // gated output [B][c_v] fp32 (RMS applied by the output projection)
+    float* ohat;                      // gated output [B][c_v] fp32 (RMS applied when it is packed)
     float* psum;                      // partial sums of o^2 [B][hv][DECODE_MID_SPLIT]
-    uint16_t* xc; float* sx;          // codes of x [B][H] and of o_hat [B][c_v], with row scales,
-    uint16_t* oc; float* so;          // when B > GDN_DECODE_GEMV_TOKENS (quantised once, not per CTA)
+    uint32_t* xp; float* sx;          // packed codes of x [B][H] and of o_hat [B][c_v] with row scales
+    uint32_t* op; float* so;          // (Q4_K / Q6_K layers)
     size_t total;
 };
 
@@ -326,10 +326,10 @@ DecodeWs carve_decode(const gdn_layer* L, const Sizes& s, int64_t B, void* base)
     w.ba = static_cast<float*>(take(B * 2 * s.hv * 4));
     w.ohat = static_cast<float*>(take(B * s.c_v * 4));
     w.psum = static_cast<float*>(take(B * s.hv * DECODE_MID_SPLIT * 4));
-    if (L->wtype == GDN_W_Q4K && B > GDN_DECODE_GEMV_TOKENS) {
-        w.xc = static_cast<uint16_t*>(take(B * s.H * 2));
+    if (L->wtype == GDN_W_Q4K) {
+        w.xp = static_cast<uint32_t*>(take(B * decode_pack_stride(s.H) * 4));
         w.sx = static_cast<float*>(take(B * 4));
-        w.oc = static_cast<uint16_t*>(take(B * s.c_v * 2));
+        w.op = static_cast<uint32_t*>(take(B * decode_pack_stride(s.c_v) * 4));
         w.so = static_cast<float*>(take(B * 4));
     }
     w.total = off;
@@ -816,44 +816,38 @@ int gdn_decode(const gdn_layer* layer, const void* x, int n_seqs, float* state, 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const bool q4k = layer->wtype == GDN_W_Q4K;
     const int64_t B = n_seqs;
-    // K1, steps 1b + 1c: each CTA quantises the tokens to int8 rows, then
-    // reads the weight rows once (Q4_K layers); F32 layers: plain product
-    // (more tokens than one projection launch takes: quantised once beforehand)
-    const bool once = B > GDN_DECODE_GEMV_TOKENS;
-    if (q4k && once) {
-        GDN_LAUNCH(launch_quant_rows(static_cast<const uint16_t*>(x), B, s.H, w.xc, w.sx, st), "decode: quantise x");
-        GDN_LAUNCH(launch_gemv_dot(layer->w_in, layer->q6k_mask & 1, s.r_in, s.H, w.xc, w.sx, B, w.qkvz, s.n_bf16,
-                                   s.n_bf16, w.ba, 2 * s.hv, st),
-                   "decode: input projection");
-    } else if (q4k) {
-        GDN_LAUNCH(launch_gemv_dot(layer->w_in, layer->q6k_mask & 1, s.r_in, s.H, nullptr, nullptr, B, w.qkvz, s.n_bf16,
-                                   s.n_bf16, w.ba, 2 * s.hv, st, 1, x),
+    // Q4_K / Q6_K layers, five launches, each a programmatic dependent of the
+    // one before (it starts while that one ends and waits for it before it
+    // reads its results; the projections' weight copies start earlier):
+    //   steps 1b + 1c: x quantised to packed int8 rows once, then the weight
+    //   rows read once against them;
+    //   steps 2-4 per (value head, row block, sequence): conv, norms, gates,
+    //   one token of the recurrence, gated output o_hat (fp32) and o^2 sums;
+    //   step 5: o_hat with the RMS of each head packed once, then the output
+    //   weights; that kernel also moves the conv tails up by one token.
+    // F32 layers: plain products.
+    if (q4k) {
+        GDN_LAUNCH(launch_decode_pack(x, false, B, s.H, nullptr, 0, 0, 0, 0.0f, w.xp, w.sx, st), "decode: pack x");
+        GDN_LAUNCH(launch_gemv_dot(layer->w_in, layer->q6k_mask & 1, s.r_in, s.H, nullptr, w.xp, decode_pack_stride(s.H),
+                                   w.sx, B, w.qkvz, s.n_bf16, s.n_bf16, w.ba, 2 * s.hv, st, nullptr, nullptr, 0, 0, 0),
                    "decode: input projection");
     } else {
         GDN_LAUNCH(launch_gemm_f32(static_cast<const float*>(x), static_cast<const float*>(layer->w_in), B, s.r_in, s.H,
                                    w.qkvz, s.n_bf16, s.n_bf16, w.ba, 2 * s.hv, st),
                    "decode: input projection");
     }
-    // K2, steps 2-4 per (value head, sequence): conv, norms, gates, one token of
-    // the recurrence, gated RMSNorm -> o_hat (fp32)
     GDN_LAUNCH(launch_decode_mid(*layer, w.qkvz, s.n_bf16, w.ba, 2 * s.hv, conv_state, B, state, w.ohat, w.psum, st),
                "decode: conv, recurrence and gated norm");
-    // K3, step 5: the conv tails move up by one token, o_hat is quantised to
-    // int8 rows in each CTA and meets the output weights (Q4_K layers)
-    if (!q4k || once) GDN_LAUNCH(launch_decode_rms_apply(*layer, w.ohat, w.psum, B, st), "decode: gated-norm RMS");
-    if (q4k && once) {
-        GDN_LAUNCH(launch_quant_rows_f32(w.ohat, B, s.c_v, w.oc, w.so, st), "decode: quantise o_hat");
-        GDN_LAUNCH(launch_gemv_dot(layer->w_out, layer->q6k_mask & 2, s.H, s.c_v, w.oc, w.so, B,
-                                   static_cast<uint16_t*>(y), s.H, s.H, nullptr, 0, st, 0, nullptr, conv_state, w.qkvz,
-                                   s.n_bf16, static_cast<int>(s.c_conv), n_seqs),
-                   "decode: conv state and output projection");
-    } else if (q4k) {
-        GDN_LAUNCH(launch_gemv_dot(layer->w_out, layer->q6k_mask & 2, s.H, s.c_v, nullptr, nullptr, B,
-                                   static_cast<uint16_t*>(y), s.H, s.H, nullptr, 0, st, 2, w.ohat, conv_state, w.qkvz,
-                                   s.n_bf16, static_cast<int>(s.c_conv), n_seqs, w.psum, static_cast<int>(s.hv),
-                                   static_cast<int>(s.d), DECODE_MID_SPLIT, layer->eps_rms),
+    if (q4k) {
+        GDN_LAUNCH(launch_decode_pack(w.ohat, true, B, s.c_v, w.psum, static_cast<int>(s.hv), static_cast<int>(s.d),
+                                      DECODE_MID_SPLIT, layer->eps_rms, w.op, w.so, st),
+                   "decode: pack o_hat");
+        GDN_LAUNCH(launch_gemv_dot(layer->w_out, layer->q6k_mask & 2, s.H, s.c_v, nullptr, w.op,
+                                   decode_pack_stride(s.c_v), w.so, B, static_cast<uint16_t*>(y), s.H, s.H, nullptr, 0,
+                                   st, conv_state, w.qkvz, s.n_bf16, static_cast<int>(s.c_conv), n_seqs),
                    "decode: conv state and output projection");
     } else {
+        GDN_LAUNCH(launch_decode_rms_apply(*layer, w.ohat, w.psum, B, st), "decode: gated-norm RMS");
         std::vector<int64_t> cu(static_cast<size_t>(B) + 1);
         for (int64_t i = 0; i <= B; ++i) cu[static_cast<size_t>(i)] = i;
         GDN_LAUNCH(launch_conv_state(*layer, w.qkvz, s.n_bf16, B, conv_state, st, cu.data(), n_seqs), "decode: conv state");
@@ -876,8 +870,8 @@ int gdn_decode_gemv(const void* blocks, int q6k, int64_t rows, int64_t cols, con
     if (n_bf16 > 0 && (!out_bf16 || ld_bf16 < (n_bf16 < rows ? n_bf16 : rows))) return fail(GDN_EINVAL, "gdn_decode_gemv: bf16 output");
     if (n_bf16 < rows && (!out_f32 || ld_f32 < rows - n_bf16)) return fail(GDN_EINVAL, "gdn_decode_gemv: fp32 output");
     if (!aligned(blocks, 16) || !aligned(xc, 16)) return fail(GDN_EINVAL, "gdn_decode_gemv: 16-byte alignment required");
-    GDN_LAUNCH(launch_gemv_dot(blocks, q6k == 1, rows, cols, xc, sx, n, out_bf16, ld_bf16, n_bf16, out_f32, ld_f32,
-                                 static_cast<cudaStream_t>(stream)),
+    GDN_LAUNCH(launch_gemv_dot(blocks, q6k == 1, rows, cols, xc, nullptr, 0, sx, n, out_bf16, ld_bf16, n_bf16, out_f32,
+                               ld_f32, static_cast<cudaStream_t>(stream), nullptr, nullptr, 0, 0, 0),
                "gdn_decode_gemv");
     return GDN_OK;
 }

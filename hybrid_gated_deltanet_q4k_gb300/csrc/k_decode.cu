@@ -59,50 +59,19 @@ struct GemvArgs {
     int n_bf16;
     float* out_f32;          // r >= n_bf16: at t * ld_f32 + r - n_bf16
     int64_t ld_f32;
-    // in_mode 0: xc / sx hold the tokens' int8 codes and scales.  1, 2: xraw
-    // holds the tokens' rows [g][cols] in bf16 (1) or fp32 (2), quantised here
-    // per row exactly as step 1b does (scale amax/127, the same codes).
+    // in_mode 0: xc holds the tokens' int8 codes as fp16 patterns; 1: xpack
+    // holds them packed by decode_pack_kernel (per token stride_words words:
+    // cols/4 words of 4 codes, then cols/16 sums of 16 codes).  sx: the scales.
     int in_mode;
-    const void* xraw;
+    const uint32_t* xpack;
+    int64_t xpack_stride;
     // optional (cs_state non-null): shift the conv tails of cs_n sequences by
     // one token, [x_{t-2}, x_{t-1}, x_t] from the raw projection row cs_qkvz
     float* cs_state;         // [cs_n][cs_c_conv][3]
     const uint16_t* cs_qkvz; // [cs_n][cs_ld] bf16
     int64_t cs_ld;
     int cs_c_conv, cs_n;
-    // optional with in_mode 2 (rms_psum non-null): the rows are gated but not yet
-    // RMS-normalised; head h of token t is multiplied by rsqrt(sum_p
-    // rms_psum[(t*rms_hv + h)*rms_split + p] / rms_d + rms_eps) first (the
-    // partial sums of o^2 over the head's row blocks, added in order)
-    const float* rms_psum;
-    int rms_hv, rms_d, rms_split;
-    float rms_eps;
 };
-
-// Elements 16b .. 16b+15 of raw input row t as floats (rh: per token and head
-// scale of in_mode 2 with rms_psum, else unused).
-__device__ __forceinline__ void gemv_raw16(const GemvArgs& a, int t, int b, float (&w)[16], const float* rh) {
-    if (a.in_mode == 1) {
-        const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.xraw) +
-                                                        static_cast<int64_t>(t) * a.cols + 16 * b);
-        const uint4 u0 = __ldg(p), u1 = __ldg(p + 1);
-        const uint32_t u[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            w[2 * e] = __uint_as_float(u[e] << 16);
-            w[2 * e + 1] = __uint_as_float(u[e] & 0xffff0000u);
-        }
-    } else {
-        const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(a.xraw) +
-                                                          static_cast<int64_t>(t) * a.cols + 16 * b);
-        const float sc = a.rms_psum ? rh[t * 64 + (16 * b) / a.rms_d] : 1.0f;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float4 v = __ldg(p + e);
-            w[4 * e] = v.x * sc; w[4 * e + 1] = v.y * sc; w[4 * e + 2] = v.z * sc; w[4 * e + 3] = v.w * sc;
-        }
-    }
-}
 
 // Shared memory: the tokens' codes (g * cols bytes), their sums over blocks
 // of 16 (g * cols/16 ints), then `stages` tiles of GEMV_WARPS weight rows,
@@ -112,9 +81,11 @@ __host__ __device__ inline int64_t gemv_xsum_offset(int g, int cols) { return (s
 __host__ __device__ inline int64_t gemv_ring_offset(int g, int cols) {
     return (gemv_xsum_offset(g, cols) + static_cast<int64_t>(g) * (cols / 16) * 4 + 127) & ~127LL;
 }
-// ... then per stage a count of the warps done with it, and an abort flag.
+// ... then the barrier of the tokens' packed codes, per stage a count of the
+// warps done with it, and an abort flag.
 __host__ __device__ inline int64_t gemv_smem_bytes(int g, int cols, int64_t row_bytes, int stages) {
-    return gemv_ring_offset(g, cols) + stages * gemv_tile_bytes(row_bytes) + 12 * GEMV_MAX_STAGES + 4;
+    return gemv_ring_offset(g, cols) + stages * gemv_tile_bytes(row_bytes) + 8 * (GEMV_MAX_STAGES + 1) +
+           4 * GEMV_MAX_STAGES + 4;
 }
 
 // Copy tile `tile` into stage `s`: the whole bytes by one bulk copy (a tile
@@ -132,13 +103,22 @@ __device__ __forceinline__ void gemv_issue(const GemvArgs& a, unsigned char* rin
     if (b16) bulk_load_1d(dst, a.blocks + off, static_cast<uint32_t>(b16), full + s);
 }
 
+// dot product of 4 unsigned bytes (a) with 4 signed bytes (b), plus c
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
 // One lane takes one 32-weight span of a superblock (a Q4_K sub-block; two
 // 16-weight Q6_K sub-blocks): lane l of a warp step works on superblock
 // step*4 + l/8, span l%8, so a warp covers 4 superblocks per step and each
 // lane decodes its scales once per 32 weights.  Its codes come as 8 words of
 // 4 packed bytes (weights 32j .. 32j+31 of the superblock, in order), and
 //   sum_k w_k x_k = mul0 * dot(codes[0..15], x) + mul1 * dot(codes[16..31], x)
-//                 + add0 * sum(x[0..15]) + add1 * sum(x[16..31]).
+//                 + add0 * sum(x[0..15]) + add1 * sum(x[16..31]);
+// for Q4_K one scale and one min cover the 32 weights (mul0 = mul1, add0 =
+// add1), so the span takes a single dot product.
 template <bool Q6>
 __device__ __forceinline__ void span_codes(const uint8_t* blk, int j, uint32_t (&c)[8], float& mul0, float& mul1,
                                            float& add0, float& add1) {
@@ -152,14 +132,15 @@ __device__ __forceinline__ void span_codes(const uint8_t* blk, int j, uint32_t (
         const float d = __half2float(__ushort_as_half(static_cast<uint16_t>(hdr.x & 0xffffu)));
         const float dmin = __half2float(__ushort_as_half(static_cast<uint16_t>(hdr.x >> 16)));
         const float ds = __fmul_rn(d, small_uint_to_float(sc)), dm = __fmul_rn(dmin, small_uint_to_float(m));
+        // the span's codes in place: low nibbles (even j), or high nibbles
+        // left at 16 q (odd j, their dot product 16 times too large: the
+        // scale takes the 1/16, exactly)
         const uint4* q = reinterpret_cast<const uint4*>(blk + 16 + 32 * (j >> 1));
         const uint4 a = q[0], b = q[1];
-        const int sh = 4 * (j & 1);
-        c[0] = (a.x >> sh) & 0x0f0f0f0fu; c[1] = (a.y >> sh) & 0x0f0f0f0fu;
-        c[2] = (a.z >> sh) & 0x0f0f0f0fu; c[3] = (a.w >> sh) & 0x0f0f0f0fu;
-        c[4] = (b.x >> sh) & 0x0f0f0f0fu; c[5] = (b.y >> sh) & 0x0f0f0f0fu;
-        c[6] = (b.z >> sh) & 0x0f0f0f0fu; c[7] = (b.w >> sh) & 0x0f0f0f0fu;
-        mul0 = mul1 = ds;
+        const uint32_t mask = (j & 1) ? 0xf0f0f0f0u : 0x0f0f0f0fu;
+        c[0] = a.x & mask; c[1] = a.y & mask; c[2] = a.z & mask; c[3] = a.w & mask;
+        c[4] = b.x & mask; c[5] = b.y & mask; c[6] = b.z & mask; c[7] = b.w & mask;
+        mul0 = mul1 = (j & 1) ? __fmul_rn(ds, 0.0625f) : ds;
         add0 = add1 = -dm;
     } else {
         const int h = j >> 2, g = j & 3;
@@ -201,7 +182,8 @@ __global__ void __launch_bounds__(GEMV_THREADS, G <= 2 ? 4 : 2) gemv_dot_kernel(
     unsigned char* ring = gsm + gemv_ring_offset(G, a.cols);
     const int64_t tb = gemv_tile_bytes(a.row_bytes);
     uint64_t* full = reinterpret_cast<uint64_t*>(ring + a.stages * tb);
-    int* done = reinterpret_cast<int*>(full + GEMV_MAX_STAGES);      // warps done with each stage
+    uint64_t* xbar = full + GEMV_MAX_STAGES;                         // the packed codes (in_mode 1)
+    int* done = reinterpret_cast<int*>(xbar + 1);                    // warps done with each stage
     volatile int* abort = reinterpret_cast<volatile int*>(done + GEMV_MAX_STAGES);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
@@ -210,17 +192,31 @@ __global__ void __launch_bounds__(GEMV_THREADS, G <= 2 ? 4 : 2) gemv_dot_kernel(
             mbar_init_cta(full + i, 1);
             done[i] = 0;
         }
+        mbar_init_cta(xbar, 1);
         *abort = 0;
         mbar_init_fence();
         for (int i = 0; i < a.stages; ++i) gemv_issue(a, ring, full, blockIdx.x + i * gridDim.x, i);
     }
-    static_assert(GEMV_TOKENS <= GEMV_WARPS, "each token has at least one warp");
-    __shared__ float sxs[GEMV_TOKENS], wmax[GEMV_WARPS], rh[GEMV_TOKENS * 64];
+    __shared__ float sxs[GEMV_TOKENS];
     // launched as a dependent of the previous kernel in the stream (programmatic
     // launch): the weight copies above read only the weights; everything the
     // previous kernels write (the inputs, the conv tails, the outputs' readers)
-    // is touched only after that kernel has completed
+    // is touched only after that kernel has completed.  The next kernel may be
+    // scheduled at once: it too waits for this one before it reads anything.
+    pdl_trigger();
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int kw = a.cols >> 2, k16 = a.cols >> 4;
+    if (a.in_mode == 1 && tid == 0) {
+        // the tokens' packed codes and sums: two bulk copies per token
+        const uint32_t bytes = static_cast<uint32_t>(a.cols + a.cols / 4);
+        mbar_expect_tx(xbar, static_cast<uint32_t>(a.g) * bytes);
+        for (int t = 0; t < a.g; ++t) {
+            const uint32_t* src = a.xpack + t * a.xpack_stride;
+            bulk_load_1d(xs + t * kw, src, static_cast<uint32_t>(a.cols), xbar);
+            bulk_load_1d(xsum + t * k16, src + kw, static_cast<uint32_t>(a.cols / 4), xbar);
+        }
+    }
+    if (tid < a.g) sxs[tid] = a.sx[tid];
     if (a.cs_state) {
         // conv tails move up by one token (the readers of the old tails have finished)
         const int64_t total = static_cast<int64_t>(a.cs_n) * a.cs_c_conv;
@@ -234,66 +230,13 @@ __global__ void __launch_bounds__(GEMV_THREADS, G <= 2 ? 4 : 2) gemv_dot_kernel(
             t3[2] = bf16_bits_to_float(a.cs_qkvz[sq * a.cs_ld + c]);
         }
     }
-    // the tokens' codes as packed int8, and their sums over every 16 codes
-    const int kw = a.cols >> 2, k16 = a.cols >> 4;
+    // tokens a.g .. G-1: zero codes (computed, not stored)
     for (int i = a.g * k16 + tid; i < G * k16; i += GEMV_THREADS) {
         const int t = i / k16, b = i - t * k16;
         *reinterpret_cast<uint4*>(xs + t * kw + 4 * b) = make_uint4(0u, 0u, 0u, 0u);
         xsum[i] = 0;
     }
-    if (a.in_mode != 0) {
-        if (a.rms_psum) {
-            for (int i = tid; i < a.g * a.rms_hv; i += GEMV_THREADS) {
-                const int t = i / a.rms_hv, hh = i - t * a.rms_hv;
-                const float* ps = a.rms_psum + (static_cast<int64_t>(t) * a.rms_hv + hh) * a.rms_split;
-                float sum = 0.0f;
-                for (int p = 0; p < a.rms_split; ++p) sum += ps[p];
-                rh[t * 64 + hh] = rsqrtf(sum / static_cast<float>(a.rms_d) + a.rms_eps);
-            }
-            __syncthreads();
-        }
-        // the warps split evenly over the tokens (wpt warps each): the row
-        // amax (warp maxima combined through shared memory), then the codes
-        const int wpt = GEMV_WARPS / a.g, t = warp / wpt, gl = (warp - t * wpt) * 32 + lane, gs = wpt * 32;
-        float amax = 0.0f;
-        if (t < a.g) {
-            for (int b = gl; b < k16; b += gs) {
-                float w[16];
-                gemv_raw16(a, t, b, w, rh);
-#pragma unroll
-                for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fabsf(w[e]));
-            }
-        }
-        amax = warp_max(amax);
-        if (lane == 0) wmax[warp] = amax;
-        __syncthreads();
-        if (t < a.g) {
-            amax = 0.0f;
-            for (int w = 0; w < wpt; ++w) amax = fmaxf(amax, wmax[t * wpt + w]);
-            const QScale qsc = make_qscale(amax);
-            if (gl == 0) sxs[t] = qsc.s;
-            for (int b = gl; b < k16; b += gs) {
-                float w[16], c[16];
-                gemv_raw16(a, t, b, w, rh);
-                bool redo = !qsc.fast;
-#pragma unroll
-                for (int e = 0; e < 16; ++e) c[e] = qcode_fast(w[e], qsc, redo);
-                if (redo) {
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) c[e] = qcode_exact(w[e], qsc.s);
-                }
-                int sum = 0;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint32_t packed = codes_to_i8x4(c[4 * q], c[4 * q + 1], c[4 * q + 2], c[4 * q + 3]);
-                    xs[t * kw + 4 * b + q] = packed;
-                    sum = __dp4a(static_cast<int>(packed), 0x01010101, sum);
-                }
-                xsum[t * k16 + b] = sum;
-            }
-        }
-    } else {
-        if (tid < a.g) sxs[tid] = a.sx[tid];
+    if (a.in_mode == 0) {
         for (int i = tid; i < a.g * k16; i += GEMV_THREADS) {
             const int t = i / k16, b = i - t * k16;
             const uint4 h0 = __ldg(reinterpret_cast<const uint4*>(a.xc + static_cast<int64_t>(t) * a.cols + 16 * b));
@@ -311,6 +254,8 @@ __global__ void __launch_bounds__(GEMV_THREADS, G <= 2 ? 4 : 2) gemv_dot_kernel(
             }
             xsum[i] = sum;
         }
+    } else {
+        gemv_wait(xbar, 0, abort);
     }
     __syncthreads();
     // Each warp takes its row of every tile the CTA walks, waiting on the
@@ -339,16 +284,29 @@ __global__ void __launch_bounds__(GEMV_THREADS, G <= 2 ? 4 : 2) gemv_dot_kernel(
                     const uint4 xa = *reinterpret_cast<const uint4*>(xs + t * kw + w0);
                     const uint4 xb = *reinterpret_cast<const uint4*>(xs + t * kw + w0 + 4);
                     const int2 sx = *reinterpret_cast<const int2*>(xsum + t * k16 + 16 * i + 2 * j);
-                    int d0 = __dp4a(static_cast<int>(c[0]), static_cast<int>(xa.x), 0);
-                    d0 = __dp4a(static_cast<int>(c[1]), static_cast<int>(xa.y), d0);
-                    d0 = __dp4a(static_cast<int>(c[2]), static_cast<int>(xa.z), d0);
-                    d0 = __dp4a(static_cast<int>(c[3]), static_cast<int>(xa.w), d0);
-                    int d1 = __dp4a(static_cast<int>(c[4]), static_cast<int>(xb.x), 0);
-                    d1 = __dp4a(static_cast<int>(c[5]), static_cast<int>(xb.y), d1);
-                    d1 = __dp4a(static_cast<int>(c[6]), static_cast<int>(xb.z), d1);
-                    d1 = __dp4a(static_cast<int>(c[7]), static_cast<int>(xb.w), d1);
-                    const float r = fmaf(mul0, static_cast<float>(d0), fmaf(add0, static_cast<float>(sx.x), acc[t]));
-                    acc[t] = fmaf(mul1, static_cast<float>(d1), fmaf(add1, static_cast<float>(sx.y), r));
+                    if constexpr (!Q6) {
+                        // one scale for the 32 weights: one dot product
+                        int d = dp4a_us(c[0], xa.x, 0);
+                        d = dp4a_us(c[1], xa.y, d);
+                        d = dp4a_us(c[2], xa.z, d);
+                        d = dp4a_us(c[3], xa.w, d);
+                        d = dp4a_us(c[4], xb.x, d);
+                        d = dp4a_us(c[5], xb.y, d);
+                        d = dp4a_us(c[6], xb.z, d);
+                        d = dp4a_us(c[7], xb.w, d);
+                        acc[t] = fmaf(mul0, static_cast<float>(d), fmaf(add0, static_cast<float>(sx.x + sx.y), acc[t]));
+                    } else {
+                        int d0 = dp4a_us(c[0], xa.x, 0);
+                        d0 = dp4a_us(c[1], xa.y, d0);
+                        d0 = dp4a_us(c[2], xa.z, d0);
+                        d0 = dp4a_us(c[3], xa.w, d0);
+                        int d1 = dp4a_us(c[4], xb.x, 0);
+                        d1 = dp4a_us(c[5], xb.y, d1);
+                        d1 = dp4a_us(c[6], xb.z, d1);
+                        d1 = dp4a_us(c[7], xb.w, d1);
+                        const float r = fmaf(mul0, static_cast<float>(d0), fmaf(add0, static_cast<float>(sx.x), acc[t]));
+                        acc[t] = fmaf(mul1, static_cast<float>(d1), fmaf(add1, static_cast<float>(sx.y), r));
+                    }
                 }
             }
             float mine = 0.0f;
@@ -420,18 +378,19 @@ static cudaError_t gemv_launch(int G, unsigned grid, size_t smem, cudaStream_t s
     return gemv_launch_g<Q6, 8>(grid, smem, st, a);
 }
 
-// out[t][r] = s_x[t] * sum_k xc[t][k] W[r][k] (W exactly decoded), for n tokens in launches of at most
-// GEMV_TOKENS (fewer when a token's codes and the tiles would not fit shared
-// memory); W in Q4_K (q6k false) or Q6_K.  A persistent grid of at most two
-// CTAs per SM walks the tiles.
-// in_mode 1 / 2: the tokens come as raw bf16 / fp32 rows xraw [n][cols] and
-// are quantised in each CTA (xc, sx unused).  cs_state non-null: the first
-// launch also shifts the conv tails of cs_n sequences (see GemvArgs).
+// out[t][r] = s_x[t] * sum_k x[t][k] W[r][k] (W exactly decoded), for n tokens
+// in launches of at most GEMV_TOKENS (fewer when a token's codes and the
+// tiles would not fit shared memory); W in Q4_K (q6k false) or Q6_K.  The
+// codes come as fp16 patterns xc [n][cols] or packed (xpack, stride
+// xpack_stride words per token, written by launch_decode_pack); sx [n] the
+// scales.  A persistent grid of up to four CTAs per SM walks the tiles.
+// cs_state non-null: the first launch also shifts the conv tails of cs_n
+// sequences (see GemvArgs).
 cudaError_t launch_gemv_dot(const void* blocks, bool q6k, int64_t rows, int64_t cols, const uint16_t* xc,
-                              const float* sx, int64_t n, uint16_t* out_bf16, int64_t ld_bf16, int64_t n_bf16,
-                              float* out_f32, int64_t ld_f32, cudaStream_t st, int in_mode, const void* xraw,
-                              float* cs_state, const uint16_t* cs_qkvz, int64_t cs_ld, int cs_c_conv, int cs_n,
-                              const float* rms_psum, int rms_hv, int rms_d, int rms_split, float rms_eps) {
+                              const uint32_t* xpack, int64_t xpack_stride, const float* sx, int64_t n,
+                              uint16_t* out_bf16, int64_t ld_bf16, int64_t n_bf16, float* out_f32, int64_t ld_f32,
+                              cudaStream_t st, float* cs_state, const uint16_t* cs_qkvz, int64_t cs_ld, int cs_c_conv,
+                              int cs_n) {
     static int sms = 0, max_optin = 0, fa_static = 0;
     if (!sms) {
         int dev = 0;
@@ -462,19 +421,15 @@ cudaError_t launch_gemv_dot(const void* blocks, bool q6k, int64_t rows, int64_t 
         a.ntiles = ntiles;
         a.total_bytes = rows * row_bytes;
         a.xc = xc ? xc + t0 * cols : nullptr;
-        a.sx = sx ? sx + t0 : nullptr;
-        a.in_mode = in_mode;
-        a.xraw = xraw ? static_cast<const uint8_t*>(xraw) + t0 * cols * (in_mode == 1 ? 2 : 4) : nullptr;
+        a.xpack = xpack ? xpack + t0 * xpack_stride : nullptr;
+        a.xpack_stride = xpack_stride;
+        a.sx = sx + t0;
+        a.in_mode = xpack ? 1 : 0;
         a.cs_state = t0 == 0 ? cs_state : nullptr;
         a.cs_qkvz = cs_qkvz;
         a.cs_ld = cs_ld;
         a.cs_c_conv = cs_c_conv;
         a.cs_n = cs_n;
-        a.rms_psum = rms_psum ? rms_psum + t0 * rms_hv * rms_split : nullptr;
-        a.rms_hv = rms_hv;
-        a.rms_d = rms_d > 0 ? rms_d : 1;
-        a.rms_split = rms_split;
-        a.rms_eps = rms_eps;
         a.g = static_cast<int>(n - t0 < gmax ? n - t0 : gmax);
         a.out_bf16 = out_bf16 ? out_bf16 + t0 * ld_bf16 : nullptr;
         a.ld_bf16 = ld_bf16;
@@ -504,6 +459,128 @@ cudaError_t launch_gemv_dot(const void* blocks, bool q6k, int64_t rows, int64_t 
     }
     (void)tb;
     return cudaSuccess;
+}
+
+// ------------------------------------------------------------ packed token rows
+
+constexpr int PACK_THREADS = 256;
+
+// Words per packed token row of `cols` codes (a multiple of 64, so every row
+// starts on 16 bytes).
+__host__ __device__ int64_t decode_pack_stride(int64_t cols) { return cols / 4 + cols / 16; }
+
+// Elements off .. off+15 of a bf16 (f32 false) or fp32 row as floats, times sc.
+__device__ __forceinline__ void pack_raw16(const void* src, bool f32, int64_t off, float sc, float (&w)[16]) {
+    if (!f32) {
+        const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(src) + off);
+        const uint4 u0 = __ldg(p), u1 = __ldg(p + 1);
+        const uint32_t u[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            w[2 * e] = __uint_as_float(u[e] << 16);
+            w[2 * e + 1] = __uint_as_float(u[e] & 0xffff0000u);
+        }
+    } else {
+        const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(src) + off);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float4 v = __ldg(p + e);
+            w[4 * e] = v.x * sc; w[4 * e + 1] = v.y * sc; w[4 * e + 2] = v.z * sc; w[4 * e + 3] = v.w * sc;
+        }
+    }
+}
+
+// Token row t quantised once, by one CTA of PACK_THREADS threads, as the
+// projection kernel takes it: scale amax/127 and the same codes as step 1b,
+// written as cols/4 words of 4 int8 codes followed by cols/16 sums of 16
+// codes (stride words per token), and the row's scale.  The row is bf16 (the
+// decode input) or fp32 with head h multiplied first by rsqrt(sum_p
+// psum[h][p] / d + eps) (the gated norm's RMS of o, from the partial sums of
+// o^2 over the head's row blocks, added in order).  rh: hv floats, red:
+// PACK_THREADS / 32 floats of shared memory.
+__device__ void pack_row(const void* src, bool f32, int cols, const float* psum, int hv, int d, int split, float eps,
+                         int t, uint32_t* pack, int64_t stride, float* scale, float* rh, float* red) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (psum) {
+        for (int h = tid; h < hv; h += PACK_THREADS) {
+            const float* ps = psum + (static_cast<int64_t>(t) * hv + h) * split;
+            float sum = 0.0f;
+            for (int p = 0; p < split; ++p) sum += ps[p];
+            rh[h] = rsqrtf(sum / static_cast<float>(d) + eps);
+        }
+        __syncthreads();
+    }
+    const int k16 = cols >> 4;
+    const int64_t row = static_cast<int64_t>(t) * cols;
+    float amax = 0.0f;
+    for (int b = tid; b < k16; b += PACK_THREADS) {
+        float w[16];
+        pack_raw16(src, f32, row + 16 * b, psum ? rh[(16 * b) / d] : 1.0f, w);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fabsf(w[e]));
+    }
+    amax = warp_max(amax);
+    if (lane == 0) red[warp] = amax;
+    __syncthreads();
+    amax = red[0];
+#pragma unroll
+    for (int w = 1; w < PACK_THREADS / 32; ++w) amax = fmaxf(amax, red[w]);
+    const QScale qsc = make_qscale(amax);
+    if (tid == 0) scale[t] = qsc.s;
+    uint32_t* words = pack + static_cast<int64_t>(t) * stride;
+    int* sums = reinterpret_cast<int*>(words + (cols >> 2));
+    for (int b = tid; b < k16; b += PACK_THREADS) {
+        float w[16], c[16];
+        pack_raw16(src, f32, row + 16 * b, psum ? rh[(16 * b) / d] : 1.0f, w);
+        bool redo = !qsc.fast;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) c[e] = qcode_fast(w[e], qsc, redo);
+        if (redo) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) c[e] = qcode_exact(w[e], qsc.s);
+        }
+        uint32_t pk[4];
+        int sum = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            pk[q] = codes_to_i8x4(c[4 * q], c[4 * q + 1], c[4 * q + 2], c[4 * q + 3]);
+            sum = __dp4a(static_cast<int>(pk[q]), 0x01010101, sum);
+        }
+        *reinterpret_cast<uint4*>(words + 4 * b) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        sums[b] = sum;
+    }
+}
+
+// Rows packed one CTA per token (pack_row): bf16 x, or fp32 o_hat with
+// psum / hv / d / split / eps for the RMS of each head.  A programmatic
+// dependent: it lets the next kernel be scheduled, then waits for the
+// previous one before it reads or writes anything.
+__global__ void __launch_bounds__(PACK_THREADS) decode_pack_kernel(const void* src, int f32, int cols, const float* psum,
+                                                                    int hv, int d, int split, float eps, uint32_t* pack,
+                                                                    int64_t stride, float* scale) {
+    pdl_trigger();
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    __shared__ float rh[64], red[PACK_THREADS / 32];
+    pack_row(src, f32 != 0, cols, psum, hv, d, split, eps, blockIdx.x, pack, stride, scale, rh, red);
+}
+
+// n rows of src (bf16, or fp32 with psum / hv / d / split / eps for the RMS
+// of each head) into pack [n][decode_pack_stride(cols)] and scale [n]; a
+// programmatic dependent launch.
+cudaError_t launch_decode_pack(const void* src, bool f32, int64_t n, int64_t cols, const float* psum, int hv, int d,
+                               int split, float eps, uint32_t* pack, float* scale, cudaStream_t st) {
+    if (cols % 256 != 0 || (psum && (hv > 64 || d < 16 || d % 16 != 0))) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(n), 1, 1);
+    cfg.blockDim = dim3(PACK_THREADS, 1, 1);
+    cfg.stream = st;
+    cudaLaunchAttribute at;
+    at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_pack_kernel, src, f32 ? 1 : 0, static_cast<int>(cols), psum, hv, d, split, eps,
+                              pack, decode_pack_stride(cols), scale);
 }
 
 // ------------------------------------------------------------ conv, recurrence, gated norm
@@ -559,7 +636,10 @@ __global__ void __launch_bounds__(MID_THREADS) decode_mid_kernel(MidArgs a) {
     constexpr int R = NR / MID_WARPS;                // rows per warp
     __shared__ float qs[D], ks[D], vs[NR], gz[NR], red[MID_WARPS];
     __shared__ float gate[2];
+    // a programmatic dependent of the input projection: the next kernel may be
+    // scheduled at once; nothing is read before the projection has completed
     pdl_trigger();
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int h = blockIdx.x / MID_SPLIT, part = blockIdx.x % MID_SPLIT, sq = blockIdx.y, hk = h / a.ratio;
     const int i0 = part * NR;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -705,12 +785,19 @@ cudaError_t launch_decode_mid(const gdn_layer& L, const uint16_t* qkvz, int64_t 
     a.eps_l2 = L.eps_l2;
     a.eps_rms = L.eps_rms;
     a.q_scale = L.q_scale;
-    const dim3 grid(static_cast<unsigned>(a.hv * MID_SPLIT), static_cast<unsigned>(n_seqs));
-    if (d == 128)
-        decode_mid_kernel<128><<<grid, MID_THREADS, 0, st>>>(a);
-    else
-        decode_mid_kernel<64><<<grid, MID_THREADS, 0, st>>>(a);
-    return cudaGetLastError();
+    // a programmatic dependent launch (the kernel waits for the projection first)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(a.hv * MID_SPLIT), static_cast<unsigned>(n_seqs), 1);
+    cfg.blockDim = dim3(MID_THREADS, 1, 1);
+    cfg.stream = st;
+    cudaLaunchAttribute at;
+    at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &at;
+    cfg.numAttrs = 1;
+    const cudaError_t e = d == 128 ? cudaLaunchKernelEx(&cfg, decode_mid_kernel<128>, a)
+                                   : cudaLaunchKernelEx(&cfg, decode_mid_kernel<64>, a);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 int read_and_clear_decode_error() {

@@ -70,47 +70,6 @@ quant_rows_bf16_kernel(const uint16_t* __restrict__ x, int cols, uint16_t* __res
     }
 }
 
-// The same quantisation of fp32 rows (the decode step's gated-norm output):
-// one CTA per row, 8 values a thread per pass, the row read twice (L1).
-__global__ void __launch_bounds__(256) quant_rows_f32_kernel(const float* __restrict__ x, int cols,
-                                                             uint16_t* __restrict__ codes, float* __restrict__ scale) {
-    pdl_trigger();
-    __shared__ float red[32];
-    const int64_t row = blockIdx.x;
-    const float4* src = reinterpret_cast<const float4*>(x + row * cols);
-    const int n8 = cols >> 3;
-    float amax = 0.0f;
-    for (int j = threadIdx.x; j < n8; j += 256) {
-        const float4 a = __ldg(src + 2 * j), b = __ldg(src + 2 * j + 1);
-        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))));
-        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(b.x), fabsf(b.y)), fmaxf(fabsf(b.z), fabsf(b.w))));
-    }
-    amax = block_max(amax, red);
-    const QScale qsc = make_qscale(amax);
-    if (threadIdx.x == 0) scale[row] = qsc.s;
-    uint4* dst = reinterpret_cast<uint4*>(codes + row * cols);
-    for (int j = threadIdx.x; j < n8; j += 256) {
-        const float4 a = __ldg(src + 2 * j), b = __ldg(src + 2 * j + 1);
-        const float xv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-        float c[8];
-        bool redo = !qsc.fast;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) c[e] = qcode_fast(xv[e], qsc, redo);
-        if (redo) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) c[e] = qcode_exact(xv[e], qsc.s);
-        }
-        dst[j] = make_uint4(codes_to_f16x2(c[0], c[1]), codes_to_f16x2(c[2], c[3]), codes_to_f16x2(c[4], c[5]),
-                            codes_to_f16x2(c[6], c[7]));
-    }
-}
-
-cudaError_t launch_quant_rows_f32(const float* x, int64_t rows, int64_t cols, uint16_t* codes, float* scale,
-                                  cudaStream_t st) {
-    quant_rows_f32_kernel<<<static_cast<unsigned>(rows), 256, 0, st>>>(x, static_cast<int>(cols), codes, scale);
-    return cudaGetLastError();
-}
-
 cudaError_t launch_quant_rows(const uint16_t* x, int64_t rows, int64_t cols, uint16_t* codes, float* scale,
                               cudaStream_t st) {
     static_assert(16384 / 8 <= QR_VEC * 256, "the widest row must fit a 256-thread CTA");

@@ -233,9 +233,11 @@ int gdn_prefill_batch(const gdn_layer *layer, const void *x, const int64_t *cu_s
  * L2 norms, gates, one token of the recurrence (S <- a S (I - b k k^T) +
  * b v k^T, o = S q) and the gated RMSNorm run in fp32 in one kernel per
  * (value head, sequence), with none of the prefill's fp16 operand roundings;
- * the quantisation of each token (before the input projection) and of its
- * gated-norm output (before the output projection) happens inside the
- * projection kernels.  Three launches in all.  A decoded token therefore
+ * each token (before the input projection) and its gated-norm output with
+ * the RMS of each head (before the output projection) are quantised once by
+ * a small packing kernel.  Five launches in all, each started while the one
+ * before it ends (programmatic dependent launches: the projections' weight
+ * copies begin before their inputs exist).  A decoded token therefore
  * agrees with a prefill of it within the stated tolerances, not bit for bit.
  * 1 <= n_seqs <= GDN_MAX_SEQS.
  */
