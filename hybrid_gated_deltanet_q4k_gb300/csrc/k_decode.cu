@@ -1,5 +1,12 @@
 // The decode step of the layer: one new token for each of B sequences, in
-// three launches:
+// five launches, each a programmatic dependent of the one before (it may be
+// scheduled while that one runs; griddepcontrol.wait comes before anything it
+// reads of that kernel's results):
+//
+// decode_pack_kernel -- the tokens' rows quantised once to int8 codes as the
+//   prefill's step 1b does (scale s_x per token), packed four to a word with
+//   the sums of every 16 codes; later the gated-norm output o_hat the same
+//   way, after the RMS of each head.
 //
 // gemv_dot_kernel -- the projections for a few tokens.  Decoding a whole
 //   weight matrix to int8 rows in HBM (step 1a of the prefill) would move 3.5x
@@ -7,15 +14,15 @@
 //   instructions than reading it; a decode GEMV is bound by reading the
 //   quantised weights once ("Qwen3.5 speed: prefill and decode parity with
 //   llama.cpp" #5305, child ticket #5221: decode GEMV bandwidth against
-//   llama.cpp's quantised GEMV, Q4_K and Q6_K).  So the tokens keep the int8
-//   row codes the prefill gives them (scale s_x per token), and each weight
-//   sub-block meets them as integers: for a Q4_K sub-block
+//   llama.cpp's quantised GEMV, Q4_K and Q6_K).  So each weight sub-block
+//   meets the tokens' codes as integers: for a Q4_K sub-block
 //       sum_k w_k x_k = d*sc * sum q_k x_k - dmin*m * sum x_k,
 //   for a Q6_K sub-block d*scale * (sum c_k x_k - 32 sum x_k), the integer
 //   sums by dp4a on the packed 4-bit / 6-bit codes, the rest in fp32; the
 //   token's total is then multiplied by s_x.  Weight tiles of 8 rows (one per
-//   warp) arrive in shared memory by bulk copies through a ring of stages, so
-//   each row is read from HBM once with many bytes in flight.
+//   warp) arrive in shared memory by bulk copies through a ring of stages,
+//   the first ones issued before the dependency wait, so each row is read
+//   from HBM once with many bytes in flight.
 //
 // decode_mid_kernel -- per (value head, block of its state rows, sequence):
 //   the conv, SiLU and L2 norms of the token's q, k, v, the gates, and one
@@ -29,8 +36,8 @@
 //   name llama.cpp's form as prior art (a token loop with the state in
 //   registers, "CRUX parity spike" #4220, technique table row 1).  It writes
 //   the gated output o * norm_w * SiLU(z) and partial sums of o^2; the
-//   output projection's kernel applies the RMS of each head, quantises the
-//   row and shifts the conv tails (the readers of the old tails are done).
+//   output projection's kernel also shifts the conv tails (the readers of the
+//   old tails are done).
 #include "common.cuh"
 #include "qk_decode.cuh"
 #include "tma.cuh"
