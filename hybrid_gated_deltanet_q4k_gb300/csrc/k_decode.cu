@@ -413,7 +413,6 @@ cudaError_t launch_gemv_dot(const void* blocks, bool q6k, int64_t rows, int64_t 
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     }
     const int64_t row_bytes = (cols / 256) * (q6k ? 210 : 144);
-    const int64_t tb = gemv_tile_bytes(row_bytes);
     // tokens per launch (a power of two): what fits beside one stage
     int64_t gmax = GEMV_TOKENS;
     while (gmax > 1 && gemv_smem_bytes(static_cast<int>(gmax), static_cast<int>(cols), row_bytes, 1) > max_optin) gmax /= 2;
@@ -464,7 +463,6 @@ cudaError_t launch_gemv_dot(const void* blocks, bool q6k, int64_t rows, int64_t 
         if (e == cudaSuccess) e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    (void)tb;
     return cudaSuccess;
 }
 
