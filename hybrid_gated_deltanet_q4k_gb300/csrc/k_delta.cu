@@ -89,6 +89,13 @@ __device__ __forceinline__ uint4 f16x8(const float (&v)[8]) {
 // true when x is not a finite value fp16 can hold
 __device__ __forceinline__ bool f16_out_of_range(float x) { return !(fabsf(x) <= F16_MAX); }
 
+// max(a, b), a NaN if either is one
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+
 // ------------------------------------------------------------------ prep
 
 constexpr int PREP_MAX_RATIO = 8;  // value heads per key head handled by one CTA
@@ -496,9 +503,12 @@ struct StateSmem {
     static constexpr int KT0 = QK0 + NSLAB * QK_SLAB;   // K^T [2][D][DC] (bulk copies)
     static constexpr int TA0 = KT0 + 2 * KT_BYTES; // [A T; T] [2*DC][DC] (bulk copy of the prep image)
     static constexpr int V0 = TA0 + QK_SLAB;       // V [DC][64]        (TMA; this CTA's NV columns at i0 % 64)
-    static constexpr int S0 = V0 + SLAB;           // S [NV][D]         fp16 operand of X, Y
-    static constexpr int R0 = S0 + NSLAB * SOP;    // R^T [NV][DC]
-    static constexpr int E0 = R0 + SOP;            // Delta~^T [NV][DC]
+    // the three B operands the compute warps write are stored MN-major (row =
+    // K index, NV = 32 fp16 of 64 bytes each, 64-byte swizzle), so a thread
+    // holding 16 consecutive v of one K index writes two 16-byte chunks
+    static constexpr int S0 = V0 + SLAB;           // S [D][NV]         fp16 operand of X, Y
+    static constexpr int R0 = S0 + NSLAB * SOP;    // R [DC][NV]
+    static constexpr int E0 = R0 + SOP;            // Delta~ [DC][NV]
     static constexpr int G0 = E0 + SOP;            // gate table [2][DC] x (gamma, e^gamma, b, e^{gamma_C-gamma})
     static constexpr int B0 = G0 + 2 * DC * 16;    // mbarriers
     static constexpr int NBAR = 14;
@@ -557,6 +567,16 @@ __device__ __forceinline__ void mma_chain(uint32_t d_tmem, uint64_t adesc, uint6
     for (int k = 0; k < NK; ++k)
         t5::mma_f16(d_tmem, adesc + static_cast<uint64_t>((k >> 2) * (A_SLAB >> 4) + 2 * (k & 3)),
                     bdesc + static_cast<uint64_t>((k >> 2) * (B_SLAB >> 4) + 2 * (k & 3)), idesc, k > 0 ? 1u : 0u);
+}
+
+// The same with an MN-major B operand (desc_sw64_mn): a K step of 16 rows of
+// 64 bytes is 1024 bytes further on.
+template <int NK, int A_SLAB>
+__device__ __forceinline__ void mma_chain_bmn(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc) {
+#pragma unroll
+    for (int k = 0; k < NK; ++k)
+        t5::mma_f16(d_tmem, adesc + static_cast<uint64_t>((k >> 2) * (A_SLAB >> 4) + 2 * (k & 3)),
+                    bdesc + static_cast<uint64_t>(k * (1024 >> 4)), idesc, k > 0 ? 1u : 0u);
 }
 
 // One CTA per (value head, NV rows of S); 320 threads:
@@ -653,11 +673,12 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a, con
         }
     } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
-        constexpr uint32_t ID128 = t5::idesc_f16(128, NV);
-        constexpr uint32_t IDU = t5::idesc_f16(D, NV);
-        const uint64_t dQK = t5::desc_sw128(sbase + L::QK0), dS = t5::desc_sw128(sbase + L::S0);
-        const uint64_t dTA = t5::desc_sw128(sbase + L::TA0), dR = t5::desc_sw128(sbase + L::R0);
-        const uint64_t dE = t5::desc_sw128(sbase + L::E0);
+        // B operands MN-major (bit 16 of the instruction descriptor)
+        constexpr uint32_t ID128 = t5::idesc_f16(128, NV) | (1u << 16);
+        constexpr uint32_t IDU = t5::idesc_f16(D, NV) | (1u << 16);
+        const uint64_t dQK = t5::desc_sw128(sbase + L::QK0), dS = t5::desc_sw64_mn(sbase + L::S0);
+        const uint64_t dTA = t5::desc_sw128(sbase + L::TA0), dR = t5::desc_sw64_mn(sbase + L::R0);
+        const uint64_t dE = t5::desc_sw64_mn(sbase + L::E0);
         const uint64_t dKT = t5::desc_sw128(sbase + L::KT0);
         const bool leader = lane == 0;
         // leader only: the copy has landed and nothing has failed
@@ -670,21 +691,21 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a, con
             const uint32_t ph = j & 1;
             nb_sync(NB_S);                      // S of chunk j written
             if (leader && ready(F_QK, ph)) {
-                mma_chain<D / 16, L::QK_SLAB, L::SOP>(tmem + TM_XY + 32 * ph, dQK, dS, ID128);
+                mma_chain_bmn<D / 16, L::QK_SLAB>(tmem + TM_XY + 32 * ph, dQK, dS, ID128);
                 t5::commit(bars + M_XY);
                 t5::commit(bars + E_QK);
             }
             __syncwarp();
             nb_sync(NB_R);                      // R^T written
             if (leader && ready(F_TA, ph)) {
-                mma_chain<DC / 16, L::QK_SLAB, L::SOP>(tmem + TM_DZ, dTA, dR, ID128);
+                mma_chain_bmn<DC / 16, L::QK_SLAB>(tmem + TM_DZ, dTA, dR, ID128);
                 t5::commit(bars + M_DZ);
                 t5::commit(bars + E_TA);
             }
             __syncwarp();
             nb_sync(NB_D);                      // Delta~^T written
             if (leader && ready(F_KT0 + ph, (j >> 1) & 1)) {
-                mma_chain<DC / 16, L::KT_BYTES, L::SOP>(tmem + TM_U, dKT + ph * (L::KT_BYTES >> 4), dE, IDU);
+                mma_chain_bmn<DC / 16, L::KT_BYTES>(tmem + TM_U, dKT + ph * (L::KT_BYTES >> 4), dE, IDU);
                 t5::commit(bars + M_U);
                 t5::commit(bars + E_KT0 + ph);
             }
@@ -714,25 +735,29 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a, con
 #pragma unroll
         for (int v = 0; v < 16; ++v)
             S[v] = (own_d && st_in) ? st_in[(static_cast<int64_t>(h) * D + i0 + v0 + v) * D + d] : 0.f;
+        // values v0 .. v0+15 of row k of an MN-major [K][NV] operand at off: two
+        // 16-byte chunks of the 64-byte row, placed by the 64-byte swizzle
+        auto write_row = [&](int off, int k, const float (&x)[16]) {
+            float m = 0.0f;
+#pragma unroll
+            for (int v = 0; v < 16; ++v) m = fmax_nan(m, fabsf(x[v]));
+            bad |= !(m <= F16_MAX);              // an infinity, a NaN or a value past the fp16 range
+            float lo[8], hi[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                lo[e] = x[e];
+                hi[e] = x[8 + e];
+            }
+            unsigned char* row = base + off + k * 64;
+            const int c0 = v0 >> 3, sw = (k >> 1) & 3;
+            *reinterpret_cast<uint4*>(row + ((c0 ^ sw) << 4)) = f16x8(lo);
+            *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ sw) << 4)) = f16x8(hi);
+        };
         auto write_s = [&]() {
-            if (own_d) {
-                unsigned char* sp = base + L::S0 + (d >> 6) * L::SOP;
-#pragma unroll
-                for (int v = 0; v < 16; ++v) {
-                    bad |= f16_out_of_range(S[v]);
-                    *reinterpret_cast<uint16_t*>(sp + sw128_f16(v0 + v, d & 63)) = f16_bits(S[v]);
-                }
-            }
+            if (own_d) write_row(L::S0, d, S);
         };
-        // column t of an [NV][DC] operand (R^T, Delta~^T), rows v0 .. v0+15
-        auto write_col = [&](int off, int t, const float (&x)[16]) {
-            unsigned char* cp = base + off;
-#pragma unroll
-            for (int v = 0; v < 16; ++v) {
-                bad |= f16_out_of_range(x[v]);
-                *reinterpret_cast<uint16_t*>(cp + sw128_f16(v0 + v, t)) = f16_bits(x[v]);
-            }
-        };
+        // the row of token t of an [DC][NV] operand (R, Delta~)
+        auto write_col = [&](int off, int t, const float (&x)[16]) { write_row(off, t, x); };
         // the operands this thread wrote go to the tensor cores
         auto handover = [&](int id) {
             fence_proxy_async_smem();

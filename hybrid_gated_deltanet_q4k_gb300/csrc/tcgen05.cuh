@@ -57,6 +57,19 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
            (static_cast<uint64_t>(2) << 61);
 }
 
+// Shared-memory descriptor of an MN-major operand stored with the 64-byte
+// swizzle: at each K index a row of 64 bytes holds 32 consecutive fp16 of the
+// M (or N) dimension, the 16-byte chunk c of row k at chunk c ^ ((k >> 1) & 3);
+// groups of 8 rows (512 bytes) follow each other (stride 512 B >> 4 at bits
+// 32-45); one swizzle atom along M/N, so the leading offset (16 B) is unused;
+// descriptor version 1 (bit 46), layout type 4 = 64-byte swizzle (bits 61-63).
+// A K step of 16 rows adds 1024 B >> 4 = 64 to the start field.
+__device__ __forceinline__ uint64_t desc_sw64_mn(uint32_t saddr) {
+    return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(1) << 16) |
+           (static_cast<uint64_t>(512 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+           (static_cast<uint64_t>(4) << 61);
+}
+
 // D[tmem] (+)= A * B^T, one elected thread.
 __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                          uint32_t accumulate) {
