@@ -42,6 +42,8 @@
 #include "qk_decode.cuh"
 #include "tma.cuh"
 
+#include <mutex>
+
 namespace gdn {
 
 static __device__ int g_decode_error;
@@ -399,7 +401,8 @@ cudaError_t launch_gemv_dot(const void* blocks, bool q6k, int64_t rows, int64_t 
                               cudaStream_t st, float* cs_state, const uint16_t* cs_qkvz, int64_t cs_ld, int cs_c_conv,
                               int cs_n) {
     static int sms = 0, max_optin = 0, fa_static = 0;
-    if (!sms) {
+    static std::once_flag once;
+    std::call_once(once, [] {
         int dev = 0;
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
@@ -411,7 +414,7 @@ cudaError_t launch_gemv_dot(const void* blocks, bool q6k, int64_t rows, int64_t 
         gemv_set_smem<false>(max_optin);
         gemv_set_smem<true>(max_optin);
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    }
+    });
     const int64_t row_bytes = (cols / 256) * (q6k ? 210 : 144);
     // tokens per launch (a power of two): what fits beside one stage
     int64_t gmax = GEMV_TOKENS;
