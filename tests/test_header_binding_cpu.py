@@ -50,3 +50,21 @@ def test_layer_struct_layout_matches_the_header(tmp_path):
     assert int(got["size"]) == ctypes.sizeof(gl.GdnLayer)
     for f in fields:
         assert int(got[f]) == getattr(gl.GdnLayer, f).offset, f
+
+
+def _prototypes():
+    text = re.sub(r"/\*.*?\*/", " ", open(HEADER).read(), flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    protos = {}
+    for m in re.finditer(r"\b((?:gdn|q4k|q6k)_\w+)\s*\(([^;{}()]*)\)\s*;", text):
+        args = m.group(2).strip()
+        protos[m.group(1)] = 0 if args in ("", "void") else len(args.split(","))
+    return protos
+
+
+def test_binding_signatures_have_the_header_arity():
+    protos = _prototypes()
+    assert len(protos) >= 20
+    for name, (_, argtypes) in gl._SIGNATURES.items():
+        assert name in protos, name
+        assert len(argtypes) == protos[name], (name, len(argtypes), protos[name])
