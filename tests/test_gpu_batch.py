@@ -81,6 +81,8 @@ def _batch(dl, spec, tok, cu, state0, conv0, gates, state_in_null=False):
     ([1, 63, 64, 65, 200, 0, 700], True),
     ([5000, 130, 0, 3000, 1], True),        # token segments (rounds) with sequences ending in different ones
     ([300, 17, 129], False),                # gates from the projection
+    # the maximum number of sequences, ragged lengths 0..39
+    ([int(v) for v in np.random.default_rng(256).integers(0, 40, gl.GDN_MAX_SEQS)], True),
 ])
 def test_batch_equals_each_sequence_alone(lens, gates):
     spec = SMALL

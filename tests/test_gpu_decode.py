@@ -197,3 +197,30 @@ def test_decode_argument_checks(L):
     import ctypes
     assert L.gdn_decode(ctypes.byref(s), gl.ptr(x), 0, gl.ptr(st), gl.ptr(cv), gl.ptr(y), gl.ptr(ws), ws.numel(),
                         stream(), check=False) == gl.GDN_EINVAL
+
+
+def test_decode_at_the_maximum_number_of_sequences():
+    """GDN_MAX_SEQS sequences in one call (32 launches of the 8-token
+    projection kernels): sampled sequences, the last included, against the
+    oracle's decode step."""
+    spec = SMALL
+    layer = synth.make_layer(spec)
+    n = gl.GDN_MAX_SEQS
+    tok = synth.make_tokens(spec, n, seed=77)
+    dl = DeviceLayer(spec, layer)
+    st0, cv0 = _saved_states(spec, n, seed=78)
+    state, conv = torch.from_numpy(st0).to(DEV), torch.from_numpy(cv0).to(DEV)
+    y = torch.empty(n, spec.hidden, dtype=torch.bfloat16, device=DEV)
+    dl.decode(bf16_dev(tok["x_bits"]), state, conv, y, dl.new_decode_workspace(n), gate_log_a=f32_dev(tok["log_a"]),
+              gate_b=f32_dev(tok["b"]))
+    sync(dl.lib)
+    p = oracle_params(spec, layer)
+    yh = bf16_host_f32(y)
+    for s in (0, 1, 7, 8, 129, n - 1):
+        ref = OL.layer_forward(p, tok["x"][s:s + 1], S0=st0[s].astype(np.float64), conv_tail=cv0[s],
+                               gate_log_a=tok["log_a"][s:s + 1], gate_b=tok["b"][s:s + 1], decode=True)
+        assert rel_l2(yh[s:s + 1], ref["y"]) <= 1e-2, s
+        assert rel_l2(state[s].cpu().numpy(), ref["state"]) <= 2e-3, s
+        c = conv[s].cpu().numpy()
+        assert np.array_equal(c[:, :2], cv0[s][:, 1:]), s
+        assert _tail_close(c[:, 2], ref["conv_tail"][:, 2]), s
