@@ -22,7 +22,9 @@
 //   token's total is then multiplied by s_x.  Weight tiles of 8 rows (one per
 //   warp) arrive in shared memory by bulk copies through a ring of stages,
 //   the first ones issued before the dependency wait, so each row is read
-//   from HBM once with many bytes in flight.
+//   from HBM once with many bytes in flight.  Q4_K weights whose rows fit
+//   shared memory beside 8 tokens' codes go to gemv_q4k_mma_kernel (below)
+//   instead: the same sums on the fp16 tensor-core form.
 //
 // decode_mid_kernel -- per (value head, block of its state rows, sequence):
 //   the conv, SiLU and L2 norms of the token's q, k, v, the gates, and one
@@ -387,6 +389,408 @@ static cudaError_t gemv_launch(int G, unsigned grid, size_t smem, cudaStream_t s
     return gemv_launch_g<Q6, 8>(grid, smem, st, a);
 }
 
+// gemv_q4k_mma_kernel -- the Q4_K projection with the per-sub-block dot
+// products on the fp16 tensor-core form (mma.sync m16n8k16, fp32 sums): 16
+// weight rows x 16 weights of a sub-block against 8 tokens' codes.  The same
+// sum as gemv_dot_kernel,
+//     sum_k w_k x_k = d*sc_j * sum_k q_k x_k - dmin*m_j * sum_k x_k,
+// taken per superblock with every intermediate an exact integer:
+//     y += d * (sum_j sum_k (sc_j q_k) x_k) - dmin * (sum_j sum_k m_j x_k).
+// The A operand holds sc_j q_k (<= 63 * 15, exact in fp16: one fma on the
+// fp16 pattern 1024 + q), or m_j repeated over the sub-block's positions; B
+// holds the tokens' int8 codes as fp16 (exact).  Products are exact and the
+// fp32 sums are integers, exact below 2^24 (a sub-block contributes at most
+// 32 * 945 * 127 < 2^22, a superblock's min term < 2^21), so the superblock's
+// two sums are, in practice, the exact integers.  Each token's result takes
+// the same operations in the same order whatever the other tokens of the
+// launch, so a batch gives each token's result bit for bit as that token
+// alone.  (The int8 form of the instruction would take the codes as they are,
+// but the int8 tensor rate of this part is far below its fp16 rate.)
+//
+// The contraction order within a sub-block is free: lane (g, q) of the
+// instruction takes the weights and token codes 8q .. 8q+7 of the sub-block
+// (its four fp16 pairs over the two k16 steps), which makes the weights one
+// 8-byte load of consecutive Q4_K code bytes and the codes one 16-byte load.
+//
+// Work: tiles of 16 rows; the 8 warps of a CTA split a tile's superblocks
+// (warp w takes superblocks w, w+8, ...) and their partial sums meet in
+// shared memory in warp order.  Each tile's rows arrive by bulk copies (one
+// per row, into rows padded to 32 mod 128 bytes so that the fragment loads
+// are free of bank conflicts) through a ring of stages; the first stages are
+// requested before the dependency wait.  Up to 16 tokens per launch (NT
+// groups of 8), so the weights are read once for all of them.
+constexpr int QM_WARPS = 8;
+constexpr int QM_THREADS = QM_WARPS * 32;
+constexpr int QM_ROWS = 16;
+constexpr int QM_MAX_STAGES = 6;
+constexpr int QM_MAX_NT = 2;
+constexpr int QM_CTAS_PER_SM = 1;
+
+struct QmArgs {
+    const uint8_t* blocks;   // [rows][cols/256] Q4_K superblocks
+    int rows, cols;
+    int64_t row_bytes;       // 144 * cols/256
+    int row_stride;          // bytes of a row in a shared-memory stage
+    int ntiles, stages;
+    int in_mode;             // 0: xc fp16 patterns; 1: xpack (see GemvArgs)
+    const uint16_t* xc;
+    const uint32_t* xpack;
+    int64_t xpack_stride;
+    const float* sx;
+    int g;                   // tokens of this launch, 1 .. 8 * NT
+    uint16_t* out_bf16;
+    int64_t ld_bf16;
+    int n_bf16;
+    float* out_f32;
+    int64_t ld_f32;
+    float* cs_state;
+    const uint16_t* cs_qkvz;
+    int64_t cs_ld;
+    int cs_c_conv, cs_n;
+};
+
+// Shared memory: the tokens' codes as fp16 [8 NT][cols + 32] (rows 64 mod 128
+// bytes apart: conflict-free 16-byte fragment loads), the warps' partial sums
+// [QM_WARPS][NT][32 lanes] float4, the ring of stages [stages][16][row_stride],
+// then one mbarrier per stage, the tokens' barrier and an abort flag.
+__host__ __device__ inline int qm_row_stride(int64_t row_bytes) {
+    const int rs = static_cast<int>((row_bytes + 15) & ~15LL);
+    return rs + ((32 - rs % 128) + 128) % 128;
+}
+__host__ __device__ inline int64_t qm_x_stride(int cols) { return 2LL * cols + 64; }   // bytes
+__host__ __device__ inline int64_t qm_red_offset(int nt, int cols) {
+    return (8LL * nt * qm_x_stride(cols) + 127) & ~127LL;
+}
+__host__ __device__ inline int64_t qm_ring_offset(int nt, int cols) {
+    return (qm_red_offset(nt, cols) + static_cast<int64_t>(QM_WARPS) * nt * 32 * 16 + 127) & ~127LL;
+}
+__host__ __device__ inline int64_t qm_smem_bytes(int nt, int cols, int64_t row_bytes, int stages) {
+    return qm_ring_offset(nt, cols) + static_cast<int64_t>(stages) * QM_ROWS * qm_row_stride(row_bytes) +
+           8 * (QM_MAX_STAGES + 1) + 4;
+}
+
+// Copy the valid rows of tile `tile` into stage `s`, one bulk copy per row
+// (row_bytes is a multiple of 16: 144 bytes per superblock).  Thread 0.
+__device__ __forceinline__ void qm_issue(const QmArgs& a, unsigned char* ring, uint64_t* full, int tile, int s) {
+    if (tile >= a.ntiles) return;
+    const int r0 = tile * QM_ROWS;
+    const int nr = a.rows - r0 < QM_ROWS ? a.rows - r0 : QM_ROWS;
+    mbar_expect_tx(full + s, static_cast<uint32_t>(nr * a.row_bytes));
+    unsigned char* dst = ring + static_cast<int64_t>(s) * QM_ROWS * a.row_stride;
+    for (int r = 0; r < nr; ++r)
+        bulk_load_1d(dst + r * a.row_stride, a.blocks + static_cast<int64_t>(r0 + r) * a.row_bytes,
+                     static_cast<uint32_t>(a.row_bytes), full + s);
+}
+
+// d += A (16 x 16 fp16) * B (16 x 8 fp16), fp32
+__device__ __forceinline__ void mma_f16_m16n8k16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                                 uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+__device__ __forceinline__ __half2 bits_h2(uint32_t b) { return *reinterpret_cast<__half2*>(&b); }
+
+// Byte k of w (an integer < 1024) in both halves of an fp16 pair, exactly:
+// the pattern 0x64nn is 1024 + nn.
+__device__ __forceinline__ __half2 byte_h2(uint32_t w, int k) {
+    const uint32_t m = __byte_perm(w, 0x64646464u, 0x4040u + 0x0101u * k);
+    return __hsub2(bits_h2(m), __float2half2_rn(1024.0f));
+}
+
+// Bytes (0, 1) or (2, 3) of w as the fp16 pair (1024 + b0, 1024 + b1).
+__device__ __forceinline__ uint32_t bytes_magic_h2(uint32_t w, int hi) {
+    return __byte_perm(w, 0x64646464u, hi ? 0x7362u : 0x5140u);
+}
+
+// The 6-bit scales and mins of a Q4_K superblock's 8 sub-blocks, one per
+// byte: sl = sc[0..3], sh = sc[4..7], ml = m[0..3], mh = m[4..7] (sub-blocks
+// 4..7 take their two high bits from the top bits of the bytes of 0..3).
+__device__ __forceinline__ void q4k_unpack_scales(const uint4& h, uint32_t& sl, uint32_t& sh, uint32_t& ml,
+                                                  uint32_t& mh) {
+    sl = h.y & 0x3f3f3f3fu;
+    ml = h.z & 0x3f3f3f3fu;
+    sh = (h.w & 0x0f0f0f0fu) | ((h.y >> 2) & 0x30303030u);
+    mh = ((h.w >> 4) & 0x0f0f0f0fu) | ((h.z >> 2) & 0x30303030u);
+}
+
+template <int NT>
+__global__ void __launch_bounds__(QM_THREADS, 1) gemv_q4k_mma_kernel(QmArgs a) {
+    extern __shared__ __align__(128) unsigned char qsm[];
+    unsigned char* xs = qsm;                                                      // [8 NT][cols + 32] fp16
+    float4* red = reinterpret_cast<float4*>(qsm + qm_red_offset(NT, a.cols));     // [warps][NT][32]
+    unsigned char* ring = qsm + qm_ring_offset(NT, a.cols);
+    const int64_t tb = static_cast<int64_t>(QM_ROWS) * a.row_stride;
+    uint64_t* full = reinterpret_cast<uint64_t*>(ring + a.stages * tb);
+    uint64_t* xbar = full + QM_MAX_STAGES;
+    volatile int* abort = reinterpret_cast<volatile int*>(xbar + 1);
+    __shared__ float sxs[8 * QM_MAX_NT];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t xst = qm_x_stride(a.cols);
+
+    if (tid == 0) {
+        for (int i = 0; i < a.stages; ++i) mbar_init_cta(full + i, 1);
+        mbar_init_cta(xbar, 1);
+        *abort = 0;
+        mbar_init_fence();
+        for (int i = 0; i < a.stages; ++i) qm_issue(a, ring, full, blockIdx.x + i * gridDim.x, i);
+    }
+    // a programmatic dependent launch, as gemv_dot_kernel: only the weight
+    // copies come before the wait
+    pdl_trigger();
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (a.in_mode == 0 && tid == 0) {
+        // fp16 patterns of the codes: one bulk copy per token
+        mbar_expect_tx(xbar, static_cast<uint32_t>(a.g) * static_cast<uint32_t>(2 * a.cols));
+        for (int t = 0; t < a.g; ++t)
+            bulk_load_1d(xs + t * xst, a.xc + static_cast<int64_t>(t) * a.cols, static_cast<uint32_t>(2 * a.cols), xbar);
+    }
+    if (tid < a.g) sxs[tid] = a.sx[tid];
+    if (a.cs_state) {
+        const int64_t total = static_cast<int64_t>(a.cs_n) * a.cs_c_conv;
+        for (int64_t i = static_cast<int64_t>(blockIdx.x) * QM_THREADS + tid; i < total;
+             i += static_cast<int64_t>(gridDim.x) * QM_THREADS) {
+            const int64_t sq = i / a.cs_c_conv, c = i - sq * a.cs_c_conv;
+            float* t3 = a.cs_state + i * 3;
+            const float x1 = t3[1], x2 = t3[2];
+            t3[0] = x1;
+            t3[1] = x2;
+            t3[2] = bf16_bits_to_float(a.cs_qkvz[sq * a.cs_ld + c]);
+        }
+    }
+    if (a.in_mode == 1) {
+        // packed int8 codes to fp16: byte x + 128 under the pattern 0x64nn is
+        // 1024 + x + 128, less 1152 exactly
+        const int k16 = a.cols >> 4;
+        const __half2 off = __float2half2_rn(1152.0f);
+        for (int i = tid; i < a.g * k16; i += QM_THREADS) {
+            const int t = i / k16, b = i - t * k16;
+            const uint4 w = __ldg(reinterpret_cast<const uint4*>(a.xpack + t * a.xpack_stride + 4 * b));
+            const uint32_t wv[4] = {w.x ^ 0x80808080u, w.y ^ 0x80808080u, w.z ^ 0x80808080u, w.w ^ 0x80808080u};
+            uint32_t h[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                h[2 * e] = h2_bits(__hsub2(bits_h2(bytes_magic_h2(wv[e], 0)), off));
+                h[2 * e + 1] = h2_bits(__hsub2(bits_h2(bytes_magic_h2(wv[e], 1)), off));
+            }
+            uint4* dst = reinterpret_cast<uint4*>(xs + t * xst + 32 * b);
+            dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
+            dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
+        }
+    }
+    __syncthreads();
+    if (a.in_mode == 0) gemv_wait(xbar, 0, abort);
+
+    const int nsb = a.cols >> 8;
+    const int gq = lane >> 2, q = lane & 3;
+    const __half2 sixteenth = __float2half2_rn(0.0625f), m1024 = __float2half2_rn(-1024.0f);
+    int it = 0;
+    for (int tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x, ++it) {
+        const int s = it % a.stages;
+        const bool ok = gemv_wait(full + s, (it / a.stages) & 1, abort);
+        float y[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) y[nt][0] = y[nt][1] = y[nt][2] = y[nt][3] = 0.0f;
+        if (ok) {
+            const unsigned char* r0 = ring + s * tb + gq * a.row_stride;     // rows gq and gq + 8 of the tile
+            const unsigned char* r1 = r0 + 8 * a.row_stride;
+#pragma unroll 1
+            for (int i = warp; i < nsb; i += QM_WARPS) {
+                const unsigned char* p0 = r0 + i * 144;
+                const unsigned char* p1 = r1 + i * 144;
+                const uint4 h0 = *reinterpret_cast<const uint4*>(p0);
+                const uint4 h1 = *reinterpret_cast<const uint4*>(p1);
+                uint32_t sl0, sh0, ml0, mh0, sl1, sh1, ml1, mh1;
+                q4k_unpack_scales(h0, sl0, sh0, ml0, mh0);
+                q4k_unpack_scales(h1, sl1, sh1, ml1, mh1);
+                // sums of sc_j q_k x_k and m_j x_k over the superblock, each
+                // split over the two k16 steps of a sub-block (shorter chains)
+                float sa[NT][4], sb[NT][4], ma[NT][4], mb[NT][4];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) sa[nt][c] = sb[nt][c] = ma[nt][c] = mb[nt][c] = 0.0f;
+                const unsigned char* xb = xs + gq * xst + 16 * q + 512 * i;
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    // code bytes 32p + 8q .. +7 of both rows: sub-block 2p in
+                    // the low nibbles, 2p + 1 in the high ones (as 16 q)
+                    const uint2 c0 = *reinterpret_cast<const uint2*>(p0 + 16 + 32 * p + 8 * q);
+                    const uint2 c1 = *reinterpret_cast<const uint2*>(p1 + 16 + 32 * p + 8 * q);
+#pragma unroll
+                    for (int hn = 0; hn < 2; ++hn) {
+                        const int j = 2 * p + hn, k = j & 3;
+                        const uint32_t msk = hn ? 0xf0f0f0f0u : 0x0f0f0f0fu;
+                        __half2 s0 = byte_h2(j < 4 ? sl0 : sh0, k), s1 = byte_h2(j < 4 ? sl1 : sh1, k);
+                        if (hn) {
+                            s0 = __hmul2(s0, sixteenth);
+                            s1 = __hmul2(s1, sixteenth);
+                        }
+                        const __half2 n0 = __hmul2(s0, m1024), n1 = __hmul2(s1, m1024);
+                        // (1024 + q) s - 1024 s = q s, one rounding of an exact value
+                        const uint32_t u0x = c0.x & msk, u0y = c0.y & msk, u1x = c1.x & msk, u1y = c1.y & msk;
+                        const uint32_t a00 = h2_bits(__hfma2(bits_h2(bytes_magic_h2(u0x, 0)), s0, n0));
+                        const uint32_t a02 = h2_bits(__hfma2(bits_h2(bytes_magic_h2(u0x, 1)), s0, n0));
+                        const uint32_t a01 = h2_bits(__hfma2(bits_h2(bytes_magic_h2(u1x, 0)), s1, n1));
+                        const uint32_t a03 = h2_bits(__hfma2(bits_h2(bytes_magic_h2(u1x, 1)), s1, n1));
+                        const uint32_t a10 = h2_bits(__hfma2(bits_h2(bytes_magic_h2(u0y, 0)), s0, n0));
+                        const uint32_t a12 = h2_bits(__hfma2(bits_h2(bytes_magic_h2(u0y, 1)), s0, n0));
+                        const uint32_t a11 = h2_bits(__hfma2(bits_h2(bytes_magic_h2(u1y, 0)), s1, n1));
+                        const uint32_t a13 = h2_bits(__hfma2(bits_h2(bytes_magic_h2(u1y, 1)), s1, n1));
+                        const uint32_t m0 = h2_bits(byte_h2(j < 4 ? ml0 : mh0, k));
+                        const uint32_t m1 = h2_bits(byte_h2(j < 4 ? ml1 : mh1, k));
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            const uint4 xv = *reinterpret_cast<const uint4*>(xb + nt * 8 * xst + 64 * j);
+                            mma_f16_m16n8k16(sa[nt], a00, a01, a02, a03, xv.x, xv.y);
+                            mma_f16_m16n8k16(sb[nt], a10, a11, a12, a13, xv.z, xv.w);
+                            mma_f16_m16n8k16(ma[nt], m0, m1, m0, m1, xv.x, xv.y);
+                            mma_f16_m16n8k16(mb[nt], m0, m1, m0, m1, xv.z, xv.w);
+                        }
+                    }
+                }
+                const float d0 = __half2float(__ushort_as_half(static_cast<uint16_t>(h0.x & 0xffffu)));
+                const float e0 = -__half2float(__ushort_as_half(static_cast<uint16_t>(h0.x >> 16)));
+                const float d1 = __half2float(__ushort_as_half(static_cast<uint16_t>(h1.x & 0xffffu)));
+                const float e1 = -__half2float(__ushort_as_half(static_cast<uint16_t>(h1.x >> 16)));
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const float d = c < 2 ? d0 : d1, e = c < 2 ? e0 : e1;
+                        y[nt][c] = fmaf(e, ma[nt][c] + mb[nt][c], fmaf(d, sa[nt][c] + sb[nt][c], y[nt][c]));
+                    }
+            }
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) red[(warp * NT + nt) * 32 + lane] = make_float4(y[nt][0], y[nt][1], y[nt][2], y[nt][3]);
+        __syncthreads();   // every warp is done with stage s, and its partial sums are in place
+        if (*abort) break;
+        if (tid == 0) {
+            fence_proxy_async_smem();
+            qm_issue(a, ring, full, tile + a.stages * gridDim.x, s);
+        }
+        // output (row r, token t) sums the warps' partials in warp order;
+        // lane (r % 8) * 4 + (t % 8) / 2 of each warp holds it in component
+        // (r / 8) * 2 + t % 2 of its float4 for the token group t / 8
+        const float* redf = reinterpret_cast<const float*>(red);
+        for (int o = tid; o < QM_ROWS * 8 * NT; o += QM_THREADS) {
+            const int r = o & (QM_ROWS - 1), t = o / QM_ROWS;
+            const int row = tile * QM_ROWS + r;
+            if (t < a.g && row < a.rows) {
+                const int nt = t >> 3, tt = t & 7;
+                const int li = (r & 7) * 4 + (tt >> 1), c = (r >> 3) * 2 + (tt & 1);
+                float v = 0.0f;
+#pragma unroll
+                for (int w = 0; w < QM_WARPS; ++w) v += redf[((w * NT + nt) * 32 + li) * 4 + c];
+                const float yv = v * sxs[t];
+                if (row < a.n_bf16)
+                    a.out_bf16[t * a.ld_bf16 + row] = float_to_bf16_bits(yv);
+                else
+                    a.out_f32[t * a.ld_f32 + (row - a.n_bf16)] = yv;
+            }
+        }
+        __syncthreads();   // the partial sums are read
+    }
+    if (*abort && tid == 0) {
+        // a wait ran out: let copies already issued land (bounded) before the
+        // shared memory is released
+        if (a.in_mode == 0) mbar_wait_bounded(xbar, 0, nullptr, 0, 20000000ull);
+        for (int i = 0; i < a.stages; ++i)
+            for (uint32_t par = 0; par < 2; ++par) mbar_wait_bounded(full + i, par, nullptr, 0, 20000000ull);
+    }
+}
+
+template <int NT>
+static cudaError_t qm_launch_nt(unsigned grid, size_t smem, cudaStream_t st, const QmArgs& a) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(QM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at;
+    at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemv_q4k_mma_kernel<NT>, a);
+}
+
+// The Q4_K projection on gemv_q4k_mma_kernel: launches of up to 16 tokens
+// (fewer when their codes and two stages would not fit shared memory),
+// QM_CTAS_PER_SM CTAs per SM, as many stages as fit up to the tiles a CTA
+// walks.  Returns false, launching nothing, when
+// not even 8 tokens' codes and two stages fit (very long rows).
+static bool launch_gemv_q4k_mma(const void* blocks, int64_t rows, int64_t cols, const uint16_t* xc,
+                                const uint32_t* xpack, int64_t xpack_stride, const float* sx, int64_t n,
+                                uint16_t* out_bf16, int64_t ld_bf16, int64_t n_bf16, float* out_f32, int64_t ld_f32,
+                                cudaStream_t st, float* cs_state, const uint16_t* cs_qkvz, int64_t cs_ld,
+                                int cs_c_conv, int cs_n, cudaError_t& err) {
+    static int sms = 0, budget = 0;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        int dev = 0, optin = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaFuncAttributes fa{};
+        cudaFuncGetAttributes(&fa, gemv_q4k_mma_kernel<QM_MAX_NT>);
+        const int stat = static_cast<int>(fa.sharedSizeBytes);
+        const int per_cta = GEMV_SM_SMEM / QM_CTAS_PER_SM - 1024 - stat;
+        budget = optin - stat < per_cta ? optin - stat : per_cta;
+        cudaFuncSetAttribute(gemv_q4k_mma_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, budget);
+        cudaFuncSetAttribute(gemv_q4k_mma_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, budget);
+    });
+    const int64_t row_bytes = (cols / 256) * 144;
+    const int c = static_cast<int>(cols);
+    if (qm_smem_bytes(1, c, row_bytes, 2) > budget) return false;
+    int ntmax = QM_MAX_NT;
+    while (ntmax > 1 && qm_smem_bytes(ntmax, c, row_bytes, 2) > budget) ntmax /= 2;
+    const int ntiles = static_cast<int>((rows + QM_ROWS - 1) / QM_ROWS);
+    const int ctas = QM_CTAS_PER_SM * sms;
+    const unsigned grid = static_cast<unsigned>(ntiles < ctas ? ntiles : ctas);
+    const int walk = (ntiles + static_cast<int>(grid) - 1) / static_cast<int>(grid);   // tiles of the busiest CTA
+    err = cudaSuccess;
+    for (int64_t t0 = 0; t0 < n; t0 += 8 * ntmax) {
+        QmArgs a;
+        a.blocks = static_cast<const uint8_t*>(blocks);
+        a.rows = static_cast<int>(rows);
+        a.cols = c;
+        a.row_bytes = row_bytes;
+        a.row_stride = qm_row_stride(row_bytes);
+        a.ntiles = ntiles;
+        a.in_mode = xpack ? 1 : 0;
+        a.xc = xc ? xc + t0 * cols : nullptr;
+        a.xpack = xpack ? xpack + t0 * xpack_stride : nullptr;
+        a.xpack_stride = xpack_stride;
+        a.sx = sx + t0;
+        a.g = static_cast<int>(n - t0 < 8 * ntmax ? n - t0 : 8 * ntmax);
+        a.out_bf16 = out_bf16 ? out_bf16 + t0 * ld_bf16 : nullptr;
+        a.ld_bf16 = ld_bf16;
+        a.n_bf16 = static_cast<int>(n_bf16);
+        a.out_f32 = out_f32 ? out_f32 + t0 * ld_f32 : nullptr;
+        a.ld_f32 = ld_f32;
+        a.cs_state = t0 == 0 ? cs_state : nullptr;
+        a.cs_qkvz = cs_qkvz;
+        a.cs_ld = cs_ld;
+        a.cs_c_conv = cs_c_conv;
+        a.cs_n = cs_n;
+        const int nt = a.g <= 8 ? 1 : 2;
+        // no more stages than the busiest CTA has tiles: a small matrix
+        // leaves the SMs' shared memory to the kernels beside it
+        int stages = walk < QM_MAX_STAGES ? walk : QM_MAX_STAGES;
+        while (stages > 1 && qm_smem_bytes(nt, c, row_bytes, stages) > budget) --stages;
+        a.stages = stages;
+        const size_t smem = static_cast<size_t>(qm_smem_bytes(nt, c, row_bytes, stages));
+        err = nt == 1 ? qm_launch_nt<1>(grid, smem, st, a) : qm_launch_nt<2>(grid, smem, st, a);
+        if (err == cudaSuccess) err = cudaGetLastError();
+        if (err != cudaSuccess) return true;
+    }
+    return true;
+}
+
 // out[t][r] = s_x[t] * sum_k x[t][k] W[r][k] (W exactly decoded), for n tokens
 // in launches of at most GEMV_TOKENS (fewer when a token's codes and the
 // tiles would not fit shared memory); W in Q4_K (q6k false) or Q6_K.  The
@@ -415,6 +819,12 @@ cudaError_t launch_gemv_dot(const void* blocks, bool q6k, int64_t rows, int64_t 
         gemv_set_smem<true>(max_optin);
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     });
+    if (!q6k) {
+        cudaError_t e = cudaSuccess;
+        if (launch_gemv_q4k_mma(blocks, rows, cols, xc, xpack, xpack_stride, sx, n, out_bf16, ld_bf16, n_bf16, out_f32,
+                                ld_f32, st, cs_state, cs_qkvz, cs_ld, cs_c_conv, cs_n, e))
+            return e;
+    }
     const int64_t row_bytes = (cols / 256) * (q6k ? 210 : 144);
     // tokens per launch (a power of two): what fits beside one stage
     int64_t gmax = GEMV_TOKENS;

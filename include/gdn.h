@@ -66,7 +66,7 @@ extern "C" {
 
 #define GDN_CHUNK 64 /* tokens per chunk of the chunked delta rule */
 #define GDN_MAX_SEQS 256 /* sequences per gdn_prefill_batch or gdn_decode call */
-#define GDN_DECODE_GEMV_TOKENS 8 /* tokens per launch of the decode step's fused weight-decode GEMV */
+#define GDN_DECODE_GEMV_TOKENS 8 /* tokens per launch of the decode step's fused weight-decode GEMV (dp4a form; the Q4_K tensor-core form takes twice as many) */
 
 /*
  * One GDN layer.  Sizes: Hk = n_qk_heads, Hv = n_v_heads (a multiple of Hk,
@@ -250,7 +250,8 @@ int gdn_decode(const gdn_layer *layer, const void *x, int n_seqs, float *state, 
  * out[t][r] = sx[t] * sum_k xc[t][k] * W[r][k], W the exactly decoded Q4_K
  * (q6k = 0) or Q6_K (q6k = 1) rows [rows][cols/256 blocks] (16-byte aligned),
  * xc the int8 codes of n tokens as fp16 patterns [n][cols] (16-byte aligned),
- * sx [n]; integer dot products per weight sub-block, fp32 sums.  Rows r <
+ * sx [n]; integer dot products per weight sub-block, fp32 sums; a token's
+ * result does not depend on n or on the other tokens, bit for bit.  Rows r <
  * n_bf16 go to out_bf16[t*ld_bf16 + r] (bf16), the others to out_f32[t*ld_f32 +
  * r - n_bf16].  256 <= cols <= 16384, cols % 256 == 0, 1 <= n <= GDN_MAX_SEQS.
  */

@@ -224,3 +224,30 @@ def test_decode_at_the_maximum_number_of_sequences():
         c = conv[s].cpu().numpy()
         assert np.array_equal(c[:, :2], cv0[s][:, 1:]), s
         assert _tail_close(c[:, 2], ref["conv_tail"][:, 2]), s
+
+
+@pytest.mark.parametrize("fmt", ["q4k", "q6k"])
+def test_decode_gemv_token_result_independent_of_the_batch(L, fmt):
+    """21 tokens in one call (launches of 16 + 5 tokens, or 8 + 8 + 5) give,
+    bit for bit, what each token gives alone."""
+    rng = np.random.default_rng(21)
+    rows, cols, n = 500, 2048, 21
+    w = rng.normal(0, 0.02, size=(rows, cols)).astype(np.float32)
+    blocks = (q6k.pack_q6k if fmt == "q6k" else q4k.pack_q4k)(w)
+    x = (rng.normal(0, 1, size=(n, cols)) * 10.0 ** rng.uniform(-2, 2, size=(n, 1))).astype(np.float32)
+    qx, sx = quant.quant_rows_i8(x)
+    xc = torch.from_numpy(qx.astype(np.float16)).to(DEV)
+    sxd = f32_dev(sx)
+    b = torch.from_numpy(blocks).to(DEV)
+    ob = torch.zeros(1, dtype=torch.int16, device=DEV)
+
+    def run(t0, t1):
+        of = torch.zeros(t1 - t0, rows, dtype=torch.float32, device=DEV)
+        L.gdn_decode_gemv(gl.ptr(b), int(fmt == "q6k"), rows, cols, gl.ptr(xc[t0:t1]), gl.ptr(sxd[t0:t1]), t1 - t0,
+                          gl.ptr(ob), 1, 0, gl.ptr(of), rows, stream())
+        sync(L)
+        return of
+
+    together = run(0, n)
+    for t in range(n):
+        assert torch.equal(run(t, t + 1)[0], together[t]), t
