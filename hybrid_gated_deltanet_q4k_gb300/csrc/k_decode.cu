@@ -173,6 +173,84 @@ __device__ __forceinline__ void span_codes(const uint8_t* blk, int j, uint32_t (
     }
 }
 
+// The 6-bit scales and mins of a Q4_K superblock's 8 sub-blocks, one per
+// byte: sl = sc[0..3], sh = sc[4..7], ml = m[0..3], mh = m[4..7] (sub-blocks
+// 4..7 take their two high bits from the top bits of the bytes of 0..3).
+__device__ __forceinline__ void q4k_unpack_scales(const uint4& h, uint32_t& sl, uint32_t& sh, uint32_t& ml,
+                                                  uint32_t& mh) {
+    sl = h.y & 0x3f3f3f3fu;
+    ml = h.z & 0x3f3f3f3fu;
+    sh = (h.w & 0x0f0f0f0fu) | ((h.y >> 2) & 0x30303030u);
+    mh = ((h.w >> 4) & 0x0f0f0f0fu) | ((h.z >> 2) & 0x30303030u);
+}
+
+// One token's sum over a Q4_K row in the fp32 operations of
+// gemv_q4k_mma_kernel, so that a token decodes bit for bit the same alone as
+// in a batch.  Per superblock i, the exact integer sums S = sum_j sc_j D_j and
+// M = sum_j m_j X_j (D_j the sub-block's code-token dot product, X_j its token
+// sum), then y_w = fma(-dmin, M, fma(d, S, y_w)) for the slice w = i mod 8,
+// superblocks in increasing order; the eight slices are summed in order.  That
+// kernel rounds the sum of S's two exact halves once, which is the conversion
+// of the exact integer here.  Lane (sbl, j) takes sub-block j of superblocks
+// sbl, sbl + 4, ...: slice sbl (ya) and slice sbl + 4 (yb).  Odd sub-blocks
+// keep their codes at 16 q and even ones take 16 sc, so S arrives 16 times too
+// large and d / 16 (exact) undoes it inside the same fma.
+__device__ __forceinline__ float q4k_token_sum_mma_order(const uint8_t* rb, const uint32_t* xs, const int* xsum,
+                                                         int nsb, int lane) {
+    const int j = lane & 7, sbl = lane >> 3, k = j & 3;
+    const uint32_t mask = (j & 1) ? 0xf0f0f0f0u : 0x0f0f0f0fu;
+    float ya = 0.0f, yb = 0.0f;
+    const int nst = (nsb + 3) >> 2;
+#pragma unroll 4
+    for (int st = 0; st < nst; ++st) {
+        const int i = sbl + 4 * st;
+        int S = 0, M = 0;
+        float d16 = 0.0f, e = 0.0f;
+        if (i < nsb) {
+            const uint8_t* blk = rb + i * 144;
+            const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
+            uint32_t sl, sh, ml, mh;
+            q4k_unpack_scales(hdr, sl, sh, ml, mh);
+            const int sc = static_cast<int>(__byte_perm(j < 4 ? sl : sh, 0u, 0x4440 + k));
+            const int m = static_cast<int>(__byte_perm(j < 4 ? ml : mh, 0u, 0x4440 + k));
+            const uint4* q = reinterpret_cast<const uint4*>(blk + 16 + 32 * (j >> 1));
+            const uint4 qa = q[0], qb = q[1];
+            const int w0 = 64 * i + 8 * j;
+            const uint4 xa = *reinterpret_cast<const uint4*>(xs + w0);
+            const uint4 xb = *reinterpret_cast<const uint4*>(xs + w0 + 4);
+            const int2 xm = *reinterpret_cast<const int2*>(xsum + 16 * i + 2 * j);
+            int D = dp4a_us(qa.x & mask, xa.x, 0);
+            D = dp4a_us(qa.y & mask, xa.y, D);
+            D = dp4a_us(qa.z & mask, xa.z, D);
+            D = dp4a_us(qa.w & mask, xa.w, D);
+            D = dp4a_us(qb.x & mask, xb.x, D);
+            D = dp4a_us(qb.y & mask, xb.y, D);
+            D = dp4a_us(qb.z & mask, xb.z, D);
+            D = dp4a_us(qb.w & mask, xb.w, D);
+            S = ((j & 1) ? sc : (sc << 4)) * D;
+            M = m * (xm.x + xm.y);
+            d16 = __fmul_rn(__half2float(__ushort_as_half(static_cast<uint16_t>(hdr.x & 0xffffu))), 0.0625f);
+            e = -__half2float(__ushort_as_half(static_cast<uint16_t>(hdr.x >> 16)));
+        }
+        S += __shfl_xor_sync(0xffffffffu, S, 1);
+        S += __shfl_xor_sync(0xffffffffu, S, 2);
+        S += __shfl_xor_sync(0xffffffffu, S, 4);
+        M += __shfl_xor_sync(0xffffffffu, M, 1);
+        M += __shfl_xor_sync(0xffffffffu, M, 2);
+        M += __shfl_xor_sync(0xffffffffu, M, 4);
+        if (i < nsb) {
+            if (st & 1)
+                yb = fmaf(e, static_cast<float>(M), fmaf(d16, static_cast<float>(S), yb));
+            else
+                ya = fmaf(e, static_cast<float>(M), fmaf(d16, static_cast<float>(S), ya));
+        }
+    }
+    float v = 0.0f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) v += __shfl_sync(0xffffffffu, w < 4 ? ya : yb, (w & 3) * 8);
+    return v;
+}
+
 // Bounded wait of one warp on a stage: gives up at once after any earlier
 // wait of the CTA ran out.
 __device__ __forceinline__ bool gemv_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
@@ -184,8 +262,10 @@ __device__ __forceinline__ bool gemv_wait(uint64_t* bar, uint32_t parity, volati
 
 // G: tokens the kernel computes (a power of two >= a.g; the codes of tokens
 // a.g .. G-1 are zero and their sums are not stored).
-template <bool Q6, int G>
+// MC (Q4_K, one token): the sums in the fp32 operations of gemv_q4k_mma_kernel.
+template <bool Q6, int G, bool MC = false>
 __global__ void __launch_bounds__(GEMV_THREADS, G <= 2 ? 4 : 2) gemv_dot_kernel(GemvArgs a) {
+    static_assert(!MC || (!Q6 && G == 1), "the tensor-core order is for one token of Q4_K rows");
     constexpr int BYTES = Q6 ? 210 : 144;
     extern __shared__ __align__(128) unsigned char gsm[];
     uint32_t* xs = reinterpret_cast<uint32_t*>(gsm);                 // [G][cols / 4] packed int8
@@ -281,50 +361,54 @@ __global__ void __launch_bounds__(GEMV_THREADS, G <= 2 ? 4 : 2) gemv_dot_kernel(
         const int row = tile * GEMV_WARPS + warp;
         if (row < a.rows) {
             const uint8_t* rb = ring + s * tb + static_cast<int64_t>(warp) * a.row_bytes;
-            float acc[G];
+            float mine = 0.0f;
+            if constexpr (MC) {
+                mine = q4k_token_sum_mma_order(rb, xs, xsum, nsb, lane);
+            } else {
+                float acc[G];
 #pragma unroll
-            for (int t = 0; t < G; ++t) acc[t] = 0.0f;
+                for (int t = 0; t < G; ++t) acc[t] = 0.0f;
 #pragma unroll 4
-            for (int i = sbl; i < nsb; i += 4) {
-                uint32_t c[8];
-                float mul0, mul1, add0, add1;
-                span_codes<Q6>(rb + i * BYTES, j, c, mul0, mul1, add0, add1);
-                const int w0 = 64 * i + 8 * j;           // first x word of the span (256 i + 32 j bytes)
+                for (int i = sbl; i < nsb; i += 4) {
+                    uint32_t c[8];
+                    float mul0, mul1, add0, add1;
+                    span_codes<Q6>(rb + i * BYTES, j, c, mul0, mul1, add0, add1);
+                    const int w0 = 64 * i + 8 * j;           // first x word of the span (256 i + 32 j bytes)
 #pragma unroll
-                for (int t = 0; t < G; ++t) {
-                    const uint4 xa = *reinterpret_cast<const uint4*>(xs + t * kw + w0);
-                    const uint4 xb = *reinterpret_cast<const uint4*>(xs + t * kw + w0 + 4);
-                    const int2 sx = *reinterpret_cast<const int2*>(xsum + t * k16 + 16 * i + 2 * j);
-                    if constexpr (!Q6) {
-                        // one scale for the 32 weights: one dot product
-                        int d = dp4a_us(c[0], xa.x, 0);
-                        d = dp4a_us(c[1], xa.y, d);
-                        d = dp4a_us(c[2], xa.z, d);
-                        d = dp4a_us(c[3], xa.w, d);
-                        d = dp4a_us(c[4], xb.x, d);
-                        d = dp4a_us(c[5], xb.y, d);
-                        d = dp4a_us(c[6], xb.z, d);
-                        d = dp4a_us(c[7], xb.w, d);
-                        acc[t] = fmaf(mul0, static_cast<float>(d), fmaf(add0, static_cast<float>(sx.x + sx.y), acc[t]));
-                    } else {
-                        int d0 = dp4a_us(c[0], xa.x, 0);
-                        d0 = dp4a_us(c[1], xa.y, d0);
-                        d0 = dp4a_us(c[2], xa.z, d0);
-                        d0 = dp4a_us(c[3], xa.w, d0);
-                        int d1 = dp4a_us(c[4], xb.x, 0);
-                        d1 = dp4a_us(c[5], xb.y, d1);
-                        d1 = dp4a_us(c[6], xb.z, d1);
-                        d1 = dp4a_us(c[7], xb.w, d1);
-                        const float r = fmaf(mul0, static_cast<float>(d0), fmaf(add0, static_cast<float>(sx.x), acc[t]));
-                        acc[t] = fmaf(mul1, static_cast<float>(d1), fmaf(add1, static_cast<float>(sx.y), r));
+                    for (int t = 0; t < G; ++t) {
+                        const uint4 xa = *reinterpret_cast<const uint4*>(xs + t * kw + w0);
+                        const uint4 xb = *reinterpret_cast<const uint4*>(xs + t * kw + w0 + 4);
+                        const int2 sx = *reinterpret_cast<const int2*>(xsum + t * k16 + 16 * i + 2 * j);
+                        if constexpr (!Q6) {
+                            // one scale for the 32 weights: one dot product
+                            int d = dp4a_us(c[0], xa.x, 0);
+                            d = dp4a_us(c[1], xa.y, d);
+                            d = dp4a_us(c[2], xa.z, d);
+                            d = dp4a_us(c[3], xa.w, d);
+                            d = dp4a_us(c[4], xb.x, d);
+                            d = dp4a_us(c[5], xb.y, d);
+                            d = dp4a_us(c[6], xb.z, d);
+                            d = dp4a_us(c[7], xb.w, d);
+                            acc[t] = fmaf(mul0, static_cast<float>(d), fmaf(add0, static_cast<float>(sx.x + sx.y), acc[t]));
+                        } else {
+                            int d0 = dp4a_us(c[0], xa.x, 0);
+                            d0 = dp4a_us(c[1], xa.y, d0);
+                            d0 = dp4a_us(c[2], xa.z, d0);
+                            d0 = dp4a_us(c[3], xa.w, d0);
+                            int d1 = dp4a_us(c[4], xb.x, 0);
+                            d1 = dp4a_us(c[5], xb.y, d1);
+                            d1 = dp4a_us(c[6], xb.z, d1);
+                            d1 = dp4a_us(c[7], xb.w, d1);
+                            const float r = fmaf(mul0, static_cast<float>(d0), fmaf(add0, static_cast<float>(sx.x), acc[t]));
+                            acc[t] = fmaf(mul1, static_cast<float>(d1), fmaf(add1, static_cast<float>(sx.y), r));
+                        }
                     }
                 }
-            }
-            float mine = 0.0f;
 #pragma unroll
-            for (int t = 0; t < G; ++t) {
-                const float sum = warp_sum(acc[t]);
-                if (lane == t) mine = sum;
+                for (int t = 0; t < G; ++t) {
+                    const float sum = warp_sum(acc[t]);
+                    if (lane == t) mine = sum;
+                }
             }
             if (lane < a.g) {
                 const float y = mine * sxs[lane];
@@ -361,12 +445,14 @@ static void gemv_set_smem(int bytes) {
     cudaFuncSetAttribute(gemv_dot_kernel<Q6, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     cudaFuncSetAttribute(gemv_dot_kernel<Q6, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     cudaFuncSetAttribute(gemv_dot_kernel<Q6, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if constexpr (!Q6)
+        cudaFuncSetAttribute(gemv_dot_kernel<false, 1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
 // A programmatic dependent launch: the CTAs may start while the previous
 // kernel in the stream finishes (it signals when; see griddepcontrol in the
 // kernel), so the weight copies start before the inputs exist.
-template <bool Q6, int G>
+template <bool Q6, int G, bool MC = false>
 static cudaError_t gemv_launch_g(unsigned grid, size_t smem, cudaStream_t st, const GemvArgs& a) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
@@ -378,11 +464,13 @@ static cudaError_t gemv_launch_g(unsigned grid, size_t smem, cudaStream_t st, co
     at.val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = &at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemv_dot_kernel<Q6, G>, a);
+    return cudaLaunchKernelEx(&cfg, gemv_dot_kernel<Q6, G, MC>, a);
 }
 
 template <bool Q6>
-static cudaError_t gemv_launch(int G, unsigned grid, size_t smem, cudaStream_t st, const GemvArgs& a) {
+static cudaError_t gemv_launch(int G, bool mc, unsigned grid, size_t smem, cudaStream_t st, const GemvArgs& a) {
+    if constexpr (!Q6)
+        if (G == 1 && mc) return gemv_launch_g<false, 1, true>(grid, smem, st, a);
     if (G == 1) return gemv_launch_g<Q6, 1>(grid, smem, st, a);
     if (G == 2) return gemv_launch_g<Q6, 2>(grid, smem, st, a);
     if (G == 4) return gemv_launch_g<Q6, 4>(grid, smem, st, a);
@@ -420,6 +508,7 @@ static cudaError_t gemv_launch(int G, unsigned grid, size_t smem, cudaStream_t s
 // requested before the dependency wait.  Up to 16 tokens per launch (NT
 // groups of 8), so the weights are read once for all of them.
 constexpr int QM_WARPS = 8;
+static_assert(QM_WARPS == 8, "q4k_token_sum_mma_order sums eight superblock slices, one per warp here");
 constexpr int QM_THREADS = QM_WARPS * 32;
 constexpr int QM_ROWS = 16;
 constexpr int QM_MAX_STAGES = 6;
@@ -503,17 +592,6 @@ __device__ __forceinline__ __half2 byte_h2(uint32_t w, int k) {
 // Bytes (0, 1) or (2, 3) of w as the fp16 pair (1024 + b0, 1024 + b1).
 __device__ __forceinline__ uint32_t bytes_magic_h2(uint32_t w, int hi) {
     return __byte_perm(w, 0x64646464u, hi ? 0x7362u : 0x5140u);
-}
-
-// The 6-bit scales and mins of a Q4_K superblock's 8 sub-blocks, one per
-// byte: sl = sc[0..3], sh = sc[4..7], ml = m[0..3], mh = m[4..7] (sub-blocks
-// 4..7 take their two high bits from the top bits of the bytes of 0..3).
-__device__ __forceinline__ void q4k_unpack_scales(const uint4& h, uint32_t& sl, uint32_t& sh, uint32_t& ml,
-                                                  uint32_t& mh) {
-    sl = h.y & 0x3f3f3f3fu;
-    ml = h.z & 0x3f3f3f3fu;
-    sh = (h.w & 0x0f0f0f0fu) | ((h.y >> 2) & 0x30303030u);
-    mh = ((h.w >> 4) & 0x0f0f0f0fu) | ((h.z >> 2) & 0x30303030u);
 }
 
 template <int NT>
@@ -721,31 +799,41 @@ static cudaError_t qm_launch_nt(unsigned grid, size_t smem, cudaStream_t st, con
 // The Q4_K projection on gemv_q4k_mma_kernel: launches of up to 16 tokens
 // (fewer when their codes and two stages would not fit shared memory),
 // QM_CTAS_PER_SM CTAs per SM, as many stages as fit up to the tiles a CTA
-// walks.  Returns false, launching nothing, when
-// not even 8 tokens' codes and two stages fit (very long rows).
-static bool launch_gemv_q4k_mma(const void* blocks, int64_t rows, int64_t cols, const uint16_t* xc,
-                                const uint32_t* xpack, int64_t xpack_stride, const float* sx, int64_t n,
-                                uint16_t* out_bf16, int64_t ld_bf16, int64_t n_bf16, float* out_f32, int64_t ld_f32,
-                                cudaStream_t st, float* cs_state, const uint16_t* cs_qkvz, int64_t cs_ld,
-                                int cs_c_conv, int cs_n, cudaError_t& err) {
-    static int sms = 0, budget = 0;
+// walks.  Only for rows where qm_fits holds.
+static int qm_sms = 0, qm_budget = 0;
+static void qm_init() {
     static std::once_flag once;
     std::call_once(once, [] {
         int dev = 0, optin = 0;
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaDeviceGetAttribute(&qm_sms, cudaDevAttrMultiProcessorCount, dev);
         cudaFuncAttributes fa{};
         cudaFuncGetAttributes(&fa, gemv_q4k_mma_kernel<QM_MAX_NT>);
         const int stat = static_cast<int>(fa.sharedSizeBytes);
         const int per_cta = GEMV_SM_SMEM / QM_CTAS_PER_SM - 1024 - stat;
-        budget = optin - stat < per_cta ? optin - stat : per_cta;
-        cudaFuncSetAttribute(gemv_q4k_mma_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, budget);
-        cudaFuncSetAttribute(gemv_q4k_mma_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, budget);
+        qm_budget = optin - stat < per_cta ? optin - stat : per_cta;
+        cudaFuncSetAttribute(gemv_q4k_mma_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, qm_budget);
+        cudaFuncSetAttribute(gemv_q4k_mma_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, qm_budget);
     });
+}
+
+// Whether Q4_K rows of `cols` weights take the tensor-core form: 8 tokens'
+// codes and two stages fit shared memory.
+static bool qm_fits(int64_t cols) {
+    qm_init();
+    return qm_smem_bytes(1, static_cast<int>(cols), (cols / 256) * 144, 2) <= qm_budget;
+}
+
+static void launch_gemv_q4k_mma(const void* blocks, int64_t rows, int64_t cols, const uint16_t* xc,
+                                const uint32_t* xpack, int64_t xpack_stride, const float* sx, int64_t n,
+                                uint16_t* out_bf16, int64_t ld_bf16, int64_t n_bf16, float* out_f32, int64_t ld_f32,
+                                cudaStream_t st, float* cs_state, const uint16_t* cs_qkvz, int64_t cs_ld,
+                                int cs_c_conv, int cs_n, cudaError_t& err) {
+    qm_init();
+    const int sms = qm_sms, budget = qm_budget;
     const int64_t row_bytes = (cols / 256) * 144;
     const int c = static_cast<int>(cols);
-    if (qm_smem_bytes(1, c, row_bytes, 2) > budget) return false;
     int ntmax = QM_MAX_NT;
     while (ntmax > 1 && qm_smem_bytes(ntmax, c, row_bytes, 2) > budget) ntmax /= 2;
     const int ntiles = static_cast<int>((rows + QM_ROWS - 1) / QM_ROWS);
@@ -786,9 +874,8 @@ static bool launch_gemv_q4k_mma(const void* blocks, int64_t rows, int64_t cols, 
         const size_t smem = static_cast<size_t>(qm_smem_bytes(nt, c, row_bytes, stages));
         err = nt == 1 ? qm_launch_nt<1>(grid, smem, st, a) : qm_launch_nt<2>(grid, smem, st, a);
         if (err == cudaSuccess) err = cudaGetLastError();
-        if (err != cudaSuccess) return true;
+        if (err != cudaSuccess) return;
     }
-    return true;
 }
 
 // out[t][r] = s_x[t] * sum_k x[t][k] W[r][k] (W exactly decoded), for n tokens
@@ -819,11 +906,15 @@ cudaError_t launch_gemv_dot(const void* blocks, bool q6k, int64_t rows, int64_t 
         gemv_set_smem<true>(max_optin);
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     });
-    if (!q6k) {
+    // Q4_K rows that fit the tensor-core form take it for several tokens; one
+    // token takes the dp4a kernel in the same fp32 operations (a token's
+    // result does not depend on the batch)
+    const bool mma_q4k = !q6k && qm_fits(cols);
+    if (mma_q4k && n > 1) {
         cudaError_t e = cudaSuccess;
-        if (launch_gemv_q4k_mma(blocks, rows, cols, xc, xpack, xpack_stride, sx, n, out_bf16, ld_bf16, n_bf16, out_f32,
-                                ld_f32, st, cs_state, cs_qkvz, cs_ld, cs_c_conv, cs_n, e))
-            return e;
+        launch_gemv_q4k_mma(blocks, rows, cols, xc, xpack, xpack_stride, sx, n, out_bf16, ld_bf16, n_bf16, out_f32,
+                            ld_f32, st, cs_state, cs_qkvz, cs_ld, cs_c_conv, cs_n, e);
+        return e;
     }
     const int64_t row_bytes = (cols / 256) * (q6k ? 210 : 144);
     // tokens per launch (a power of two): what fits beside one stage
@@ -872,7 +963,7 @@ cudaError_t launch_gemv_dot(const void* blocks, bool q6k, int64_t rows, int64_t 
         const size_t smem = static_cast<size_t>(gemv_smem_bytes(G, a.cols, row_bytes, stages));
         if (smem > static_cast<size_t>(max_optin)) return cudaErrorInvalidValue;
         const unsigned grid = static_cast<unsigned>(ntiles < per_sm * sms ? ntiles : per_sm * sms);
-        cudaError_t e = q6k ? gemv_launch<true>(G, grid, smem, st, a) : gemv_launch<false>(G, grid, smem, st, a);
+        cudaError_t e = q6k ? gemv_launch<true>(G, false, grid, smem, st, a) : gemv_launch<false>(G, mma_q4k, grid, smem, st, a);
         if (e == cudaSuccess) e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
