@@ -19,22 +19,18 @@
 
 namespace gdn {
 
-// Byte i (0..11) of the 12 Q4_K scale bytes, held in three little-endian words.
-__device__ __forceinline__ int scale_byte(uint32_t y, uint32_t z, uint32_t w, int i) {
-    const uint32_t word = i < 4 ? y : (i < 8 ? z : w);
-    return static_cast<int>((word >> (8 * (i & 3))) & 0xffu);
-}
-
-// 6-bit scale and min of Q4_K sub-block j.
+// 6-bit scale and min of Q4_K sub-block j from the 12 scale bytes, held in
+// three little-endian words y, z, w: sub-blocks 0..3 take the low six bits of
+// bytes j and j + 4; 4..7 take the nibbles of byte j + 4 and the top two bits
+// of bytes j - 4 and j.  Byte permutes pick byte j % 4 of each word, with no
+// branch on j.
 __device__ __forceinline__ void q4k_scale_min(uint32_t y, uint32_t z, uint32_t w, int j, int& sc, int& m) {
-    if (j < 4) {
-        sc = scale_byte(y, z, w, j) & 63;
-        m = scale_byte(y, z, w, j + 4) & 63;
-    } else {
-        const int hi = scale_byte(y, z, w, j + 4);
-        sc = (hi & 15) | ((scale_byte(y, z, w, j - 4) >> 6) << 4);
-        m = (hi >> 4) | ((scale_byte(y, z, w, j) >> 6) << 4);
-    }
+    const int k = j & 3;
+    const uint32_t yk = __byte_perm(y, 0u, 0x4440 + k), zk = __byte_perm(z, 0u, 0x4440 + k);
+    const uint32_t wk = __byte_perm(w, 0u, 0x4440 + k);
+    const bool lo = j < 4;
+    sc = static_cast<int>(lo ? (yk & 63u) : ((wk & 15u) | ((yk >> 2) & 0x30u)));
+    m = static_cast<int>(lo ? (zk & 63u) : ((wk >> 4) | ((zk >> 2) & 0x30u)));
 }
 
 // d*sc and dmin*m of Q4_K sub-block `sub` of a superblock header; both products
@@ -44,8 +40,8 @@ __device__ __forceinline__ void q4k_sub_affine(const uint4& hdr, int sub, float&
     const float dmin = __half2float(__ushort_as_half(static_cast<uint16_t>(hdr.x >> 16)));
     int sc, m;
     q4k_scale_min(hdr.y, hdr.z, hdr.w, sub, sc, m);
-    ds = __fmul_rn(d, static_cast<float>(sc));
-    dm = __fmul_rn(dmin, static_cast<float>(m));
+    ds = __fmul_rn(d, small_uint_to_float(static_cast<uint32_t>(sc)));
+    dm = __fmul_rn(dmin, small_uint_to_float(static_cast<uint32_t>(m)));
 }
 
 // Loads of the decoders: read-only global loads (G = true) or plain loads (G =
