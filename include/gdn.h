@@ -239,6 +239,10 @@ int gdn_prefill_batch(const gdn_layer *layer, const void *x, const int64_t *cu_s
  * before it ends (programmatic dependent launches: the projections' weight
  * copies begin before their inputs exist).  A decoded token therefore
  * agrees with a prefill of it within the stated tolerances, not bit for bit.
+ * A sequence's results do not depend on the other sequences of the call: a
+ * batch decodes each sequence bit for bit as that sequence alone (with Q4_K
+ * the several-token projections run on the tensor cores and one token on
+ * dp4a, in the same fp32 operations).
  * 1 <= n_seqs <= GDN_MAX_SEQS.
  */
 size_t gdn_decode_workspace_size(const gdn_layer *layer, int n_seqs);
