@@ -116,7 +116,7 @@ def test_batch_zero_state_and_tiny_f32_layer():
     a, b = cu[3], cu[4]
     ref = OL.layer_forward(p, tok["x"][a:b], gate_log_a=tok["log_a"][a:b], gate_b=tok["b"][a:b])
     assert rel_l2(yb[a:b].cpu().numpy(), ref["y"]) <= 1e-2
-    assert rel_l2(sb[3].cpu().numpy(), ref["state"]) <= 1e-2
+    assert rel_l2(sb[3].cpu().numpy(), ref["state"]) <= 2e-3   # recurrence tolerance
 
 
 def test_batch_session_extend_4b_layer():
@@ -151,7 +151,7 @@ def test_batch_session_extend_4b_layer():
     c = cases[0]
     ref = OL.layer_forward(oracle_params(spec, layer), c["x"], gate_log_a=c["log_a"], gate_b=c["b"])
     assert rel_l2(bf16_host_f32(y2[: ext[0]]), ref["y"][c["prefix"]:]) <= 1e-2
-    assert rel_l2(s2[0].cpu().numpy(), ref["state"]) <= 1e-2
+    assert rel_l2(s2[0].cpu().numpy(), ref["state"]) <= 2e-3   # recurrence tolerance
 
 
 def test_batch_argument_checks():

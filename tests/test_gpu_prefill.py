@@ -4,9 +4,11 @@ ubatching and determinism properties.
 End to end the oracle is fed only x, the drawn gates and the packed weights.
 The projections are bit-exact, so every difference comes from the
 floating-point stages (bf16 activations between stages, fp32 recurrence,
-int8 re-quantisation of the gated-norm output): y and the final state must
-agree within relative L2 1e-2 (the tolerance for int8 projections), the conv
-state exactly (it holds raw projection outputs).
+int8 re-quantisation of the gated-norm output).  y must agree within
+relative L2 1e-2 (the tolerance for int8 projections: re-quantising o_hat to
+int8 amplifies o's rounding), the final state within 2e-3 (the tolerance for
+the recurrence with fp32 state: the projections feeding it are bit-exact), the
+conv state exactly (it holds raw projection outputs).
 """
 import numpy as np
 import pytest
@@ -19,6 +21,9 @@ from oracle import layer as OL
 from gpu_util import DEV, bf16_dev, bf16_host_f32, f32_dev, oracle_params, rel_l2
 
 pytestmark = pytest.mark.gpu
+
+Y_TOL = 1e-2        # end to end through two int8 projections
+STATE_TOL = 2e-3    # the recurrence with fp32 state
 
 
 def _x_dev(spec, tok):
@@ -50,8 +55,8 @@ def _run(dl, spec, tok, n=None, ws_tokens=None, state=None, conv=None, start=0):
 def _check_vs_oracle(spec, dl, layer, tok, y, state, conv):
     p = oracle_params(spec, layer)
     ref = OL.layer_forward(p, tok["x"], gate_log_a=tok["log_a"], gate_b=tok["b"])
-    assert rel_l2(_y_host(spec, y), ref["y"]) <= 1e-2
-    assert rel_l2(state.cpu().numpy(), ref["state"]) <= 1e-2
+    assert rel_l2(_y_host(spec, y), ref["y"]) <= Y_TOL
+    assert rel_l2(state.cpu().numpy(), ref["state"]) <= STATE_TOL
     if spec.wtype == "q4k":
         assert np.array_equal(conv.cpu().numpy(), ref["conv_tail"].astype(np.float32))
     else:
@@ -96,8 +101,8 @@ def test_prefill_computed_gates():
     dl.prefill(bf16_dev(tok["x_bits"]), None, state, conv, y, ws)
     torch.cuda.synchronize()
     ref = OL.layer_forward(oracle_params(spec, layer), tok["x"])
-    assert rel_l2(bf16_host_f32(y), ref["y"]) <= 1e-2
-    assert rel_l2(state.cpu().numpy(), ref["state"]) <= 1e-2
+    assert rel_l2(bf16_host_f32(y), ref["y"]) <= Y_TOL
+    assert rel_l2(state.cpu().numpy(), ref["state"]) <= STATE_TOL
 
 
 def test_extend_equals_full_prefill_4b_layer():
@@ -130,7 +135,7 @@ def test_extend_at_odd_boundaries(n0):
     ya, sa, ca = _run(dl, spec, tok, n=n0)
     yb, sb, cb = _run(dl, spec, tok, start=n0, state=sa, conv=ca)
     # both runs are within tolerance of the exact layer; they differ by the rounding of
-    # the tf32 chunk products at different chunk boundaries (state: recurrence bound;
+    # the fp16 chunk products at different chunk boundaries (state: recurrence bound;
     # y: the end-to-end int8 bound, since re-quantising o_hat amplifies o's rounding)
     y2 = torch.cat([ya, yb])
     assert rel_l2(bf16_host_f32(y2), bf16_host_f32(yf)) <= 1e-2
@@ -230,13 +235,11 @@ def _stage_by_stage(dl, spec, x, la, bb, state_in, conv_state):
 @pytest.mark.parametrize("n", [1, 2, 3, 4, 127, 128, 130, 300, 515])
 @pytest.mark.parametrize("gates", ["drawn", "computed"])
 def test_prefill_equals_stage_calls(n, gates):
-    """gdn_prefill runs the conv in the input projection's epilogue (one thread
-    holds a token's head; the three tokens before it come from the lanes below,
-    the previous quarter of the tile, or the conv state) and fixes up the first
-    three tokens of every 128-token tile after the first in a separate pass.
-    It must give the same bits as the stage entry points called one by one,
-    whose conv is its own kernel: for lengths around the tile and quarter
-    boundaries, a nonzero initial conv state (not bf16-exact), drawn and
+    """gdn_prefill chains the step kernels inside one call (dequant, x
+    quantisation, projection, conv, delta rule with its prep on a second
+    stream, gated norm, output projection).  It must give the same bits as the
+    stage entry points called one by one: for lengths around the chunk and
+    tile boundaries, a nonzero initial conv state (not bf16-exact), drawn and
     computed gates."""
     spec = SMALL
     layer = synth.make_layer(spec)
@@ -293,7 +296,7 @@ def test_prefill_host_equals_device_prefill(name, n, pass_tokens):
     if n <= 1024:
         yy = synth.bf16_bits_to_f32(yh.numpy().view(np.uint16)) if q4k else yh.numpy()
         ref = OL.layer_forward(oracle_params(spec, layer), tok["x"], gate_log_a=tok["log_a"], gate_b=tok["b"])
-        assert rel_l2(yy, ref["y"]) <= 1e-2
+        assert rel_l2(yy, ref["y"]) <= Y_TOL
 
 
 def test_prefill_host_computed_gates_and_extend():
@@ -348,5 +351,5 @@ def test_prefill_with_q6k_matrices(q6k):
         p[name + "_fmt"] = "q6k"
         assert np.array_equal(dl.host_blocks[name], p[name])
     ref = OL.layer_forward(p, tok["x"], gate_log_a=tok["log_a"], gate_b=tok["b"])
-    assert rel_l2(_y_host(spec, y), ref["y"]) <= 1e-2
-    assert rel_l2(state.cpu().numpy(), ref["state"]) <= 1e-2
+    assert rel_l2(_y_host(spec, y), ref["y"]) <= Y_TOL
+    assert rel_l2(state.cpu().numpy(), ref["state"]) <= STATE_TOL

@@ -4,11 +4,11 @@ Integer and byte work (Q4_K decode to int8 rows, activation quantisation, the
 integer product and its fp32 rescale) must be bit-exact.  Floating-point
 stages are fed the same inputs as the oracle and compared within tolerances
 derived from their arithmetic:
-  * conv + SiLU + L2 norm (fp32 out, rounded to tf32 for the recurrence's
-    tensor cores): each element within 2^-11 + 3e-5 relative of the fp64
-    value (the tf32 rounding, plus a few fp32 roundings in the 4-tap sum,
-    expf, the 128-term norm and rsqrtf) plus 1e-6 of the tensor's largest
-    magnitude (cancellation in the tap sum);
+  * conv + SiLU + L2 norm (fp16 out, the recurrence's tensor-core operand
+    type): each element within 2^-11 + 3e-5 relative of the fp64 value (the
+    fp16 rounding, plus a few fp32 roundings in the 4-tap sum, the
+    exponential, the 128-term norm and the reciprocal square root) plus 1e-6
+    of the tensor's largest magnitude (cancellation in the tap sum);
   * gated delta rule (fp32 state, chunked): relative L2 <= 2e-3 for o and the
     final state;
   * gated RMSNorm: fp32 output within relative L2 1e-5; int8 codes within
