@@ -8,7 +8,26 @@
 
 #include "../../include/gdn.h"
 
+#include <mutex>
+
 namespace gdn {
+
+// Host: kernel attributes (dynamic shared memory, carveout) and device
+// queries belong to one device, so a launcher's one-time setup runs once per
+// device, on the first call made with that device current.  run(f) calls
+// f(device) at most once per device ordinal below MAX_DEVICES and returns the
+// current device, or -1 (nothing run) for an ordinal past the table.
+constexpr int MAX_DEVICES = 256;
+struct PerDeviceOnce {
+    std::once_flag flag[MAX_DEVICES];
+    template <class F>
+    int run(F&& f) {
+        int d = -1;
+        if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= MAX_DEVICES) return -1;
+        std::call_once(flag[d], f, d);
+        return d;
+    }
+};
 
 // Kernels whose waits are bounded keep an error word in their own translation
 // unit (`static __device__ int`, no relocatable device code): when a wait runs

@@ -963,14 +963,22 @@ extern "C" int gdn_delta_rule_noalloc(const gdn_layer* layer, const uint16_t* qk
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "gdn_delta_rule_noalloc: cudaGetDevice");
     if (dev < 0 || dev >= kMaxDevices) return fail(GDN_EINVAL, "gdn_delta_rule_noalloc: device ordinal %d out of range", dev);
+    // Outside a stream capture the address is looked up on every call (a
+    // cudaDeviceReset reloads the module and may move the array); inside one,
+    // the address of this device's last call outside a capture is used.
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    e = cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &cap);
+    if (e != cudaSuccess) return cuda_fail(e, "gdn_delta_rule_noalloc: cudaStreamIsCapturing");
     void* scratch = nullptr;
     {
         std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-        if (!g_noalloc_addr[dev]) {
+        if (cap == cudaStreamCaptureStatusNone) {
             void* p = nullptr;
             e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
             if (e != cudaSuccess) return cuda_fail(e, "gdn_delta_rule_noalloc: cudaGetSymbolAddress");
             g_noalloc_addr[dev] = p;
+        } else if (!g_noalloc_addr[dev]) {
+            return fail(GDN_EINVAL, "gdn_delta_rule_noalloc: the first call on a device must come before any stream capture");
         }
         scratch = g_noalloc_addr[dev];
     }

@@ -431,10 +431,11 @@ size_t attn_workspace_bytes(int64_t nk, int hkv, int d) {
 template <int D>
 static cudaError_t launch_attn_d(const uint16_t* q, const uint16_t* k, const uint16_t* vt, int64_t nq, int64_t nk, int hq,
                                  int hkv, float scale, uint16_t* o, cudaStream_t st) {
-    static std::once_flag attr_once;
+    static PerDeviceOnce attr_once;
     // at least 120 KB, so that one CTA holds an SM (it allocates all 512 TMEM columns)
     constexpr int smem = AttSmem<D>::BYTES + 1024 > 120 * 1024 ? AttSmem<D>::BYTES + 1024 : 120 * 1024;
-    std::call_once(attr_once, [] { cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); });
+    if (attr_once.run([](int) { cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); }) < 0)
+        return cudaErrorInvalidDevice;
     CUtensorMap mq, mk, mv;
     if (!attn_map(&mq, q, nq, static_cast<int64_t>(hq) * D, static_cast<int64_t>(hq) * D, ATT_BM) ||
         !attn_map(&mk, k, nk, static_cast<int64_t>(hkv) * D, static_cast<int64_t>(hkv) * D, ATT_BN) ||

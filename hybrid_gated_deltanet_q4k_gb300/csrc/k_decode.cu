@@ -800,29 +800,30 @@ static cudaError_t qm_launch_nt(unsigned grid, size_t smem, cudaStream_t st, con
 // (fewer when their codes and two stages would not fit shared memory),
 // QM_CTAS_PER_SM CTAs per SM, as many stages as fit up to the tiles a CTA
 // walks.  Only for rows where qm_fits holds.
-static int qm_sms = 0, qm_budget = 0;
-static void qm_init() {
-    static std::once_flag once;
-    std::call_once(once, [] {
-        int dev = 0, optin = 0;
-        cudaGetDevice(&dev);
+// SM count and dynamic shared-memory budget of the tensor-core form, per device.
+static int qm_sms[MAX_DEVICES] = {}, qm_budget[MAX_DEVICES] = {};
+// The current device, its attributes set and figures queried (-1: none).
+static int qm_init() {
+    static PerDeviceOnce once;
+    return once.run([](int dev) {
+        int optin = 0;
         cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-        cudaDeviceGetAttribute(&qm_sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaDeviceGetAttribute(&qm_sms[dev], cudaDevAttrMultiProcessorCount, dev);
         cudaFuncAttributes fa{};
         cudaFuncGetAttributes(&fa, gemv_q4k_mma_kernel<QM_MAX_NT>);
         const int stat = static_cast<int>(fa.sharedSizeBytes);
         const int per_cta = GEMV_SM_SMEM / QM_CTAS_PER_SM - 1024 - stat;
-        qm_budget = optin - stat < per_cta ? optin - stat : per_cta;
-        cudaFuncSetAttribute(gemv_q4k_mma_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, qm_budget);
-        cudaFuncSetAttribute(gemv_q4k_mma_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, qm_budget);
+        qm_budget[dev] = optin - stat < per_cta ? optin - stat : per_cta;
+        cudaFuncSetAttribute(gemv_q4k_mma_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, qm_budget[dev]);
+        cudaFuncSetAttribute(gemv_q4k_mma_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, qm_budget[dev]);
     });
 }
 
 // Whether Q4_K rows of `cols` weights take the tensor-core form: 8 tokens'
 // codes and two stages fit shared memory.
 static bool qm_fits(int64_t cols) {
-    qm_init();
-    return qm_smem_bytes(1, static_cast<int>(cols), (cols / 256) * 144, 2) <= qm_budget;
+    const int dev = qm_init();
+    return dev >= 0 && qm_smem_bytes(1, static_cast<int>(cols), (cols / 256) * 144, 2) <= qm_budget[dev];
 }
 
 static void launch_gemv_q4k_mma(const void* blocks, int64_t rows, int64_t cols, const uint16_t* xc,
@@ -830,8 +831,12 @@ static void launch_gemv_q4k_mma(const void* blocks, int64_t rows, int64_t cols, 
                                 uint16_t* out_bf16, int64_t ld_bf16, int64_t n_bf16, float* out_f32, int64_t ld_f32,
                                 cudaStream_t st, float* cs_state, const uint16_t* cs_qkvz, int64_t cs_ld,
                                 int cs_c_conv, int cs_n, cudaError_t& err) {
-    qm_init();
-    const int sms = qm_sms, budget = qm_budget;
+    const int dev = qm_init();
+    if (dev < 0) {
+        err = cudaErrorInvalidDevice;
+        return;
+    }
+    const int sms = qm_sms[dev], budget = qm_budget[dev];
     const int64_t row_bytes = (cols / 256) * 144;
     const int c = static_cast<int>(cols);
     int ntmax = QM_MAX_NT;
@@ -891,21 +896,24 @@ cudaError_t launch_gemv_dot(const void* blocks, bool q6k, int64_t rows, int64_t 
                               uint16_t* out_bf16, int64_t ld_bf16, int64_t n_bf16, float* out_f32, int64_t ld_f32,
                               cudaStream_t st, float* cs_state, const uint16_t* cs_qkvz, int64_t cs_ld, int cs_c_conv,
                               int cs_n) {
-    static int sms = 0, max_optin = 0, fa_static = 0;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    // per device: SM count and the dynamic shared memory the kernels may take
+    static int sms_of[MAX_DEVICES] = {}, optin_of[MAX_DEVICES] = {}, static_of[MAX_DEVICES] = {};
+    static PerDeviceOnce once;
+    const int dev = once.run([](int d) {
+        int optin = 0;
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, d);
         // dynamic shared memory: the opt-in maximum less the kernels' static arrays
         cudaFuncAttributes fa{};
         cudaFuncGetAttributes(&fa, gemv_dot_kernel<true, 8>);
-        fa_static = static_cast<int>(fa.sharedSizeBytes);
-        max_optin -= fa_static;
-        gemv_set_smem<false>(max_optin);
-        gemv_set_smem<true>(max_optin);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        static_of[d] = static_cast<int>(fa.sharedSizeBytes);
+        optin -= static_of[d];
+        gemv_set_smem<false>(optin);
+        gemv_set_smem<true>(optin);
+        optin_of[d] = optin;
+        cudaDeviceGetAttribute(&sms_of[d], cudaDevAttrMultiProcessorCount, d);
     });
+    if (dev < 0) return cudaErrorInvalidDevice;
+    const int sms = sms_of[dev], max_optin = optin_of[dev], fa_static = static_of[dev];
     // Q4_K rows that fit the tensor-core form take it for several tokens; one
     // token takes the dp4a kernel in the same fp32 operations (a token's
     // result does not depend on the batch)

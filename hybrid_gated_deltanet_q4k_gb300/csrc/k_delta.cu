@@ -941,14 +941,15 @@ static void launch_state(const CUtensorMap& map, const DeltaArgs& a, const SeqTa
 template <int D>
 static cudaError_t launch_delta_d(DeltaArgs& a, const SeqTable& sq, cudaStream_t st, bool overlap,
                                   const TokenRangeHook* after_state) {
-    static std::once_flag attr_once;
-    std::call_once(attr_once, [] {
+    static PerDeviceOnce attr_once;
+    const int dev = attr_once.run([](int) {
         cudaFuncSetAttribute(delta_prep_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, PrepSmem<D>::BYTES + 1024);
         cudaFuncSetAttribute(delta_state_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, StateSmem<D>::BYTES + 1024);
         // the whole unified L1 as shared memory, so that a state CTA and a prep CTA fit on one SM
         cudaFuncSetAttribute(delta_prep_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
         cudaFuncSetAttribute(delta_state_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     });
+    if (dev < 0) return cudaErrorInvalidDevice;
     CUtensorMap map;
     if (!make_qkv_map(&map, a.qkv, a.n, a.c_conv)) return cudaErrorInvalidValue;
     int nch = 0;  // chunks of the longest sequence

@@ -501,11 +501,12 @@ static bool make_store_map(CUtensorMap* map, const void* base, int64_t rows, int
     return r == CUDA_SUCCESS;
 }
 
-// Clusters of 2 CTAs of the projection kernel that fit on the device at once.
-static int resident_pairs() {
-    static int cached = 0;
-    static std::once_flag once;
-    std::call_once(once, [] {
+// Clusters of 2 CTAs of the projection kernel that fit on device `dev` (the
+// current one) at once; the kernel's shared-memory attribute is set first.
+static int resident_pairs(int dev) {
+    static int cached[MAX_DEVICES] = {};
+    static PerDeviceOnce once;
+    once.run([](int d) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(static_cast<unsigned>(sm_count()), 1, 1);
         cfg.blockDim = dim3(tc::THREADS, 1, 1);
@@ -522,9 +523,9 @@ static int resident_pairs() {
             cudaGetLastError();
             n = sm_count() / 2;
         }
-        cached = n;
+        cached[d] = n;
     });
-    return cached;
+    return cached[dev];
 }
 
 // Returns cudaErrorInvalidValue when a tensor map cannot be built (caller
@@ -534,10 +535,11 @@ cudaError_t launch_gemm_codes(const uint16_t* a, const float* sa, const uint16_t
                               float* out_f32, int64_t ld_f32, cudaStream_t st) {
     CUtensorMap ma, mb;
     if (!make_map(&ma, a, M, K, tc::BM) || !make_map(&mb, b, N, K, tc::BN / 2)) return cudaErrorInvalidValue;
-    static std::once_flag attr_once;
-    std::call_once(attr_once, [] {
+    static PerDeviceOnce attr_once;
+    const int dev = attr_once.run([](int) {
         cudaFuncSetAttribute(gemm_codes_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_BYTES);
     });
+    if (dev < 0) return cudaErrorInvalidDevice;
     GemmArgs g;
     g.sa = sa;
     g.sb = sb;
@@ -560,7 +562,7 @@ cudaError_t launch_gemm_codes(const uint16_t* a, const float* sa, const uint16_t
     // pairs of CTAs (clusters of 2): as many as can be resident at once (a
     // cluster stays within one GPC), at most one per tile
     const int64_t tiles = ((M + 2 * tc::BM - 1) / (2 * tc::BM)) * ((N + tc::BN - 1) / tc::BN);
-    const int max_pairs = resident_pairs();
+    const int max_pairs = resident_pairs(dev);
     const int pairs = static_cast<int>(tiles < max_pairs ? tiles : max_pairs);
     const int grid = 2 * (pairs > 0 ? pairs : 1);
     gemm_codes_kernel<<<grid, tc::THREADS, tc::SMEM_BYTES, st>>>(ma, mb, mc, g);

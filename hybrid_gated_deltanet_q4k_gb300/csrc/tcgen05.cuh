@@ -23,14 +23,6 @@ __device__ __forceinline__ void dealloc(uint32_t base, uint32_t cols) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(base), "r"(cols) : "memory");
 }
 
-// Instruction descriptor for kind::tf32: D fp32 (bits 4-5 = 1), A and B tf32
-// (bits 7-9 and 10-12 = 2), both K-major (bits 15, 16 = 0), N>>3 at bits
-// 17-22, M>>4 at bits 24-28.
-__host__ __device__ constexpr uint32_t idesc_tf32(int m, int n) {
-    return (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
-           (static_cast<uint32_t>(m >> 4) << 24);
-}
-
 // Instruction descriptor for kind::f16 with fp16 A and B: D fp32 (bits 4-5 =
 // 1), A and B fp16 (bits 7-9 and 10-12 = 0), both K-major, N>>3 at bits
 // 17-22, M>>4 at bits 24-28.
@@ -68,17 +60,6 @@ __device__ __forceinline__ uint64_t desc_sw64_mn(uint32_t saddr) {
     return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(1) << 16) |
            (static_cast<uint64_t>(512 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
            (static_cast<uint64_t>(4) << 61);
-}
-
-// D[tmem] (+)= A * B^T, one elected thread.
-__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                         uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
 }
 
 // D[tmem] (+)= A * B^T with fp16 operands (K = 16 per instruction), one

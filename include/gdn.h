@@ -22,7 +22,10 @@
  * Conventions shared by every entry point:
  *   - Pointers named "host" are host memory; every other pointer is device
  *     memory on the current CUDA device, owned by the caller.  The library
- *     never allocates, frees or keeps device memory across calls.
+ *     never allocates or frees device memory, and keeps none across calls
+ *     with one exception: the static scratch array of
+ *     gdn_delta_rule_noalloc (GDN_NOALLOC_SCRATCH_BYTES on every device
+ *     that loads the library, held until the process exits).
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Device
  *     work is enqueued asynchronously on it; the call returns when the work is
  *     enqueued.  A fault inside a kernel shows up at gdn_sync_status().
@@ -472,9 +475,12 @@ size_t gdn_delta_rule_scratch_size(const gdn_layer *layer, int64_t n_tokens);
  *   - A call whose gdn_delta_rule_scratch_size(layer, n_tokens) exceeds that
  *     size returns GDN_EINVAL with a message (e.g. at most 3904 tokens, 61
  *     chunks of 64, for 32 value heads over 16 key heads of d = 128).
- *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *   - A call outside a stream capture looks up the array's device address
+ *     (cudaGetSymbolAddress) with the current device, so a cudaDeviceReset,
+ *     which may move the array, is followed; a call inside a capture reuses
+ *     the address found by that device's last call outside one.  Make the
+ *     first call on each device before any stream capture (inside one, a
+ *     device that has no address yet gets GDN_EINVAL).
  *   - Every call shares the one array and it keeps the last call's contents
  *     (nothing in it needs to start at zero: each call writes every scratch
  *     entry it reads).  Calls that overlap on the GPU (other streams, other
