@@ -57,6 +57,14 @@ struct DeltaCkpt {
     int chunk_base;
 };
 
+// Test of the bounded waits (gdn_test_delta_wait_timeout): the delta rule's
+// prep runs alone and issues no copy of its [Q; K] tile, so its wait for that
+// copy runs out after wait_ns; the kernel records the timeout, frees its TMEM
+// and returns.
+struct DeltaFault {
+    uint64_t wait_ns;
+};
+
 // The sequence holding work unit u: the last s with unit[s] <= u (an empty
 // sequence owns no unit, so it is passed over).
 __device__ __forceinline__ int seq_of_unit(const SeqTable& t, int u) {

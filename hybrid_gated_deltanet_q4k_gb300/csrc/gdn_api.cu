@@ -37,7 +37,8 @@ cudaError_t launch_conv_state(const gdn_layer&, const uint16_t*, int64_t, int64_
                               const int64_t* cu_seqlens = nullptr, int n_seqs = 1);
 cudaError_t launch_delta(const gdn_layer&, const uint16_t*, const float*, const float*, int64_t, const float*, float*,
                          uint16_t*, void*, cudaStream_t, bool overlap, const TokenRangeHook* after_state,
-                         const int64_t* cu_seqlens = nullptr, int n_seqs = 1, const DeltaCkpt* ckpt = nullptr);
+                         const int64_t* cu_seqlens = nullptr, int n_seqs = 1, const DeltaCkpt* ckpt = nullptr,
+                         const DeltaFault* fault = nullptr);
 cudaError_t launch_conv_ckpt(const gdn_layer&, const uint16_t*, int64_t, int64_t, int64_t, int64_t, float*, cudaStream_t);
 size_t delta_scratch_bytes(int hv, int hk, int d, int64_t n);
 cudaError_t launch_gated_norm(const gdn_layer&, const uint16_t*, const uint16_t*, int64_t, int64_t, uint16_t*, float*,
@@ -490,6 +491,27 @@ int gdn_delta_rule(const gdn_layer* layer, const uint16_t* qkv, const float* log
     GDN_LAUNCH(launch_delta(*layer, qkv, log_a, b, n_tokens, state_in, state_out, o, scratch, static_cast<cudaStream_t>(stream),
                             true, nullptr),
                "gdn_delta_rule");
+    return GDN_OK;
+}
+
+int gdn_test_delta_wait_timeout(const gdn_layer* layer, const uint16_t* qkv, const float* log_a, const float* b,
+                                int64_t n_tokens, void* scratch, size_t scratch_bytes, uint64_t wait_ns, void* stream) {
+    Sizes s;
+    int r = check_layer(layer, &s);
+    if (r) return r;
+    if (n_tokens < 1 || n_tokens > 0x7fffffff) return fail(GDN_EINVAL, "gdn_test_delta_wait_timeout: n_tokens >= 1 required");
+    if (!qkv || !log_a || !b || !scratch) return fail(GDN_EINVAL, "gdn_test_delta_wait_timeout: NULL pointer");
+    if (!aligned(qkv, 16) || !aligned(scratch, 16))
+        return fail(GDN_EINVAL, "gdn_test_delta_wait_timeout: qkv and scratch 16-byte alignment required");
+    if (wait_ns < 1000 || wait_ns > 100000000ull)
+        return fail(GDN_EINVAL, "gdn_test_delta_wait_timeout: wait_ns in [1 us, 100 ms] required");
+    if (scratch_bytes < delta_scratch_bytes(static_cast<int>(s.hv), static_cast<int>(s.hk), static_cast<int>(s.d), n_tokens))
+        return fail(GDN_ENOMEM, "gdn_test_delta_wait_timeout: scratch too small");
+    const DeltaFault fault{wait_ns};
+    // the prep alone writes no state and no output: state_out and o are unused
+    GDN_LAUNCH(launch_delta(*layer, qkv, log_a, b, n_tokens, nullptr, nullptr, nullptr, scratch,
+                            static_cast<cudaStream_t>(stream), false, nullptr, nullptr, 1, nullptr, &fault),
+               "gdn_test_delta_wait_timeout");
     return GDN_OK;
 }
 

@@ -77,6 +77,8 @@ struct DeltaArgs {
     float* state_out;
     uint16_t* o;   // [n][c_v] fp16
     DeltaCkpt ckpt;  // state snapshots (ckpt.state null: none); one sequence only
+    uint64_t prep_wait_ns;  // limit of the prep's wait for its [Q; K] copy
+    int prep_no_copy;       // test only: the prep issues no copy, so that wait runs out
 };
 
 __device__ __forceinline__ uint16_t f16_bits(float x) { return __half_as_ushort(__float2half_rn(x)); }
@@ -227,11 +229,13 @@ __global__ void __maxnreg__(88) delta_prep_kernel(const __grid_constant__ CUtens
         mbar_init_cta(bars + 0, 1);
         mbar_init_cta(bars + 1, 1);
         mbar_init_fence();
-        mbar_expect_tx(bars + 0, 2 * L::NSLAB * L::SLAB);
-        for (int sl = 0; sl < L::NSLAB; ++sl) {
-            unsigned char* dst = base + L::QK0 + sl * 2 * L::SLAB;
-            tma_load_2d_tile(dst, &qkv_map, bars + 0, hk * D + 64 * sl, t0);
-            tma_load_2d_tile(dst + L::SLAB, &qkv_map, bars + 0, a.c_qk + hk * D + 64 * sl, t0);
+        if (!a.prep_no_copy) {
+            mbar_expect_tx(bars + 0, 2 * L::NSLAB * L::SLAB);
+            for (int sl = 0; sl < L::NSLAB; ++sl) {
+                unsigned char* dst = base + L::QK0 + sl * 2 * L::SLAB;
+                tma_load_2d_tile(dst, &qkv_map, bars + 0, hk * D + 64 * sl, t0);
+                tma_load_2d_tile(dst + L::SLAB, &qkv_map, bars + 0, a.c_qk + hk * D + 64 * sl, t0);
+            }
         }
     }
     if (warp == 0) t5::alloc(tslot, 128);
@@ -268,7 +272,7 @@ __global__ void __maxnreg__(88) delta_prep_kernel(const __grid_constant__ CUtens
 
     bool ok = true;
     if (tid == 0) {
-        ok = mbar_wait_bounded(bars + 0, 0, &g_delta_error, ERR_WAIT_TIMEOUT);
+        ok = mbar_wait_bounded(bars + 0, 0, &g_delta_error, ERR_WAIT_TIMEOUT, a.prep_wait_ns);
         if (ok) {
             t5::fence_after();
             const uint32_t sb = smem_addr(base);
@@ -938,9 +942,10 @@ static void launch_state(const CUtensorMap& map, const DeltaArgs& a, const SeqTa
 // state segments; without segments it runs on st after the state pass.  With
 // several sequences a segment's tokens are not contiguous, and the hook runs
 // once over all tokens after the last state segment.
+// prep_only: the prep alone, one launch (the wait-expiry test).
 template <int D>
 static cudaError_t launch_delta_d(DeltaArgs& a, const SeqTable& sq, cudaStream_t st, bool overlap,
-                                  const TokenRangeHook* after_state) {
+                                  const TokenRangeHook* after_state, bool prep_only) {
     static PerDeviceOnce attr_once;
     const int dev = attr_once.run([](int) {
         cudaFuncSetAttribute(delta_prep_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, PrepSmem<D>::BYTES + 1024);
@@ -957,6 +962,10 @@ static cudaError_t launch_delta_d(DeltaArgs& a, const SeqTable& sq, cudaStream_t
     a.chunk0 = 0;
     a.nchunks = nch;
     if (nch == 0) return cudaSuccess;
+    if (prep_only) {
+        launch_prep<D>(map, a, sq, st);
+        return cudaGetLastError();
+    }
     if (!overlap || nch <= DELTA_SEG_CHUNKS) {
         launch_prep<D>(map, a, sq, st);
         cudaError_t e = cudaGetLastError();
@@ -1012,7 +1021,7 @@ static cudaError_t launch_delta_d(DeltaArgs& a, const SeqTable& sq, cudaStream_t
 cudaError_t launch_delta(const gdn_layer& L, const uint16_t* qkv, const float* log_a, const float* b, int64_t n,
                          const float* state_in, float* state_out, uint16_t* o, void* scratch, cudaStream_t st,
                          bool overlap, const TokenRangeHook* after_state, const int64_t* cu_seqlens, int n_seqs,
-                         const DeltaCkpt* ckpt) {
+                         const DeltaCkpt* ckpt, const DeltaFault* fault) {
     DeltaArgs a;
     const int d = L.dk;
     // the call's sequences (host token offsets; null: one sequence of n tokens),
@@ -1038,8 +1047,11 @@ cudaError_t launch_delta(const gdn_layer& L, const uint16_t* qkv, const float* l
     a.state_out = state_out;
     a.o = o;
     a.ckpt = ckpt && !cu_seqlens ? *ckpt : DeltaCkpt{nullptr, 1, 0};
-    return d == 128 ? launch_delta_d<128>(a, sq, st, overlap, after_state)
-                    : launch_delta_d<64>(a, sq, st, overlap, after_state);
+    a.prep_wait_ns = fault ? fault->wait_ns : 2000000000ull;
+    a.prep_no_copy = fault ? 1 : 0;
+    const bool prep_only = fault != nullptr;
+    return d == 128 ? launch_delta_d<128>(a, sq, st, overlap, after_state, prep_only)
+                    : launch_delta_d<64>(a, sq, st, overlap, after_state, prep_only);
 }
 
 }  // namespace gdn

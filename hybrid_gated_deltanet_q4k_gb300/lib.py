@@ -66,6 +66,7 @@ _SIGNATURES = {
     "gdn_delta_rule": (c_int32, [_P, _P, _P, _P, c_int64, _P, _P, _P, _P, c_size_t, _P]),
     "gdn_delta_rule_scratch_size": (c_size_t, [_P, c_int64]),
     "gdn_delta_rule_noalloc": (c_int32, [_P, _P, _P, _P, c_int64, _P, _P, _P, _P]),
+    "gdn_test_delta_wait_timeout": (c_int32, [_P, _P, _P, _P, c_int64, _P, c_size_t, ctypes.c_uint64, _P]),
     "gdn_gated_norm": (c_int32, [_P, _P, _P, c_int64, c_int64, _P, _P, _P, _P]),
 }
 

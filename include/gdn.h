@@ -493,6 +493,22 @@ int gdn_delta_rule_noalloc(const gdn_layer *layer, const uint16_t *qkv, const fl
                            void *stream);
 
 /*
+ * gdn_test_delta_wait_timeout -- a test of the bounded device waits (the
+ * pages' lesson that an infrastructure failure must surface as a failure,
+ * not as a result: sparkinfer PR #464, eval-bot thread).  Runs only the
+ * delta rule's prep kernel of gdn_delta_rule on these inputs, with its copy
+ * of the [Q; K] tile never issued, so the kernel's wait for that copy runs
+ * out after wait_ns nanoseconds (1 us .. 100 ms).  The kernel records the
+ * timeout in its error word, frees its tensor memory and returns; nothing
+ * faults and the context stays usable.  gdn_sync_status() then reports
+ * GDN_ETIMEOUT once (reading clears the word) and the next call runs
+ * normally.  Writes only into `scratch` (gdn_delta_rule_scratch_size bytes).
+ */
+int gdn_test_delta_wait_timeout(const gdn_layer *layer, const uint16_t *qkv, const float *log_a, const float *b,
+                                int64_t n_tokens, void *scratch, size_t scratch_bytes, uint64_t wait_ns,
+                                void *stream);
+
+/*
  * gdn_gated_norm -- step 4: per token and value head
  * o_hat = o / sqrt(mean(o^2) + eps_rms) * norm_w * SiLU(z), o fp16 [N][C_v]
  * (8-byte aligned) as gdn_delta_rule writes it, z bf16 at z[t*ld_z + h*dv + i].  Q4_K layers: each token row of o_hat (all C_v

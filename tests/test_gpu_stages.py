@@ -365,6 +365,38 @@ def test_delta_rule_segments_bitwise(L):
     assert rel_l2(st_one.cpu().numpy(), rS) <= 2e-3
 
 
+@pytest.mark.parametrize("spec", DELTA_SPECS[:2], ids=lambda s: s.name)
+def test_delta_rule_wait_runs_out_then_recovers(L, spec):
+    """Fail closed on a bounded device wait (sparkinfer PR #464, eval-bot
+    thread: an infrastructure failure must surface as a failure, not as a
+    result).  gdn_test_delta_wait_timeout runs the delta rule's prep with its
+    [Q; K] copy never issued and a 1 ms limit on the wait for it: the kernel
+    records the timeout, frees its tensor memory and returns, nothing faults,
+    gdn_sync_status reports GDN_ETIMEOUT once, and the next gdn_delta_rule
+    call runs normally and matches the oracle."""
+    _, dev, s = _layer(spec, L)
+    rng = np.random.default_rng(91)
+    n = 200
+    qkv_h, qe, ke, ve, la, b = _delta_inputs(spec, n, rng)
+    qkv, lad, bd = f16_dev(qkv_h), f32_dev(la), f32_dev(b)
+    nbytes = L.gdn_delta_rule_scratch_size(ctypes.byref(s), n)
+    scratch = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    args = (ctypes.byref(s), gl.ptr(qkv), gl.ptr(lad), gl.ptr(bd), n, gl.ptr(scratch), nbytes)
+    assert L.gdn_test_delta_wait_timeout(*args, 10, stream(), check=False) == gl.GDN_EINVAL   # limit below 1 us
+    assert L.gdn_test_delta_wait_timeout(*args, 1_000_000, stream()) == gl.GDN_OK
+    assert L.gdn_sync_status(stream(), check=False) == gl.GDN_ETIMEOUT
+    assert "delta-rule" in L.last_error()
+    assert L.gdn_sync_status(stream(), check=False) == gl.GDN_OK      # reading cleared the error word
+    sout = torch.empty(spec.n_v_heads, spec.dv, spec.dk, dtype=torch.float32, device=DEV)
+    o = torch.empty(n, spec.c_v, dtype=torch.float16, device=DEV)
+    L.gdn_delta_rule(ctypes.byref(s), gl.ptr(qkv), gl.ptr(lad), gl.ptr(bd), n, 0, gl.ptr(sout), gl.ptr(o),
+                     gl.ptr(scratch), nbytes, stream())
+    sync(L)
+    ro, rS = OL.gated_delta_rule(qe, ke, ve, la, b, np.zeros((spec.n_v_heads, spec.dv, spec.dk)))
+    assert rel_l2(o.float().cpu().numpy(), ro.reshape(n, -1)) <= 2e-3
+    assert rel_l2(sout.cpu().numpy(), rS) <= 2e-3
+
+
 def test_delta_rule_state_aliasing(L):
     spec = DELTA_SPECS[1]
     _, dev, s = _layer(spec, L)

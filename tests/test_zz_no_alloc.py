@@ -67,10 +67,13 @@ def test_noalloc_rejects_more_tokens_than_its_scratch():
     L = gl.load(build=True)
     spec = synth.SPECS["h4096"]
     s, _keep = _layer_struct(spec)
-    n = 3905                                       # 62 chunks of 64 > the 61 that fit in 48 MiB
+    per_chunk = L.gdn_delta_rule_scratch_size(ctypes.byref(s), 64)
+    fit = gl.GDN_NOALLOC_SCRATCH_BYTES // per_chunk * 64   # whole chunks of 64 tokens that fit the static array
+    n = fit + 1
+    assert L.gdn_delta_rule_scratch_size(ctypes.byref(s), fit) <= gl.GDN_NOALLOC_SCRATCH_BYTES
     assert L.gdn_delta_rule_scratch_size(ctypes.byref(s), n) > gl.GDN_NOALLOC_SCRATCH_BYTES
     buf = torch.zeros(16, dtype=torch.float32, device=DEV)
     r = L.gdn_delta_rule_noalloc(ctypes.byref(s), gl.ptr(buf), gl.ptr(buf), gl.ptr(buf), n, 0, gl.ptr(buf),
                                  gl.ptr(buf), stream(), check=False)
     assert r == gl.GDN_EINVAL
-    assert "at most 3904 tokens" in L.last_error()
+    assert f"at most {fit} tokens" in L.last_error()
