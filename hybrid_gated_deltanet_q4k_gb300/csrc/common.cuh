@@ -201,10 +201,35 @@ __device__ __forceinline__ float small_uint_to_float(uint32_t v) {
     return __fsub_rn(__uint_as_float(0x4B000000u | v), 8388608.0f);
 }
 
-// SiLU(u) = u / (1 + e^-u) with the hardware exponential and reciprocal
-// (a few ulp; its consumers round to tf32 or to int8 codes).  u << 0 gives
-// e^-u = inf and the quotient -0.
-__device__ __forceinline__ float silu_f(float u) { return __fdividef(u, 1.0f + __expf(-u)); }
+// max(a, b), a NaN if either is one
+__device__ __forceinline__ float fmaxf_nan(float a, float b) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+
+// The hardware base-2 exponential and reciprocal (MUFU; a few ulp), with
+// subnormal inputs and results flushed to zero, which skips the scaling the
+// subnormal-preserving forms add around the operation.
+__device__ __forceinline__ float ex2_ftz(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ float rcp_ftz(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+// SiLU(u) = u / (1 + e^-u) = u * 1/(1 + 2^(-u log2 e)) with the hardware
+// exponential and reciprocal (a few ulp; its consumers round to fp16 or to
+// int8 codes).  u << 0 gives 2^(-u log2 e) = inf, a reciprocal of 0 and the
+// product -0; e^-u below fp32's normal range (u > 87) flushes to 0, where
+// 1 + e^-u is 1 either way.
+__device__ __forceinline__ float silu_f(float u) {
+    return u * rcp_ftz(1.0f + ex2_ftz(u * -1.4426950408889634f));
+}
 
 // The causal depthwise conv of one channel at token t (taps w.x .. w.w on
 // x_{t-3} .. x_t) followed by SiLU.  Every kernel that evaluates the conv calls

@@ -73,6 +73,10 @@ __device__ __forceinline__ void conv_head_tokens(const ConvArgs& a, int head, in
     for (int i = 0; i < CPL; ++i) w[i] = *reinterpret_cast<const float4*>(a.conv_w + static_cast<int64_t>(c0 + i) * 4);
     const bool norm = head < a.n_qk_norm;
     const float mul = head < a.n_q ? a.q_scale : 1.0f;
+    // An L2-normed head has |y| <= |mul| whenever its sum of squares is finite,
+    // so it is checked once per token (the sum, and mul once); every value of a
+    // head that is not normed is checked.
+    const bool mul_ok = fabsf(mul) <= 65504.0f;
 #pragma unroll
     for (int k = 0; k < NT; ++k) {
         const int t = t0 + k;
@@ -86,17 +90,21 @@ __device__ __forceinline__ void conv_head_tokens(const ConvArgs& a, int head, in
             ss = fmaf(y[i], y[i], ss);
             h0[i] = h1[i]; h1[i] = h2[i]; h2[i] = x;
         }
+        bool over;
         if (norm) {
             ss = warp_sum(ss);
+            over = !(ss <= 3.0e38f) || !mul_ok;
             const float r = rsqrtf(ss + a.eps) * mul;
 #pragma unroll
             for (int i = 0; i < CPL; ++i) y[i] *= r;
+        } else {
+            float m = 0.0f;
+#pragma unroll
+            for (int i = 0; i < CPL; ++i) m = fmaxf_nan(m, fabsf(y[i]));
+            over = !(m <= 65504.0f);
         }
         if (t < t1) {
             uint16_t* dst = a.out + static_cast<int64_t>(t) * a.c_conv + c0;
-            bool over = false;
-#pragma unroll
-            for (int i = 0; i < CPL; ++i) over |= !(fabsf(y[i]) <= 65504.0f);
             if (over) atomicCAS(&g_conv_error, 0, ERR_RANGE);
             const uint32_t p0 = f16x2_bits(y[0], y[1 % CPL]);
             if (CPL == 4)

@@ -91,12 +91,6 @@ __device__ __forceinline__ uint4 f16x8(const float (&v)[8]) {
 // true when x is not a finite value fp16 can hold
 __device__ __forceinline__ bool f16_out_of_range(float x) { return !(fabsf(x) <= F16_MAX); }
 
-// max(a, b), a NaN if either is one
-__device__ __forceinline__ float fmax_nan(float a, float b) {
-    float r;
-    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
-    return r;
-}
 
 // ------------------------------------------------------------------ prep
 
@@ -744,7 +738,7 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a, con
         auto write_row = [&](int off, int k, const float (&x)[16]) {
             float m = 0.0f;
 #pragma unroll
-            for (int v = 0; v < 16; ++v) m = fmax_nan(m, fabsf(x[v]));
+            for (int v = 0; v < 16; ++v) m = fmaxf_nan(m, fabsf(x[v]));
             bad |= !(m <= F16_MAX);              // an infinity, a NaN or a value past the fp16 range
             float lo[8], hi[8];
 #pragma unroll
