@@ -34,11 +34,12 @@ class DeviceLayer:
     """One GDN layer's parameters in device memory, in the layouts ``gdn_layer`` names."""
 
     def __init__(self, spec, params: dict, device: str = "cuda", eps_l2: float = 1e-6, eps_rms: float = 1e-6,
-                 q_scale: float | None = None, blocks: dict | None = None, q6k: tuple = ()):
-        """q6k: names of the matrices ("w_in", "w_out") to hold in Q6_K instead of Q4_K."""
+                 q_scale: float | None = None, blocks: dict | None = None, q6k: tuple = (), debug: bool = False):
+        """q6k: names of the matrices ("w_in", "w_out") to hold in Q6_K instead of Q4_K.
+        debug: run on the library's debug variant (index-checked kernels)."""
         self.spec = spec
         self.device = device
-        self.lib = gl.load()
+        self.lib = gl.load(debug=debug)
         self.q6k_mask = (1 if "w_in" in q6k else 0) | (2 if "w_out" in q6k else 0)
         t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)  # noqa: E731
         if spec.wtype == "q4k":

@@ -33,7 +33,22 @@ struct PerDeviceOnce {
 // unit (`static __device__ int`, no relocatable device code): when a wait runs
 // out they record a code there and return early; gdn_sync_status() reads and
 // clears every such word through the unit's host accessor.
-enum : int { ERR_NONE = 0, ERR_WAIT_TIMEOUT = 1, ERR_RANGE = 2 };
+enum : int { ERR_NONE = 0, ERR_WAIT_TIMEOUT = 1, ERR_RANGE = 2, ERR_INDEX = 3 };
+
+// Index checks of the debug build (compiled with GDN_DEBUG): a global store
+// whose index lies outside the extent its kernel was given records ERR_INDEX
+// in the unit's error word and is skipped (gdn_sync_status then reports
+// GDN_EINDEX), where a sanitizer would have reported an out-of-bounds access.
+// Release builds compile the checks away: GDN_IN_RANGE is `true`.
+#ifdef GDN_DEBUG
+__device__ __forceinline__ bool gdn_debug_in_range(int& word, bool ok) {
+    if (!ok) atomicCAS(&word, 0, static_cast<int>(ERR_INDEX));
+    return ok;
+}
+#define GDN_IN_RANGE(word, cond) ::gdn::gdn_debug_in_range((word), (cond))
+#else
+#define GDN_IN_RANGE(word, cond) true
+#endif
 
 // The sequences of one call, passed to kernels as a __grid_constant__
 // parameter (2 KB, no device memory): sequence s holds tokens [tok[s],

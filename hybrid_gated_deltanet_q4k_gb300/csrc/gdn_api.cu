@@ -60,6 +60,9 @@ size_t attn_workspace_bytes(int64_t nk, int hkv, int d);
 int read_and_clear_attn_error();
 int read_and_clear_gemm_error();
 int read_and_clear_delta_error();
+int read_and_clear_q4k_error();
+int read_and_clear_q6k_error();
+int read_and_clear_quant_error();
 int read_and_clear_conv_error();
 int read_and_clear_norm_error();
 }  // namespace gdn
@@ -933,14 +936,26 @@ int gdn_sync_status(void* stream) {
     if (e != cudaSuccess) return cuda_fail(e, "gdn_sync_status");
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "gdn_sync_status");
-    if (read_and_clear_gemm_error()) return fail(GDN_ETIMEOUT, "a bounded wait in the projection kernel ran out");
-    if (read_and_clear_attn_error()) return fail(GDN_ETIMEOUT, "a bounded wait in the attention kernel ran out");
+    // every unit's error word is read (and cleared) once
+    const int gcode = read_and_clear_gemm_error();
+    const int acode = read_and_clear_attn_error();
     const int dcode = read_and_clear_delta_error();
     const int rcode = read_and_clear_decode_error();
     const int ccode = read_and_clear_conv_error();
-    if (read_and_clear_norm_error() == ERR_WAIT_TIMEOUT)
-        return fail(GDN_ETIMEOUT, "a bounded wait in the gated-norm kernel ran out");
+    const int ncode = read_and_clear_norm_error();
+    const int words[] = {read_and_clear_q4k_error(), read_and_clear_q6k_error(), read_and_clear_quant_error(),
+                         gcode, ccode, dcode, ncode, rcode, acode};
+    const char* units[] = {"Q4_K decode", "Q6_K decode", "activation quantisation", "projection", "conv",
+                           "delta-rule", "gated-norm", "decode-step", "attention"};
+    for (int i = 0; i < static_cast<int>(sizeof(words) / sizeof(words[0])); ++i)
+        if (words[i] == ERR_INDEX)
+            return fail(GDN_EINDEX, "an index check of the %s kernel failed (the store was skipped; debug library)",
+                        units[i]);
+    if (gcode == ERR_WAIT_TIMEOUT) return fail(GDN_ETIMEOUT, "a bounded wait in the projection kernel ran out");
+    if (acode == ERR_WAIT_TIMEOUT) return fail(GDN_ETIMEOUT, "a bounded wait in the attention kernel ran out");
+    if (ncode == ERR_WAIT_TIMEOUT) return fail(GDN_ETIMEOUT, "a bounded wait in the gated-norm kernel ran out");
     if (dcode == ERR_WAIT_TIMEOUT) return fail(GDN_ETIMEOUT, "a bounded wait in the delta-rule kernel ran out");
+    if (rcode == ERR_WAIT_TIMEOUT) return fail(GDN_ETIMEOUT, "a bounded wait in a decode-step kernel ran out");
     if (rcode == ERR_RANGE) return fail(GDN_ERANGE, "a decode-step output o exceeded the fp16 range (|x| > 65504)");
     if (ccode == ERR_RANGE || dcode == ERR_RANGE)
         return fail(GDN_ERANGE, "a %s value exceeded the fp16 operand range (|x| > 65504)",

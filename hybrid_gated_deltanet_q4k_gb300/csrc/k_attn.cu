@@ -349,7 +349,7 @@ attn_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUte
         if (ok) {
             t5::fence_after();
             const float inv = 1.0f / (lsum[r] + lsum[ATT_BM + r]);
-            const bool store = q0 + r < a.nq;
+            const bool store = q0 + r < a.nq && GDN_IN_RANGE(g_attn_error, h < a.hq);
             uint16_t* orow = a.o + (static_cast<int64_t>(q0 + r) * a.hq + h) * D;
 #pragma unroll 1
             for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 32) {
@@ -392,7 +392,8 @@ __global__ void __launch_bounds__(256) attn_vt_kernel(const uint16_t* __restrict
     __syncthreads();
     for (int i = threadIdx.x; i < 64 * 64; i += 256) {
         const int e = i >> 6, key = i & 63;
-        if (k0 + key < nk) vt[(static_cast<int64_t>(g) * d + e0 + e) * nkp + k0 + key] = t[e][key];
+        if (k0 + key < nk && GDN_IN_RANGE(g_attn_error, g < hkv && e0 + e < d && k0 + key < nkp))
+            vt[(static_cast<int64_t>(g) * d + e0 + e) * nkp + k0 + key] = t[e][key];
     }
 }
 

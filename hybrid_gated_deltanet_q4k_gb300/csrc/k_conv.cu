@@ -103,7 +103,7 @@ __device__ __forceinline__ void conv_head_tokens(const ConvArgs& a, int head, in
             for (int i = 0; i < CPL; ++i) m = fmaxf_nan(m, fabsf(y[i]));
             over = !(m <= 65504.0f);
         }
-        if (t < t1) {
+        if (t < t1 && GDN_IN_RANGE(g_conv_error, t < a.n && c0 + CPL <= a.c_conv)) {
             uint16_t* dst = a.out + static_cast<int64_t>(t) * a.c_conv + c0;
             if (over) atomicCAS(&g_conv_error, 0, ERR_RANGE);
             const uint32_t p0 = f16x2_bits(y[0], y[1 % CPL]);
@@ -137,6 +137,7 @@ __device__ __forceinline__ void conv_head_run(const ConvArgs& a, int head, int t
         // raw input x_t of channel c0+i; a token before the sequence's first
         // reads its conv state (oldest first)
         if (t >= ts) return bf16_bits_to_float(a.qkvz[static_cast<int64_t>(t) * a.ld_qkvz + c0 + i]);
+        if (!GDN_IN_RANGE(g_conv_error, t - ts >= -3 && c0 + i < a.c_conv)) return 0.0f;
         return tail[static_cast<int64_t>(c0 + i) * 3 + (3 + t - ts)];
     };
 #pragma unroll
@@ -179,8 +180,9 @@ __global__ void __launch_bounds__(CONV_WARPS * 32, 3) conv_kernel(ConvArgs a, co
         const int t = t0 + i / a.hv, h = i % a.hv;
         const float beta = a.ba[static_cast<int64_t>(t) * a.ld_ba + h];
         const float alpha = a.ba[static_cast<int64_t>(t) * a.ld_ba + a.hv + h];
-        gate_values(beta, alpha, a.A_log[h], a.dt_bias[h], a.log_a[static_cast<int64_t>(t) * a.hv + h],
-                    a.b[static_cast<int64_t>(t) * a.hv + h]);
+        if (GDN_IN_RANGE(g_conv_error, t < a.n))
+            gate_values(beta, alpha, a.A_log[h], a.dt_bias[h], a.log_a[static_cast<int64_t>(t) * a.hv + h],
+                        a.b[static_cast<int64_t>(t) * a.hv + h]);
     }
 }
 
@@ -238,6 +240,7 @@ __global__ void conv_state_kernel(const uint16_t* __restrict__ qkvz, int64_t ld,
     const int c = blockIdx.x * blockDim.x + threadIdx.x;
     if (c >= c_conv) return;
     const int s = blockIdx.y, ts = sq.tok[s], n = sq.tok[s + 1] - ts;
+    if (!GDN_IN_RANGE(g_conv_error, s < sq.n)) return;
     float* st = state + static_cast<int64_t>(s) * c_conv * 3;
     float old[3] = {st[c * 3 + 0], st[c * 3 + 1], st[c * 3 + 2]};
     float nw[3];

@@ -410,7 +410,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, G <= 2 ? 4 : 2) gemv_dot_kernel(
                     if (lane == t) mine = sum;
                 }
             }
-            if (lane < a.g) {
+            if (lane < a.g && GDN_IN_RANGE(g_decode_error, row < a.rows)) {
                 const float y = mine * sxs[lane];
                 if (row < a.n_bf16)
                     a.out_bf16[lane * a.ld_bf16 + row] = float_to_bf16_bits(y);
@@ -757,7 +757,7 @@ __global__ void __launch_bounds__(QM_THREADS, 1) gemv_q4k_mma_kernel(QmArgs a) {
         for (int o = tid; o < QM_ROWS * 8 * NT; o += QM_THREADS) {
             const int r = o & (QM_ROWS - 1), t = o / QM_ROWS;
             const int row = tile * QM_ROWS + r;
-            if (t < a.g && row < a.rows) {
+            if (t < a.g && row < a.rows && GDN_IN_RANGE(g_decode_error, tile < a.ntiles)) {
                 const int nt = t >> 3, tt = t & 7;
                 const int li = (r & 7) * 4 + (tt >> 1), c = (r >> 3) * 2 + (tt & 1);
                 float v = 0.0f;

@@ -70,6 +70,7 @@ struct DeltaArgs {
     const float* b;       // [n][hv]
     int n, hv, ratio, c_qk, c_conv, c_v;
     int chunk0, nchunks;  // the chunks [chunk0, chunk0 + nchunks) of this launch (indices are absolute)
+    int nch_total;        // chunks of all sequences: the extent of the scratch tables
     uint16_t* TA;  // [nchunks][hv][2*DC][DC] [A T; T], fp16, in the swizzled operand image
     float* G;      // [nchunks][hv][DC][4]    gamma, e^gamma, b, e^{gamma_C - gamma}
     uint16_t* KT;  // [nchunks][hk][D][DC]    K^T, fp16, in the swizzled operand image
@@ -215,6 +216,7 @@ __global__ void __maxnreg__(88) delta_prep_kernel(const __grid_constant__ CUtens
     const int sq_i = blockIdx.z, local = a.chunk0 + blockIdx.x;
     if (local >= sq.unit[sq_i + 1] - sq.unit[sq_i]) return;
     const int chunk = sq.unit[sq_i] + local, hk = blockIdx.y;
+    if (!GDN_IN_RANGE(g_delta_error, chunk < a.nch_total && (hk + 1) * a.ratio <= a.hv)) return;
     const int t0 = sq.tok[sq_i] + local * DC, t_end = sq.tok[sq_i + 1];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int r = a.ratio;
@@ -612,6 +614,7 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a, con
 
     const int h = blockIdx.x, i0 = blockIdx.y * NV, hk = h / a.ratio;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (!GDN_IN_RANGE(g_delta_error, h < a.hv && i0 + NV <= D)) return;
     const uint32_t sbase = smem_addr(base);
     // chunks chunk0 .. chunk0 + nchunks - 1 of sequence blockIdx.z, those it has
     const int sq_i = blockIdx.z;
@@ -646,6 +649,10 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a, con
             auto cb = [&](int c) { return static_cast<int64_t>(c) * a.hv + h; };
             for (int j = 0; j < nch; ++j) {
                 const int c = cg0 + j, tc = tc0 + j * DC;
+                if (!GDN_IN_RANGE(g_delta_error, c < a.nch_total)) {
+                    *abort = 1;
+                    break;
+                }
                 const uint32_t pp = (j - 1) & 1;   // phase of the previous chunk's release
                 if (j >= 1 && !state_wait(bars + E_QK, pp, abort)) break;
                 mbar_expect_tx(bars + F_QK, 2 * L::NSLAB * L::SLAB);
@@ -838,7 +845,7 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a, con
                 float y[16], z[16];
                 t5::ld16x2(tl + TM_XY + 32 * ph, y, tl + TM_DZ, z);
                 const int t = tc + tok;
-                if (t < t_end) {
+                if (t < t_end && GDN_IN_RANGE(g_delta_error, t < a.n && h * D + i0 + v0 + 16 <= a.c_v)) {
                     float ov[2][8];
 #pragma unroll
                     for (int v = 0; v < 16; ++v) {
@@ -1033,6 +1040,7 @@ cudaError_t launch_delta(const gdn_layer& L, const uint16_t* qkv, const float* l
     a.chunk0 = 0;
     a.nchunks = 0;
     const int64_t nch = sq.unit[sq.n];   // chunks of all sequences: the scratch tables' extent
+    a.nch_total = static_cast<int>(nch);
     unsigned char* base = static_cast<unsigned char*>(scratch);
     a.TA = reinterpret_cast<uint16_t*>(base);
     a.G = reinterpret_cast<float*>(base + nch * a.hv * 2 * DC * DC * 2);

@@ -194,6 +194,7 @@ struct GemmArgs {
 };
 
 __device__ __forceinline__ void store_group8(const GemmArgs& g, int row, int n, const float* y) {
+    if (!GDN_IN_RANGE(g_gemm_error, row < g.M && n < g.N)) return;
     if (g.vec_ok && n + 8 <= g.N && n + 8 <= g.n_bf16) {
         uint32_t w[4];
 #pragma unroll

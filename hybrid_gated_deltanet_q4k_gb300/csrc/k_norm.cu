@@ -23,12 +23,13 @@ constexpr int NORM_THREADS = 256;
 // enough for 6 CTAs per SM and so enough loads in flight to cover HBM latency.
 template <int CPL, bool QUANT, int HPW>
 __global__ void __launch_bounds__(NORM_THREADS, HPW <= 4 ? 6 : 4)
-gated_norm_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ z, int64_t ld_z, int hv,
+gated_norm_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ z, int64_t ld_z, int hv, int64_t n,
                   const float* __restrict__ norm_w, float eps, uint16_t* __restrict__ codes,
                   float* __restrict__ scale, float* __restrict__ out_f32) {
     __shared__ float red[32];
     constexpr int D = CPL * 32;
     const int64_t t = blockIdx.x;
+    if (!GDN_IN_RANGE(g_norm_error, t < n)) return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c_v = hv * D;
     float wv[CPL];
@@ -257,15 +258,16 @@ int read_and_clear_norm_error() {
 template <int CPL, bool QUANT>
 static void launch_norm_hpw(const gdn_layer& L, const uint16_t* o, const uint16_t* z, int64_t ld_z, unsigned grid,
                             uint16_t* codes, float* scale, float* out_f32, cudaStream_t st) {
+    const int64_t n = grid;
     const int hpw = (L.n_v_heads + 7) / 8;
     if (hpw <= 1)
-        gated_norm_kernel<CPL, QUANT, 1><<<grid, NORM_THREADS, 0, st>>>(o, z, ld_z, L.n_v_heads, L.norm_w, L.eps_rms, codes, scale, out_f32);
+        gated_norm_kernel<CPL, QUANT, 1><<<grid, NORM_THREADS, 0, st>>>(o, z, ld_z, L.n_v_heads, n, L.norm_w, L.eps_rms, codes, scale, out_f32);
     else if (hpw <= 2)
-        gated_norm_kernel<CPL, QUANT, 2><<<grid, NORM_THREADS, 0, st>>>(o, z, ld_z, L.n_v_heads, L.norm_w, L.eps_rms, codes, scale, out_f32);
+        gated_norm_kernel<CPL, QUANT, 2><<<grid, NORM_THREADS, 0, st>>>(o, z, ld_z, L.n_v_heads, n, L.norm_w, L.eps_rms, codes, scale, out_f32);
     else if (hpw <= 4)
-        gated_norm_kernel<CPL, QUANT, 4><<<grid, NORM_THREADS, 0, st>>>(o, z, ld_z, L.n_v_heads, L.norm_w, L.eps_rms, codes, scale, out_f32);
+        gated_norm_kernel<CPL, QUANT, 4><<<grid, NORM_THREADS, 0, st>>>(o, z, ld_z, L.n_v_heads, n, L.norm_w, L.eps_rms, codes, scale, out_f32);
     else
-        gated_norm_kernel<CPL, QUANT, 8><<<grid, NORM_THREADS, 0, st>>>(o, z, ld_z, L.n_v_heads, L.norm_w, L.eps_rms, codes, scale, out_f32);
+        gated_norm_kernel<CPL, QUANT, 8><<<grid, NORM_THREADS, 0, st>>>(o, z, ld_z, L.n_v_heads, n, L.norm_w, L.eps_rms, codes, scale, out_f32);
 }
 
 cudaError_t launch_gated_norm(const gdn_layer& L, const uint16_t* o, const uint16_t* z, int64_t ld_z, int64_t n,

@@ -18,6 +18,8 @@
 
 namespace gdn {
 
+static __device__ int g_q4k_error;   // index checks of the debug build
+
 // One warp per weight row: in iteration i the warp decodes superblock i, lane
 // l the 8 weights 8l .. 8l+7 (sub-block l/4, the low or high nibbles of 8 code
 // bytes).  Pass 1 finds the row amax without decoding every weight: d*sc*q -
@@ -59,14 +61,14 @@ q4k_deq_rows_warp_kernel(DeqJob<OutT> j0, DeqJob<OutT> j1) {
     for (int i = 0; i < nsb; ++i) amax = fmaxf(amax, Q4KLane::amax(rb + i * 144, lane));
     amax = warp_max(amax);
     const QScale qsc = make_qscale(amax);
-    if (lane == 0) j.scale[row] = qsc.s;
+    if (lane == 0 && GDN_IN_RANGE(g_q4k_error, row < j.rows)) j.scale[row] = qsc.s;
     OutT* out = j.codes + row * static_cast<int64_t>(j.cols) + lane * 8;
 #pragma unroll 4
     for (int i = 0; i < nsb; ++i) {
         float w[8], c[8];
         Q4KLane::decode(rb + i * 144, lane, w);
         quantise8(w, qsc, c);
-        store_codes8<OutT>(out + i * 256, c);
+        if (GDN_IN_RANGE(g_q4k_error, i * 256 + lane * 8 + 8 <= j.cols)) store_codes8<OutT>(out + i * 256, c);
     }
 }
 
@@ -97,6 +99,13 @@ cudaError_t launch_q4k_deq_codes2(const void* b0, int64_t rows0, int64_t cols0, 
     const DeqJob<uint16_t> j0{static_cast<const uint8_t*>(b0), rows0, static_cast<int>(cols0), q0, s0};
     const DeqJob<uint16_t> j1{static_cast<const uint8_t*>(b1), rows1, static_cast<int>(cols1), q1, s1};
     return launch_deq<uint16_t>(j0, j1, st);
+}
+
+int read_and_clear_q4k_error() {
+    int v = 0, z = 0;
+    cudaMemcpyFromSymbol(&v, g_q4k_error, sizeof(int));
+    if (v) cudaMemcpyToSymbol(g_q4k_error, &z, sizeof(int));
+    return v;
 }
 
 }  // namespace gdn

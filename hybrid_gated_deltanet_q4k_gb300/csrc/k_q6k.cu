@@ -26,6 +26,8 @@
 
 namespace gdn {
 
+static __device__ int g_q6k_error;   // index checks of the debug build
+
 constexpr int Q6_THREADS = 256;
 constexpr int Q6_BLOCK = 210;
 
@@ -51,14 +53,14 @@ __global__ void __launch_bounds__(Q6_THREADS, 4) q6k_deq_rows_warp_kernel(Q6Job<
     for (int i = 0; i < nsb; ++i) amax = fmaxf(amax, Q6KLane::amax(rb + i * Q6_BLOCK, lane));
     amax = warp_max(amax);
     const QScale qsc = make_qscale(amax);
-    if (lane == 0) j.scale[row] = qsc.s;
+    if (lane == 0 && GDN_IN_RANGE(g_q6k_error, row < j.rows)) j.scale[row] = qsc.s;
     OutT* out = j.codes + row * static_cast<int64_t>(j.cols) + lane * 8;
 #pragma unroll 4
     for (int i = 0; i < nsb; ++i) {
         float w[8], c[8];
         Q6KLane::decode(rb + i * Q6_BLOCK, lane, w);
         quantise8(w, qsc, c);
-        store_codes8<OutT>(out + i * 256, c);
+        if (GDN_IN_RANGE(g_q6k_error, i * 256 + lane * 8 + 8 <= j.cols)) store_codes8<OutT>(out + i * 256, c);
     }
 }
 
@@ -77,6 +79,13 @@ cudaError_t launch_q6k_deq_i8(const void* blocks, int64_t rows, int64_t cols, in
 cudaError_t launch_q6k_deq_codes(const void* blocks, int64_t rows, int64_t cols, uint16_t* q, float* s,
                                  cudaStream_t st) {
     return launch_q6k<uint16_t>(blocks, rows, cols, q, s, st);
+}
+
+int read_and_clear_q6k_error() {
+    int v = 0, z = 0;
+    cudaMemcpyFromSymbol(&v, g_q6k_error, sizeof(int));
+    if (v) cudaMemcpyToSymbol(g_q6k_error, &z, sizeof(int));
+    return v;
 }
 
 }  // namespace gdn

@@ -13,11 +13,13 @@
 
 namespace gdn {
 
+static __device__ int g_quant_error;   // index checks of the debug build
+
 constexpr int QR_VEC = 8;   // 16-byte vectors per thread
 
 template <int THREADS>
 __global__ void __launch_bounds__(THREADS)
-quant_rows_bf16_kernel(const uint16_t* __restrict__ x, int cols, uint16_t* __restrict__ codes,
+quant_rows_bf16_kernel(const uint16_t* __restrict__ x, int64_t rows, int cols, uint16_t* __restrict__ codes,
                        float* __restrict__ scale) {
     pdl_trigger();
     __shared__ float red[32];
@@ -44,12 +46,13 @@ quant_rows_bf16_kernel(const uint16_t* __restrict__ x, int cols, uint16_t* __res
     }
     amax = block_max(amax, red);
     const QScale qsc = make_qscale(amax);
-    if (threadIdx.x == 0) scale[row] = qsc.s;
+    const bool row_ok = GDN_IN_RANGE(g_quant_error, row < rows);
+    if (threadIdx.x == 0 && row_ok) scale[row] = qsc.s;
     uint4* dst = reinterpret_cast<uint4*>(codes + row * cols);
 #pragma unroll
     for (int i = 0; i < QR_VEC; ++i) {
         const int j = threadIdx.x + i * THREADS;
-        if (j < nvec) {
+        if (j < nvec && row_ok) {
             const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
             float xv[8], c[8];
             bool redo = !qsc.fast;
@@ -74,10 +77,17 @@ cudaError_t launch_quant_rows(const uint16_t* x, int64_t rows, int64_t cols, uin
                               cudaStream_t st) {
     static_assert(16384 / 8 <= QR_VEC * 256, "the widest row must fit a 256-thread CTA");
     if (cols <= QR_VEC * 64 * 8)
-        quant_rows_bf16_kernel<64><<<static_cast<unsigned>(rows), 64, 0, st>>>(x, static_cast<int>(cols), codes, scale);
+        quant_rows_bf16_kernel<64><<<static_cast<unsigned>(rows), 64, 0, st>>>(x, rows, static_cast<int>(cols), codes, scale);
     else
-        quant_rows_bf16_kernel<256><<<static_cast<unsigned>(rows), 256, 0, st>>>(x, static_cast<int>(cols), codes, scale);
+        quant_rows_bf16_kernel<256><<<static_cast<unsigned>(rows), 256, 0, st>>>(x, rows, static_cast<int>(cols), codes, scale);
     return cudaGetLastError();
+}
+
+int read_and_clear_quant_error() {
+    int v = 0, z = 0;
+    cudaMemcpyFromSymbol(&v, g_quant_error, sizeof(int));
+    if (v) cudaMemcpyToSymbol(g_quant_error, &z, sizeof(int));
+    return v;
 }
 
 }  // namespace gdn

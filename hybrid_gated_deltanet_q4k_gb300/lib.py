@@ -15,7 +15,7 @@ from . import build as _build
 
 c_int32, c_int64, c_float, c_void_p, c_size_t = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
 
-GDN_OK, GDN_EINVAL, GDN_ENOMEM, GDN_ECUDA, GDN_ETIMEOUT, GDN_ERANGE = 0, -1, -2, -3, -4, -5
+GDN_OK, GDN_EINVAL, GDN_ENOMEM, GDN_ECUDA, GDN_ETIMEOUT, GDN_ERANGE, GDN_EINDEX = 0, -1, -2, -3, -4, -5, -6
 GDN_W_Q4K, GDN_W_F32 = 0, 1
 GDN_CHUNK = 64
 GDN_MAX_SEQS = 256
@@ -113,18 +113,23 @@ class Lib:
         raise AttributeError(name)
 
 
-_LIB = None
+_LIBS = {}
 
 
-def load(build: bool = False) -> Lib:
-    """Load ``_lib/libgdn.so`` (building it first if ``build``)."""
-    global _LIB
-    if _LIB is None:
-        path = _build.build() if build else _build.LIB
+def load(build: bool = False, debug: bool = False) -> Lib:
+    """Load ``_lib/libgdn.so`` (building it first if ``build``), or with
+    ``debug`` its debug variant ``_lib/libgdn_debug.so``: the same kernels with
+    every global store's index checked (a failed check is skipped and reported
+    by gdn_sync_status as GDN_EINDEX).  The two are separate libraries with
+    separate device state; both may be loaded at once."""
+    if debug not in _LIBS:
+        if build:
+            _build.build()
+        path = _build.DEBUG_LIB if debug else _build.LIB
         if not os.path.exists(path):
             raise RuntimeError(f"libgdn is not built ({path} missing): run hybrid_gated_deltanet_q4k_gb300/build.py")
-        _LIB = Lib(path)
-    return _LIB
+        _LIBS[debug] = Lib(path)
+    return _LIBS[debug]
 
 
 def ptr(t) -> int:

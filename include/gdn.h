@@ -63,6 +63,7 @@ extern "C" {
 #define GDN_ECUDA (-3)    /* a CUDA call or kernel launch failed */
 #define GDN_ETIMEOUT (-4) /* a bounded device-side wait ran out; the kernel returned early */
 #define GDN_ERANGE (-5)   /* a value beyond the fp16 operand range (|x| > 65504) reached the recurrence */
+#define GDN_EINDEX (-6)   /* debug library only: a kernel's index check failed (the store was skipped) */
 
 #define GDN_W_Q4K 0 /* weights are GGUF Q4_K superblocks, activations bf16 */
 #define GDN_W_F32 1 /* weights and activations fp32, no quantisation anywhere */

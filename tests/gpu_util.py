@@ -62,3 +62,38 @@ def stream() -> int:
 
 def sync(L):
     assert L.gdn_sync_status(stream(), check=False) == gl.GDN_OK, L.last_error()
+
+
+class Guarded:
+    """A device buffer of n_bytes between two guard regions filled with a
+    sentinel byte, so that any write outside the buffer shows up as a changed
+    guard byte (the tests' substitute for a sanitizer).  The buffer starts
+    4096 bytes into the allocation, so it keeps the allocation's alignment."""
+
+    GUARD = 4096
+    FILL = 0xA5
+
+    def __init__(self, n_bytes: int, fill_inside: int | None = None):
+        self.n = int(n_bytes)
+        self.raw = torch.full((self.GUARD + self.n + self.GUARD,), self.FILL, dtype=torch.uint8, device=DEV)
+        if fill_inside is not None:
+            self.raw[self.GUARD:self.GUARD + self.n] = fill_inside
+
+    def view(self, dtype: torch.dtype, shape) -> torch.Tensor:
+        return self.raw[self.GUARD:self.GUARD + self.n].view(dtype).view(shape)
+
+    def intact(self) -> bool:
+        return bool((self.raw[:self.GUARD] == self.FILL).all().item()) and bool(
+            (self.raw[self.GUARD + self.n:] == self.FILL).all().item())
+
+
+def guarded(shape, dtype: torch.dtype, init: torch.Tensor | None = None):
+    """(Guarded, view) for a tensor of this shape and dtype, optionally copied from init."""
+    n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+    g = Guarded(n)
+    v = g.view(dtype, shape)
+    if init is not None:
+        v.copy_(init)
+    else:
+        v.zero_()
+    return g, v

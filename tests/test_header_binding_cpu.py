@@ -27,7 +27,7 @@ def _defines():
 
 def test_constants_match_the_header():
     d = _defines()
-    for name in ("GDN_OK", "GDN_EINVAL", "GDN_ENOMEM", "GDN_ECUDA", "GDN_ETIMEOUT", "GDN_ERANGE", "GDN_W_Q4K",
+    for name in ("GDN_OK", "GDN_EINVAL", "GDN_ENOMEM", "GDN_ECUDA", "GDN_ETIMEOUT", "GDN_ERANGE", "GDN_EINDEX", "GDN_W_Q4K",
                  "GDN_W_F32", "GDN_CHUNK", "GDN_MAX_SEQS", "GDN_N_STAGE_EVENTS", "GDN_NOALLOC_SCRATCH_BYTES"):
         assert name in d, name
         assert getattr(gl, name) == d[name], name
