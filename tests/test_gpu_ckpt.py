@@ -13,7 +13,9 @@ from hybrid_gated_deltanet_q4k_gb300 import lib as gl
 from hybrid_gated_deltanet_q4k_gb300 import synth
 from hybrid_gated_deltanet_q4k_gb300.api import DeviceLayer
 
-from gpu_util import DEV, bf16_dev, f32_dev, sync
+from oracle import layer as OL
+
+from gpu_util import DEV, bf16_dev, bf16_host_f32, f32_dev, oracle_params, rel_l2, sync
 
 pytestmark = pytest.mark.gpu
 
@@ -65,6 +67,38 @@ def test_snapshots_equal_prefix_prefills(spec_name, n, every, ws_tokens):
         sync(dl.lib)
         assert torch.equal(yr.view(torch.int16), yf[p:].view(torch.int16))
         assert torch.equal(sr, sf) and torch.equal(cr, cf)
+
+
+@pytest.mark.parametrize("n,every", [(700, 256), (1000, 192)])
+def test_oracle_resumed_from_a_snapshot_continues_the_prompt(n, every):
+    """A GPU snapshot handed to the oracle: the oracle, started from snapshot k
+    (its state and conv tail, fp32 values taken exactly), runs the rest of the
+    prompt, and its outputs and final state agree with the GPU's full prefill
+    within the end-to-end tolerances (y 1e-2 through the int8 projections, the
+    state 2e-3 of the recurrence).  So a snapshot is a state the method can
+    resume from, not only a copy of the GPU's own prefix prefill."""
+    spec = SMALL
+    layer = synth.make_layer(spec)
+    tok = synth.make_tokens(spec, n, seed=n + 7 * every)
+    dl = DeviceLayer(spec, layer)
+    k = n // every
+    cs = torch.empty(k, spec.n_v_heads, spec.dv, spec.dk, device=DEV)
+    cc = torch.empty(k, spec.c_conv, 3, device=DEV)
+    state, conv = dl.new_state()
+    y = torch.empty(n, spec.hidden, dtype=torch.bfloat16, device=DEV)
+    dl.prefill_ckpt(_x(tok, 0, n), None, state, conv, y, dl.new_workspace(n), every, cs, cc,
+                    gate_log_a=f32_dev(tok["log_a"]), gate_b=f32_dev(tok["b"]))
+    sync(dl.lib)
+    p = oracle_params(spec, layer)
+    yh = bf16_host_f32(y)
+    for j in (0, k - 1):
+        t0 = (j + 1) * every
+        ref = OL.layer_forward(p, tok["x"][t0:], S0=cs[j].cpu().numpy().astype(np.float64),
+                               conv_tail=cc[j].cpu().numpy().astype(np.float64),
+                               gate_log_a=tok["log_a"][t0:], gate_b=tok["b"][t0:])
+        assert rel_l2(yh[t0:], ref["y"]) <= 1e-2, j
+        assert rel_l2(state.cpu().numpy(), ref["state"]) <= 2e-3, j
+        assert np.array_equal(conv.cpu().numpy(), ref["conv_tail"].astype(np.float32)), j
 
 
 def test_ckpt_argument_checks():

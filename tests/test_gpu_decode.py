@@ -87,7 +87,8 @@ def _saved_states(spec, n, seed):
 
 
 @pytest.mark.parametrize("name,n,gates,q6", [("small", 1, True, ()), ("small", 5, False, ()),
-                                              ("small", 11, True, ("w_out",)), ("h2560", 3, True, ()),
+                                              ("small", 11, True, ("w_out",)), ("small", 1, False, ("w_in", "w_out")),
+                                              ("h2560", 3, True, ()), ("h2560", 1, True, ()),
                                               ("tiny_f32", 4, True, ())])
 def test_decode_step_matches_oracle(name, n, gates, q6):
     spec = SMALL if name == "small" else synth.SPECS[name]
@@ -162,12 +163,16 @@ def test_prefill_then_decode_matches_oracle_prefill():
     assert rel_l2(state.cpu().numpy(), full["state"]) <= 3e-2
 
 
-def test_decode_batch_equals_each_sequence_alone():
+@pytest.mark.parametrize("q6", [(), ("w_in", "w_out")])
+def test_decode_batch_equals_each_sequence_alone(q6):
+    """One sequence alone takes the one-token projection kernels; 13 take two
+    launches of the batched ones (8 + 5 tokens).  Every sequence's results are
+    the same bits, for Q4_K and for Q6_K projections."""
     spec = synth.SPECS["h2560"]
     layer = synth.make_layer(spec)
-    n = 13                                     # two launches of the projection (8 + 5 tokens)
+    n = 13
     tok = synth.make_tokens(spec, n, seed=5)
-    dl = DeviceLayer(spec, layer)
+    dl = DeviceLayer(spec, layer, q6k=q6)
     st0, cv0 = _saved_states(spec, n, seed=9)
     sb, cb = torch.from_numpy(st0).to(DEV), torch.from_numpy(cv0).to(DEV)
     yb = torch.empty(n, spec.hidden, dtype=torch.bfloat16, device=DEV)
