@@ -10,6 +10,7 @@
 // writes each code once.  Rows of up to 4096 values take 64-thread CTAs (two
 // warps per row, up to 32 rows resident per SM), longer rows 256 threads.
 #include "common.cuh"
+#include "qk_decode.cuh"
 
 namespace gdn {
 
@@ -55,18 +56,12 @@ quant_rows_bf16_kernel(const uint16_t* __restrict__ x, int64_t rows, int cols, u
         if (j < nvec && row_ok) {
             const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
             float xv[8], c[8];
-            bool redo = !qsc.fast;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 xv[2 * e] = __uint_as_float(w[e] << 16);
                 xv[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
             }
-#pragma unroll
-            for (int e = 0; e < 8; ++e) c[e] = qcode_fast(xv[e], qsc, redo);
-            if (redo) {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) c[e] = qcode_exact(xv[e], qsc.s);
-            }
+            quantise8(xv, qsc, c);
             dst[j] = make_uint4(codes_to_f16x2(c[0], c[1]), codes_to_f16x2(c[2], c[3]), codes_to_f16x2(c[4], c[5]),
                                 codes_to_f16x2(c[6], c[7]));
         }

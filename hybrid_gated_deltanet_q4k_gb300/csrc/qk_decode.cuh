@@ -80,12 +80,18 @@ struct Q4KLaneT {
         const uint2 qs = ldq<G>(reinterpret_cast<const uint2*>(blk + 16 + 32 * p + l0));
         float ds, dm;
         q4k_sub_affine(hdr, sub, ds, dm);
-        // the lane's 8 nibbles, one per byte, then each byte as 2^23 + q (byte permutes)
+        // the lane's 8 nibbles, one per byte, then each byte as 2^23 + q (byte
+        // permutes); q = (2^23 + q) - 2^23 and the fma on the packed f32x2
+        // instructions, two weights at a time (each half rounds as the scalar
+        // instruction would)
         const uint32_t n0 = (qs.x >> shift) & 0x0f0f0f0fu, n1 = (qs.y >> shift) & 0x0f0f0f0fu;
+        const F2 two23 = f2(8388608.0f, 8388608.0f), ds2 = f2(ds, ds), ndm2 = f2(-dm, -dm);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const uint32_t bits = __byte_perm(e < 4 ? n0 : n1, 0x4B000000u, 0x7440 + (e & 3));
-            w[e] = __fmaf_rn(ds, __fsub_rn(__uint_as_float(bits), 8388608.0f), -dm);
+        for (int e = 0; e < 8; e += 2) {
+            const uint32_t b0 = __byte_perm(e < 4 ? n0 : n1, 0x4B000000u, 0x7440 + (e & 3));
+            const uint32_t b1 = __byte_perm(e < 4 ? n0 : n1, 0x4B000000u, 0x7440 + ((e + 1) & 3));
+            const F2 q = f2_sub(f2(__uint_as_float(b0), __uint_as_float(b1)), two23);
+            f2_split(f2_fma(ds2, q, ndm2), w[e], w[e + 1]);
         }
     }
 };
@@ -131,9 +137,14 @@ struct Q6KLaneT {
         uint32_t c[8];
         float ds;
         q6k_lane<G>(blk, lane, c, ds);
-        // c - 32 exactly: (2^23 + c) - (2^23 + 32); the product with d*scale is exact
+        // c - 32 exactly: (2^23 + c) - (2^23 + 32); the product with d*scale is
+        // exact (packed f32x2 instructions, two weights at a time)
+        const F2 off = f2(8388640.0f, 8388640.0f), ds2 = f2(ds, ds);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) w[e] = __fmul_rn(ds, __fsub_rn(__uint_as_float(0x4B000000u | c[e]), 8388640.0f));
+        for (int e = 0; e < 8; e += 2) {
+            const F2 cm = f2_sub(f2(__uint_as_float(0x4B000000u | c[e]), __uint_as_float(0x4B000000u | c[e + 1])), off);
+            f2_split(f2_mul(ds2, cm), w[e], w[e + 1]);
+        }
     }
 };
 using Q6KLane = Q6KLaneT<true>;
@@ -141,10 +152,20 @@ using Q6KLane = Q6KLaneT<true>;
 // The int8 codes of 8 decoded weights for the row's scale, as magic floats:
 // the fast quantiser, with the exact fallback where it may round differently
 // (results equal qcode_exact for every weight).
+// The fast path is qcode_fast on the packed f32x2 instructions, two weights
+// at a time: the same roundings, so the same codes and the same fallbacks.
 __device__ __forceinline__ void quantise8(const float (&w)[8], const QScale& qsc, float (&c)[8]) {
     bool redo = !qsc.fast;
+    const F2 rs = f2(qsc.rs, qsc.rs), mg = f2(QCODE_MAGIC, QCODE_MAGIC);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) c[e] = qcode_fast(w[e], qsc, redo);
+    for (int e = 0; e < 8; e += 2) {
+        const F2 y = f2_mul(f2(w[e], w[e + 1]), rs);
+        const F2 t = f2_add(y, mg);
+        float d0, d1;
+        f2_split(f2_sub(y, f2_sub(t, mg)), d0, d1);
+        redo |= !(fabsf(d0) <= 0.499f) || !(fabsf(d1) <= 0.499f);
+        f2_split(t, c[e], c[e + 1]);
+    }
     if (redo) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) c[e] = qcode_exact(w[e], qsc.s);
