@@ -258,7 +258,7 @@ __device__ __forceinline__ float conv4_silu(const float4 w, float xm3, float xm2
 }
 
 // Two fp32 values in one 64-bit register pair, for the packed fp32
-// instructions (mul / add / fma .rn.f32x2: each half rounds as the scalar
+// instructions (mul / add / sub / fma .rn.f32x2: each half rounds as the scalar
 // instruction does, so a packed evaluation gives the scalar one's bits).
 struct F2 {
     unsigned long long v;
