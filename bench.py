@@ -513,8 +513,28 @@ def run_stage(args, spec):
     torch.cuda.synchronize()
     assert L.gdn_sync_status(st, check=False) == 0, L.last_error()
     ms = e0.elapsed_time(e1) / args.steps
-    print(json.dumps({"stage": args.stage, "workload": spec.workload, "tokens": n, "ms_per_launch": ms,
-                      "rate": work / (ms / 1e3), "rate_unit": unit + "/s"}), flush=True)
+    rate = work / (ms / 1e3)
+    out = {"stage": args.stage, "workload": spec.workload, "tokens": n, "ms_per_launch": ms, "rate": rate,
+           "rate_unit": unit + "/s"}
+    pk = peaks()
+    if unit == "GB":
+        out["roofline"] = {"bound": "hbm", "achieved": rate, "peak": pk["hbm"], "unit": "GB/s",
+                           "frac": rate / pk["hbm"], "peak_source": pk["src"]}
+        # the oracle beside it: the same decode and quantisation of the first 256 rows
+        from oracle import q4k as O4, q6k as O6, quant as OQ
+        rs = 256
+        fmt = O6 if args.stage == "q6k_deq" else O4
+        blk = (O6.pack_q6k if args.stage == "q6k_deq" else O4.pack_q4k)(layer["w_in"][:rs])
+        t0 = time.perf_counter()
+        w = (O6.unpack_q6k if args.stage == "q6k_deq" else O4.unpack_q4k)(blk, rs, H)
+        OQ.quant_rows_i8(w)
+        t_or = time.perf_counter() - t0
+        out["cpu_baseline"] = {"value": (blk.nbytes + rs * H + 4 * rs) / 1e9 / t_or, "unit": "GB/s", "cores": _CORES,
+                               "kind": "oracle", "sample": f"the first {rs} rows of W_in ({fmt.__name__}: decode, int8 rows)"}
+    elif unit == "TFLOP":
+        out["roofline"] = {"bound": "tensor", "achieved": rate, "peak": pk["tensor"], "unit": "TFLOP/s",
+                           "frac": rate / pk["tensor"], "peak_source": pk["src"]}
+    print(json.dumps(out), flush=True)
 
 
 def run_extend(args, spec):
@@ -571,9 +591,30 @@ def run_extend(args, spec):
         assert L.gdn_sync_status(stream.cuda_stream, check=False) == 0, L.last_error()
         ms = e0.elapsed_time(e1) / args.steps
         res[name] = {"ms_per_step": ms, "value": T / (ms / 1e3)}
+    # whole-call tensor roofline: the two projections' FLOPs over the batch call
+    pk = peaks()
+    tflop = 2.0 * T * (spec.r_in * spec.hidden + spec.hidden * spec.c_v) / 1e12
+    tf = tflop / (res["batch"]["ms_per_step"] / 1e3)
+    roofline = {"bound": "tensor", "achieved": tf, "peak": pk["tensor"], "unit": "TFLOP/s", "frac": tf / pk["tensor"],
+                "peak_source": pk["src"],
+                "work": f"both projections, {tflop:.3f} TFLOP per call, over the whole call's time (conv and delta "
+                        "rule included: a lower bound on the projections' own rate)"}
+    # the oracle beside it: the first 128 tokens of the first extension, from its saved state
+    from oracle import layer as OL
+    ns = min(128, ext[0])
+    c0 = cases[0]
+    t0 = time.perf_counter()
+    OL.layer_forward(oracle_params(spec, layer), c0["x"][pre:pre + ns], S0=s_saved[0].cpu().numpy().astype(np.float64),
+                     conv_tail=c_saved[0].cpu().numpy().astype(np.float64), gate_log_a=c0["log_a"][pre:pre + ns],
+                     gate_b=c0["b"][pre:pre + ns])
+    t_or = time.perf_counter() - t0
+    cpu = {"value": ns / t_or, "unit": UNIT, "cores": _CORES, "kind": "oracle",
+           "sample": f"the first {ns} tokens of the first sequence's extension, from its saved state (one call: "
+                     "weight decode, fp64 projections on the exact int8 operands, recurrence one token at a time)"}
     print(json.dumps({"metric": "GDN-layer extend tokens/s, 8 sequences (1 GB300)", "unit": UNIT,
                       "value": res["batch"]["value"], "ms_per_step": res["batch"]["ms_per_step"],
                       "per_sequence_calls": res["per_sequence"], "steps": args.steps, "warmup": max(args.warmup, 3),
+                      "roofline": roofline, "cpu_baseline": cpu,
                       "dtype": "int8", "data": "synthetic",
                       "config": {"workload": "extend_h2560_8seq", "hidden": spec.hidden, "prefix": pre,
                                  "extensions": ext, "tokens": T, "call": "gdn_prefill_batch"}}), flush=True)
@@ -635,9 +676,21 @@ def run_decode(args, spec):
         rows.append({"n_seqs": B, "us_per_step": us, "l2": "flushed before each step",
                      "us_per_step_l2_warm": us_warm, "tokens_per_s": B / (us * 1e-6), "hbm_bytes": wbytes + sbytes,
                      "achieved_gbs": gbs, "frac": gbs / pk["hbm"]})
+    # the oracle beside it: one decode step of one sequence (weights decoded each call)
+    from oracle import layer as OL
+    tok = synth.make_tokens(spec, 1, seed=91)
+    rng = np.random.default_rng(1)
+    s0 = rng.normal(0, 0.05, size=(spec.n_v_heads, spec.dv, spec.dk))
+    t0 = time.perf_counter()
+    OL.layer_forward(oracle_params(spec, layer), tok["x"][:1], S0=s0, conv_tail=np.zeros((spec.c_conv, 3)),
+                     gate_log_a=tok["log_a"][:1], gate_b=tok["b"][:1], decode=True)
+    t_or = time.perf_counter() - t0
+    cpu = {"value": 1.0 / t_or, "unit": "tokens/s", "us_per_step": t_or * 1e6, "cores": _CORES, "kind": "oracle",
+           "sample": "one decode step of one sequence (B = 1): Q4_K decode of both matrices, fp64 products on the "
+                     "exact int8 operands, one token of the recurrence"}
     print(json.dumps({"metric": "GDN-layer decode step (1 GB300)", "workload": spec.workload, "steps": args.steps,
-                      "peak_gbs": pk["hbm"], "peak_source": pk["src"], "rows": rows, "dtype": "int8",
-                      "data": "synthetic", "call": "gdn_decode"}), flush=True)
+                      "peak_gbs": pk["hbm"], "peak_source": pk["src"], "rows": rows, "cpu_baseline": cpu,
+                      "dtype": "int8", "data": "synthetic", "call": "gdn_decode"}), flush=True)
 
 
 def run_attn(args):
@@ -679,8 +732,21 @@ def run_attn(args):
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     peak = json.load(open(path))["bf16_tflops"] if os.path.exists(path) else 1900.0
     tf = flops / (ms / 1e3) / 1e12
+    # the oracle beside it: the last 16 queries (the longest rows) against all keys,
+    # scaled to tokens/s of the causal prefill by FLOPs (an average query does
+    # (n + 1) / 2 of the n key products these do)
+    from oracle.attention import attention as oracle_attention
+    ns = min(16, n)
+    t0 = time.perf_counter()
+    oracle_attention(inp["q"][n - ns:], inp["k"], inp["v"])
+    t_or = time.perf_counter() - t0
+    f_sample = 4.0 * d * hq * ns * n
+    cpu = {"value": f_sample / t_or / (flops / n), "unit": "tokens/s", "tflops": f_sample / t_or / 1e12,
+           "cores": _CORES, "kind": "oracle",
+           "sample": f"the last {ns} queries against all {n} keys, fp64 (tokens/s of the causal prefill at the same "
+                     "FLOP rate)"}
     print(json.dumps({"metric": "full-attention layer prefill tokens/s (1 GB300)", "unit": "tokens/s",
-                      "value": n / (ms / 1e3), "ms_per_step": ms, "steps": args.steps,
+                      "value": n / (ms / 1e3), "ms_per_step": ms, "steps": args.steps, "cpu_baseline": cpu,
                       "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
                                    "peak_source": "of measured (MEASURED_PEAKS.json bf16_tflops, burst)"},
                       "dtype": "bf16", "data": "synthetic",
