@@ -632,12 +632,29 @@ int gdn_prefill_host(const gdn_layer* layer, const void* x_host, int64_t n_token
             gas[i] = reinterpret_cast<float*>(stage + 4 * xb + (2 * i) * gbytes);
             gbs[i] = reinterpret_cast<float*>(stage + 4 * xb + (2 * i + 1) * gbytes);
         }
-    // Pass boundaries: passes of B tokens, except that the first and the last
-    // are a quarter of B when B is a whole number of 4 chunks and there is more
-    // than one pass -- the copy-in of the first pass and the copy-out of the
-    // last are the ones nothing hides.  Every boundary is a chunk boundary.
+    // Pass boundaries, every one a chunk boundary.  The copy-in of the first
+    // pass and the copy-out of the last are the ones nothing hides, so those
+    // passes are short.  A pass's copy-in takes about a third of the time its
+    // tokens take to compute, so when B is a whole number of 8 chunks and the
+    // prompt holds the ramps, the passes grow B/8, 3B/8, up to B, and shrink
+    // 3B/8, B/8 again (the ragged tail, if any, in the last one); otherwise
+    // passes of B, the first and the last B/4 when B is a whole number of 4
+    // chunks and there is more than one pass.
     std::vector<int64_t> bounds{0};
-    {
+    const int64_t e1 = B / 8, e2 = 3 * (B / 8);
+    const int64_t n_whole = n_tokens - n_tokens % GDN_CHUNK;
+    if (n_tokens > B && B % (8 * GDN_CHUNK) == 0 && n_whole >= 2 * (e1 + e2)) {
+        int64_t t = 0;
+        for (int64_t len : {e1, e2}) bounds.push_back(t += len);
+        const int64_t mid = n_whole - 2 * (e1 + e2);
+        if (mid > 0) {
+            const int64_t k = (mid + B - 1) / B;
+            const int64_t m = ((mid + k - 1) / k + GDN_CHUNK - 1) / GDN_CHUNK * GDN_CHUNK;
+            for (int64_t left = mid; left > 0; left -= m) bounds.push_back(t += left < m ? left : m);
+        }
+        bounds.push_back(t += e2);
+        bounds.push_back(n_tokens);
+    } else {
         const int64_t qb = B / 4;
         const bool short_ends = n_tokens > B && B % (4 * GDN_CHUNK) == 0;
         int64_t t = short_ends ? qb : (B < n_tokens ? B : n_tokens);

@@ -275,7 +275,11 @@ int gdn_decode_gemv(const void *blocks, int q6k, int64_t rows, int64_t cols, con
  * the device-to-host copy of pass p-1 run on two copy streams of the library
  * while pass p computes (two device staging slots each of x, y and the
  * drawn gates), so the copies hide behind the compute except for the first
- * input and the last output; those two passes are B/4 tokens when B is a
+ * input and the last output.  Those ends are short: when N > B, B is a
+ * multiple of 8 * GDN_CHUNK and N holds the ramps, the passes are B/8, 3B/8,
+ * passes of at most B, 3B/8 and B/8 (a pass's copy-in takes about a third of
+ * its compute time, so each pass's input arrives while one a third its size
+ * computes); otherwise passes of B, the first and the last B/4 when B is a
  * multiple of 4 * GDN_CHUNK and N > B.  Every pass boundary is a chunk
  * boundary (an exact extend), so the results are bitwise those of
  * gdn_prefill.

@@ -266,8 +266,10 @@ def _pinned(a: np.ndarray, dtype=None) -> torch.Tensor:
     return (t.view(dtype) if dtype is not None else t).pin_memory()
 
 
+# passes of B (first and last B/4) for B = 256 and 128; ramped passes B/8, 3B/8,
+# B, ..., 3B/8, B/8 for B = 1024, and with a ragged tail for B = 512
 @pytest.mark.parametrize("name,n,pass_tokens", [("h2560", 1000, 256), ("h2560", 4096, 1024), ("tiny_f32", 64, 0),
-                                                ("h1024", 513, 128)])
+                                                ("h1024", 513, 128), ("h1024", 2085, 512)])
 def test_prefill_host_equals_device_prefill(name, n, pass_tokens):
     """gdn_prefill_host (pinned host x, y and gates, copies overlapped with the
     passes) gives bit for bit what gdn_prefill gives with passes of the same
