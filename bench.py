@@ -367,6 +367,12 @@ def run_ours(args, dist, spec):
         else:
             a = amount / sec / 1e9
             stages[nm] = {"ms": stage_ms[nm], "bound": "hbm", "achieved": a, "unit": "GB/s", "frac": a / pk["hbm"]}
+        if nm.startswith("delta_rule"):
+            # the recurrence against the tensor roofline too: the chunked form's
+            # FLOPs, N Hv (10 C dk + 6 dk^2) with chunks of C = 64
+            fl = n * spec.n_v_heads * (10 * 64 * spec.dk + 6 * spec.dk * spec.dk)
+            stages[nm]["tensor_achieved_tflops"] = fl / sec / 1e12
+            stages[nm]["tensor_frac"] = fl / sec / 1e12 / pk["tensor"]
     dom = stages["in_proj"]
     traffic = traffic_from_profile(os.path.join(ROOT, "hybrid_gated_deltanet_q4k_gb300", "csrc", "k_gemm.cu"),
                                    os.path.join(ROOT, "profiles", "gemm_codes_in_proj_h4096_n32768.md"))
