@@ -152,14 +152,22 @@ __device__ __forceinline__ void block_mm(const float* a, const float* b, float* 
 // The same with one 2 x 4 output tile per thread (threads 0 .. (R/2)(Cc/4) - 1):
 // per k a warp reads four rows of A and 128 contiguous bytes of B, half the
 // shared-memory wavefronts of the 2 x 2 tiling for the same products.
-template <int R, int KK, int Cc>
+// TRI 1: B is lower triangular (B[k][j] = 0 for k < j) and a warp's tiles
+// share their columns, so its k loop starts at its first column; TRI 2: A is
+// lower triangular (A[i][k] = 0 for k > i), so a warp's k loop ends past its
+// last row.  The products skipped are exact zeros added to a sum that is
+// still +0 (TRI 1) or to the finished sum (TRI 2): the results do not change.
+template <int R, int KK, int Cc, int TRI = 0>
 __device__ __forceinline__ void block_mm24(const float* a, const float* b, float* c, float s, int t) {
-    constexpr int TC = Cc / 4;
-    if (t < 0 || t >= (R / 2) * TC) return;
-    const int r0 = 2 * (t / TC), c0 = 4 * (t % TC);
+    constexpr int TC = Cc / 4, TR = R / 2;
+    if (t < 0 || t >= TR * TC) return;
+    const int r0 = TRI == 1 ? 2 * (t % TR) : 2 * (t / TC), c0 = TRI == 1 ? 4 * (t / TR) : 4 * (t % TC);
+    const int tw0 = t & ~31, tw1 = min(t | 31, TR * TC - 1);   // the warp's first and last active thread
+    const int k0 = TRI == 1 ? 4 * (tw0 / TR) : 0;
+    const int k1 = TRI == 2 ? min(KK, 2 * (tw1 / TC) + 2) : KK;
     float x[2][4] = {};
 #pragma unroll 8
-    for (int k = 0; k < KK; ++k) {
+    for (int k = k0; k < k1; ++k) {
         const float a0 = a[r0 * PL + k], a1 = a[(r0 + 1) * PL + k];
         const float4 bv = *reinterpret_cast<const float4*>(b + k * PL + c0);
         x[0][0] = fmaf(a0, bv.x, x[0][0]);
@@ -401,9 +409,9 @@ __global__ void __maxnreg__(88) delta_prep_kernel(const __grid_constant__ CUtens
             __syncthreads();
         }
         // 64 x 64: T[32:64, 0:32] = -T[32:64, 32:64] (L[32:64, 0:32] T[0:32, 0:32])
-        block_mm24<32, 32, 32>(Ls + 32 * PL, Ts, Ws, 1.f, tid);
+        block_mm24<32, 32, 32, 1>(Ls + 32 * PL, Ts, Ws, 1.f, tid);
         __syncthreads();
-        block_mm24<32, 32, 32>(Ts + 32 * PL + 32, Ws, Ts + 32 * PL, -1.f, tid);
+        block_mm24<32, 32, 32, 2>(Ts + 32 * PL + 32, Ws, Ts + 32 * PL, -1.f, tid);
         __syncthreads();
         // T^T operand image (row m, column j = T_jm) and the T rows of the output
         // (rows 64-127 of [A T; T]), fp16; thread -> row tid%64, columns 16(tid/64) ..
