@@ -60,7 +60,8 @@ struct GemvArgs {
     const uint8_t* blocks;   // [rows][cols/256] superblocks
     int rows, cols;
     int64_t row_bytes;       // cols/256 superblocks of the format's size
-    int ntiles, stages;      // tiles of GEMV_WARPS rows; shared-memory ring depth
+    int tile_rows;           // rows per tile: GEMV_WARPS, or 2 GEMV_WARPS for the one-token Q4_K form
+    int ntiles, stages;      // tiles of tile_rows rows; shared-memory ring depth
     int64_t total_bytes;     // rows * row_bytes
     const uint16_t* xc;      // [g][cols] int8 codes as fp16 patterns
     const float* sx;         // [g]
@@ -85,18 +86,26 @@ struct GemvArgs {
 };
 
 // Shared memory: the tokens' codes (g * cols bytes), their sums over blocks
-// of 16 (g * cols/16 ints), then `stages` tiles of GEMV_WARPS weight rows,
-// then one mbarrier per stage.
-__host__ __device__ inline int64_t gemv_tile_bytes(int64_t row_bytes) { return GEMV_WARPS * row_bytes; }
-__host__ __device__ inline int64_t gemv_xsum_offset(int g, int cols) { return (static_cast<int64_t>(g) * cols + 127) & ~127LL; }
-__host__ __device__ inline int64_t gemv_ring_offset(int g, int cols) {
-    return (gemv_xsum_offset(g, cols) + static_cast<int64_t>(g) * (cols / 16) * 4 + 127) & ~127LL;
+// of 16 (g * cols/16 ints), then `stages` tiles of tile_rows weight rows,
+// then one mbarrier per stage.  The one-token Q4_K form (mc) pads each
+// superblock's 256 codes to 272 bytes and its 16 sums to 17 ints, so that 16
+// lanes on 16 consecutive superblocks load from distinct banks at the same
+// offset within a superblock.
+__host__ __device__ inline int gemv_tile_rows(bool mc) { return mc ? 2 * GEMV_WARPS : GEMV_WARPS; }
+__host__ __device__ inline int64_t gemv_tile_bytes(int64_t row_bytes, int tile_rows) { return tile_rows * row_bytes; }
+__host__ __device__ inline int64_t gemv_xsum_offset(int g, int cols, bool mc) {
+    const int64_t xs_bytes = mc ? cols + cols / 16 : static_cast<int64_t>(g) * cols;
+    return (xs_bytes + 127) & ~127LL;
+}
+__host__ __device__ inline int64_t gemv_ring_offset(int g, int cols, bool mc) {
+    const int64_t sums = mc ? cols / 16 + cols / 256 : static_cast<int64_t>(g) * (cols / 16);
+    return (gemv_xsum_offset(g, cols, mc) + sums * 4 + 127) & ~127LL;
 }
 // ... then the barrier of the tokens' packed codes, per stage a count of the
 // warps done with it, and an abort flag.
-__host__ __device__ inline int64_t gemv_smem_bytes(int g, int cols, int64_t row_bytes, int stages) {
-    return gemv_ring_offset(g, cols) + stages * gemv_tile_bytes(row_bytes) + 8 * (GEMV_MAX_STAGES + 1) +
-           4 * GEMV_MAX_STAGES + 4;
+__host__ __device__ inline int64_t gemv_smem_bytes(int g, int cols, int64_t row_bytes, int stages, bool mc) {
+    return gemv_ring_offset(g, cols, mc) + stages * gemv_tile_bytes(row_bytes, gemv_tile_rows(mc)) +
+           8 * (GEMV_MAX_STAGES + 1) + 4 * GEMV_MAX_STAGES + 4;
 }
 
 // Copy tile `tile` into stage `s`: the whole bytes by one bulk copy (a tile
@@ -104,7 +113,7 @@ __host__ __device__ inline int64_t gemv_smem_bytes(int g, int cols, int64_t row_
 // of 16), a ragged end of the last tile (< 16 bytes) by plain loads.  Thread 0.
 __device__ __forceinline__ void gemv_issue(const GemvArgs& a, unsigned char* ring, uint64_t* full, int tile, int s) {
     if (tile >= a.ntiles) return;
-    const int64_t tb = gemv_tile_bytes(a.row_bytes);
+    const int64_t tb = gemv_tile_bytes(a.row_bytes, a.tile_rows);
     const int64_t off = static_cast<int64_t>(tile) * tb;
     const int64_t bytes = (a.total_bytes - off) < tb ? (a.total_bytes - off) : tb;
     const int64_t b16 = bytes & ~15LL;
@@ -184,71 +193,98 @@ __device__ __forceinline__ void q4k_unpack_scales(const uint4& h, uint32_t& sl, 
     mh = ((h.w >> 4) & 0x0f0f0f0fu) | ((h.z >> 2) & 0x30303030u);
 }
 
-// One token's sum over a Q4_K row in the fp32 operations of
+// One token's sums over two Q4_K rows in the fp32 operations of
 // gemv_q4k_mma_kernel, so that a token decodes bit for bit the same alone as
 // in a batch.  Per superblock i, the exact integer sums S = sum_j sc_j D_j and
 // M = sum_j m_j X_j (D_j the sub-block's code-token dot product, X_j its token
 // sum), then y_w = fma(-dmin, M, fma(d, S, y_w)) for the slice w = i mod 8,
 // superblocks in increasing order; the eight slices are summed in order.  That
 // kernel rounds the sum of S's two exact halves once, which is the conversion
-// of the exact integer here.  Lane (sbl, j) takes sub-block j of superblocks
-// sbl, sbl + 4, ...: slice sbl (ya) and slice sbl + 4 (yb).  Odd sub-blocks
-// keep their codes at 16 q and even ones take 16 sc, so S arrives 16 times too
-// large and d / 16 (exact) undoes it inside the same fma.
-__device__ __forceinline__ float q4k_token_sum_mma_order(const uint8_t* rb, const uint32_t* xs, const int* xsum,
-                                                         int nsb, int lane) {
-    const int j = lane & 7, sbl = lane >> 3, k = j & 3;
-    const uint32_t mask = (j & 1) ? 0xf0f0f0f0u : 0x0f0f0f0fu;
-    float ya = 0.0f, yb = 0.0f;
-    const int nst = (nsb + 3) >> 2;
-#pragma unroll 4
-    for (int st = 0; st < nst; ++st) {
-        const int i = sbl + 4 * st;
+// of the exact integer here.  Odd sub-blocks keep their codes at 16 q and even
+// ones take 16 sc, so S arrives 16 times too large and d / 16 (exact) undoes
+// it inside the same fma.
+//
+// The row at rb is summed in lanes 0-15, the row at rb + row_bytes in lanes
+// 16-31, with the token's codes and sums in the padded layout (superblock i at
+// 272 i bytes and 17 i ints).  Lane l of a half takes the whole superblocks l,
+// l + 16, ...: their S and M by dp4a in one lane, with no shuffles; then slice
+// w (lane w < 8) adds superblock w + 16 r (its own) and w + 8 + 16 r (from lane
+// w + 8), in increasing order.  Every lane of a half returns its row's sum.
+__device__ __forceinline__ float q4k_token_sum_mma_order(const uint8_t* rb, int64_t row_bytes, const uint32_t* xs,
+                                                               const int* xsum, int nsb, int lane) {
+    const int l = lane & 15, hb = lane & 16;
+    const uint8_t* row = rb + (hb ? row_bytes : 0);
+    float y = 0.0f;
+    for (int r0 = 0; r0 < nsb; r0 += 16) {
+        const int i = r0 + l;
         int S = 0, M = 0;
         float d16 = 0.0f, e = 0.0f;
         if (i < nsb) {
-            const uint8_t* blk = rb + i * 144;
+            const uint8_t* blk = row + i * 144;
             const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
             uint32_t sl, sh, ml, mh;
             q4k_unpack_scales(hdr, sl, sh, ml, mh);
-            const int sc = static_cast<int>(__byte_perm(j < 4 ? sl : sh, 0u, 0x4440 + k));
-            const int m = static_cast<int>(__byte_perm(j < 4 ? ml : mh, 0u, 0x4440 + k));
-            const uint4* q = reinterpret_cast<const uint4*>(blk + 16 + 32 * (j >> 1));
-            const uint4 qa = q[0], qb = q[1];
-            const int w0 = 64 * i + 8 * j;
-            const uint4 xa = *reinterpret_cast<const uint4*>(xs + w0);
-            const uint4 xb = *reinterpret_cast<const uint4*>(xs + w0 + 4);
-            const int2 xm = *reinterpret_cast<const int2*>(xsum + 16 * i + 2 * j);
-            int D = dp4a_us(qa.x & mask, xa.x, 0);
-            D = dp4a_us(qa.y & mask, xa.y, D);
-            D = dp4a_us(qa.z & mask, xa.z, D);
-            D = dp4a_us(qa.w & mask, xa.w, D);
-            D = dp4a_us(qb.x & mask, xb.x, D);
-            D = dp4a_us(qb.y & mask, xb.y, D);
-            D = dp4a_us(qb.z & mask, xb.z, D);
-            D = dp4a_us(qb.w & mask, xb.w, D);
-            S = ((j & 1) ? sc : (sc << 4)) * D;
-            M = m * (xm.x + xm.y);
+            const uint4* q = reinterpret_cast<const uint4*>(blk + 16);
+            const uint4* xi = reinterpret_cast<const uint4*>(xs) + 17 * i;
+            const int* si = xsum + 17 * i;
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+                // code bytes 16 v .. 16 v + 15: their low nibbles are weights 64 p + 16 qq
+                // + (0..15), of sub-block 2 p (x unit 4 p + qq); the high nibbles weights
+                // 64 p + 32 + 16 qq + (0..15), of sub-block 2 p + 1 (unit 4 p + 2 + qq)
+                const int p = v >> 1, qq = v & 1, ul = 4 * p + qq, uh = 4 * p + 2 + qq;
+                const uint4 c = q[v], xl = xi[ul], xh = xi[uh];
+                int dl = dp4a_us(c.x & 0x0f0f0f0fu, xl.x, 0);
+                dl = dp4a_us(c.y & 0x0f0f0f0fu, xl.y, dl);
+                dl = dp4a_us(c.z & 0x0f0f0f0fu, xl.z, dl);
+                dl = dp4a_us(c.w & 0x0f0f0f0fu, xl.w, dl);
+                int dh = dp4a_us(c.x & 0xf0f0f0f0u, xh.x, 0);
+                dh = dp4a_us(c.y & 0xf0f0f0f0u, xh.y, dh);
+                dh = dp4a_us(c.z & 0xf0f0f0f0u, xh.z, dh);
+                dh = dp4a_us(c.w & 0xf0f0f0f0u, xh.w, dh);
+                const uint32_t sw = p < 2 ? sl : sh, mw = p < 2 ? ml : mh, k0 = (2 * p) & 3;
+                const int sc0 = static_cast<int>(__byte_perm(sw, 0u, 0x4440u + k0));
+                const int sc1 = static_cast<int>(__byte_perm(sw, 0u, 0x4441u + k0));
+                const int m0 = static_cast<int>(__byte_perm(mw, 0u, 0x4440u + k0));
+                const int m1 = static_cast<int>(__byte_perm(mw, 0u, 0x4441u + k0));
+                // the even sub-block's codes count once and the odd one's 16 times: 16 sc D either way
+                S += (sc0 << 4) * dl + sc1 * dh;
+                M += m0 * si[ul] + m1 * si[uh];
+            }
             d16 = __fmul_rn(__half2float(__ushort_as_half(static_cast<uint16_t>(hdr.x & 0xffffu))), 0.0625f);
             e = -__half2float(__ushort_as_half(static_cast<uint16_t>(hdr.x >> 16)));
         }
-        S += __shfl_xor_sync(0xffffffffu, S, 1);
-        S += __shfl_xor_sync(0xffffffffu, S, 2);
-        S += __shfl_xor_sync(0xffffffffu, S, 4);
-        M += __shfl_xor_sync(0xffffffffu, M, 1);
-        M += __shfl_xor_sync(0xffffffffu, M, 2);
-        M += __shfl_xor_sync(0xffffffffu, M, 4);
-        if (i < nsb) {
-            if (st & 1)
-                yb = fmaf(e, static_cast<float>(M), fmaf(d16, static_cast<float>(S), yb));
-            else
-                ya = fmaf(e, static_cast<float>(M), fmaf(d16, static_cast<float>(S), ya));
+        const int src = hb + ((l + 8) & 15);
+        const int S8 = __shfl_sync(0xffffffffu, S, src), M8 = __shfl_sync(0xffffffffu, M, src);
+        const float d8 = __shfl_sync(0xffffffffu, d16, src), e8 = __shfl_sync(0xffffffffu, e, src);
+        if (l < 8) {
+            if (i < nsb) y = fmaf(e, static_cast<float>(M), fmaf(d16, static_cast<float>(S), y));
+            if (i + 8 < nsb) y = fmaf(e8, static_cast<float>(M8), fmaf(d8, static_cast<float>(S8), y));
         }
     }
     float v = 0.0f;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) v += __shfl_sync(0xffffffffu, w < 4 ? ya : yb, (w & 3) * 8);
+    for (int w = 0; w < 8; ++w) v += __shfl_sync(0xffffffffu, y, hb + w);
     return v;
+}
+
+// One 16-code unit of a token's codes given as fp16 patterns of the integers
+// (xc): the codes packed into 4 words of 4 int8, and their sum.
+__device__ __forceinline__ void xc_unit(const uint16_t* src, uint4& w, int& sum) {
+    const uint4 h0 = __ldg(reinterpret_cast<const uint4*>(src));
+    const uint4 h1 = __ldg(reinterpret_cast<const uint4*>(src + 8));
+    const uint32_t hw[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+    uint32_t pk[4];
+    sum = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&hw[2 * q]));
+        const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&hw[2 * q + 1]));
+        pk[q] = codes_to_i8x4(__fadd_rn(f0.x, QCODE_MAGIC), __fadd_rn(f0.y, QCODE_MAGIC), __fadd_rn(f1.x, QCODE_MAGIC),
+                              __fadd_rn(f1.y, QCODE_MAGIC));
+        sum = __dp4a(static_cast<int>(pk[q]), 0x01010101, sum);
+    }
+    w = make_uint4(pk[0], pk[1], pk[2], pk[3]);
 }
 
 // Bounded wait of one warp on a stage: gives up at once after any earlier
@@ -262,16 +298,17 @@ __device__ __forceinline__ bool gemv_wait(uint64_t* bar, uint32_t parity, volati
 
 // G: tokens the kernel computes (a power of two >= a.g; the codes of tokens
 // a.g .. G-1 are zero and their sums are not stored).
-// MC (Q4_K, one token): the sums in the fp32 operations of gemv_q4k_mma_kernel.
+// MC (Q4_K, one token): the sums in the fp32 operations of gemv_q4k_mma_kernel,
+// two rows per warp (tiles of 2 GEMV_WARPS rows) and the token's codes padded.
 template <bool Q6, int G, bool MC = false>
 __global__ void __launch_bounds__(GEMV_THREADS, G <= 2 ? 4 : 2) gemv_dot_kernel(GemvArgs a) {
     static_assert(!MC || (!Q6 && G == 1), "the tensor-core order is for one token of Q4_K rows");
     constexpr int BYTES = Q6 ? 210 : 144;
     extern __shared__ __align__(128) unsigned char gsm[];
     uint32_t* xs = reinterpret_cast<uint32_t*>(gsm);                 // [G][cols / 4] packed int8
-    int* xsum = reinterpret_cast<int*>(gsm + gemv_xsum_offset(G, a.cols));   // [G][cols / 16] block sums
-    unsigned char* ring = gsm + gemv_ring_offset(G, a.cols);
-    const int64_t tb = gemv_tile_bytes(a.row_bytes);
+    int* xsum = reinterpret_cast<int*>(gsm + gemv_xsum_offset(G, a.cols, MC));   // [G][cols / 16] block sums
+    unsigned char* ring = gsm + gemv_ring_offset(G, a.cols, MC);
+    const int64_t tb = gemv_tile_bytes(a.row_bytes, a.tile_rows);
     uint64_t* full = reinterpret_cast<uint64_t*>(ring + a.stages * tb);
     uint64_t* xbar = full + GEMV_MAX_STAGES;                         // the packed codes (in_mode 1)
     int* done = reinterpret_cast<int*>(xbar + 1);                    // warps done with each stage
@@ -297,7 +334,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, G <= 2 ? 4 : 2) gemv_dot_kernel(
     pdl_trigger();
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int kw = a.cols >> 2, k16 = a.cols >> 4;
-    if (a.in_mode == 1 && tid == 0) {
+    if (!MC && a.in_mode == 1 && tid == 0) {
         // the tokens' packed codes and sums: two bulk copies per token
         const uint32_t bytes = static_cast<uint32_t>(a.cols + a.cols / 4);
         mbar_expect_tx(xbar, static_cast<uint32_t>(a.g) * bytes);
@@ -327,23 +364,26 @@ __global__ void __launch_bounds__(GEMV_THREADS, G <= 2 ? 4 : 2) gemv_dot_kernel(
         *reinterpret_cast<uint4*>(xs + t * kw + 4 * b) = make_uint4(0u, 0u, 0u, 0u);
         xsum[i] = 0;
     }
-    if (a.in_mode == 0) {
+    if constexpr (MC) {
+        // one token: unit b of 16 codes (and its sum) to the padded place b + b / 16
+        for (int b = tid; b < k16; b += GEMV_THREADS) {
+            uint4 w;
+            int sum;
+            if (a.in_mode == 1) {
+                w = __ldcg(reinterpret_cast<const uint4*>(a.xpack) + b);
+                sum = __ldcg(reinterpret_cast<const int*>(a.xpack + kw) + b);
+            } else {
+                xc_unit(a.xc + 16 * b, w, sum);
+            }
+            reinterpret_cast<uint4*>(xs)[b + (b >> 4)] = w;
+            xsum[b + (b >> 4)] = sum;
+        }
+    } else if (a.in_mode == 0) {
         for (int i = tid; i < a.g * k16; i += GEMV_THREADS) {
             const int t = i / k16, b = i - t * k16;
-            const uint4 h0 = __ldg(reinterpret_cast<const uint4*>(a.xc + static_cast<int64_t>(t) * a.cols + 16 * b));
-            const uint4 h1 = __ldg(reinterpret_cast<const uint4*>(a.xc + static_cast<int64_t>(t) * a.cols + 16 * b + 8));
-            const uint32_t hw[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-            int sum = 0;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&hw[2 * q]));
-                const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&hw[2 * q + 1]));
-                const uint32_t packed = codes_to_i8x4(__fadd_rn(f0.x, QCODE_MAGIC), __fadd_rn(f0.y, QCODE_MAGIC),
-                                                      __fadd_rn(f1.x, QCODE_MAGIC), __fadd_rn(f1.y, QCODE_MAGIC));
-                xs[t * kw + 4 * b + q] = packed;
-                sum = __dp4a(static_cast<int>(packed), 0x01010101, sum);
-            }
-            xsum[i] = sum;
+            uint4 w;
+            xc_unit(a.xc + static_cast<int64_t>(t) * a.cols + 16 * b, w, xsum[i]);
+            *reinterpret_cast<uint4*>(xs + t * kw + 4 * b) = w;
         }
     } else {
         gemv_wait(xbar, 0, abort);
@@ -358,12 +398,18 @@ __global__ void __launch_bounds__(GEMV_THREADS, G <= 2 ? 4 : 2) gemv_dot_kernel(
     for (int tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x, ++it) {
         const int s = it % a.stages;
         if (!__all_sync(0xffffffffu, gemv_wait(full + s, (it / a.stages) & 1, abort))) break;
-        const int row = tile * GEMV_WARPS + warp;
+        const int wr = MC ? 2 * warp : warp;        // the warp's first row in the tile
+        int row = tile * a.tile_rows + wr;
         if (row < a.rows) {
-            const uint8_t* rb = ring + s * tb + static_cast<int64_t>(warp) * a.row_bytes;
+            const uint8_t* rb = ring + s * tb + static_cast<int64_t>(wr) * a.row_bytes;
             float mine = 0.0f;
+            int t_out = lane;                          // the token whose sum this lane stores
+            bool store = lane < a.g;
             if constexpr (MC) {
-                mine = q4k_token_sum_mma_order(rb, xs, xsum, nsb, lane);
+                mine = q4k_token_sum_mma_order(rb, a.row_bytes, xs, xsum, nsb, lane);
+                row += lane >> 4;
+                t_out = 0;
+                store = (lane & 15) == 0 && row < a.rows;
             } else {
                 float acc[G];
 #pragma unroll
@@ -410,12 +456,12 @@ __global__ void __launch_bounds__(GEMV_THREADS, G <= 2 ? 4 : 2) gemv_dot_kernel(
                     if (lane == t) mine = sum;
                 }
             }
-            if (lane < a.g && GDN_IN_RANGE(g_decode_error, row < a.rows)) {
-                const float y = mine * sxs[lane];
+            if (store && GDN_IN_RANGE(g_decode_error, row < a.rows)) {
+                const float y = mine * sxs[t_out];
                 if (row < a.n_bf16)
-                    a.out_bf16[lane * a.ld_bf16 + row] = float_to_bf16_bits(y);
+                    a.out_bf16[t_out * a.ld_bf16 + row] = float_to_bf16_bits(y);
                 else
-                    a.out_f32[lane * a.ld_f32 + (row - a.n_bf16)] = y;
+                    a.out_f32[t_out * a.ld_f32 + (row - a.n_bf16)] = y;
             }
         }
         // this warp is done reading stage s (its loads have been consumed)
@@ -927,15 +973,20 @@ cudaError_t launch_gemv_dot(const void* blocks, bool q6k, int64_t rows, int64_t 
     const int64_t row_bytes = (cols / 256) * (q6k ? 210 : 144);
     // tokens per launch (a power of two): what fits beside one stage
     int64_t gmax = GEMV_TOKENS;
-    while (gmax > 1 && gemv_smem_bytes(static_cast<int>(gmax), static_cast<int>(cols), row_bytes, 1) > max_optin) gmax /= 2;
-    if (gemv_smem_bytes(1, static_cast<int>(cols), row_bytes, 1) > max_optin) return cudaErrorInvalidValue;
-    const int ntiles = static_cast<int>((rows + GEMV_WARPS - 1) / GEMV_WARPS);
+    while (gmax > 1 && gemv_smem_bytes(static_cast<int>(gmax), static_cast<int>(cols), row_bytes, 1, false) > max_optin)
+        gmax /= 2;
+    // one Q4_K token (n == 1 here when mma_q4k): the tensor-core order, two rows per warp
+    const bool mc = mma_q4k;
+    if (gemv_smem_bytes(1, static_cast<int>(cols), row_bytes, 1, mc) > max_optin) return cudaErrorInvalidValue;
+    const int tile_rows = gemv_tile_rows(mc);
+    const int ntiles = static_cast<int>((rows + tile_rows - 1) / tile_rows);
     for (int64_t t0 = 0; t0 < n; t0 += gmax) {
         GemvArgs a;
         a.blocks = static_cast<const uint8_t*>(blocks);
         a.rows = static_cast<int>(rows);
         a.cols = static_cast<int>(cols);
         a.row_bytes = row_bytes;
+        a.tile_rows = tile_rows;
         a.ntiles = ntiles;
         a.total_bytes = rows * row_bytes;
         a.xc = xc ? xc + t0 * cols : nullptr;
@@ -963,12 +1014,12 @@ cudaError_t launch_gemv_dot(const void* blocks, bool q6k, int64_t rows, int64_t 
         for (; per_sm >= 1; --per_sm) {
             const int64_t budget = GEMV_SM_SMEM / per_sm - 1024 - static_cast<int64_t>(fa_static);
             stages = GEMV_MAX_STAGES;
-            while (stages > 1 && gemv_smem_bytes(G, a.cols, row_bytes, stages) > budget) --stages;
+            while (stages > 1 && gemv_smem_bytes(G, a.cols, row_bytes, stages, mc) > budget) --stages;
             if (stages >= 2 || per_sm == 1) break;
         }
         if (per_sm < 1) per_sm = 1;
         a.stages = stages;
-        const size_t smem = static_cast<size_t>(gemv_smem_bytes(G, a.cols, row_bytes, stages));
+        const size_t smem = static_cast<size_t>(gemv_smem_bytes(G, a.cols, row_bytes, stages, mc));
         if (smem > static_cast<size_t>(max_optin)) return cudaErrorInvalidValue;
         const unsigned grid = static_cast<unsigned>(ntiles < per_sm * sms ? ntiles : per_sm * sms);
         cudaError_t e = q6k ? gemv_launch<true>(G, false, grid, smem, st, a) : gemv_launch<false>(G, mma_q4k, grid, smem, st, a);
