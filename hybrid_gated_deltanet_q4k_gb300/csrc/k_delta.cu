@@ -110,16 +110,16 @@ struct PrepSmem {
     static constexpr int W0 = T0 + DC * PL * 4;          // block temporaries [DC/2][PL]
     static constexpr int GL0 = W0 + DC / 2 * PL * 4;     // gamma [PREP_MAX_RATIO][DC]
     static constexpr int BB0 = GL0 + PREP_MAX_RATIO * DC * 4;  // b [PREP_MAX_RATIO][DC]
+    static constexpr int EN0 = BB0 + PREP_MAX_RATIO * DC * 4;  // e^{-gamma} [PREP_MAX_RATIO][DC]
     // 8 KB pieces 0-5 of operand and output images once the Gram product is
     // done: the [Q; K] region, extended by a region of its own.
     static constexpr int NPIECE = 6;
-    static constexpr int EX0 = align1k(BB0 + PREP_MAX_RATIO * DC * 4);
+    static constexpr int EX0 = align1k(EN0 + PREP_MAX_RATIO * DC * 4);
     static constexpr int B0 = EX0 + (NPIECE - 2 * NSLAB) * SLAB;   // mbarriers: TMA, MMA
     static constexpr int MISC0 = B0 + 16;                          // TMEM base address
     static constexpr int BYTES = MISC0 + 16;
     static __device__ __forceinline__ int piece(int p) { return p < 2 * NSLAB ? QK0 + p * SLAB : EX0 + (p - 2 * NSLAB) * SLAB; }
-    static constexpr int AI = 0;    // A operand [DC][DC] (piece 0)
-    static constexpr int TTI = 1;   // T^T operand [DC][DC] (piece 1)
+    static constexpr int AI = 0;    // A operand [DC][DC] (piece 0; piece 1 unused)
     // [A T; T] output staging [2*DC][DC], two buffers (pieces 2-3 and 4-5, one
     // 16 KB slab each) used by alternate value heads; the second buffer first
     // stages K^T (key rows 64p .. 64p+63 in piece 4 + p).
@@ -249,11 +249,13 @@ __global__ void __maxnreg__(88) delta_prep_kernel(const __grid_constant__ CUtens
         const int o = 32 * (idx >> 8), rr = (idx >> 4) & 15, cc = idx & 15;
         Ts[(o + rr) * PL + o + 16 + cc] = 0.f;
     }
-    // gates of the value heads h = hk*r + j: log a -> inclusive prefix sum (one warp per head)
+    // gates of the value heads h = hk*r + j: log a -> inclusive prefix sum gamma
+    // and e^{-gamma} (one warp per head)
     for (int j = warp; j < r; j += DELTA_THREADS / 32) {
         const int h = hk * r + j;
         float* gl = reinterpret_cast<float*>(base + L::GL0) + j * DC;
         float* bb = reinterpret_cast<float*>(base + L::BB0) + j * DC;
+        float* en = reinterpret_cast<float*>(base + L::EN0) + j * DC;
         float x0 = 0.f, x1 = 0.f;
         const int ta = t0 + 2 * lane, tb = ta + 1;
         if (ta < t_end) x0 = a.log_a[static_cast<int64_t>(ta) * a.hv + h];
@@ -268,6 +270,8 @@ __global__ void __maxnreg__(88) delta_prep_kernel(const __grid_constant__ CUtens
         }
         gl[2 * lane] = s - x1;
         gl[2 * lane + 1] = s;
+        en[2 * lane] = __expf(x1 - s);
+        en[2 * lane + 1] = __expf(-s);
     }
     t5::fence_before();
     __syncthreads();
@@ -348,37 +352,55 @@ __global__ void __maxnreg__(88) delta_prep_kernel(const __grid_constant__ CUtens
         const int64_t cb = static_cast<int64_t>(chunk) * a.hv + h;
         const float* gl = reinterpret_cast<const float*>(base + L::GL0) + j * DC;
         const float* bb = reinterpret_cast<const float*>(base + L::BB0) + j * DC;
+        const float* en = reinterpret_cast<const float*>(base + L::EN0) + j * DC;
         const float gi = gl[row];
         // this head's output buffer was last read by the store two heads back
         // (or, for head 1, by the K^T store): let that read finish first
         if (tid == 0 && j >= 1) bulk_wait_read_but_last();
-        if (qrow) {
-            // A_ij = e^{gamma_i - gamma_j} q_i.k_j (j <= i), |A_ij| <= |q_i||k_j| <= 1:
-            // half of one 128-byte row of the swizzled image
-            unsigned char* arow = base + L::piece(L::AI) + row * 128;
+        // The decay e^{gamma_i - gamma_j} of an entry (j <= i, so at most 1): as
+        // e^{gamma_i} e^{-gamma_j} when the chunk's whole decay gamma_C >= -64, so
+        // that every factor is a normal fp32 value, else by its own exponential.
+        auto entries = [&](auto decay) {
+            if (qrow) {
+                // A_ij = e^{gamma_i - gamma_j} q_i.k_j (j <= i), |A_ij| <= |q_i||k_j| <= 1:
+                // half of one 128-byte row of the swizzled image (zeros above the diagonal block)
+                unsigned char* arow = base + L::piece(L::AI) + row * 128;
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                float v[8];
+                for (int m = 0; m < 4; ++m) {
+                    uint4 w = make_uint4(0u, 0u, 0u, 0u);
+                    if (!upper) {
+                        float v[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int c = c0 + 8 * m + e;
-                    v[e] = (!upper && c <= row) ? __expf(gi - gl[c]) * g[8 * m + e] : 0.f;
+                        for (int e = 0; e < 8; ++e) {
+                            const int c = c0 + 8 * m + e;
+                            v[e] = c <= row ? decay(c) * g[8 * m + e] : 0.f;
+                        }
+                        w = f16x8(v);
+                    }
+                    *reinterpret_cast<uint4*>(arow + ((((c0 >> 3) + m) ^ (row & 7)) << 4)) = w;
                 }
-                *reinterpret_cast<uint4*>(arow + ((((c0 >> 3) + m) ^ (row & 7)) << 4)) = f16x8(v);
+            } else {
+                // L_ij = b_i e^{gamma_i - gamma_j} k_i.k_j (j < i)
+                const float bi = bb[row];
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    float v[4] = {0.f, 0.f, 0.f, 0.f};
+                    if (!upper) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int c = c0 + 4 * m + e;
+                            v[e] = c < row ? bi * decay(c) * g[4 * m + e] : 0.f;
+                        }
+                    }
+                    *reinterpret_cast<float4*>(Ls + row * PL + c0 + 4 * m) = make_float4(v[0], v[1], v[2], v[3]);
+                }
             }
+        };
+        if (gl[DC - 1] >= -64.f) {
+            const float egi = __expf(gi);
+            entries([&](int c) { return egi * en[c]; });
         } else {
-            // L_ij = b_i e^{gamma_i - gamma_j} k_i.k_j (j < i)
-            const float bi = bb[row];
-#pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                float v[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int c = c0 + 4 * m + e;
-                    v[e] = (!upper && c < row) ? bi * __expf(gi - gl[c]) * g[4 * m + e] : 0.f;
-                }
-                *reinterpret_cast<float4*>(Ls + row * PL + c0 + 4 * m) = make_float4(v[0], v[1], v[2], v[3]);
-            }
+            entries([&](int c) { return __expf(gi - gl[c]); });
         }
         __syncthreads();
         // 16 x 16 diagonal blocks of T: warp 0 blocks 0, 1; warp 1 blocks 2, 3; lane = column.
@@ -413,29 +435,28 @@ __global__ void __maxnreg__(88) delta_prep_kernel(const __grid_constant__ CUtens
         __syncthreads();
         block_mm24<32, 32, 32, 2>(Ts + 32 * PL + 32, Ws, Ts + 32 * PL, -1.f, tid);
         __syncthreads();
-        // T^T operand image (row m, column j = T_jm) and the T rows of the output
-        // (rows 64-127 of [A T; T]), fp16; thread -> row tid%64, columns 16(tid/64) ..
+        // The T rows of the output (rows 64-127 of [A T; T]), fp16, which are also
+        // the B operand of A T (MN-major: row k holds T_k0 .. T_k63); thread -> row
+        // tid%64, columns 16(tid/64) ..
         {
             const int rr = tid & 63, cq = 16 * (tid >> 6);
-            unsigned char* ttrow = base + L::piece(L::TTI) + rr * 128;
             unsigned char* orow = base + L::out(j) + (DC + rr) * 128;
+            float mx = 0.f;
 #pragma unroll
             for (int m = 0; m < 2; ++m) {
                 const int c = cq + 8 * m;
                 const float4 r0 = *reinterpret_cast<const float4*>(Ts + rr * PL + c);
                 const float4 r1 = *reinterpret_cast<const float4*>(Ts + rr * PL + c + 4);
                 const float rv[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-                float v[8], w[8];
+                float v[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     v[e] = c + e <= rr ? rv[e] : 0.f;
-                    w[e] = c + e >= rr ? Ts[(c + e) * PL + rr] : 0.f;
-                    bad |= f16_out_of_range(v[e]);
+                    mx = fmaxf_nan(mx, fabsf(v[e]));
                 }
-                const int ch = (((c >> 3) ^ (rr & 7)) & 7) << 4;
-                *reinterpret_cast<uint4*>(orow + ch) = f16x8(v);
-                *reinterpret_cast<uint4*>(ttrow + ch) = f16x8(w);
+                *reinterpret_cast<uint4*>(orow + ((((c >> 3) ^ (rr & 7)) & 7) << 4)) = f16x8(v);
             }
+            bad |= !(mx <= F16_MAX);
         }
         if (tid < DC) {
             const float gv = gl[tid];
@@ -444,15 +465,19 @@ __global__ void __maxnreg__(88) delta_prep_kernel(const __grid_constant__ CUtens
         fence_proxy_async_smem();
         t5::fence_before();
         __syncthreads();
-        // A T on the tensor cores (M = 64, N = 64, K = 64) into TMEM columns 64-127
+        // A T on the tensor cores (M = 64, N = 64, K = 64) into TMEM columns 64-127;
+        // B = the T rows, MN-major (bit 16 of the instruction descriptor).  With N =
+        // 64 fp16, one 128-byte swizzle atom wide, its descriptor is the K-major one
+        // (8-row groups 1024 bytes apart); a K step of 16 rows is 2048 bytes further.
         bool mok = true;
         if (tid == 0) {
             t5::fence_after();
             const uint32_t sb = smem_addr(base);
-            const uint64_t dA = t5::desc_sw128(sb + L::piece(L::AI)), dB = t5::desc_sw128(sb + L::piece(L::TTI));
-            constexpr uint32_t ID = t5::idesc_f16(64, DC);
+            const uint64_t dA = t5::desc_sw128(sb + L::piece(L::AI)), dB = t5::desc_sw128(sb + L::out(j) + DC * 128);
+            constexpr uint32_t ID = t5::idesc_f16(64, DC) | (1u << 16);
 #pragma unroll
-            for (int k = 0; k < DC / 16; ++k) t5::mma_f16(tmem + 64, dA + 2 * k, dB + 2 * k, ID, k > 0 ? 1u : 0u);
+            for (int k = 0; k < DC / 16; ++k)
+                t5::mma_f16(tmem + 64, dA + 2 * k, dB + static_cast<uint64_t>(k * (2048 >> 4)), ID, k > 0 ? 1u : 0u);
             t5::commit(bars + 1);
         }
         if (!mbar_wait_bounded(bars + 1, (j + 1) & 1, &g_delta_error, ERR_WAIT_TIMEOUT)) mok = false;
@@ -465,16 +490,18 @@ __global__ void __maxnreg__(88) delta_prep_kernel(const __grid_constant__ CUtens
             if (lane < 16) {
                 const int ri = 16 * q + lane;
                 unsigned char* orow = base + L::out(j) + ri * 128;
+                float mx = 0.f;
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
                     float v[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         v[e] = at[8 * m + e];
-                        bad |= f16_out_of_range(v[e]);
+                        mx = fmaxf_nan(mx, fabsf(v[e]));
                     }
                     *reinterpret_cast<uint4*>(orow + ((((c0 >> 3) + m) ^ (ri & 7)) << 4)) = f16x8(v);
                 }
+                bad |= !(mx <= F16_MAX);
             }
         }
         fence_proxy_async_smem();
