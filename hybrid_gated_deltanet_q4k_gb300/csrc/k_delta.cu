@@ -554,8 +554,12 @@ struct StateSmem {
 
 // TMEM columns (fp32 accumulators of NV = 32 columns).  [Q; K] S^T is
 // double-buffered: the output reads Y of chunk c while X, Y of chunk c+1 run.
-constexpr uint32_t TM_XY = 0, TM_DZ = 64, TM_U = 96;
-constexpr uint32_t TM_COLS = 128;
+// Its eight K steps alternate between two accumulators (the second TM_XY2
+// columns further on), summed when read: two chains of four dependent
+// products complete sooner than one of eight.  256 columns, so a prep CTA
+// (128) still fits beside a state CTA.
+constexpr uint32_t TM_XY = 0, TM_DZ = 64, TM_U = 96, TM_XY2 = 128;
+constexpr uint32_t TM_COLS = 256;
 
 enum StateBar : int {
     F_QK, F_KT0, F_KT1, F_V, F_TA,       // copies landed (tx bytes)
@@ -614,6 +618,16 @@ __device__ __forceinline__ void mma_chain_bmn(uint32_t d_tmem, uint64_t adesc, u
                     bdesc + static_cast<uint64_t>(k * (1024 >> 4)), idesc, k > 0 ? 1u : 0u);
 }
 
+// The same with the even K steps into d_tmem and the odd ones into d_tmem +
+// TM_XY2 (each accumulator's first step overwrites it).
+template <int NK, int A_SLAB>
+__device__ __forceinline__ void mma_chain_bmn_split(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc) {
+#pragma unroll
+    for (int k = 0; k < NK; ++k)
+        t5::mma_f16(d_tmem + ((k & 1) ? TM_XY2 : 0u), adesc + static_cast<uint64_t>((k >> 2) * (A_SLAB >> 4) + 2 * (k & 3)),
+                    bdesc + static_cast<uint64_t>(k * (1024 >> 4)), idesc, k > 1 ? 1u : 0u);
+}
+
 // One CTA per (value head, NV rows of S); 320 threads:
 //   warps 0-7  compute.  Warp w reads TMEM lanes 32*(w%4) .. +31 and columns
 //              16*(w/4) .. +15 of each 32-column accumulator.
@@ -623,7 +637,8 @@ __device__ __forceinline__ void mma_chain_bmn(uint32_t d_tmem, uint64_t adesc, u
 //              barrier once they have written an operand, then issues (one
 //              thread).
 // Per chunk, with S the NV x D slice of the state (fp16 operands, fp32 sums):
-//   MMA  [Y; X] = [Q; K] S^T          (M = 128: Y in lanes 0-63, X in 64-127)
+//   MMA  [Y; X] = [Q; K] S^T          (M = 128: Y in lanes 0-63, X in 64-127;
+//        even and odd K steps in two accumulators, added when read)
 //   warps 2,3,6,7 (lanes 64-127)  R = diag(b)(V - diag(e^gamma) X) -> R^T
 //   MMA  [Z; Delta] = [A T; T] R      (M = 128: Z = A Delta in lanes 0-63,
 //        Delta in lanes 64-127; delta_prep folds A T, so A Delta costs no
@@ -731,7 +746,7 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a, con
             const uint32_t ph = j & 1;
             nb_sync(NB_S);                      // S of chunk j written
             if (leader && ready(F_QK, ph)) {
-                mma_chain_bmn<D / 16, L::QK_SLAB>(tmem + TM_XY + 32 * ph, dQK, dS, ID128);
+                mma_chain_bmn_split<D / 16, L::QK_SLAB>(tmem + TM_XY + 32 * ph, dQK, dS, ID128);
                 t5::commit(bars + M_XY);
                 t5::commit(bars + E_QK);
             }
@@ -827,8 +842,10 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a, con
 
             // ---- R = diag(b) (V - diag(e^gamma) X), stored as R^T (X rows: lanes 64-127)
             if (xw && mma_done(M_XY, ph)) {
-                float x[16];
-                t5::ld16(tl + TM_XY + 32 * ph, x);
+                float x[16], x2[16];
+                t5::ld16x2(tl + TM_XY + 32 * ph, x, tl + TM_XY2 + TM_XY + 32 * ph, x2);
+#pragma unroll
+                for (int v = 0; v < 16; ++v) x[v] += x2[v];
                 const unsigned char* vp = base + L::V0;
 #pragma unroll
                 for (int m = 0; m < 2; ++m) {
@@ -879,6 +896,12 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a, con
             if (!xw && mma_done(M_DZ, ph)) {
                 float y[16], z[16];
                 t5::ld16x2(tl + TM_XY + 32 * ph, y, tl + TM_DZ, z);
+                {
+                    float y2[16];
+                    t5::ld16(tl + TM_XY2 + TM_XY + 32 * ph, y2);
+#pragma unroll
+                    for (int v = 0; v < 16; ++v) y[v] += y2[v];
+                }
                 const int t = tc + tok;
                 if (t < t_end && GDN_IN_RANGE(g_delta_error, t < a.n && h * D + i0 + v0 + 16 <= a.c_v)) {
                     float ov[2][8];
