@@ -736,36 +736,46 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a, con
         const uint64_t dE = t5::desc_sw64_mn(sbase + L::E0);
         const uint64_t dKT = t5::desc_sw128(sbase + L::KT0);
         const bool leader = lane == 0;
-        // leader only: the copy has landed and nothing has failed
+        // Leader only: the copy a product reads has landed and nothing has failed.
+        // It is checked before the named barrier, while the compute warps still
+        // write their operand, so that after the barrier only the tcgen05 fence
+        // stands between it and the issue.  (A wait that ran out sets the abort
+        // flag; products issued after another role aborted read stale operands,
+        // which is harmless: nothing reads their results.)
         auto ready = [&](int bar, uint32_t parity) {
-            if (*abort || !state_wait(bars + bar, parity, abort)) return false;
-            t5::fence_after();
-            return true;
+            bool ok = false;
+            if (leader) ok = !*abort && state_wait(bars + bar, parity, abort);
+            __syncwarp();
+            return ok;
         };
         for (int j = 0; j < nch; ++j) {
             const uint32_t ph = j & 1;
+            bool go = ready(F_QK, ph);
             nb_sync(NB_S);                      // S of chunk j written
-            if (leader && ready(F_QK, ph)) {
+            if (go) {
+                t5::fence_after();
                 mma_chain_bmn_split<D / 16, L::QK_SLAB>(tmem + TM_XY + 32 * ph, dQK, dS, ID128);
                 t5::commit(bars + M_XY);
                 t5::commit(bars + E_QK);
             }
-            __syncwarp();
+            go = ready(F_TA, ph);
             nb_sync(NB_R);                      // R^T written
-            if (leader && ready(F_TA, ph)) {
+            if (go) {
+                t5::fence_after();
                 mma_chain_bmn<DC / 16, L::QK_SLAB>(tmem + TM_DZ, dTA, dR, ID128);
                 t5::commit(bars + M_DZ);
                 t5::commit(bars + E_TA);
             }
-            __syncwarp();
+            go = ready(F_KT0 + ph, (j >> 1) & 1);
             nb_sync(NB_D);                      // Delta~^T written
-            if (leader && ready(F_KT0 + ph, (j >> 1) & 1)) {
+            if (go) {
+                t5::fence_after();
                 mma_chain_bmn<DC / 16, L::KT_BYTES>(tmem + TM_U, dKT + ph * (L::KT_BYTES >> 4), dE, IDU);
                 t5::commit(bars + M_U);
                 t5::commit(bars + E_KT0 + ph);
             }
-            __syncwarp();
         }
+        __syncwarp();
         if (leader) {
             // every MMA issued above has completed before TMEM is released
             t5::commit(bars + M_FIN);
