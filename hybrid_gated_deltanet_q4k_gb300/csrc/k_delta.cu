@@ -652,8 +652,12 @@ __device__ __forceinline__ void mma_chain_bmn_split(uint32_t d_tmem, uint64_t ad
 // output stays off it.  Every thread meets every named barrier of
 // every chunk, also after a wait ran out (it then skips the work, and the MMA
 // warp issues nothing more), so no barrier is ever left waiting.
+// At most 112 registers a thread: three of this CTA's warps share a
+// sub-partition's 16K registers, and 112 leaves room for two warps of a prep
+// CTA (88 registers) beside them, so the next segment's prep runs in the
+// shadow of this pass; without the cap the compiler may take more.
 template <int D>
-__global__ void __launch_bounds__(STATE_THREADS, 1)
+__global__ void __maxnreg__(112)
 delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a, const __grid_constant__ SeqTable sq) {
     using L = StateSmem<D>;
     extern __shared__ __align__(1024) unsigned char smb[];
@@ -682,7 +686,7 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a, con
     if (tid == 0) {
         for (int i = F_QK; i <= F_TA; ++i) mbar_init_cta(bars + i, 1);
         for (int i = E_QK; i <= E_TA; ++i) mbar_init_cta(bars + i, 1);
-        mbar_init_cta(bars + E_V, DELTA_THREADS);
+        mbar_init_cta(bars + E_V, DELTA_THREADS / 32);
         for (int i = M_XY; i <= M_FIN; ++i) mbar_init_cta(bars + i, 1);
         mbar_init_fence();
         *abort = 0;
@@ -831,7 +835,7 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a, con
         };
         // an MMA group has completed (warp-uniform; false once anything failed)
         auto mma_done = [&](int bar, uint32_t parity) {
-            bool ok = !*abort && state_wait(bars + bar, parity, abort);
+            bool ok = state_wait(bars + bar, parity, abort);
             ok = __all_sync(0xffffffffu, ok);
             if (ok) t5::fence_after();
             return ok;
@@ -850,17 +854,21 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a, con
                 dec = G[DC - 1].y;      // e^{gamma_C}
             }
 
-            // ---- R = diag(b) (V - diag(e^gamma) X), stored as R^T (X rows: lanes 64-127)
+            // ---- R = diag(b) (V - diag(e^gamma) X), stored as R^T (X rows: lanes 64-127);
+            // this lane's V columns are read before the product's wait
+            uint4 vraw[2];
+            if (xw) {
+#pragma unroll
+                for (int m = 0; m < 2; ++m) vraw[m] = *reinterpret_cast<const uint4*>(base + L::V0 + sw128_f16(tok, vc + 8 * m));
+            }
             if (xw && mma_done(M_XY, ph)) {
                 float x[16], x2[16];
                 t5::ld16x2(tl + TM_XY + 32 * ph, x, tl + TM_XY2 + TM_XY + 32 * ph, x2);
 #pragma unroll
                 for (int v = 0; v < 16; ++v) x[v] += x2[v];
-                const unsigned char* vp = base + L::V0;
 #pragma unroll
                 for (int m = 0; m < 2; ++m) {
-                    const uint4 raw = *reinterpret_cast<const uint4*>(vp + sw128_f16(tok, vc + 8 * m));
-                    const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+                    const uint32_t w4[4] = {vraw[m].x, vraw[m].y, vraw[m].z, vraw[m].w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const float2 vv = __half22float2(*reinterpret_cast<const __half2*>(&w4[e]));
@@ -871,7 +879,10 @@ delta_state_kernel(const __grid_constant__ CUtensorMap qkv_map, DeltaArgs a, con
                 }
                 write_col(L::R0, tok, x);
             }
-            mbar_arrive_cta(bars + E_V);         // V and this chunk's gate reads are done
+            // V and this chunk's gate reads are done (every lane's values are in
+            // registers): one arrival per compute warp
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cta(bars + E_V);
             handover(NB_R);
 
             // ---- [Z; Delta] = [A T; T] R -> Delta~^T (Delta rows: lanes 64-127)
