@@ -77,40 +77,57 @@ __device__ __forceinline__ void conv_head_tokens(const ConvArgs& a, int head, in
     // so it is checked once per token (the sum, and mul once); every value of a
     // head that is not normed is checked.
     const bool mul_ok = fabsf(mul) <= 65504.0f;
+    // Tokens in groups of G: the sums of squares of a group's tokens go through
+    // the butterfly together, so their shuffles overlap (each token's sum is
+    // formed in the same order as warp_sum's).
+    constexpr int G = 4;
+    static_assert(NT % G == 0, "token runs are whole groups");
 #pragma unroll
-    for (int k = 0; k < NT; ++k) {
-        const int t = t0 + k;
-        float y[CPL];
-        float ss = 0.0f;
+    for (int k0 = 0; k0 < NT; k0 += G) {
+        float y[G][CPL], ss[G];
 #pragma unroll
-        for (int i = 0; i < CPL; ++i) {
-            const uint32_t xw = xr[k][i >> 1];
-            const float x = __uint_as_float((i & 1) ? (xw & 0xffff0000u) : (xw << 16));
-            y[i] = conv4_silu(w[i], h0[i], h1[i], h2[i], x);
-            ss = fmaf(y[i], y[i], ss);
-            h0[i] = h1[i]; h1[i] = h2[i]; h2[i] = x;
+        for (int g = 0; g < G; ++g) {
+            ss[g] = 0.0f;
+#pragma unroll
+            for (int i = 0; i < CPL; ++i) {
+                const uint32_t xw = xr[k0 + g][i >> 1];
+                const float x = __uint_as_float((i & 1) ? (xw & 0xffff0000u) : (xw << 16));
+                y[g][i] = conv4_silu(w[i], h0[i], h1[i], h2[i], x);
+                ss[g] = fmaf(y[g][i], y[g][i], ss[g]);
+                h0[i] = h1[i]; h1[i] = h2[i]; h2[i] = x;
+            }
         }
-        bool over;
         if (norm) {
-            ss = warp_sum(ss);
-            over = !(ss <= 3.0e38f) || !mul_ok;
-            const float r = rsqrtf(ss + a.eps) * mul;
 #pragma unroll
-            for (int i = 0; i < CPL; ++i) y[i] *= r;
-        } else {
-            float m = 0.0f;
+            for (int o = 16; o > 0; o >>= 1) {
 #pragma unroll
-            for (int i = 0; i < CPL; ++i) m = fmaxf_nan(m, fabsf(y[i]));
-            over = !(m <= 65504.0f);
+                for (int g = 0; g < G; ++g) ss[g] += __shfl_xor_sync(0xffffffffu, ss[g], o);
+            }
         }
-        if (t < t1 && GDN_IN_RANGE(g_conv_error, t < a.n && c0 + CPL <= a.c_conv)) {
-            uint16_t* dst = a.out + static_cast<int64_t>(t) * a.c_conv + c0;
-            if (over) atomicCAS(&g_conv_error, 0, ERR_RANGE);
-            const uint32_t p0 = f16x2_bits(y[0], y[1 % CPL]);
-            if (CPL == 4)
-                *reinterpret_cast<uint2*>(dst) = make_uint2(p0, f16x2_bits(y[2 % CPL], y[3 % CPL]));
-            else
-                *reinterpret_cast<uint32_t*>(dst) = p0;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const int t = t0 + k0 + g;
+            bool over;
+            if (norm) {
+                over = !(ss[g] <= 3.0e38f) || !mul_ok;
+                const float r = rsqrtf(ss[g] + a.eps) * mul;
+#pragma unroll
+                for (int i = 0; i < CPL; ++i) y[g][i] *= r;
+            } else {
+                float m = 0.0f;
+#pragma unroll
+                for (int i = 0; i < CPL; ++i) m = fmaxf_nan(m, fabsf(y[g][i]));
+                over = !(m <= 65504.0f);
+            }
+            if (t < t1 && GDN_IN_RANGE(g_conv_error, t < a.n && c0 + CPL <= a.c_conv)) {
+                uint16_t* dst = a.out + static_cast<int64_t>(t) * a.c_conv + c0;
+                if (over) atomicCAS(&g_conv_error, 0, ERR_RANGE);
+                const uint32_t p0 = f16x2_bits(y[g][0], y[g][1 % CPL]);
+                if (CPL == 4)
+                    *reinterpret_cast<uint2*>(dst) = make_uint2(p0, f16x2_bits(y[g][2 % CPL], y[g][3 % CPL]));
+                else
+                    *reinterpret_cast<uint32_t*>(dst) = p0;
+            }
         }
     }
 }
