@@ -999,7 +999,8 @@ int read_and_clear_delta_error() {
     return v;
 }
 
-// Token segments of DELTA_SEG_CHUNKS chunks of every sequence.  With more
+// Token segments of DELTA_SEG_CHUNKS chunks of every sequence (twice that
+// in calls of at least 512 chunks, below).  With more
 // than one, the prep of segment i+1 runs on the library's low-priority stream
 // while the state pass of segment i runs on its high-priority one (the state
 // is carried between segments in state_out, fp32, so the results are those of
@@ -1063,12 +1064,17 @@ static cudaError_t launch_delta_d(DeltaArgs& a, const SeqTable& sq, cudaStream_t
     if ((e = cudaEventRecord(ls->ev_a, st)) != cudaSuccess) return e;
     if ((e = cudaStreamWaitEvent(prep_st, ls->ev_a, 0)) != cudaSuccess) return e;
     if ((e = cudaStreamWaitEvent(state_st, ls->ev_a, 0)) != cudaSuccess) return e;
+    // Every segment boundary costs a state-pass launch, its start and its
+    // drain, against the prep of the first segment, which nothing hides: calls
+    // of at least 512 chunks take segments of twice the length (at 32768
+    // tokens four of 128 chunks beat eight of 64 and two of 256).
+    const int seg = nch >= 512 ? 2 * DELTA_SEG_CHUNKS : DELTA_SEG_CHUNKS;
     cudaError_t first = cudaSuccess;
     int nseg = 0;
-    for (int c0 = 0; c0 < nch && first == cudaSuccess; c0 += DELTA_SEG_CHUNKS) {
+    for (int c0 = 0; c0 < nch && first == cudaSuccess; c0 += seg) {
         DeltaArgs s = a;
         s.chunk0 = c0;
-        s.nchunks = nch - c0 < DELTA_SEG_CHUNKS ? nch - c0 : DELTA_SEG_CHUNKS;
+        s.nchunks = nch - c0 < seg ? nch - c0 : seg;
         launch_prep<D>(map, s, sq, prep_st);
         if ((first = cudaGetLastError()) != cudaSuccess) break;
         if ((first = cudaEventRecord(ls->ev_b, prep_st)) != cudaSuccess) break;
@@ -1084,8 +1090,8 @@ static cudaError_t launch_delta_d(DeltaArgs& a, const SeqTable& sq, cudaStream_t
         for (int i = 0; i < nseg && first == cudaSuccess; ++i) {
             first = cudaStreamWaitEvent(prep_st, i < LIB_EVENT_POOL ? ls->pool[i] : ls->ev_a, 0);
             if (first != cudaSuccess) break;
-            const int64_t tb = static_cast<int64_t>(i) * DELTA_SEG_CHUNKS * DC;
-            const int64_t te = std::min<int64_t>(a.n, tb + static_cast<int64_t>(DELTA_SEG_CHUNKS) * DC);
+            const int64_t tb = static_cast<int64_t>(i) * seg * DC;
+            const int64_t te = std::min<int64_t>(a.n, tb + static_cast<int64_t>(seg) * DC);
             first = (*after_state)(tb, te, prep_st);
         }
     }
