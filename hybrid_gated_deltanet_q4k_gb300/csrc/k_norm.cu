@@ -117,7 +117,10 @@ gated_norm_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ z
 // shared-memory stages by bulk copies issued NORM_STAGES - 1 tokens ahead, so
 // loads stay in flight while the CTA normalises, reduces and quantises the
 // current token.  Same arithmetic as gated_norm_kernel, element for element.
-constexpr int NORM_STAGES = 4;
+// Two stages (32 KB at Hv = 32): more CTAs share an SM than with a
+// four-stage ring (64 KB), which keeps more tokens in flight per SM than a
+// deeper ring per CTA.
+constexpr int NORM_STAGES = 2;
 
 template <int HPW>
 __global__ void __launch_bounds__(NORM_THREADS)
