@@ -506,7 +506,7 @@ __global__ void __maxnreg__(88) delta_prep_kernel(const __grid_constant__ CUtens
         }
         fence_proxy_async_smem();
         t5::fence_before();
-        mok = __syncthreads_and(mok);   // also: A, T^T and L are free for the next head
+        mok = __syncthreads_and(mok);   // also: A and L are free for the next head
         if (tid == 0 && mok) {
             bulk_store_1d(a.TA + cb * 2 * DC * DC, base + L::out(j), 2 * L::SLAB);
             bulk_commit();
