@@ -432,12 +432,14 @@ def run_ours(args, dist, spec):
 
     passes = 1
     # per step: weight decode (one launch, both matrices); per token pass: x
-    # quantisation, input projection, conv, conv state, the delta rule's prep
-    # and state pass per token segment of 64 chunks (one segment up to 64
-    # chunks), gated norm, output projection
+    # quantisation, input projection, conv, conv state, output projection, and
+    # per token segment of the delta rule its prep, its state pass and its
+    # gated norm (segments of 64 chunks, of 128 from 512 chunks on; one segment
+    # up to 64 chunks)
     nch = (n + 63) // 64
-    segments = 1 if nch <= 64 else (nch + 63) // 64
-    launches = (1 + (1 + 1 + 2 + 2 * segments + 2) * passes) * K
+    seg = 128 if nch >= 512 else 64
+    segments = 1 if nch <= 64 else (nch + seg - 1) // seg
+    launches = (1 + (5 + 3 * segments) * passes) * K
     if dist.rank == 0:
         print(json.dumps({
             "metric": METRIC, "value": whole_job_rate(n, dist.world, ms_max), "unit": UNIT, "n_gpus": dist.world,
