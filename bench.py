@@ -55,7 +55,7 @@ def parse():
     ap.add_argument("--config", default="h4096")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--e2e-pass", type=int, default=8192, help="tokens per pass of the host-fed call")
+    ap.add_argument("--e2e-pass", type=int, default=12288, help="tokens per pass of the host-fed call")
     ap.add_argument("--seqs", type=int, default=None, help="--config decode: one batch size only (a profiling case)")
     ap.add_argument("--stage", choices=["in_proj", "delta_rule", "q6k_deq", "q4k_deq"], default=None,
                     help="time one stage kernel alone through its stage entry point (profiling case)")
