@@ -330,6 +330,37 @@ def test_delta_rule_stage(L, spec, n, with_state):
     assert rel_l2(sout.cpu().numpy(), rS) <= 2e-3
 
 
+def test_delta_rule_decay_paths(L):
+    """The prep evaluates a chunk's decays e^{gamma_i - gamma_j} as e^{gamma_i}
+    e^{-gamma_j} when the chunk's whole decay gamma_C is at least -64 and by
+    their own exponentials below that.  Value heads here decay by 0.1 to 2 per
+    token (gamma_C from -6 to -128 over a chunk), so both ways are taken, also
+    by the two value heads of one key head within a CTA; o and the state match
+    the fp64 recurrence either way."""
+    spec = DELTA_SPECS[1]
+    _, dev, s = _layer(spec, L)
+    rng = np.random.default_rng(4242)
+    n = 1000
+    qkv_h, qe, ke, ve, _, b = _delta_inputs(spec, n, rng)
+    rate = np.array([0.1, 2.0, 0.9, 1.1])[: spec.n_v_heads]          # per value head: gamma_C ~ -64 * rate
+    la = (-rate[None, :] * rng.uniform(0.8, 1.2, size=(n, spec.n_v_heads))).astype(np.float32)
+    S0 = rng.normal(0, 0.3, size=(spec.n_v_heads, spec.dv, spec.dk)).astype(np.float32)
+    qkv, lad, bd = f16_dev(qkv_h), f32_dev(la), f32_dev(b)
+    sout = torch.empty(spec.n_v_heads, spec.dv, spec.dk, dtype=torch.float32, device=DEV)
+    o = torch.empty(n, spec.c_v, dtype=torch.float16, device=DEV)
+    nbytes = L.gdn_delta_rule_scratch_size(ctypes.byref(s), n)
+    scratch = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    L.gdn_delta_rule(ctypes.byref(s), gl.ptr(qkv), gl.ptr(lad), gl.ptr(bd), n, gl.ptr(f32_dev(S0)), gl.ptr(sout),
+                     gl.ptr(o), gl.ptr(scratch), nbytes, stream())
+    sync(L)
+    whole = n - n % 64
+    gamma_c = la[:whole].astype(np.float64).reshape(whole // 64, 64, spec.n_v_heads).sum(axis=1)
+    assert (gamma_c >= -64).any() and (gamma_c < -64).any()
+    ro, rS = OL.gated_delta_rule(qe, ke, ve, la, b, S0)
+    assert rel_l2(o.float().cpu().numpy(), ro.reshape(n, -1)) <= 2e-3
+    assert rel_l2(sout.cpu().numpy(), rS) <= 2e-3
+
+
 def test_delta_rule_segments_bitwise(L):
     """Inputs longer than 64 chunks run as token segments (the prep of the next
     segment beside the state pass of the current one) with the fp32 state
