@@ -302,15 +302,6 @@ __device__ __forceinline__ void gate_values(float beta, float alpha, float A_log
     b = 1.0f / (1.0f + expf(-beta));
 }
 
-// fp32 -> tf32 (10 explicit mantissa bits), round to nearest with ties away
-// from zero, as fp32 bits: half a tf32 unit (0x1000) is added to the
-// magnitude bits and the 13 low bits cleared; a carry into the exponent rounds
-// up correctly and values past the largest tf32 number become infinity.  For
-// finite inputs this is the rounding of cvt.rna.tf32.f32, in two integer
-// operations.
-__device__ __forceinline__ uint32_t tf32_bits(float x) { return (__float_as_uint(x) + 0x1000u) & 0xffffe000u; }
-__device__ __forceinline__ float round_tf32(float x) { return __uint_as_float(tf32_bits(x)); }
-
 // Block-wide max of a non-negative value; all threads get the result.
 // `red` must hold 32 floats of shared memory.
 __device__ __forceinline__ float block_max(float v, float* red) {

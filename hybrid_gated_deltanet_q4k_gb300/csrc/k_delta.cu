@@ -165,24 +165,26 @@ __device__ __forceinline__ void block_mm24(const float* a, const float* b, float
     const int tw0 = t & ~31, tw1 = min(t | 31, TR * TC - 1);   // the warp's first and last active thread
     const int k0 = TRI == 1 ? 4 * (tw0 / TR) : 0;
     const int k1 = TRI == 2 ? min(KK, 2 * (tw1 / TC) + 2) : KK;
-    float x[2][4] = {};
+    // the four sums of a row in two packed pairs (fma.rn.f32x2: each half
+    // rounds as fmaf does, so the products and sums are those of the scalar form)
+    F2 x[2][2] = {{f2(0.f, 0.f), f2(0.f, 0.f)}, {f2(0.f, 0.f), f2(0.f, 0.f)}};
 #pragma unroll 8
     for (int k = k0; k < k1; ++k) {
         const float a0 = a[r0 * PL + k], a1 = a[(r0 + 1) * PL + k];
         const float4 bv = *reinterpret_cast<const float4*>(b + k * PL + c0);
-        x[0][0] = fmaf(a0, bv.x, x[0][0]);
-        x[0][1] = fmaf(a0, bv.y, x[0][1]);
-        x[0][2] = fmaf(a0, bv.z, x[0][2]);
-        x[0][3] = fmaf(a0, bv.w, x[0][3]);
-        x[1][0] = fmaf(a1, bv.x, x[1][0]);
-        x[1][1] = fmaf(a1, bv.y, x[1][1]);
-        x[1][2] = fmaf(a1, bv.z, x[1][2]);
-        x[1][3] = fmaf(a1, bv.w, x[1][3]);
+        const F2 b01 = f2(bv.x, bv.y), b23 = f2(bv.z, bv.w), a00 = f2(a0, a0), a11 = f2(a1, a1);
+        x[0][0] = f2_fma(a00, b01, x[0][0]);
+        x[0][1] = f2_fma(a00, b23, x[0][1]);
+        x[1][0] = f2_fma(a11, b01, x[1][0]);
+        x[1][1] = f2_fma(a11, b23, x[1][1]);
     }
 #pragma unroll
-    for (int i = 0; i < 2; ++i)
-        *reinterpret_cast<float4*>(c + (r0 + i) * PL + c0) =
-            make_float4(s * x[i][0], s * x[i][1], s * x[i][2], s * x[i][3]);
+    for (int i = 0; i < 2; ++i) {
+        float v0, v1, v2, v3;
+        f2_split(x[i][0], v0, v1);
+        f2_split(x[i][1], v2, v3);
+        *reinterpret_cast<float4*>(c + (r0 + i) * PL + c0) = make_float4(s * v0, s * v1, s * v2, s * v3);
+    }
 }
 
 // One CTA per (chunk, key head), 256 threads:
