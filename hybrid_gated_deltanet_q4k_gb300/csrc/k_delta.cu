@@ -1077,10 +1077,15 @@ static cudaError_t launch_delta_d(DeltaArgs& a, const SeqTable& sq, cudaStream_t
         DeltaArgs s = a;
         s.chunk0 = c0;
         s.nchunks = nch - c0 < seg ? nch - c0 : seg;
+        // the second prep waits for the first to complete, so that the first
+        // state segment (high priority) and it become ready together and the
+        // state pass takes its SMs before the prep's CTAs fill them
+        if (c0 == seg && (first = cudaStreamWaitEvent(prep_st, ls->ev_a, 0)) != cudaSuccess) break;
         launch_prep<D>(map, s, sq, prep_st);
         if ((first = cudaGetLastError()) != cudaSuccess) break;
         if ((first = cudaEventRecord(ls->ev_b, prep_st)) != cudaSuccess) break;
         if ((first = cudaStreamWaitEvent(state_st, ls->ev_b, 0)) != cudaSuccess) break;
+        if (c0 == 0 && (first = cudaEventRecord(ls->ev_a, state_st)) != cudaSuccess) break;   // passed once prep 0 is done
         launch_state<D>(map, s, sq, state_st);
         if ((first = cudaGetLastError()) != cudaSuccess) break;
         if (per_segment_hook && nseg < LIB_EVENT_POOL) first = cudaEventRecord(ls->pool[nseg], state_st);
