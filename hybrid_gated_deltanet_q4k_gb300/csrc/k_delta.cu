@@ -653,7 +653,8 @@ __device__ __forceinline__ void mma_chain_bmn_split(uint32_t d_tmem, uint64_t ad
 // The state's chain per chunk is four dependent steps (X, R, Delta, U); the
 // output stays off it.  Every thread meets every named barrier of
 // every chunk, also after a wait ran out (it then skips the work, and the MMA
-// warp issues nothing more), so no barrier is ever left waiting.
+// warp issues nothing once its own check has seen the abort), so no barrier is
+// ever left waiting.
 // At most 112 registers a thread: three of this CTA's warps share a
 // sub-partition's 16K registers, and 112 leaves room for two warps of a prep
 // CTA (88 registers) beside them, so the next segment's prep runs in the
