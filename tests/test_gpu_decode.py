@@ -39,6 +39,9 @@ def L():
 @pytest.mark.parametrize("fmt,rows,cols,n,n_bf16", [("q4k", 300, 1024, 1, 300), ("q4k", 1000, 4096, 8, 700),
                                                      ("q6k", 517, 2048, 9, 0), ("q6k", 64, 16384, 3, 40),
                                                      ("q4k", 12352, 4096, 1, 12288),
+                                                     # one token, an odd row count: the last row pair has one row,
+                                                     # and rows 150 / 151 of a pair go to the bf16 / fp32 outputs
+                                                     ("q4k", 301, 1024, 1, 151),
                                                      # 2 tokens, and 6 tokens computed as 8 (two zero rows)
                                                      ("q4k", 200, 512, 2, 100), ("q6k", 300, 1024, 6, 150)])
 def test_decode_gemv_matches_oracle(L, fmt, rows, cols, n, n_bf16):
