@@ -132,10 +132,6 @@ __device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
-__device__ __forceinline__ uint16_t code_to_f16_bits(int q) {
-    return __half_as_ushort(__int2half_rn(q));
-}
-
 // Codes are carried between the quantiser and the stores as "magic" floats
 // t = q + QCODE_MAGIC (q the integer code).  QCODE_MAGIC = 1.5 * 2^23 + 0x6480
 // puts t in [2^23, 2^24), where consecutive fp32 values are the integers, so

@@ -82,8 +82,6 @@ struct DeltaArgs {
     int prep_no_copy;       // test only: the prep issues no copy, so that wait runs out
 };
 
-__device__ __forceinline__ uint16_t f16_bits(float x) { return __half_as_ushort(__float2half_rn(x)); }
-
 // Eight floats as eight fp16 (16 bytes, first value in the lowest half).
 __device__ __forceinline__ uint4 f16x8(const float (&v)[8]) {
     return make_uint4(f16x2_bits(v[0], v[1]), f16x2_bits(v[2], v[3]), f16x2_bits(v[4], v[5]), f16x2_bits(v[6], v[7]));
@@ -600,17 +598,9 @@ __device__ __forceinline__ void mbar_arrive_cta(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
-// Issue the k steps [0, NK) of one MMA chain; a K step is 16 fp16 = 32 bytes,
-// four per 128-byte swizzle row, then the next slab.
-template <int NK, int A_SLAB, int B_SLAB>
-__device__ __forceinline__ void mma_chain(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc) {
-#pragma unroll
-    for (int k = 0; k < NK; ++k)
-        t5::mma_f16(d_tmem, adesc + static_cast<uint64_t>((k >> 2) * (A_SLAB >> 4) + 2 * (k & 3)),
-                    bdesc + static_cast<uint64_t>((k >> 2) * (B_SLAB >> 4) + 2 * (k & 3)), idesc, k > 0 ? 1u : 0u);
-}
-
-// The same with an MN-major B operand (desc_sw64_mn): a K step of 16 rows of
+// Issue the k steps [0, NK) of one MMA chain with a K-major A operand (a K
+// step is 16 fp16 = 32 bytes, four per 128-byte swizzle row, then the next
+// slab) and an MN-major B operand (desc_sw64_mn): a K step of 16 rows of
 // 64 bytes is 1024 bytes further on.
 template <int NK, int A_SLAB>
 __device__ __forceinline__ void mma_chain_bmn(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc) {

@@ -124,9 +124,7 @@ __device__ __forceinline__ void bulk_store_1d(void* dst, const void* src, uint32
                  : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// This thread's committed bulk stores have finished reading shared memory.
-__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-// ... and have completed.
+// This thread's committed bulk stores have completed.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // All but this thread's most recent committed bulk store have finished reading.
 __device__ __forceinline__ void bulk_wait_read_but_last() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
@@ -146,13 +144,6 @@ __device__ __forceinline__ void stsm_x4(uint32_t addr, const uint32_t (&r)[4]) {
     asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(r[0]), "r"(r[1]),
                  "r"(r[2]), "r"(r[3])
                  : "memory");
-}
-
-// Byte offset of fp32 element (r, c), c < 32, inside a 128-byte-swizzled slab
-// of 128-byte rows (the layout a 2-D TMA box with SWIZZLE_128B and a 32-float
-// inner extent writes): the 16-byte chunk index is XORed with r mod 8.
-__host__ __device__ __forceinline__ uint32_t sw128_f32(int r, int c) {
-    return static_cast<uint32_t>(r * 128 + ((((c >> 2) ^ (r & 7)) & 7) << 4) + ((c & 3) << 2));
 }
 
 // Byte offset of fp16 element (r, c), c < 64, in an image of 128-byte rows
